@@ -1,0 +1,396 @@
+#!/usr/bin/env python3
+"""Benchmark of the hot path on GB300: one training step of the last
+transformer layer plus its tied-embedding LM head.
+
+Step (all on the GPU, through the C ABI):
+  y = layer_fwd(x)                                   (GQA 32q/8kv x 128, SwiGLU 11008,
+                                                      causal, Pre-LN, B2 S4096 H4096)
+  loss, d_y, d_E = vocab_ce_fwd_bwd(y, E, targets)   (V 128256, chunks of 16032)
+  d_x, d_W = layer_bwd(d_y)
+
+`value` = model TFLOP/s of the step (2MNK per GEMM, attention 4*B*nq*d*pairs,
+backward 2x forward, recompute not counted), inputs resident in HBM. `e2e`
+times the same step with x and targets copied from pinned host memory each
+step and the mean loss read back. `roofline` is the tcgen05 GEMM kernel,
+timed live with CUDA events on its stream inside the timed region.
+
+Usage: python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+Under torchrun (N > 1) every rank runs its own replica (no collective on the
+data path); the step time is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from megatron_transformer_layer_fwd_gb300.inputs import (CE_WORKLOADS, WORKLOADS, ce_flops,  # noqa: E402
+                                                         ce_inputs, ce_stream_bytes, layer_flops,
+                                                         layer_inputs)
+
+METRIC = "layer fwd+bwd TFLOP/s and tokens/s (bf16) + vocab-CE GB/s, % of roofline"
+LAYER = "bf16_gqa_swiglu_b2s4096h4096"
+CE = "bf16_ce_t8192h4096v128256"
+WORKLOAD = (f"{LAYER} -> {CE}: layer fwd, tied-embedding CE fwd+bwd on the layer output, "
+            "layer bwd from the CE gradient")
+
+
+def load_peaks() -> dict:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained", d["bf16_tflops"]),
+                "source": "measured"}
+    return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0,
+            "source": "fallback"}
+
+
+# ----------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi sampling of SM clocks and throttle reasons (every 200 ms)."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: str):
+        self.index = index
+        self.proc = None
+        self.lines: list[str] = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-i", self.index, "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                text=True)
+            threading.Thread(target=self._read, daemon=True).start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                smax.append(float(parts[1]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[3:7]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None, "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+def smi_index() -> str:
+    vis = os.environ.get("CUDA_VISIBLE_DEVICES", "")
+    first = vis.split(",")[0].strip() if vis else ""
+    if first.isdigit():
+        return first
+    return os.environ.get("LOCAL_RANK", "0")
+
+
+# ------------------------------------------------------------ distributed
+
+def dist_setup():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(world, v: float) -> float:
+    if world == 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if torch.cuda.is_available() and dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([v], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------ CPU oracle
+
+class OracleSample:
+    """The float64 oracle on a bounded sample of the same workload: the layer
+    fwd+bwd at full width (hidden, heads, ffn) with 128 tokens, and the CE
+    fwd+bwd of 32 tokens against the full vocabulary. Inputs are drawn once."""
+
+    SEQ, CE_TOKENS = 128, 32
+
+    def __init__(self):
+        import oracle
+        self.oracle = oracle
+        self.shape = WORKLOADS[LAYER].replace(batch=1, seq=self.SEQ)
+        arr = layer_inputs(self.shape, seed=0)
+        self.w = {k: arr[k] for k in ("w_qkv", "b_qkv", "w_o", "b_o", "w_1", "b_1", "w_2", "b_2",
+                                      "ln1_g", "ln1_b", "ln2_g", "ln2_b")}
+        self.x = arr["x"]
+        self.dy = np.full((self.shape.tokens, self.shape.hidden),
+                          1.0 / (self.shape.tokens * self.shape.hidden))
+        self.ce = CE_WORKLOADS[CE]
+        rng = np.random.default_rng(0)
+        n = self.CE_TOKENS
+        self.hid = rng.standard_normal((n, self.ce.hidden))
+        self.emb = rng.standard_normal((self.ce.vocab, self.ce.hidden), dtype=np.float32) * 0.02
+        self.emb = self.emb.astype(np.float64)
+        self.tg = rng.integers(0, self.ce.vocab, n)
+        self.flops = layer_flops(self.shape)["total"] + 3 * 2.0 * n * self.ce.vocab * self.ce.hidden
+        self.desc = (f"layer fwd+bwd at B1 S{self.SEQ} (full hidden/heads/ffn of {LAYER}) + CE "
+                     f"fwd+bwd for {n} tokens x the full {self.ce.vocab}-entry vocabulary, "
+                     "float64 numpy")
+
+    def run_once(self) -> float:
+        """One sample; returns seconds."""
+        o = self.oracle
+        t0 = time.perf_counter()
+        _, c = o.block_fwd(self.shape, self.w, self.x)
+        o.block_bwd(self.shape, self.w, c, self.dy)
+        n = self.CE_TOKENS
+        _, lse, _ = o.ce_full(self.hid, self.emb, self.tg, row_block=n)
+        o.ce_grads(self.hid, self.emb, self.tg, lse, 1.0 / n, row_block=n)
+        return time.perf_counter() - t0
+
+    def timed(self, budget_s: float) -> dict:
+        t, reps = 0.0, 0
+        while reps == 0 or (t < budget_s and reps < 50):
+            t += self.run_once()
+            reps += 1
+        return {"value": reps * self.flops / t / 1e12, "unit": "TFLOP/s", "cores": os.cpu_count(),
+                "kind": "oracle", "seconds": round(t, 2), "sample": f"{reps} x [{self.desc}]"}
+
+
+# ------------------------------------------------------------ our arm
+
+def traffic_record(kernel_src: str) -> float | None:
+    """Per-launch DRAM bytes from the committed ncu summary, if it was taken
+    on the current kernel source."""
+    p = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(p):
+        return None
+    d = json.load(open(p))
+    h = hashlib.sha256(open(kernel_src, "rb").read()).hexdigest()[:16]
+    if d.get("source_sha256_16") != h:
+        return None
+    return d.get("bytes_per_launch")
+
+
+def run_ours(args, world, rank, local):
+    import torch
+    from megatron_transformer_layer_fwd_gb300 import build, mgb
+    from megatron_transformer_layer_fwd_gb300.runner import CERunner, LayerRunner, to_device
+
+    build.build()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    shape = WORKLOADS[LAYER]
+    ce = CE_WORKLOADS[CE]
+    arr = layer_inputs(shape, seed=rank)
+    layer = LayerRunner(shape, arr, device=dev)
+    cin = ce_inputs(ce, seed=rank)
+    emb = to_device(cin["emb"], torch.bfloat16, dev)
+    targets = torch.from_numpy(cin["targets"]).to(dev)
+    del cin, arr
+    cer = CERunner(ce.tokens, ce.hidden, ce.vocab, ce.chunk, layer.y, emb, targets)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        layer.fwd(stream)
+        cer.run(stream)
+        layer.bwd(cer.d_hidden, stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    if mgb.mgb_device_status(stream) != mgb.MGB_OK:
+        raise RuntimeError("device error during warm-up")
+
+    # ---- timed region: inputs resident in HBM (working set >> L2)
+    mgb.mgb_profile_reset()
+    mgb.mgb_profile_enable(True)
+    clocks = ClockSampler(smi_index())
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    clocks.start()
+    n0 = mgb.mgb_launch_count()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    clk = clocks.stop()
+    launches = (mgb.mgb_launch_count() - n0) // args.steps
+    mgb.mgb_profile_enable(False)
+    prof = mgb.mgb_profile_read()
+    ms = e0.elapsed_time(e1) / args.steps
+    ms = max_over_ranks(world, ms)
+    if mgb.mgb_device_status(stream) != mgb.MGB_OK:
+        raise RuntimeError("device error during the timed region")
+
+    # ---- end to end through host buffers
+    x_host = layer.x.cpu().pin_memory()
+    t_host = targets.cpu().pin_memory()
+    loss_host = torch.empty(1, dtype=torch.float32).pin_memory()
+    e2e_steps = max(3, args.steps // 2)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    h0, h1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    h0.record(stream)
+    for _ in range(e2e_steps):
+        layer.x.copy_(x_host, non_blocking=True)
+        targets.copy_(t_host, non_blocking=True)
+        step()
+        loss_host.copy_(cer.loss_mean[:1], non_blocking=True)
+    h1.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = max_over_ranks(world, h0.elapsed_time(h1) / e2e_steps)
+
+    lf, cf = layer_flops(shape), ce_flops(ce)
+    step_flops = lf["total"] + cf["total"]
+    value = world * step_flops / (ms / 1e3) / 1e12
+    peaks = load_peaks()
+    # GEMM kernel roofline (all tcgen05 GEMM launches of the step; 2MNK each,
+    # including the CE logits recompute the kernel executes)
+    gemm_flops_step = 3 * lf["gemm_fwd"] + 4 * 2.0 * ce.tokens * ce.vocab * ce.hidden
+    gemm_kinds = ("gemm_tc_fwd", "gemm_tc_dgrad", "gemm_tc_wgrad")
+    gemm_ms = sum(prof[k][0] for k in gemm_kinds) / args.steps
+    gemm_launches = sum(prof[k][1] for k in gemm_kinds) / args.steps
+    gemm_tflops = gemm_flops_step / (gemm_ms / 1e3) / 1e12 if gemm_ms > 0 else None
+    traffic = traffic_record(os.path.join(ROOT, "megatron_transformer_layer_fwd_gb300", "csrc",
+                                          "gemm_tc.cu"))
+    roofline = {"kernel": "gemm_tc_kernel (tcgen05, all launches of the step)", "bound": "tensor",
+                "achieved": round(gemm_tflops, 1) if gemm_tflops else None,
+                "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s",
+                "frac": round(gemm_tflops / peaks["bf16_tflops_sustained"], 4) if gemm_tflops else None,
+                "peak_source": f"{peaks['source']} bf16_tflops_sustained",
+                "launches_per_step": gemm_launches,
+                "traffic": traffic}
+    ce_ms = (prof["ce_stats"][0] + prof["ce_grad"][0]) / args.steps
+    ce_bytes = ce_stream_bytes(ce)
+    ce_gbs = ce_bytes / (ce_ms / 1e3) / 1e9 if ce_ms > 0 else None
+    roofline_ce = {"kernel": "ce_stats + ce_grad", "bound": "hbm",
+                   "achieved": round(ce_gbs, 1) if ce_gbs else None, "peak": peaks["hbm_gbs"],
+                   "unit": "GB/s", "frac": round(ce_gbs / peaks["hbm_gbs"], 4) if ce_gbs else None,
+                   "peak_source": f"{peaks['source']} hbm_gbs", "bytes_per_step": ce_bytes}
+    layer_kinds = ("attn_fwd", "attn_bwd", "layernorm_fwd", "layernorm_bwd", "colsum")
+    breakdown = {k: round(v[0] / args.steps, 4) for k, v in prof.items() if v[1] > 0}
+    out = {
+        "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded: x~N(0,1), W~N(0,0.02^2), biases 0, LN gamma 1 beta 0, "
+                "E~N(0,0.02^2), targets~U[0,V))",
+        "config": {"workload": WORKLOAD, "tokens_per_step": shape.tokens,
+                   "l2": "inputs larger than L2 (weights 0.35 GB + embedding 1.05 GB + activations)",
+                   "parallelism": f"replicas x{world}"},
+        "tokens_per_s": round(world * shape.tokens / (ms / 1e3), 1),
+        "step_tflop": round(step_flops / 1e12, 4),
+        "clocks": clk,
+        "e2e": {"value": round(world * step_flops / (e2e_ms / 1e3) / 1e12, 2), "unit": "TFLOP/s",
+                "ms_per_step": round(e2e_ms, 4),
+                "h2d_bytes_per_step": layer.x.numel() * layer.x.element_size() + targets.numel() * 4,
+                "d2h_bytes_per_step": 4},
+        "gpu_launches": int(launches),
+        "roofline": roofline,
+        "roofline_ce": roofline_ce,
+        "kernel_ms_per_step": breakdown,
+    }
+    return out
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    world, rank, local = dist_setup()
+
+    if args.impl == "reference":
+        # the reference arm is the float64 oracle on the host cores, rank 0 only
+        if rank != 0:
+            return
+        sample = OracleSample()
+        for _ in range(args.warmup):
+            sample.run_once()
+        secs = statistics.median(sample.run_once() for _ in range(args.steps))
+        tfl = sample.flops / secs / 1e12
+        per_step = [{"sample": f"1 x [{sample.desc}] per step"}]
+        out = {"impl": "reference", "metric": METRIC, "value": round(tfl, 6), "unit": "TFLOP/s",
+               "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+               "ms_per_step": round(secs * 1e3, 1), "higher_is_better": True, "scaling": "weak",
+               "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+               "config": {"workload": WORKLOAD, "parallelism": "host cores, rank 0 only"},
+               "cpu_baseline": {"value": round(tfl, 6), "unit": "TFLOP/s", "cores": os.cpu_count(),
+                                "kind": "oracle", "sample": per_step[0]["sample"]},
+               "e2e": {"value": round(tfl, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                       "d2h_bytes_per_step": 0}}
+        print(json.dumps(out), flush=True)
+        return
+
+    # CPU baseline first (before any CUDA context: no fork after GPU use here)
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = OracleSample().timed(budget_s=12.0)
+    out = run_ours(args, world, rank, local)
+    if rank == 0:
+        if cpu is not None:
+            out["cpu_baseline"] = {k: cpu[k] for k in ("value", "unit", "cores", "kind", "sample")}
+        print(json.dumps(out), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

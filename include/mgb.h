@@ -1,0 +1,227 @@
+/*
+ * mgb.h - C ABI of the GB300 (sm_103a) Megatron-style transformer layer library.
+ *
+ * One transformer layer (LayerNorm, fused QKV projection, per-head softmax
+ * attention, output projection, residual, LayerNorm, fc1 + GELU/SwiGLU, fc2,
+ * residual; Pre-LN or Post-LN) forward and backward, and the tied-embedding
+ * cross-entropy computed from per-vocab-chunk partials, on one GPU.
+ *
+ * Sources the operations follow (web pages on the subject, by title/section):
+ *   [P1] "LLM Lab 06: build a Megatron-style Transformer Block from scratch",
+ *        section 2 (code walk-through: the layer's dataflow, loss = mean(out),
+ *        end-to-end backward), section 5 (Post-LN vs Pre-LN: only the position
+ *        of the norm relative to the residual changes).
+ *   [P2] "02 - How a whole Transformer block is split", section 1 (MLP
+ *        column -> row; SwiGLU gate/up kept together by interleaving),
+ *        section 2 (attention split by head; fused linear_qkv of width
+ *        q_proj + 2*kv_proj; GQA), section 3 (tied input/output embedding),
+ *        section 4 (vocab-parallel cross-entropy: global max, target logit and
+ *        sum-exp combined from shard partials; backward softmax - onehot).
+ *
+ * Conventions for every call:
+ *   - All pointers are caller-owned DEVICE pointers unless stated otherwise;
+ *     the library allocates no device memory per call and keeps no state
+ *     besides a per-process cache of kernel attributes. Scratch memory is the
+ *     caller's `ws` buffer; sizes come from the *_sizes queries.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t passed as void*;
+ *     NULL = the legacy default stream). Argument errors are returned before
+ *     any kernel is launched. Kernel-side failures (a bounded device wait that
+ *     ran out) are recorded in a per-device error word read by
+ *     mgb_device_status().
+ *   - Tensors are dense and row-major: activations [T, features] with token
+ *     t = b*S + s (batch-major); weights [out, in] (y = x W^T + b).
+ *   - dtype MGB_BF16: every tensor is bfloat16 except LayerNorm statistics,
+ *     attention log-sum-exp and losses, which are float32; accumulation is
+ *     float32. dtype MGB_F32: every tensor is float32 (SIMT float32 path).
+ *   - Device pointers must be 16-byte aligned; feature sizes (hidden, ffn,
+ *     head dims, vocab chunk) must keep every row a multiple of 16 bytes.
+ *   - Gradients are overwritten, never accumulated into.
+ *   - Any status other than MGB_OK leaves outputs unspecified.
+ */
+#ifndef MGB_H
+#define MGB_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MGB_OK = 0,
+  MGB_ERR_INVALID_ARG = -1,         /* bad shape/flag combination or NULL pointer */
+  MGB_ERR_UNSUPPORTED = -2,         /* valid but not supported (e.g. head_dim 96 in bf16) */
+  MGB_ERR_MISALIGNED = -3,          /* a pointer or row stride is not 16-byte aligned */
+  MGB_ERR_WORKSPACE_TOO_SMALL = -4, /* ws/saved smaller than the *_sizes query */
+  MGB_ERR_ARCH = -5,                /* current device is not sm_103 */
+  MGB_ERR_CUDA = -6,                /* a CUDA runtime call failed */
+  MGB_ERR_DEVICE_TIMEOUT = -7,      /* a bounded device-side wait ran out */
+  MGB_ERR_NOT_IMPLEMENTED = -8
+} mgb_status;
+
+typedef enum { MGB_F32 = 0, MGB_BF16 = 1 } mgb_dtype;
+typedef enum { MGB_PRE_LN = 0, MGB_POST_LN = 1 } mgb_norm_pos;
+typedef enum { MGB_GELU_ERF = 0, MGB_SWIGLU = 1 } mgb_act;
+
+/* Shape and options of one layer [P1 section 2; P2 sections 1-2].
+ * Enum-valued fields are int32_t so the struct layout is fixed. */
+typedef struct {
+  int32_t batch, seq, hidden;
+  int32_t n_q_heads, n_kv_heads, head_dim; /* n_q_heads % n_kv_heads == 0 (GQA) */
+  int32_t ffn;                             /* fc1 width (SwiGLU: fc1 emits 2*ffn) */
+  int32_t dtype;                           /* mgb_dtype */
+  int32_t norm_pos;                        /* mgb_norm_pos */
+  int32_t act;                             /* mgb_act */
+  int32_t causal;                          /* 1: key j visible to query i iff j <= i */
+  int32_t ln_affine;                       /* 1: LayerNorms have gamma/beta */
+  int32_t has_bias;                        /* 1: the four linears have biases */
+  int32_t glu_block;                       /* SwiGLU interleave block (fc1 columns) */
+  float ln_eps;                            /* LayerNorm epsilon (1e-5) */
+} mgb_block_desc;
+
+/* Layer parameters. Shapes (H hidden, d head_dim, W = ffn or 2*ffn for SwiGLU):
+ *   w_qkv [(nq+2*nkv)*d, H]  rows [Q heads | K heads | V heads]   b_qkv [(nq+2nkv)d]
+ *   w_o   [H, nq*d]                                                b_o   [H]
+ *   w_1   [W, H]  (SwiGLU: row blocks of glu_block gate, glu_block up, ...)  b_1 [W]
+ *   w_2   [H, ffn]                                                 b_2   [H]
+ *   ln1_g/ln1_b/ln2_g/ln2_b [H]: LN1 belongs to the attention sublayer, LN2 to the MLP.
+ * Biases must be NULL iff !has_bias; LN params NULL iff !ln_affine. */
+typedef struct {
+  const void *w_qkv, *b_qkv, *w_o, *b_o, *w_1, *b_1, *w_2, *b_2;
+  const void *ln1_g, *ln1_b, *ln2_g, *ln2_b;
+} mgb_block_weights;
+
+/* Gradient outputs, same shapes/dtype as the weights. Any entry may be NULL
+ * (that gradient is not written). */
+typedef struct {
+  void *w_qkv, *b_qkv, *w_o, *b_o, *w_1, *b_1, *w_2, *b_2;
+  void *ln1_g, *ln1_b, *ln2_g, *ln2_b;
+} mgb_block_grads;
+
+/* Sizes in bytes of the `saved` buffer (written by fwd, read by bwd) and of
+ * the scratch workspaces of fwd and bwd. Host-only; no device work. */
+mgb_status mgb_block_sizes(const mgb_block_desc* desc, size_t* saved_bytes,
+                           size_t* fwd_ws_bytes, size_t* bwd_ws_bytes);
+
+/* Layer forward [P1 section 2; P2 sections 1-2]:
+ *   Pre-LN : xn = LN1(x); qkv = xn Wqkv^T + bqkv; O = Attn(qkv);
+ *            h = x + O Wo^T + bo; hn = LN2(h); a = act(hn W1^T + b1);
+ *            y = h + a W2^T + b2
+ *   Post-LN: O = Attn(x Wqkv^T + bqkv); h = LN1(x + O Wo^T + bo);
+ *            a = act(h W1^T + b1); y = LN2(h + a W2^T + b2)
+ * Attn: per batch and query head h, softmax(Q_h K_g^T / sqrt(d)) V_g with
+ * g = h / (nq/nkv), causal mask optional. x, y: [T, H]. `saved` receives what
+ * the backward needs (layout private). */
+mgb_status mgb_block_fwd(const mgb_block_desc* desc, const mgb_block_weights* w,
+                         const void* x, void* y, void* saved, size_t saved_bytes,
+                         void* ws, size_t ws_bytes, void* stream);
+
+/* Layer backward [P1 section 2 "end-to-end backward"]: given dy = dL/dy [T, H]
+ * and the `saved` buffer of the matching forward (same x and weights), writes
+ * dx = dL/dx [T, H] and every non-NULL gradient in `grads`. Attention
+ * probabilities are recomputed from the saved log-sum-exp. */
+mgb_status mgb_block_bwd(const mgb_block_desc* desc, const mgb_block_weights* w,
+                         const void* x, const void* dy, const void* saved, size_t saved_bytes,
+                         void* dx, const mgb_block_grads* grads,
+                         void* ws, size_t ws_bytes, void* stream);
+
+/* Tied-embedding cross-entropy [P2 sections 3-4]. */
+typedef struct {
+  int32_t tokens, hidden, vocab;
+  int32_t chunk;        /* vocab chunk; the last chunk may be ragged */
+  int32_t dtype;        /* MGB_BF16 (hidden/emb/grads bf16) */
+  float grad_scale;     /* dL/dloss_t for every token: 1/tokens for the mean */
+} mgb_ce_desc;
+
+mgb_status mgb_vocab_ce_sizes(const mgb_ce_desc* desc, size_t* ws_bytes);
+
+/* logits l = hidden E^T ([T,H] x [V,H]^T), computed chunk by chunk; per chunk
+ * the row max m_c, sum exp(l - m_c) and the target logit (0 unless the target
+ * falls in the chunk) are kept; LSE = M + log sum_c s_c exp(m_c - M),
+ * loss_t = LSE_t - target logit_t, loss_mean = mean_t loss_t. Backward:
+ * G = (softmax(l) - onehot(target)) * grad_scale, d_hidden = G E,
+ * d_emb = G^T hidden, again chunk by chunk (logits recomputed per chunk).
+ *   targets [T] int32 in [0, vocab) (device); loss_per_token [T] f32;
+ *   loss_mean: one f32 (device); lse [T] f32 or NULL;
+ *   d_hidden [T,H], d_emb [V,H]: NULL skips that gradient (both NULL = fwd only). */
+mgb_status mgb_vocab_ce_fwd_bwd(const mgb_ce_desc* desc, const void* hidden, const void* emb,
+                                const int32_t* targets, float* loss_per_token, float* loss_mean,
+                                float* lse, void* d_hidden, void* d_emb,
+                                void* ws, size_t ws_bytes, void* stream);
+
+/* ---- building blocks of the path (also used by the calls above) ---- */
+
+typedef enum { MGB_K_MAJOR = 0, MGB_MN_MAJOR = 1 } mgb_major;
+
+/* C[M,N] = alpha * op(A) op(B)^T (+ bias[N]) [(+ C if accumulate)]; float32
+ * accumulation. A is [M,K] stored row-major with leading dim lda (K_MAJOR)
+ * or stored [K,M] (MN_MAJOR); B likewise [N,K] / [K,N]. The dense
+ * contractions of every linear layer [P1 section 2; P2 sections 1-2] and their
+ * input/weight gradients are this product with one of the three operand
+ * layouts (K/K forward, K/MN input grad, MN/MN weight grad).
+ * dtype MGB_BF16: A, B, bias bf16; C bf16 unless c_f32 (then float32).
+ * dtype MGB_F32: everything float32. `accumulate` needs c_f32 or MGB_F32. */
+typedef struct {
+  int32_t m, n, k;
+  int32_t a_major, b_major;   /* mgb_major */
+  int64_t lda, ldb, ldc;      /* in elements */
+  int32_t dtype;
+  int32_t c_f32;
+  int32_t accumulate;
+  float alpha;
+} mgb_gemm_desc;
+
+mgb_status mgb_gemm(const mgb_gemm_desc* desc, const void* a, const void* b, const void* bias,
+                    void* c, void* stream);
+
+/* LayerNorm over the last dim [P1 section 2, F.layer_norm(x, (hidden,))]:
+ * y = gamma*(x-mean)*rstd + beta, biased variance. mean/rstd [rows] f32
+ * (may be NULL). gamma/beta NULL = no affine. */
+mgb_status mgb_layernorm_fwd(int32_t rows, int32_t cols, int32_t dtype, float eps, const void* x,
+                             const void* gamma, const void* beta, void* y, float* mean,
+                             float* rstd, void* stream);
+
+/* Attention core [P2 section 2]: q [B*S, nq*d] (head h at columns h*d), k, v
+ * [B*S, nkv*d] (row stride ld_q / ld_kv elements, so they may be column slices
+ * of one fused qkv buffer); o [B*S, nq*d]; lse [B, nq, S] f32. */
+mgb_status mgb_attention_fwd(int32_t batch, int32_t seq, int32_t n_q_heads, int32_t n_kv_heads,
+                             int32_t head_dim, int32_t causal, int32_t dtype,
+                             const void* q, const void* k, const void* v, int64_t ld_q,
+                             int64_t ld_kv, void* o, float* lse, void* stream);
+
+/* ---- status and diagnostics ---- */
+
+const char* mgb_status_string(mgb_status s);
+
+/* Synchronises `stream`, then returns and clears the current device's error
+ * word (MGB_ERR_DEVICE_TIMEOUT if a bounded device wait ran out since the last
+ * call, else MGB_OK), or MGB_ERR_CUDA if the synchronisation failed. */
+mgb_status mgb_device_status(void* stream);
+
+/* Launches one block that waits on a device flag nothing ever sets, bounded
+ * by `limit_ns` nanoseconds (<= 5e9), through the same bounded-wait routine the
+ * kernels use; the wait runs out and records MGB_ERR_DEVICE_TIMEOUT in the
+ * error word. Exists to test that path without hanging or faulting a GPU. */
+mgb_status mgb_selftest_wait_timeout(uint64_t limit_ns, void* stream);
+
+/* ---- tracing ----
+ * Every kernel the library launches is counted; with profiling enabled each
+ * launch (or group of launches of one step, e.g. a LayerNorm backward and its
+ * partial-sum reduction) is bracketed by CUDA events on the launching stream,
+ * grouped by kernel kind (names from mgb_profile_kind_name). Host-side state,
+ * process-wide; reading synchronises the recorded events. */
+uint64_t mgb_launch_count(void);
+mgb_status mgb_profile_enable(int32_t on);
+mgb_status mgb_profile_reset(void);
+int32_t mgb_profile_kinds(void);
+const char* mgb_profile_kind_name(int32_t kind);
+mgb_status mgb_profile_read(int32_t kind, double* total_ms, int64_t* launches);
+
+/* Library version (major*10000 + minor*100 + patch). */
+int32_t mgb_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* MGB_H */

@@ -1,0 +1,622 @@
+// C ABI (include/mgb.h): argument validation, buffer plans, and the launch
+// sequences of the layer forward/backward and the chunked cross-entropy.
+//
+// Layer dataflow: "LLM Lab 06: build a Megatron-style Transformer Block from
+// scratch", section 2 (LN -> attention -> residual -> LN -> fc1 -> GELU -> fc2
+// -> residual, loss = mean(out), end-to-end backward) and section 5 (Post-LN
+// moves the norm after each residual add); "02 - How a whole Transformer block
+// is split", sections 1-2 (SwiGLU interleave, fused QKV, GQA, output
+// projection) and sections 3-4 (tied embedding, chunked cross-entropy).
+// On one GPU the tensor-parallel all-gather / all-reduce points of those pages
+// disappear: each head writes its own column slice of the attention output and
+// the row-parallel partial sums are the K loop of the projection / fc2 GEMMs.
+#include <stdlib.h>
+#include <string.h>
+
+#include <mutex>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace mgb {
+
+// One error word per device that loads the library (see mgb_device_status).
+__device__ int g_error_word = 0;
+
+int* device_error_word() {
+  static int* addr[64] = {};
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (addr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_error_word) != cudaSuccess) return nullptr;
+    addr[dev] = static_cast<int*>(p);
+  }
+  return addr[dev];
+}
+
+mgb_status attention_bf16_fwd(const AttnArgs& a, cudaStream_t st);
+mgb_status attention_bf16_bwd(const AttnArgs& a, cudaStream_t st);
+mgb_status attention_f32_fwd(const AttnArgs& a, cudaStream_t st);
+mgb_status attention_f32_bwd(const AttnArgs& a, cudaStream_t st);
+
+mgb_status attention_fwd_launch(const AttnArgs& a, cudaStream_t st) {
+  if (a.B == 0 || a.S == 0) return MGB_OK;
+  LaunchScope scope(PROF_ATTN_FWD, st, 1);
+  return a.dtype == MGB_BF16 ? attention_bf16_fwd(a, st) : attention_f32_fwd(a, st);
+}
+mgb_status attention_bwd_launch(const AttnArgs& a, cudaStream_t st) {
+  if (a.B == 0 || a.S == 0) return MGB_OK;
+  LaunchScope scope(PROF_ATTN_BWD, st, 3);
+  return a.dtype == MGB_BF16 ? attention_bf16_bwd(a, st) : attention_f32_bwd(a, st);
+}
+
+namespace {
+
+__global__ void selftest_wait_kernel(unsigned long long limit_ns, int* err) {
+  __shared__ uint64_t bar;
+  const uint32_t b = smem_u32(&bar);
+  if (threadIdx.x == 0) {
+    mbar_init(b, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  // nothing ever arrives on this barrier: the bounded wait (the same routine
+  // the GEMM pipeline uses) must run out and record the timeout
+  if (threadIdx.x == 0) mbar_wait(b, 0, err, limit_ns);
+}
+
+#define MGB_TRY(expr)                    \
+  do {                                   \
+    const mgb_status s_ = (expr);        \
+    if (s_ != MGB_OK) return s_;         \
+  } while (0)
+
+inline size_t al256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+inline cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
+
+bool fault_injected() {
+  const char* f = getenv("MGB_FAULT");
+  return f != nullptr && strcmp(f, "validate") == 0;
+}
+
+mgb_status check_arch() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return MGB_ERR_CUDA;
+  int major = 0, minor = 0;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+    return MGB_ERR_CUDA;
+  return (major == 10 && minor == 3) ? MGB_OK : MGB_ERR_ARCH;
+}
+
+struct Plan {
+  int B, S, T, H, nq, nkv, d, F, W, Wqkv, Dq;
+  size_t es;
+  bool pre, swiglu;
+  // saved buffer
+  size_t s_mu1, s_rs1, s_mu2, s_rs2, s_lse, s_xn, s_qkv, s_O, s_h, s_r1, s_hn, s_u, s_a, s_r2;
+  size_t saved;
+  // backward workspace
+  size_t w_dffn, w_dh, w_dr2, w_du, w_dO, w_dqkv, w_dxn, w_delta, w_cparts, w_lparts;
+  size_t bwd;
+  int cparts, lparts;
+};
+
+mgb_status validate_desc(const mgb_block_desc* d) {
+  if (d == nullptr) return MGB_ERR_INVALID_ARG;
+  if (fault_injected()) return MGB_ERR_INVALID_ARG;
+  if (d->batch < 0 || d->seq < 1 || d->hidden < 1 || d->n_q_heads < 1 || d->n_kv_heads < 1 ||
+      d->head_dim < 1 || d->ffn < 1)
+    return MGB_ERR_INVALID_ARG;
+  if (d->n_q_heads % d->n_kv_heads != 0) return MGB_ERR_INVALID_ARG;
+  if (d->dtype != MGB_F32 && d->dtype != MGB_BF16) return MGB_ERR_INVALID_ARG;
+  if (d->norm_pos != MGB_PRE_LN && d->norm_pos != MGB_POST_LN) return MGB_ERR_INVALID_ARG;
+  if (d->act != MGB_GELU_ERF && d->act != MGB_SWIGLU) return MGB_ERR_INVALID_ARG;
+  if (!(d->ln_eps >= 0.0f)) return MGB_ERR_INVALID_ARG;
+  if ((d->causal | d->ln_affine | d->has_bias) & ~1) return MGB_ERR_INVALID_ARG;
+  const int64_t lim = (int64_t)1 << 31;
+  if ((int64_t)d->batch * d->seq >= lim || (int64_t)d->n_q_heads * d->head_dim >= lim)
+    return MGB_ERR_INVALID_ARG;
+  if (d->act == MGB_SWIGLU) {
+    if (d->glu_block < 1 || d->ffn % d->glu_block != 0) return MGB_ERR_INVALID_ARG;
+    if (d->dtype == MGB_BF16 && d->glu_block != 32 && d->glu_block != 64 && d->glu_block != 128)
+      return MGB_ERR_UNSUPPORTED;
+  }
+  // every row of every activation / weight a multiple of 16 bytes
+  const int vmul = d->dtype == MGB_BF16 ? 8 : 4;
+  if (d->hidden % vmul || d->ffn % vmul || (d->n_q_heads * d->head_dim) % vmul ||
+      (d->n_kv_heads * d->head_dim) % vmul)
+    return MGB_ERR_MISALIGNED;
+  if (d->dtype == MGB_BF16 && d->head_dim != 64 && d->head_dim != 128) return MGB_ERR_UNSUPPORTED;
+  if (d->dtype == MGB_F32 && (d->head_dim > 256 || d->seq > 2048)) return MGB_ERR_UNSUPPORTED;
+  // LayerNorm keeps a row in registers: at most 1024 threads x 4 vectors of 16 bytes
+  if (d->hidden > (d->dtype == MGB_BF16 ? 32768 : 16384)) return MGB_ERR_UNSUPPORTED;
+  return MGB_OK;
+}
+
+void make_plan(const mgb_block_desc* d, Plan* p) {
+  p->B = d->batch; p->S = d->seq; p->T = d->batch * d->seq;
+  p->H = d->hidden; p->nq = d->n_q_heads; p->nkv = d->n_kv_heads; p->d = d->head_dim;
+  p->F = d->ffn;
+  p->swiglu = d->act == MGB_SWIGLU;
+  p->W = p->swiglu ? 2 * d->ffn : d->ffn;
+  p->Dq = p->nq * p->d;
+  p->Wqkv = (p->nq + 2 * p->nkv) * p->d;
+  p->es = d->dtype == MGB_BF16 ? 2 : 4;
+  p->pre = d->norm_pos == MGB_PRE_LN;
+  const size_t T = p->T, es = p->es;
+  size_t o = 0;
+  auto take = [&](size_t bytes) { const size_t at = o; o += al256(bytes); return at; };
+  p->s_mu1 = take(4 * T); p->s_rs1 = take(4 * T);
+  p->s_mu2 = take(4 * T); p->s_rs2 = take(4 * T);
+  p->s_lse = take(4 * (size_t)p->B * p->nq * p->S);
+  p->s_xn = p->pre ? take(es * T * p->H) : 0;
+  p->s_qkv = take(es * T * p->Wqkv);
+  p->s_O = take(es * T * p->Dq);
+  p->s_h = take(es * T * p->H);
+  p->s_r1 = p->pre ? 0 : take(es * T * p->H);
+  p->s_hn = p->pre ? take(es * T * p->H) : 0;
+  p->s_u = take(es * T * p->W);
+  p->s_a = take(es * T * p->F);
+  p->s_r2 = p->pre ? 0 : take(es * T * p->H);
+  p->saved = o;
+  o = 0;
+  p->cparts = colsum_parts(p->T);
+  p->lparts = layernorm_bwd_parts(p->T);
+  const size_t maxN = (size_t)((p->W > p->Wqkv ? p->W : p->Wqkv) > p->H
+                                   ? (p->W > p->Wqkv ? p->W : p->Wqkv) : p->H);
+  p->w_dffn = take(es * T * p->H);
+  p->w_dh = take(es * T * p->H);
+  p->w_dr2 = take(es * T * p->H);
+  p->w_du = take(es * T * p->W);
+  p->w_dO = take(es * T * p->Dq);
+  p->w_dqkv = take(es * T * p->Wqkv);
+  p->w_dxn = take(es * T * p->H);
+  p->w_delta = take(4 * (size_t)p->B * p->nq * p->S);
+  p->w_cparts = take(4 * (size_t)p->cparts * maxN);
+  p->w_lparts = take(4 * 2 * (size_t)p->lparts * p->H);
+  p->bwd = o;
+}
+
+mgb_status check_weights(const mgb_block_desc* d, const mgb_block_weights* w) {
+  if (w == nullptr) return MGB_ERR_INVALID_ARG;
+  if (!w->w_qkv || !w->w_o || !w->w_1 || !w->w_2) return MGB_ERR_INVALID_ARG;
+  const bool hb = d->has_bias, ha = d->ln_affine;
+  if (hb != (w->b_qkv != nullptr) || hb != (w->b_o != nullptr) || hb != (w->b_1 != nullptr) ||
+      hb != (w->b_2 != nullptr))
+    return MGB_ERR_INVALID_ARG;
+  if (ha != (w->ln1_g != nullptr) || ha != (w->ln1_b != nullptr) || ha != (w->ln2_g != nullptr) ||
+      ha != (w->ln2_b != nullptr))
+    return MGB_ERR_INVALID_ARG;
+  const void* ps[] = {w->w_qkv, w->b_qkv, w->w_o, w->b_o, w->w_1, w->b_1,
+                      w->w_2,   w->b_2,   w->ln1_g, w->ln1_b, w->ln2_g, w->ln2_b};
+  for (const void* p : ps)
+    if (!aligned16(p)) return MGB_ERR_MISALIGNED;
+  return MGB_OK;
+}
+
+template <typename P>
+P* at(void* base, size_t off) {
+  return reinterpret_cast<P*>(static_cast<char*>(base) + off);
+}
+template <typename P>
+const P* at(const void* base, size_t off) {
+  return reinterpret_cast<const P*>(static_cast<const char*>(base) + off);
+}
+
+GemmArgs mk_gemm(int dtype, int M, int N, int K, int a_mn, const void* A, int64_t lda, int b_mn,
+                 const void* B, int64_t ldb, int epi, void* C, int64_t ldc) {
+  GemmArgs g;
+  g.dtype = dtype; g.M = M; g.N = N; g.K = K;
+  g.a_mn = a_mn; g.A = A; g.lda = lda;
+  g.b_mn = b_mn; g.B = B; g.ldb = ldb;
+  g.epi = epi; g.C = C; g.ldc = ldc;
+  return g;
+}
+
+}  // namespace
+}  // namespace mgb
+
+using namespace mgb;
+
+extern "C" {
+
+int32_t mgb_version(void) { return 100; }
+
+const char* mgb_status_string(mgb_status s) {
+  switch (s) {
+    case MGB_OK: return "ok";
+    case MGB_ERR_INVALID_ARG: return "invalid argument";
+    case MGB_ERR_UNSUPPORTED: return "unsupported configuration";
+    case MGB_ERR_MISALIGNED: return "pointer or row stride not 16-byte aligned";
+    case MGB_ERR_WORKSPACE_TOO_SMALL: return "workspace or saved buffer too small";
+    case MGB_ERR_ARCH: return "device is not sm_103 (GB300)";
+    case MGB_ERR_CUDA: return "CUDA runtime error";
+    case MGB_ERR_DEVICE_TIMEOUT: return "a bounded device-side wait ran out";
+    case MGB_ERR_NOT_IMPLEMENTED: return "not implemented";
+  }
+  return "unknown status";
+}
+
+mgb_status mgb_device_status(void* stream) {
+  if (cudaStreamSynchronize(as_stream(stream)) != cudaSuccess) return MGB_ERR_CUDA;
+  int w = 0;
+  if (cudaMemcpyFromSymbol(&w, g_error_word, sizeof(int)) != cudaSuccess) return MGB_ERR_CUDA;
+  if (w != 0) {
+    const int zero = 0;
+    if (cudaMemcpyToSymbol(g_error_word, &zero, sizeof(int)) != cudaSuccess) return MGB_ERR_CUDA;
+  }
+  return (w & kErrTimeout) ? MGB_ERR_DEVICE_TIMEOUT : MGB_OK;
+}
+
+mgb_status mgb_selftest_wait_timeout(uint64_t limit_ns, void* stream) {
+  if (limit_ns > 5000000000ull) return MGB_ERR_INVALID_ARG;
+  MGB_TRY(check_arch());
+  int* err = device_error_word();
+  if (err == nullptr) return MGB_ERR_CUDA;
+  selftest_wait_kernel<<<1, 32, 0, as_stream(stream)>>>(limit_ns, err);
+  return cudaGetLastError() == cudaSuccess ? MGB_OK : MGB_ERR_CUDA;
+}
+
+mgb_status mgb_block_sizes(const mgb_block_desc* desc, size_t* saved_bytes, size_t* fwd_ws_bytes,
+                           size_t* bwd_ws_bytes) {
+  MGB_TRY(validate_desc(desc));
+  Plan p;
+  make_plan(desc, &p);
+  if (saved_bytes) *saved_bytes = p.saved;
+  if (fwd_ws_bytes) *fwd_ws_bytes = 0;
+  if (bwd_ws_bytes) *bwd_ws_bytes = p.bwd;
+  return MGB_OK;
+}
+
+mgb_status mgb_block_fwd(const mgb_block_desc* desc, const mgb_block_weights* w, const void* x,
+                         void* y, void* saved, size_t saved_bytes, void* ws, size_t ws_bytes,
+                         void* stream) {
+  (void)ws; (void)ws_bytes;
+  MGB_TRY(validate_desc(desc));
+  MGB_TRY(check_weights(desc, w));
+  Plan p;
+  make_plan(desc, &p);
+  if (!x || !y || !saved) return MGB_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(y) || !aligned16(saved)) return MGB_ERR_MISALIGNED;
+  if (saved_bytes < p.saved) return MGB_ERR_WORKSPACE_TOO_SMALL;
+  MGB_TRY(check_arch());
+  if (p.T == 0) return MGB_OK;
+  cudaStream_t st = as_stream(stream);
+  const int dt = desc->dtype;
+  const int T = p.T, H = p.H;
+  float* mu1 = at<float>(saved, p.s_mu1); float* rs1 = at<float>(saved, p.s_rs1);
+  float* mu2 = at<float>(saved, p.s_mu2); float* rs2 = at<float>(saved, p.s_rs2);
+  float* lse = at<float>(saved, p.s_lse);
+  void* qkv = at<char>(saved, p.s_qkv);
+  void* O = at<char>(saved, p.s_O);
+  void* h = at<char>(saved, p.s_h);
+  void* u = at<char>(saved, p.s_u);
+  void* a = at<char>(saved, p.s_a);
+
+  // attention sublayer input
+  const void* a_in = x;
+  if (p.pre) {
+    void* xn = at<char>(saved, p.s_xn);
+    MGB_TRY(layernorm_fwd_launch(T, H, dt, desc->ln_eps, x, w->ln1_g, w->ln1_b, xn, mu1, rs1, st));
+    a_in = xn;
+  }
+  GemmArgs g = mk_gemm(dt, T, p.Wqkv, H, 0, a_in, H, 0, w->w_qkv, H, EPI_STORE, qkv, p.Wqkv);
+  g.bias = w->b_qkv;
+  MGB_TRY(gemm_launch(g, st));
+
+  AttnArgs at_{};
+  at_.B = p.B; at_.S = p.S; at_.nq = p.nq; at_.nkv = p.nkv; at_.d = p.d;
+  at_.causal = desc->causal; at_.dtype = dt;
+  at_.q = qkv;
+  at_.k = static_cast<char*>(qkv) + p.es * p.Dq;
+  at_.v = static_cast<char*>(qkv) + p.es * (p.Dq + (size_t)p.nkv * p.d);
+  at_.ld_q = p.Wqkv; at_.ld_kv = p.Wqkv;
+  at_.o = O; at_.ld_o = p.Dq; at_.lse = lse;
+  MGB_TRY(attention_fwd_launch(at_, st));
+
+  // output projection + residual (Pre: h; Post: r1 then h = LN1(r1))
+  void* r1 = p.pre ? h : at<char>(saved, p.s_r1);
+  g = mk_gemm(dt, T, H, p.Dq, 0, O, p.Dq, 0, w->w_o, p.Dq, EPI_BIAS_RESID, r1, H);
+  g.bias = w->b_o; g.resid = x; g.ldr = H;
+  MGB_TRY(gemm_launch(g, st));
+  const void* f_in;
+  if (p.pre) {
+    void* hn = at<char>(saved, p.s_hn);
+    MGB_TRY(layernorm_fwd_launch(T, H, dt, desc->ln_eps, h, w->ln2_g, w->ln2_b, hn, mu2, rs2, st));
+    f_in = hn;
+  } else {
+    MGB_TRY(layernorm_fwd_launch(T, H, dt, desc->ln_eps, r1, w->ln1_g, w->ln1_b, h, mu1, rs1, st));
+    f_in = h;
+  }
+  // fc1 + activation
+  g = mk_gemm(dt, T, p.W, H, 0, f_in, H, 0, w->w_1, H,
+              p.swiglu ? EPI_BIAS_SWIGLU : EPI_BIAS_GELU, u, p.W);
+  g.bias = w->b_1; g.C2 = a; g.ldc2 = p.F; g.glu_block = desc->glu_block;
+  MGB_TRY(gemm_launch(g, st));
+  // fc2 + residual (Pre: y; Post: r2 then y = LN2(r2))
+  void* r2 = p.pre ? y : at<char>(saved, p.s_r2);
+  g = mk_gemm(dt, T, H, p.F, 0, a, p.F, 0, w->w_2, p.F, EPI_BIAS_RESID, r2, H);
+  g.bias = w->b_2; g.resid = h; g.ldr = H;
+  MGB_TRY(gemm_launch(g, st));
+  if (!p.pre)
+    MGB_TRY(layernorm_fwd_launch(T, H, dt, desc->ln_eps, r2, w->ln2_g, w->ln2_b, y, mu2, rs2, st));
+  return MGB_OK;
+}
+
+mgb_status mgb_block_bwd(const mgb_block_desc* desc, const mgb_block_weights* w, const void* x,
+                         const void* dy, const void* saved, size_t saved_bytes, void* dx,
+                         const mgb_block_grads* gr, void* ws, size_t ws_bytes, void* stream) {
+  MGB_TRY(validate_desc(desc));
+  MGB_TRY(check_weights(desc, w));
+  Plan p;
+  make_plan(desc, &p);
+  if (!x || !dy || !saved || !dx || !gr || (!ws && p.bwd > 0)) return MGB_ERR_INVALID_ARG;
+  if (!aligned16(x) || !aligned16(dy) || !aligned16(saved) || !aligned16(dx) || !aligned16(ws))
+    return MGB_ERR_MISALIGNED;
+  {
+    const void* gs[] = {gr->w_qkv, gr->b_qkv, gr->w_o, gr->b_o, gr->w_1, gr->b_1,
+                        gr->w_2,   gr->b_2,   gr->ln1_g, gr->ln1_b, gr->ln2_g, gr->ln2_b};
+    for (const void* q : gs)
+      if (!aligned16(q)) return MGB_ERR_MISALIGNED;
+    if (!desc->has_bias && (gr->b_qkv || gr->b_o || gr->b_1 || gr->b_2)) return MGB_ERR_INVALID_ARG;
+    if (!desc->ln_affine && (gr->ln1_g || gr->ln1_b || gr->ln2_g || gr->ln2_b))
+      return MGB_ERR_INVALID_ARG;
+  }
+  if (saved_bytes < p.saved) return MGB_ERR_WORKSPACE_TOO_SMALL;
+  if (ws_bytes < p.bwd) return MGB_ERR_WORKSPACE_TOO_SMALL;
+  MGB_TRY(check_arch());
+  cudaStream_t st = as_stream(stream);
+  const int dt = desc->dtype;
+  const int T = p.T, H = p.H;
+  const float* mu1 = at<float>(saved, p.s_mu1); const float* rs1 = at<float>(saved, p.s_rs1);
+  const float* mu2 = at<float>(saved, p.s_mu2); const float* rs2 = at<float>(saved, p.s_rs2);
+  const float* lse = at<float>(saved, p.s_lse);
+  const void* qkv = at<char>(saved, p.s_qkv);
+  const void* O = at<char>(saved, p.s_O);
+  const void* h = at<char>(saved, p.s_h);
+  const void* u = at<char>(saved, p.s_u);
+  const void* a = at<char>(saved, p.s_a);
+  const void* a_in = p.pre ? at<char>(saved, p.s_xn) : x;
+  const void* f_in = p.pre ? at<char>(saved, p.s_hn) : h;
+  void* d_ffn = at<char>(ws, p.w_dffn);
+  void* d_h = at<char>(ws, p.w_dh);
+  void* d_r2 = at<char>(ws, p.w_dr2);
+  void* du = at<char>(ws, p.w_du);
+  void* dO = at<char>(ws, p.w_dO);
+  void* dqkv = at<char>(ws, p.w_dqkv);
+  void* dxn = at<char>(ws, p.w_dxn);
+  float* delta = at<float>(ws, p.w_delta);
+  float* cparts = at<float>(ws, p.w_cparts);
+  float* lparts = at<float>(ws, p.w_lparts);
+
+  // gradient at the fc2 residual sum (Pre: dy itself; Post: through LN2)
+  const void* dr2 = dy;
+  if (!p.pre) {
+    MGB_TRY(layernorm_bwd_launch(T, H, dt, at<char>(saved, p.s_r2), mu2, rs2, w->ln2_g, dy, nullptr,
+                                 d_r2, gr->ln2_g, gr->ln2_b, lparts, p.lparts, st));
+    dr2 = d_r2;
+  }
+  // fc2: db2, dW2 = dr2^T a, du = (dr2 W2) * act'(u)
+  if (gr->b_2) MGB_TRY(colsum_launch(T, H, dt, dr2, H, gr->b_2, cparts, p.cparts, st));
+  if (gr->w_2)
+    MGB_TRY(gemm_launch(mk_gemm(dt, H, p.F, T, 1, dr2, H, 1, a, p.F, EPI_STORE, gr->w_2, p.F), st));
+  {
+    GemmArgs g = mk_gemm(dt, T, p.F, H, 0, dr2, H, 1, w->w_2, p.F,
+                         p.swiglu ? EPI_DSWIGLU : EPI_DGELU, du, p.W);
+    g.aux = u; g.ldaux = p.W; g.glu_block = desc->glu_block;
+    MGB_TRY(gemm_launch(g, st));
+  }
+  // fc1: db1, dW1 = du^T f_in, d f_in = du W1
+  if (gr->b_1) MGB_TRY(colsum_launch(T, p.W, dt, du, p.W, gr->b_1, cparts, p.cparts, st));
+  if (gr->w_1)
+    MGB_TRY(gemm_launch(mk_gemm(dt, p.W, H, T, 1, du, p.W, 1, f_in, H, EPI_STORE, gr->w_1, H), st));
+  const void* dr1;
+  if (p.pre) {
+    MGB_TRY(gemm_launch(mk_gemm(dt, T, H, p.W, 0, du, p.W, 1, w->w_1, H, EPI_STORE, d_ffn, H), st));
+    // dh = dy + LN2_bwd(d hn)
+    MGB_TRY(layernorm_bwd_launch(T, H, dt, h, mu2, rs2, w->ln2_g, d_ffn, dy, d_h, gr->ln2_g,
+                                 gr->ln2_b, lparts, p.lparts, st));
+    dr1 = d_h;
+  } else {
+    // dh = du W1 + dr2 (h feeds fc1 and the fc2 residual), dr1 = LN1_bwd(dh)
+    GemmArgs g = mk_gemm(dt, T, H, p.W, 0, du, p.W, 1, w->w_1, H, EPI_BIAS_RESID, d_h, H);
+    g.resid = dr2; g.ldr = H;
+    MGB_TRY(gemm_launch(g, st));
+    MGB_TRY(layernorm_bwd_launch(T, H, dt, at<char>(saved, p.s_r1), mu1, rs1, w->ln1_g, d_h,
+                                 nullptr, d_ffn, gr->ln1_g, gr->ln1_b, lparts, p.lparts, st));
+    dr1 = d_ffn;
+  }
+  // output projection: dbo, dWo = dr1^T O, dO = dr1 Wo
+  if (gr->b_o) MGB_TRY(colsum_launch(T, H, dt, dr1, H, gr->b_o, cparts, p.cparts, st));
+  if (gr->w_o)
+    MGB_TRY(gemm_launch(mk_gemm(dt, H, p.Dq, T, 1, dr1, H, 1, O, p.Dq, EPI_STORE, gr->w_o, p.Dq), st));
+  MGB_TRY(gemm_launch(mk_gemm(dt, T, p.Dq, H, 0, dr1, H, 1, w->w_o, p.Dq, EPI_STORE, dO, p.Dq), st));
+  // attention backward into the fused dqkv buffer
+  {
+    AttnArgs at_{};
+    at_.B = p.B; at_.S = p.S; at_.nq = p.nq; at_.nkv = p.nkv; at_.d = p.d;
+    at_.causal = desc->causal; at_.dtype = dt;
+    at_.q = qkv;
+    at_.k = static_cast<const char*>(qkv) + p.es * p.Dq;
+    at_.v = static_cast<const char*>(qkv) + p.es * (p.Dq + (size_t)p.nkv * p.d);
+    at_.ld_q = p.Wqkv; at_.ld_kv = p.Wqkv;
+    at_.o = const_cast<void*>(O); at_.ld_o = p.Dq; at_.lse = const_cast<float*>(lse);
+    at_.dout = dO; at_.ld_do = p.Dq;
+    at_.dq = dqkv;
+    at_.dk = static_cast<char*>(dqkv) + p.es * p.Dq;
+    at_.dv = static_cast<char*>(dqkv) + p.es * (p.Dq + (size_t)p.nkv * p.d);
+    at_.ld_dq = p.Wqkv; at_.ld_dkv = p.Wqkv;
+    at_.delta = delta;
+    MGB_TRY(attention_bwd_launch(at_, st));
+  }
+  // QKV: dbqkv, dWqkv = dqkv^T a_in, d a_in = dqkv Wqkv
+  if (gr->b_qkv) MGB_TRY(colsum_launch(T, p.Wqkv, dt, dqkv, p.Wqkv, gr->b_qkv, cparts, p.cparts, st));
+  if (gr->w_qkv)
+    MGB_TRY(gemm_launch(
+        mk_gemm(dt, p.Wqkv, H, T, 1, dqkv, p.Wqkv, 1, a_in, H, EPI_STORE, gr->w_qkv, H), st));
+  if (p.pre) {
+    MGB_TRY(gemm_launch(mk_gemm(dt, T, H, p.Wqkv, 0, dqkv, p.Wqkv, 1, w->w_qkv, H, EPI_STORE, dxn, H),
+                        st));
+    MGB_TRY(layernorm_bwd_launch(T, H, dt, x, mu1, rs1, w->ln1_g, dxn, dr1, dx, gr->ln1_g, gr->ln1_b,
+                                 lparts, p.lparts, st));
+  } else {
+    GemmArgs g = mk_gemm(dt, T, H, p.Wqkv, 0, dqkv, p.Wqkv, 1, w->w_qkv, H, EPI_BIAS_RESID, dx, H);
+    g.resid = dr1; g.ldr = H;
+    MGB_TRY(gemm_launch(g, st));
+  }
+  return MGB_OK;
+}
+
+// ------------------------------------------------------------ cross-entropy
+
+static mgb_status validate_ce(const mgb_ce_desc* d) {
+  if (d == nullptr) return MGB_ERR_INVALID_ARG;
+  if (fault_injected()) return MGB_ERR_INVALID_ARG;
+  if (d->tokens < 0 || d->hidden < 1 || d->vocab < 1 || d->chunk < 1) return MGB_ERR_INVALID_ARG;
+  if (d->dtype != MGB_BF16) return MGB_ERR_UNSUPPORTED;
+  if (d->hidden % 8 || d->vocab % 8 || d->chunk % 8) return MGB_ERR_MISALIGNED;
+  if (!(d->grad_scale == d->grad_scale)) return MGB_ERR_INVALID_ARG;
+  return MGB_OK;
+}
+
+struct CEPlan {
+  int n_chunks, C;
+  size_t logits, m, s, t, lse, dh, total;
+};
+
+static void ce_plan(const mgb_ce_desc* d, CEPlan* p) {
+  const size_t T = d->tokens;
+  p->C = d->chunk < d->vocab ? d->chunk : d->vocab;
+  p->n_chunks = (d->vocab + p->C - 1) / p->C;
+  size_t o = 0;
+  auto take = [&](size_t bytes) { const size_t a = o; o += al256(bytes); return a; };
+  p->logits = take(2 * T * p->C);
+  p->m = take(4 * T * p->n_chunks);
+  p->s = take(4 * T * p->n_chunks);
+  p->t = take(4 * T * p->n_chunks);
+  p->lse = take(4 * T);
+  p->dh = take(4 * T * d->hidden);
+  p->total = o;
+}
+
+mgb_status mgb_vocab_ce_sizes(const mgb_ce_desc* desc, size_t* ws_bytes) {
+  MGB_TRY(validate_ce(desc));
+  CEPlan p;
+  ce_plan(desc, &p);
+  if (ws_bytes) *ws_bytes = p.total;
+  return MGB_OK;
+}
+
+mgb_status mgb_vocab_ce_fwd_bwd(const mgb_ce_desc* desc, const void* hidden, const void* emb,
+                                const int32_t* targets, float* loss_per_token, float* loss_mean,
+                                float* lse, void* d_hidden, void* d_emb, void* ws, size_t ws_bytes,
+                                void* stream) {
+  MGB_TRY(validate_ce(desc));
+  CEPlan p;
+  ce_plan(desc, &p);
+  if (!hidden || !emb || !targets || !loss_per_token || !loss_mean || !ws)
+    return MGB_ERR_INVALID_ARG;
+  const void* ptrs[] = {hidden, emb, targets, loss_per_token, lse, d_hidden, d_emb, ws};
+  for (const void* q : ptrs)
+    if (!aligned16(q)) return MGB_ERR_MISALIGNED;
+  if (ws_bytes < p.total) return MGB_ERR_WORKSPACE_TOO_SMALL;
+  MGB_TRY(check_arch());
+  cudaStream_t st = as_stream(stream);
+  const int T = desc->tokens, H = desc->hidden, V = desc->vocab, C = p.C;
+  void* logits = at<char>(ws, p.logits);
+  float* m = at<float>(ws, p.m);
+  float* s = at<float>(ws, p.s);
+  float* t = at<float>(ws, p.t);
+  float* lse_buf = lse ? lse : at<float>(ws, p.lse);
+  float* dh_acc = at<float>(ws, p.dh);
+  const bf16* E = static_cast<const bf16*>(emb);
+  for (int c = 0; c < p.n_chunks; ++c) {
+    const int v0 = c * C, Cc = (V - v0) < C ? (V - v0) : C;
+    MGB_TRY(gemm_launch(mk_gemm(MGB_BF16, T, Cc, H, 0, hidden, H, 0, E + (size_t)v0 * H, H,
+                                EPI_STORE, logits, C), st));
+    MGB_TRY(ce_stats_launch(T, Cc, v0, logits, C, targets, m + (size_t)c * T, s + (size_t)c * T,
+                            t + (size_t)c * T, st));
+  }
+  MGB_TRY(ce_combine_launch(T, p.n_chunks, m, s, t, lse_buf, loss_per_token, loss_mean, st));
+  if (!d_hidden && !d_emb) return MGB_OK;
+  for (int c = 0; c < p.n_chunks; ++c) {
+    const int v0 = c * C, Cc = (V - v0) < C ? (V - v0) : C;
+    MGB_TRY(gemm_launch(mk_gemm(MGB_BF16, T, Cc, H, 0, hidden, H, 0, E + (size_t)v0 * H, H,
+                                EPI_STORE, logits, C), st));
+    MGB_TRY(ce_grad_launch(T, Cc, v0, logits, C, targets, lse_buf, desc->grad_scale, st));
+    if (d_hidden) {
+      GemmArgs g = mk_gemm(MGB_BF16, T, H, Cc, 0, logits, C, 1, E + (size_t)v0 * H, H, EPI_F32,
+                           dh_acc, H);
+      g.accumulate = c > 0;
+      if (c == p.n_chunks - 1) { g.C2 = d_hidden; g.ldc2 = H; }
+      MGB_TRY(gemm_launch(g, st));
+    }
+    if (d_emb)
+      MGB_TRY(gemm_launch(mk_gemm(MGB_BF16, Cc, H, T, 1, logits, C, 1, hidden, H, EPI_STORE,
+                                  static_cast<bf16*>(d_emb) + (size_t)v0 * H, H), st));
+  }
+  return MGB_OK;
+}
+
+// ------------------------------------------------------------ building blocks
+
+mgb_status mgb_gemm(const mgb_gemm_desc* d, const void* a, const void* b, const void* bias, void* c,
+                    void* stream) {
+  if (d == nullptr) return MGB_ERR_INVALID_ARG;
+  if (fault_injected()) return MGB_ERR_INVALID_ARG;
+  GemmArgs g = mk_gemm(d->dtype, d->m, d->n, d->k, d->a_major, a, d->lda, d->b_major, b, d->ldb,
+                       (d->c_f32 || d->dtype == MGB_F32) ? EPI_F32 : EPI_STORE, c, d->ldc);
+  if ((d->a_major | d->b_major) & ~1) return MGB_ERR_INVALID_ARG;
+  if (d->accumulate && !(d->c_f32 || d->dtype == MGB_F32)) return MGB_ERR_INVALID_ARG;
+  g.bias = bias;
+  g.alpha = d->alpha;
+  g.accumulate = d->accumulate;
+  MGB_TRY(gemm_check(g));
+  MGB_TRY(check_arch());
+  return gemm_launch(g, as_stream(stream));
+}
+
+mgb_status mgb_layernorm_fwd(int32_t rows, int32_t cols, int32_t dtype, float eps, const void* x,
+                             const void* gamma, const void* beta, void* y, float* mean, float* rstd,
+                             void* stream) {
+  if (fault_injected()) return MGB_ERR_INVALID_ARG;
+  if (dtype != MGB_BF16 && dtype != MGB_F32) return MGB_ERR_INVALID_ARG;
+  if (rows < 0 || cols < 1 || !x || !y) return MGB_ERR_INVALID_ARG;
+  const void* ps[] = {x, gamma, beta, y, mean, rstd};
+  for (const void* q : ps)
+    if (!aligned16(q)) return MGB_ERR_MISALIGNED;
+  MGB_TRY(check_arch());
+  return layernorm_fwd_launch(rows, cols, dtype, eps, x, gamma, beta, y, mean, rstd,
+                              as_stream(stream));
+}
+
+mgb_status mgb_attention_fwd(int32_t batch, int32_t seq, int32_t n_q_heads, int32_t n_kv_heads,
+                             int32_t head_dim, int32_t causal, int32_t dtype, const void* q,
+                             const void* k, const void* v, int64_t ld_q, int64_t ld_kv, void* o,
+                             float* lse, void* stream) {
+  if (fault_injected()) return MGB_ERR_INVALID_ARG;
+  if (batch < 0 || seq < 1 || n_q_heads < 1 || n_kv_heads < 1 || n_q_heads % n_kv_heads)
+    return MGB_ERR_INVALID_ARG;
+  if (dtype != MGB_BF16 && dtype != MGB_F32) return MGB_ERR_INVALID_ARG;
+  if (!q || !k || !v || !o || !lse) return MGB_ERR_INVALID_ARG;
+  if (dtype == MGB_BF16 && head_dim != 64 && head_dim != 128) return MGB_ERR_UNSUPPORTED;
+  if (ld_q < (int64_t)n_q_heads * head_dim || ld_kv < (int64_t)n_kv_heads * head_dim)
+    return MGB_ERR_INVALID_ARG;
+  const int vm = dtype == MGB_BF16 ? 8 : 1;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(o) || ld_q % vm || ld_kv % vm)
+    return MGB_ERR_MISALIGNED;
+  MGB_TRY(check_arch());
+  AttnArgs a{};
+  a.B = batch; a.S = seq; a.nq = n_q_heads; a.nkv = n_kv_heads; a.d = head_dim;
+  a.causal = causal ? 1 : 0; a.dtype = dtype;
+  a.q = q; a.k = k; a.v = v; a.ld_q = ld_q; a.ld_kv = ld_kv;
+  a.o = o; a.ld_o = (int64_t)n_q_heads * head_dim; a.lse = lse;
+  return attention_fwd_launch(a, as_stream(stream));
+}
+
+}  // extern "C"

@@ -1,0 +1,197 @@
+// Streaming kernels of the vocab-chunked cross-entropy.
+//
+// "02 - How a whole Transformer block is split", section 4: the loss is
+// assembled from per-vocab-shard partials - the shard's row max, its sum of
+// exp(l - max), and the target logit (nonzero only in the shard owning the
+// target) - combined across shards by a max and two sums:
+//   M = max_c m_c,  S = sum_c s_c exp(m_c - M),  LSE = M + log S,
+//   loss_t = LSE_t - sum_c target_c.
+// Backward is local per shard: G = (softmax - onehot(target)) * scale.
+// Here the shards are vocab chunks processed one after another on one GPU.
+//
+//   ce_stats   one block per token row of a [T, C] bf16 logits chunk: a single
+//              pass of 16-byte loads with a running (max, sum) pair per thread
+//              (rescaled when the max grows), merged across the block.
+//   ce_combine one block: chunk partials -> LSE, per-token loss, mean loss
+//              (fixed-order reduction, deterministic).
+//   ce_grad    one block per row: rewrites the logits chunk in place with G.
+#include "common.cuh"
+#include "internal.h"
+
+namespace mgb {
+
+namespace {
+
+constexpr float LOG2E = 1.4426950408889634f;
+constexpr float LN2 = 0.6931471805599453f;
+constexpr int CE_THREADS = 256;
+
+// merge running (max, sum) pairs in the log2 domain
+__device__ __forceinline__ void ms_merge(float& m, float& s, float m2, float s2) {
+  const float mn = fmaxf(m, m2);
+  if (mn == -INFINITY) return;
+  s = s * exp2f(m - mn) + s2 * exp2f(m2 - mn);
+  m = mn;
+}
+
+__global__ void __launch_bounds__(CE_THREADS) ce_stats_kernel(int T, int C, int v0,
+                                                               const bf16* __restrict__ logits,
+                                                               int64_t ldl,
+                                                               const int32_t* __restrict__ tgt,
+                                                               float* m_out, float* s_out,
+                                                               float* t_out) {
+  const int row = blockIdx.x;
+  const bf16* l = logits + (int64_t)row * ldl;
+  const int nvec = C / 8;
+  float m = -INFINITY, s = 0.0f;
+  int v = threadIdx.x;
+  // four 16-byte loads in flight per thread
+  for (; v + 3 * CE_THREADS < nvec; v += 4 * CE_THREADS) {
+    uint4 w[4];
+#pragma unroll
+    for (int u = 0; u < 4; ++u) w[u] = __ldg(reinterpret_cast<const uint4*>(l) + v + u * CE_THREADS);
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      const uint32_t ww[4] = {w[u].x, w[u].y, w[u].z, w[u].w};
+      float x[8];
+      float mx = -INFINITY;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float2 f = unpack_bf16x2(ww[i]);
+        x[2 * i] = f.x * LOG2E;
+        x[2 * i + 1] = f.y * LOG2E;
+        mx = fmaxf(mx, fmaxf(x[2 * i], x[2 * i + 1]));
+      }
+      float acc = 0.0f;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc += exp2f(x[i] - mx);
+      ms_merge(m, s, mx, acc);
+    }
+  }
+  for (; v < nvec; v += CE_THREADS) {
+    const uint4 w = __ldg(reinterpret_cast<const uint4*>(l) + v);
+    const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+    float x[8];
+    float mx = -INFINITY;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 f = unpack_bf16x2(ww[i]);
+      x[2 * i] = f.x * LOG2E;
+      x[2 * i + 1] = f.y * LOG2E;
+      mx = fmaxf(mx, fmaxf(x[2 * i], x[2 * i + 1]));
+    }
+    float acc = 0.0f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc += exp2f(x[i] - mx);
+    ms_merge(m, s, mx, acc);
+  }
+  // block merge
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
+    const float s2 = __shfl_xor_sync(0xffffffffu, s, o);
+    ms_merge(m, s, m2, s2);
+  }
+  __shared__ float sm_m[CE_THREADS / 32], sm_s[CE_THREADS / 32];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (lane == 0) {
+    sm_m[warp] = m;
+    sm_s[warp] = s;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float M = sm_m[0], Ssum = sm_s[0];
+    for (int w = 1; w < CE_THREADS / 32; ++w) ms_merge(M, Ssum, sm_m[w], sm_s[w]);
+    m_out[row] = M * LN2;
+    s_out[row] = Ssum;
+    const int tc = tgt[row] - v0;
+    t_out[row] = (tc >= 0 && tc < C) ? __bfloat162float(l[tc]) : 0.0f;
+  }
+}
+
+__global__ void __launch_bounds__(1024) ce_combine_kernel(int T, int n_chunks, const float* m,
+                                                          const float* s, const float* t,
+                                                          float* lse, float* loss,
+                                                          float* loss_mean) {
+  float part = 0.0f;
+  for (int i = threadIdx.x; i < T; i += blockDim.x) {
+    float M = -INFINITY;
+    for (int c = 0; c < n_chunks; ++c) M = fmaxf(M, m[(int64_t)c * T + i]);
+    float S = 0.0f, tl = 0.0f;
+    for (int c = 0; c < n_chunks; ++c) {
+      S += s[(int64_t)c * T + i] * expf(m[(int64_t)c * T + i] - M);
+      tl += t[(int64_t)c * T + i];
+    }
+    const float L = M + logf(S);
+    lse[i] = L;
+    const float li = L - tl;
+    if (loss) loss[i] = li;
+    part += li;
+  }
+  __shared__ float red[32];
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = part;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float tot = 0.0f;
+    for (int w = 0; w < (int)(blockDim.x >> 5); ++w) tot += red[w];
+    if (loss_mean) *loss_mean = T > 0 ? tot / T : 0.0f;
+  }
+}
+
+__global__ void __launch_bounds__(CE_THREADS) ce_grad_kernel(int T, int C, int v0,
+                                                              bf16* __restrict__ logits,
+                                                              int64_t ldl,
+                                                              const int32_t* __restrict__ tgt,
+                                                              const float* __restrict__ lse,
+                                                              float scale) {
+  const int row = blockIdx.x;
+  bf16* l = logits + (int64_t)row * ldl;
+  const float L2 = lse[row] * LOG2E;
+  const int tc = tgt[row] - v0;
+  const int nvec = C / 8;
+  for (int v = threadIdx.x; v < nvec; v += CE_THREADS) {
+    uint4 w = *(reinterpret_cast<const uint4*>(l) + v);
+    uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 f = unpack_bf16x2(ww[i]);
+      float g0 = exp2f(f.x * LOG2E - L2);
+      float g1 = exp2f(f.y * LOG2E - L2);
+      const int c0 = v * 8 + 2 * i;
+      if (c0 == tc) g0 -= 1.0f;
+      if (c0 + 1 == tc) g1 -= 1.0f;
+      ww[i] = pack_bf16x2(g0 * scale, g1 * scale);
+    }
+    w.x = ww[0]; w.y = ww[1]; w.z = ww[2]; w.w = ww[3];
+    *(reinterpret_cast<uint4*>(l) + v) = w;
+  }
+}
+
+}  // namespace
+
+mgb_status ce_stats_launch(int T, int C, int v0, const void* logits, int64_t ldl,
+                           const int32_t* targets, float* m, float* s, float* t, cudaStream_t st) {
+  if (T == 0) return MGB_OK;
+  LaunchScope scope(PROF_CE_STATS, st);
+  ce_stats_kernel<<<T, CE_THREADS, 0, st>>>(T, C, v0, (const bf16*)logits, ldl, targets, m, s, t);
+  return cudaGetLastError() == cudaSuccess ? MGB_OK : MGB_ERR_CUDA;
+}
+
+mgb_status ce_combine_launch(int T, int n_chunks, const float* m, const float* s, const float* t,
+                             float* lse, float* loss, float* loss_mean, cudaStream_t st) {
+  LaunchScope scope(PROF_CE_COMBINE, st);
+  ce_combine_kernel<<<1, 1024, 0, st>>>(T, n_chunks, m, s, t, lse, loss, loss_mean);
+  return cudaGetLastError() == cudaSuccess ? MGB_OK : MGB_ERR_CUDA;
+}
+
+mgb_status ce_grad_launch(int T, int C, int v0, void* logits, int64_t ldl, const int32_t* targets,
+                          const float* lse, float scale, cudaStream_t st) {
+  if (T == 0) return MGB_OK;
+  LaunchScope scope(PROF_CE_GRAD, st);
+  ce_grad_kernel<<<T, CE_THREADS, 0, st>>>(T, C, v0, (bf16*)logits, ldl, targets, lse, scale);
+  return cudaGetLastError() == cudaSuccess ? MGB_OK : MGB_ERR_CUDA;
+}
+
+}  // namespace mgb

@@ -1,0 +1,200 @@
+// float32 GEMM on the CUDA cores (FFMA), for the float32 layer.
+//
+// Same contract as the tensor-core GEMM (internal.h GemmArgs): acc[m][n] =
+// alpha * sum_k A(m,k) B(n,k) with either operand K-major or MN-major, and the
+// same epilogues. TF32 tensor cores are not used: their 10-bit mantissa inputs
+// cannot meet a 1e-4 relative error on float32 layers.
+//
+// 64 x 64 output tile per 256-thread block, 4 x 4 outputs per thread, K
+// staged through shared memory 16 at a time.
+#include "common.cuh"
+#include "internal.h"
+
+namespace mgb {
+
+mgb_status gemm_tc_launch(const GemmArgs& g, cudaStream_t st);
+
+namespace {
+
+constexpr int TM = 64, TN = 64, TK = 16;
+
+struct SimtParams {
+  int M, N, K, a_mn, b_mn;
+  const float* A; int64_t lda;
+  const float* B; int64_t ldb;
+  int epi; float alpha;
+  float* C; int64_t ldc;
+  const float* bias;
+  const float* resid; int64_t ldr;
+  float* C2; int64_t ldc2;
+  const float* aux; int64_t ldaux;
+  int glu_block, accumulate;
+};
+
+__device__ __forceinline__ void epi_elem(const SimtParams& p, int m, int n, float acc) {
+  switch (p.epi) {
+    case EPI_STORE:
+    case EPI_F32: {
+      float v = acc + (p.bias ? p.bias[n] : 0.0f);
+      float* c = p.C + (int64_t)m * p.ldc + n;
+      if (p.accumulate) v += *c;
+      *c = v;
+      if (p.C2) p.C2[(int64_t)m * p.ldc2 + n] = v;
+      break;
+    }
+    case EPI_BIAS_GELU: {
+      const float u = acc + (p.bias ? p.bias[n] : 0.0f);
+      p.C[(int64_t)m * p.ldc + n] = u;
+      p.C2[(int64_t)m * p.ldc2 + n] = gelu_erf(u);
+      break;
+    }
+    case EPI_BIAS_SWIGLU:  // u only; the activation is a separate pass
+      p.C[(int64_t)m * p.ldc + n] = acc + (p.bias ? p.bias[n] : 0.0f);
+      break;
+    case EPI_BIAS_RESID:
+      p.C[(int64_t)m * p.ldc + n] =
+          p.resid[(int64_t)m * p.ldr + n] + acc + (p.bias ? p.bias[n] : 0.0f);
+      break;
+    case EPI_DGELU:
+      p.C[(int64_t)m * p.ldc + n] = acc * gelu_erf_grad(p.aux[(int64_t)m * p.ldaux + n]);
+      break;
+    case EPI_DSWIGLU: {
+      const int gb = p.glu_block;
+      const int i = n / gb, cc = n % gb;
+      const int64_t cg = (int64_t)2 * i * gb + cc, cu = cg + gb;
+      const float g = p.aux[(int64_t)m * p.ldaux + cg], u = p.aux[(int64_t)m * p.ldaux + cu];
+      const float s = 1.0f / (1.0f + expf(-g));
+      p.C[(int64_t)m * p.ldc + cg] = acc * u * s * (1.0f + g * (1.0f - s));
+      p.C[(int64_t)m * p.ldc + cu] = acc * g * s;
+      break;
+    }
+    default:
+      break;
+  }
+}
+
+__global__ void __launch_bounds__(256) gemm_simt_kernel(const SimtParams p) {
+  __shared__ float As[TK][TM + 4];
+  __shared__ float Bs[TK][TN + 4];
+  const int tx = threadIdx.x % 16, ty = threadIdx.x / 16;
+  const int m0 = blockIdx.y * TM, n0 = blockIdx.x * TN;
+  float acc[4][4] = {};
+  for (int k0 = 0; k0 < p.K; k0 += TK) {
+    for (int i = threadIdx.x; i < TM * TK; i += 256) {
+      int mm, kk;
+      if (p.a_mn) { kk = i / TM; mm = i % TM; } else { mm = i / TK; kk = i % TK; }
+      const int m = m0 + mm, k = k0 + kk;
+      float v = 0.0f;
+      if (m < p.M && k < p.K) v = p.a_mn ? p.A[(int64_t)k * p.lda + m] : p.A[(int64_t)m * p.lda + k];
+      As[kk][mm] = v;
+    }
+    for (int i = threadIdx.x; i < TN * TK; i += 256) {
+      int nn, kk;
+      if (p.b_mn) { kk = i / TN; nn = i % TN; } else { nn = i / TK; kk = i % TK; }
+      const int n = n0 + nn, k = k0 + kk;
+      float v = 0.0f;
+      if (n < p.N && k < p.K) v = p.b_mn ? p.B[(int64_t)k * p.ldb + n] : p.B[(int64_t)n * p.ldb + k];
+      Bs[kk][nn] = v;
+    }
+    __syncthreads();
+#pragma unroll
+    for (int kk = 0; kk < TK; ++kk) {
+      float a[4], b[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) a[i] = As[kk][ty + 16 * i];
+#pragma unroll
+      for (int j = 0; j < 4; ++j) b[j] = Bs[kk][tx + 16 * j];
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(a[i], b[j], acc[i][j]);
+    }
+    __syncthreads();
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int m = m0 + ty + 16 * i;
+    if (m >= p.M) continue;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int n = n0 + tx + 16 * j;
+      if (n < p.N) epi_elem(p, m, n, p.alpha * acc[i][j]);
+    }
+  }
+}
+
+// a[m, i*gb + c] = silu(u[m, 2i*gb + c]) * u[m, (2i+1)*gb + c]   (float32)
+__global__ void swiglu_f32_kernel(int M, int F, int gb, const float* u, int64_t ldu, float* a,
+                                  int64_t lda) {
+  const int64_t total = (int64_t)M * F;
+  for (int64_t idx = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; idx < total;
+       idx += (int64_t)gridDim.x * blockDim.x) {
+    const int m = (int)(idx / F), c = (int)(idx % F);
+    const int i = c / gb, cc = c % gb;
+    const float g = u[(int64_t)m * ldu + 2 * i * gb + cc];
+    const float up = u[(int64_t)m * ldu + (2 * i + 1) * gb + cc];
+    a[(int64_t)m * lda + c] = g / (1.0f + expf(-g)) * up;
+  }
+}
+
+}  // namespace
+
+mgb_status gemm_check(const GemmArgs& g) {
+  if (g.M < 0 || g.N < 0 || g.K < 0) return MGB_ERR_INVALID_ARG;
+  if (g.dtype != MGB_BF16 && g.dtype != MGB_F32) return MGB_ERR_INVALID_ARG;
+  if (g.epi < EPI_STORE || g.epi > EPI_F32) return MGB_ERR_INVALID_ARG;
+  if ((g.M > 0 && g.N > 0) && (g.C == nullptr)) return MGB_ERR_INVALID_ARG;
+  if (g.K > 0 && g.M > 0 && g.N > 0 && (g.A == nullptr || g.B == nullptr)) return MGB_ERR_INVALID_ARG;
+  const int64_t a_inner = g.a_mn ? g.M : g.K, b_inner = g.b_mn ? g.N : g.K;
+  if (g.lda < a_inner || g.ldb < b_inner) return MGB_ERR_INVALID_ARG;
+  if ((g.epi == EPI_BIAS_GELU || g.epi == EPI_BIAS_SWIGLU) && g.C2 == nullptr) return MGB_ERR_INVALID_ARG;
+  if (g.epi == EPI_BIAS_RESID && g.resid == nullptr) return MGB_ERR_INVALID_ARG;
+  if ((g.epi == EPI_DGELU || g.epi == EPI_DSWIGLU) && g.aux == nullptr) return MGB_ERR_INVALID_ARG;
+  if (g.epi == EPI_BIAS_SWIGLU || g.epi == EPI_DSWIGLU) {
+    const int gb = g.glu_block;
+    if (gb <= 0) return MGB_ERR_INVALID_ARG;
+    const int width = g.epi == EPI_BIAS_SWIGLU ? g.N : 2 * g.N;
+    if (width % (2 * gb) != 0) return MGB_ERR_INVALID_ARG;
+    if (g.dtype == MGB_BF16 && (gb % 32 != 0 || 256 % (2 * gb) != 0)) return MGB_ERR_UNSUPPORTED;
+  }
+  if (g.dtype == MGB_BF16) {
+    // TMA: 16-byte aligned bases and row strides; 16-byte epilogue vectors.
+    auto al = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
+    if (!al(g.A) || !al(g.B) || !al(g.C) || !al(g.C2) || !al(g.resid) || !al(g.aux) || !al(g.bias))
+      return MGB_ERR_MISALIGNED;
+    if (g.lda % 8 || g.ldb % 8 || g.N % 8) return MGB_ERR_MISALIGNED;
+    const int64_t c_mult = g.epi == EPI_F32 ? 4 : 8;
+    if (g.ldc % c_mult || (g.C2 && g.ldc2 % 8) || (g.resid && g.ldr % 8) || (g.aux && g.ldaux % 8))
+      return MGB_ERR_MISALIGNED;
+    if (g.accumulate && g.epi != EPI_F32) return MGB_ERR_INVALID_ARG;
+  }
+  return MGB_OK;
+}
+
+mgb_status gemm_launch(const GemmArgs& g, cudaStream_t st) {
+  mgb_status s = gemm_check(g);
+  if (s != MGB_OK) return s;
+  if (g.M == 0 || g.N == 0) return MGB_OK;
+  if (g.dtype == MGB_BF16) return gemm_tc_launch(g, st);
+  SimtParams p{};
+  p.M = g.M; p.N = g.N; p.K = g.K; p.a_mn = g.a_mn; p.b_mn = g.b_mn;
+  p.A = static_cast<const float*>(g.A); p.lda = g.lda;
+  p.B = static_cast<const float*>(g.B); p.ldb = g.ldb;
+  p.epi = g.epi; p.alpha = g.alpha;
+  p.C = static_cast<float*>(g.C); p.ldc = g.ldc;
+  p.bias = static_cast<const float*>(g.bias);
+  p.resid = static_cast<const float*>(g.resid); p.ldr = g.ldr;
+  p.C2 = static_cast<float*>(g.C2); p.ldc2 = g.ldc2;
+  p.aux = static_cast<const float*>(g.aux); p.ldaux = g.ldaux;
+  p.glu_block = g.glu_block; p.accumulate = g.accumulate;
+  dim3 grid((g.N + TN - 1) / TN, (g.M + TM - 1) / TM);
+  LaunchScope scope(PROF_GEMM_F32, st, g.epi == EPI_BIAS_SWIGLU ? 2 : 1);
+  gemm_simt_kernel<<<grid, 256, 0, st>>>(p);
+  if (g.epi == EPI_BIAS_SWIGLU) {
+    const int F = g.N / 2;
+    swiglu_f32_kernel<<<1024, 256, 0, st>>>(g.M, F, g.glu_block, p.C, g.ldc, p.C2, g.ldc2);
+  }
+  return cudaGetLastError() == cudaSuccess ? MGB_OK : MGB_ERR_CUDA;
+}
+
+}  // namespace mgb

@@ -1,0 +1,465 @@
+// bf16 GEMM on the 5th-generation tensor cores (tcgen05, sm_103a).
+//
+// acc[m][n] = alpha * sum_k A(m,k) * B(n,k), float32 accumulation in TMEM.
+// The dense contractions of the layer - QKV, output projection, fc1, fc2 and
+// the vocab logits ("LLM Lab 06: build a Megatron-style Transformer Block
+// from scratch", section 2; "02 - How a whole Transformer block is split",
+// sections 1, 2 and 4) - and their input/weight gradients are all this product
+// with one of three operand layouts:
+//   forward      Y = X W^T       A K-major [M,K], B K-major [N,K]
+//   input grad   dX = dY W       A K-major,       B MN-major (W stored [K_red, N])
+//   weight grad  dW = dY^T X     A MN-major,      B MN-major (token dim reduced)
+//
+// One CTA computes one BM x BN output tile (BM = 128 rows = 128 TMEM lanes,
+// BN columns of float32 accumulator). Four warps:
+//   warp 0 lane 0  TMA producer: K-blocks of 64 into a STAGES-deep smem ring
+//   warp 1 lane 0  MMA issuer: 4 x tcgen05.mma (K = 16 each) per K-block, then
+//                  tcgen05.commit to the stage's "empty" barrier
+//   all 4 warps    epilogue: tcgen05.ld rows out of TMEM (warp w owns TMEM
+//                  lanes 32w..32w+31 = tile rows), fused bias / activation /
+//                  residual / activation-gradient, 16-byte global stores.
+// Tiles are visited in groups of GROUP_M row-tiles so concurrently resident
+// CTAs share A and B tiles through L2.
+//
+// Shared-memory operand layouts (128-byte swizzle, as TMA writes them):
+//   K-major tile: rows of 64 bf16 (128 B); 8-row atoms of 1024 B (SBO = 1024);
+//                 the k-th K=16 slice starts 32*k bytes into the tile.
+//   MN-major tile: boxes of 64 MN-elements x 64 K-rows (8 KB) side by side along
+//                 MN (LBO = 8192); 8-K-row atoms 1024 B apart (SBO = 1024); the
+//                 k-th K=16 slice starts 2048*k bytes in.
+// Every device wait is bounded (common.cuh); a wait that runs out records an
+// error and the CTA drains and frees its TMEM instead of spinning forever.
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace mgb {
+
+namespace {
+
+constexpr int BM = 128;
+constexpr int BK = 64;
+constexpr int GROUP_M = 16;
+
+struct EpiParams {
+  int M, N, K;
+  int epi;
+  float alpha;
+  void* C;
+  int64_t ldc;
+  const bf16* bias;
+  const bf16* resid;
+  int64_t ldr;
+  void* C2;
+  int64_t ldc2;
+  const bf16* aux;
+  int64_t ldaux;
+  int glu_block;
+  int accumulate;
+  int tiles_m, tiles_n;
+  int* err;
+};
+
+template <int BN, int STAGES>
+struct Cfg {
+  static constexpr int A_BYTES = BM * BK * 2;
+  static constexpr int B_BYTES = BN * BK * 2;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int TILE_BYTES = STAGE_BYTES * STAGES;
+  static constexpr int SMEM_BYTES = TILE_BYTES + 1024 + 256;
+};
+
+__device__ __forceinline__ void load8(const bf16* p, float (&f)[8]) {
+  uint4 v = *reinterpret_cast<const uint4*>(p);
+  uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    float2 t = unpack_bf16x2(w[i]);
+    f[2 * i] = t.x;
+    f[2 * i + 1] = t.y;
+  }
+}
+__device__ __forceinline__ void store8(bf16* p, const float* f) {
+  uint4 v;
+  v.x = pack_bf16x2(f[0], f[1]);
+  v.y = pack_bf16x2(f[2], f[3]);
+  v.z = pack_bf16x2(f[4], f[5]);
+  v.w = pack_bf16x2(f[6], f[7]);
+  *reinterpret_cast<uint4*>(p) = v;
+}
+
+// Bias for 32 columns starting at n (all lanes read the same addresses).
+__device__ __forceinline__ void add_bias32(const bf16* bias, int n, int N, float* acc) {
+  if (bias == nullptr) return;
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    if (n + 8 * q < N) {
+      float b[8];
+      load8(bias + n + 8 * q, b);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) acc[8 * q + j] += b[j];
+    }
+  }
+}
+
+__device__ __forceinline__ void tmem_chunk(uint32_t taddr, float alpha, bool have_acc,
+                                           float (&acc)[32]) {
+  uint32_t r[32];
+  tmem_ld32(taddr, r);
+  tmem_ld_wait();
+#pragma unroll
+  for (int j = 0; j < 32; ++j) acc[j] = have_acc ? alpha * __uint_as_float(r[j]) : 0.0f;
+}
+
+// Epilogue for one thread = one output row `row` of the tile.
+template <int BN>
+__device__ void epilogue_row(const EpiParams& p, uint32_t tmem_row, int row, int n0,
+                             bool have_acc) {
+  const bool row_ok = row < p.M;
+  if (p.epi == EPI_BIAS_SWIGLU) {
+    const int gb = p.glu_block;
+    for (int lc = 0; lc < BN; lc += 32) {
+      if ((lc / gb) & 1) continue;  // visit gate chunks; the up chunk is gb further
+      float g[32], u[32];
+      tmem_chunk(tmem_row + lc, p.alpha, have_acc, g);
+      tmem_chunk(tmem_row + lc + gb, p.alpha, have_acc, u);
+      const int ng = n0 + lc, nu = ng + gb;
+      if (!row_ok || ng >= p.N) continue;
+      add_bias32(p.bias, ng, p.N, g);
+      add_bias32(p.bias, nu, p.N, u);
+      bf16* c = reinterpret_cast<bf16*>(p.C) + (int64_t)row * p.ldc;
+      bf16* c2 = reinterpret_cast<bf16*>(p.C2) + (int64_t)row * p.ldc2;
+      const int na = (ng / (2 * gb)) * gb + (ng % gb);
+      float a[32];
+#pragma unroll
+      for (int j = 0; j < 32; ++j) a[j] = g[j] * sigmoidf_(g[j]) * u[j];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        store8(c + ng + 8 * q, g + 8 * q);
+        store8(c + nu + 8 * q, u + 8 * q);
+        store8(c2 + na + 8 * q, a + 8 * q);
+      }
+    }
+    return;
+  }
+  for (int lc = 0; lc < BN; lc += 32) {
+    float acc[32];
+    tmem_chunk(tmem_row + lc, p.alpha, have_acc, acc);
+    const int n = n0 + lc;
+    if (!row_ok || n >= p.N) continue;
+    switch (p.epi) {
+      case EPI_STORE: {
+        add_bias32(p.bias, n, p.N, acc);
+        bf16* c = reinterpret_cast<bf16*>(p.C) + (int64_t)row * p.ldc + n;
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          if (n + 8 * q < p.N) store8(c + 8 * q, acc + 8 * q);
+        break;
+      }
+      case EPI_BIAS_GELU: {
+        add_bias32(p.bias, n, p.N, acc);
+        bf16* c = reinterpret_cast<bf16*>(p.C) + (int64_t)row * p.ldc + n;
+        bf16* c2 = reinterpret_cast<bf16*>(p.C2) + (int64_t)row * p.ldc2 + n;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          if (n + 8 * q < p.N) {
+            float a[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) a[j] = gelu_erf(acc[8 * q + j]);
+            store8(c + 8 * q, acc + 8 * q);
+            store8(c2 + 8 * q, a);
+          }
+        }
+        break;
+      }
+      case EPI_BIAS_RESID: {
+        add_bias32(p.bias, n, p.N, acc);
+        const bf16* r = p.resid + (int64_t)row * p.ldr + n;
+        bf16* c = reinterpret_cast<bf16*>(p.C) + (int64_t)row * p.ldc + n;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          if (n + 8 * q < p.N) {
+            float x[8];
+            load8(r + 8 * q, x);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) x[j] += acc[8 * q + j];
+            store8(c + 8 * q, x);
+          }
+        }
+        break;
+      }
+      case EPI_DGELU: {
+        const bf16* ua = p.aux + (int64_t)row * p.ldaux + n;
+        bf16* c = reinterpret_cast<bf16*>(p.C) + (int64_t)row * p.ldc + n;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          if (n + 8 * q < p.N) {
+            float u[8];
+            load8(ua + 8 * q, u);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) u[j] = acc[8 * q + j] * gelu_erf_grad(u[j]);
+            store8(c + 8 * q, u);
+          }
+        }
+        break;
+      }
+      case EPI_DSWIGLU: {
+        const int gb = p.glu_block;
+        const int i = n / gb, cc = n % gb;
+        const int colg = 2 * i * gb + cc, colu = colg + gb;
+        const bf16* ar = p.aux + (int64_t)row * p.ldaux;
+        bf16* c = reinterpret_cast<bf16*>(p.C) + (int64_t)row * p.ldc;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          float g[8], u[8], dg[8], du[8];
+          load8(ar + colg + 8 * q, g);
+          load8(ar + colu + 8 * q, u);
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const float s = sigmoidf_(g[j]);
+            const float da = acc[8 * q + j];
+            du[j] = da * g[j] * s;
+            dg[j] = da * u[j] * s * (1.0f + g[j] * (1.0f - s));
+          }
+          store8(c + colg + 8 * q, dg);
+          store8(c + colu + 8 * q, du);
+        }
+        break;
+      }
+      case EPI_F32: {
+        add_bias32(p.bias, n, p.N, acc);
+        float* c = reinterpret_cast<float*>(p.C) + (int64_t)row * p.ldc + n;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          if (n + 4 * q < p.N) {
+            float4 v = make_float4(acc[4 * q], acc[4 * q + 1], acc[4 * q + 2], acc[4 * q + 3]);
+            if (p.accumulate) {
+              const float4 o = *reinterpret_cast<const float4*>(c + 4 * q);
+              v.x += o.x; v.y += o.y; v.z += o.z; v.w += o.w;
+            }
+            *reinterpret_cast<float4*>(c + 4 * q) = v;
+            acc[4 * q] = v.x; acc[4 * q + 1] = v.y; acc[4 * q + 2] = v.z; acc[4 * q + 3] = v.w;
+          }
+        }
+        if (p.C2 != nullptr) {
+          bf16* c2 = reinterpret_cast<bf16*>(p.C2) + (int64_t)row * p.ldc2 + n;
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            if (n + 8 * q < p.N) store8(c2 + 8 * q, acc + 8 * q);
+        }
+        break;
+      }
+      default:
+        break;
+    }
+  }
+}
+
+template <int BN, int STAGES, int A_MN, int B_MN>
+__global__ void __launch_bounds__(128, 1)
+    gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
+                   const __grid_constant__ CUtensorMap tmB, const EpiParams p) {
+  using C = Cfg<BN, STAGES>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::TILE_BYTES);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 1);
+  const uint32_t tiles = smem_u32(smem);
+  const uint32_t full0 = smem_u32(bars);
+  const uint32_t empty0 = full0 + 8 * STAGES;
+  const uint32_t done = full0 + 16 * STAGES;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+  // grouped raster: GROUP_M row tiles per group, columns advance slowest in a group
+  const int tile = blockIdx.x;
+  const int per_group = GROUP_M * p.tiles_n;
+  const int group = tile / per_group;
+  const int first_m = group * GROUP_M;
+  const int gm = min(p.tiles_m - first_m, GROUP_M);
+  const int in_group = tile - group * per_group;
+  const int tm = first_m + in_group % gm;
+  const int tn = in_group / gm;
+  const int m0 = tm * BM, n0 = tn * BN;
+  const int num_k = (p.K + BK - 1) / BK;
+
+  if (threadIdx.x == 0) {
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full0 + 8 * s, 1);
+      mbar_init(empty0 + 8 * s, 1);
+    }
+    mbar_init(done, 1);
+    fence_mbar_init();
+  }
+  if (warp == 0) tmem_alloc(smem_u32(tmem_slot), BN);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0 && lane == 0) {
+    // ---------------- TMA producer
+    for (int kb = 0; kb < num_k; ++kb) {
+      const int s = kb % STAGES;
+      const uint32_t round = kb / STAGES;
+      if (!mbar_wait(empty0 + 8 * s, (round & 1) ^ 1, p.err)) break;
+      const uint32_t sa = tiles + s * C::STAGE_BYTES;
+      const uint32_t sb = sa + C::A_BYTES;
+      const uint32_t fb = full0 + 8 * s;
+      mbar_arrive_expect_tx(fb, C::STAGE_BYTES);
+      const int k0 = kb * BK;
+      if (A_MN == 0) {
+        tma_load_2d(sa, &tmA, k0, m0, fb);
+      } else {
+        tma_load_2d(sa, &tmA, m0, k0, fb);
+        tma_load_2d(sa + 8192, &tmA, m0 + 64, k0, fb);
+      }
+      if (B_MN == 0) {
+        tma_load_2d(sb, &tmB, k0, n0, fb);
+      } else {
+#pragma unroll
+        for (int j = 0; j < BN / 64; ++j) tma_load_2d(sb + 8192 * j, &tmB, n0 + 64 * j, k0, fb);
+      }
+    }
+  } else if (warp == 1 && lane == 0) {
+    // ---------------- MMA issuer
+    constexpr uint32_t idesc = idesc_bf16_f32(BM, BN, A_MN, B_MN);
+    for (int kb = 0; kb < num_k; ++kb) {
+      const int s = kb % STAGES;
+      const uint32_t round = kb / STAGES;
+      if (!mbar_wait(full0 + 8 * s, round & 1, p.err)) break;
+      tc_fence_after();
+      const uint32_t sa = tiles + s * C::STAGE_BYTES;
+      const uint32_t sb = sa + C::A_BYTES;
+#pragma unroll
+      for (int kk = 0; kk < BK / 16; ++kk) {
+        const uint64_t ad = A_MN ? smem_desc_sw128(sa + 2048 * kk, 8192, 1024)
+                                 : smem_desc_sw128(sa + 32 * kk, 16, 1024);
+        const uint64_t bd = B_MN ? smem_desc_sw128(sb + 2048 * kk, 8192, 1024)
+                                 : smem_desc_sw128(sb + 32 * kk, 16, 1024);
+        tc_mma_f16(tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+      }
+      tc_commit(empty0 + 8 * s);
+    }
+    tc_commit(done);
+  }
+  __syncwarp();
+
+  // ---------------- epilogue (all 128 threads; warp w reads TMEM lanes 32w..)
+  const bool ok = mbar_wait(done, 0, p.err);
+  tc_fence_after();
+  if (ok) {
+    const uint32_t tmem_row = tmem + ((uint32_t)(warp * 32) << 16);
+    epilogue_row<BN>(p, tmem_row, m0 + warp * 32 + lane, n0, num_k > 0);
+  } else if (warp == 0 && lane == 0) {
+    // a wait ran out: give copies still in flight into this CTA's shared
+    // memory time to land (bounded) before the CTA exits
+    const uint64_t t0 = global_ns();
+    while (global_ns() - t0 < 10000000ull) {
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, BN);
+  }
+}
+
+// ---------------------------------------------------------------- host side
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  });
+  return fn;
+}
+
+// 2-D bf16 tensor map: inner dimension `inner` (contiguous), `outer` rows of
+// stride ld elements; box = box_inner x box_outer, 128-byte swizzle, zero fill.
+bool make_tmap(CUtensorMap* tm, const void* base, uint64_t inner, uint64_t outer, int64_t ld,
+               uint32_t box_inner, uint32_t box_outer) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {(cuuint64_t)ld * 2};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t es[2] = {1, 1};
+  CUresult r = fn(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+                  box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+template <int BN, int STAGES, int A_MN, int B_MN>
+mgb_status launch_variant(const GemmArgs& g, const EpiParams& ep, cudaStream_t st) {
+  using C = Cfg<BN, STAGES>;
+  auto kern = gemm_tc_kernel<BN, STAGES, A_MN, B_MN>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES) !=
+      cudaSuccess)
+    return MGB_ERR_CUDA;
+  CUtensorMap ta, tb;
+  if (g.K == 0) {
+    // no K blocks: the kernel writes the epilogue of a zero accumulator and
+    // never reads the operands; encode harmless maps over the output buffer
+    const bool ok0 = make_tmap(&ta, g.C, 64, 64, 64, 64, 64) && make_tmap(&tb, g.C, 64, 64, 64, 64, 64);
+    if (!ok0) return MGB_ERR_CUDA;
+    LaunchScope scope(A_MN ? PROF_GEMM_WGRAD : (B_MN ? PROF_GEMM_DGRAD : PROF_GEMM_FWD), st);
+    kern<<<ep.tiles_m * ep.tiles_n, 128, C::SMEM_BYTES, st>>>(ta, tb, ep);
+    return cudaGetLastError() == cudaSuccess ? MGB_OK : MGB_ERR_CUDA;
+  }
+  bool ok = A_MN ? make_tmap(&ta, g.A, g.M, g.K, g.lda, 64, 64)
+                 : make_tmap(&ta, g.A, g.K, g.M, g.lda, 64, BM);
+  ok = ok && (B_MN ? make_tmap(&tb, g.B, g.N, g.K, g.ldb, 64, 64)
+                   : make_tmap(&tb, g.B, g.K, g.N, g.ldb, 64, BN));
+  if (!ok) return MGB_ERR_CUDA;
+  const int grid = ep.tiles_m * ep.tiles_n;
+  LaunchScope scope(A_MN ? PROF_GEMM_WGRAD : (B_MN ? PROF_GEMM_DGRAD : PROF_GEMM_FWD), st);
+  kern<<<grid, 128, C::SMEM_BYTES, st>>>(ta, tb, ep);
+  return cudaGetLastError() == cudaSuccess ? MGB_OK : MGB_ERR_CUDA;
+}
+
+template <int BN, int STAGES>
+mgb_status launch_bn(const GemmArgs& g, EpiParams ep, cudaStream_t st) {
+  ep.tiles_m = (g.M + BM - 1) / BM;
+  ep.tiles_n = (g.N + BN - 1) / BN;
+  if (!g.a_mn && !g.b_mn) return launch_variant<BN, STAGES, 0, 0>(g, ep, st);
+  if (!g.a_mn && g.b_mn) return launch_variant<BN, STAGES, 0, 1>(g, ep, st);
+  if (g.a_mn && g.b_mn) return launch_variant<BN, STAGES, 1, 1>(g, ep, st);
+  return launch_variant<BN, STAGES, 1, 0>(g, ep, st);
+}
+
+}  // namespace
+
+mgb_status gemm_tc_launch(const GemmArgs& g, cudaStream_t st) {
+  EpiParams ep{};
+  ep.M = g.M; ep.N = g.N; ep.K = g.K;
+  ep.epi = g.epi; ep.alpha = g.alpha;
+  ep.C = g.C; ep.ldc = g.ldc;
+  ep.bias = reinterpret_cast<const bf16*>(g.bias);
+  ep.resid = reinterpret_cast<const bf16*>(g.resid); ep.ldr = g.ldr;
+  ep.C2 = g.C2; ep.ldc2 = g.ldc2;
+  ep.aux = reinterpret_cast<const bf16*>(g.aux); ep.ldaux = g.ldaux;
+  ep.glu_block = g.glu_block; ep.accumulate = g.accumulate;
+  ep.err = device_error_word();
+  // Column tile: 256 unless the problem is too narrow to fill the GPU with it.
+  const long tiles256 = (long)((g.M + BM - 1) / BM) * ((g.N + 255) / 256);
+  if (g.epi == EPI_BIAS_SWIGLU || (tiles256 >= 148 && g.N > 128))
+    return launch_bn<256, 4>(g, ep, st);
+  return launch_bn<128, 6>(g, ep, st);
+}
+
+}  // namespace mgb

@@ -1,0 +1,109 @@
+// Internal launch interfaces shared by the kernels and the C-ABI layer.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/mgb.h"
+
+namespace mgb {
+
+// Epilogue of the GEMM: what happens to acc[m][n] = alpha * sum_k A(m,k) B(n,k).
+enum EpiMode : int {
+  EPI_STORE = 0,        // C = acc (+ bias)
+  EPI_BIAS_GELU = 1,    // u = acc + bias; C = u; C2 = gelu(u)
+  EPI_BIAS_SWIGLU = 2,  // u = acc + bias (interleaved gate/up); C = u; C2 = silu(gate)*up
+  EPI_BIAS_RESID = 3,   // C = resid + acc + bias
+  EPI_DGELU = 4,        // C = acc * gelu'(aux)             (acc = da, aux = u)
+  EPI_DSWIGLU = 5,      // C = interleaved [dgate | dup]     (acc = da, aux = u)
+  EPI_F32 = 6,          // Cf = (accumulate ? Cf : 0) + acc (+ bias); optional C2 = bf16(Cf)
+};
+
+struct GemmArgs {
+  int M = 0, N = 0, K = 0;
+  int a_mn = 0, b_mn = 0;          // operand storage: 0 = K-major, 1 = MN-major
+  const void* A = nullptr; int64_t lda = 0;
+  const void* B = nullptr; int64_t ldb = 0;
+  int dtype = MGB_BF16;            // operand / tensor dtype
+  int epi = EPI_STORE;
+  float alpha = 1.0f;
+  void* C = nullptr; int64_t ldc = 0;       // main output (EPI_F32: float32)
+  const void* bias = nullptr;               // [N] (dtype), may be null
+  const void* resid = nullptr; int64_t ldr = 0;
+  void* C2 = nullptr; int64_t ldc2 = 0;     // second output (dtype)
+  const void* aux = nullptr; int64_t ldaux = 0;
+  int glu_block = 128;
+  int accumulate = 0;
+};
+
+// Validates operand geometry for the chosen path; returns MGB_OK or an error.
+mgb_status gemm_check(const GemmArgs& g);
+// Launches the bf16 tcgen05 GEMM (dtype MGB_BF16) or the float32 SIMT GEMM.
+mgb_status gemm_launch(const GemmArgs& g, cudaStream_t st);
+
+// LayerNorm over `cols` for `rows` rows; x, y of dtype; mean/rstd f32 (nullable).
+mgb_status layernorm_fwd_launch(int rows, int cols, int dtype, float eps, const void* x,
+                                const void* gamma, const void* beta, void* y, float* mean,
+                                float* rstd, cudaStream_t st);
+// dx = dres + LN_bwd(dy); partial dgamma/dbeta per block written to part
+// ([2, nparts, cols] f32) then reduced into dgamma/dbeta (dtype, nullable).
+mgb_status layernorm_bwd_launch(int rows, int cols, int dtype, const void* x, const float* mean,
+                                const float* rstd, const void* gamma, const void* dy,
+                                const void* dres, void* dx, void* dgamma, void* dbeta,
+                                float* part, int nparts, cudaStream_t st);
+int layernorm_bwd_parts(int rows);
+
+// db[n] = sum_m dY[m, n] (dY row stride ld); partial buffer [nparts, N] f32.
+mgb_status colsum_launch(int M, int N, int dtype, const void* dY, int64_t ld, void* db,
+                         float* part, int nparts, cudaStream_t st);
+int colsum_parts(int M);
+
+// Attention (fused online softmax); layouts as mgb_attention_fwd.
+struct AttnArgs {
+  int B, S, nq, nkv, d, causal, dtype;
+  const void *q, *k, *v;
+  int64_t ld_q, ld_kv;   // row strides (elements) of q and k/v
+  void* o; int64_t ld_o;
+  float* lse;            // [B, nq, S]
+  // backward
+  const void* dout; int64_t ld_do;
+  void *dq, *dk, *dv; int64_t ld_dq, ld_dkv;
+  float* delta;          // [B, nq, S] scratch
+};
+mgb_status attention_fwd_launch(const AttnArgs& a, cudaStream_t st);
+mgb_status attention_bwd_launch(const AttnArgs& a, cudaStream_t st);
+
+// Cross-entropy streaming kernels over one logits chunk [T, C] (row stride ldl).
+mgb_status ce_stats_launch(int T, int C, int v0, const void* logits, int64_t ldl,
+                           const int32_t* targets, float* m, float* s, float* t, cudaStream_t st);
+mgb_status ce_combine_launch(int T, int n_chunks, const float* m, const float* s, const float* t,
+                             float* lse, float* loss, float* loss_mean, cudaStream_t st);
+mgb_status ce_grad_launch(int T, int C, int v0, void* logits, int64_t ldl, const int32_t* targets,
+                          const float* lse, float scale, cudaStream_t st);
+
+// Device address of the current device's error word (nullptr on failure).
+int* device_error_word();
+
+// Kernel kinds for timing (mgb_profile_*).
+enum ProfKind : int {
+  PROF_GEMM_FWD = 0, PROF_GEMM_DGRAD, PROF_GEMM_WGRAD, PROF_GEMM_F32, PROF_ATTN_FWD,
+  PROF_ATTN_BWD, PROF_LN_FWD, PROF_LN_BWD, PROF_COLSUM, PROF_CE_STATS, PROF_CE_COMBINE,
+  PROF_CE_GRAD, PROF_KINDS
+};
+
+// Counts `launches` kernel launches and, when profiling is on, brackets them
+// with CUDA events on stream `st` (construct right before the launches).
+class LaunchScope {
+ public:
+  LaunchScope(int kind, cudaStream_t st, int launches = 1);
+  ~LaunchScope();
+  LaunchScope(const LaunchScope&) = delete;
+  LaunchScope& operator=(const LaunchScope&) = delete;
+
+ private:
+  int kind_, launches_;
+  cudaStream_t st_;
+  void* a_;
+};
+
+}  // namespace mgb

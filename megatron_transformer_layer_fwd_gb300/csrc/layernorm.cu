@@ -1,0 +1,360 @@
+// LayerNorm over the hidden dimension (forward and backward) and column sums.
+//
+// "LLM Lab 06: build a Megatron-style Transformer Block from scratch",
+// section 2: F.layer_norm(x, (hidden,)) - per token, mean and biased variance
+// over the hidden features, eps 1e-5; optional affine gamma/beta.
+//
+// Forward: one block per row; each thread keeps up to 4 16-byte vectors of the
+// row in registers (one global read, one write), warp-shuffle + shared-memory
+// block reduction for the mean, then for the centred sum of squares (two-pass
+// in registers; no E[x^2]-E[x]^2 cancellation).
+// Backward (per row, xhat = (x - mean) * rstd, g = dy * gamma):
+//   dx = dres + rstd * (g - mean(g) - xhat * mean(g * xhat))
+// rows are strided over a fixed number of blocks; each thread accumulates the
+// dgamma = sum dy*xhat and dbeta = sum dy partials of its own columns, written
+// per block and reduced by a second small kernel.
+// Column sums db[n] = sum_m dY[m, n] (bias gradients) use the same
+// partial-then-reduce scheme with coalesced 16-byte row reads.
+#include "common.cuh"
+#include "internal.h"
+
+namespace mgb {
+
+namespace {
+
+constexpr int MAXV = 4;  // 16-byte vectors per thread
+
+template <typename T> struct Vec;
+template <> struct Vec<bf16> { static constexpr int N = 8; };
+template <> struct Vec<float> { static constexpr int N = 4; };
+
+template <typename T>
+__device__ __forceinline__ void vload(const T* p, float* f) {
+  const uint4 v = *reinterpret_cast<const uint4*>(p);
+  if constexpr (sizeof(T) == 2) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 t = unpack_bf16x2(w[i]);
+      f[2 * i] = t.x;
+      f[2 * i + 1] = t.y;
+    }
+  } else {
+    f[0] = __uint_as_float(v.x); f[1] = __uint_as_float(v.y);
+    f[2] = __uint_as_float(v.z); f[3] = __uint_as_float(v.w);
+  }
+}
+template <typename T>
+__device__ __forceinline__ void vstore(T* p, const float* f) {
+  uint4 v;
+  if constexpr (sizeof(T) == 2) {
+    v.x = pack_bf16x2(f[0], f[1]); v.y = pack_bf16x2(f[2], f[3]);
+    v.z = pack_bf16x2(f[4], f[5]); v.w = pack_bf16x2(f[6], f[7]);
+  } else {
+    v.x = __float_as_uint(f[0]); v.y = __float_as_uint(f[1]);
+    v.z = __float_as_uint(f[2]); v.w = __float_as_uint(f[3]);
+  }
+  *reinterpret_cast<uint4*>(p) = v;
+}
+
+// Sum over the block; `red` holds >= 32 floats. All threads get the result.
+__device__ __forceinline__ float block_sum(float v, float* red) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nw = blockDim.x >> 5;
+  __syncthreads();
+  if (lane == 0) red[warp] = v;
+  __syncthreads();
+  float t = lane < nw ? red[lane] : 0.0f;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+  return t;
+}
+
+template <typename T>
+__global__ void ln_fwd_kernel(int rows, int cols, float eps, const T* __restrict__ x,
+                              const T* __restrict__ gamma, const T* __restrict__ beta,
+                              T* __restrict__ y, float* __restrict__ mean_out,
+                              float* __restrict__ rstd_out) {
+  constexpr int VN = Vec<T>::N;
+  __shared__ float red[32];
+  const int row = blockIdx.x;
+  const int nvec = cols / VN;
+  const T* xr = x + (int64_t)row * cols;
+  float v[MAXV][VN];
+  float s = 0.0f;
+#pragma unroll
+  for (int i = 0; i < MAXV; ++i) {
+    const int vi = threadIdx.x + i * blockDim.x;
+    if (vi < nvec) {
+      vload(xr + vi * VN, v[i]);
+#pragma unroll
+      for (int j = 0; j < VN; ++j) s += v[i][j];
+    }
+  }
+  const float mean = block_sum(s, red) / cols;
+  float ss = 0.0f;
+#pragma unroll
+  for (int i = 0; i < MAXV; ++i) {
+    const int vi = threadIdx.x + i * blockDim.x;
+    if (vi < nvec) {
+#pragma unroll
+      for (int j = 0; j < VN; ++j) {
+        const float d = v[i][j] - mean;
+        ss += d * d;
+      }
+    }
+  }
+  const float var = block_sum(ss, red) / cols;
+  const float rstd = rsqrtf(var + eps);
+  T* yr = y + (int64_t)row * cols;
+#pragma unroll
+  for (int i = 0; i < MAXV; ++i) {
+    const int vi = threadIdx.x + i * blockDim.x;
+    if (vi < nvec) {
+      float o[VN];
+      float g[VN], b[VN];
+      if (gamma) vload(gamma + vi * VN, g);
+      if (beta) vload(beta + vi * VN, b);
+#pragma unroll
+      for (int j = 0; j < VN; ++j) {
+        float t = (v[i][j] - mean) * rstd;
+        if (gamma) t *= g[j];
+        if (beta) t += b[j];
+        o[j] = t;
+      }
+      vstore(yr + vi * VN, o);
+    }
+  }
+  if (threadIdx.x == 0) {
+    if (mean_out) mean_out[row] = mean;
+    if (rstd_out) rstd_out[row] = rstd;
+  }
+}
+
+template <typename T>
+__global__ void ln_bwd_kernel(int rows, int cols, const T* __restrict__ x,
+                              const float* __restrict__ mean, const float* __restrict__ rstd,
+                              const T* __restrict__ gamma, const T* __restrict__ dy,
+                              const T* __restrict__ dres, T* __restrict__ dx,
+                              float* __restrict__ part) {
+  constexpr int VN = Vec<T>::N;
+  __shared__ float red[32];
+  const int nvec = cols / VN;
+  float pg[MAXV][VN], pb[MAXV][VN];
+  float gam[MAXV][VN];
+#pragma unroll
+  for (int i = 0; i < MAXV; ++i)
+#pragma unroll
+    for (int j = 0; j < VN; ++j) { pg[i][j] = 0.0f; pb[i][j] = 0.0f; gam[i][j] = 1.0f; }
+  if (gamma) {
+#pragma unroll
+    for (int i = 0; i < MAXV; ++i) {
+      const int vi = threadIdx.x + i * blockDim.x;
+      if (vi < nvec) vload(gamma + vi * VN, gam[i]);
+    }
+  }
+  for (int row = blockIdx.x; row < rows; row += gridDim.x) {
+    const float mu = mean[row], rs = rstd[row];
+    float xh[MAXV][VN], g[MAXV][VN];
+    float s1 = 0.0f, s2 = 0.0f;
+#pragma unroll
+    for (int i = 0; i < MAXV; ++i) {
+      const int vi = threadIdx.x + i * blockDim.x;
+      if (vi < nvec) {
+        float xv[VN], dv[VN];
+        vload(x + (int64_t)row * cols + vi * VN, xv);
+        vload(dy + (int64_t)row * cols + vi * VN, dv);
+#pragma unroll
+        for (int j = 0; j < VN; ++j) {
+          xh[i][j] = (xv[j] - mu) * rs;
+          g[i][j] = dv[j] * gam[i][j];
+          s1 += g[i][j];
+          s2 += g[i][j] * xh[i][j];
+          pg[i][j] += dv[j] * xh[i][j];
+          pb[i][j] += dv[j];
+        }
+      }
+    }
+    const float mg = block_sum(s1, red) / cols;
+    const float mgx = block_sum(s2, red) / cols;
+#pragma unroll
+    for (int i = 0; i < MAXV; ++i) {
+      const int vi = threadIdx.x + i * blockDim.x;
+      if (vi < nvec) {
+        float o[VN], r[VN];
+        if (dres) vload(dres + (int64_t)row * cols + vi * VN, r);
+#pragma unroll
+        for (int j = 0; j < VN; ++j) {
+          o[j] = rs * (g[i][j] - mg - xh[i][j] * mgx);
+          if (dres) o[j] += r[j];
+        }
+        vstore(dx + (int64_t)row * cols + vi * VN, o);
+      }
+    }
+  }
+  if (part) {
+    float* pgr = part + (int64_t)blockIdx.x * cols;
+    float* pbr = part + (int64_t)(gridDim.x + blockIdx.x) * cols;
+#pragma unroll
+    for (int i = 0; i < MAXV; ++i) {
+      const int vi = threadIdx.x + i * blockDim.x;
+      if (vi < nvec) {
+#pragma unroll
+        for (int j = 0; j < VN; ++j) {
+          pgr[vi * VN + j] = pg[i][j];
+          pbr[vi * VN + j] = pb[i][j];
+        }
+      }
+    }
+  }
+}
+
+// out[c] = sum_p part[p * cols + c], written as T (nullable outputs skipped).
+template <typename T>
+__global__ void reduce_parts_kernel(int nparts, int cols, const float* __restrict__ part,
+                                    T* __restrict__ out0, T* __restrict__ out1) {
+  const int c = blockIdx.x * blockDim.x + threadIdx.x;
+  if (c >= cols) return;
+  if (out0) {
+    float s = 0.0f;
+    for (int p = 0; p < nparts; ++p) s += part[(int64_t)p * cols + c];
+    out0[c] = from_f<T>(s);
+  }
+  if (out1) {
+    float s = 0.0f;
+    for (int p = 0; p < nparts; ++p) s += part[(int64_t)(nparts + p) * cols + c];
+    out1[c] = from_f<T>(s);
+  }
+}
+
+// part[p, n] = sum over rows m in split p of dY[m, n]; block (32 x 8): x covers
+// 32 vectors of a row, y strides rows.
+template <typename T>
+__global__ void colsum_kernel(int M, int N, const T* __restrict__ dY, int64_t ld,
+                              float* __restrict__ part) {
+  constexpr int VN = Vec<T>::N;
+  __shared__ float red[8][32 * 8 + 1];
+  const int n = (blockIdx.x * 32 + threadIdx.x) * VN;
+  float acc[VN];
+#pragma unroll
+  for (int j = 0; j < VN; ++j) acc[j] = 0.0f;
+  const int rows_per = (M + gridDim.y - 1) / gridDim.y;
+  const int r0 = blockIdx.y * rows_per, r1 = min(M, r0 + rows_per);
+  if (n < N) {
+    for (int m = r0 + threadIdx.y; m < r1; m += 8) {
+      float v[VN];
+      vload(dY + (int64_t)m * ld + n, v);
+#pragma unroll
+      for (int j = 0; j < VN; ++j) acc[j] += v[j];
+    }
+  }
+#pragma unroll
+  for (int j = 0; j < VN; ++j) red[threadIdx.y][threadIdx.x * VN + j] = acc[j];
+  __syncthreads();
+  if (threadIdx.y == 0 && n < N) {
+#pragma unroll
+    for (int j = 0; j < VN; ++j) {
+      float s = 0.0f;
+#pragma unroll
+      for (int y = 0; y < 8; ++y) s += red[y][threadIdx.x * VN + j];
+      part[(int64_t)blockIdx.y * N + n + j] = s;
+    }
+  }
+}
+
+int ln_threads(int cols, int vn) {
+  const int nvec = cols / vn;
+  int t = (nvec + MAXV - 1) / MAXV;
+  t = ((t + 31) / 32) * 32;
+  return t < 32 ? 32 : t;
+}
+
+}  // namespace
+
+int layernorm_bwd_parts(int rows) { return rows < 304 ? (rows > 0 ? rows : 1) : 304; }
+int colsum_parts(int M) { return M < 64 * 8 ? 1 : 64; }
+
+mgb_status layernorm_fwd_launch(int rows, int cols, int dtype, float eps, const void* x,
+                                const void* gamma, const void* beta, void* y, float* mean,
+                                float* rstd, cudaStream_t st) {
+  const int vn = dtype == MGB_BF16 ? 8 : 4;
+  if (rows < 0 || cols <= 0 || cols % vn) return MGB_ERR_INVALID_ARG;
+  const int threads = ln_threads(cols, vn);
+  if (threads > 1024) return MGB_ERR_UNSUPPORTED;
+  if (rows == 0) return MGB_OK;
+  LaunchScope scope(PROF_LN_FWD, st);
+  if (dtype == MGB_BF16)
+    ln_fwd_kernel<bf16><<<rows, threads, 0, st>>>(
+        rows, cols, eps, (const bf16*)x, (const bf16*)gamma, (const bf16*)beta, (bf16*)y, mean, rstd);
+  else
+    ln_fwd_kernel<float><<<rows, threads, 0, st>>>(rows, cols, eps, (const float*)x,
+                                                    (const float*)gamma, (const float*)beta,
+                                                    (float*)y, mean, rstd);
+  return cudaGetLastError() == cudaSuccess ? MGB_OK : MGB_ERR_CUDA;
+}
+
+mgb_status layernorm_bwd_launch(int rows, int cols, int dtype, const void* x, const float* mean,
+                                const float* rstd, const void* gamma, const void* dy,
+                                const void* dres, void* dx, void* dgamma, void* dbeta,
+                                float* part, int nparts, cudaStream_t st) {
+  const int vn = dtype == MGB_BF16 ? 8 : 4;
+  if (rows < 0 || cols <= 0 || cols % vn) return MGB_ERR_INVALID_ARG;
+  const int threads = ln_threads(cols, vn);
+  if (threads > 1024) return MGB_ERR_UNSUPPORTED;
+  const bool want = (dgamma || dbeta) && part;
+  if (rows == 0) nparts = 1;
+  LaunchScope scope(PROF_LN_BWD, st, (rows > 0 ? 1 : 0) + (want ? 1 : 0));
+  if (rows > 0) {
+    if (dtype == MGB_BF16)
+      ln_bwd_kernel<bf16><<<nparts, threads, 0, st>>>(rows, cols, (const bf16*)x, mean, rstd,
+                                                       (const bf16*)gamma, (const bf16*)dy,
+                                                       (const bf16*)dres, (bf16*)dx,
+                                                       want ? part : nullptr);
+    else
+      ln_bwd_kernel<float><<<nparts, threads, 0, st>>>(rows, cols, (const float*)x, mean, rstd,
+                                                        (const float*)gamma, (const float*)dy,
+                                                        (const float*)dres, (float*)dx,
+                                                        want ? part : nullptr);
+  } else if (want) {
+    cudaMemsetAsync(part, 0, sizeof(float) * 2 * cols, st);
+  }
+  if (want) {
+    const int blocks = (cols + 255) / 256;
+    if (dtype == MGB_BF16)
+      reduce_parts_kernel<bf16><<<blocks, 256, 0, st>>>(nparts, cols, part, (bf16*)dgamma,
+                                                         (bf16*)dbeta);
+    else
+      reduce_parts_kernel<float><<<blocks, 256, 0, st>>>(nparts, cols, part, (float*)dgamma,
+                                                          (float*)dbeta);
+  }
+  return cudaGetLastError() == cudaSuccess ? MGB_OK : MGB_ERR_CUDA;
+}
+
+mgb_status colsum_launch(int M, int N, int dtype, const void* dY, int64_t ld, void* db,
+                         float* part, int nparts, cudaStream_t st) {
+  const int vn = dtype == MGB_BF16 ? 8 : 4;
+  if (N % vn || ld % vn) return MGB_ERR_INVALID_ARG;
+  if (N == 0) return MGB_OK;
+  LaunchScope scope(PROF_COLSUM, st, M == 0 ? 1 : 2);
+  if (M == 0) {
+    cudaMemsetAsync(part, 0, sizeof(float) * N, st);
+    nparts = 1;
+  } else {
+    dim3 grid((N / vn + 31) / 32, nparts);
+    dim3 block(32, 8);
+    if (dtype == MGB_BF16)
+      colsum_kernel<bf16><<<grid, block, 0, st>>>(M, N, (const bf16*)dY, ld, part);
+    else
+      colsum_kernel<float><<<grid, block, 0, st>>>(M, N, (const float*)dY, ld, part);
+  }
+  const int blocks = (N + 255) / 256;
+  if (dtype == MGB_BF16)
+    reduce_parts_kernel<bf16><<<blocks, 256, 0, st>>>(nparts, N, part, (bf16*)db, nullptr);
+  else
+    reduce_parts_kernel<float><<<blocks, 256, 0, st>>>(nparts, N, part, (float*)db, nullptr);
+  return cudaGetLastError() == cudaSuccess ? MGB_OK : MGB_ERR_CUDA;
+}
+
+}  // namespace mgb

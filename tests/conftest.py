@@ -11,3 +11,27 @@ if ROOT not in sys.path:
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a CUDA GPU (sm_103a) and the built library")
     config.addinivalue_line("markers", "slow: long-running (full-size workloads)")
+
+
+def pytest_collection_modifyitems(config, items):
+    """GPU tests need a CUDA device; without one they are skipped (the CPU
+    suite deselects them with -m "not gpu")."""
+    try:
+        import torch
+        has_gpu = torch.cuda.is_available()
+    except Exception:  # pragma: no cover
+        has_gpu = False
+    if has_gpu:
+        return
+    skip = pytest.mark.skip(reason="no CUDA device")
+    for it in items:
+        if "gpu" in it.keywords:
+            it.add_marker(skip)
+
+
+@pytest.fixture(scope="session")
+def mgb_lib():
+    """The built library (built in-tree first if missing)."""
+    from megatron_transformer_layer_fwd_gb300 import build, mgb
+    build.build()
+    return mgb.load()

@@ -1,0 +1,122 @@
+"""Host-side checks of the C ABI (no GPU needed): the library loads, exports
+every function include/mgb.h declares, and rejects bad arguments with the
+documented status before touching a device."""
+import ctypes
+import os
+
+import pytest
+
+from megatron_transformer_layer_fwd_gb300 import mgb
+from megatron_transformer_layer_fwd_gb300.inputs import WORKLOADS, LayerShape
+
+
+@pytest.fixture(scope="module")
+def lib():
+    if not os.path.exists(mgb.LIB_PATH):
+        from megatron_transformer_layer_fwd_gb300 import build
+        build.build()
+    return mgb.load()
+
+
+def test_library_exports_every_header_function(lib):
+    names = mgb.header_functions()
+    assert len(names) >= 12
+    for n in names:
+        assert hasattr(lib, n), n
+
+
+def test_status_strings(lib):
+    for s in range(-8, 1):
+        assert mgb.status_string(s) not in ("", "unknown status")
+    assert mgb.status_string(-99) == "unknown status"
+
+
+def _desc(**kw):
+    return mgb.block_desc(WORKLOADS["bf16_preln_b4s512h1024"].replace(**kw))
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(n_kv_heads=3), mgb.MGB_ERR_INVALID_ARG),          # nq % nkv != 0
+    (dict(seq=0), mgb.MGB_ERR_INVALID_ARG),
+    (dict(batch=-1), mgb.MGB_ERR_INVALID_ARG),
+    (dict(head_dim=96), mgb.MGB_ERR_UNSUPPORTED),           # bf16 path: d in {64, 128}
+    (dict(hidden=1020), mgb.MGB_ERR_MISALIGNED),             # rows must be 16-byte multiples
+    (dict(act="swiglu", ffn=4800, glu_block=48), mgb.MGB_ERR_UNSUPPORTED),
+    (dict(act="swiglu", ffn=4000, glu_block=128), mgb.MGB_ERR_INVALID_ARG),
+    (dict(ln_eps=-1.0), mgb.MGB_ERR_INVALID_ARG),
+])
+def test_block_sizes_rejects_bad_descriptors(lib, kw, status):
+    d = _desc(**kw)
+    s = ctypes.c_size_t()
+    assert lib.mgb_block_sizes(ctypes.byref(d), ctypes.byref(s), None, None) == status
+
+
+def test_block_sizes_cover_saved_activations(lib):
+    shape = WORKLOADS["bf16_gqa_swiglu_b2s4096h4096"]
+    saved, fwd, bwd = mgb.mgb_block_sizes(mgb.block_desc(shape))
+    T, H = shape.tokens, shape.hidden
+    # at least: qkv, O, h, u (2F), a (F) in bf16
+    floor = 2 * T * (shape.qkv_width + shape.n_q_heads * shape.head_dim + H + 3 * shape.ffn)
+    assert saved >= floor and fwd == 0 and bwd > 0
+
+
+def test_fwd_argument_errors_before_any_launch(lib):
+    d = _desc()
+    w = mgb.BlockWeights()
+    # missing weights
+    assert lib.mgb_block_fwd(ctypes.byref(d), ctypes.byref(w), 16, 16, 16, 1 << 40, None, 0,
+                             None) == mgb.MGB_ERR_INVALID_ARG
+    # misaligned x
+    w = mgb.BlockWeights(**{k: 4096 for k in mgb._WEIGHT_FIELDS})
+    assert lib.mgb_block_fwd(ctypes.byref(d), ctypes.byref(w), 4097, 4096, 4096, 1 << 40, None, 0,
+                             None) == mgb.MGB_ERR_MISALIGNED
+    # saved buffer too small
+    assert lib.mgb_block_fwd(ctypes.byref(d), ctypes.byref(w), 4096, 4096, 4096, 16, None, 0,
+                             None) == mgb.MGB_ERR_WORKSPACE_TOO_SMALL
+    # biases present although has_bias = 0
+    d0 = _desc(has_bias=False)
+    assert lib.mgb_block_fwd(ctypes.byref(d0), ctypes.byref(w), 4096, 4096, 4096, 1 << 40, None, 0,
+                             None) == mgb.MGB_ERR_INVALID_ARG
+
+
+def test_bwd_workspace_too_small(lib):
+    d = _desc()
+    w = mgb.BlockWeights(**{k: 4096 for k in mgb._WEIGHT_FIELDS})
+    g = mgb.BlockGrads()
+    assert lib.mgb_block_bwd(ctypes.byref(d), ctypes.byref(w), 4096, 4096, 4096, 1 << 40, 4096,
+                             ctypes.byref(g), 4096, 16, None) == mgb.MGB_ERR_WORKSPACE_TOO_SMALL
+
+
+def test_ce_validation(lib):
+    ok = mgb.ce_desc(8192, 4096, 128256, 16032, 1 / 8192)
+    assert mgb.mgb_vocab_ce_sizes(ok) > 2 * 8192 * 16032
+    s = ctypes.c_size_t()
+    bad = mgb.ce_desc(8192, 4096, 128250, 16032, 1.0)       # vocab not a multiple of 8
+    assert lib.mgb_vocab_ce_sizes(ctypes.byref(bad), ctypes.byref(s)) == mgb.MGB_ERR_MISALIGNED
+    f32 = mgb.CEDesc(tokens=8, hidden=8, vocab=8, chunk=8, dtype=mgb.MGB_F32, grad_scale=1.0)
+    assert lib.mgb_vocab_ce_sizes(ctypes.byref(f32), ctypes.byref(s)) == mgb.MGB_ERR_UNSUPPORTED
+
+
+def test_gemm_validation(lib):
+    d = mgb.GemmDesc(m=128, n=100, k=64, a_major=0, b_major=0, lda=64, ldb=64, ldc=100,
+                     dtype=mgb.MGB_BF16, c_f32=0, accumulate=0, alpha=1.0)
+    assert lib.mgb_gemm(ctypes.byref(d), 4096, 4096, None, 4096, None) == mgb.MGB_ERR_MISALIGNED
+    d.n, d.ldc, d.lda = 128, 128, 32                          # lda < K
+    assert lib.mgb_gemm(ctypes.byref(d), 4096, 4096, None, 4096, None) == mgb.MGB_ERR_INVALID_ARG
+    d.lda, d.accumulate = 64, 1                               # accumulate needs float32 C
+    assert lib.mgb_gemm(ctypes.byref(d), 4096, 4096, None, 4096, None) == mgb.MGB_ERR_INVALID_ARG
+
+
+def test_injected_validation_fault(lib, monkeypatch):
+    """MGB_FAULT=validate makes every descriptor check fail (host-side fault injection)."""
+    d = _desc()
+    s = ctypes.c_size_t()
+    assert lib.mgb_block_sizes(ctypes.byref(d), ctypes.byref(s), None, None) == mgb.MGB_OK
+    monkeypatch.setenv("MGB_FAULT", "validate")
+    assert lib.mgb_block_sizes(ctypes.byref(d), ctypes.byref(s), None, None) == mgb.MGB_ERR_INVALID_ARG
+    monkeypatch.delenv("MGB_FAULT")
+    assert lib.mgb_block_sizes(ctypes.byref(d), ctypes.byref(s), None, None) == mgb.MGB_OK
+
+
+def test_selftest_limit_is_validated(lib):
+    assert lib.mgb_selftest_wait_timeout(10 ** 10, None) == mgb.MGB_ERR_INVALID_ARG

@@ -1,0 +1,76 @@
+"""GPU parity of the vocab-chunked tied-embedding cross-entropy
+(mgb_vocab_ce_fwd_bwd through the C ABI) against the float64 oracle."""
+import time
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from megatron_transformer_layer_fwd_gb300 import mgb
+from megatron_transformer_layer_fwd_gb300.inputs import CE_WORKLOADS, CEShape, ce_inputs
+from megatron_transformer_layer_fwd_gb300.runner import CERunner, to_device
+from tests.util import CE_LOSS_ABS, rel_l2, to_np
+
+pytestmark = pytest.mark.gpu
+
+
+def _runner(shape, inp):
+    h = to_device(inp["hidden"], torch.bfloat16)
+    e = to_device(inp["emb"], torch.bfloat16)
+    t = torch.from_numpy(inp["targets"]).to("cuda")
+    return CERunner(shape.tokens, shape.hidden, shape.vocab, shape.chunk, h, e, t)
+
+
+@pytest.mark.parametrize("T,H,V,C", [(300, 256, 1000, 136), (256, 128, 2048, 2048), (130, 64, 520, 64),
+                                     (512, 1024, 8192, 1000)])
+def test_ce_small_full_parity(mgb_lib, T, H, V, C):
+    shape = CEShape(T, H, V, C)
+    inp = ce_inputs(shape, seed=5)
+    r = _runner(shape, inp)
+    r.run()
+    assert mgb.mgb_device_status() == mgb.MGB_OK
+    loss, lse, mean, _ = oracle.ce_chunked(inp["hidden"], inp["emb"], inp["targets"], C)
+    dh, de = oracle.ce_grads(inp["hidden"], inp["emb"], inp["targets"], lse, 1.0 / T)
+    assert np.abs(to_np(r.loss) - loss).max() < CE_LOSS_ABS
+    assert np.abs(to_np(r.lse) - lse).max() < CE_LOSS_ABS
+    assert abs(float(r.loss_mean[0]) - mean) < CE_LOSS_ABS
+    assert rel_l2(to_np(r.d_hidden), dh) < 2e-2
+    assert rel_l2(to_np(r.d_emb), de) < 2e-2
+
+
+def test_ce_forward_only(mgb_lib):
+    shape = CEShape(128, 64, 256, 96)
+    inp = ce_inputs(shape, seed=1)
+    h = to_device(inp["hidden"], torch.bfloat16)
+    e = to_device(inp["emb"], torch.bfloat16)
+    t = torch.from_numpy(inp["targets"]).to("cuda")
+    r = CERunner(128, 64, 256, 96, h, e, t, want_grads=False)
+    r.run()
+    loss, _, _, _ = oracle.ce_chunked(inp["hidden"], inp["emb"], inp["targets"], 96)
+    assert np.abs(to_np(r.loss) - loss).max() < CE_LOSS_ABS
+
+
+@pytest.mark.slow
+def test_ce_full_size_sampled(mgb_lib):
+    """Full tied-embedding CE workload: sampled tokens' loss / LSE / d_hidden
+    rows against the oracle one row at a time; the mean against the per-token
+    losses; d_emb column sums vanish (grad rows sum to 0)."""
+    shape = CE_WORKLOADS["bf16_ce_t8192h4096v128256"]
+    inp = ce_inputs(shape, seed=0)
+    r = _runner(shape, inp)
+    r.run()
+    assert mgb.mgb_device_status() == mgb.MGB_OK
+    rows = np.random.default_rng(0).choice(shape.tokens, 48, replace=False)
+    t0 = time.time()
+    loss, lse, dh = oracle.ce_rows(inp["hidden"][rows], inp["emb"], inp["targets"][rows],
+                                   1.0 / shape.tokens)
+    print(f"oracle rows {time.time() - t0:.1f}s")
+    gl = to_np(r.loss)
+    assert np.abs(gl[rows] - loss).max() < CE_LOSS_ABS
+    assert np.abs(to_np(r.lse)[rows] - lse).max() < CE_LOSS_ABS
+    assert abs(float(r.loss_mean[0]) - gl.mean()) < 1e-4
+    assert rel_l2(to_np(r.d_hidden)[rows], dh) < 2e-2
+    de = r.d_emb.double()
+    col = de.sum(dim=0)
+    assert float(col.norm() / de.norm()) < 2e-2

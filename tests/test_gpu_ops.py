@@ -1,0 +1,130 @@
+"""GPU parity of the building blocks through the C ABI: the tcgen05 GEMM in
+every operand layout, the float32 GEMM, LayerNorm and the attention core,
+against the float64 oracle (or, for the plain product, numpy's matmul of the
+same bf16-rounded operands)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from megatron_transformer_layer_fwd_gb300 import mgb
+from megatron_transformer_layer_fwd_gb300.inputs import round_to_bf16
+from tests.util import rel_l2, to_np
+
+pytestmark = pytest.mark.gpu
+RNG = np.random.default_rng(2024)
+
+
+def _bf16(shape, scale=1.0):
+    return round_to_bf16(RNG.standard_normal(shape) * scale)
+
+
+def _dev(a, dtype):
+    return torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).to("cuda", dtype)
+
+
+@pytest.mark.parametrize("a_mn,b_mn", [(0, 0), (0, 1), (1, 1), (1, 0)])
+@pytest.mark.parametrize("M,N,K", [(128, 128, 64), (328, 200, 136), (256, 520, 1000), (1000, 1304, 64)])
+def test_gemm_bf16_layouts_f32_out(mgb_lib, a_mn, b_mn, M, N, K):
+    A = _bf16((M, K))
+    B = _bf16((N, K))
+    a_st = A.T.copy() if a_mn else A
+    b_st = B.T.copy() if b_mn else B
+    c = torch.full((M, N), float("nan"), device="cuda", dtype=torch.float32)
+    d = mgb.GemmDesc(m=M, n=N, k=K, a_major=a_mn, b_major=b_mn, lda=a_st.shape[1], ldb=b_st.shape[1],
+                     ldc=N, dtype=mgb.MGB_BF16, c_f32=1, accumulate=0, alpha=1.0)
+    mgb.mgb_gemm(d, _dev(a_st, torch.bfloat16), _dev(b_st, torch.bfloat16), None, c)
+    assert mgb.mgb_device_status() == mgb.MGB_OK
+    ref = A @ B.T
+    err = rel_l2(to_np(c), ref)
+    assert err < 1e-5, err
+
+
+@pytest.mark.parametrize("M,N,K", [(384, 768, 256), (200, 136, 72)])
+def test_gemm_bf16_bias_out_and_accumulate(mgb_lib, M, N, K):
+    A, B, bias = _bf16((M, K)), _bf16((N, K)), _bf16((N,))
+    c = torch.empty((M, N), device="cuda", dtype=torch.bfloat16)
+    d = mgb.GemmDesc(m=M, n=N, k=K, a_major=0, b_major=0, lda=K, ldb=K, ldc=N, dtype=mgb.MGB_BF16,
+                     c_f32=0, accumulate=0, alpha=0.5)
+    mgb.mgb_gemm(d, _dev(A, torch.bfloat16), _dev(B, torch.bfloat16), _dev(bias, torch.bfloat16), c)
+    ref = 0.5 * (A @ B.T) + bias
+    assert rel_l2(to_np(c), ref) < 4e-3
+    # float32 accumulate: C = C + A B^T
+    c32 = _dev(ref, torch.float32)
+    d.c_f32, d.accumulate, d.alpha = 1, 1, 1.0
+    mgb.mgb_gemm(d, _dev(A, torch.bfloat16), _dev(B, torch.bfloat16), None, c32)
+    assert rel_l2(to_np(c32), ref + A @ B.T) < 1e-5
+    assert mgb.mgb_device_status() == mgb.MGB_OK
+
+
+@pytest.mark.parametrize("a_mn,b_mn", [(0, 0), (0, 1), (1, 1)])
+def test_gemm_f32_simt(mgb_lib, a_mn, b_mn):
+    M, N, K = 100, 72, 200
+    A, B = RNG.standard_normal((M, K)), RNG.standard_normal((N, K))
+    a_st = A.T.copy() if a_mn else A
+    b_st = B.T.copy() if b_mn else B
+    c = torch.empty((M, N), device="cuda", dtype=torch.float32)
+    d = mgb.GemmDesc(m=M, n=N, k=K, a_major=a_mn, b_major=b_mn, lda=a_st.shape[1], ldb=b_st.shape[1],
+                     ldc=N, dtype=mgb.MGB_F32, c_f32=1, accumulate=0, alpha=1.0)
+    mgb.mgb_gemm(d, _dev(a_st, torch.float32), _dev(b_st, torch.float32), None, c)
+    assert rel_l2(to_np(c), A.astype(np.float32).astype(np.float64) @ B.astype(np.float32).T) < 1e-6
+
+
+def test_gemm_zero_k_writes_bias_only(mgb_lib):
+    M, N = 130, 64
+    bias = _bf16((N,))
+    c = torch.full((M, N), 7.0, device="cuda", dtype=torch.bfloat16)
+    d = mgb.GemmDesc(m=M, n=N, k=0, a_major=0, b_major=0, lda=8, ldb=8, ldc=N, dtype=mgb.MGB_BF16,
+                     c_f32=0, accumulate=0, alpha=1.0)
+    dummy = torch.zeros(64, device="cuda", dtype=torch.bfloat16)
+    mgb.mgb_gemm(d, dummy, dummy, _dev(bias, torch.bfloat16), c)
+    np.testing.assert_array_equal(to_np(c), np.broadcast_to(bias, (M, N)))
+
+
+@pytest.mark.parametrize("dtype,rows,cols", [("bf16", 300, 1024), ("bf16", 7, 4096), ("f32", 64, 256)])
+def test_layernorm_fwd(mgb_lib, dtype, rows, cols):
+    x = RNG.standard_normal((rows, cols)) * 2 + 0.5
+    g, b = 1 + 0.1 * RNG.standard_normal(cols), 0.1 * RNG.standard_normal(cols)
+    if dtype == "bf16":
+        x, g, b = round_to_bf16(x), round_to_bf16(g), round_to_bf16(b)
+    td = torch.bfloat16 if dtype == "bf16" else torch.float32
+    y = torch.empty((rows, cols), device="cuda", dtype=td)
+    mean = torch.empty(rows, device="cuda")
+    rstd = torch.empty(rows, device="cuda")
+    mgb.mgb_layernorm_fwd(rows, cols, mgb.MGB_BF16 if dtype == "bf16" else mgb.MGB_F32, 1e-5,
+                          _dev(x, td), _dev(g, td), _dev(b, td), y, mean, rstd)
+    ry, rm, rr = oracle.ln_fwd(x, g, b, 1e-5)
+    assert rel_l2(to_np(y), ry) < (5e-3 if dtype == "bf16" else 1e-6)
+    assert rel_l2(to_np(mean), rm) < 1e-6 and rel_l2(to_np(rstd), rr) < 1e-6
+
+
+@pytest.mark.parametrize("B,S,nq,nkv,d,causal", [
+    (1, 64, 1, 1, 64, False), (2, 100, 4, 2, 64, True), (1, 200, 4, 1, 128, False),
+    (2, 130, 2, 2, 128, True)])
+def test_attention_fwd_bf16(mgb_lib, B, S, nq, nkv, d, causal):
+    q = _bf16((B, nq, S, d))
+    k = _bf16((B, nkv, S, d))
+    v = _bf16((B, nkv, S, d))
+    pack = lambda t: t.transpose(0, 2, 1, 3).reshape(B * S, -1)
+    qkv = np.concatenate([pack(q), pack(k), pack(v)], axis=1)
+    tq = _dev(qkv, torch.bfloat16)
+    W = qkv.shape[1]
+    o = torch.empty((B * S, nq * d), device="cuda", dtype=torch.bfloat16)
+    lse = torch.empty((B, nq, S), device="cuda", dtype=torch.float32)
+    e = 2
+    mgb.mgb_attention_fwd(B, S, nq, nkv, d, causal, mgb.MGB_BF16, tq, tq[:, nq * d:],
+                          tq[:, (nq + nkv) * d:], W, W, o, lse)
+    ro, rl = oracle.attention_fwd(q, k, v, causal)
+    assert rel_l2(to_np(o), pack(ro)) < 1e-2
+    assert rel_l2(to_np(lse), rl) < 1e-3
+
+
+def test_device_wait_timeout_is_reported(mgb_lib):
+    """A bounded wait on a barrier nobody arrives on returns a timeout status
+    (no hang, no fault) and the context stays usable."""
+    assert mgb.mgb_device_status() == mgb.MGB_OK
+    mgb.mgb_selftest_wait_timeout(20_000_000)          # 20 ms
+    assert mgb.mgb_device_status() == mgb.MGB_ERR_DEVICE_TIMEOUT
+    assert mgb.mgb_device_status() == mgb.MGB_OK        # cleared
+    x = torch.ones(16, device="cuda")
+    assert float(x.sum()) == 16.0
