@@ -344,6 +344,94 @@ def run_ours(args, world, rank, local):
     return out
 
 
+def _time_loop(fn, steps, warmup, stream):
+    import torch
+    from megatron_transformer_layer_fwd_gb300 import mgb
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    mgb.mgb_profile_reset()
+    mgb.mgb_profile_enable(True)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        fn()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    mgb.mgb_profile_enable(False)
+    prof = {k: round(v[0] / steps, 4) for k, v in mgb.mgb_profile_read().items() if v[1] > 0}
+    if mgb.mgb_device_status(stream) != mgb.MGB_OK:
+        raise RuntimeError("device error")
+    return e0.elapsed_time(e1) / steps, prof
+
+
+def run_case(args):
+    """Sub-paths and single kernels of the step (for ncu captures and the
+    sequence sweep); prints one JSON line per measurement."""
+    import torch
+    from megatron_transformer_layer_fwd_gb300 import build, mgb
+    from megatron_transformer_layer_fwd_gb300.runner import CERunner, LayerRunner, to_device
+    build.build()
+    torch.cuda.set_device(0)
+    st = torch.cuda.current_stream()
+    peaks = load_peaks()
+    if args.case == "gemm":
+        M, N, K = args.mnk
+        a = torch.randn(M, K, device="cuda").to(torch.bfloat16)
+        b = torch.randn(N, K, device="cuda").to(torch.bfloat16)
+        c = torch.empty(M, N, device="cuda", dtype=torch.bfloat16)
+        d = mgb.GemmDesc(m=M, n=N, k=K, a_major=0, b_major=0, lda=K, ldb=K, ldc=N, dtype=mgb.MGB_BF16,
+                         c_f32=0, accumulate=0, alpha=1.0)
+        ms, prof = _time_loop(lambda: mgb.mgb_gemm(d, a, b, None, c), args.steps, args.warmup, st)
+        tf = 2.0 * M * N * K / (ms / 1e3) / 1e12
+        print(json.dumps({"case": "gemm", "mnk": [M, N, K], "ms": round(ms, 4), "tflops": round(tf, 1),
+                          "frac_of_burst_peak": round(tf / peaks["bf16_tflops"], 4)}))
+        return
+    if args.case in ("layer", "sweep"):
+        names = [LAYER] if args.case == "layer" else [f"bf16_causal_b8s{s}h2048"
+                                                      for s in (128, 256, 512, 1024, 2048)]
+        for name in names:
+            shape = WORKLOADS[name]
+            r = LayerRunner(shape, layer_inputs(shape, seed=0))
+            dy = torch.full_like(r.x, 1.0 / (shape.tokens * shape.hidden))
+
+            def fb():
+                r.fwd(st)
+                r.bwd(dy, st)
+            ms, prof = _time_loop(fb, args.steps, args.warmup, st)
+            lf = layer_flops(shape)
+            gem = ("gemm_tc_fwd", "gemm_tc_dgrad", "gemm_tc_wgrad")
+            out = {"case": args.case, "workload": name, "ms": round(ms, 4),
+                   "tflops": round(lf["total"] / (ms / 1e3) / 1e12, 1),
+                   "frac_of_nominal_2250": round(lf["total"] / (ms / 1e3) / 2.25e15, 4),
+                   "tokens_per_s": round(shape.tokens / (ms / 1e3), 1),
+                   "attention_ms": round(prof.get("attn_fwd", 0) + prof.get("attn_bwd", 0), 4),
+                   "gemm_ms": round(sum(prof.get(k, 0) for k in gem), 4),
+                   "kernel_ms": prof}
+            if args.case == "sweep":
+                # page 1's three segments: Attention (LN1..proj), FFN (LN2..fc2), Backward
+                out["stage_ms"] = {"attention_fwd_core": prof.get("attn_fwd", 0),
+                                   "attention_bwd_core": prof.get("attn_bwd", 0)}
+            print(json.dumps(out), flush=True)
+            del r
+        return
+    if args.case == "ce":
+        ce = CE_WORKLOADS[CE]
+        cin = ce_inputs(ce, seed=0)
+        r = CERunner(ce.tokens, ce.hidden, ce.vocab, ce.chunk,
+                     to_device(cin["hidden"], torch.bfloat16), to_device(cin["emb"], torch.bfloat16),
+                     torch.from_numpy(cin["targets"]).to("cuda"))
+        ms, prof = _time_loop(lambda: r.run(st), args.steps, args.warmup, st)
+        sb = ce_stream_bytes(ce)
+        sms = prof.get("ce_stats", 0) + prof.get("ce_grad", 0)
+        print(json.dumps({"case": "ce", "ms": round(ms, 4), "stream_ms": round(sms, 4),
+                          "stream_gbs": round(sb / (sms / 1e3) / 1e9, 1),
+                          "frac_of_hbm": round(sb / (sms / 1e3) / 1e9 / peaks["hbm_gbs"], 4),
+                          "kernel_ms": prof}))
+        return
+    raise SystemExit(f"unknown case {args.case}")
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -351,9 +439,15 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--case", default="step", choices=("step", "layer", "sweep", "ce", "gemm"),
+                    help="step (default, the driver's line) or a sub-path / single kernel")
+    ap.add_argument("--mnk", type=int, nargs=3, default=(8192, 22016, 4096))
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.case != "step":
+        run_case(args)
+        return
     world, rank, local = dist_setup()
 
     if args.impl == "reference":

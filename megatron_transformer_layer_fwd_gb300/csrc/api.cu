@@ -537,8 +537,12 @@ mgb_status mgb_vocab_ce_fwd_bwd(const mgb_ce_desc* desc, const void* hidden, con
   const bf16* E = static_cast<const bf16*>(emb);
   for (int c = 0; c < p.n_chunks; ++c) {
     const int v0 = c * C, Cc = (V - v0) < C ? (V - v0) : C;
-    MGB_TRY(gemm_launch(mk_gemm(MGB_BF16, T, Cc, H, 0, hidden, H, 0, E + (size_t)v0 * H, H,
-                                EPI_STORE, logits, C), st));
+    GemmArgs g = mk_gemm(MGB_BF16, T, Cc, H, 0, hidden, H, 0, E + (size_t)v0 * H, H, EPI_STORE,
+                         logits, C);
+    // the target logit is taken in float32 from the accumulator, not from
+    // the bf16 logits the streaming pass reads
+    g.tgt = targets; g.tgt_v0 = v0; g.tgt_out = t + (size_t)c * T;
+    MGB_TRY(gemm_launch(g, st));
     MGB_TRY(ce_stats_launch(T, Cc, v0, logits, C, targets, m + (size_t)c * T, s + (size_t)c * T,
                             t + (size_t)c * T, st));
   }

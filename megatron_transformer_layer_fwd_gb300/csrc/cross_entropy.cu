@@ -104,8 +104,10 @@ __global__ void __launch_bounds__(CE_THREADS) ce_stats_kernel(int T, int C, int 
     for (int w = 1; w < CE_THREADS / 32; ++w) ms_merge(M, Ssum, sm_m[w], sm_s[w]);
     m_out[row] = M * LN2;
     s_out[row] = Ssum;
+    // rows whose target lies in this chunk already hold the float32 target
+    // logit (written by the logits GEMM epilogue); the rest contribute 0
     const int tc = tgt[row] - v0;
-    t_out[row] = (tc >= 0 && tc < C) ? __bfloat162float(l[tc]) : 0.0f;
+    if (tc < 0 || tc >= C) t_out[row] = 0.0f;
   }
 }
 

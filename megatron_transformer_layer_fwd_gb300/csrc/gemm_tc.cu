@@ -61,6 +61,9 @@ struct EpiParams {
   int accumulate;
   int tiles_m, tiles_n;
   int* err;
+  const int32_t* tgt;
+  int tgt_v0;
+  float* tgt_out;
 };
 
 template <int BN, int STAGES>
@@ -145,6 +148,9 @@ __device__ void epilogue_row(const EpiParams& p, uint32_t tmem_row, int row, int
     }
     return;
   }
+  // target column of this row relative to the tile (CE logits: fp32 capture)
+  int tcol = -1;
+  if (p.tgt != nullptr && row_ok) tcol = p.tgt[row] - p.tgt_v0 - n0;
   for (int lc = 0; lc < BN; lc += 32) {
     float acc[32];
     tmem_chunk(tmem_row + lc, p.alpha, have_acc, acc);
@@ -153,6 +159,13 @@ __device__ void epilogue_row(const EpiParams& p, uint32_t tmem_row, int row, int
     switch (p.epi) {
       case EPI_STORE: {
         add_bias32(p.bias, n, p.N, acc);
+        const int tc = tcol - lc;
+        if (tc >= 0 && tc < 32 && n + tc < p.N) {
+          float v = 0.0f;
+#pragma unroll
+          for (int j = 0; j < 32; ++j) v = (j == tc) ? acc[j] : v;
+          p.tgt_out[row] = v;
+        }
         bf16* c = reinterpret_cast<bf16*>(p.C) + (int64_t)row * p.ldc + n;
 #pragma unroll
         for (int q = 0; q < 4; ++q)
@@ -455,6 +468,9 @@ mgb_status gemm_tc_launch(const GemmArgs& g, cudaStream_t st) {
   ep.aux = reinterpret_cast<const bf16*>(g.aux); ep.ldaux = g.ldaux;
   ep.glu_block = g.glu_block; ep.accumulate = g.accumulate;
   ep.err = device_error_word();
+  ep.tgt = g.epi == EPI_STORE ? g.tgt : nullptr;
+  ep.tgt_v0 = g.tgt_v0;
+  ep.tgt_out = g.tgt_out;
   // Column tile: 256 unless the problem is too narrow to fill the GPU with it.
   const long tiles256 = (long)((g.M + BM - 1) / BM) * ((g.N + 255) / 256);
   if (g.epi == EPI_BIAS_SWIGLU || (tiles256 >= 148 && g.N > 128))

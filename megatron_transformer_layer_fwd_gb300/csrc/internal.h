@@ -34,6 +34,11 @@ struct GemmArgs {
   const void* aux = nullptr; int64_t ldaux = 0;
   int glu_block = 128;
   int accumulate = 0;
+  // EPI_STORE only: for each row m whose target column tgt[m] - tgt_v0 lies in
+  // [0, N), tgt_out[m] = that column's float32 value (before bf16 rounding)
+  const int32_t* tgt = nullptr;
+  int tgt_v0 = 0;
+  float* tgt_out = nullptr;
 };
 
 // Validates operand geometry for the chosen path; returns MGB_OK or an error.
