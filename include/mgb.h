@@ -182,6 +182,20 @@ mgb_status mgb_layernorm_fwd(int32_t rows, int32_t cols, int32_t dtype, float ep
                              const void* gamma, const void* beta, void* y, float* mean,
                              float* rstd, void* stream);
 
+/* LayerNorm backward [P1 section 2, "end-to-end backward" through
+ * F.layer_norm]: with xhat = (x - mean) * rstd and g = dy * gamma,
+ *   dx = dres + rstd * (g - mean(g) - xhat * mean(g * xhat)),
+ *   dgamma = sum_rows dy * xhat,  dbeta = sum_rows dy.
+ * x, dy, dres (may be NULL), dx: [rows, cols] of dtype; mean/rstd from the
+ * forward; gamma NULL = no affine (then dgamma/dbeta must be NULL). dgamma,
+ * dbeta (dtype, may be NULL) are summed over rows through float32 partials in
+ * `ws` (size from mgb_layernorm_bwd_ws_bytes; deterministic order). */
+size_t mgb_layernorm_bwd_ws_bytes(int32_t rows, int32_t cols);
+mgb_status mgb_layernorm_bwd(int32_t rows, int32_t cols, int32_t dtype, const void* x,
+                             const float* mean, const float* rstd, const void* gamma,
+                             const void* dy, const void* dres, void* dx, void* dgamma, void* dbeta,
+                             void* ws, size_t ws_bytes, void* stream);
+
 /* Attention core [P2 section 2]: q [B*S, nq*d] (head h at columns h*d), k, v
  * [B*S, nkv*d] (row stride ld_q / ld_kv elements, so they may be column slices
  * of one fused qkv buffer); o [B*S, nq*d]; lse [B, nq, S] f32. */

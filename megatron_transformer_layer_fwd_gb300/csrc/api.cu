@@ -542,6 +542,7 @@ mgb_status mgb_vocab_ce_fwd_bwd(const mgb_ce_desc* desc, const void* hidden, con
     // the target logit is taken in float32 from the accumulator, not from
     // the bf16 logits the streaming pass reads
     g.tgt = targets; g.tgt_v0 = v0; g.tgt_out = t + (size_t)c * T;
+    g.prof_kind = PROF_GEMM_CE_LOGITS;
     MGB_TRY(gemm_launch(g, st));
     MGB_TRY(ce_stats_launch(T, Cc, v0, logits, C, targets, m + (size_t)c * T, s + (size_t)c * T,
                             t + (size_t)c * T, st));
@@ -550,8 +551,12 @@ mgb_status mgb_vocab_ce_fwd_bwd(const mgb_ce_desc* desc, const void* hidden, con
   if (!d_hidden && !d_emb) return MGB_OK;
   for (int c = 0; c < p.n_chunks; ++c) {
     const int v0 = c * C, Cc = (V - v0) < C ? (V - v0) : C;
-    MGB_TRY(gemm_launch(mk_gemm(MGB_BF16, T, Cc, H, 0, hidden, H, 0, E + (size_t)v0 * H, H,
-                                EPI_STORE, logits, C), st));
+    {
+      GemmArgs g = mk_gemm(MGB_BF16, T, Cc, H, 0, hidden, H, 0, E + (size_t)v0 * H, H, EPI_STORE,
+                           logits, C);
+      g.prof_kind = PROF_GEMM_CE_LOGITS;
+      MGB_TRY(gemm_launch(g, st));
+    }
     MGB_TRY(ce_grad_launch(T, Cc, v0, logits, C, targets, lse_buf, desc->grad_scale, st));
     if (d_hidden) {
       GemmArgs g = mk_gemm(MGB_BF16, T, H, Cc, 0, logits, C, 1, E + (size_t)v0 * H, H, EPI_F32,
@@ -596,6 +601,31 @@ mgb_status mgb_layernorm_fwd(int32_t rows, int32_t cols, int32_t dtype, float ep
     if (!aligned16(q)) return MGB_ERR_MISALIGNED;
   MGB_TRY(check_arch());
   return layernorm_fwd_launch(rows, cols, dtype, eps, x, gamma, beta, y, mean, rstd,
+                              as_stream(stream));
+}
+
+size_t mgb_layernorm_bwd_ws_bytes(int32_t rows, int32_t cols) {
+  if (rows < 0 || cols < 1) return 0;
+  return sizeof(float) * 2 * (size_t)layernorm_bwd_parts(rows) * (size_t)cols;
+}
+
+mgb_status mgb_layernorm_bwd(int32_t rows, int32_t cols, int32_t dtype, const void* x,
+                             const float* mean, const float* rstd, const void* gamma,
+                             const void* dy, const void* dres, void* dx, void* dgamma, void* dbeta,
+                             void* ws, size_t ws_bytes, void* stream) {
+  if (fault_injected()) return MGB_ERR_INVALID_ARG;
+  if (dtype != MGB_BF16 && dtype != MGB_F32) return MGB_ERR_INVALID_ARG;
+  if (rows < 0 || cols < 1 || !x || !mean || !rstd || !dy || !dx) return MGB_ERR_INVALID_ARG;
+  if (!gamma && (dgamma || dbeta)) return MGB_ERR_INVALID_ARG;
+  const void* ps[] = {x, mean, rstd, gamma, dy, dres, dx, dgamma, dbeta, ws};
+  for (const void* q : ps)
+    if (!aligned16(q)) return MGB_ERR_MISALIGNED;
+  const bool want = dgamma || dbeta;
+  if (want && (ws == nullptr || ws_bytes < mgb_layernorm_bwd_ws_bytes(rows, cols)))
+    return MGB_ERR_WORKSPACE_TOO_SMALL;
+  MGB_TRY(check_arch());
+  return layernorm_bwd_launch(rows, cols, dtype, x, mean, rstd, gamma, dy, dres, dx, dgamma, dbeta,
+                              want ? static_cast<float*>(ws) : nullptr, layernorm_bwd_parts(rows),
                               as_stream(stream));
 }
 

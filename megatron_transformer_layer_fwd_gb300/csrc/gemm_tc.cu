@@ -430,7 +430,9 @@ mgb_status launch_variant(const GemmArgs& g, const EpiParams& ep, cudaStream_t s
     // never reads the operands; encode harmless maps over the output buffer
     const bool ok0 = make_tmap(&ta, g.C, 64, 64, 64, 64, 64) && make_tmap(&tb, g.C, 64, 64, 64, 64, 64);
     if (!ok0) return MGB_ERR_CUDA;
-    LaunchScope scope(A_MN ? PROF_GEMM_WGRAD : (B_MN ? PROF_GEMM_DGRAD : PROF_GEMM_FWD), st);
+    LaunchScope scope(g.prof_kind >= 0 ? g.prof_kind
+                               : (A_MN ? PROF_GEMM_WGRAD : (B_MN ? PROF_GEMM_DGRAD : PROF_GEMM_FWD)),
+                    st);
     kern<<<ep.tiles_m * ep.tiles_n, 128, C::SMEM_BYTES, st>>>(ta, tb, ep);
     return cudaGetLastError() == cudaSuccess ? MGB_OK : MGB_ERR_CUDA;
   }
@@ -440,7 +442,9 @@ mgb_status launch_variant(const GemmArgs& g, const EpiParams& ep, cudaStream_t s
                    : make_tmap(&tb, g.B, g.K, g.N, g.ldb, 64, BN));
   if (!ok) return MGB_ERR_CUDA;
   const int grid = ep.tiles_m * ep.tiles_n;
-  LaunchScope scope(A_MN ? PROF_GEMM_WGRAD : (B_MN ? PROF_GEMM_DGRAD : PROF_GEMM_FWD), st);
+  LaunchScope scope(g.prof_kind >= 0 ? g.prof_kind
+                               : (A_MN ? PROF_GEMM_WGRAD : (B_MN ? PROF_GEMM_DGRAD : PROF_GEMM_FWD)),
+                    st);
   kern<<<grid, 128, C::SMEM_BYTES, st>>>(ta, tb, ep);
   return cudaGetLastError() == cudaSuccess ? MGB_OK : MGB_ERR_CUDA;
 }

@@ -34,6 +34,7 @@ struct GemmArgs {
   const void* aux = nullptr; int64_t ldaux = 0;
   int glu_block = 128;
   int accumulate = 0;
+  int prof_kind = -1;  // timing group (-1: by operand layout)
   // EPI_STORE only: for each row m whose target column tgt[m] - tgt_v0 lies in
   // [0, N), tgt_out[m] = that column's float32 value (before bf16 rounding)
   const int32_t* tgt = nullptr;
@@ -93,7 +94,7 @@ int* device_error_word();
 enum ProfKind : int {
   PROF_GEMM_FWD = 0, PROF_GEMM_DGRAD, PROF_GEMM_WGRAD, PROF_GEMM_F32, PROF_ATTN_FWD,
   PROF_ATTN_BWD, PROF_LN_FWD, PROF_LN_BWD, PROF_COLSUM, PROF_CE_STATS, PROF_CE_COMBINE,
-  PROF_CE_GRAD, PROF_KINDS
+  PROF_CE_GRAD, PROF_GEMM_CE_LOGITS, PROF_KINDS
 };
 
 // Counts `launches` kernel launches and, when profiling is on, brackets them

@@ -211,21 +211,34 @@ __global__ void ln_bwd_kernel(int rows, int cols, const T* __restrict__ x,
   }
 }
 
-// out[c] = sum_p part[p * cols + c], written as T (nullable outputs skipped).
+// out0[c] = sum_p part[p, c] and out1[c] = sum_p part[nparts + p, c], written
+// as T (nullable outputs skipped). Block (32 x 8): lane = column (coalesced
+// 128-byte rows of the partial buffer), the 8 warps split the partials, fixed
+// order of summation (deterministic).
 template <typename T>
 __global__ void reduce_parts_kernel(int nparts, int cols, const float* __restrict__ part,
                                     T* __restrict__ out0, T* __restrict__ out1) {
-  const int c = blockIdx.x * blockDim.x + threadIdx.x;
-  if (c >= cols) return;
-  if (out0) {
-    float s = 0.0f;
-    for (int p = 0; p < nparts; ++p) s += part[(int64_t)p * cols + c];
-    out0[c] = from_f<T>(s);
+  __shared__ float red[2][8][33];
+  const int c = blockIdx.x * 32 + threadIdx.x;
+  float s0 = 0.0f, s1 = 0.0f;
+  if (c < cols) {
+    for (int p = threadIdx.y; p < nparts; p += 8) {
+      if (out0) s0 += part[(int64_t)p * cols + c];
+      if (out1) s1 += part[(int64_t)(nparts + p) * cols + c];
+    }
   }
-  if (out1) {
-    float s = 0.0f;
-    for (int p = 0; p < nparts; ++p) s += part[(int64_t)(nparts + p) * cols + c];
-    out1[c] = from_f<T>(s);
+  red[0][threadIdx.y][threadIdx.x] = s0;
+  red[1][threadIdx.y][threadIdx.x] = s1;
+  __syncthreads();
+  if (threadIdx.y == 0 && c < cols) {
+    float a = 0.0f, b = 0.0f;
+#pragma unroll
+    for (int y = 0; y < 8; ++y) {
+      a += red[0][y][threadIdx.x];
+      b += red[1][y][threadIdx.x];
+    }
+    if (out0) out0[c] = from_f<T>(a);
+    if (out1) out1[c] = from_f<T>(b);
   }
 }
 
@@ -273,7 +286,9 @@ int ln_threads(int cols, int vn) {
 
 }  // namespace
 
-int layernorm_bwd_parts(int rows) { return rows < 304 ? (rows > 0 ? rows : 1) : 304; }
+// Row blocks of the backward: enough resident blocks (8 per SM) to hide the
+// latency of the per-row reductions; each writes one partial dgamma/dbeta row.
+int layernorm_bwd_parts(int rows) { return rows < 1216 ? (rows > 0 ? rows : 1) : 1216; }
 int colsum_parts(int M) { return M < 64 * 8 ? 1 : 64; }
 
 mgb_status layernorm_fwd_launch(int rows, int cols, int dtype, float eps, const void* x,
@@ -321,13 +336,13 @@ mgb_status layernorm_bwd_launch(int rows, int cols, int dtype, const void* x, co
     cudaMemsetAsync(part, 0, sizeof(float) * 2 * cols, st);
   }
   if (want) {
-    const int blocks = (cols + 255) / 256;
+    const dim3 blocks((cols + 31) / 32), block(32, 8);
     if (dtype == MGB_BF16)
-      reduce_parts_kernel<bf16><<<blocks, 256, 0, st>>>(nparts, cols, part, (bf16*)dgamma,
-                                                         (bf16*)dbeta);
+      reduce_parts_kernel<bf16><<<blocks, block, 0, st>>>(nparts, cols, part, (bf16*)dgamma,
+                                                           (bf16*)dbeta);
     else
-      reduce_parts_kernel<float><<<blocks, 256, 0, st>>>(nparts, cols, part, (float*)dgamma,
-                                                          (float*)dbeta);
+      reduce_parts_kernel<float><<<blocks, block, 0, st>>>(nparts, cols, part, (float*)dgamma,
+                                                            (float*)dbeta);
   }
   return cudaGetLastError() == cudaSuccess ? MGB_OK : MGB_ERR_CUDA;
 }
@@ -349,11 +364,11 @@ mgb_status colsum_launch(int M, int N, int dtype, const void* dY, int64_t ld, vo
     else
       colsum_kernel<float><<<grid, block, 0, st>>>(M, N, (const float*)dY, ld, part);
   }
-  const int blocks = (N + 255) / 256;
+  const dim3 blocks((N + 31) / 32), block(32, 8);
   if (dtype == MGB_BF16)
-    reduce_parts_kernel<bf16><<<blocks, 256, 0, st>>>(nparts, N, part, (bf16*)db, nullptr);
+    reduce_parts_kernel<bf16><<<blocks, block, 0, st>>>(nparts, N, part, (bf16*)db, nullptr);
   else
-    reduce_parts_kernel<float><<<blocks, 256, 0, st>>>(nparts, N, part, (float*)db, nullptr);
+    reduce_parts_kernel<float><<<blocks, block, 0, st>>>(nparts, N, part, (float*)db, nullptr);
   return cudaGetLastError() == cudaSuccess ? MGB_OK : MGB_ERR_CUDA;
 }
 

@@ -58,7 +58,8 @@ mgb_status drain_locked() {
 
 const char* kKindNames[PROF_KINDS] = {
     "gemm_tc_fwd",  "gemm_tc_dgrad", "gemm_tc_wgrad", "gemm_f32",  "attn_fwd",   "attn_bwd",
-    "layernorm_fwd", "layernorm_bwd", "colsum",       "ce_stats", "ce_combine", "ce_grad"};
+    "layernorm_fwd", "layernorm_bwd", "colsum",       "ce_stats", "ce_combine", "ce_grad",
+    "gemm_tc_ce_logits"};
 
 }  // namespace
 

@@ -93,6 +93,7 @@ def load() -> ctypes.CDLL:
             "mgb_vocab_ce_fwd_bwd": [ctypes.POINTER(CEDesc), P, P, P, P, P, P, P, P, P, SZ, P],
             "mgb_gemm": [ctypes.POINTER(GemmDesc), P, P, P, P, P],
             "mgb_layernorm_fwd": [I32, I32, I32, F32, P, P, P, P, P, P, P],
+            "mgb_layernorm_bwd": [I32, I32, I32, P, P, P, P, P, P, P, P, P, P, SZ, P],
             "mgb_attention_fwd": [I32, I32, I32, I32, I32, I32, I32, P, P, P, I64, I64, P, P, P],
             "mgb_device_status": [P],
             "mgb_selftest_wait_timeout": [U64, P],
@@ -105,6 +106,8 @@ def load() -> ctypes.CDLL:
         lib.mgb_status_string.restype = ctypes.c_char_p
         lib.mgb_version.argtypes = []
         lib.mgb_version.restype = ctypes.c_int32
+        lib.mgb_layernorm_bwd_ws_bytes.argtypes = [I32, I32]
+        lib.mgb_layernorm_bwd_ws_bytes.restype = SZ
         lib.mgb_launch_count.argtypes = []
         lib.mgb_launch_count.restype = ctypes.c_uint64
         lib.mgb_profile_enable.argtypes = [I32]
@@ -223,6 +226,18 @@ def mgb_layernorm_fwd(rows: int, cols: int, dtype: int, eps: float, x, gamma, be
                       stream=None) -> None:
     _check(load().mgb_layernorm_fwd(rows, cols, dtype, eps, _ptr(x), _ptr(gamma), _ptr(beta), _ptr(y),
                                     _ptr(mean), _ptr(rstd), _stream(stream)), "mgb_layernorm_fwd")
+
+
+def mgb_layernorm_bwd_ws_bytes(rows: int, cols: int) -> int:
+    return load().mgb_layernorm_bwd_ws_bytes(rows, cols)
+
+
+def mgb_layernorm_bwd(rows: int, cols: int, dtype: int, x, mean, rstd, gamma, dy, dres, dx, dgamma,
+                      dbeta, ws, stream=None) -> None:
+    ws_bytes = ws.numel() * ws.element_size() if ws is not None else 0
+    _check(load().mgb_layernorm_bwd(rows, cols, dtype, _ptr(x), _ptr(mean), _ptr(rstd), _ptr(gamma),
+                                    _ptr(dy), _ptr(dres), _ptr(dx), _ptr(dgamma), _ptr(dbeta),
+                                    _ptr(ws), ws_bytes, _stream(stream)), "mgb_layernorm_bwd")
 
 
 def mgb_attention_fwd(batch, seq, n_q_heads, n_kv_heads, head_dim, causal, dtype, q, k, v, ld_q,
