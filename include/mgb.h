@@ -196,6 +196,33 @@ mgb_status mgb_layernorm_bwd(int32_t rows, int32_t cols, int32_t dtype, const vo
                              const void* dy, const void* dres, void* dx, void* dgamma, void* dbeta,
                              void* ws, size_t ws_bytes, void* stream);
 
+/* LayerNorm backward for callers that cannot allocate device memory. The
+ * pages have no counterpart; this is a library-side convenience.
+ *
+ * Some callers cannot obtain scratch memory at the point where they run this
+ * operation: a serving engine that reserved all device memory up front and
+ * forbids allocation while a request is in flight, or a plugin inside a host
+ * framework that owns the device allocator and offers no workspace. Such a
+ * caller cannot supply the `ws` buffer of mgb_layernorm_bwd. This entry point
+ * computes the same result (same arguments minus ws/ws_bytes) and keeps the
+ * float32 partial sums of dgamma/dbeta in a fixed array inside the library:
+ *   - size: 2 x 64 x 16384 floats (8 MiB), held by every GPU that loads the
+ *     library until the process exits; cols > 16384 with dgamma or dbeta
+ *     requested returns MGB_ERR_UNSUPPORTED before any launch;
+ *   - the library calls no cudaMalloc/cudaFree or allocating routine (keep
+ *     the tracing of mgb_profile_enable off: when on, it creates CUDA events);
+ *   - the first call on each device looks up the array's device address with
+ *     that device current; make that first call before any stream capture;
+ *   - every call on a device shares the array: calls that may run at the same
+ *     time on the GPU (different streams, no ordering between them) race and
+ *     give wrong dgamma/dbeta; serialise them.
+ * The dgamma/dbeta sums use 64 row blocks (mgb_layernorm_bwd uses more), so
+ * the two entry points agree to float32 rounding, not bit for bit. */
+mgb_status mgb_layernorm_bwd_noalloc(int32_t rows, int32_t cols, int32_t dtype, const void* x,
+                                     const float* mean, const float* rstd, const void* gamma,
+                                     const void* dy, const void* dres, void* dx, void* dgamma,
+                                     void* dbeta, void* stream);
+
 /* Attention core [P2 section 2]: q [B*S, nq*d] (head h at columns h*d), k, v
  * [B*S, nkv*d] (row stride ld_q / ld_kv elements, so they may be column slices
  * of one fused qkv buffer); o [B*S, nq*d]; lse [B, nq, S] f32. */

@@ -15,6 +15,8 @@
 // per block and reduced by a second small kernel.
 // Column sums db[n] = sum_m dY[m, n] (bias gradients) use the same
 // partial-then-reduce scheme with coalesced 16-byte row reads.
+#include <mutex>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -347,6 +349,32 @@ mgb_status layernorm_bwd_launch(int rows, int cols, int dtype, const void* x, co
   return cudaGetLastError() == cudaSuccess ? MGB_OK : MGB_ERR_CUDA;
 }
 
+// ------------------------------------------- LayerNorm backward, no allocation
+// Scratch of mgb_layernorm_bwd_noalloc: the float32 partial sums of dgamma and
+// dbeta, [2][kNoAllocParts][cols] with cols <= kNoAllocMaxCols (8 MiB). It is
+// a file-scope device array, so every GPU that loads the library holds it until
+// the process exits, and every call on a device shares it.
+constexpr int kNoAllocParts = 64;
+constexpr int kNoAllocMaxCols = 16384;
+static __device__ __align__(256) float g_ln_bwd_scratch[2 * kNoAllocParts * kNoAllocMaxCols];
+
+// Device address of g_ln_bwd_scratch on the current device. Looked up once per
+// device (the first call on that device), with that device current; host code
+// must never pass the symbol itself to a kernel.
+static float* ln_bwd_scratch_address() {
+  static float* addr[64] = {};
+  static std::mutex mu;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  std::lock_guard<std::mutex> lock(mu);
+  if (addr[dev] == nullptr) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_ln_bwd_scratch) != cudaSuccess) return nullptr;
+    addr[dev] = static_cast<float*>(p);
+  }
+  return addr[dev];
+}
+
 mgb_status colsum_launch(int M, int N, int dtype, const void* dY, int64_t ld, void* db,
                          float* part, int nparts, cudaStream_t st) {
   const int vn = dtype == MGB_BF16 ? 8 : 4;
@@ -373,3 +401,36 @@ mgb_status colsum_launch(int M, int N, int dtype, const void* dY, int64_t ld, vo
 }
 
 }  // namespace mgb
+
+extern "C" mgb_status mgb_layernorm_bwd_noalloc(int32_t rows, int32_t cols, int32_t dtype,
+                                                const void* x, const float* mean,
+                                                const float* rstd, const void* gamma,
+                                                const void* dy, const void* dres, void* dx,
+                                                void* dgamma, void* dbeta, void* stream) {
+  using namespace mgb;
+  if (dtype != MGB_BF16 && dtype != MGB_F32) return MGB_ERR_INVALID_ARG;
+  if (rows < 0 || cols < 1 || !x || !mean || !rstd || !dy || !dx) return MGB_ERR_INVALID_ARG;
+  if (!gamma && (dgamma || dbeta)) return MGB_ERR_INVALID_ARG;
+  const void* ps[] = {x, mean, rstd, gamma, dy, dres, dx, dgamma, dbeta};
+  for (const void* q : ps)
+    if ((reinterpret_cast<uintptr_t>(q) & 15u) != 0) return MGB_ERR_MISALIGNED;
+  const bool want = dgamma || dbeta;
+  // the partial sums must fit the fixed scratch array
+  if (want && cols > kNoAllocMaxCols) return MGB_ERR_UNSUPPORTED;
+  int dev = 0, major = 0, minor = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+    return MGB_ERR_CUDA;
+  if (major != 10 || minor != 3) return MGB_ERR_ARCH;
+  float* part = nullptr;
+  if (want) {
+    part = ln_bwd_scratch_address();
+    if (part == nullptr) return MGB_ERR_CUDA;
+  }
+  // each row block overwrites its whole partial row, so nothing left in the
+  // array by an earlier call is read (rows == 0 zeroes the slots it reduces)
+  const int nparts = rows < kNoAllocParts ? (rows > 0 ? rows : 1) : kNoAllocParts;
+  return layernorm_bwd_launch(rows, cols, dtype, x, mean, rstd, gamma, dy, dres, dx, dgamma, dbeta,
+                              part, nparts, reinterpret_cast<cudaStream_t>(stream));
+}

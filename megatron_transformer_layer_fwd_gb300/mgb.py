@@ -94,6 +94,7 @@ def load() -> ctypes.CDLL:
             "mgb_gemm": [ctypes.POINTER(GemmDesc), P, P, P, P, P],
             "mgb_layernorm_fwd": [I32, I32, I32, F32, P, P, P, P, P, P, P],
             "mgb_layernorm_bwd": [I32, I32, I32, P, P, P, P, P, P, P, P, P, P, SZ, P],
+            "mgb_layernorm_bwd_noalloc": [I32, I32, I32, P, P, P, P, P, P, P, P, P, P],
             "mgb_attention_fwd": [I32, I32, I32, I32, I32, I32, I32, P, P, P, I64, I64, P, P, P],
             "mgb_device_status": [P],
             "mgb_selftest_wait_timeout": [U64, P],
@@ -238,6 +239,15 @@ def mgb_layernorm_bwd(rows: int, cols: int, dtype: int, x, mean, rstd, gamma, dy
     _check(load().mgb_layernorm_bwd(rows, cols, dtype, _ptr(x), _ptr(mean), _ptr(rstd), _ptr(gamma),
                                     _ptr(dy), _ptr(dres), _ptr(dx), _ptr(dgamma), _ptr(dbeta),
                                     _ptr(ws), ws_bytes, _stream(stream)), "mgb_layernorm_bwd")
+
+
+def mgb_layernorm_bwd_noalloc(rows: int, cols: int, dtype: int, x, mean, rstd, gamma, dy, dres, dx,
+                              dgamma, dbeta, stream=None) -> None:
+    """mgb_layernorm_bwd without a workspace (library-held scratch; see mgb.h)."""
+    _check(load().mgb_layernorm_bwd_noalloc(rows, cols, dtype, _ptr(x), _ptr(mean), _ptr(rstd),
+                                            _ptr(gamma), _ptr(dy), _ptr(dres), _ptr(dx),
+                                            _ptr(dgamma), _ptr(dbeta), _stream(stream)),
+           "mgb_layernorm_bwd_noalloc")
 
 
 def mgb_attention_fwd(batch, seq, n_q_heads, n_kv_heads, head_dim, causal, dtype, q, k, v, ld_q,
