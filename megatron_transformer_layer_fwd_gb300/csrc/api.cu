@@ -37,7 +37,7 @@ int* device_error_word() {
   return addr[dev];
 }
 
-mgb_status attention_bf16_fwd(const AttnArgs& a, cudaStream_t st);
+mgb_status attention_tc_fwd(const AttnArgs& a, cudaStream_t st);
 mgb_status attention_bf16_bwd(const AttnArgs& a, cudaStream_t st);
 mgb_status attention_f32_fwd(const AttnArgs& a, cudaStream_t st);
 mgb_status attention_f32_bwd(const AttnArgs& a, cudaStream_t st);
@@ -45,7 +45,7 @@ mgb_status attention_f32_bwd(const AttnArgs& a, cudaStream_t st);
 mgb_status attention_fwd_launch(const AttnArgs& a, cudaStream_t st) {
   if (a.B == 0 || a.S == 0) return MGB_OK;
   LaunchScope scope(PROF_ATTN_FWD, st, 1);
-  return a.dtype == MGB_BF16 ? attention_bf16_fwd(a, st) : attention_f32_fwd(a, st);
+  return a.dtype == MGB_BF16 ? attention_tc_fwd(a, st) : attention_f32_fwd(a, st);
 }
 mgb_status attention_bwd_launch(const AttnArgs& a, cudaStream_t st) {
   if (a.B == 0 || a.S == 0) return MGB_OK;

@@ -461,6 +461,14 @@ mgb_status launch_bn(const GemmArgs& g, EpiParams ep, cudaStream_t st) {
 
 }  // namespace
 
+// 2-D bf16 tensor map with 128-byte swizzle and zero fill (shared with the
+// attention kernels).
+CUresult tmap_encode_bf16_2d(CUtensorMap* tm, const void* base, uint64_t inner, uint64_t outer,
+                             int64_t ld, uint32_t box_inner, uint32_t box_outer) {
+  return make_tmap(tm, base, inner, outer, ld, box_inner, box_outer) ? CUDA_SUCCESS
+                                                                     : CUDA_ERROR_INVALID_VALUE;
+}
+
 mgb_status gemm_tc_launch(const GemmArgs& g, cudaStream_t st) {
   EpiParams ep{};
   ep.M = g.M; ep.N = g.N; ep.K = g.K;
