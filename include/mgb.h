@@ -231,6 +231,18 @@ mgb_status mgb_attention_fwd(int32_t batch, int32_t seq, int32_t n_q_heads, int3
                              const void* q, const void* k, const void* v, int64_t ld_q,
                              int64_t ld_kv, void* o, float* lse, void* stream);
 
+/* Attention core backward [P1 section 2, end-to-end backward]: given the
+ * forward's q, k, v, o, lse and dO = dL/dO (same layouts; do [B*S, nq*d] with
+ * row stride ld_do), writes dq (row stride ld_dq) and dk, dv (row stride
+ * ld_dkv; the sum over the query heads of each GQA group). P is recomputed
+ * from lse. `ws` holds delta = rowsum(dO * O): at least 4*B*nq*S bytes. */
+mgb_status mgb_attention_bwd(int32_t batch, int32_t seq, int32_t n_q_heads, int32_t n_kv_heads,
+                             int32_t head_dim, int32_t causal, int32_t dtype,
+                             const void* q, const void* k, const void* v, int64_t ld_q,
+                             int64_t ld_kv, const void* o, const float* lse, const void* dout,
+                             int64_t ld_do, void* dq, void* dk, void* dv, int64_t ld_dq,
+                             int64_t ld_dkv, void* ws, size_t ws_bytes, void* stream);
+
 /* ---- status and diagnostics ---- */
 
 const char* mgb_status_string(mgb_status s);

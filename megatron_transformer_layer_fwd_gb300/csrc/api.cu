@@ -133,8 +133,9 @@ mgb_status validate_desc(const mgb_block_desc* d) {
     return MGB_ERR_MISALIGNED;
   if (d->dtype == MGB_BF16 && d->head_dim != 64 && d->head_dim != 128) return MGB_ERR_UNSUPPORTED;
   if (d->dtype == MGB_F32 && (d->head_dim > 256 || d->seq > 2048)) return MGB_ERR_UNSUPPORTED;
-  // LayerNorm keeps a row in registers: at most 1024 threads x 4 vectors of 16 bytes
-  if (d->hidden > (d->dtype == MGB_BF16 ? 32768 : 16384)) return MGB_ERR_UNSUPPORTED;
+  // LayerNorm keeps a row in registers (at most 1024 threads x 4 vectors of 16
+  // bytes) and its backward keeps dgamma/dbeta partials of a row in shared memory
+  if (d->hidden > 16384) return MGB_ERR_UNSUPPORTED;
   return MGB_OK;
 }
 
@@ -651,6 +652,40 @@ mgb_status mgb_attention_fwd(int32_t batch, int32_t seq, int32_t n_q_heads, int3
   a.q = q; a.k = k; a.v = v; a.ld_q = ld_q; a.ld_kv = ld_kv;
   a.o = o; a.ld_o = (int64_t)n_q_heads * head_dim; a.lse = lse;
   return attention_fwd_launch(a, as_stream(stream));
+}
+
+mgb_status mgb_attention_bwd(int32_t batch, int32_t seq, int32_t n_q_heads, int32_t n_kv_heads,
+                             int32_t head_dim, int32_t causal, int32_t dtype, const void* q,
+                             const void* k, const void* v, int64_t ld_q, int64_t ld_kv,
+                             const void* o, const float* lse, const void* dout, int64_t ld_do,
+                             void* dq, void* dk, void* dv, int64_t ld_dq, int64_t ld_dkv, void* ws,
+                             size_t ws_bytes, void* stream) {
+  if (fault_injected()) return MGB_ERR_INVALID_ARG;
+  if (batch < 0 || seq < 1 || n_q_heads < 1 || n_kv_heads < 1 || n_q_heads % n_kv_heads)
+    return MGB_ERR_INVALID_ARG;
+  if (dtype != MGB_BF16 && dtype != MGB_F32) return MGB_ERR_INVALID_ARG;
+  if (!q || !k || !v || !o || !lse || !dout || !dq || !dk || !dv || !ws) return MGB_ERR_INVALID_ARG;
+  if (dtype == MGB_BF16 && head_dim != 64 && head_dim != 128) return MGB_ERR_UNSUPPORTED;
+  if (dtype == MGB_F32 && (head_dim > 256 || seq > 2048)) return MGB_ERR_UNSUPPORTED;
+  const int64_t wq = (int64_t)n_q_heads * head_dim, wkv = (int64_t)n_kv_heads * head_dim;
+  if (ld_q < wq || ld_do < wq || ld_dq < wq || ld_kv < wkv || ld_dkv < wkv)
+    return MGB_ERR_INVALID_ARG;
+  const int vm = dtype == MGB_BF16 ? 8 : 1;
+  const void* ps[] = {q, k, v, o, dout, dq, dk, dv, ws};
+  for (const void* pp : ps)
+    if (!aligned16(pp)) return MGB_ERR_MISALIGNED;
+  if (ld_q % vm || ld_kv % vm || ld_do % vm || ld_dq % vm || ld_dkv % vm) return MGB_ERR_MISALIGNED;
+  if (ws_bytes < 4 * (size_t)batch * n_q_heads * seq) return MGB_ERR_WORKSPACE_TOO_SMALL;
+  MGB_TRY(check_arch());
+  AttnArgs a{};
+  a.B = batch; a.S = seq; a.nq = n_q_heads; a.nkv = n_kv_heads; a.d = head_dim;
+  a.causal = causal ? 1 : 0; a.dtype = dtype;
+  a.q = q; a.k = k; a.v = v; a.ld_q = ld_q; a.ld_kv = ld_kv;
+  a.o = const_cast<void*>(o); a.ld_o = wq; a.lse = const_cast<float*>(lse);
+  a.dout = dout; a.ld_do = ld_do;
+  a.dq = dq; a.dk = dk; a.dv = dv; a.ld_dq = ld_dq; a.ld_dkv = ld_dkv;
+  a.delta = static_cast<float*>(ws);
+  return attention_bwd_launch(a, as_stream(stream));
 }
 
 }  // extern "C"

@@ -87,8 +87,10 @@ __global__ void __launch_bounds__(128, 2)
 
   const int tid = threadIdx.x, warp = tid >> 5;
   const int nqt = (p.S + TQ - 1) / TQ;
-  const int qt = nqt - 1 - (int)blockIdx.x;  // longest causal rows first
-  const int h = blockIdx.y, b = blockIdx.z;
+  // grid: x = (head, batch) pairs, y = query tile from the last (longest causal
+  // rows) to the first, so the heaviest tiles of every head start first
+  const int qt = nqt - 1 - (int)blockIdx.y;
+  const int h = blockIdx.x % p.nq, b = blockIdx.x / p.nq;
   const int g = h / (p.nq / p.nkv);
   const int q0 = qt * TQ;
   const int row = q0 + tid;  // this thread's query position in the sequence
@@ -317,7 +319,7 @@ mgb_status fwd_tc_d(const AttnArgs& a, cudaStream_t st) {
   auto k = attn_fwd_tc_kernel<D>;
   if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess)
     return MGB_ERR_CUDA;
-  dim3 grid((a.S + TQ - 1) / TQ, a.nq, a.B);
+  dim3 grid(a.nq * a.B, (a.S + TQ - 1) / TQ);
   k<<<grid, 128, C::SMEM, st>>>(tq, tk, tv, p);
   return cudaGetLastError() == cudaSuccess ? MGB_OK : MGB_ERR_CUDA;
 }

@@ -1,0 +1,558 @@
+// bf16 attention backward on the 5th-generation tensor cores (tcgen05).
+//
+// From the saved LSE ("02 - How a whole Transformer block is split",
+// section 2 defines the forward; page 1, section 2 asks for the end-to-end
+// backward): with s = q.k / sqrt(d), P = exp(s - LSE) recomputed, dP = dO V^T,
+// delta = rowsum(dO * O) (precomputed), dS = P * (dP - delta):
+//   dV_g = sum_h P^T dO_h,   dK_g = sum_h dS^T Q_h / sqrt(d),   dQ_h = dS K_g / sqrt(d),
+// summing over the query heads h of the GQA group g.
+//
+// Kernel A (dK, dV): one CTA = 128 keys of one KV head; thread t owns key row
+// t (= TMEM lane t). It loops over every query head of the group and every
+// 64-query tile that can see its keys (Q/dO tiles in a 3-stage TMA ring):
+//   S^T  = K Q^T     M=128 N=64 K=d     TMEM [0, 64)
+//   dP^T = V dO^T    M=128 N=64 K=d     TMEM [64, 128)
+//   registers: P^T = exp2(S^T*log2e/sqrt(d) - LSE*log2e), dS^T = P^T (dP^T - delta)
+//   (bf16, K-major 128-byte-swizzled smem tiles)
+//   dV  += P^T dO    M=128 N=d K=64     TMEM [128, 128+d)
+//   dK  += dS^T Q    M=128 N=d K=64     TMEM [128+d, 128+2d)
+// The Q and dO tiles are read as K-major operands by the first two products and
+// as MN-major operands (d contiguous) by the last two: the same smem bytes.
+// dK and dV stay in TMEM across the whole loop, so the GQA sum costs nothing.
+//
+// Kernel B (dQ): one CTA = 128 queries of one head; per 64-key tile (K/V in a
+// 3-stage ring): S = Q K^T, dP = dO V^T (TMEM), dS in registers -> smem,
+// dQ += dS K (TMEM; the K tile read as an MN-major operand).
+//
+// Thread 0 issues copies and MMAs. After the barrier that publishes tile i's
+// P/dS, it issues tile i+1's first two products before tile i's accumulating
+// ones, so the softmax-backward of tile i+1 overlaps them. Every wait is
+// bounded; a wait that runs out sets a shared abort flag that all threads read
+// only right after a CTA barrier, where the loop is also the only place left.
+#include "common.cuh"
+#include "internal.h"
+
+namespace mgb {
+
+CUresult tmap_encode_bf16_2d(CUtensorMap* tm, const void* base, uint64_t inner, uint64_t outer,
+                             int64_t ld, uint32_t box_inner, uint32_t box_outer);
+
+namespace {
+
+constexpr float LOG2E = 1.4426950408889634f;
+constexpr int TR = 128;  // rows (keys in A, queries in B) per CTA
+constexpr int TC = 64;   // columns per inner tile (queries in A, keys in B)
+constexpr int NS = 3;    // stages of the streamed operand ring
+
+struct BwdParams {
+  int B, S, nq, nkv, causal;
+  const float* lse;    // [B, nq, S]
+  const float* delta;  // [B, nq, S]
+  bf16 *d0, *d1;       // A: dk, dv; B: dq
+  int64_t ld_out;
+  int* err;
+  float sl2, scale;
+};
+
+__device__ __forceinline__ void fence_proxy_async() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void ld_cols64(uint32_t taddr, float (&v)[64]) {
+  uint32_t r[32];
+  tmem_ld32(taddr, r);
+  tmem_ld_wait();
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+  tmem_ld32(taddr + 32, r);
+  tmem_ld_wait();
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[32 + i] = __uint_as_float(r[i]);
+}
+
+// 64 floats -> bf16 row of a K-major 128-byte-swizzled [rows][64] tile
+__device__ __forceinline__ void store_row_sw128(uint8_t* row_ptr, int row, const float (&v)[64]) {
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    uint4 w;
+    w.x = pack_bf16x2(v[8 * c], v[8 * c + 1]);
+    w.y = pack_bf16x2(v[8 * c + 2], v[8 * c + 3]);
+    w.z = pack_bf16x2(v[8 * c + 4], v[8 * c + 5]);
+    w.w = pack_bf16x2(v[8 * c + 6], v[8 * c + 7]);
+    *reinterpret_cast<uint4*>(row_ptr + ((c ^ (row & 7)) << 4)) = w;
+  }
+}
+
+// TMEM row (this thread's lane) of d columns, scaled, to global bf16 (all
+// lanes must call; out == nullptr skips the store)
+template <int D>
+__device__ __forceinline__ void store_tmem_row(uint32_t taddr, float scale, bf16* out) {
+#pragma unroll
+  for (int c = 0; c < D / 32; ++c) {
+    uint32_t r[32];
+    tmem_ld32(taddr + c * 32, r);
+    tmem_ld_wait();
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      uint4 w;
+      w.x = pack_bf16x2(__uint_as_float(r[8 * q]) * scale, __uint_as_float(r[8 * q + 1]) * scale);
+      w.y = pack_bf16x2(__uint_as_float(r[8 * q + 2]) * scale, __uint_as_float(r[8 * q + 3]) * scale);
+      w.z = pack_bf16x2(__uint_as_float(r[8 * q + 4]) * scale, __uint_as_float(r[8 * q + 5]) * scale);
+      w.w = pack_bf16x2(__uint_as_float(r[8 * q + 6]) * scale, __uint_as_float(r[8 * q + 7]) * scale);
+      if (out) *reinterpret_cast<uint4*>(out + c * 32 + 8 * q) = w;
+    }
+  }
+}
+
+__device__ __forceinline__ void spin_10ms() {
+  const uint64_t t0 = global_ns();
+  while (global_ns() - t0 < 10000000ull) {
+  }
+}
+
+// ------------------------------------------------------------ kernel A: dK, dV
+template <int D>
+struct DkvCfg {
+  static constexpr int KB = D / 64;
+  static constexpr int KV_BYTES = TR * D * 2;   // K or V rows of this CTA
+  static constexpr int QT_BYTES = TC * D * 2;   // one Q or dO tile
+  static constexpr int PT_BYTES = TR * TC * 2;  // P^T or dS^T tile
+  static constexpr int OFF_K = 0;
+  static constexpr int OFF_V = OFF_K + KV_BYTES;
+  static constexpr int OFF_Q = OFF_V + KV_BYTES;         // NS stages
+  static constexpr int OFF_DO = OFF_Q + NS * QT_BYTES;   // NS stages
+  static constexpr int OFF_P = OFF_DO + NS * QT_BYTES;
+  static constexpr int OFF_DS = OFF_P + PT_BYTES;
+  static constexpr int OFF_LD = OFF_DS + PT_BYTES;       // [2][lse2 64 | delta 64] f32
+  static constexpr int OFF_BAR = OFF_LD + 2 * 2 * TC * 4;
+  static constexpr int SMEM = OFF_BAR + 128 + 1024;
+  static constexpr int COL_DP = 64, COL_DV = 128, COL_DK = 128 + D;
+  static constexpr int TMEM_COLS = D == 128 ? 512 : 256;
+};
+
+template <int D>
+__global__ void __launch_bounds__(128, 1)
+    attn_bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
+                            const __grid_constant__ CUtensorMap tmK,
+                            const __grid_constant__ CUtensorMap tmV,
+                            const __grid_constant__ CUtensorMap tmO, const BwdParams p) {
+  using C = DkvCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const uint32_t sb = smem_u32(smem);
+  const uint32_t sK = sb + C::OFF_K, sV = sb + C::OFF_V, sQ = sb + C::OFF_Q, sO = sb + C::OFF_DO,
+                 sP = sb + C::OFF_P, sS = sb + C::OFF_DS;
+  float* sLD = reinterpret_cast<float*>(smem + C::OFF_LD);
+  const uint32_t bar = sb + C::OFF_BAR;
+  // kv_full | qd_full[3] | qd_empty[3] | pds_empty | sp_full | acc_done
+  const uint32_t kv_full = bar, qd_full0 = bar + 8, qd_empty0 = bar + 32, pds_empty = bar + 56,
+                 sp_full = bar + 64, acc_done = bar + 72;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_BAR + 80);
+  volatile int* abort = reinterpret_cast<volatile int*>(smem + C::OFF_BAR + 84);
+
+  const int tid = threadIdx.x, warp = tid >> 5;
+  // grid: x = (KV head, batch) pairs, y = key tile (the first key tiles see the
+  // most causal queries, so they start first)
+  const int kt = blockIdx.y, g = blockIdx.x % p.nkv, b = blockIdx.x / p.nkv;
+  const int rep = p.nq / p.nkv;
+  const int kv0 = kt * TR;
+  const int kr = kv0 + tid;  // this thread's key position
+  const int nqt = (p.S + TC - 1) / TC;
+  const int qt_start = p.causal ? kv0 / TC : 0;
+  const int per_head = nqt - qt_start;
+  const int n_it = per_head * rep;  // >= 1: the tile at kv0 is always visible
+  const int grow0 = b * p.S;
+
+  if (tid == 0) {
+    tma_prefetch_desc(&tmQ);
+    tma_prefetch_desc(&tmK);
+    tma_prefetch_desc(&tmV);
+    tma_prefetch_desc(&tmO);
+    for (int i = 0; i < 10; ++i) mbar_init(bar + 8 * i, 1);
+    fence_mbar_init();
+    *abort = 0;
+  }
+  if (warp == 0) tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  auto it_head = [&](int it) { return g * rep + it / per_head; };
+  auto it_q0 = [&](int it) { return (qt_start + it % per_head) * TC; };
+  auto load_qd = [&](int it) {
+    const int s = it % NS;
+    const uint32_t fb = qd_full0 + 8 * s;
+    const int h = it_head(it), q0 = it_q0(it);
+    mbar_arrive_expect_tx(fb, 2 * C::QT_BYTES);
+#pragma unroll
+    for (int kb = 0; kb < C::KB; ++kb) {
+      tma_load_2d(sQ + s * C::QT_BYTES + kb * 8192, &tmQ, h * D + kb * 64, grow0 + q0, fb);
+      tma_load_2d(sO + s * C::QT_BYTES + kb * 8192, &tmO, h * D + kb * 64, grow0 + q0, fb);
+    }
+  };
+  // per-query LSE (log2 units) and delta of iteration `it` into buffer it & 1
+  auto load_ld = [&](int it) {
+    if (tid < TC) {
+      const int h = it_head(it), q = it_q0(it) + tid;
+      const int64_t off = ((int64_t)b * p.nq + h) * p.S + q;
+      float* dst = sLD + (it & 1) * 2 * TC;
+      dst[tid] = q < p.S ? p.lse[off] * LOG2E : INFINITY;
+      dst[TC + tid] = q < p.S ? p.delta[off] : 0.0f;
+    }
+  };
+  constexpr uint32_t idesc_sp = idesc_bf16_f32(TR, TC, 0, 0);
+  constexpr uint32_t idesc_acc = idesc_bf16_f32(TR, D, 0, 1);
+  auto issue_sp = [&](int it) {
+    const int s = it % NS;
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) {
+      const uint32_t off = (kk >> 2) * (TR * 128) + (kk & 3) * 32;
+      const uint32_t offq = (kk >> 2) * 8192 + (kk & 3) * 32;
+      tc_mma_f16(tmem, smem_desc_sw128(sK + off, 16, 1024),
+                 smem_desc_sw128(sQ + s * C::QT_BYTES + offq, 16, 1024), idesc_sp, kk > 0);
+      tc_mma_f16(tmem + C::COL_DP, smem_desc_sw128(sV + off, 16, 1024),
+                 smem_desc_sw128(sO + s * C::QT_BYTES + offq, 16, 1024), idesc_sp, kk > 0);
+    }
+    tc_commit(sp_full);
+  };
+  auto issue_acc = [&](int it) {
+    const int s = it % NS;
+#pragma unroll
+    for (int kk = 0; kk < TC / 16; ++kk) {
+      const uint32_t b_off = s * C::QT_BYTES + kk * 2048;
+      tc_mma_f16(tmem + C::COL_DV, smem_desc_sw128(sP + kk * 32, 16, 1024),
+                 smem_desc_sw128(sO + b_off, 8192, 1024), idesc_acc, (it > 0 || kk > 0));
+      tc_mma_f16(tmem + C::COL_DK, smem_desc_sw128(sS + kk * 32, 16, 1024),
+                 smem_desc_sw128(sQ + b_off, 8192, 1024), idesc_acc, (it > 0 || kk > 0));
+    }
+    tc_commit(qd_empty0 + 8 * s);
+    tc_commit(pds_empty);
+  };
+
+  load_ld(0);
+  if (tid == 0) {
+    mbar_arrive_expect_tx(kv_full, 2 * C::KV_BYTES);
+#pragma unroll
+    for (int kb = 0; kb < C::KB; ++kb) {
+      tma_load_2d(sK + kb * (TR * 128), &tmK, g * D + kb * 64, grow0 + kv0, kv_full);
+      tma_load_2d(sV + kb * (TR * 128), &tmV, g * D + kb * 64, grow0 + kv0, kv_full);
+    }
+    load_qd(0);
+    if (n_it > 1) load_qd(1);
+    if (mbar_wait(kv_full, 0, p.err) && mbar_wait(qd_full0, 0, p.err)) {
+      tc_fence_after();
+      issue_sp(0);
+    } else {
+      *abort = 1;
+    }
+  }
+  __syncthreads();
+
+  const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+  for (int it = 0; it < n_it; ++it) {
+    const int q0 = it_q0(it);
+    if (!*abort && !mbar_wait(sp_full, it & 1, p.err)) *abort = 1;
+    tc_fence_after();
+    float st[64], dp[64];
+    ld_cols64(tmem + lane_base, st);
+    ld_cols64(tmem + lane_base + C::COL_DP, dp);
+    // refill the ring with tile it + 2: its stage was released by the
+    // accumulating products of it - 1
+    if (tid == 0 && it + 2 < n_it && !*abort) {
+      if (it == 0 || mbar_wait(qd_empty0 + 8 * ((it + 2) % NS), ((it - 1) / NS) & 1, p.err))
+        load_qd(it + 2);
+      else
+        *abort = 1;
+    }
+    if (it + 1 < n_it) load_ld(it + 1);
+    // P^T and dS^T of this key row against the 64 queries of the tile
+    const float* L = sLD + (it & 1) * 2 * TC;
+    const float* Dl = L + TC;
+#pragma unroll
+    for (int c = 0; c < TC; ++c) {
+      const int q = q0 + c;
+      const bool vis = q < p.S && kr < p.S && !(p.causal && q < kr);
+      const float pt = vis ? exp2f(st[c] * p.sl2 - L[c]) : 0.0f;
+      st[c] = pt;
+      dp[c] = pt * (dp[c] - Dl[c]);
+    }
+    // the P / dS tiles were last read by the accumulating products of it - 1
+    if (it >= 1 && !*abort && !mbar_wait(pds_empty, (it - 1) & 1, p.err)) *abort = 1;
+    store_row_sw128(smem + C::OFF_P + tid * 128, tid, st);
+    store_row_sw128(smem + C::OFF_DS + tid * 128, tid, dp);
+    fence_proxy_async();
+    tc_fence_before();
+    __syncthreads();
+    if (*abort) break;
+    if (tid == 0) {
+      tc_fence_after();
+      // next tile's S^T / dP^T first (every thread has read the current ones):
+      // its softmax-backward then overlaps this tile's dV / dK products
+      if (it + 1 < n_it) {
+        if (mbar_wait(qd_full0 + 8 * ((it + 1) % NS), ((it + 1) / NS) & 1, p.err)) issue_sp(it + 1);
+        else *abort = 1;
+      }
+      issue_acc(it);
+    }
+    __syncwarp();
+  }
+  // ---- all products done: dK (scaled) and dV rows out of TMEM
+  __syncthreads();
+  bool ok = !*abort;
+  if (tid == 0 && ok) tc_commit(acc_done);
+  if (ok && !mbar_wait(acc_done, 0, p.err)) ok = false;
+  tc_fence_after();
+  const bool row_ok = kr < p.S;
+  const int64_t orow = (int64_t)(grow0 + kr) * p.ld_out + g * D;
+  if (ok) {
+    store_tmem_row<D>(tmem + lane_base + C::COL_DK, p.scale, row_ok ? p.d0 + orow : nullptr);
+    store_tmem_row<D>(tmem + lane_base + C::COL_DV, 1.0f, row_ok ? p.d1 + orow : nullptr);
+  } else if (tid == 0) {
+    spin_10ms();  // let tensor-core work and copies still in flight finish
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+// --------------------------------------------------------------- kernel B: dQ
+template <int D>
+struct DqCfg {
+  static constexpr int KB = D / 64;
+  static constexpr int QO_BYTES = TR * D * 2;  // Q or dO rows of this CTA
+  static constexpr int KV_BYTES = TC * D * 2;  // one K or V tile
+  static constexpr int DS_BYTES = TR * TC * 2;
+  static constexpr int OFF_Q = 0;
+  static constexpr int OFF_DO = OFF_Q + QO_BYTES;
+  static constexpr int OFF_K = OFF_DO + QO_BYTES;      // NS stages
+  static constexpr int OFF_V = OFF_K + NS * KV_BYTES;  // NS stages
+  static constexpr int OFF_DS = OFF_V + NS * KV_BYTES;
+  static constexpr int OFF_BAR = OFF_DS + DS_BYTES;
+  static constexpr int SMEM = OFF_BAR + 128 + 1024;
+  static constexpr int COL_DP = 64, COL_DQ = 128;
+  static constexpr int TMEM_COLS = 256;
+};
+
+template <int D>
+__global__ void __launch_bounds__(128, 1)
+    attn_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
+                          const __grid_constant__ CUtensorMap tmK,
+                          const __grid_constant__ CUtensorMap tmV,
+                          const __grid_constant__ CUtensorMap tmO, const BwdParams p) {
+  using C = DqCfg<D>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const uint32_t sb = smem_u32(smem);
+  const uint32_t sQ = sb + C::OFF_Q, sO = sb + C::OFF_DO, sK = sb + C::OFF_K, sV = sb + C::OFF_V,
+                 sS = sb + C::OFF_DS;
+  const uint32_t bar = sb + C::OFF_BAR;
+  // qo_full | kv_full[3] | kv_empty[3] | ds_empty | sp_full | acc_done
+  const uint32_t qo_full = bar, kv_full0 = bar + 8, kv_empty0 = bar + 32, ds_empty = bar + 56,
+                 sp_full = bar + 64, acc_done = bar + 72;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_BAR + 80);
+  volatile int* abort = reinterpret_cast<volatile int*>(smem + C::OFF_BAR + 84);
+
+  const int tid = threadIdx.x, warp = tid >> 5;
+  const int nqt = (p.S + TR - 1) / TR;
+  const int qt = nqt - 1 - (int)blockIdx.y;  // longest causal rows first
+  const int h = blockIdx.x % p.nq, b = blockIdx.x / p.nq;
+  const int g = h / (p.nq / p.nkv);
+  const int q0 = qt * TR;
+  const int row = q0 + tid;
+  const int kv_end = p.causal ? min(p.S, q0 + TR) : p.S;
+  const int nkt = (kv_end + TC - 1) / TC;
+  const int grow0 = b * p.S;
+  const int64_t lrow = ((int64_t)b * p.nq + h) * p.S;
+  const float L2 = row < p.S ? p.lse[lrow + row] * LOG2E : INFINITY;
+  const float Dr = row < p.S ? p.delta[lrow + row] : 0.0f;
+
+  if (tid == 0) {
+    tma_prefetch_desc(&tmQ);
+    tma_prefetch_desc(&tmK);
+    tma_prefetch_desc(&tmV);
+    tma_prefetch_desc(&tmO);
+    for (int i = 0; i < 10; ++i) mbar_init(bar + 8 * i, 1);
+    fence_mbar_init();
+    *abort = 0;
+  }
+  if (warp == 0) tmem_alloc(smem_u32(tmem_slot), C::TMEM_COLS);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  auto load_kv = [&](int j) {
+    const int s = j % NS;
+    const uint32_t fb = kv_full0 + 8 * s;
+    mbar_arrive_expect_tx(fb, 2 * C::KV_BYTES);
+#pragma unroll
+    for (int kb = 0; kb < C::KB; ++kb) {
+      tma_load_2d(sK + s * C::KV_BYTES + kb * 8192, &tmK, g * D + kb * 64, grow0 + j * TC, fb);
+      tma_load_2d(sV + s * C::KV_BYTES + kb * 8192, &tmV, g * D + kb * 64, grow0 + j * TC, fb);
+    }
+  };
+  constexpr uint32_t idesc_sp = idesc_bf16_f32(TR, TC, 0, 0);
+  constexpr uint32_t idesc_acc = idesc_bf16_f32(TR, D, 0, 1);
+  auto issue_sp = [&](int j) {
+    const int s = j % NS;
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) {
+      const uint32_t off = (kk >> 2) * (TR * 128) + (kk & 3) * 32;
+      const uint32_t offk = (kk >> 2) * 8192 + (kk & 3) * 32;
+      tc_mma_f16(tmem, smem_desc_sw128(sQ + off, 16, 1024),
+                 smem_desc_sw128(sK + s * C::KV_BYTES + offk, 16, 1024), idesc_sp, kk > 0);
+      tc_mma_f16(tmem + C::COL_DP, smem_desc_sw128(sO + off, 16, 1024),
+                 smem_desc_sw128(sV + s * C::KV_BYTES + offk, 16, 1024), idesc_sp, kk > 0);
+    }
+    tc_commit(sp_full);
+  };
+  auto issue_acc = [&](int j) {
+    const int s = j % NS;
+#pragma unroll
+    for (int kk = 0; kk < TC / 16; ++kk)
+      tc_mma_f16(tmem + C::COL_DQ, smem_desc_sw128(sS + kk * 32, 16, 1024),
+                 smem_desc_sw128(sK + s * C::KV_BYTES + kk * 2048, 8192, 1024), idesc_acc,
+                 (j > 0 || kk > 0));
+    tc_commit(kv_empty0 + 8 * s);
+    tc_commit(ds_empty);
+  };
+
+  if (tid == 0) {
+    mbar_arrive_expect_tx(qo_full, 2 * C::QO_BYTES);
+#pragma unroll
+    for (int kb = 0; kb < C::KB; ++kb) {
+      tma_load_2d(sQ + kb * (TR * 128), &tmQ, h * D + kb * 64, grow0 + q0, qo_full);
+      tma_load_2d(sO + kb * (TR * 128), &tmO, h * D + kb * 64, grow0 + q0, qo_full);
+    }
+    load_kv(0);
+    if (nkt > 1) load_kv(1);
+    if (mbar_wait(qo_full, 0, p.err) && mbar_wait(kv_full0, 0, p.err)) {
+      tc_fence_after();
+      issue_sp(0);
+    } else {
+      *abort = 1;
+    }
+  }
+  __syncthreads();
+
+  const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+  for (int j = 0; j < nkt; ++j) {
+    if (!*abort && !mbar_wait(sp_full, j & 1, p.err)) *abort = 1;
+    tc_fence_after();
+    float sc[64], dp[64];
+    ld_cols64(tmem + lane_base, sc);
+    ld_cols64(tmem + lane_base + C::COL_DP, dp);
+    if (tid == 0 && j + 2 < nkt && !*abort) {
+      if (j == 0 || mbar_wait(kv_empty0 + 8 * ((j + 2) % NS), ((j - 1) / NS) & 1, p.err))
+        load_kv(j + 2);
+      else
+        *abort = 1;
+    }
+    const int kv0 = j * TC;
+#pragma unroll
+    for (int c = 0; c < TC; ++c) {
+      const int kv = kv0 + c;
+      const bool vis = kv < p.S && !(p.causal && kv > row);
+      const float pr = vis ? exp2f(sc[c] * p.sl2 - L2) : 0.0f;
+      dp[c] = pr * (dp[c] - Dr);
+    }
+    if (j >= 1 && !*abort && !mbar_wait(ds_empty, (j - 1) & 1, p.err)) *abort = 1;
+    store_row_sw128(smem + C::OFF_DS + tid * 128, tid, dp);
+    fence_proxy_async();
+    tc_fence_before();
+    __syncthreads();
+    if (*abort) break;
+    if (tid == 0) {
+      tc_fence_after();
+      // next tile's S / dP first, so its softmax-backward overlaps this dQ product
+      if (j + 1 < nkt) {
+        if (mbar_wait(kv_full0 + 8 * ((j + 1) % NS), ((j + 1) / NS) & 1, p.err)) issue_sp(j + 1);
+        else *abort = 1;
+      }
+      issue_acc(j);
+    }
+    __syncwarp();
+  }
+  __syncthreads();
+  bool ok = !*abort;
+  if (tid == 0 && ok) tc_commit(acc_done);
+  if (ok && !mbar_wait(acc_done, 0, p.err)) ok = false;
+  tc_fence_after();
+  if (ok) {
+    const bool row_ok = row < p.S;
+    store_tmem_row<D>(tmem + lane_base + C::COL_DQ, p.scale,
+                      row_ok ? p.d0 + (int64_t)(grow0 + row) * p.ld_out + h * D : nullptr);
+  } else if (tid == 0) {
+    spin_10ms();
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, C::TMEM_COLS);
+  }
+}
+
+template <int D>
+mgb_status bwd_tc_d(const AttnArgs& a, cudaStream_t st) {
+  const uint64_t T = (uint64_t)a.B * a.S;
+  BwdParams p{};
+  p.B = a.B; p.S = a.S; p.nq = a.nq; p.nkv = a.nkv; p.causal = a.causal;
+  p.lse = a.lse; p.delta = a.delta;
+  p.err = device_error_word();
+  p.sl2 = LOG2E / sqrtf((float)D);
+  p.scale = 1.0f / sqrtf((float)D);
+  // kernel A: K/V rows of 128, Q/dO tiles of 64
+  {
+    using C = DkvCfg<D>;
+    CUtensorMap tq, tk, tv, to;
+    if (tmap_encode_bf16_2d(&tq, a.q, (uint64_t)a.nq * D, T, a.ld_q, 64, TC) != CUDA_SUCCESS ||
+        tmap_encode_bf16_2d(&to, a.dout, (uint64_t)a.nq * D, T, a.ld_do, 64, TC) != CUDA_SUCCESS ||
+        tmap_encode_bf16_2d(&tk, a.k, (uint64_t)a.nkv * D, T, a.ld_kv, 64, TR) != CUDA_SUCCESS ||
+        tmap_encode_bf16_2d(&tv, a.v, (uint64_t)a.nkv * D, T, a.ld_kv, 64, TR) != CUDA_SUCCESS)
+      return MGB_ERR_CUDA;
+    p.d0 = reinterpret_cast<bf16*>(a.dk);
+    p.d1 = reinterpret_cast<bf16*>(a.dv);
+    p.ld_out = a.ld_dkv;
+    auto k = attn_bwd_dkdv_tc_kernel<D>;
+    if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess)
+      return MGB_ERR_CUDA;
+    dim3 grid(a.nkv * a.B, (a.S + TR - 1) / TR);
+    k<<<grid, 128, C::SMEM, st>>>(tq, tk, tv, to, p);
+  }
+  // kernel B: Q/dO rows of 128, K/V tiles of 64
+  {
+    using C = DqCfg<D>;
+    CUtensorMap tq, tk, tv, to;
+    if (tmap_encode_bf16_2d(&tq, a.q, (uint64_t)a.nq * D, T, a.ld_q, 64, TR) != CUDA_SUCCESS ||
+        tmap_encode_bf16_2d(&to, a.dout, (uint64_t)a.nq * D, T, a.ld_do, 64, TR) != CUDA_SUCCESS ||
+        tmap_encode_bf16_2d(&tk, a.k, (uint64_t)a.nkv * D, T, a.ld_kv, 64, TC) != CUDA_SUCCESS ||
+        tmap_encode_bf16_2d(&tv, a.v, (uint64_t)a.nkv * D, T, a.ld_kv, 64, TC) != CUDA_SUCCESS)
+      return MGB_ERR_CUDA;
+    p.d0 = reinterpret_cast<bf16*>(a.dq);
+    p.d1 = nullptr;
+    p.ld_out = a.ld_dq;
+    auto k = attn_bwd_dq_tc_kernel<D>;
+    if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess)
+      return MGB_ERR_CUDA;
+    dim3 grid(a.nq * a.B, (a.S + TR - 1) / TR);
+    k<<<grid, 128, C::SMEM, st>>>(tq, tk, tv, to, p);
+  }
+  return cudaGetLastError() == cudaSuccess ? MGB_OK : MGB_ERR_CUDA;
+}
+
+}  // namespace
+
+mgb_status attention_tc_bwd_main(const AttnArgs& a, cudaStream_t st) {
+  if (a.d == 64) return bwd_tc_d<64>(a, st);
+  if (a.d == 128) return bwd_tc_d<128>(a, st);
+  return MGB_ERR_UNSUPPORTED;
+}
+
+}  // namespace mgb

@@ -25,6 +25,8 @@ namespace mgb {
 namespace {
 
 constexpr int MAXV = 4;  // 16-byte vectors per thread
+// Widest row whose dgamma/dbeta partial sums fit one block's shared memory.
+constexpr int kLnBwdMaxCols = 16384;
 
 template <typename T> struct Vec;
 template <> struct Vec<bf16> { static constexpr int N = 8; };
@@ -135,6 +137,31 @@ __global__ void ln_fwd_kernel(int rows, int cols, float eps, const T* __restrict
   }
 }
 
+// Sum of a float2 over the block (one pass of shuffles + shared memory).
+__device__ __forceinline__ float2 block_sum2(float2 v, float2* red) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    v.x += __shfl_xor_sync(0xffffffffu, v.x, o);
+    v.y += __shfl_xor_sync(0xffffffffu, v.y, o);
+  }
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nw = blockDim.x >> 5;
+  __syncthreads();
+  if (lane == 0) red[warp] = v;
+  __syncthreads();
+  float2 t = lane < nw ? red[lane] : make_float2(0.0f, 0.0f);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    t.x += __shfl_xor_sync(0xffffffffu, t.x, o);
+    t.y += __shfl_xor_sync(0xffffffffu, t.y, o);
+  }
+  return t;
+}
+
+// Row blocks stride over the rows. The dgamma/dbeta partial sums of the
+// block's columns live in shared memory (2 * cols floats, laid out [j][vector]
+// so that lanes touch consecutive words), which keeps registers low enough for
+// several blocks per SM.
 template <typename T>
 __global__ void ln_bwd_kernel(int rows, int cols, const T* __restrict__ x,
                               const float* __restrict__ mean, const float* __restrict__ rstd,
@@ -142,19 +169,20 @@ __global__ void ln_bwd_kernel(int rows, int cols, const T* __restrict__ x,
                               const T* __restrict__ dres, T* __restrict__ dx,
                               float* __restrict__ part) {
   constexpr int VN = Vec<T>::N;
-  __shared__ float red[32];
+  extern __shared__ float sacc[];  // [2][VN][nvec] when part != nullptr
+  __shared__ float2 red[32];
   const int nvec = cols / VN;
-  float pg[MAXV][VN], pb[MAXV][VN];
-  float gam[MAXV][VN];
-#pragma unroll
-  for (int i = 0; i < MAXV; ++i)
-#pragma unroll
-    for (int j = 0; j < VN; ++j) { pg[i][j] = 0.0f; pb[i][j] = 0.0f; gam[i][j] = 1.0f; }
-  if (gamma) {
+  float* spg = sacc;
+  float* spb = sacc + cols;
+  if (part) {
+    // every thread zeroes exactly the slots it accumulates into
 #pragma unroll
     for (int i = 0; i < MAXV; ++i) {
       const int vi = threadIdx.x + i * blockDim.x;
-      if (vi < nvec) vload(gamma + vi * VN, gam[i]);
+      if (vi < nvec) {
+#pragma unroll
+        for (int j = 0; j < VN; ++j) spg[j * nvec + vi] = spb[j * nvec + vi] = 0.0f;
+      }
     }
   }
   for (int row = blockIdx.x; row < rows; row += gridDim.x) {
@@ -165,22 +193,26 @@ __global__ void ln_bwd_kernel(int rows, int cols, const T* __restrict__ x,
     for (int i = 0; i < MAXV; ++i) {
       const int vi = threadIdx.x + i * blockDim.x;
       if (vi < nvec) {
-        float xv[VN], dv[VN];
+        float xv[VN], dv[VN], gm[VN];
         vload(x + (int64_t)row * cols + vi * VN, xv);
         vload(dy + (int64_t)row * cols + vi * VN, dv);
+        if (gamma) vload(gamma + vi * VN, gm);
 #pragma unroll
         for (int j = 0; j < VN; ++j) {
           xh[i][j] = (xv[j] - mu) * rs;
-          g[i][j] = dv[j] * gam[i][j];
+          g[i][j] = gamma ? dv[j] * gm[j] : dv[j];
           s1 += g[i][j];
           s2 += g[i][j] * xh[i][j];
-          pg[i][j] += dv[j] * xh[i][j];
-          pb[i][j] += dv[j];
+          if (part) {
+            spg[j * nvec + vi] += dv[j] * xh[i][j];
+            spb[j * nvec + vi] += dv[j];
+          }
         }
       }
     }
-    const float mg = block_sum(s1, red) / cols;
-    const float mgx = block_sum(s2, red) / cols;
+    const float2 tot = block_sum2(make_float2(s1, s2), red);
+    const float mg = tot.x / cols;
+    const float mgx = tot.y / cols;
 #pragma unroll
     for (int i = 0; i < MAXV; ++i) {
       const int vi = threadIdx.x + i * blockDim.x;
@@ -197,16 +229,23 @@ __global__ void ln_bwd_kernel(int rows, int cols, const T* __restrict__ x,
     }
   }
   if (part) {
+    // each thread wrote only its own columns; no barrier needed before reading them
     float* pgr = part + (int64_t)blockIdx.x * cols;
     float* pbr = part + (int64_t)(gridDim.x + blockIdx.x) * cols;
 #pragma unroll
     for (int i = 0; i < MAXV; ++i) {
       const int vi = threadIdx.x + i * blockDim.x;
       if (vi < nvec) {
+        float a[VN], b[VN];
 #pragma unroll
         for (int j = 0; j < VN; ++j) {
-          pgr[vi * VN + j] = pg[i][j];
-          pbr[vi * VN + j] = pb[i][j];
+          a[j] = spg[j * nvec + vi];
+          b[j] = spb[j * nvec + vi];
+        }
+#pragma unroll
+        for (int j = 0; j < VN; j += 4) {
+          *reinterpret_cast<float4*>(pgr + vi * VN + j) = make_float4(a[j], a[j + 1], a[j + 2], a[j + 3]);
+          *reinterpret_cast<float4*>(pbr + vi * VN + j) = make_float4(b[j], b[j + 1], b[j + 2], b[j + 3]);
         }
       }
     }
@@ -288,9 +327,10 @@ int ln_threads(int cols, int vn) {
 
 }  // namespace
 
-// Row blocks of the backward: enough resident blocks (8 per SM) to hide the
-// latency of the per-row reductions; each writes one partial dgamma/dbeta row.
-int layernorm_bwd_parts(int rows) { return rows < 1216 ? (rows > 0 ? rows : 1) : 1216; }
+// Row blocks of the backward: about one resident wave (several blocks per SM)
+// to hide the latency of the per-row reductions; each writes one partial
+// dgamma/dbeta row.
+int layernorm_bwd_parts(int rows) { return rows < 1024 ? (rows > 0 ? rows : 1) : 1024; }
 int colsum_parts(int M) { return M < 64 * 8 ? 1 : 64; }
 
 mgb_status layernorm_fwd_launch(int rows, int cols, int dtype, float eps, const void* x,
@@ -321,19 +361,29 @@ mgb_status layernorm_bwd_launch(int rows, int cols, int dtype, const void* x, co
   const int threads = ln_threads(cols, vn);
   if (threads > 1024) return MGB_ERR_UNSUPPORTED;
   const bool want = (dgamma || dbeta) && part;
+  // dgamma/dbeta partials live in shared memory: 2 * cols floats per block
+  if (want && cols > kLnBwdMaxCols) return MGB_ERR_UNSUPPORTED;
+  const int smem = want ? 2 * cols * (int)sizeof(float) : 0;
   if (rows == 0) nparts = 1;
+  if (rows > 0 && smem > 48 * 1024) {
+    const cudaError_t e =
+        dtype == MGB_BF16
+            ? cudaFuncSetAttribute(ln_bwd_kernel<bf16>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)
+            : cudaFuncSetAttribute(ln_bwd_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return MGB_ERR_CUDA;
+  }
   LaunchScope scope(PROF_LN_BWD, st, (rows > 0 ? 1 : 0) + (want ? 1 : 0));
   if (rows > 0) {
     if (dtype == MGB_BF16)
-      ln_bwd_kernel<bf16><<<nparts, threads, 0, st>>>(rows, cols, (const bf16*)x, mean, rstd,
-                                                       (const bf16*)gamma, (const bf16*)dy,
-                                                       (const bf16*)dres, (bf16*)dx,
-                                                       want ? part : nullptr);
+      ln_bwd_kernel<bf16><<<nparts, threads, smem, st>>>(rows, cols, (const bf16*)x, mean, rstd,
+                                                          (const bf16*)gamma, (const bf16*)dy,
+                                                          (const bf16*)dres, (bf16*)dx,
+                                                          want ? part : nullptr);
     else
-      ln_bwd_kernel<float><<<nparts, threads, 0, st>>>(rows, cols, (const float*)x, mean, rstd,
-                                                        (const float*)gamma, (const float*)dy,
-                                                        (const float*)dres, (float*)dx,
-                                                        want ? part : nullptr);
+      ln_bwd_kernel<float><<<nparts, threads, smem, st>>>(rows, cols, (const float*)x, mean, rstd,
+                                                           (const float*)gamma, (const float*)dy,
+                                                           (const float*)dres, (float*)dx,
+                                                           want ? part : nullptr);
   } else if (want) {
     cudaMemsetAsync(part, 0, sizeof(float) * 2 * cols, st);
   }

@@ -96,6 +96,8 @@ def load() -> ctypes.CDLL:
             "mgb_layernorm_bwd": [I32, I32, I32, P, P, P, P, P, P, P, P, P, P, SZ, P],
             "mgb_layernorm_bwd_noalloc": [I32, I32, I32, P, P, P, P, P, P, P, P, P, P],
             "mgb_attention_fwd": [I32, I32, I32, I32, I32, I32, I32, P, P, P, I64, I64, P, P, P],
+            "mgb_attention_bwd": [I32, I32, I32, I32, I32, I32, I32, P, P, P, I64, I64, P, P, P,
+                                  I64, P, P, P, I64, I64, P, SZ, P],
             "mgb_device_status": [P],
             "mgb_selftest_wait_timeout": [U64, P],
         }
@@ -255,6 +257,16 @@ def mgb_attention_fwd(batch, seq, n_q_heads, n_kv_heads, head_dim, causal, dtype
     _check(load().mgb_attention_fwd(batch, seq, n_q_heads, n_kv_heads, head_dim, int(causal), dtype,
                                     _ptr(q), _ptr(k), _ptr(v), ld_q, ld_kv, _ptr(o), _ptr(lse),
                                     _stream(stream)), "mgb_attention_fwd")
+
+
+def mgb_attention_bwd(batch, seq, n_q_heads, n_kv_heads, head_dim, causal, dtype, q, k, v, ld_q,
+                      ld_kv, o, lse, dout, ld_do, dq, dk, dv, ld_dq, ld_dkv, ws,
+                      stream=None) -> None:
+    _check(load().mgb_attention_bwd(batch, seq, n_q_heads, n_kv_heads, head_dim, int(causal), dtype,
+                                    _ptr(q), _ptr(k), _ptr(v), ld_q, ld_kv, _ptr(o), _ptr(lse),
+                                    _ptr(dout), ld_do, _ptr(dq), _ptr(dk), _ptr(dv), ld_dq, ld_dkv,
+                                    _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)),
+           "mgb_attention_bwd")
 
 
 def mgb_device_status(stream=None) -> int:
