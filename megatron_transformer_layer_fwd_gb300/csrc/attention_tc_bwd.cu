@@ -7,9 +7,12 @@
 //   dV_g = sum_h P^T dO_h,   dK_g = sum_h dS^T Q_h / sqrt(d),   dQ_h = dS K_g / sqrt(d),
 // summing over the query heads h of the GQA group g.
 //
-// Kernel A (dK, dV): one CTA = 128 keys of one KV head; thread t owns key row
-// t (= TMEM lane t). It loops over every query head of the group and every
-// 64-query tile that can see its keys (Q/dO tiles in a 3-stage TMA ring):
+// Both kernels run 8 warps: the warps w and w+4 share TMEM lane quarter w
+// (32 rows) and split each 64-column tile into two halves of 32 columns.
+//
+// Kernel A (dK, dV): one CTA = 128 keys of one KV head (key row = TMEM lane).
+// It loops over every query head of the group and every 64-query tile that
+// can see its keys (Q/dO tiles in a 3-stage TMA ring):
 //   S^T  = K Q^T     M=128 N=64 K=d     TMEM [0, 64)
 //   dP^T = V dO^T    M=128 N=64 K=d     TMEM [64, 128)
 //   registers: P^T = exp2(S^T*log2e/sqrt(d) - LSE*log2e), dS^T = P^T (dP^T - delta)
@@ -58,37 +61,35 @@ __device__ __forceinline__ void fence_proxy_async() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
-__device__ __forceinline__ void ld_cols64(uint32_t taddr, float (&v)[64]) {
+__device__ __forceinline__ void ld_cols32(uint32_t taddr, float (&v)[32]) {
   uint32_t r[32];
   tmem_ld32(taddr, r);
   tmem_ld_wait();
 #pragma unroll
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
-  tmem_ld32(taddr + 32, r);
-  tmem_ld_wait();
-#pragma unroll
-  for (int i = 0; i < 32; ++i) v[32 + i] = __uint_as_float(r[i]);
 }
 
-// 64 floats -> bf16 row of a K-major 128-byte-swizzled [rows][64] tile
-__device__ __forceinline__ void store_row_sw128(uint8_t* row_ptr, int row, const float (&v)[64]) {
+// 32 floats -> bf16, the 16-byte chunks half*4 .. half*4+3 of row `row` of a
+// K-major 128-byte-swizzled [rows][64] tile (chunk c sits at c ^ (row & 7))
+__device__ __forceinline__ void store_half_row_sw128(uint8_t* row_ptr, int row, int half,
+                                                     const float (&v)[32]) {
 #pragma unroll
-  for (int c = 0; c < 8; ++c) {
+  for (int c = 0; c < 4; ++c) {
     uint4 w;
     w.x = pack_bf16x2(v[8 * c], v[8 * c + 1]);
     w.y = pack_bf16x2(v[8 * c + 2], v[8 * c + 3]);
     w.z = pack_bf16x2(v[8 * c + 4], v[8 * c + 5]);
     w.w = pack_bf16x2(v[8 * c + 6], v[8 * c + 7]);
-    *reinterpret_cast<uint4*>(row_ptr + ((c ^ (row & 7)) << 4)) = w;
+    *reinterpret_cast<uint4*>(row_ptr + (((half * 4 + c) ^ (row & 7)) << 4)) = w;
   }
 }
 
-// TMEM row (this thread's lane) of d columns, scaled, to global bf16 (all
-// lanes must call; out == nullptr skips the store)
-template <int D>
+// NC columns of this thread's TMEM lane, scaled, to global bf16 (all lanes of
+// the warp must call; out == nullptr skips the store)
+template <int NC>
 __device__ __forceinline__ void store_tmem_row(uint32_t taddr, float scale, bf16* out) {
 #pragma unroll
-  for (int c = 0; c < D / 32; ++c) {
+  for (int c = 0; c < NC / 32; ++c) {
     uint32_t r[32];
     tmem_ld32(taddr + c * 32, r);
     tmem_ld_wait();
@@ -131,7 +132,7 @@ struct DkvCfg {
 };
 
 template <int D>
-__global__ void __launch_bounds__(128, 1)
+__global__ void __launch_bounds__(256, 1)
     attn_bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
                             const __grid_constant__ CUtensorMap tmK,
                             const __grid_constant__ CUtensorMap tmV,
@@ -151,13 +152,16 @@ __global__ void __launch_bounds__(128, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_BAR + 80);
   volatile int* abort = reinterpret_cast<volatile int*>(smem + C::OFF_BAR + 84);
 
+  // 8 warps: warp w reads TMEM lanes 32*(w%4).. (its key rows) and handles the
+  // column half w/4 of every 64-column tile
   const int tid = threadIdx.x, warp = tid >> 5;
+  const int rrow = (warp & 3) * 32 + (tid & 31), half = warp >> 2;
   // grid: x = (KV head, batch) pairs, y = key tile (the first key tiles see the
   // most causal queries, so they start first)
   const int kt = blockIdx.y, g = blockIdx.x % p.nkv, b = blockIdx.x / p.nkv;
   const int rep = p.nq / p.nkv;
   const int kv0 = kt * TR;
-  const int kr = kv0 + tid;  // this thread's key position
+  const int kr = kv0 + rrow;  // this thread's key position
   const int nqt = (p.S + TC - 1) / TC;
   const int qt_start = p.causal ? kv0 / TC : 0;
   const int per_head = nqt - qt_start;
@@ -250,14 +254,15 @@ __global__ void __launch_bounds__(128, 1)
   }
   __syncthreads();
 
-  const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+  const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+  const uint32_t col0 = half * 32;  // this warp's columns of the 64-wide tiles
   for (int it = 0; it < n_it; ++it) {
-    const int q0 = it_q0(it);
+    const int q0 = it_q0(it) + half * 32;  // first query of this thread's columns
     if (!*abort && !mbar_wait(sp_full, it & 1, p.err)) *abort = 1;
     tc_fence_after();
-    float st[64], dp[64];
-    ld_cols64(tmem + lane_base, st);
-    ld_cols64(tmem + lane_base + C::COL_DP, dp);
+    float st[32], dp[32];
+    ld_cols32(tmem + lane_base + col0, st);
+    ld_cols32(tmem + lane_base + C::COL_DP + col0, dp);
     // refill the ring with tile it + 2: its stage was released by the
     // accumulating products of it - 1
     if (tid == 0 && it + 2 < n_it && !*abort) {
@@ -267,21 +272,32 @@ __global__ void __launch_bounds__(128, 1)
         *abort = 1;
     }
     if (it + 1 < n_it) load_ld(it + 1);
-    // P^T and dS^T of this key row against the 64 queries of the tile
-    const float* L = sLD + (it & 1) * 2 * TC;
+    // P^T and dS^T of this key row against its 32 queries of the tile
+    const float* L = sLD + (it & 1) * 2 * TC + col0;
     const float* Dl = L + TC;
+    // mask-free when every query of the half-tile sees every key of the CTA
+    const bool full = q0 + 32 <= p.S && kv0 + TR <= p.S && (!p.causal || q0 >= kv0 + TR - 1);
+    if (full) {
 #pragma unroll
-    for (int c = 0; c < TC; ++c) {
-      const int q = q0 + c;
-      const bool vis = q < p.S && kr < p.S && !(p.causal && q < kr);
-      const float pt = vis ? exp2f(st[c] * p.sl2 - L[c]) : 0.0f;
-      st[c] = pt;
-      dp[c] = pt * (dp[c] - Dl[c]);
+      for (int c = 0; c < 32; ++c) {
+        const float pt = exp2f(fmaf(st[c], p.sl2, -L[c]));
+        st[c] = pt;
+        dp[c] = pt * (dp[c] - Dl[c]);
+      }
+    } else {
+#pragma unroll
+      for (int c = 0; c < 32; ++c) {
+        const int q = q0 + c;
+        const bool vis = q < p.S && kr < p.S && !(p.causal && q < kr);
+        const float pt = vis ? exp2f(fmaf(st[c], p.sl2, -L[c])) : 0.0f;
+        st[c] = pt;
+        dp[c] = pt * (dp[c] - Dl[c]);
+      }
     }
     // the P / dS tiles were last read by the accumulating products of it - 1
     if (it >= 1 && !*abort && !mbar_wait(pds_empty, (it - 1) & 1, p.err)) *abort = 1;
-    store_row_sw128(smem + C::OFF_P + tid * 128, tid, st);
-    store_row_sw128(smem + C::OFF_DS + tid * 128, tid, dp);
+    store_half_row_sw128(smem + C::OFF_P + rrow * 128, rrow, half, st);
+    store_half_row_sw128(smem + C::OFF_DS + rrow * 128, rrow, half, dp);
     fence_proxy_async();
     tc_fence_before();
     __syncthreads();
@@ -307,8 +323,12 @@ __global__ void __launch_bounds__(128, 1)
   const bool row_ok = kr < p.S;
   const int64_t orow = (int64_t)(grow0 + kr) * p.ld_out + g * D;
   if (ok) {
-    store_tmem_row<D>(tmem + lane_base + C::COL_DK, p.scale, row_ok ? p.d0 + orow : nullptr);
-    store_tmem_row<D>(tmem + lane_base + C::COL_DV, 1.0f, row_ok ? p.d1 + orow : nullptr);
+    // the two warps of a lane quarter store one half of the d columns each
+    const int c0 = half * (D / 2);
+    store_tmem_row<D / 2>(tmem + lane_base + C::COL_DK + c0, p.scale,
+                          row_ok ? p.d0 + orow + c0 : nullptr);
+    store_tmem_row<D / 2>(tmem + lane_base + C::COL_DV + c0, 1.0f,
+                          row_ok ? p.d1 + orow + c0 : nullptr);
   } else if (tid == 0) {
     spin_10ms();  // let tensor-core work and copies still in flight finish
   }
@@ -339,7 +359,7 @@ struct DqCfg {
 };
 
 template <int D>
-__global__ void __launch_bounds__(128, 1)
+__global__ void __launch_bounds__(256, 1)
     attn_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
                           const __grid_constant__ CUtensorMap tmK,
                           const __grid_constant__ CUtensorMap tmV,
@@ -358,13 +378,16 @@ __global__ void __launch_bounds__(128, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_BAR + 80);
   volatile int* abort = reinterpret_cast<volatile int*>(smem + C::OFF_BAR + 84);
 
+  // 8 warps: warp w reads TMEM lanes 32*(w%4).. (its query rows) and handles
+  // the column half w/4 of every 64-column tile
   const int tid = threadIdx.x, warp = tid >> 5;
+  const int rrow = (warp & 3) * 32 + (tid & 31), half = warp >> 2;
   const int nqt = (p.S + TR - 1) / TR;
   const int qt = nqt - 1 - (int)blockIdx.y;  // longest causal rows first
   const int h = blockIdx.x % p.nq, b = blockIdx.x / p.nq;
   const int g = h / (p.nq / p.nkv);
   const int q0 = qt * TR;
-  const int row = q0 + tid;
+  const int row = q0 + rrow;
   const int kv_end = p.causal ? min(p.S, q0 + TR) : p.S;
   const int nkt = (kv_end + TC - 1) / TC;
   const int grow0 = b * p.S;
@@ -441,29 +464,37 @@ __global__ void __launch_bounds__(128, 1)
   }
   __syncthreads();
 
-  const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+  const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+  const uint32_t col0 = half * 32;  // this warp's columns of the 64-wide tiles
   for (int j = 0; j < nkt; ++j) {
     if (!*abort && !mbar_wait(sp_full, j & 1, p.err)) *abort = 1;
     tc_fence_after();
-    float sc[64], dp[64];
-    ld_cols64(tmem + lane_base, sc);
-    ld_cols64(tmem + lane_base + C::COL_DP, dp);
+    float sc[32], dp[32];
+    ld_cols32(tmem + lane_base + col0, sc);
+    ld_cols32(tmem + lane_base + C::COL_DP + col0, dp);
     if (tid == 0 && j + 2 < nkt && !*abort) {
       if (j == 0 || mbar_wait(kv_empty0 + 8 * ((j + 2) % NS), ((j - 1) / NS) & 1, p.err))
         load_kv(j + 2);
       else
         *abort = 1;
     }
-    const int kv0 = j * TC;
+    const int kv0 = j * TC + col0;  // first key of this thread's columns
+    // mask-free when every query row of the CTA sees every key of the half-tile
+    const bool full = kv0 + 32 <= p.S && (!p.causal || kv0 + 31 <= q0);
+    if (full) {
 #pragma unroll
-    for (int c = 0; c < TC; ++c) {
-      const int kv = kv0 + c;
-      const bool vis = kv < p.S && !(p.causal && kv > row);
-      const float pr = vis ? exp2f(sc[c] * p.sl2 - L2) : 0.0f;
-      dp[c] = pr * (dp[c] - Dr);
+      for (int c = 0; c < 32; ++c) dp[c] = exp2f(fmaf(sc[c], p.sl2, -L2)) * (dp[c] - Dr);
+    } else {
+#pragma unroll
+      for (int c = 0; c < 32; ++c) {
+        const int kv = kv0 + c;
+        const bool vis = kv < p.S && !(p.causal && kv > row);
+        const float pr = vis ? exp2f(fmaf(sc[c], p.sl2, -L2)) : 0.0f;
+        dp[c] = pr * (dp[c] - Dr);
+      }
     }
     if (j >= 1 && !*abort && !mbar_wait(ds_empty, (j - 1) & 1, p.err)) *abort = 1;
-    store_row_sw128(smem + C::OFF_DS + tid * 128, tid, dp);
+    store_half_row_sw128(smem + C::OFF_DS + rrow * 128, rrow, half, dp);
     fence_proxy_async();
     tc_fence_before();
     __syncthreads();
@@ -486,8 +517,9 @@ __global__ void __launch_bounds__(128, 1)
   tc_fence_after();
   if (ok) {
     const bool row_ok = row < p.S;
-    store_tmem_row<D>(tmem + lane_base + C::COL_DQ, p.scale,
-                      row_ok ? p.d0 + (int64_t)(grow0 + row) * p.ld_out + h * D : nullptr);
+    const int c0 = half * (D / 2);
+    store_tmem_row<D / 2>(tmem + lane_base + C::COL_DQ + c0, p.scale,
+                          row_ok ? p.d0 + (int64_t)(grow0 + row) * p.ld_out + h * D + c0 : nullptr);
   } else if (tid == 0) {
     spin_10ms();
   }
@@ -524,7 +556,7 @@ mgb_status bwd_tc_d(const AttnArgs& a, cudaStream_t st) {
     if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess)
       return MGB_ERR_CUDA;
     dim3 grid(a.nkv * a.B, (a.S + TR - 1) / TR);
-    k<<<grid, 128, C::SMEM, st>>>(tq, tk, tv, to, p);
+    k<<<grid, 256, C::SMEM, st>>>(tq, tk, tv, to, p);
   }
   // kernel B: Q/dO rows of 128, K/V tiles of 64
   {
@@ -542,7 +574,7 @@ mgb_status bwd_tc_d(const AttnArgs& a, cudaStream_t st) {
     if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess)
       return MGB_ERR_CUDA;
     dim3 grid(a.nq * a.B, (a.S + TR - 1) / TR);
-    k<<<grid, 128, C::SMEM, st>>>(tq, tk, tv, to, p);
+    k<<<grid, 256, C::SMEM, st>>>(tq, tk, tv, to, p);
   }
   return cudaGetLastError() == cudaSuccess ? MGB_OK : MGB_ERR_CUDA;
 }
