@@ -10,16 +10,19 @@
 //   input grad   dX = dY W       A K-major,       B MN-major (W stored [K_red, N])
 //   weight grad  dW = dY^T X     A MN-major,      B MN-major (token dim reduced)
 //
-// One CTA computes one BM x BN output tile (BM = 128 rows = 128 TMEM lanes,
-// BN columns of float32 accumulator). Four warps:
+// Output tiles are BM x BN (BM = 128 rows = 128 TMEM lanes, BN columns of
+// float32 accumulator). One persistent CTA per SM walks its tiles with six
+// warps:
 //   warp 0 lane 0  TMA producer: K-blocks of 64 into a STAGES-deep smem ring
 //   warp 1 lane 0  MMA issuer: 4 x tcgen05.mma (K = 16 each) per K-block, then
-//                  tcgen05.commit to the stage's "empty" barrier
-//   all 4 warps    epilogue: tcgen05.ld rows out of TMEM (warp w owns TMEM
-//                  lanes 32w..32w+31 = tile rows), fused bias / activation /
-//                  residual / activation-gradient, 16-byte global stores.
-// Tiles are visited in groups of GROUP_M row-tiles so concurrently resident
-// CTAs share A and B tiles through L2.
+//                  tcgen05.commit to the stage's "empty" barrier; tile i
+//                  accumulates into TMEM buffer i & 1
+//   warps 2-5      epilogue: tcgen05.ld rows out of TMEM (warp w reads lanes
+//                  32*(w%4).. = tile rows), fused bias / activation / residual
+//                  / activation-gradient, 16-byte global stores - while the
+//                  MMAs of the next tile run into the other TMEM buffer.
+// Tiles are visited in groups of row tiles sized so the group's A panel stays
+// in L2 while B streams past (concurrently resident CTAs share both).
 //
 // Shared-memory operand layouts (128-byte swizzle, as TMA writes them):
 //   K-major tile: rows of 64 bf16 (128 B); 8-row atoms of 1024 B (SBO = 1024);
@@ -42,7 +45,6 @@ namespace {
 
 constexpr int BM = 128;
 constexpr int BK = 64;
-constexpr int GROUP_M = 16;
 
 struct EpiParams {
   int M, N, K;
@@ -59,7 +61,7 @@ struct EpiParams {
   int64_t ldaux;
   int glu_block;
   int accumulate;
-  int tiles_m, tiles_n;
+  int tiles_m, tiles_n, group_m;
   int* err;
   const int32_t* tgt;
   int tgt_v0;
@@ -271,8 +273,30 @@ __device__ void epilogue_row(const EpiParams& p, uint32_t tmem_row, int row, int
   }
 }
 
+// Tile `tile` of the grouped raster: group_m row tiles per group, the row
+// tile advancing fastest inside a group.
+__device__ __forceinline__ void tile_origin(const EpiParams& p, int tile, int bn, int& m0,
+                                            int& n0) {
+  const int per_group = p.group_m * p.tiles_n;
+  const int group = tile / per_group;
+  const int first_m = group * p.group_m;
+  const int gm = min(p.tiles_m - first_m, p.group_m);
+  const int in_group = tile - group * per_group;
+  m0 = (first_m + in_group % gm) * BM;
+  n0 = (in_group / gm) * bn;
+}
+
+// Persistent and warp-specialised: one CTA per SM walks the tiles
+// blockIdx.x, blockIdx.x + gridDim.x, ... Six warps:
+//   warp 0 (one lane)  TMA producer over every k-block of every tile of the CTA
+//   warp 1 (one lane)  MMA issuer: tile i accumulates into TMEM buffer i & 1
+//   warps 2-5          epilogue of tile i from buffer i & 1 (warp w reads TMEM
+//                      lanes 32*(w%4)..) while tile i+1's MMAs fill the other
+// The two accumulators take 2*BN TMEM columns. A wait that runs out sets a
+// shared abort flag; every role then leaves its loop (no CTA barrier inside
+// the loops) and the CTA meets once more to free TMEM.
 template <int BN, int STAGES, int A_MN, int B_MN>
-__global__ void __launch_bounds__(128, 1)
+__global__ void __launch_bounds__(192, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                    const __grid_constant__ CUtensorMap tmB, const EpiParams p) {
   using C = Cfg<BN, STAGES>;
@@ -280,25 +304,17 @@ __global__ void __launch_bounds__(128, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::TILE_BYTES);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 1);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 4);
+  volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
   const uint32_t tiles = smem_u32(smem);
   const uint32_t full0 = smem_u32(bars);
   const uint32_t empty0 = full0 + 8 * STAGES;
-  const uint32_t done = full0 + 16 * STAGES;
+  const uint32_t accf0 = empty0 + 8 * STAGES;  // accumulator ready, per buffer
+  const uint32_t acce0 = accf0 + 16;           // accumulator drained, per buffer
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-
-  // grouped raster: GROUP_M row tiles per group, columns advance slowest in a group
-  const int tile = blockIdx.x;
-  const int per_group = GROUP_M * p.tiles_n;
-  const int group = tile / per_group;
-  const int first_m = group * GROUP_M;
-  const int gm = min(p.tiles_m - first_m, GROUP_M);
-  const int in_group = tile - group * per_group;
-  const int tm = first_m + in_group % gm;
-  const int tn = in_group / gm;
-  const int m0 = tm * BM, n0 = tn * BN;
   const int num_k = (p.K + BK - 1) / BK;
+  const int total = p.tiles_m * p.tiles_n;
 
   if (threadIdx.x == 0) {
     tma_prefetch_desc(&tmA);
@@ -307,72 +323,118 @@ __global__ void __launch_bounds__(128, 1)
       mbar_init(full0 + 8 * s, 1);
       mbar_init(empty0 + 8 * s, 1);
     }
-    mbar_init(done, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(accf0 + 8 * b, 1);
+      mbar_init(acce0 + 8 * b, 4);  // one arrival per epilogue warp
+    }
     fence_mbar_init();
+    *abort = 0;
   }
-  if (warp == 0) tmem_alloc(smem_u32(tmem_slot), BN);
+  if (warp == 0) tmem_alloc(smem_u32(tmem_slot), 2 * BN);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 0 && lane == 0) {
-    // ---------------- TMA producer
-    for (int kb = 0; kb < num_k; ++kb) {
-      const int s = kb % STAGES;
-      const uint32_t round = kb / STAGES;
-      if (!mbar_wait(empty0 + 8 * s, (round & 1) ^ 1, p.err)) break;
-      const uint32_t sa = tiles + s * C::STAGE_BYTES;
-      const uint32_t sb = sa + C::A_BYTES;
-      const uint32_t fb = full0 + 8 * s;
-      mbar_arrive_expect_tx(fb, C::STAGE_BYTES);
-      const int k0 = kb * BK;
-      if (A_MN == 0) {
-        tma_load_2d(sa, &tmA, k0, m0, fb);
-      } else {
-        tma_load_2d(sa, &tmA, m0, k0, fb);
-        tma_load_2d(sa + 8192, &tmA, m0 + 64, k0, fb);
-      }
-      if (B_MN == 0) {
-        tma_load_2d(sb, &tmB, k0, n0, fb);
-      } else {
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------- TMA producer
+      uint32_t kg = 0;  // k-blocks issued by this CTA so far (ring position)
+      for (int tile = blockIdx.x; tile < total && !*abort; tile += gridDim.x) {
+        int m0, n0;
+        tile_origin(p, tile, BN, m0, n0);
+        for (int kb = 0; kb < num_k; ++kb, ++kg) {
+          const int s = kg % STAGES;
+          if (!mbar_wait(empty0 + 8 * s, ((kg / STAGES) & 1) ^ 1, p.err)) {
+            *abort = 1;
+            break;
+          }
+          const uint32_t sa = tiles + s * C::STAGE_BYTES;
+          const uint32_t sb = sa + C::A_BYTES;
+          const uint32_t fb = full0 + 8 * s;
+          mbar_arrive_expect_tx(fb, C::STAGE_BYTES);
+          const int k0 = kb * BK;
+          if (A_MN == 0) {
+            tma_load_2d(sa, &tmA, k0, m0, fb);
+          } else {
+            tma_load_2d(sa, &tmA, m0, k0, fb);
+            tma_load_2d(sa + 8192, &tmA, m0 + 64, k0, fb);
+          }
+          if (B_MN == 0) {
+            tma_load_2d(sb, &tmB, k0, n0, fb);
+          } else {
 #pragma unroll
-        for (int j = 0; j < BN / 64; ++j) tma_load_2d(sb + 8192 * j, &tmB, n0 + 64 * j, k0, fb);
+            for (int j = 0; j < BN / 64; ++j) tma_load_2d(sb + 8192 * j, &tmB, n0 + 64 * j, k0, fb);
+          }
+        }
       }
     }
-  } else if (warp == 1 && lane == 0) {
-    // ---------------- MMA issuer
-    constexpr uint32_t idesc = idesc_bf16_f32(BM, BN, A_MN, B_MN);
-    for (int kb = 0; kb < num_k; ++kb) {
-      const int s = kb % STAGES;
-      const uint32_t round = kb / STAGES;
-      if (!mbar_wait(full0 + 8 * s, round & 1, p.err)) break;
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ---------------- MMA issuer
+      constexpr uint32_t idesc = idesc_bf16_f32(BM, BN, A_MN, B_MN);
+      uint32_t kg = 0;
+      int t = 0;  // tiles of this CTA so far
+      for (int tile = blockIdx.x; tile < total && !*abort; tile += gridDim.x, ++t) {
+        const int buf = t & 1;
+        if (!mbar_wait(acce0 + 8 * buf, ((t >> 1) & 1) ^ 1, p.err)) {
+          *abort = 1;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t acc = tmem + buf * BN;
+        bool good = true;
+        for (int kb = 0; kb < num_k; ++kb, ++kg) {
+          const int s = kg % STAGES;
+          if (!mbar_wait(full0 + 8 * s, (kg / STAGES) & 1, p.err)) {
+            good = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sa = tiles + s * C::STAGE_BYTES;
+          const uint32_t sb = sa + C::A_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk) {
+            const uint64_t ad = A_MN ? smem_desc_sw128(sa + 2048 * kk, 8192, 1024)
+                                     : smem_desc_sw128(sa + 32 * kk, 16, 1024);
+            const uint64_t bd = B_MN ? smem_desc_sw128(sb + 2048 * kk, 8192, 1024)
+                                     : smem_desc_sw128(sb + 32 * kk, 16, 1024);
+            tc_mma_f16(acc, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+          }
+          tc_commit(empty0 + 8 * s);
+        }
+        if (!good) {
+          *abort = 1;
+          break;
+        }
+        tc_commit(accf0 + 8 * buf);
+      }
+    }
+  } else {
+    // ---------------- epilogue warps 2..5
+    const int q = warp & 3;  // TMEM lane quarter of this warp
+    int t = 0;
+    for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++t) {
+      const int buf = t & 1;
+      const bool ready = !*abort && mbar_wait(accf0 + 8 * buf, (t >> 1) & 1, p.err);
+      if (!__all_sync(0xffffffffu, ready)) {  // warp-uniform exit
+        *abort = 1;
+        break;
+      }
       tc_fence_after();
-      const uint32_t sa = tiles + s * C::STAGE_BYTES;
-      const uint32_t sb = sa + C::A_BYTES;
-#pragma unroll
-      for (int kk = 0; kk < BK / 16; ++kk) {
-        const uint64_t ad = A_MN ? smem_desc_sw128(sa + 2048 * kk, 8192, 1024)
-                                 : smem_desc_sw128(sa + 32 * kk, 16, 1024);
-        const uint64_t bd = B_MN ? smem_desc_sw128(sb + 2048 * kk, 8192, 1024)
-                                 : smem_desc_sw128(sb + 32 * kk, 16, 1024);
-        tc_mma_f16(tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
-      }
-      tc_commit(empty0 + 8 * s);
+      int m0, n0;
+      tile_origin(p, tile, BN, m0, n0);
+      epilogue_row<BN>(p, tmem + buf * BN + ((uint32_t)(q * 32) << 16), m0 + q * 32 + lane, n0,
+                       num_k > 0);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(acce0 + 8 * buf);
     }
-    tc_commit(done);
   }
-  __syncwarp();
 
-  // ---------------- epilogue (all 128 threads; warp w reads TMEM lanes 32w..)
-  const bool ok = mbar_wait(done, 0, p.err);
-  tc_fence_after();
-  if (ok) {
-    const uint32_t tmem_row = tmem + ((uint32_t)(warp * 32) << 16);
-    epilogue_row<BN>(p, tmem_row, m0 + warp * 32 + lane, n0, num_k > 0);
-  } else if (warp == 0 && lane == 0) {
-    // a wait ran out: give copies still in flight into this CTA's shared
-    // memory time to land (bounded) before the CTA exits
+  __syncthreads();
+  if (*abort && threadIdx.x == 0) {
+    // give copies and MMAs still in flight time to land (bounded)
     const uint64_t t0 = global_ns();
     while (global_ns() - t0 < 10000000ull) {
     }
@@ -381,7 +443,7 @@ __global__ void __launch_bounds__(128, 1)
   __syncthreads();
   if (warp == 0) {
     tc_fence_after();
-    tmem_dealloc(tmem, BN);
+    tmem_dealloc(tmem, 2 * BN);
   }
 }
 
@@ -417,6 +479,23 @@ bool make_tmap(CUtensorMap* tm, const void* base, uint64_t inner, uint64_t outer
   return r == CUDA_SUCCESS;
 }
 
+// One persistent CTA per SM (the kernel's shared memory allows one), never
+// more CTAs than tiles.
+int persistent_grid(const EpiParams& ep) {
+  static int sms[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) dev = 0;
+  if (sms[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+      n = 148;
+    sms[dev] = n;
+  }
+  const long total = (long)ep.tiles_m * ep.tiles_n;
+  return (int)std::max(1L, std::min<long>(total, sms[dev]));
+}
+
 template <int BN, int STAGES, int A_MN, int B_MN>
 mgb_status launch_variant(const GemmArgs& g, const EpiParams& ep, cudaStream_t st) {
   using C = Cfg<BN, STAGES>;
@@ -433,7 +512,7 @@ mgb_status launch_variant(const GemmArgs& g, const EpiParams& ep, cudaStream_t s
     LaunchScope scope(g.prof_kind >= 0 ? g.prof_kind
                                : (A_MN ? PROF_GEMM_WGRAD : (B_MN ? PROF_GEMM_DGRAD : PROF_GEMM_FWD)),
                     st);
-    kern<<<ep.tiles_m * ep.tiles_n, 128, C::SMEM_BYTES, st>>>(ta, tb, ep);
+    kern<<<persistent_grid(ep), 192, C::SMEM_BYTES, st>>>(ta, tb, ep);
     return cudaGetLastError() == cudaSuccess ? MGB_OK : MGB_ERR_CUDA;
   }
   bool ok = A_MN ? make_tmap(&ta, g.A, g.M, g.K, g.lda, 64, 64)
@@ -441,11 +520,10 @@ mgb_status launch_variant(const GemmArgs& g, const EpiParams& ep, cudaStream_t s
   ok = ok && (B_MN ? make_tmap(&tb, g.B, g.N, g.K, g.ldb, 64, 64)
                    : make_tmap(&tb, g.B, g.K, g.N, g.ldb, 64, BN));
   if (!ok) return MGB_ERR_CUDA;
-  const int grid = ep.tiles_m * ep.tiles_n;
   LaunchScope scope(g.prof_kind >= 0 ? g.prof_kind
                                : (A_MN ? PROF_GEMM_WGRAD : (B_MN ? PROF_GEMM_DGRAD : PROF_GEMM_FWD)),
                     st);
-  kern<<<grid, 128, C::SMEM_BYTES, st>>>(ta, tb, ep);
+  kern<<<persistent_grid(ep), 192, C::SMEM_BYTES, st>>>(ta, tb, ep);
   return cudaGetLastError() == cudaSuccess ? MGB_OK : MGB_ERR_CUDA;
 }
 
@@ -453,6 +531,11 @@ template <int BN, int STAGES>
 mgb_status launch_bn(const GemmArgs& g, EpiParams ep, cudaStream_t st) {
   ep.tiles_m = (g.M + BM - 1) / BM;
   ep.tiles_n = (g.N + BN - 1) / BN;
+  // Row tiles per raster group: the group's A panel (group_m x 128 rows x K)
+  // should stay resident in L2 (about 48 MB) while the B columns stream by.
+  const long panel = (long)BM * (g.K > 0 ? g.K : 1) * 2;
+  ep.group_m = (int)std::max(4L, std::min(64L, (48L << 20) / panel));
+  ep.group_m = std::min(ep.group_m, ep.tiles_m);
   if (!g.a_mn && !g.b_mn) return launch_variant<BN, STAGES, 0, 0>(g, ep, st);
   if (!g.a_mn && g.b_mn) return launch_variant<BN, STAGES, 0, 1>(g, ep, st);
   if (g.a_mn && g.b_mn) return launch_variant<BN, STAGES, 1, 1>(g, ep, st);
