@@ -63,70 +63,6 @@ struct BwdParams {
   float sl2, scale;
 };
 
-__device__ __forceinline__ void fence_proxy_async() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
-// warp-uniform bounded wait: true only if every lane saw the phase complete
-__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, int* err) {
-  return __all_sync(0xffffffffu, mbar_wait(bar, parity, err));
-}
-// warp-uniform view of the abort flag
-__device__ __forceinline__ bool warp_aborted(volatile int* abort) {
-  return __any_sync(0xffffffffu, *abort != 0);
-}
-
-// 32 columns of this thread's TMEM lane
-__device__ __forceinline__ void ld_cols32(uint32_t taddr, float (&v)[32]) {
-  uint32_t r[32];
-  tmem_ld32(taddr, r);
-  tmem_ld_wait();
-#pragma unroll
-  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
-}
-
-// 32 floats -> bf16, the 16-byte chunks half*4 .. half*4+3 of row `row` of a
-// K-major 128-byte-swizzled [rows][64] tile (chunk c sits at c ^ (row & 7))
-__device__ __forceinline__ void store_half_row_sw128(uint8_t* row_ptr, int row, int half,
-                                                     const float (&v)[32]) {
-#pragma unroll
-  for (int c = 0; c < 4; ++c) {
-    uint4 w;
-    w.x = pack_bf16x2(v[8 * c], v[8 * c + 1]);
-    w.y = pack_bf16x2(v[8 * c + 2], v[8 * c + 3]);
-    w.z = pack_bf16x2(v[8 * c + 4], v[8 * c + 5]);
-    w.w = pack_bf16x2(v[8 * c + 6], v[8 * c + 7]);
-    *reinterpret_cast<uint4*>(row_ptr + (((half * 4 + c) ^ (row & 7)) << 4)) = w;
-  }
-}
-
-// NC columns of this thread's TMEM lane, scaled, to global bf16 (all lanes of
-// the warp must call; out == nullptr skips the store)
-template <int NC>
-__device__ __forceinline__ void store_tmem_row(uint32_t taddr, float scale, bf16* out) {
-#pragma unroll
-  for (int c = 0; c < NC / 32; ++c) {
-    uint32_t r[32];
-    tmem_ld32(taddr + c * 32, r);
-    tmem_ld_wait();
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      uint4 w;
-      w.x = pack_bf16x2(__uint_as_float(r[8 * q]) * scale, __uint_as_float(r[8 * q + 1]) * scale);
-      w.y = pack_bf16x2(__uint_as_float(r[8 * q + 2]) * scale, __uint_as_float(r[8 * q + 3]) * scale);
-      w.z = pack_bf16x2(__uint_as_float(r[8 * q + 4]) * scale, __uint_as_float(r[8 * q + 5]) * scale);
-      w.w = pack_bf16x2(__uint_as_float(r[8 * q + 6]) * scale, __uint_as_float(r[8 * q + 7]) * scale);
-      if (out) *reinterpret_cast<uint4*>(out + c * 32 + 8 * q) = w;
-    }
-  }
-}
-
-__device__ __forceinline__ void spin_10ms() {
-  const uint64_t t0 = global_ns();
-  while (global_ns() - t0 < 10000000ull) {
-  }
-}
-
 // ------------------------------------------------------------ kernel A: dK, dV
 template <int D>
 struct DkvCfg {

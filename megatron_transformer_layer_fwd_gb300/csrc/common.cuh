@@ -76,15 +76,30 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
+// As mbar_try_wait, but a thread whose phase is not complete is suspended
+// until it completes or for at most about `hint_ns` (instead of polling).
+__device__ __forceinline__ bool mbar_try_wait_suspend(uint32_t bar, uint32_t parity,
+                                                      uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
 // Wait for the phase with the given parity to complete, for at most
 // limit_ns. Returns false (and records kErrTimeout in *err) if it ran out.
+// The waiting thread sleeps in the barrier unit rather than spinning, so it
+// takes no issue slots from the warps doing work.
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, int* err,
                                           unsigned long long limit_ns = kWaitLimitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_ns();
-  for (uint32_t it = 1;; ++it) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((it & 63u) == 0 && global_ns() - t0 > limit_ns) {
+  for (;;) {
+    if (mbar_try_wait_suspend(bar, parity, 50000u)) return true;
+    if (global_ns() - t0 > limit_ns) {
       record_error(err, kErrTimeout);
       return false;
     }
@@ -133,6 +148,17 @@ __device__ __forceinline__ void tc_mma_f16(uint32_t d_tmem, uint64_t a_desc, uin
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
+// As tc_mma_f16, with the A operand read from tensor memory at a_tmem (row m
+// of A in TMEM lane m; two bf16 K-elements per 32-bit column, lower index in
+// the low half).
+__device__ __forceinline__ void tc_mma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                              uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
 // Arrive once on `bar` when all previously issued tcgen05.mma of this thread complete.
 __device__ __forceinline__ void tc_commit(uint32_t bar) {
   asm volatile(
@@ -153,6 +179,97 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
 }
 __device__ __forceinline__ void tmem_ld_wait() {
   asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// 32 lanes x 32 consecutive 32-bit columns from registers: thread i writes lane (base + i).
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,"
+      "%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
+      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
+      "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]),
+      "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]),
+      "r"(r[29]), "r"(r[30]), "r"(r[31])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_st_wait() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+// 32 columns of this thread's TMEM lane as floats (whole warp)
+__device__ __forceinline__ void ld_cols32(uint32_t taddr, float (&v)[32]) {
+  uint32_t r[32];
+  tmem_ld32(taddr, r);
+  tmem_ld_wait();
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// Generic-proxy shared-memory writes made visible to the async proxy (TMA, tcgen05).
+__device__ __forceinline__ void fence_proxy_async() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// ---------------------------------------------------------------- warp roles
+// One lane of a converged warp is elected (the same lane on every call).
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred;
+  asm volatile(
+      "{\n .reg .b32 r;\n .reg .pred p;\n elect.sync r|p, 0xffffffff;\n"
+      " selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(pred));
+  return pred != 0;
+}
+// Warp-uniform bounded wait: true only if every lane saw the phase complete.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, int* err) {
+  return __all_sync(0xffffffffu, mbar_wait(bar, parity, err));
+}
+// Warp-uniform view of a shared abort flag.
+__device__ __forceinline__ bool warp_aborted(volatile int* abort) {
+  return __any_sync(0xffffffffu, *abort != 0);
+}
+// Lets tensor-core work and copies still in flight land before a CTA that gave
+// up on a wait releases its TMEM and exits.
+__device__ __forceinline__ void spin_10ms() {
+  const uint64_t t0 = global_ns();
+  while (global_ns() - t0 < 10000000ull) {
+  }
+}
+
+// 32 floats -> bf16 into the 16-byte chunks half*4 .. half*4+3 of row `row` of
+// a K-major 128-byte-swizzled [rows][64] tile (chunk c sits at c ^ (row & 7)).
+__device__ __forceinline__ void store_half_row_sw128(uint8_t* row_ptr, int row, int half,
+                                                     const float (&v)[32]) {
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    uint4 w;
+    w.x = pack_bf16x2(v[8 * c], v[8 * c + 1]);
+    w.y = pack_bf16x2(v[8 * c + 2], v[8 * c + 3]);
+    w.z = pack_bf16x2(v[8 * c + 4], v[8 * c + 5]);
+    w.w = pack_bf16x2(v[8 * c + 6], v[8 * c + 7]);
+    *reinterpret_cast<uint4*>(row_ptr + (((half * 4 + c) ^ (row & 7)) << 4)) = w;
+  }
+}
+
+// NC columns of this thread's TMEM lane, scaled, to global bf16 (all lanes of
+// the warp must call; out == nullptr skips the store).
+template <int NC>
+__device__ __forceinline__ void store_tmem_row(uint32_t taddr, float scale, bf16* out) {
+#pragma unroll
+  for (int c = 0; c < NC / 32; ++c) {
+    uint32_t r[32];
+    tmem_ld32(taddr + c * 32, r);
+    tmem_ld_wait();
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      uint4 w;
+      w.x = pack_bf16x2(__uint_as_float(r[8 * q]) * scale, __uint_as_float(r[8 * q + 1]) * scale);
+      w.y = pack_bf16x2(__uint_as_float(r[8 * q + 2]) * scale, __uint_as_float(r[8 * q + 3]) * scale);
+      w.z = pack_bf16x2(__uint_as_float(r[8 * q + 4]) * scale, __uint_as_float(r[8 * q + 5]) * scale);
+      w.w = pack_bf16x2(__uint_as_float(r[8 * q + 6]) * scale, __uint_as_float(r[8 * q + 7]) * scale);
+      if (out) *reinterpret_cast<uint4*>(out + c * 32 + 8 * q) = w;
+    }
+  }
 }
 
 // Shared-memory matrix descriptor (tcgen05 format): start address, leading and
@@ -180,6 +297,34 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int m, int n, int a_mn, in
 }
 
 // ---------------------------------------------------------------- math
+// max(a, b, c) in one instruction (sm_100 and later).
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+// 2^x on the special-function unit (flushes subnormal results to zero).
+__device__ __forceinline__ float ex2_ftz(float x) {
+  float r;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(x));
+  return r;
+}
+// Two float32 lanes at once: (a0, a1) * (b0, b1) + (c0, c1), round to nearest.
+__device__ __forceinline__ void fma2(float& r0, float& r1, float a0, float a1, float b0, float b1,
+                                     float c0, float c1) {
+  asm("{\n .reg .b64 a, b, c, d;\n mov.b64 a, {%2, %3};\n mov.b64 b, {%4, %5};\n"
+      " mov.b64 c, {%6, %7};\n fma.rn.f32x2 d, a, b, c;\n mov.b64 {%0, %1}, d;\n}\n"
+      : "=f"(r0), "=f"(r1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1), "f"(c0), "f"(c1));
+}
+// (a0, a1) + (b0, b1), round to nearest.
+__device__ __forceinline__ void add2(float& r0, float& r1, float a0, float a1, float b0, float b1) {
+  asm("{\n .reg .b64 a, b, d;\n mov.b64 a, {%2, %3};\n mov.b64 b, {%4, %5};\n"
+      " add.rn.f32x2 d, a, b;\n mov.b64 {%0, %1}, d;\n}\n"
+      : "=f"(r0), "=f"(r1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
+
 __device__ __forceinline__ float gelu_erf(float u) {
   return 0.5f * u * (1.0f + erff(u * 0.70710678118654752f));
 }

@@ -482,18 +482,8 @@ bool make_tmap(CUtensorMap* tm, const void* base, uint64_t inner, uint64_t outer
 // One persistent CTA per SM (the kernel's shared memory allows one), never
 // more CTAs than tiles.
 int persistent_grid(const EpiParams& ep) {
-  static int sms[64] = {};
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev < 0 || dev >= 64) dev = 0;
-  if (sms[dev] == 0) {
-    int n = 0;
-    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
-      n = 148;
-    sms[dev] = n;
-  }
   const long total = (long)ep.tiles_m * ep.tiles_n;
-  return (int)std::max(1L, std::min<long>(total, sms[dev]));
+  return (int)std::max(1L, std::min<long>(total, device_sm_count()));
 }
 
 template <int BN, int STAGES, int A_MN, int B_MN>
@@ -571,6 +561,20 @@ mgb_status gemm_tc_launch(const GemmArgs& g, cudaStream_t st) {
   if (g.epi == EPI_BIAS_SWIGLU || (tiles256 >= 148 && g.N > 128))
     return launch_bn<256, 4>(g, ep, st);
   return launch_bn<128, 6>(g, ep, st);
+}
+
+int device_sm_count() {
+  static int sms[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) dev = 0;
+  if (sms[dev] == 0) {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+      n = 148;
+    sms[dev] = n;
+  }
+  return sms[dev];
 }
 
 }  // namespace mgb

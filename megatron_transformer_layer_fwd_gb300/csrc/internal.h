@@ -87,6 +87,9 @@ mgb_status ce_combine_launch(int T, int n_chunks, const float* m, const float* s
 mgb_status ce_grad_launch(int T, int C, int v0, void* logits, int64_t ldl, const int32_t* targets,
                           const float* lse, float scale, cudaStream_t st);
 
+// Streaming multiprocessors of the current device (cached per device).
+int device_sm_count();
+
 // Device address of the current device's error word (nullptr on failure).
 int* device_error_word();
 

@@ -23,6 +23,9 @@ CASES = [
     (1, 64, 1, 1, 64, False), (2, 100, 4, 2, 64, True), (1, 200, 4, 1, 128, False),
     (2, 130, 2, 2, 128, True), (1, 384, 8, 2, 128, True), (2, 257, 4, 4, 64, False),
     (1, 1000, 4, 1, 128, True),
+    # more (batch, head, query tile) items than SMs: every CTA of the persistent
+    # forward runs several items through its double-buffered Q and O
+    (4, 640, 16, 4, 128, True), (3, 520, 16, 2, 64, False),
 ]
 
 
@@ -31,11 +34,25 @@ CASES = [
 def test_attention_fwd_bwd(mgb_lib, dtype, B, S, nq, nkv, d, causal):
     if dtype == "f32" and S > 400:
         pytest.skip("float32 path is for the small float32 layer")
+    _check(dtype, B, S, nq, nkv, d, causal, 1.0, 0.0)
+
+
+@pytest.mark.parametrize("B,S,nq,nkv,d,causal", [(1, 700, 2, 1, 128, True), (2, 384, 2, 2, 64, False)])
+def test_attention_sharp_growing_scores(mgb_lib, B, S, nq, nkv, d, causal):
+    """Scores with a spread of ~13 (log2 units) and keys whose norm grows along
+    the sequence: a row's running maximum keeps rising tile after tile, so the
+    forward's lazily moved softmax reference and the O rescale in TMEM run many
+    times per row."""
+    _check("bf16", B, S, nq, nkv, d, causal, 3.0, 4.0)
+
+
+def _check(dtype, B, S, nq, nkv, d, causal, amp, ramp):
     rnd = round_to_bf16 if dtype == "bf16" else (lambda a: a.astype(np.float32).astype(np.float64))
     td = torch.bfloat16 if dtype == "bf16" else torch.float32
     mdt = mgb.MGB_BF16 if dtype == "bf16" else mgb.MGB_F32
-    q = rnd(RNG.standard_normal((B, nq, S, d)))
-    k = rnd(RNG.standard_normal((B, nkv, S, d)))
+    grow = 1.0 + ramp * np.arange(S)[None, None, :, None] / S
+    q = rnd(amp * RNG.standard_normal((B, nq, S, d)))
+    k = rnd(amp * grow * RNG.standard_normal((B, nkv, S, d)))
     v = rnd(RNG.standard_normal((B, nkv, S, d)))
     do = rnd(RNG.standard_normal((B, nq, S, d)))
     pack = lambda t: t.transpose(0, 2, 1, 3).reshape(B * S, -1)
