@@ -231,11 +231,19 @@ mgb_status mgb_attention_fwd(int32_t batch, int32_t seq, int32_t n_q_heads, int3
                              const void* q, const void* k, const void* v, int64_t ld_q,
                              int64_t ld_kv, void* o, float* lse, void* stream);
 
+/* Bytes of the workspace mgb_attention_bwd needs: two float32 planes
+ * [batch * n_q_heads][seq rounded up to a multiple of 128] (LSE * log2(e) and
+ * delta = rowsum(dO * O), per query; the padding holds +inf and 0). No
+ * counterpart on the pages: it sizes the buffer below. 0 for negative sizes. */
+size_t mgb_attention_bwd_ws_bytes(int32_t batch, int32_t seq, int32_t n_q_heads);
+
 /* Attention core backward [P1 section 2, end-to-end backward]: given the
  * forward's q, k, v, o, lse and dO = dL/dO (same layouts; do [B*S, nq*d] with
  * row stride ld_do), writes dq (row stride ld_dq) and dk, dv (row stride
  * ld_dkv; the sum over the query heads of each GQA group). P is recomputed
- * from lse. `ws` holds delta = rowsum(dO * O): at least 4*B*nq*S bytes. */
+ * from lse. `ws` (16-byte aligned, caller-owned, overwritten) holds the
+ * per-query LSE and delta: at least mgb_attention_bwd_ws_bytes(batch, seq,
+ * n_q_heads) bytes, else MGB_ERR_WORKSPACE_TOO_SMALL before any launch. */
 mgb_status mgb_attention_bwd(int32_t batch, int32_t seq, int32_t n_q_heads, int32_t n_kv_heads,
                              int32_t head_dim, int32_t causal, int32_t dtype,
                              const void* q, const void* k, const void* v, int64_t ld_q,

@@ -177,7 +177,7 @@ void make_plan(const mgb_block_desc* d, Plan* p) {
   p->w_dO = take(es * T * p->Dq);
   p->w_dqkv = take(es * T * p->Wqkv);
   p->w_dxn = take(es * T * p->H);
-  p->w_delta = take(4 * (size_t)p->B * p->nq * p->S);
+  p->w_delta = take(attn_bwd_ws_bytes(p->B, p->S, p->nq));
   p->w_cparts = take(4 * (size_t)p->cparts * maxN);
   p->w_lparts = take(4 * 2 * (size_t)p->lparts * p->H);
   p->bwd = o;
@@ -654,6 +654,11 @@ mgb_status mgb_attention_fwd(int32_t batch, int32_t seq, int32_t n_q_heads, int3
   return attention_fwd_launch(a, as_stream(stream));
 }
 
+size_t mgb_attention_bwd_ws_bytes(int32_t batch, int32_t seq, int32_t n_q_heads) {
+  if (batch < 0 || seq < 0 || n_q_heads < 0) return 0;
+  return attn_bwd_ws_bytes(batch, seq, n_q_heads);
+}
+
 mgb_status mgb_attention_bwd(int32_t batch, int32_t seq, int32_t n_q_heads, int32_t n_kv_heads,
                              int32_t head_dim, int32_t causal, int32_t dtype, const void* q,
                              const void* k, const void* v, int64_t ld_q, int64_t ld_kv,
@@ -675,7 +680,7 @@ mgb_status mgb_attention_bwd(int32_t batch, int32_t seq, int32_t n_q_heads, int3
   for (const void* pp : ps)
     if (!aligned16(pp)) return MGB_ERR_MISALIGNED;
   if (ld_q % vm || ld_kv % vm || ld_do % vm || ld_dq % vm || ld_dkv % vm) return MGB_ERR_MISALIGNED;
-  if (ws_bytes < 4 * (size_t)batch * n_q_heads * seq) return MGB_ERR_WORKSPACE_TOO_SMALL;
+  if (ws_bytes < attn_bwd_ws_bytes(batch, seq, n_q_heads)) return MGB_ERR_WORKSPACE_TOO_SMALL;
   MGB_TRY(check_arch());
   AttnArgs a{};
   a.B = batch; a.S = seq; a.nq = n_q_heads; a.nkv = n_kv_heads; a.d = head_dim;

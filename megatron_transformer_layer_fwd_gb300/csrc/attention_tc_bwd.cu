@@ -7,13 +7,18 @@
 //   dV_g = sum_h P^T dO_h,   dK_g = sum_h dS^T Q_h / sqrt(d),   dQ_h = dS K_g / sqrt(d),
 // summing over the query heads h of the GQA group g.
 //
+// The per-query inputs come from a workspace the pre-pass fills: two planes
+// [B * nq][s_pad] of float32, LSE * log2(e) (+inf past the sequence end) and
+// delta (0 there), rows padded to a multiple of 128 so that any query tile is
+// one aligned, in-bounds 16-byte-multiple block.
+//
 // Kernel A (dK, dV): one CTA = 128 keys of one KV head (key row = TMEM lane).
 // It loops over every query head of the group and every 64-query tile that
-// can see its keys (Q/dO tiles in a 3-stage TMA ring):
-//   S^T  = K Q^T     M=128 N=64 K=d     TMEM buffer i & 1, columns [0, 64)
-//   dP^T = V dO^T    M=128 N=64 K=d     TMEM buffer i & 1, columns [64, 128)
+// can see its keys (Q, dO and that tile's LSE/delta in a 4-stage TMA ring):
+//   S^T  = K Q^T     M=128 N=64 K=d     TMEM columns [0, 64)
+//   dP^T = V dO^T    M=128 N=64 K=d     TMEM columns [64, 128)
 //   registers: P^T = exp2(S^T*log2e/sqrt(d) - LSE*log2e), dS^T = P^T (dP^T - delta)
-//   (bf16, K-major 128-byte-swizzled smem tiles)
+//   as bf16 pairs into TMEM buffer i & 1 (columns [128, 256)), the A operands of
 //   dV  += P^T dO    M=128 N=d K=64     TMEM [256, 256+d)
 //   dK  += dS^T Q    M=128 N=d K=64     TMEM [256+d, 256+2d)
 // The Q and dO tiles are read as K-major operands by the first two products and
@@ -21,20 +26,29 @@
 // dK and dV stay in TMEM across the whole loop, so the GQA sum costs nothing.
 //
 // Kernel B (dQ): one CTA = 128 queries of one head; per 64-key tile (K/V in a
-// 3-stage ring): S = Q K^T, dP = dO V^T (TMEM buffer i & 1), dS in registers
-// -> smem, dQ += dS K (TMEM [256, 256+d); the K tile read as MN-major).
+// 5-stage ring): S = Q K^T, dP = dO V^T (TMEM [0, 128)), dS in registers -> TMEM
+// buffer j & 1 (bf16 pairs, [128, 192)), dQ += dS K (TMEM [256, 256+d), A from
+// TMEM, the K tile read as MN-major).
 //
-// Warp-specialised, 10 warps:
-//   warps 0-7  compute: warps w and w+4 share TMEM lane quarter w%4 (32 rows)
-//              and take one 32-column half of each 64-column tile
-//   warp 8     producer: TMA ring refills (and, in kernel A, the per-query LSE
-//              and delta of each tile into a double-buffered smem slot)
-//   warp 9     MMA issuer (one lane)
-// No CTA barrier inside the loop: the roles hand tiles to each other through
-// mbarriers only. The score products of a tile are double-buffered in TMEM and
-// issued two tiles ahead, so the compute warps find them ready. Every wait is
-// bounded; a wait that runs out sets a shared abort flag and every role leaves
-// its loop (warp-uniformly) before the single closing barrier.
+// Warp-specialised, 18 warps:
+//   warps 0-15 compute, in two groups of 8 that take alternate tiles (group
+//              g the tiles i with i & 1 == g): one group's exponentials and
+//              stores overlap the other's. In a group, warps w and w+4 share
+//              TMEM lane quarter w%4 (32 rows) and take one 32-column half of
+//              each 64-column tile
+//   warp 16    producer (one lane): TMA ring refills
+//   warp 17    MMA issuer: the whole warp runs the loop (warp-uniform values)
+//              and one elected lane issues each tcgen05 instruction from
+//              shared-memory descriptors built once (base + offset / 16)
+// The score products have one TMEM buffer: a group releases it as soon as it
+// has loaded its tile's scores into registers, and the next tile's products
+// are issued right then, so they run while the group computes. Products whose
+// A operand is a tile of the compute warps read it from TMEM, which keeps
+// those tiles out of shared memory (whose bandwidth the other operands and the
+// TMA copies need) and leaves room for deep copy rings. No CTA barrier inside
+// the loop: the roles hand tiles to each other through mbarriers only. Every
+// wait is bounded; a wait that runs out sets a shared abort flag and every role
+// leaves its loop (warp-uniformly) before the single closing barrier.
 #include "common.cuh"
 #include "internal.h"
 
@@ -45,18 +59,19 @@ CUresult tmap_encode_bf16_2d(CUtensorMap* tm, const void* base, uint64_t inner, 
 
 namespace {
 
-constexpr float LOG2E = 1.4426950408889634f;
 constexpr int TR = 128;        // rows (keys in A, queries in B) per CTA
 constexpr int TC = 64;         // columns per inner tile (queries in A, keys in B)
-constexpr int NS = 3;          // stages of the streamed operand ring
+constexpr int NSA = 4;         // Q/dO ring stages (kernel A)
+constexpr int NSB = 5;         // K/V ring stages (kernel B)
 constexpr int COL_ACC = 256;   // first TMEM column of the accumulators
-constexpr int NCOMPUTE = 256;  // compute threads (warps 0-7)
-constexpr int NTHREADS = 320;  // + producer warp + MMA warp
+constexpr int NGROUP = 256;    // compute threads of one group (8 warps)
+constexpr int NTHREADS = 576;  // 2 compute groups + producer warp + MMA warp
+constexpr int W_PROD = 16, W_MMA = 17;
 
 struct BwdParams {
-  int B, S, nq, nkv, causal;
-  const float* lse;    // [B, nq, S]
-  const float* delta;  // [B, nq, S]
+  int B, S, nq, nkv, causal, s_pad;
+  const float* lse2;   // [B * nq][s_pad]: LSE * log2(e)
+  const float* delta;  // [B * nq][s_pad]
   bf16 *d0, *d1;       // A: dk, dv; B: dq
   int64_t ld_out;
   int* err;
@@ -69,17 +84,17 @@ struct DkvCfg {
   static constexpr int KB = D / 64;
   static constexpr int KV_BYTES = TR * D * 2;   // K or V rows of this CTA
   static constexpr int QT_BYTES = TC * D * 2;   // one Q or dO tile
-  static constexpr int PT_BYTES = TR * TC * 2;  // P^T or dS^T tile
+  static constexpr int LD_BYTES = 2 * TC * 4;   // a tile's LSE*log2e and delta
   static constexpr int OFF_K = 0;
   static constexpr int OFF_V = OFF_K + KV_BYTES;
-  static constexpr int OFF_Q = OFF_V + KV_BYTES;         // NS stages
-  static constexpr int OFF_DO = OFF_Q + NS * QT_BYTES;   // NS stages
-  static constexpr int OFF_P = OFF_DO + NS * QT_BYTES;
-  static constexpr int OFF_DS = OFF_P + PT_BYTES;
-  static constexpr int OFF_LD = OFF_DS + PT_BYTES;       // [2][lse2 64 | delta 64] f32
-  static constexpr int OFF_BAR = OFF_LD + 2 * 2 * TC * 4;
+  static constexpr int OFF_Q = OFF_V + KV_BYTES;          // NSA stages
+  static constexpr int OFF_DO = OFF_Q + NSA * QT_BYTES;   // NSA stages
+  static constexpr int OFF_LD = OFF_DO + NSA * QT_BYTES;  // NSA stages
+  static constexpr int OFF_BAR = OFF_LD + NSA * LD_BYTES;
   static constexpr int SMEM = OFF_BAR + 256 + 1024;
-  static constexpr int COL_DV = COL_ACC, COL_DK = COL_ACC + D;
+  // TMEM: scores [0, 128), P^T/dS^T buffers [128, 256) (64 columns each: P^T
+  // then dS^T, 32 columns = 64 bf16 queries apiece), dV, dK
+  static constexpr int COL_PDS = 128, COL_DV = COL_ACC, COL_DK = COL_ACC + D;
 };
 
 template <int D>
@@ -94,20 +109,19 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const uint32_t sb = smem_u32(smem);
   const uint32_t sK = sb + C::OFF_K, sV = sb + C::OFF_V, sQ = sb + C::OFF_Q, sO = sb + C::OFF_DO,
-                 sP = sb + C::OFF_P, sS = sb + C::OFF_DS;
-  float* sLD = reinterpret_cast<float*>(smem + C::OFF_LD);
+                 sLDa = sb + C::OFF_LD;
+  const float* sLD = reinterpret_cast<const float*>(smem + C::OFF_LD);
   const uint32_t bar = sb + C::OFF_BAR;
-  const uint32_t kv_full = bar;                // K, V loaded            (tx)
-  const uint32_t qd_full0 = bar + 8;           // [3] Q/dO stage loaded (tx)
-  const uint32_t qd_empty0 = bar + 32;         // [3] stage read by dV/dK (commit)
-  const uint32_t sp_full0 = bar + 56;          // [2] S^T/dP^T ready   (commit)
-  const uint32_t pds_full = bar + 72;          // P^T/dS^T written      (256 arrivals)
-  const uint32_t pds_empty = bar + 80;         // dV/dK read them       (commit)
-  const uint32_t ld_full0 = bar + 88;          // [2] LSE/delta slot written (32)
-  const uint32_t ld_empty0 = bar + 104;        // [2] slot read          (256)
-  const uint32_t acc_done = bar + 120;         // all products done     (commit)
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_BAR + 128);
-  volatile int* abort = reinterpret_cast<volatile int*>(smem + C::OFF_BAR + 132);
+  const uint32_t kv_full = bar;          // K, V loaded                       (tx)
+  const uint32_t qd_full0 = bar + 8;     // [4] Q/dO/LSE/delta stage loaded   (tx)
+  const uint32_t qd_empty0 = bar + 40;   // [4] stage read by dV/dK           (commit)
+  const uint32_t sp_full0 = bar + 72;    // [2] S^T/dP^T of tile i ready      (commit)
+  const uint32_t sp_free0 = bar + 88;    // [2] group read them out of TMEM   (256 arrivals)
+  const uint32_t pds_full0 = bar + 104;  // [2] P^T/dS^T buffer written       (256 arrivals)
+  const uint32_t pds_empty0 = bar + 120; // [2] dV/dK read the buffer         (commit)
+  const uint32_t acc_done = bar + 136;   // all products done                 (commit)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_BAR + 160);
+  volatile int* abort = reinterpret_cast<volatile int*>(smem + C::OFF_BAR + 164);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   // grid: x = (KV head, batch) pairs, y = key tile (the first key tiles see the
@@ -120,21 +134,23 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   const int per_head = nqt - qt_start;
   const int n_it = per_head * rep;  // >= 1: the query tile at kv0 sees key kv0
   const int grow0 = b * p.S;
-  auto it_head = [&](int it) { return g * rep + it / per_head; };
-  auto it_q0 = [&](int it) { return (qt_start + it % per_head) * TC; };
 
   if (tid == 0) {
     tma_prefetch_desc(&tmQ);
     tma_prefetch_desc(&tmK);
     tma_prefetch_desc(&tmV);
     tma_prefetch_desc(&tmO);
-    for (int i = 0; i < 9; ++i) mbar_init(bar + 8 * i, 1);  // kv, qd_full, qd_empty, sp_full
-    mbar_init(pds_full, NCOMPUTE);
-    mbar_init(pds_empty, 1);
-    mbar_init(ld_full0, 32);
-    mbar_init(ld_full0 + 8, 32);
-    mbar_init(ld_empty0, NCOMPUTE);
-    mbar_init(ld_empty0 + 8, NCOMPUTE);
+    mbar_init(kv_full, 1);
+    for (int i = 0; i < NSA; ++i) {
+      mbar_init(qd_full0 + 8 * i, 1);
+      mbar_init(qd_empty0 + 8 * i, 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(sp_full0 + 8 * i, 1);
+      mbar_init(sp_free0 + 8 * i, NGROUP);
+      mbar_init(pds_full0 + 8 * i, NGROUP);
+      mbar_init(pds_empty0 + 8 * i, 1);
+    }
     mbar_init(acc_done, 1);
     fence_mbar_init();
     *abort = 0;
@@ -145,7 +161,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 8) {
+  if (warp == W_PROD) {
     // ---------------- producer
     if (lane == 0) {
       mbar_arrive_expect_tx(kv_full, 2 * C::KV_BYTES);
@@ -154,157 +170,175 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         tma_load_2d(sK + kb * (TR * 128), &tmK, g * D + kb * 64, grow0 + kv0, kv_full);
         tma_load_2d(sV + kb * (TR * 128), &tmV, g * D + kb * 64, grow0 + kv0, kv_full);
       }
-    }
-    for (int it = 0; it < n_it; ++it) {
-      if (warp_aborted(abort)) break;
-      // Q/dO of tile it into stage it % 3 once dV/dK of tile it - 3 read it
-      if (lane == 0) {
-        const int s = it % NS;
-        if (it >= NS && !mbar_wait(qd_empty0 + 8 * s, ((it - NS) / NS) & 1, p.err)) *abort = 1;
-        if (!*abort) {
-          const uint32_t fb = qd_full0 + 8 * s;
-          const int h = it_head(it), q0 = it_q0(it);
-          mbar_arrive_expect_tx(fb, 2 * C::QT_BYTES);
-#pragma unroll
-          for (int kb = 0; kb < C::KB; ++kb) {
-            tma_load_2d(sQ + s * C::QT_BYTES + kb * 8192, &tmQ, h * D + kb * 64, grow0 + q0, fb);
-            tma_load_2d(sO + s * C::QT_BYTES + kb * 8192, &tmO, h * D + kb * 64, grow0 + q0, fb);
-          }
-        }
-      }
-      __syncwarp();
-      // per-query LSE (log2 units) and delta of tile it into slot it & 1
-      if (it >= 2 && !warp_wait(ld_empty0 + 8 * (it & 1), ((it - 2) >> 1) & 1, p.err)) {
-        *abort = 1;
-        break;
-      }
-      const int h = it_head(it);
-      float* dst = sLD + (it & 1) * 2 * TC;
-#pragma unroll
-      for (int u = 0; u < 2; ++u) {
-        const int c = lane + 32 * u, q = it_q0(it) + c;
-        const int64_t off = ((int64_t)b * p.nq + h) * p.S + q;
-        dst[c] = q < p.S ? p.lse[off] * LOG2E : INFINITY;
-        dst[TC + c] = q < p.S ? p.delta[off] : 0.0f;
-      }
-      mbar_arrive(ld_full0 + 8 * (it & 1));
-    }
-  } else if (warp == 9) {
-    // ---------------- MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t idesc_sp = idesc_bf16_f32(TR, TC, 0, 0);
-      constexpr uint32_t idesc_acc = idesc_bf16_f32(TR, D, 0, 1);
-      auto issue_sp = [&](int it) -> bool {
-        const int s = it % NS;
-        if (!mbar_wait(qd_full0 + 8 * s, (it / NS) & 1, p.err)) return false;
-        tc_fence_after();
-        const uint32_t tb = tmem + (it & 1) * 128;
-#pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * (TR * 128) + (kk & 3) * 32;
-          const uint32_t offq = (kk >> 2) * 8192 + (kk & 3) * 32;
-          tc_mma_f16(tb, smem_desc_sw128(sK + off, 16, 1024),
-                     smem_desc_sw128(sQ + s * C::QT_BYTES + offq, 16, 1024), idesc_sp, kk > 0);
-          tc_mma_f16(tb + 64, smem_desc_sw128(sV + off, 16, 1024),
-                     smem_desc_sw128(sO + s * C::QT_BYTES + offq, 16, 1024), idesc_sp, kk > 0);
-        }
-        tc_commit(sp_full0 + 8 * (it & 1));
-        return true;
-      };
-      bool good = mbar_wait(kv_full, 0, p.err) && issue_sp(0) && (n_it < 2 || issue_sp(1));
-      for (int it = 0; it < n_it && good && !*abort; ++it) {
-        // P^T / dS^T of tile it written by every compute thread (which also
-        // means every thread has read tile it's scores out of TMEM)
-        if (!mbar_wait(pds_full, it & 1, p.err)) {
-          good = false;
+      int h = g * rep, qt = qt_start;  // head and query tile of iteration it
+      for (int it = 0; it < n_it && !*abort; ++it) {
+        // Q/dO of tile it into stage it % NSA once dV/dK of the tile before read it
+        const int s = it % NSA;
+        if (it >= NSA && !mbar_wait(qd_empty0 + 8 * s, ((it - NSA) / NSA) & 1, p.err)) {
+          *abort = 1;
           break;
         }
-        tc_fence_after();
-        const int s = it % NS;
+        const uint32_t fb = qd_full0 + 8 * s;
+        const int q0 = qt * TC;
+        mbar_arrive_expect_tx(fb, 2 * C::QT_BYTES + C::LD_BYTES);
 #pragma unroll
-        for (int kk = 0; kk < TC / 16; ++kk) {
-          const uint32_t b_off = s * C::QT_BYTES + kk * 2048;
-          tc_mma_f16(tmem + C::COL_DV, smem_desc_sw128(sP + kk * 32, 16, 1024),
-                     smem_desc_sw128(sO + b_off, 8192, 1024), idesc_acc, (it > 0 || kk > 0));
-          tc_mma_f16(tmem + C::COL_DK, smem_desc_sw128(sS + kk * 32, 16, 1024),
-                     smem_desc_sw128(sQ + b_off, 8192, 1024), idesc_acc, (it > 0 || kk > 0));
+        for (int kb = 0; kb < C::KB; ++kb) {
+          tma_load_2d(sQ + s * C::QT_BYTES + kb * 8192, &tmQ, h * D + kb * 64, grow0 + q0, fb);
+          tma_load_2d(sO + s * C::QT_BYTES + kb * 8192, &tmO, h * D + kb * 64, grow0 + q0, fb);
         }
-        tc_commit(qd_empty0 + 8 * s);
-        tc_commit(pds_empty);
-        if (it + 2 < n_it && !issue_sp(it + 2)) good = false;
+        const int64_t lrow = ((int64_t)b * p.nq + h) * p.s_pad + q0;
+        bulk_load(sLDa + s * C::LD_BYTES, p.lse2 + lrow, TC * 4, fb);
+        bulk_load(sLDa + s * C::LD_BYTES + TC * 4, p.delta + lrow, TC * 4, fb);
+        if (++qt == nqt) {
+          qt = qt_start;
+          ++h;
+        }
       }
-      if (good && !*abort) tc_commit(acc_done);
-      else *abort = 1;
     }
-  } else {
-    // ---------------- compute warps 0-7
-    const int rrow = (warp & 3) * 32 + lane, half = warp >> 2;
-    const int kr = kv0 + rrow;  // this thread's key position
-    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
-    const uint32_t col0 = half * 32;  // this warp's columns of the 64-wide tiles
-    bool good = true;
-    for (int it = 0; it < n_it; ++it) {
-      if (warp_aborted(abort) || !warp_wait(sp_full0 + 8 * (it & 1), (it >> 1) & 1, p.err) ||
-          !warp_wait(ld_full0 + 8 * (it & 1), (it >> 1) & 1, p.err)) {
+  } else if (warp == W_MMA) {
+    // ---------------- MMA issuer
+    constexpr uint32_t idesc_sp = idesc_bf16_f32(TR, TC, 0, 0);
+    constexpr uint32_t idesc_acc = idesc_bf16_f32(TR, D, 0, 1);
+    const uint64_t dk = smem_desc_sw128(sK, 16, 1024), dv = smem_desc_sw128(sV, 16, 1024);
+    const uint64_t dqk = smem_desc_sw128(sQ, 16, 1024), dok = smem_desc_sw128(sO, 16, 1024);
+    const uint64_t dqm = smem_desc_sw128(sQ, 8192, 1024), dom = smem_desc_sw128(sO, 8192, 1024);
+    // S^T / dP^T of tile it into the score columns
+    auto issue_sp = [&](int it) -> bool {
+      const int s = it % NSA;
+      if (!warp_wait(qd_full0 + 8 * s, (it / NSA) & 1, p.err)) return false;
+      tc_fence_after();
+      if (elect_one()) {
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = ((kk >> 2) * (TR * 128) + (kk & 3) * 32) >> 4;
+          const uint32_t offq = (s * C::QT_BYTES + (kk >> 2) * 8192 + (kk & 3) * 32) >> 4;
+          tc_mma_f16(tmem, dk + off, dqk + offq, idesc_sp, kk > 0);
+          tc_mma_f16(tmem + 64, dv + off, dok + offq, idesc_sp, kk > 0);
+        }
+        tc_commit(sp_full0 + 8 * (it & 1));
+      }
+      __syncwarp();
+      return true;
+    };
+    bool good = warp_wait(kv_full, 0, p.err) && issue_sp(0);
+    for (int it = 0; it < n_it && good; ++it) {
+      // the group of tile it has its scores in registers: the next tile's go in
+      // (no abort-flag poll here: a role that gave up stops arriving, so this
+      // warp's next bounded wait runs out as well)
+      if (!warp_wait(sp_free0 + 8 * (it & 1), (it >> 1) & 1, p.err) ||
+          (it + 1 < n_it && !issue_sp(it + 1)) ||
+          !warp_wait(pds_full0 + 8 * (it & 1), (it >> 1) & 1, p.err)) {
         good = false;
         break;
       }
       tc_fence_after();
-      float st[32], dp[32], L[32], Dl[32];
-      const uint32_t tb = tmem + (it & 1) * 128;
-      ld_cols32(tb + lane_base + col0, st);
-      ld_cols32(tb + lane_base + 64 + col0, dp);
-      const float* ldp = sLD + (it & 1) * 2 * TC + col0;
+      const int s = it % NSA;
+      const uint32_t ta = tmem + C::COL_PDS + (it & 1) * 64;  // P^T, then dS^T at + 32
+      if (elect_one()) {
 #pragma unroll
-      for (int c = 0; c < 32; c += 4) {
-        const float4 a = *reinterpret_cast<const float4*>(ldp + c);
-        const float4 d = *reinterpret_cast<const float4*>(ldp + TC + c);
-        L[c] = a.x; L[c + 1] = a.y; L[c + 2] = a.z; L[c + 3] = a.w;
-        Dl[c] = d.x; Dl[c + 1] = d.y; Dl[c + 2] = d.z; Dl[c + 3] = d.w;
-      }
-      mbar_arrive(ld_empty0 + 8 * (it & 1));
-      // P^T and dS^T of this key row against its 32 queries of the tile
-      const int q0 = it_q0(it) + col0;
-      const bool full = q0 + 32 <= p.S && kv0 + TR <= p.S && (!p.causal || q0 >= kv0 + TR - 1);
-      if (full) {
-#pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          const float pt = exp2f(fmaf(st[c], p.sl2, -L[c]));
-          st[c] = pt;
-          dp[c] = pt * (dp[c] - Dl[c]);
+        for (int kk = 0; kk < TC / 16; ++kk) {
+          const uint32_t b_off = (s * C::QT_BYTES + kk * 2048) >> 4;
+          tc_mma_f16_ts(tmem + C::COL_DV, ta + kk * 8, dom + b_off, idesc_acc, (it > 0 || kk > 0));
+          tc_mma_f16_ts(tmem + C::COL_DK, ta + 32 + kk * 8, dqm + b_off, idesc_acc,
+                        (it > 0 || kk > 0));
         }
-      } else {
-#pragma unroll
-        for (int c = 0; c < 32; ++c) {
-          const int q = q0 + c;
-          const bool vis = q < p.S && kr < p.S && !(p.causal && q < kr);
-          const float pt = vis ? exp2f(fmaf(st[c], p.sl2, -L[c])) : 0.0f;
-          st[c] = pt;
-          dp[c] = pt * (dp[c] - Dl[c]);
-        }
+        tc_commit(qd_empty0 + 8 * s);
+        tc_commit(pds_empty0 + 8 * (it & 1));
+        if (it == n_it - 1) tc_commit(acc_done);
       }
-      // the P / dS tiles were last read by dV/dK of tile it - 1
-      if (it >= 1 && !warp_wait(pds_empty, (it - 1) & 1, p.err)) {
+      __syncwarp();
+    }
+    if (!good) *abort = 1;
+  } else {
+    // ---------------- compute warps 0-15 (group grp takes the tiles it & 1 == grp)
+    const int grp = warp >> 3, half = (warp >> 2) & 1;
+    const int rrow = (warp & 3) * 32 + lane;
+    const int kr = kv0 + rrow;  // this thread's key position
+    const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+    const uint32_t col0 = half * 32;  // this warp's columns of the 64-wide tiles
+    bool good = true;
+    int qt = qt_start + grp;  // query tile of iteration it (it mod per_head past qt_start)
+    while (qt >= nqt) qt -= per_head;
+    for (int it = grp; it < n_it; it += 2) {
+      if (warp_aborted(abort) || !warp_wait(sp_full0 + 8 * grp, (it >> 1) & 1, p.err)) {
         good = false;
         break;
       }
-      store_half_row_sw128(smem + C::OFF_P + rrow * 128, rrow, half, st);
-      store_half_row_sw128(smem + C::OFF_DS + rrow * 128, rrow, half, dp);
-      fence_proxy_async();
+      tc_fence_after();
+      float st[32], dp[32];
+      {
+        uint32_t rs[32], rd[32];
+        tmem_ld32(tmem + lane_base + col0, rs);
+        tmem_ld32(tmem + lane_base + 64 + col0, rd);
+        tmem_ld_wait();
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+          st[c] = __uint_as_float(rs[c]);
+          dp[c] = __uint_as_float(rd[c]);
+        }
+      }
+      // the scores are in registers: the MMA warp may overwrite them
       tc_fence_before();
-      mbar_arrive(pds_full);
+      mbar_arrive(sp_free0 + 8 * grp);
+      const float* ldp = sLD + (it % NSA) * (2 * TC) + col0;
+      // P^T and dS^T of this key row against its 32 queries of the tile (past
+      // the sequence end the workspace holds LSE = +inf, so P = 0 there);
+      // LSE/delta are read from smem four at a time
+      const int q0 = qt * TC + col0;
+      const bool full = kr < p.S && (!p.causal || q0 >= kv0 + TR - 1);
+#pragma unroll
+      for (int c = 0; c < 32; c += 4) {
+        const float4 L = *reinterpret_cast<const float4*>(ldp + c);
+        const float4 Dl = *reinterpret_cast<const float4*>(ldp + TC + c);
+        const float l4[4] = {L.x, L.y, L.z, L.w}, d4[4] = {Dl.x, Dl.y, Dl.z, Dl.w};
+        if (full) {
+          fma2(st[c], st[c + 1], st[c], st[c + 1], p.sl2, p.sl2, -l4[0], -l4[1]);
+          fma2(st[c + 2], st[c + 3], st[c + 2], st[c + 3], p.sl2, p.sl2, -l4[2], -l4[3]);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) st[c + e] = ex2_ftz(st[c + e]);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const bool vis = kr < p.S && !(p.causal && q0 + c + e < kr);
+            st[c + e] = vis ? ex2_ftz(fmaf(st[c + e], p.sl2, -l4[e])) : 0.0f;
+          }
+        }
+#pragma unroll
+        for (int e = 0; e < 4; ++e) dp[c + e] = st[c + e] * (dp[c + e] - d4[e]);
+      }
+      uint32_t pp[16], pd[16];
+#pragma unroll
+      for (int c = 0; c < 16; ++c) {
+        pp[c] = pack_bf16x2(st[2 * c], st[2 * c + 1]);
+        pd[c] = pack_bf16x2(dp[2 * c], dp[2 * c + 1]);
+      }
+      // P^T / dS^T buffer grp was last read by dV/dK of tile it - 2
+      if (it >= 2 && !warp_wait(pds_empty0 + 8 * grp, ((it - 2) >> 1) & 1, p.err)) {
+        good = false;
+        break;
+      }
+      const uint32_t tpd = tmem + lane_base + C::COL_PDS + grp * 64 + half * 16;
+      tmem_st16(tpd, pp);
+      tmem_st16(tpd + 32, pd);
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(pds_full0 + 8 * grp);
+      qt += 2;
+      while (qt >= nqt) qt -= per_head;
     }
     if (!good) *abort = 1;
-    // ---- all products done: dK (scaled) and dV rows out of TMEM
+    // ---- all products done: group 0 stores dK (scaled), group 1 dV, out of TMEM
     if (good && warp_wait(acc_done, 0, p.err) && !warp_aborted(abort)) {
       tc_fence_after();
       const bool row_ok = kr < p.S;
       const int64_t orow = (int64_t)(grow0 + kr) * p.ld_out + g * D;
       const int c0 = half * (D / 2);  // the two warps of a quarter split the d columns
-      store_tmem_row<D / 2>(tmem + lane_base + C::COL_DK + c0, p.scale,
-                            row_ok ? p.d0 + orow + c0 : nullptr);
-      store_tmem_row<D / 2>(tmem + lane_base + C::COL_DV + c0, 1.0f,
-                            row_ok ? p.d1 + orow + c0 : nullptr);
+      if (grp == 0)
+        store_tmem_row<D / 2>(tmem + lane_base + C::COL_DK + c0, p.scale,
+                              row_ok ? p.d0 + orow + c0 : nullptr);
+      else
+        store_tmem_row<D / 2>(tmem + lane_base + C::COL_DV + c0, 1.0f,
+                              row_ok ? p.d1 + orow + c0 : nullptr);
     } else {
       *abort = 1;
     }
@@ -325,15 +359,14 @@ struct DqCfg {
   static constexpr int KB = D / 64;
   static constexpr int QO_BYTES = TR * D * 2;  // Q or dO rows of this CTA
   static constexpr int KV_BYTES = TC * D * 2;  // one K or V tile
-  static constexpr int DS_BYTES = TR * TC * 2;
   static constexpr int OFF_Q = 0;
   static constexpr int OFF_DO = OFF_Q + QO_BYTES;
-  static constexpr int OFF_K = OFF_DO + QO_BYTES;      // NS stages
-  static constexpr int OFF_V = OFF_K + NS * KV_BYTES;  // NS stages
-  static constexpr int OFF_DS = OFF_V + NS * KV_BYTES;
-  static constexpr int OFF_BAR = OFF_DS + DS_BYTES;
+  static constexpr int OFF_K = OFF_DO + QO_BYTES;        // NSB stages
+  static constexpr int OFF_V = OFF_K + NSB * KV_BYTES;   // NSB stages
+  static constexpr int OFF_BAR = OFF_V + NSB * KV_BYTES;
   static constexpr int SMEM = OFF_BAR + 256 + 1024;
-  static constexpr int COL_DQ = COL_ACC;
+  // TMEM: scores [0, 128), dS buffers [128, 192) (32 columns = 64 bf16 keys each), dQ
+  static constexpr int COL_DS = 128, COL_DQ = COL_ACC;
 };
 
 template <int D>
@@ -347,18 +380,18 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const uint32_t sb = smem_u32(smem);
-  const uint32_t sQ = sb + C::OFF_Q, sO = sb + C::OFF_DO, sK = sb + C::OFF_K, sV = sb + C::OFF_V,
-                 sS = sb + C::OFF_DS;
+  const uint32_t sQ = sb + C::OFF_Q, sO = sb + C::OFF_DO, sK = sb + C::OFF_K, sV = sb + C::OFF_V;
   const uint32_t bar = sb + C::OFF_BAR;
-  const uint32_t qo_full = bar;          // Q, dO loaded              (tx)
-  const uint32_t kv_full0 = bar + 8;     // [3] K/V stage loaded      (tx)
-  const uint32_t kv_empty0 = bar + 32;   // [3] stage read by dQ      (commit)
-  const uint32_t sp_full0 = bar + 56;    // [2] S/dP ready            (commit)
-  const uint32_t ds_full = bar + 72;     // dS written                (256 arrivals)
-  const uint32_t ds_empty = bar + 80;    // dQ read it                (commit)
-  const uint32_t acc_done = bar + 88;    // all products done         (commit)
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_BAR + 128);
-  volatile int* abort = reinterpret_cast<volatile int*>(smem + C::OFF_BAR + 132);
+  const uint32_t qo_full = bar;          // Q, dO loaded                  (tx)
+  const uint32_t kv_full0 = bar + 8;     // [5] K/V stage loaded          (tx)
+  const uint32_t kv_empty0 = bar + 48;   // [5] stage read by dQ          (commit)
+  const uint32_t sp_full0 = bar + 88;    // [2] S/dP of tile j ready      (commit)
+  const uint32_t sp_free0 = bar + 104;   // [2] group read them out       (256 arrivals)
+  const uint32_t ds_full0 = bar + 120;   // [2] dS buffer written         (256 arrivals)
+  const uint32_t ds_empty0 = bar + 136;  // [2] dQ read the buffer        (commit)
+  const uint32_t acc_done = bar + 152;   // all products done             (commit)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_BAR + 176);
+  volatile int* abort = reinterpret_cast<volatile int*>(smem + C::OFF_BAR + 180);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int nqt = (p.S + TR - 1) / TR;
@@ -375,9 +408,17 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     tma_prefetch_desc(&tmK);
     tma_prefetch_desc(&tmV);
     tma_prefetch_desc(&tmO);
-    for (int i = 0; i < 9; ++i) mbar_init(bar + 8 * i, 1);
-    mbar_init(ds_full, NCOMPUTE);
-    mbar_init(ds_empty, 1);
+    mbar_init(qo_full, 1);
+    for (int i = 0; i < NSB; ++i) {
+      mbar_init(kv_full0 + 8 * i, 1);
+      mbar_init(kv_empty0 + 8 * i, 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(sp_full0 + 8 * i, 1);
+      mbar_init(sp_free0 + 8 * i, NGROUP);
+      mbar_init(ds_full0 + 8 * i, NGROUP);
+      mbar_init(ds_empty0 + 8 * i, 1);
+    }
     mbar_init(acc_done, 1);
     fence_mbar_init();
     *abort = 0;
@@ -388,7 +429,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 8) {
+  if (warp == W_PROD) {
     // ---------------- producer
     if (lane == 0) {
       mbar_arrive_expect_tx(qo_full, 2 * C::QO_BYTES);
@@ -398,8 +439,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         tma_load_2d(sO + kb * (TR * 128), &tmO, h * D + kb * 64, grow0 + q0, qo_full);
       }
       for (int j = 0; j < nkt && !*abort; ++j) {
-        const int s = j % NS;
-        if (j >= NS && !mbar_wait(kv_empty0 + 8 * s, ((j - NS) / NS) & 1, p.err)) {
+        const int s = j % NSB;
+        if (j >= NSB && !mbar_wait(kv_empty0 + 8 * s, ((j - NSB) / NSB) & 1, p.err)) {
           *abort = 1;
           break;
         }
@@ -412,100 +453,132 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
       }
     }
-  } else if (warp == 9) {
+  } else if (warp == W_MMA) {
     // ---------------- MMA issuer
-    if (lane == 0) {
-      constexpr uint32_t idesc_sp = idesc_bf16_f32(TR, TC, 0, 0);
-      constexpr uint32_t idesc_acc = idesc_bf16_f32(TR, D, 0, 1);
-      auto issue_sp = [&](int j) -> bool {
-        const int s = j % NS;
-        if (!mbar_wait(kv_full0 + 8 * s, (j / NS) & 1, p.err)) return false;
-        tc_fence_after();
-        const uint32_t tb = tmem + (j & 1) * 128;
+    constexpr uint32_t idesc_sp = idesc_bf16_f32(TR, TC, 0, 0);
+    constexpr uint32_t idesc_acc = idesc_bf16_f32(TR, D, 0, 1);
+    const uint64_t dq = smem_desc_sw128(sQ, 16, 1024), dob = smem_desc_sw128(sO, 16, 1024);
+    const uint64_t dkk = smem_desc_sw128(sK, 16, 1024), dvk = smem_desc_sw128(sV, 16, 1024);
+    const uint64_t dkm = smem_desc_sw128(sK, 8192, 1024);
+    auto issue_sp = [&](int j) -> bool {
+      const int s = j % NSB;
+      if (!warp_wait(kv_full0 + 8 * s, (j / NSB) & 1, p.err)) return false;
+      tc_fence_after();
+      if (elect_one()) {
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * (TR * 128) + (kk & 3) * 32;
-          const uint32_t offk = (kk >> 2) * 8192 + (kk & 3) * 32;
-          tc_mma_f16(tb, smem_desc_sw128(sQ + off, 16, 1024),
-                     smem_desc_sw128(sK + s * C::KV_BYTES + offk, 16, 1024), idesc_sp, kk > 0);
-          tc_mma_f16(tb + 64, smem_desc_sw128(sO + off, 16, 1024),
-                     smem_desc_sw128(sV + s * C::KV_BYTES + offk, 16, 1024), idesc_sp, kk > 0);
+          const uint32_t off = ((kk >> 2) * (TR * 128) + (kk & 3) * 32) >> 4;
+          const uint32_t offk = (s * C::KV_BYTES + (kk >> 2) * 8192 + (kk & 3) * 32) >> 4;
+          tc_mma_f16(tmem, dq + off, dkk + offk, idesc_sp, kk > 0);
+          tc_mma_f16(tmem + 64, dob + off, dvk + offk, idesc_sp, kk > 0);
         }
         tc_commit(sp_full0 + 8 * (j & 1));
-        return true;
-      };
-      bool good = mbar_wait(qo_full, 0, p.err) && issue_sp(0) && (nkt < 2 || issue_sp(1));
-      for (int j = 0; j < nkt && good && !*abort; ++j) {
-        if (!mbar_wait(ds_full, j & 1, p.err)) {
-          good = false;
-          break;
-        }
-        tc_fence_after();
-        const int s = j % NS;
+      }
+      __syncwarp();
+      return true;
+    };
+    bool good = warp_wait(qo_full, 0, p.err) && issue_sp(0);
+    for (int j = 0; j < nkt && good; ++j) {
+      // the group of tile j has its scores in registers: the next tile's go in
+      if (!warp_wait(sp_free0 + 8 * (j & 1), (j >> 1) & 1, p.err) ||
+          (j + 1 < nkt && !issue_sp(j + 1)) ||
+          !warp_wait(ds_full0 + 8 * (j & 1), (j >> 1) & 1, p.err)) {
+        good = false;
+        break;
+      }
+      tc_fence_after();
+      const int s = j % NSB;
+      const uint32_t ta = tmem + C::COL_DS + (j & 1) * 32;
+      if (elect_one()) {
 #pragma unroll
         for (int kk = 0; kk < TC / 16; ++kk)
-          tc_mma_f16(tmem + C::COL_DQ, smem_desc_sw128(sS + kk * 32, 16, 1024),
-                     smem_desc_sw128(sK + s * C::KV_BYTES + kk * 2048, 8192, 1024), idesc_acc,
-                     (j > 0 || kk > 0));
+          tc_mma_f16_ts(tmem + C::COL_DQ, ta + kk * 8, dkm + ((s * C::KV_BYTES + kk * 2048) >> 4),
+                        idesc_acc, (j > 0 || kk > 0));
         tc_commit(kv_empty0 + 8 * s);
-        tc_commit(ds_empty);
-        if (j + 2 < nkt && !issue_sp(j + 2)) good = false;
+        tc_commit(ds_empty0 + 8 * (j & 1));
+        if (j == nkt - 1) tc_commit(acc_done);
       }
-      if (good && !*abort) tc_commit(acc_done);
-      else *abort = 1;
+      __syncwarp();
     }
+    if (!good) *abort = 1;
   } else {
-    // ---------------- compute warps 0-7
-    const int rrow = (warp & 3) * 32 + lane, half = warp >> 2;
+    // ---------------- compute warps 0-15 (group grp takes the tiles j & 1 == grp)
+    const int grp = warp >> 3, half = (warp >> 2) & 1;
+    const int rrow = (warp & 3) * 32 + lane;
     const int row = q0 + rrow;
-    const int64_t lrow = ((int64_t)b * p.nq + h) * p.S;
-    const float L2 = row < p.S ? p.lse[lrow + row] * LOG2E : INFINITY;
-    const float Dr = row < p.S ? p.delta[lrow + row] : 0.0f;
+    const int64_t lrow = ((int64_t)b * p.nq + h) * p.s_pad + row;
+    const float L2 = p.lse2[lrow];  // +inf past the sequence end
+    const float Dr = p.delta[lrow];
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     const uint32_t col0 = half * 32;
     bool good = true;
-    for (int j = 0; j < nkt; ++j) {
-      if (warp_aborted(abort) || !warp_wait(sp_full0 + 8 * (j & 1), (j >> 1) & 1, p.err)) {
+    for (int j = grp; j < nkt; j += 2) {
+      if (warp_aborted(abort) || !warp_wait(sp_full0 + 8 * grp, (j >> 1) & 1, p.err)) {
         good = false;
         break;
       }
       tc_fence_after();
       float sc[32], dp[32];
-      const uint32_t tb = tmem + (j & 1) * 128;
-      ld_cols32(tb + lane_base + col0, sc);
-      ld_cols32(tb + lane_base + 64 + col0, dp);
+      {
+        uint32_t rs[32], rd[32];
+        tmem_ld32(tmem + lane_base + col0, rs);
+        tmem_ld32(tmem + lane_base + 64 + col0, rd);
+        tmem_ld_wait();
+#pragma unroll
+        for (int c = 0; c < 32; ++c) {
+          sc[c] = __uint_as_float(rs[c]);
+          dp[c] = __uint_as_float(rd[c]);
+        }
+      }
+      // the scores are in registers: the MMA warp may overwrite them
+      tc_fence_before();
+      mbar_arrive(sp_free0 + 8 * grp);
       const int kv0 = j * TC + col0;  // first key of this thread's columns
       // mask-free when every query row of the CTA sees every key of the half-tile
       const bool full = kv0 + 32 <= p.S && (!p.causal || kv0 + 31 <= q0);
       if (full) {
 #pragma unroll
-        for (int c = 0; c < 32; ++c) dp[c] = exp2f(fmaf(sc[c], p.sl2, -L2)) * (dp[c] - Dr);
+        for (int c = 0; c < 32; c += 2) {
+          fma2(sc[c], sc[c + 1], sc[c], sc[c + 1], p.sl2, p.sl2, -L2, -L2);
+          sc[c] = ex2_ftz(sc[c]);
+          sc[c + 1] = ex2_ftz(sc[c + 1]);
+        }
       } else {
 #pragma unroll
         for (int c = 0; c < 32; ++c) {
           const int kv = kv0 + c;
           const bool vis = kv < p.S && !(p.causal && kv > row);
-          const float pr = vis ? exp2f(fmaf(sc[c], p.sl2, -L2)) : 0.0f;
-          dp[c] = pr * (dp[c] - Dr);
+          sc[c] = vis ? ex2_ftz(fmaf(sc[c], p.sl2, -L2)) : 0.0f;
         }
       }
-      if (j >= 1 && !warp_wait(ds_empty, (j - 1) & 1, p.err)) {
+      uint32_t pd[16];
+#pragma unroll
+      for (int c = 0; c < 16; ++c)
+        pd[c] = pack_bf16x2(sc[2 * c] * (dp[2 * c] - Dr), sc[2 * c + 1] * (dp[2 * c + 1] - Dr));
+      // dS buffer grp was last read by dQ of tile j - 2
+      if (j >= 2 && !warp_wait(ds_empty0 + 8 * grp, ((j - 2) >> 1) & 1, p.err)) {
         good = false;
         break;
       }
-      store_half_row_sw128(smem + C::OFF_DS + rrow * 128, rrow, half, dp);
-      fence_proxy_async();
+      tmem_st16(tmem + lane_base + C::COL_DS + grp * 32 + half * 16, pd);
+      tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(ds_full);
+      mbar_arrive(ds_full0 + 8 * grp);
     }
     if (!good) *abort = 1;
+    // ---- all products done: dQ (scaled) out of TMEM, the warps of each lane
+    // quarter taking 32-column slices (all four for d = 128, two for d = 64)
     if (good && warp_wait(acc_done, 0, p.err) && !warp_aborted(abort)) {
       tc_fence_after();
       const bool row_ok = row < p.S;
-      const int c0 = half * (D / 2);
-      store_tmem_row<D / 2>(tmem + lane_base + C::COL_DQ + c0, p.scale,
-                            row_ok ? p.d0 + (int64_t)(grow0 + row) * p.ld_out + h * D + c0
-                                   : nullptr);
+      constexpr int NW = D / 32;  // warps per quarter with a slice
+      const int slice = grp * 2 + half;
+      if (slice < NW) {
+        const int c0 = slice * 32;
+        store_tmem_row<32>(tmem + lane_base + C::COL_DQ + c0, p.scale,
+                           row_ok ? p.d0 + (int64_t)(grow0 + row) * p.ld_out + h * D + c0
+                                  : nullptr);
+      }
     } else {
       *abort = 1;
     }
@@ -525,9 +598,11 @@ mgb_status bwd_tc_d(const AttnArgs& a, cudaStream_t st) {
   const uint64_t T = (uint64_t)a.B * a.S;
   BwdParams p{};
   p.B = a.B; p.S = a.S; p.nq = a.nq; p.nkv = a.nkv; p.causal = a.causal;
-  p.lse = a.lse; p.delta = a.delta;
+  p.s_pad = attn_bwd_row_pad(a.S);
+  p.lse2 = a.delta;
+  p.delta = a.delta + (size_t)a.B * a.nq * p.s_pad;
   p.err = device_error_word();
-  p.sl2 = LOG2E / sqrtf((float)D);
+  p.sl2 = 1.4426950408889634f / sqrtf((float)D);
   p.scale = 1.0f / sqrtf((float)D);
   // kernel A: K/V rows of 128, Q/dO tiles of 64
   {

@@ -74,8 +74,14 @@ struct AttnArgs {
   // backward
   const void* dout; int64_t ld_do;
   void *dq, *dk, *dv; int64_t ld_dq, ld_dkv;
-  float* delta;          // [B, nq, S] scratch
+  float* delta;          // backward scratch (attn_bwd_ws_bytes)
 };
+// The bf16 backward's per-query workspace: two float32 planes [B * nq][pad]
+// (LSE * log2(e), then delta) with rows padded to a multiple of 128 queries.
+inline int attn_bwd_row_pad(int S) { return (S + 127) / 128 * 128; }
+inline size_t attn_bwd_ws_bytes(int B, int S, int nq) {
+  return 2 * sizeof(float) * (size_t)B * nq * attn_bwd_row_pad(S);
+}
 mgb_status attention_fwd_launch(const AttnArgs& a, cudaStream_t st);
 mgb_status attention_bwd_launch(const AttnArgs& a, cudaStream_t st);
 

@@ -111,6 +111,8 @@ def load() -> ctypes.CDLL:
         lib.mgb_version.restype = ctypes.c_int32
         lib.mgb_layernorm_bwd_ws_bytes.argtypes = [I32, I32]
         lib.mgb_layernorm_bwd_ws_bytes.restype = SZ
+        lib.mgb_attention_bwd_ws_bytes.argtypes = [I32, I32, I32]
+        lib.mgb_attention_bwd_ws_bytes.restype = SZ
         lib.mgb_launch_count.argtypes = []
         lib.mgb_launch_count.restype = ctypes.c_uint64
         lib.mgb_profile_enable.argtypes = [I32]
@@ -233,6 +235,10 @@ def mgb_layernorm_fwd(rows: int, cols: int, dtype: int, eps: float, x, gamma, be
 
 def mgb_layernorm_bwd_ws_bytes(rows: int, cols: int) -> int:
     return load().mgb_layernorm_bwd_ws_bytes(rows, cols)
+
+
+def mgb_attention_bwd_ws_bytes(batch: int, seq: int, n_q_heads: int) -> int:
+    return load().mgb_attention_bwd_ws_bytes(batch, seq, n_q_heads)
 
 
 def mgb_layernorm_bwd(rows: int, cols: int, dtype: int, x, mean, rstd, gamma, dy, dres, dx, dgamma,

@@ -120,3 +120,16 @@ def test_injected_validation_fault(lib, monkeypatch):
 
 def test_selftest_limit_is_validated(lib):
     assert lib.mgb_selftest_wait_timeout(10 ** 10, None) == mgb.MGB_ERR_INVALID_ARG
+
+
+def test_attention_bwd_workspace_size(lib):
+    """Two float32 planes with rows padded to 128 queries; too small a
+    workspace is refused before any launch."""
+    assert mgb.mgb_attention_bwd_ws_bytes(2, 4096, 32) == 2 * 4 * 2 * 32 * 4096
+    assert mgb.mgb_attention_bwd_ws_bytes(1, 130, 4) == 2 * 4 * 4 * 256
+    assert mgb.mgb_attention_bwd_ws_bytes(-1, 8, 1) == 0
+    need = mgb.mgb_attention_bwd_ws_bytes(1, 130, 4)
+    p = 4096
+    s = lib.mgb_attention_bwd(1, 130, 4, 2, 64, 1, mgb.MGB_BF16, p, p, p, 512, 512, p, p, p, 256,
+                              p, p, p, 512, 512, p, need - 16, None)
+    assert s == mgb.MGB_ERR_WORKSPACE_TOO_SMALL

@@ -68,7 +68,7 @@ def _check(dtype, B, S, nq, nkv, d, causal, amp, ramp):
     assert np.abs(to_np(lse) - rl).max() < (2e-2 if dtype == "bf16" else 1e-5)
     # backward against the oracle's gradient of sum(do * O) for the same q, k, v
     dqkv = torch.full((B * S, W), float("nan"), device="cuda", dtype=td)
-    ws = torch.empty(4 * B * nq * S, dtype=torch.uint8, device="cuda")
+    ws = torch.empty(mgb.mgb_attention_bwd_ws_bytes(B, S, nq), dtype=torch.uint8, device="cuda")
     mgb.mgb_attention_bwd(B, S, nq, nkv, d, causal, mdt, qs, ks, vs, W, W, o, lse,
                           _dev(pack(do), td), nq * d, dqkv, dqkv[:, nq * d:],
                           dqkv[:, (nq + nkv) * d:], W, W, ws)
