@@ -441,6 +441,36 @@ def run_case(args):
             print(json.dumps(out), flush=True)
             del r
         return
+    if args.case == "attention":
+        # the attention core of the layer workload: forward, then backward
+        # (q, k, v as column slices of one fused buffer, as in the layer)
+        shape = WORKLOADS[LAYER]
+        B, S, nq, nkv, d = shape.batch, shape.seq, shape.n_q_heads, shape.n_kv_heads, shape.head_dim
+        W = (nq + 2 * nkv) * d
+        g = torch.Generator(device="cuda").manual_seed(0)
+        qkv = torch.randn((B * S, W), device="cuda", generator=g).to(torch.bfloat16)
+        o = torch.empty((B * S, nq * d), device="cuda", dtype=torch.bfloat16)
+        lse = torch.empty((B, nq, S), device="cuda")
+        dout = torch.randn((B * S, nq * d), device="cuda", generator=g).to(torch.bfloat16)
+        dqkv = torch.empty_like(qkv)
+        ws = torch.empty(mgb.mgb_attention_bwd_ws_bytes(B, S, nq), dtype=torch.uint8, device="cuda")
+        cz = int(shape.causal)
+        q, k, v = qkv, qkv[:, nq * d:], qkv[:, (nq + nkv) * d:]
+
+        def fwd():
+            mgb.mgb_attention_fwd(B, S, nq, nkv, d, cz, mgb.MGB_BF16, q, k, v, W, W, o, lse)
+
+        def bwd():
+            mgb.mgb_attention_bwd(B, S, nq, nkv, d, cz, mgb.MGB_BF16, q, k, v, W, W, o, lse, dout,
+                                  nq * d, dqkv, dqkv[:, nq * d:], dqkv[:, (nq + nkv) * d:], W, W, ws)
+        # FLOPs: forward 2 products (S, PV); backward 5 (S, dP, dV, dK, dQ) = 2.5x
+        fl = layer_flops(shape)["attn_fwd"]
+        for name, fn, f in (("attention_fwd", fwd, fl), ("attention_bwd", bwd, 2.5 * fl)):
+            ms, prof = _time_loop(fn, args.steps, args.warmup, st)
+            print(json.dumps({"case": name, "workload": LAYER, "ms": round(ms, 4),
+                              "tflop": round(f / 1e12, 4), "tflops": round(f / (ms / 1e3) / 1e12, 1),
+                              "kernel_ms": prof}), flush=True)
+        return
     if args.case == "ce":
         ce = CE_WORKLOADS[CE]
         cin = ce_inputs(ce, seed=0)
@@ -465,7 +495,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--case", default="step", choices=("step", "layer", "sweep", "ce", "gemm"),
+    ap.add_argument("--case", default="step",
+                    choices=("step", "layer", "sweep", "ce", "gemm", "attention"),
                     help="step (default, the driver's line) or a sub-path / single kernel")
     ap.add_argument("--mnk", type=int, nargs=3, default=(8192, 22016, 4096))
     args = ap.parse_args()
