@@ -11,8 +11,8 @@
 // Backward (per row, xhat = (x - mean) * rstd, g = dy * gamma):
 //   dx = dres + rstd * (g - mean(g) - xhat * mean(g * xhat))
 // rows are strided over a fixed number of blocks; each thread accumulates the
-// dgamma = sum dy*xhat and dbeta = sum dy partials of its own columns, written
-// per block and reduced by a second small kernel.
+// dgamma = sum dy*xhat and dbeta = sum dy partials of its own columns in
+// registers, written per block and reduced by a second small kernel.
 // Column sums db[n] = sum_m dY[m, n] (bias gradients) use the same
 // partial-then-reduce scheme with coalesced 16-byte row reads.
 #include <mutex>
@@ -158,55 +158,59 @@ __device__ __forceinline__ float2 block_sum2(float2 v, float2* red) {
   return t;
 }
 
-// Row blocks stride over the rows. The dgamma/dbeta partial sums of the
-// block's columns live in shared memory (2 * cols floats, laid out [j][vector]
-// so that lanes touch consecutive words), which keeps registers low enough for
-// several blocks per SM.
-template <typename T>
+// Row blocks stride over the rows; thread t owns the VPT 16-byte vectors
+// t, t + blockDim, ... of every row, so gamma and the dgamma/dbeta partial sums
+// of those columns stay in registers for the whole block. A row's x, dy and
+// dres are all requested before the row reduction, so each thread keeps
+// 3 * VPT loads in flight.
+template <typename T, int VPT>
 __global__ void ln_bwd_kernel(int rows, int cols, const T* __restrict__ x,
                               const float* __restrict__ mean, const float* __restrict__ rstd,
                               const T* __restrict__ gamma, const T* __restrict__ dy,
                               const T* __restrict__ dres, T* __restrict__ dx,
                               float* __restrict__ part) {
   constexpr int VN = Vec<T>::N;
-  extern __shared__ float sacc[];  // [2][VN][nvec] when part != nullptr
   __shared__ float2 red[32];
   const int nvec = cols / VN;
-  float* spg = sacc;
-  float* spb = sacc + cols;
-  if (part) {
-    // every thread zeroes exactly the slots it accumulates into
+  float gm[VPT][VN], pg[VPT][VN], pb[VPT][VN];
 #pragma unroll
-    for (int i = 0; i < MAXV; ++i) {
-      const int vi = threadIdx.x + i * blockDim.x;
-      if (vi < nvec) {
+  for (int i = 0; i < VPT; ++i) {
+    const int vi = threadIdx.x + i * blockDim.x;
 #pragma unroll
-        for (int j = 0; j < VN; ++j) spg[j * nvec + vi] = spb[j * nvec + vi] = 0.0f;
-      }
+    for (int j = 0; j < VN; ++j) {
+      gm[i][j] = 1.0f;
+      pg[i][j] = pb[i][j] = 0.0f;
     }
+    if (gamma && vi < nvec) vload(gamma + vi * VN, gm[i]);
   }
   for (int row = blockIdx.x; row < rows; row += gridDim.x) {
     const float mu = mean[row], rs = rstd[row];
-    float xh[MAXV][VN], g[MAXV][VN];
-    float s1 = 0.0f, s2 = 0.0f;
+    const int64_t ro = (int64_t)row * cols;
+    float xv[VPT][VN], dv[VPT][VN], rv[VPT][VN];
 #pragma unroll
-    for (int i = 0; i < MAXV; ++i) {
+    for (int i = 0; i < VPT; ++i) {
       const int vi = threadIdx.x + i * blockDim.x;
       if (vi < nvec) {
-        float xv[VN], dv[VN], gm[VN];
-        vload(x + (int64_t)row * cols + vi * VN, xv);
-        vload(dy + (int64_t)row * cols + vi * VN, dv);
-        if (gamma) vload(gamma + vi * VN, gm);
+        vload(x + ro + vi * VN, xv[i]);
+        vload(dy + ro + vi * VN, dv[i]);
+        if (dres) vload(dres + ro + vi * VN, rv[i]);
+      }
+    }
+    float s1 = 0.0f, s2 = 0.0f;
+#pragma unroll
+    for (int i = 0; i < VPT; ++i) {
+      const int vi = threadIdx.x + i * blockDim.x;
+      if (vi < nvec) {
 #pragma unroll
         for (int j = 0; j < VN; ++j) {
-          xh[i][j] = (xv[j] - mu) * rs;
-          g[i][j] = gamma ? dv[j] * gm[j] : dv[j];
-          s1 += g[i][j];
-          s2 += g[i][j] * xh[i][j];
-          if (part) {
-            spg[j * nvec + vi] += dv[j] * xh[i][j];
-            spb[j * nvec + vi] += dv[j];
-          }
+          const float xh = (xv[i][j] - mu) * rs;
+          const float g = dv[i][j] * gm[i][j];
+          s1 += g;
+          s2 += g * xh;
+          pg[i][j] += dv[i][j] * xh;
+          pb[i][j] += dv[i][j];
+          xv[i][j] = xh;  // keep xhat
+          dv[i][j] = g;   // keep g
         }
       }
     }
@@ -214,38 +218,32 @@ __global__ void ln_bwd_kernel(int rows, int cols, const T* __restrict__ x,
     const float mg = tot.x / cols;
     const float mgx = tot.y / cols;
 #pragma unroll
-    for (int i = 0; i < MAXV; ++i) {
+    for (int i = 0; i < VPT; ++i) {
       const int vi = threadIdx.x + i * blockDim.x;
       if (vi < nvec) {
-        float o[VN], r[VN];
-        if (dres) vload(dres + (int64_t)row * cols + vi * VN, r);
+        float o[VN];
 #pragma unroll
         for (int j = 0; j < VN; ++j) {
-          o[j] = rs * (g[i][j] - mg - xh[i][j] * mgx);
-          if (dres) o[j] += r[j];
+          o[j] = rs * (dv[i][j] - mg - xv[i][j] * mgx);
+          if (dres) o[j] += rv[i][j];
         }
-        vstore(dx + (int64_t)row * cols + vi * VN, o);
+        vstore(dx + ro + vi * VN, o);
       }
     }
   }
   if (part) {
-    // each thread wrote only its own columns; no barrier needed before reading them
     float* pgr = part + (int64_t)blockIdx.x * cols;
     float* pbr = part + (int64_t)(gridDim.x + blockIdx.x) * cols;
 #pragma unroll
-    for (int i = 0; i < MAXV; ++i) {
+    for (int i = 0; i < VPT; ++i) {
       const int vi = threadIdx.x + i * blockDim.x;
       if (vi < nvec) {
-        float a[VN], b[VN];
-#pragma unroll
-        for (int j = 0; j < VN; ++j) {
-          a[j] = spg[j * nvec + vi];
-          b[j] = spb[j * nvec + vi];
-        }
 #pragma unroll
         for (int j = 0; j < VN; j += 4) {
-          *reinterpret_cast<float4*>(pgr + vi * VN + j) = make_float4(a[j], a[j + 1], a[j + 2], a[j + 3]);
-          *reinterpret_cast<float4*>(pbr + vi * VN + j) = make_float4(b[j], b[j + 1], b[j + 2], b[j + 3]);
+          *reinterpret_cast<float4*>(pgr + vi * VN + j) =
+              make_float4(pg[i][j], pg[i][j + 1], pg[i][j + 2], pg[i][j + 3]);
+          *reinterpret_cast<float4*>(pbr + vi * VN + j) =
+              make_float4(pb[i][j], pb[i][j + 1], pb[i][j + 2], pb[i][j + 3]);
         }
       }
     }
@@ -352,38 +350,58 @@ mgb_status layernorm_fwd_launch(int rows, int cols, int dtype, float eps, const 
   return cudaGetLastError() == cudaSuccess ? MGB_OK : MGB_ERR_CUDA;
 }
 
+namespace {
+
+template <typename T, int VPT>
+void ln_bwd_go(int nparts, int threads, int rows, int cols, const void* x, const float* mean,
+               const float* rstd, const void* gamma, const void* dy, const void* dres, void* dx,
+               float* part, cudaStream_t st) {
+  ln_bwd_kernel<T, VPT><<<nparts, threads, 0, st>>>(rows, cols, (const T*)x, mean, rstd,
+                                                      (const T*)gamma, (const T*)dy,
+                                                      (const T*)dres, (T*)dx, part);
+}
+
+template <typename T>
+mgb_status ln_bwd_dispatch(int nparts, int rows, int cols, const void* x, const float* mean,
+                           const float* rstd, const void* gamma, const void* dy, const void* dres,
+                           void* dx, float* part, cudaStream_t st) {
+  // one 16-byte vector per thread (64 registers: full occupancy), two or four
+  // for rows wider than 1024 vectors
+  const int nvec = cols / Vec<T>::N;
+  auto thr = [&](int vpt) { return ((nvec + vpt - 1) / vpt + 31) / 32 * 32; };
+  if (nvec <= 1024)
+    ln_bwd_go<T, 1>(nparts, thr(1), rows, cols, x, mean, rstd, gamma, dy, dres, dx, part, st);
+  else if (nvec <= 2048)
+    ln_bwd_go<T, 2>(nparts, thr(2), rows, cols, x, mean, rstd, gamma, dy, dres, dx, part, st);
+  else if (nvec <= 4096)
+    ln_bwd_go<T, 4>(nparts, thr(4), rows, cols, x, mean, rstd, gamma, dy, dres, dx, part, st);
+  else
+    return MGB_ERR_UNSUPPORTED;
+  return MGB_OK;
+}
+
+}  // namespace
+
 mgb_status layernorm_bwd_launch(int rows, int cols, int dtype, const void* x, const float* mean,
                                 const float* rstd, const void* gamma, const void* dy,
                                 const void* dres, void* dx, void* dgamma, void* dbeta,
                                 float* part, int nparts, cudaStream_t st) {
   const int vn = dtype == MGB_BF16 ? 8 : 4;
   if (rows < 0 || cols <= 0 || cols % vn) return MGB_ERR_INVALID_ARG;
-  const int threads = ln_threads(cols, vn);
-  if (threads > 1024) return MGB_ERR_UNSUPPORTED;
+  if (cols / vn > 4096) return MGB_ERR_UNSUPPORTED;
   const bool want = (dgamma || dbeta) && part;
-  // dgamma/dbeta partials live in shared memory: 2 * cols floats per block
+  // the dgamma/dbeta partial rows of the workspace are sized for this width
   if (want && cols > kLnBwdMaxCols) return MGB_ERR_UNSUPPORTED;
-  const int smem = want ? 2 * cols * (int)sizeof(float) : 0;
   if (rows == 0) nparts = 1;
-  if (rows > 0 && smem > 48 * 1024) {
-    const cudaError_t e =
-        dtype == MGB_BF16
-            ? cudaFuncSetAttribute(ln_bwd_kernel<bf16>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)
-            : cudaFuncSetAttribute(ln_bwd_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return MGB_ERR_CUDA;
-  }
   LaunchScope scope(PROF_LN_BWD, st, (rows > 0 ? 1 : 0) + (want ? 1 : 0));
   if (rows > 0) {
-    if (dtype == MGB_BF16)
-      ln_bwd_kernel<bf16><<<nparts, threads, smem, st>>>(rows, cols, (const bf16*)x, mean, rstd,
-                                                          (const bf16*)gamma, (const bf16*)dy,
-                                                          (const bf16*)dres, (bf16*)dx,
-                                                          want ? part : nullptr);
-    else
-      ln_bwd_kernel<float><<<nparts, threads, smem, st>>>(rows, cols, (const float*)x, mean, rstd,
-                                                           (const float*)gamma, (const float*)dy,
-                                                           (const float*)dres, (float*)dx,
-                                                           want ? part : nullptr);
+    const mgb_status s =
+        dtype == MGB_BF16
+            ? ln_bwd_dispatch<bf16>(nparts, rows, cols, x, mean, rstd, gamma, dy, dres, dx,
+                                    want ? part : nullptr, st)
+            : ln_bwd_dispatch<float>(nparts, rows, cols, x, mean, rstd, gamma, dy, dres, dx,
+                                     want ? part : nullptr, st);
+    if (s != MGB_OK) return s;
   } else if (want) {
     cudaMemsetAsync(part, 0, sizeof(float) * 2 * cols, st);
   }
