@@ -126,12 +126,25 @@ mgb_status mgb_block_bwd(const mgb_block_desc* desc, const mgb_block_weights* w,
                          void* dx, const mgb_block_grads* grads,
                          void* ws, size_t ws_bytes, void* stream);
 
+/* Where the per-chunk statistics and the gradient of the cross-entropy are
+ * computed (same results up to float32 rounding order). */
+typedef enum {
+  MGB_CE_STREAM = 0,  /* the logits GEMM stores a chunk's bf16 logits; streaming
+                         kernels read them for the max / sum exp partials and
+                         rewrite them into the gradient */
+  MGB_CE_FUSED = 1    /* the logits GEMM's epilogue keeps per-(token, 128-column
+                         group) max / sum exp partials of its float32
+                         accumulator and stores no logits; the recomputing
+                         GEMM's epilogue writes the gradient directly */
+} mgb_ce_mode;
+
 /* Tied-embedding cross-entropy [P2 sections 3-4]. */
 typedef struct {
   int32_t tokens, hidden, vocab;
   int32_t chunk;        /* vocab chunk; the last chunk may be ragged */
   int32_t dtype;        /* MGB_BF16 (hidden/emb/grads bf16) */
   float grad_scale;     /* dL/dloss_t for every token: 1/tokens for the mean */
+  int32_t mode;         /* mgb_ce_mode */
 } mgb_ce_desc;
 
 mgb_status mgb_vocab_ce_sizes(const mgb_ce_desc* desc, size_t* ws_bytes);
@@ -142,6 +155,8 @@ mgb_status mgb_vocab_ce_sizes(const mgb_ce_desc* desc, size_t* ws_bytes);
  * loss_t = LSE_t - target logit_t, loss_mean = mean_t loss_t. Backward:
  * G = (softmax(l) - onehot(target)) * grad_scale, d_hidden = G E,
  * d_emb = G^T hidden, again chunk by chunk (logits recomputed per chunk).
+ * MGB_CE_FUSED keeps one (max, sum) partial per token and 128 vocab columns
+ * instead of one per chunk; the combine is the same merge.
  *   targets [T] int32 in [0, vocab) (device); loss_per_token [T] f32;
  *   loss_mean: one f32 (device); lse [T] f32 or NULL;
  *   d_hidden [T,H], d_emb [V,H]: NULL skips that gradient (both NULL = fwd only). */

@@ -482,26 +482,39 @@ static mgb_status validate_ce(const mgb_ce_desc* d) {
   if (d->dtype != MGB_BF16) return MGB_ERR_UNSUPPORTED;
   if (d->hidden % 8 || d->vocab % 8 || d->chunk % 8) return MGB_ERR_MISALIGNED;
   if (!(d->grad_scale == d->grad_scale)) return MGB_ERR_INVALID_ARG;
+  if (d->mode != MGB_CE_STREAM && d->mode != MGB_CE_FUSED) return MGB_ERR_INVALID_ARG;
   return MGB_OK;
 }
 
 struct CEPlan {
-  int n_chunks, C;
-  size_t logits, m, s, t, lse, dh, total;
+  int n_chunks, C, n_parts, n_t;
+  size_t logits, m, s, t, lse, dh, bl, split, total;
 };
 
+// Partials: one per chunk (streaming) or one per chunk and 128-column group
+// (fused, written by the GEMM epilogue); target logits per chunk (streaming,
+// zero outside the chunk) or one array each token's owning tile writes (fused).
 static void ce_plan(const mgb_ce_desc* d, CEPlan* p) {
   const size_t T = d->tokens;
   p->C = d->chunk < d->vocab ? d->chunk : d->vocab;
   p->n_chunks = (d->vocab + p->C - 1) / p->C;
+  const bool fused = d->mode == MGB_CE_FUSED;
+  p->n_parts = 0;
+  for (int c = 0; c < p->n_chunks; ++c) {
+    const int v0 = c * p->C, Cc = (d->vocab - v0) < p->C ? (d->vocab - v0) : p->C;
+    p->n_parts += fused ? (Cc + 127) / 128 : 1;
+  }
+  p->n_t = fused ? 1 : p->n_chunks;
   size_t o = 0;
   auto take = [&](size_t bytes) { const size_t a = o; o += al256(bytes); return a; };
   p->logits = take(2 * T * p->C);
-  p->m = take(4 * T * p->n_chunks);
-  p->s = take(4 * T * p->n_chunks);
-  p->t = take(4 * T * p->n_chunks);
+  p->m = take(4 * T * p->n_parts);
+  p->s = take(4 * T * p->n_parts);
+  p->t = take(4 * T * p->n_t);
   p->lse = take(4 * T);
   p->dh = take(4 * T * d->hidden);
+  p->bl = take(4 * (size_t)ce_combine_blocks((int)T));
+  p->split = p->n_parts > kCeSplits ? take(4 * 2 * (size_t)kCeSplits * T) : 0;
   p->total = o;
 }
 
@@ -535,30 +548,54 @@ mgb_status mgb_vocab_ce_fwd_bwd(const mgb_ce_desc* desc, const void* hidden, con
   float* t = at<float>(ws, p.t);
   float* lse_buf = lse ? lse : at<float>(ws, p.lse);
   float* dh_acc = at<float>(ws, p.dh);
+  float* bl = at<float>(ws, p.bl);
   const bf16* E = static_cast<const bf16*>(emb);
-  for (int c = 0; c < p.n_chunks; ++c) {
+  const bool fused = desc->mode == MGB_CE_FUSED;
+  // ---- forward: per-chunk partials, then the combine
+  if (fused && T > 0 && cudaMemsetAsync(t, 0, sizeof(float) * T, st) != cudaSuccess)
+    return MGB_ERR_CUDA;
+  for (int c = 0, part = 0; c < p.n_chunks; ++c) {
     const int v0 = c * C, Cc = (V - v0) < C ? (V - v0) : C;
-    GemmArgs g = mk_gemm(MGB_BF16, T, Cc, H, 0, hidden, H, 0, E + (size_t)v0 * H, H, EPI_STORE,
-                         logits, C);
-    // the target logit is taken in float32 from the accumulator, not from
-    // the bf16 logits the streaming pass reads
-    g.tgt = targets; g.tgt_v0 = v0; g.tgt_out = t + (size_t)c * T;
-    g.prof_kind = PROF_GEMM_CE_LOGITS;
-    MGB_TRY(gemm_launch(g, st));
-    MGB_TRY(ce_stats_launch(T, Cc, v0, logits, C, targets, m + (size_t)c * T, s + (size_t)c * T,
-                            t + (size_t)c * T, st));
+    if (fused) {
+      // (max, sum exp) per token and 128 columns straight from the accumulator
+      GemmArgs g = mk_gemm(MGB_BF16, T, Cc, H, 0, hidden, H, 0, E + (size_t)v0 * H, H,
+                           EPI_CE_STATS, m + (size_t)part * T, 8);
+      g.C2 = s + (size_t)part * T; g.ldc2 = 8;
+      g.tgt = targets; g.tgt_v0 = v0; g.tgt_out = t;
+      g.prof_kind = PROF_GEMM_CE_LOGITS;
+      MGB_TRY(gemm_launch(g, st));
+      part += (Cc + 127) / 128;
+    } else {
+      GemmArgs g = mk_gemm(MGB_BF16, T, Cc, H, 0, hidden, H, 0, E + (size_t)v0 * H, H, EPI_STORE,
+                           logits, C);
+      // the target logit is taken in float32 from the accumulator, not from
+      // the bf16 logits the streaming pass reads
+      g.tgt = targets; g.tgt_v0 = v0; g.tgt_out = t + (size_t)c * T;
+      g.prof_kind = PROF_GEMM_CE_LOGITS;
+      MGB_TRY(gemm_launch(g, st));
+      MGB_TRY(ce_stats_launch(T, Cc, v0, logits, C, targets, m + (size_t)c * T, s + (size_t)c * T,
+                              t + (size_t)c * T, st));
+    }
   }
-  MGB_TRY(ce_combine_launch(T, p.n_chunks, m, s, t, lse_buf, loss_per_token, loss_mean, st));
+  MGB_TRY(ce_combine_launch(T, p.n_parts, m, s, p.n_t, t, lse_buf, loss_per_token, loss_mean, bl,
+                            p.n_parts > kCeSplits ? at<float>(ws, p.split) : nullptr, st));
   if (!d_hidden && !d_emb) return MGB_OK;
+  // ---- backward: per chunk, G then its two GEMMs
   for (int c = 0; c < p.n_chunks; ++c) {
     const int v0 = c * C, Cc = (V - v0) < C ? (V - v0) : C;
-    {
+    if (fused) {
+      GemmArgs g = mk_gemm(MGB_BF16, T, Cc, H, 0, hidden, H, 0, E + (size_t)v0 * H, H,
+                           EPI_CE_GRAD, logits, C);
+      g.tgt = targets; g.tgt_v0 = v0; g.ce_lse = lse_buf; g.ce_scale = desc->grad_scale;
+      g.prof_kind = PROF_GEMM_CE_LOGITS;
+      MGB_TRY(gemm_launch(g, st));
+    } else {
       GemmArgs g = mk_gemm(MGB_BF16, T, Cc, H, 0, hidden, H, 0, E + (size_t)v0 * H, H, EPI_STORE,
                            logits, C);
       g.prof_kind = PROF_GEMM_CE_LOGITS;
       MGB_TRY(gemm_launch(g, st));
+      MGB_TRY(ce_grad_launch(T, Cc, v0, logits, C, targets, lse_buf, desc->grad_scale, st));
     }
-    MGB_TRY(ce_grad_launch(T, Cc, v0, logits, C, targets, lse_buf, desc->grad_scale, st));
     if (d_hidden) {
       GemmArgs g = mk_gemm(MGB_BF16, T, H, Cc, 0, logits, C, 1, E + (size_t)v0 * H, H, EPI_F32,
                            dh_acc, H);

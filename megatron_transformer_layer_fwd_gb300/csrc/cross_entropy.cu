@@ -12,8 +12,10 @@
 //   ce_stats   one block per token row of a [T, C] bf16 logits chunk: a single
 //              pass of 16-byte loads with a running (max, sum) pair per thread
 //              (rescaled when the max grows), merged across the block.
-//   ce_combine one block: chunk partials -> LSE, per-token loss, mean loss
-//              (fixed-order reduction, deterministic).
+//   ce_combine one thread per token: partials -> LSE, per-token loss; block
+//              sums of the loss then summed in fixed order (deterministic).
+// The same combine serves the partials the logits GEMM's epilogue writes when
+// the statistics are fused into it (one partial per 128-column group).
 //   ce_grad    one block per row: rewrites the logits chunk in place with G.
 #include "common.cuh"
 #include "internal.h"
@@ -111,35 +113,61 @@ __global__ void __launch_bounds__(CE_THREADS) ce_stats_kernel(int T, int C, int 
   }
 }
 
-__global__ void __launch_bounds__(1024) ce_combine_kernel(int T, int n_chunks, const float* m,
-                                                          const float* s, const float* t,
-                                                          float* lse, float* loss,
-                                                          float* loss_mean) {
-  float part = 0.0f;
-  for (int i = threadIdx.x; i < T; i += blockDim.x) {
+// One thread per token: merge its n_parts (max, sum) partials and n_t target
+// logits; each block writes the sum of its tokens' losses (fixed order).
+__global__ void __launch_bounds__(256) ce_combine_kernel(int T, int n_parts, const float* m,
+                                                         const float* s, int n_t, const float* t,
+                                                         float* lse, float* loss,
+                                                         float* block_loss) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  float li = 0.0f;
+  if (i < T) {
     float M = -INFINITY;
-    for (int c = 0; c < n_chunks; ++c) M = fmaxf(M, m[(int64_t)c * T + i]);
+    for (int c = 0; c < n_parts; ++c) M = fmaxf(M, m[(int64_t)c * T + i]);
     float S = 0.0f, tl = 0.0f;
-    for (int c = 0; c < n_chunks; ++c) {
-      S += s[(int64_t)c * T + i] * expf(m[(int64_t)c * T + i] - M);
-      tl += t[(int64_t)c * T + i];
-    }
+    for (int c = 0; c < n_parts; ++c) S += s[(int64_t)c * T + i] * expf(m[(int64_t)c * T + i] - M);
+    for (int c = 0; c < n_t; ++c) tl += t[(int64_t)c * T + i];
     const float L = M + logf(S);
     lse[i] = L;
-    const float li = L - tl;
+    li = L - tl;
     if (loss) loss[i] = li;
-    part += li;
   }
-  __shared__ float red[32];
+  __shared__ float red[8];
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
-  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = part;
+  for (int o = 16; o > 0; o >>= 1) li += __shfl_xor_sync(0xffffffffu, li, o);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = li;
   __syncthreads();
   if (threadIdx.x == 0) {
     float tot = 0.0f;
-    for (int w = 0; w < (int)(blockDim.x >> 5); ++w) tot += red[w];
-    if (loss_mean) *loss_mean = T > 0 ? tot / T : 0.0f;
+    for (int w = 0; w < 8; ++w) tot += red[w];
+    block_loss[blockIdx.x] = tot;
   }
+}
+
+// First stage for many partials: split k of blockIdx.y merges partials
+// [k*per, (k+1)*per) of each token (natural-log units) into one pair.
+__global__ void __launch_bounds__(256) ce_merge_split_kernel(int T, int n_parts, int per,
+                                                             const float* m, const float* s,
+                                                             float* m2, float* s2) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= T) return;
+  const int c0 = blockIdx.y * per, c1 = min(n_parts, c0 + per);
+  float M = -INFINITY;
+  for (int c = c0; c < c1; ++c) M = fmaxf(M, m[(int64_t)c * T + i]);
+  float S = 0.0f;
+  if (M != -INFINITY)
+    for (int c = c0; c < c1; ++c) S += s[(int64_t)c * T + i] * expf(m[(int64_t)c * T + i] - M);
+  m2[(int64_t)blockIdx.y * T + i] = M;
+  s2[(int64_t)blockIdx.y * T + i] = S;
+}
+
+// loss_mean = sum of the block sums (one warp, fixed order) / T
+__global__ void ce_mean_kernel(int nb, int T, const float* block_loss, float* loss_mean) {
+  float v = 0.0f;
+  for (int b = threadIdx.x; b < nb; b += 32) v += block_loss[b];
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  if (threadIdx.x == 0 && loss_mean) *loss_mean = T > 0 ? v / T : 0.0f;
 }
 
 __global__ void __launch_bounds__(CE_THREADS) ce_grad_kernel(int T, int C, int v0,
@@ -181,10 +209,26 @@ mgb_status ce_stats_launch(int T, int C, int v0, const void* logits, int64_t ldl
   return cudaGetLastError() == cudaSuccess ? MGB_OK : MGB_ERR_CUDA;
 }
 
-mgb_status ce_combine_launch(int T, int n_chunks, const float* m, const float* s, const float* t,
-                             float* lse, float* loss, float* loss_mean, cudaStream_t st) {
-  LaunchScope scope(PROF_CE_COMBINE, st);
-  ce_combine_kernel<<<1, 1024, 0, st>>>(T, n_chunks, m, s, t, lse, loss, loss_mean);
+mgb_status ce_combine_launch(int T, int n_parts, const float* m, const float* s, int n_t,
+                             const float* t, float* lse, float* loss, float* loss_mean,
+                             float* block_loss, float* split, cudaStream_t st) {
+  const int nb = ce_combine_blocks(T);
+  const bool two = n_parts > kCeSplits && split != nullptr && nb > 0;
+  LaunchScope scope(PROF_CE_COMBINE, st, (nb > 0 ? 1 : 0) + 1 + (two ? 1 : 0));
+  if (two) {
+    // many partials (one per 128 vocab columns): merge them in kCeSplits
+    // parallel ranges first, then combine the per-range pairs
+    const int per = (n_parts + kCeSplits - 1) / kCeSplits;
+    float* m2 = split;
+    float* s2 = split + (size_t)kCeSplits * T;
+    ce_merge_split_kernel<<<dim3(nb, kCeSplits), 256, 0, st>>>(T, n_parts, per, m, s, m2, s2);
+    m = m2;
+    s = s2;
+    n_parts = kCeSplits;
+  }
+  if (nb > 0)
+    ce_combine_kernel<<<nb, 256, 0, st>>>(T, n_parts, m, s, n_t, t, lse, loss, block_loss);
+  ce_mean_kernel<<<1, 32, 0, st>>>(nb, T, block_loss, loss_mean);
   return cudaGetLastError() == cudaSuccess ? MGB_OK : MGB_ERR_CUDA;
 }
 

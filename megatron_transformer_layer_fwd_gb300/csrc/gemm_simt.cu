@@ -142,7 +142,14 @@ __global__ void swiglu_f32_kernel(int M, int F, int gb, const float* u, int64_t 
 mgb_status gemm_check(const GemmArgs& g) {
   if (g.M < 0 || g.N < 0 || g.K < 0) return MGB_ERR_INVALID_ARG;
   if (g.dtype != MGB_BF16 && g.dtype != MGB_F32) return MGB_ERR_INVALID_ARG;
-  if (g.epi < EPI_STORE || g.epi > EPI_F32) return MGB_ERR_INVALID_ARG;
+  if (g.epi < EPI_STORE || g.epi > EPI_CE_GRAD) return MGB_ERR_INVALID_ARG;
+  if (g.epi == EPI_CE_STATS || g.epi == EPI_CE_GRAD) {
+    // cross-entropy epilogues: bf16 operands only, per-row inputs present
+    if (g.dtype != MGB_BF16) return MGB_ERR_UNSUPPORTED;
+    if (g.epi == EPI_CE_STATS && g.M > 0 && g.N > 0 && g.C2 == nullptr) return MGB_ERR_INVALID_ARG;
+    if (g.epi == EPI_CE_GRAD && g.M > 0 && g.N > 0 && (g.tgt == nullptr || g.ce_lse == nullptr))
+      return MGB_ERR_INVALID_ARG;
+  }
   if ((g.M > 0 && g.N > 0) && (g.C == nullptr)) return MGB_ERR_INVALID_ARG;
   if (g.K > 0 && g.M > 0 && g.N > 0 && (g.A == nullptr || g.B == nullptr)) return MGB_ERR_INVALID_ARG;
   const int64_t a_inner = g.a_mn ? g.M : g.K, b_inner = g.b_mn ? g.N : g.K;
@@ -160,10 +167,13 @@ mgb_status gemm_check(const GemmArgs& g) {
   if (g.dtype == MGB_BF16) {
     // TMA: 16-byte aligned bases and row strides; 16-byte epilogue vectors.
     auto al = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
-    if (!al(g.A) || !al(g.B) || !al(g.C) || !al(g.C2) || !al(g.resid) || !al(g.aux) || !al(g.bias))
+    // (EPI_CE_STATS writes single floats to C and C2: any 4-byte alignment)
+    const bool vec_out = g.epi != EPI_CE_STATS;
+    if (!al(g.A) || !al(g.B) || (vec_out && (!al(g.C) || !al(g.C2))) || !al(g.resid) ||
+        !al(g.aux) || !al(g.bias))
       return MGB_ERR_MISALIGNED;
     if (g.lda % 8 || g.ldb % 8 || g.N % 8) return MGB_ERR_MISALIGNED;
-    const int64_t c_mult = g.epi == EPI_F32 ? 4 : 8;
+    const int64_t c_mult = g.epi == EPI_F32 ? 4 : g.epi == EPI_CE_STATS ? 1 : 8;
     if (g.ldc % c_mult || (g.C2 && g.ldc2 % 8) || (g.resid && g.ldr % 8) || (g.aux && g.ldaux % 8))
       return MGB_ERR_MISALIGNED;
     if (g.accumulate && g.epi != EPI_F32) return MGB_ERR_INVALID_ARG;

@@ -66,6 +66,8 @@ struct EpiParams {
   const int32_t* tgt;
   int tgt_v0;
   float* tgt_out;
+  const float* ce_lse;
+  float ce_scale;
 };
 
 template <int BN, int STAGES>
@@ -147,6 +149,76 @@ __device__ void epilogue_row(const EpiParams& p, uint32_t tmem_row, int row, int
         store8(c + nu + 8 * q, u + 8 * q);
         store8(c2 + na + 8 * q, a + 8 * q);
       }
+    }
+    return;
+  }
+  if (p.epi == EPI_CE_STATS) {
+    // per 128-column group: running (max, sum exp) of the float32 logits in
+    // the log2 domain (the sum rescaled when the max grows); no logits stored
+    int tcol = -1;
+    if (p.tgt != nullptr && row_ok) tcol = p.tgt[row] - p.tgt_v0 - n0;
+    float* pm = reinterpret_cast<float*>(p.C);
+    float* ps = reinterpret_cast<float*>(p.C2);
+    for (int h = 0; h < BN; h += 128) {
+      float mx = -INFINITY, sum = 0.0f;
+      for (int lc = h; lc < h + 128; lc += 32) {
+        float acc[32];
+        tmem_chunk(tmem_row + lc, p.alpha, have_acc, acc);
+        const int n = n0 + lc;
+        if (!row_ok || n >= p.N) continue;
+        const int tc = tcol - lc;
+        if (tc >= 0 && tc < 32 && n + tc < p.N) {
+          float v = 0.0f;
+#pragma unroll
+          for (int j = 0; j < 32; ++j) v = (j == tc) ? acc[j] : v;
+          p.tgt_out[row] = v;
+        }
+        float cm = -INFINITY;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          acc[j] = n + j < p.N ? acc[j] * 1.4426950408889634f : -INFINITY;
+          cm = fmaxf(cm, acc[j]);
+        }
+        if (cm > mx) {
+          sum = mx == -INFINITY ? 0.0f : sum * ex2_ftz(mx - cm);
+          mx = cm;
+        }
+#pragma unroll
+        for (int j = 0; j < 32; ++j) sum += ex2_ftz(acc[j] - mx);
+      }
+      const int n = n0 + h;
+      if (row_ok && n < p.N) {
+        const int64_t o = (int64_t)(n / 128) * p.M + row;
+        pm[o] = mx * 0.6931471805599453f;
+        ps[o] = sum;
+      }
+    }
+    return;
+  }
+  if (p.epi == EPI_CE_GRAD) {
+    // G = (softmax - onehot(target)) * scale from the float32 logits
+    int tcol = -1;
+    float l2 = 0.0f;
+    if (row_ok) {
+      tcol = p.tgt[row] - p.tgt_v0 - n0;
+      l2 = p.ce_lse[row] * 1.4426950408889634f;
+    }
+    for (int lc = 0; lc < BN; lc += 32) {
+      float acc[32];
+      tmem_chunk(tmem_row + lc, p.alpha, have_acc, acc);
+      const int n = n0 + lc;
+      if (!row_ok || n >= p.N) continue;
+      const int tc = tcol - lc;
+#pragma unroll
+      for (int j = 0; j < 32; ++j) {
+        float g = ex2_ftz(fmaf(acc[j], 1.4426950408889634f, -l2));
+        if (j == tc) g -= 1.0f;
+        acc[j] = g * p.ce_scale;
+      }
+      bf16* c = reinterpret_cast<bf16*>(p.C) + (int64_t)row * p.ldc + n;
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        if (n + 8 * q < p.N) store8(c + 8 * q, acc + 8 * q);
     }
     return;
   }
@@ -553,7 +625,9 @@ mgb_status gemm_tc_launch(const GemmArgs& g, cudaStream_t st) {
   ep.aux = reinterpret_cast<const bf16*>(g.aux); ep.ldaux = g.ldaux;
   ep.glu_block = g.glu_block; ep.accumulate = g.accumulate;
   ep.err = device_error_word();
-  ep.tgt = g.epi == EPI_STORE ? g.tgt : nullptr;
+  ep.tgt = (g.epi == EPI_STORE || g.epi == EPI_CE_STATS || g.epi == EPI_CE_GRAD) ? g.tgt : nullptr;
+  ep.ce_lse = g.ce_lse;
+  ep.ce_scale = g.ce_scale;
   ep.tgt_v0 = g.tgt_v0;
   ep.tgt_out = g.tgt_out;
   // Column tile: 256 unless the problem is too narrow to fill the GPU with it.

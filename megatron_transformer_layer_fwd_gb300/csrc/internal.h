@@ -17,6 +17,12 @@ enum EpiMode : int {
   EPI_DGELU = 4,        // C = acc * gelu'(aux)             (acc = da, aux = u)
   EPI_DSWIGLU = 5,      // C = interleaved [dgate | dup]     (acc = da, aux = u)
   EPI_F32 = 6,          // Cf = (accumulate ? Cf : 0) + acc (+ bias); optional C2 = bf16(Cf)
+  // vocab cross-entropy, logits in float32 straight from the accumulator:
+  EPI_CE_STATS = 7,     // no logits stored: per row and 128-column group g of the
+                        // N columns, C[g*M + row] = max (natural-log units) and
+                        // C2[g*M + row] = sum exp(acc - max) (both float32);
+                        // target capture as EPI_STORE
+  EPI_CE_GRAD = 8,      // C = bf16((exp(acc - ce_lse[row]) - [column = target]) * ce_scale)
 };
 
 struct GemmArgs {
@@ -40,6 +46,8 @@ struct GemmArgs {
   const int32_t* tgt = nullptr;
   int tgt_v0 = 0;
   float* tgt_out = nullptr;
+  const float* ce_lse = nullptr;  // EPI_CE_GRAD: LSE per row
+  float ce_scale = 1.0f;          // EPI_CE_GRAD: dL/dloss per token
 };
 
 // Validates operand geometry for the chosen path; returns MGB_OK or an error.
@@ -88,8 +96,16 @@ mgb_status attention_bwd_launch(const AttnArgs& a, cudaStream_t st);
 // Cross-entropy streaming kernels over one logits chunk [T, C] (row stride ldl).
 mgb_status ce_stats_launch(int T, int C, int v0, const void* logits, int64_t ldl,
                            const int32_t* targets, float* m, float* s, float* t, cudaStream_t st);
-mgb_status ce_combine_launch(int T, int n_chunks, const float* m, const float* s, const float* t,
-                             float* lse, float* loss, float* loss_mean, cudaStream_t st);
+// Merges n_parts (max, sum exp) partials per token ([n_parts][T] each) and
+// the target logits ([n_t][T], summed) into LSE, per-token loss and the mean
+// (fixed-order reduction through block_loss [ceil(T / 256)] scratch).
+// With more than kCeSplits partials, `split` ([2][kCeSplits][T] floats, or
+// null for the one-stage merge) holds the per-range pairs of a first stage.
+constexpr int kCeSplits = 32;
+mgb_status ce_combine_launch(int T, int n_parts, const float* m, const float* s, int n_t,
+                             const float* t, float* lse, float* loss, float* loss_mean,
+                             float* block_loss, float* split, cudaStream_t st);
+inline int ce_combine_blocks(int T) { return (T + 255) / 256; }
 mgb_status ce_grad_launch(int T, int C, int v0, void* logits, int64_t ldl, const int32_t* targets,
                           const float* lse, float scale, cudaStream_t st);
 

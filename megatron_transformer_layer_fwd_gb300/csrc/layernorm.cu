@@ -295,7 +295,18 @@ __global__ void colsum_kernel(int M, int N, const T* __restrict__ dY, int64_t ld
   const int rows_per = (M + gridDim.y - 1) / gridDim.y;
   const int r0 = blockIdx.y * rows_per, r1 = min(M, r0 + rows_per);
   if (n < N) {
-    for (int m = r0 + threadIdx.y; m < r1; m += 8) {
+    // four rows' loads in flight per thread before they are summed
+    int m = r0 + threadIdx.y;
+    for (; m + 24 < r1; m += 32) {
+      float v[4][VN];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) vload(dY + (int64_t)(m + 8 * u) * ld + n, v[u]);
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+#pragma unroll
+        for (int j = 0; j < VN; ++j) acc[j] += v[u][j];
+    }
+    for (; m < r1; m += 8) {
       float v[VN];
       vload(dY + (int64_t)m * ld + n, v);
 #pragma unroll

@@ -28,6 +28,7 @@ MGB_ERR_DEVICE_TIMEOUT = -7
 MGB_ERR_NOT_IMPLEMENTED = -8
 
 MGB_F32, MGB_BF16 = 0, 1
+MGB_CE_STREAM, MGB_CE_FUSED = 0, 1
 MGB_PRE_LN, MGB_POST_LN = 0, 1
 MGB_GELU_ERF, MGB_SWIGLU = 0, 1
 MGB_K_MAJOR, MGB_MN_MAJOR = 0, 1
@@ -58,7 +59,8 @@ class BlockGrads(ctypes.Structure):
 
 class CEDesc(ctypes.Structure):
     _fields_ = [("tokens", ctypes.c_int32), ("hidden", ctypes.c_int32), ("vocab", ctypes.c_int32),
-                ("chunk", ctypes.c_int32), ("dtype", ctypes.c_int32), ("grad_scale", ctypes.c_float)]
+                ("chunk", ctypes.c_int32), ("dtype", ctypes.c_int32), ("grad_scale", ctypes.c_float),
+                ("mode", ctypes.c_int32)]
 
 
 class GemmDesc(ctypes.Structure):
@@ -202,9 +204,10 @@ def mgb_block_bwd(desc: BlockDesc, weights: dict, x, dy, saved, dx, grads: dict,
            "mgb_block_bwd")
 
 
-def ce_desc(tokens: int, hidden: int, vocab: int, chunk: int, grad_scale: float) -> CEDesc:
+def ce_desc(tokens: int, hidden: int, vocab: int, chunk: int, grad_scale: float,
+            mode: int = MGB_CE_FUSED) -> CEDesc:
     return CEDesc(tokens=tokens, hidden=hidden, vocab=vocab, chunk=chunk, dtype=MGB_BF16,
-                  grad_scale=grad_scale)
+                  grad_scale=grad_scale, mode=mode)
 
 
 def mgb_vocab_ce_sizes(desc: CEDesc) -> int:

@@ -56,10 +56,10 @@ class CERunner:
 
     def __init__(self, tokens: int, hidden: int, vocab: int, chunk: int, hidden_t: torch.Tensor,
                  emb_t: torch.Tensor, targets_t: torch.Tensor, grad_scale: float | None = None,
-                 want_grads: bool = True):
+                 want_grads: bool = True, mode: int = mgb.MGB_CE_FUSED):
         dev = hidden_t.device
         self.desc = mgb.ce_desc(tokens, hidden, vocab, chunk,
-                                grad_scale if grad_scale is not None else 1.0 / max(tokens, 1))
+                                grad_scale if grad_scale is not None else 1.0 / max(tokens, 1), mode)
         self.hidden, self.emb, self.targets = hidden_t, emb_t, targets_t
         self.ws = torch.empty(max(mgb.mgb_vocab_ce_sizes(self.desc), 16), dtype=torch.uint8, device=dev)
         self.loss = torch.empty(max(tokens, 1), dtype=torch.float32, device=dev)

@@ -15,19 +15,26 @@ from tests.util import CE_LOSS_ABS, rel_l2, to_np
 pytestmark = pytest.mark.gpu
 
 
-def _runner(shape, inp):
+MODES = [mgb.MGB_CE_STREAM, mgb.MGB_CE_FUSED]
+
+
+def _runner(shape, inp, mode):
     h = to_device(inp["hidden"], torch.bfloat16)
     e = to_device(inp["emb"], torch.bfloat16)
     t = torch.from_numpy(inp["targets"]).to("cuda")
-    return CERunner(shape.tokens, shape.hidden, shape.vocab, shape.chunk, h, e, t)
+    return CERunner(shape.tokens, shape.hidden, shape.vocab, shape.chunk, h, e, t, mode=mode)
 
 
+@pytest.mark.parametrize("mode", MODES)
 @pytest.mark.parametrize("T,H,V,C", [(300, 256, 1000, 136), (256, 128, 2048, 2048), (130, 64, 520, 64),
                                      (512, 1024, 8192, 1000)])
-def test_ce_small_full_parity(mgb_lib, T, H, V, C):
+def test_ce_small_full_parity(mgb_lib, T, H, V, C, mode):
+    """Both places for the statistics and the gradient (streaming kernels over
+    stored logits, or the logits GEMM's epilogue): ragged chunks, chunks
+    narrower than one 128-column group, one chunk for the whole vocabulary."""
     shape = CEShape(T, H, V, C)
     inp = ce_inputs(shape, seed=5)
-    r = _runner(shape, inp)
+    r = _runner(shape, inp, mode)
     r.run()
     assert mgb.mgb_device_status() == mgb.MGB_OK
     loss, lse, mean, _ = oracle.ce_chunked(inp["hidden"], inp["emb"], inp["targets"], C)
@@ -39,26 +46,28 @@ def test_ce_small_full_parity(mgb_lib, T, H, V, C):
     assert rel_l2(to_np(r.d_emb), de) < 2e-2
 
 
-def test_ce_forward_only(mgb_lib):
+@pytest.mark.parametrize("mode", MODES)
+def test_ce_forward_only(mgb_lib, mode):
     shape = CEShape(128, 64, 256, 96)
     inp = ce_inputs(shape, seed=1)
     h = to_device(inp["hidden"], torch.bfloat16)
     e = to_device(inp["emb"], torch.bfloat16)
     t = torch.from_numpy(inp["targets"]).to("cuda")
-    r = CERunner(128, 64, 256, 96, h, e, t, want_grads=False)
+    r = CERunner(128, 64, 256, 96, h, e, t, want_grads=False, mode=mode)
     r.run()
     loss, _, _, _ = oracle.ce_chunked(inp["hidden"], inp["emb"], inp["targets"], 96)
     assert np.abs(to_np(r.loss) - loss).max() < CE_LOSS_ABS
 
 
 @pytest.mark.slow
-def test_ce_full_size_sampled(mgb_lib):
+@pytest.mark.parametrize("mode", MODES)
+def test_ce_full_size_sampled(mgb_lib, mode):
     """Full tied-embedding CE workload: sampled tokens' loss / LSE / d_hidden
     rows against the oracle one row at a time; the mean against the per-token
     losses; d_emb column sums vanish (grad rows sum to 0)."""
     shape = CE_WORKLOADS["bf16_ce_t8192h4096v128256"]
     inp = ce_inputs(shape, seed=0)
-    r = _runner(shape, inp)
+    r = _runner(shape, inp, mode)
     r.run()
     assert mgb.mgb_device_status() == mgb.MGB_OK
     rows = np.random.default_rng(0).choice(shape.tokens, 48, replace=False)
@@ -74,3 +83,20 @@ def test_ce_full_size_sampled(mgb_lib):
     de = r.d_emb.double()
     col = de.sum(dim=0)
     assert float(col.norm() / de.norm()) < 2e-2
+
+
+def test_ce_modes_agree_and_are_deterministic(mgb_lib):
+    """The two modes agree to float32 rounding, and each repeats bit for bit."""
+    shape = CEShape(384, 256, 2000, 704)
+    inp = ce_inputs(shape, seed=9)
+    outs = []
+    for mode in MODES:
+        r = _runner(shape, inp, mode)
+        r.run()
+        first = (r.loss.clone(), r.d_hidden.clone(), r.d_emb.clone())
+        r.run()
+        assert torch.equal(first[0], r.loss) and torch.equal(first[1], r.d_hidden)
+        assert torch.equal(first[2], r.d_emb)
+        outs.append(first)
+    assert float((outs[0][0] - outs[1][0]).abs().max()) < CE_LOSS_ABS
+    assert rel_l2(to_np(outs[0][1]), to_np(outs[1][1])) < 2e-2
