@@ -22,8 +22,10 @@ Sources (web pages on the subject, cited by title and section):
     section 1 (MLP column -> row, SwiGLU gate/up kept together by an
     interleaved layout), section 2 (attention split by head, fused
     linear_qkv of width q_proj + 2*kv_proj, GQA, row-parallel linear_proj),
-    section 4 (vocab-parallel cross-entropy from per-shard max, target logit
-    and sum-exp partials; backward softmax - onehot).
+    section 3 (vocab-parallel embedding: masked lookup per vocab shard,
+    summed over shards; tied input/output table), section 4 (vocab-parallel
+    cross-entropy from per-shard max, target logit and sum-exp partials;
+    backward softmax - onehot).
   * "Megatron-LM" notes, split strategy section: attention cost grows with
     batch*seq^2*heads*head_dim.
 
@@ -37,6 +39,7 @@ from .activations import gelu, gelu_grad, silu, silu_grad, swiglu_fwd, swiglu_bw
 from .attention import attention_fwd, attention_bwd
 from .layer import block_fwd, block_bwd, block_fwd_rows
 from .cross_entropy import ce_full, ce_chunked, ce_grads, ce_rows
+from .embedding import embedding_fwd, embedding_bwd
 from . import shard
 
 __all__ = [
