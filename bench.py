@@ -488,6 +488,35 @@ def run_case(args):
                               "tflop": round(f / 1e12, 4), "tflops": round(f / (ms / 1e3) / 1e12, 1),
                               "kernel_ms": prof}), flush=True)
         return
+    if args.case == "embedding":
+        # the input-side lookup of the tied table (vocab-parallel embedding, one
+        # shard = the whole vocabulary) at the CE workload's sizes; ids drawn
+        # like the CE targets (uniform); backward accumulated onto the table's
+        # gradient (the tied form)
+        ce = CE_WORKLOADS[CE]
+        T, H, V = ce.tokens, ce.hidden, ce.vocab
+        g = torch.Generator(device="cuda").manual_seed(0)
+        ids = torch.randint(0, V, (T,), device="cuda", generator=g, dtype=torch.int32)
+        E = torch.randn((V, H), device="cuda", generator=g).to(torch.bfloat16)
+        out = torch.empty((T, H), device="cuda", dtype=torch.bfloat16)
+        dout = torch.randn((T, H), device="cuda", generator=g).to(torch.bfloat16)
+        dE = torch.zeros((V, H), device="cuda", dtype=torch.bfloat16)
+        ws = torch.empty(mgb.mgb_embedding_bwd_ws_bytes(T, 0, V), dtype=torch.uint8, device="cuda")
+        uniq = int(torch.unique(ids).numel())
+        fwd_bytes = 2 * T * H * 2                         # rows read + out written
+        bwd_bytes = T * H * 2 + 2 * uniq * H * 2 + 16 * T  # dout, touched rows in/out, ids+lists
+        for name, fn, nb in (
+                ("embedding_fwd", lambda: mgb.mgb_embedding_fwd(T, H, 0, V, mgb.MGB_BF16, ids, E, out),
+                 fwd_bytes),
+                ("embedding_bwd_accumulate",
+                 lambda: mgb.mgb_embedding_bwd(T, H, 0, V, mgb.MGB_BF16, ids, dout, dE, 1, ws), bwd_bytes)):
+            ms, prof = _time_loop(fn, args.steps, args.warmup, st)
+            gbs = nb / (ms / 1e3) / 1e9
+            print(json.dumps({"case": name, "tokens": T, "hidden": H, "vocab": V, "unique_ids": uniq,
+                              "ms": round(ms, 4), "algorithmic_bytes": nb, "gbs": round(gbs, 1),
+                              "frac_of_hbm": round(gbs / peaks["hbm_gbs"], 4), "kernel_ms": prof}),
+                  flush=True)
+        return
     if args.case == "ce":
         ce = CE_WORKLOADS[CE]
         cin = ce_inputs(ce, seed=0)
@@ -522,7 +551,7 @@ def main():
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--case", default="step",
-                    choices=("step", "layer", "sweep", "ce", "gemm", "attention"),
+                    choices=("step", "layer", "sweep", "ce", "gemm", "attention", "embedding"),
                     help="step (default, the driver's line) or a sub-path / single kernel")
     ap.add_argument("--mnk", type=int, nargs=3, default=(8192, 22016, 4096))
     ap.add_argument("--ce-mode", default="both", choices=("both", "stream", "fused"),

@@ -246,6 +246,36 @@ mgb_status mgb_attention_fwd(int32_t batch, int32_t seq, int32_t n_q_heads, int3
                              const void* q, const void* k, const void* v, int64_t ld_q,
                              int64_t ld_kv, void* o, float* lse, void* stream);
 
+/* Vocab-parallel embedding lookup [P2 section 3]: the table's rows [v0, v1)
+ * are held as emb_shard [(v1 - v0), hidden] (row-major, the vocab shard of a
+ * tensor-parallel rank; v0 = 0, v1 = vocab for the whole table). For each of
+ * `tokens` ids (device int32): out[t] = emb_shard[ids[t] - v0] when
+ * v0 <= ids[t] < v1, else a zero row - the masked lookup whose sum over the
+ * shards is the full lookup. dtype MGB_BF16 or MGB_F32 for the table and out
+ * (16-byte aligned, hidden a multiple of 8 / 4 elements); the copy is exact.
+ * Errors: MGB_ERR_INVALID_ARG (sizes, v0 >= v1, NULL), MGB_ERR_MISALIGNED,
+ * all before any launch. */
+mgb_status mgb_embedding_fwd(int32_t tokens, int32_t hidden, int32_t v0, int32_t v1, int32_t dtype,
+                             const int32_t* ids, const void* emb_shard, void* out, void* stream);
+
+/* Bytes of the workspace of mgb_embedding_bwd (0 for invalid sizes). No
+ * counterpart on the pages: it sizes the buffer below. */
+size_t mgb_embedding_bwd_ws_bytes(int32_t tokens, int32_t v0, int32_t v1);
+
+/* Backward of the lookup (its adjoint) [P2 section 3]: for every shard row v,
+ * d_emb_shard[v - v0] = (accumulate ? d_emb_shard[v - v0] : 0) + the sum over
+ * the tokens t with ids[t] = v of d_out[t] [tokens, hidden]. accumulate = 1
+ * adds onto the existing contents, e.g. the output embedding's gradient from
+ * mgb_vocab_ce_fwd_bwd when the input and output tables are tied; rows no
+ * token hits are then left untouched (accumulate = 0 writes them as zeros).
+ * Each row's tokens are summed in token order in float32 (deterministic, no
+ * floating-point atomics), then rounded to dtype. `ws` (16-byte aligned,
+ * caller-owned, at least mgb_embedding_bwd_ws_bytes) holds the per-row token
+ * lists. Errors as mgb_embedding_fwd, plus MGB_ERR_WORKSPACE_TOO_SMALL. */
+mgb_status mgb_embedding_bwd(int32_t tokens, int32_t hidden, int32_t v0, int32_t v1, int32_t dtype,
+                             const int32_t* ids, const void* d_out, void* d_emb_shard,
+                             int32_t accumulate, void* ws, size_t ws_bytes, void* stream);
+
 /* Bytes of the workspace mgb_attention_bwd needs: two float32 planes
  * [batch * n_q_heads][seq rounded up to a multiple of 128] (LSE * log2(e) and
  * delta = rowsum(dO * O), per query; the padding holds +inf and 0). No

@@ -691,6 +691,46 @@ mgb_status mgb_attention_fwd(int32_t batch, int32_t seq, int32_t n_q_heads, int3
   return attention_fwd_launch(a, as_stream(stream));
 }
 
+// `table` is the shard's rows (or their gradient); `per_token` the [tokens,
+// hidden] side, which (like ids) may be NULL when tokens == 0.
+static mgb_status check_embedding(int32_t tokens, int32_t hidden, int32_t v0, int32_t v1,
+                                  int32_t dtype, const void* ids, const void* table,
+                                  const void* per_token) {
+  if (fault_injected()) return MGB_ERR_INVALID_ARG;
+  if (tokens < 0 || hidden < 1 || v0 < 0 || v1 <= v0) return MGB_ERR_INVALID_ARG;
+  if (dtype != MGB_BF16 && dtype != MGB_F32) return MGB_ERR_INVALID_ARG;
+  if (!table || (tokens > 0 && (!ids || !per_token))) return MGB_ERR_INVALID_ARG;
+  if (hidden % (dtype == MGB_BF16 ? 8 : 4)) return MGB_ERR_MISALIGNED;
+  if (!aligned16(table) || !aligned16(per_token) || (reinterpret_cast<uintptr_t>(ids) & 3u))
+    return MGB_ERR_MISALIGNED;
+  return MGB_OK;
+}
+
+mgb_status mgb_embedding_fwd(int32_t tokens, int32_t hidden, int32_t v0, int32_t v1, int32_t dtype,
+                             const int32_t* ids, const void* emb_shard, void* out, void* stream) {
+  MGB_TRY(check_embedding(tokens, hidden, v0, v1, dtype, ids, emb_shard, out));
+  MGB_TRY(check_arch());
+  return embedding_fwd_launch(tokens, hidden, dtype, v0, v1, ids, emb_shard, out,
+                              as_stream(stream));
+}
+
+size_t mgb_embedding_bwd_ws_bytes(int32_t tokens, int32_t v0, int32_t v1) {
+  if (tokens < 0 || v0 < 0 || v1 <= v0) return 0;
+  return embedding_bwd_ws(tokens, v0, v1);
+}
+
+mgb_status mgb_embedding_bwd(int32_t tokens, int32_t hidden, int32_t v0, int32_t v1, int32_t dtype,
+                             const int32_t* ids, const void* d_out, void* d_emb_shard,
+                             int32_t accumulate, void* ws, size_t ws_bytes, void* stream) {
+  MGB_TRY(check_embedding(tokens, hidden, v0, v1, dtype, ids, d_emb_shard, d_out));
+  if (ws == nullptr) return MGB_ERR_INVALID_ARG;
+  if (!aligned16(ws)) return MGB_ERR_MISALIGNED;
+  if (ws_bytes < embedding_bwd_ws(tokens, v0, v1)) return MGB_ERR_WORKSPACE_TOO_SMALL;
+  MGB_TRY(check_arch());
+  return embedding_bwd_launch(tokens, hidden, dtype, v0, v1, ids, d_out, d_emb_shard,
+                              accumulate ? 1 : 0, ws, as_stream(stream));
+}
+
 size_t mgb_attention_bwd_ws_bytes(int32_t batch, int32_t seq, int32_t n_q_heads) {
   if (batch < 0 || seq < 0 || n_q_heads < 0) return 0;
   return attn_bwd_ws_bytes(batch, seq, n_q_heads);

@@ -109,6 +109,14 @@ inline int ce_combine_blocks(int T) { return (T + 255) / 256; }
 mgb_status ce_grad_launch(int T, int C, int v0, void* logits, int64_t ldl, const int32_t* targets,
                           const float* lse, float scale, cudaStream_t st);
 
+// Vocab-parallel embedding (shard rows [v0, v1)); layouts as mgb_embedding_fwd/bwd.
+size_t embedding_bwd_ws(int T, int v0, int v1);
+mgb_status embedding_fwd_launch(int T, int H, int dtype, int v0, int v1, const int32_t* ids,
+                                const void* emb, void* out, cudaStream_t st);
+mgb_status embedding_bwd_launch(int T, int H, int dtype, int v0, int v1, const int32_t* ids,
+                                const void* dout, void* d_emb, int accumulate, void* ws,
+                                cudaStream_t st);
+
 // Streaming multiprocessors of the current device (cached per device).
 int device_sm_count();
 
@@ -119,7 +127,7 @@ int* device_error_word();
 enum ProfKind : int {
   PROF_GEMM_FWD = 0, PROF_GEMM_DGRAD, PROF_GEMM_WGRAD, PROF_GEMM_F32, PROF_ATTN_FWD,
   PROF_ATTN_BWD, PROF_LN_FWD, PROF_LN_BWD, PROF_COLSUM, PROF_CE_STATS, PROF_CE_COMBINE,
-  PROF_CE_GRAD, PROF_GEMM_CE_LOGITS, PROF_KINDS
+  PROF_CE_GRAD, PROF_GEMM_CE_LOGITS, PROF_EMBEDDING, PROF_KINDS
 };
 
 // Counts `launches` kernel launches and, when profiling is on, brackets them

@@ -100,6 +100,8 @@ def load() -> ctypes.CDLL:
             "mgb_attention_fwd": [I32, I32, I32, I32, I32, I32, I32, P, P, P, I64, I64, P, P, P],
             "mgb_attention_bwd": [I32, I32, I32, I32, I32, I32, I32, P, P, P, I64, I64, P, P, P,
                                   I64, P, P, P, I64, I64, P, SZ, P],
+            "mgb_embedding_fwd": [I32, I32, I32, I32, I32, P, P, P, P],
+            "mgb_embedding_bwd": [I32, I32, I32, I32, I32, P, P, P, I32, P, SZ, P],
             "mgb_device_status": [P],
             "mgb_selftest_wait_timeout": [U64, P],
         }
@@ -115,6 +117,8 @@ def load() -> ctypes.CDLL:
         lib.mgb_layernorm_bwd_ws_bytes.restype = SZ
         lib.mgb_attention_bwd_ws_bytes.argtypes = [I32, I32, I32]
         lib.mgb_attention_bwd_ws_bytes.restype = SZ
+        lib.mgb_embedding_bwd_ws_bytes.argtypes = [I32, I32, I32]
+        lib.mgb_embedding_bwd_ws_bytes.restype = SZ
         lib.mgb_launch_count.argtypes = []
         lib.mgb_launch_count.restype = ctypes.c_uint64
         lib.mgb_profile_enable.argtypes = [I32]
@@ -242,6 +246,23 @@ def mgb_layernorm_bwd_ws_bytes(rows: int, cols: int) -> int:
 
 def mgb_attention_bwd_ws_bytes(batch: int, seq: int, n_q_heads: int) -> int:
     return load().mgb_attention_bwd_ws_bytes(batch, seq, n_q_heads)
+
+
+def mgb_embedding_fwd(tokens, hidden, v0, v1, dtype, ids, emb_shard, out, stream=None) -> None:
+    _check(load().mgb_embedding_fwd(tokens, hidden, v0, v1, dtype, _ptr(ids), _ptr(emb_shard),
+                                    _ptr(out), _stream(stream)), "mgb_embedding_fwd")
+
+
+def mgb_embedding_bwd_ws_bytes(tokens: int, v0: int, v1: int) -> int:
+    return load().mgb_embedding_bwd_ws_bytes(tokens, v0, v1)
+
+
+def mgb_embedding_bwd(tokens, hidden, v0, v1, dtype, ids, d_out, d_emb_shard, accumulate, ws,
+                      stream=None) -> None:
+    _check(load().mgb_embedding_bwd(tokens, hidden, v0, v1, dtype, _ptr(ids), _ptr(d_out),
+                                    _ptr(d_emb_shard), int(accumulate), _ptr(ws),
+                                    ws.numel() * ws.element_size(), _stream(stream)),
+           "mgb_embedding_bwd")
 
 
 def mgb_layernorm_bwd(rows: int, cols: int, dtype: int, x, mean, rstd, gamma, dy, dres, dx, dgamma,

@@ -140,3 +140,22 @@ def test_attention_bwd_workspace_size(lib):
     s = lib.mgb_attention_bwd(1, 130, 4, 2, 64, 1, mgb.MGB_BF16, p, p, p, 512, 512, p, p, p, 256,
                               p, p, p, 512, 512, p, need - 16, None)
     assert s == mgb.MGB_ERR_WORKSPACE_TOO_SMALL
+
+
+def test_embedding_validation(lib):
+    p = 4096
+    # v0 >= v1, negative tokens, bad dtype: invalid before any launch
+    assert lib.mgb_embedding_fwd(4, 64, 5, 5, mgb.MGB_BF16, p, p, p, None) == mgb.MGB_ERR_INVALID_ARG
+    assert lib.mgb_embedding_fwd(-1, 64, 0, 5, mgb.MGB_BF16, p, p, p, None) == mgb.MGB_ERR_INVALID_ARG
+    assert lib.mgb_embedding_fwd(4, 64, 0, 5, 7, p, p, p, None) == mgb.MGB_ERR_INVALID_ARG
+    # hidden not a whole number of 16-byte vectors; misaligned table
+    assert lib.mgb_embedding_fwd(4, 60, 0, 5, mgb.MGB_BF16, p, p, p, None) == mgb.MGB_ERR_MISALIGNED
+    assert lib.mgb_embedding_fwd(4, 64, 0, 5, mgb.MGB_BF16, p, p + 8, p, None) == mgb.MGB_ERR_MISALIGNED
+    # tokens present but no ids
+    assert lib.mgb_embedding_fwd(4, 64, 0, 5, mgb.MGB_BF16, None, p, p, None) == mgb.MGB_ERR_INVALID_ARG
+    # backward workspace: token lists + row offsets
+    need = mgb.mgb_embedding_bwd_ws_bytes(100, 10, 60)
+    assert need >= 4 * (2 * 100 + 2 * 50 + 1)
+    assert mgb.mgb_embedding_bwd_ws_bytes(100, 10, 10) == 0
+    assert lib.mgb_embedding_bwd(100, 64, 10, 60, mgb.MGB_BF16, p, p, p, 1, p, need - 16,
+                                 None) == mgb.MGB_ERR_WORKSPACE_TOO_SMALL

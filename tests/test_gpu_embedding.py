@@ -1,0 +1,140 @@
+"""GPU parity of the vocab-parallel embedding lookup and its backward
+(mgb_embedding_fwd / mgb_embedding_bwd through the C ABI) against the float64
+oracle, and the tied-table round trip with the cross-entropy's gradient."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from megatron_transformer_layer_fwd_gb300 import mgb
+from megatron_transformer_layer_fwd_gb300.inputs import CEShape, ce_inputs, round_to_bf16
+from megatron_transformer_layer_fwd_gb300.runner import CERunner, to_device
+from tests.util import rel_l2, to_np
+
+pytestmark = pytest.mark.gpu
+RNG = np.random.default_rng(57)
+
+
+def _ids(T, V, repeats=False):
+    if repeats:  # a few very frequent ids plus a tail, as in text
+        return np.minimum((RNG.zipf(1.3, size=T) - 1), V - 1).astype(np.int32)
+    return RNG.integers(0, V, size=T).astype(np.int32)
+
+
+def _dev(a, td):
+    return torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).to("cuda", td)
+
+
+def _fwd(ids, E, v0, v1, td, dt):
+    T, H = ids.shape[0], E.shape[1]
+    out = torch.full((T, H), float("nan"), device="cuda", dtype=td)
+    mgb.mgb_embedding_fwd(T, H, v0, v1, dt, torch.from_numpy(ids).cuda(), _dev(E, td), out)
+    return out
+
+
+def _bwd(ids, dout, v0, v1, td, dt, init=None):
+    T, H = dout.shape
+    d_emb = _dev(init, td) if init is not None else torch.full((v1 - v0, H), float("nan"),
+                                                               device="cuda", dtype=td)
+    ws = torch.empty(mgb.mgb_embedding_bwd_ws_bytes(T, v0, v1), dtype=torch.uint8, device="cuda")
+    mgb.mgb_embedding_bwd(T, H, v0, v1, dt, torch.from_numpy(ids).cuda(), _dev(dout, td), d_emb,
+                          init is not None, ws)
+    return d_emb
+
+
+DT = [("bf16", torch.bfloat16, mgb.MGB_BF16, round_to_bf16, 1e-2),
+      ("f32", torch.float32, mgb.MGB_F32, lambda a: a.astype(np.float32).astype(np.float64), 1e-6)]
+
+
+@pytest.mark.parametrize("name,td,dt,rnd,tol", DT)
+@pytest.mark.parametrize("T,H,V", [(333, 64, 1000), (1024, 512, 300), (5, 8, 7)])
+def test_lookup_exact_and_shards_sum(mgb_lib, name, td, dt, rnd, tol, T, H, V):
+    ids = _ids(T, V, repeats=(V == 300))
+    E = rnd(RNG.standard_normal((V, H)))
+    full = _fwd(ids, E, 0, V, td, dt)
+    assert np.array_equal(to_np(full), oracle.embedding_fwd(ids, E, 0, V))
+    # three vocab shards, the last ragged: their outputs sum (exactly) to the full lookup
+    b = [0, V // 3, 2 * V // 3 + 1, V]
+    parts = [_fwd(ids, E[lo:hi], lo, hi, td, dt) for lo, hi in zip(b[:-1], b[1:])]
+    for (lo, hi), p in zip(zip(b[:-1], b[1:]), parts):
+        assert np.array_equal(to_np(p), oracle.embedding_fwd(ids, E[lo:hi], lo, hi))
+    assert torch.equal(sum(p.float() for p in parts), full.float())
+    assert mgb.mgb_device_status() == mgb.MGB_OK
+
+
+@pytest.mark.parametrize("name,td,dt,rnd,tol", DT)
+@pytest.mark.parametrize("T,H,V,v0,v1,rep", [(500, 64, 800, 0, 800, False), (2048, 256, 300, 0, 300, True),
+                                             (700, 128, 1000, 250, 613, True), (1, 8, 4, 0, 4, False)])
+def test_backward(mgb_lib, name, td, dt, rnd, tol, T, H, V, v0, v1, rep):
+    """Overwrite and accumulate; repeated ids; ids outside the shard."""
+    ids = _ids(T, V, repeats=rep)
+    dout = rnd(RNG.standard_normal((T, H)))
+    ref = oracle.embedding_bwd(ids, dout, v0, v1)
+    got = to_np(_bwd(ids, dout, v0, v1, td, dt))
+    assert rel_l2(got, ref) <= tol
+    untouched = np.setdiff1d(np.arange(v0, v1), ids) - v0
+    assert np.all(got[untouched] == 0)
+    init = rnd(RNG.standard_normal((v1 - v0, H)))
+    got = to_np(_bwd(ids, dout, v0, v1, td, dt, init=init))
+    assert rel_l2(got, init + ref) <= tol
+    assert np.array_equal(got[untouched], to_np(_dev(init, td))[untouched])
+    assert mgb.mgb_device_status() == mgb.MGB_OK
+
+
+def test_backward_deterministic(mgb_lib):
+    ids = _ids(4096, 500, repeats=True)
+    dout = round_to_bf16(RNG.standard_normal((4096, 256)))
+    a = _bwd(ids, dout, 0, 500, torch.bfloat16, mgb.MGB_BF16)
+    b = _bwd(ids, dout, 0, 500, torch.bfloat16, mgb.MGB_BF16)
+    assert torch.equal(a, b)
+
+
+def test_empty_batch(mgb_lib):
+    ids = np.zeros(0, dtype=np.int32)
+    d = _bwd(ids, np.zeros((0, 16)), 0, 10, torch.bfloat16, mgb.MGB_BF16)
+    assert float(d.float().abs().max()) == 0.0
+
+
+def test_tied_table_round_trip(mgb_lib):
+    """One table E for the input lookup and the output projection: the CE's
+    d_emb, then the lookup's backward accumulated onto it."""
+    shape = CEShape(256, 128, 2048, 704)
+    inp = ce_inputs(shape, seed=3)
+    h = to_device(inp["hidden"], torch.bfloat16)
+    e = to_device(inp["emb"], torch.bfloat16)
+    t = torch.from_numpy(inp["targets"]).to("cuda")
+    r = CERunner(shape.tokens, shape.hidden, shape.vocab, shape.chunk, h, e, t)
+    r.run()
+    ids = _ids(shape.tokens, shape.vocab, repeats=True)
+    dout = round_to_bf16(RNG.standard_normal((shape.tokens, shape.hidden)) * 1e-3)
+    ws = torch.empty(mgb.mgb_embedding_bwd_ws_bytes(shape.tokens, 0, shape.vocab), dtype=torch.uint8,
+                     device="cuda")
+    mgb.mgb_embedding_bwd(shape.tokens, shape.hidden, 0, shape.vocab, mgb.MGB_BF16,
+                          torch.from_numpy(ids).cuda(), _dev(dout, torch.bfloat16), r.d_emb, 1, ws)
+    _, lse, _, _ = oracle.ce_chunked(inp["hidden"], inp["emb"], inp["targets"], shape.chunk)
+    _, de = oracle.ce_grads(inp["hidden"], inp["emb"], inp["targets"], lse, 1.0 / shape.tokens)
+    ref = de + oracle.embedding_bwd(ids, dout, 0, shape.vocab)
+    assert rel_l2(to_np(r.d_emb), ref) < 2e-2
+    assert mgb.mgb_device_status() == mgb.MGB_OK
+
+
+@pytest.mark.slow
+def test_full_size_sampled(mgb_lib):
+    """8192 tokens over the 128256 x 4096 table: the lookup is compared whole;
+    the backward on windows of 64 rows around sampled ids."""
+    T, H, V = 8192, 4096, 128256
+    ids = _ids(T, V, repeats=True)
+    E = torch.randn((V, H), device="cuda").to(torch.bfloat16)
+    out = torch.empty((T, H), device="cuda", dtype=torch.bfloat16)
+    mgb.mgb_embedding_fwd(T, H, 0, V, mgb.MGB_BF16, torch.from_numpy(ids).cuda(), E, out)
+    assert torch.equal(out, E[torch.from_numpy(ids).long().cuda()])
+    dout = torch.randn((T, H), device="cuda").to(torch.bfloat16)
+    ws = torch.empty(mgb.mgb_embedding_bwd_ws_bytes(T, 0, V), dtype=torch.uint8, device="cuda")
+    d_emb = torch.empty((V, H), device="cuda", dtype=torch.bfloat16)
+    mgb.mgb_embedding_bwd(T, H, 0, V, mgb.MGB_BF16, torch.from_numpy(ids).cuda(), dout, d_emb, 0, ws)
+    dn = to_np(dout)
+    for v in np.unique(np.concatenate([ids[:3], [0, 1, V - 1]])):
+        lo = max(0, min(int(v) - 32, V - 64))
+        ref = oracle.embedding_bwd(ids, dn, lo, lo + 64)
+        assert rel_l2(to_np(d_emb[lo:lo + 64]), ref) < 1e-2
+    assert mgb.mgb_device_status() == mgb.MGB_OK
