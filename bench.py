@@ -430,6 +430,41 @@ def run_case(args):
         print(json.dumps({"case": "gemm", "mnk": [M, N, K], "ms": round(ms, 4), "tflops": round(tf, 1),
                           "frac_of_burst_peak": round(tf / peaks["bf16_tflops"], 4)}))
         return
+    if args.case == "gemm_layer":
+        # the layer's twelve GEMM shapes and operand layouts (forward, input
+        # gradient, weight gradient), each alone, beside torch.matmul (cuBLAS)
+        # on the same operands for scale
+        sh = WORKLOADS[LAYER]
+        T, H, Dq = sh.tokens, sh.hidden, sh.n_q_heads * sh.head_dim
+        Wqkv = (sh.n_q_heads + 2 * sh.n_kv_heads) * sh.head_dim
+        F = sh.ffn
+        W = 2 * F if sh.act == "swiglu" else F
+        cases = [("fwd_qkv", T, Wqkv, H, 0, 0), ("fwd_proj", T, H, Dq, 0, 0), ("fwd_fc1", T, W, H, 0, 0),
+                 ("fwd_fc2", T, H, F, 0, 0), ("dgrad_fc2", T, F, H, 0, 1), ("dgrad_fc1", T, H, W, 0, 1),
+                 ("dgrad_proj", T, Dq, H, 0, 1), ("dgrad_qkv", T, H, Wqkv, 0, 1),
+                 ("wgrad_fc2", H, F, T, 1, 1), ("wgrad_fc1", W, H, T, 1, 1), ("wgrad_proj", H, Dq, T, 1, 1),
+                 ("wgrad_qkv", Wqkv, H, T, 1, 1)]
+        tot_ms = tot_ref = tot_fl = 0.0
+        for name, M, N, K, am, bm in cases:
+            a = torch.randn(*((K, M) if am else (M, K)), device="cuda").to(torch.bfloat16)
+            b = torch.randn(*((K, N) if bm else (N, K)), device="cuda").to(torch.bfloat16)
+            c = torch.empty(M, N, device="cuda", dtype=torch.bfloat16)
+            d = mgb.GemmDesc(m=M, n=N, k=K, a_major=am, b_major=bm, lda=M if am else K,
+                             ldb=N if bm else K, ldc=N, dtype=mgb.MGB_BF16, c_f32=0, accumulate=0,
+                             alpha=1.0)
+            ms, _ = _time_loop(lambda: mgb.mgb_gemm(d, a, b, None, c), args.steps, args.warmup, st)
+            at = a.t() if am else a
+            bt = b if bm else b.t()
+            ref, _ = _time_loop(lambda: torch.matmul(at, bt, out=c), args.steps, args.warmup, st)
+            fl = 2.0 * M * N * K
+            tot_ms, tot_ref, tot_fl = tot_ms + ms, tot_ref + ref, tot_fl + fl
+            print(json.dumps({"case": name, "mnk": [M, N, K], "majors": [am, bm], "ms": round(ms, 4),
+                              "tflops": round(fl / ms / 1e9, 1), "cublas_ms": round(ref, 4),
+                              "cublas_tflops": round(fl / ref / 1e9, 1)}), flush=True)
+        print(json.dumps({"case": "gemm_layer_total", "ms": round(tot_ms, 4),
+                          "tflops": round(tot_fl / tot_ms / 1e9, 1), "cublas_ms": round(tot_ref, 4),
+                          "cublas_tflops": round(tot_fl / tot_ref / 1e9, 1)}), flush=True)
+        return
     if args.case in ("layer", "sweep"):
         names = [LAYER] if args.case == "layer" else [f"bf16_causal_b8s{s}h2048"
                                                       for s in (128, 256, 512, 1024, 2048)]
@@ -551,7 +586,8 @@ def main():
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--case", default="step",
-                    choices=("step", "layer", "sweep", "ce", "gemm", "attention", "embedding"),
+                    choices=("step", "layer", "sweep", "ce", "gemm", "gemm_layer", "attention",
+                             "embedding"),
                     help="step (default, the driver's line) or a sub-path / single kernel")
     ap.add_argument("--mnk", type=int, nargs=3, default=(8192, 22016, 4096))
     ap.add_argument("--ce-mode", default="both", choices=("both", "stream", "fused"),

@@ -120,7 +120,13 @@ mgb_status mgb_block_fwd(const mgb_block_desc* desc, const mgb_block_weights* w,
 /* Layer backward [P1 section 2 "end-to-end backward"]: given dy = dL/dy [T, H]
  * and the `saved` buffer of the matching forward (same x and weights), writes
  * dx = dL/dx [T, H] and every non-NULL gradient in `grads`. Attention
- * probabilities are recomputed from the saved log-sum-exp. */
+ * probabilities are recomputed from the saved log-sum-exp.
+ * Weight and bias gradients are computed on a second stream that the library
+ * owns (one per host thread and device), forked from and joined back into
+ * `stream` inside the call: all results are ordered on `stream` as usual. The
+ * first call on a thread and device creates that stream and its events; when
+ * the call is to be captured into a CUDA graph, make one call before the
+ * capture. */
 mgb_status mgb_block_bwd(const mgb_block_desc* desc, const mgb_block_weights* w,
                          const void* x, const void* dy, const void* saved, size_t saved_bytes,
                          void* dx, const mgb_block_grads* grads,

@@ -93,6 +93,68 @@ mgb_status check_arch() {
   return (major == 10 && minor == 3) ? MGB_OK : MGB_ERR_ARCH;
 }
 
+// A second, library-owned stream per (host thread, device) for work off a
+// call's critical path (weight and bias gradients), so that its kernels fill
+// the SMs the critical-path kernels leave idle in their last wave. fork()
+// makes the side stream wait for everything issued on the caller's stream so
+// far; join() (also run by the destructor, on every return path) makes the
+// caller's stream wait for the side stream. Events are reused: a wait takes
+// the event's state when it is enqueued. If the stream cannot be created the
+// side work runs on the caller's stream.
+class SideLane {
+ public:
+  explicit SideLane(cudaStream_t main) : main_(main), side_(main), ev_(nullptr) {
+    struct PerDevice {
+      cudaStream_t side = nullptr;
+      cudaEvent_t ev[kEvents] = {};
+      bool failed = false;
+    };
+    thread_local PerDevice per[16];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 16) return;
+    PerDevice& d = per[dev];
+    if (d.side == nullptr && !d.failed) {
+      bool ok = cudaStreamCreateWithFlags(&d.side, cudaStreamNonBlocking) == cudaSuccess;
+      for (int i = 0; ok && i < kEvents; ++i)
+        ok = cudaEventCreateWithFlags(&d.ev[i], cudaEventDisableTiming) == cudaSuccess;
+      if (!ok) {
+        d.failed = true;
+        d.side = nullptr;
+        cudaGetLastError();
+      }
+    }
+    if (d.side != nullptr) {
+      side_ = d.side;
+      ev_ = d.ev;
+    }
+  }
+  ~SideLane() { join(); }
+  cudaStream_t side() const { return side_; }
+  mgb_status fork() {
+    if (side_ == main_) return MGB_OK;
+    cudaEvent_t e = ev_[next_++ % (kEvents - 1)];
+    if (cudaEventRecord(e, main_) != cudaSuccess || cudaStreamWaitEvent(side_, e, 0) != cudaSuccess)
+      return MGB_ERR_CUDA;
+    forked_ = true;
+    return MGB_OK;
+  }
+  mgb_status join() {
+    if (!forked_) return MGB_OK;
+    forked_ = false;
+    cudaEvent_t e = ev_[kEvents - 1];
+    if (cudaEventRecord(e, side_) != cudaSuccess || cudaStreamWaitEvent(main_, e, 0) != cudaSuccess)
+      return MGB_ERR_CUDA;
+    return MGB_OK;
+  }
+
+ private:
+  static constexpr int kEvents = 8;
+  cudaStream_t main_, side_;
+  cudaEvent_t* ev_;
+  int next_ = 0;
+  bool forked_ = false;
+};
+
 struct Plan {
   int B, S, T, H, nq, nkv, d, F, W, Wqkv, Dq;
   size_t es;
@@ -395,6 +457,12 @@ mgb_status mgb_block_bwd(const mgb_block_desc* desc, const mgb_block_weights* w,
   float* cparts = at<float>(ws, p.w_cparts);
   float* lparts = at<float>(ws, p.w_lparts);
 
+  // The input-gradient chain (dgrad GEMMs, LayerNorm and attention backward)
+  // runs on the caller's stream; each weight gradient and bias column sum is
+  // issued on the side stream once its inputs exist there. Only the side
+  // stream uses cparts; only the caller's stream uses lparts.
+  SideLane lane(st);
+  cudaStream_t s2 = lane.side();
   // gradient at the fc2 residual sum (Pre: dy itself; Post: through LN2)
   const void* dr2 = dy;
   if (!p.pre) {
@@ -403,9 +471,10 @@ mgb_status mgb_block_bwd(const mgb_block_desc* desc, const mgb_block_weights* w,
     dr2 = d_r2;
   }
   // fc2: db2, dW2 = dr2^T a, du = (dr2 W2) * act'(u)
-  if (gr->b_2) MGB_TRY(colsum_launch(T, H, dt, dr2, H, gr->b_2, cparts, p.cparts, st));
+  MGB_TRY(lane.fork());
+  if (gr->b_2) MGB_TRY(colsum_launch(T, H, dt, dr2, H, gr->b_2, cparts, p.cparts, s2));
   if (gr->w_2)
-    MGB_TRY(gemm_launch(mk_gemm(dt, H, p.F, T, 1, dr2, H, 1, a, p.F, EPI_STORE, gr->w_2, p.F), st));
+    MGB_TRY(gemm_launch(mk_gemm(dt, H, p.F, T, 1, dr2, H, 1, a, p.F, EPI_STORE, gr->w_2, p.F), s2));
   {
     GemmArgs g = mk_gemm(dt, T, p.F, H, 0, dr2, H, 1, w->w_2, p.F,
                          p.swiglu ? EPI_DSWIGLU : EPI_DGELU, du, p.W);
@@ -413,9 +482,10 @@ mgb_status mgb_block_bwd(const mgb_block_desc* desc, const mgb_block_weights* w,
     MGB_TRY(gemm_launch(g, st));
   }
   // fc1: db1, dW1 = du^T f_in, d f_in = du W1
-  if (gr->b_1) MGB_TRY(colsum_launch(T, p.W, dt, du, p.W, gr->b_1, cparts, p.cparts, st));
+  MGB_TRY(lane.fork());
+  if (gr->b_1) MGB_TRY(colsum_launch(T, p.W, dt, du, p.W, gr->b_1, cparts, p.cparts, s2));
   if (gr->w_1)
-    MGB_TRY(gemm_launch(mk_gemm(dt, p.W, H, T, 1, du, p.W, 1, f_in, H, EPI_STORE, gr->w_1, H), st));
+    MGB_TRY(gemm_launch(mk_gemm(dt, p.W, H, T, 1, du, p.W, 1, f_in, H, EPI_STORE, gr->w_1, H), s2));
   const void* dr1;
   if (p.pre) {
     MGB_TRY(gemm_launch(mk_gemm(dt, T, H, p.W, 0, du, p.W, 1, w->w_1, H, EPI_STORE, d_ffn, H), st));
@@ -433,9 +503,10 @@ mgb_status mgb_block_bwd(const mgb_block_desc* desc, const mgb_block_weights* w,
     dr1 = d_ffn;
   }
   // output projection: dbo, dWo = dr1^T O, dO = dr1 Wo
-  if (gr->b_o) MGB_TRY(colsum_launch(T, H, dt, dr1, H, gr->b_o, cparts, p.cparts, st));
+  MGB_TRY(lane.fork());
+  if (gr->b_o) MGB_TRY(colsum_launch(T, H, dt, dr1, H, gr->b_o, cparts, p.cparts, s2));
   if (gr->w_o)
-    MGB_TRY(gemm_launch(mk_gemm(dt, H, p.Dq, T, 1, dr1, H, 1, O, p.Dq, EPI_STORE, gr->w_o, p.Dq), st));
+    MGB_TRY(gemm_launch(mk_gemm(dt, H, p.Dq, T, 1, dr1, H, 1, O, p.Dq, EPI_STORE, gr->w_o, p.Dq), s2));
   MGB_TRY(gemm_launch(mk_gemm(dt, T, p.Dq, H, 0, dr1, H, 1, w->w_o, p.Dq, EPI_STORE, dO, p.Dq), st));
   // attention backward into the fused dqkv buffer
   {
@@ -456,10 +527,11 @@ mgb_status mgb_block_bwd(const mgb_block_desc* desc, const mgb_block_weights* w,
     MGB_TRY(attention_bwd_launch(at_, st));
   }
   // QKV: dbqkv, dWqkv = dqkv^T a_in, d a_in = dqkv Wqkv
-  if (gr->b_qkv) MGB_TRY(colsum_launch(T, p.Wqkv, dt, dqkv, p.Wqkv, gr->b_qkv, cparts, p.cparts, st));
+  MGB_TRY(lane.fork());
+  if (gr->b_qkv) MGB_TRY(colsum_launch(T, p.Wqkv, dt, dqkv, p.Wqkv, gr->b_qkv, cparts, p.cparts, s2));
   if (gr->w_qkv)
     MGB_TRY(gemm_launch(
-        mk_gemm(dt, p.Wqkv, H, T, 1, dqkv, p.Wqkv, 1, a_in, H, EPI_STORE, gr->w_qkv, H), st));
+        mk_gemm(dt, p.Wqkv, H, T, 1, dqkv, p.Wqkv, 1, a_in, H, EPI_STORE, gr->w_qkv, H), s2));
   if (p.pre) {
     MGB_TRY(gemm_launch(mk_gemm(dt, T, H, p.Wqkv, 0, dqkv, p.Wqkv, 1, w->w_qkv, H, EPI_STORE, dxn, H),
                         st));
@@ -470,7 +542,7 @@ mgb_status mgb_block_bwd(const mgb_block_desc* desc, const mgb_block_weights* w,
     g.resid = dr1; g.ldr = H;
     MGB_TRY(gemm_launch(g, st));
   }
-  return MGB_OK;
+  return lane.join();
 }
 
 // ------------------------------------------------------------ cross-entropy

@@ -74,34 +74,36 @@ __global__ void emb_fwd_kernel(int T, int H, int elt, int v0, int v1, const int3
   }
 }
 
-constexpr int RANK_TILE = 1024;
+constexpr int RANK_I = 256, RANK_J = 1024;
 
-// rank[t] = number of earlier tokens with the same id (ids outside the
-// shard get -1); counts[v - v0] += 1 for tokens the shard owns.
-__global__ void __launch_bounds__(256) emb_rank_kernel(int T, int v0, int v1,
-                                                       const int32_t* __restrict__ ids,
-                                                       int32_t* __restrict__ rank,
-                                                       int32_t* __restrict__ counts) {
-  __shared__ int32_t tile[RANK_TILE];
-  const int t = blockIdx.x * blockDim.x + threadIdx.x;
+// rank[t] += number of tokens t' < t with ids[t'] = ids[t], over the tokens t'
+// of tile blockIdx.y (RANK_J of them) and the tokens t of tile blockIdx.x
+// (RANK_I, one per thread); rank starts at zero and the partial counts are
+// added with integer atomics, so the result does not depend on block order.
+// Tiles of blockIdx.y == 0 also count the shard's tokens per row.
+__global__ void __launch_bounds__(RANK_I) emb_rank_kernel(int T, int v0, int v1,
+                                                          const int32_t* __restrict__ ids,
+                                                          int32_t* __restrict__ rank,
+                                                          int32_t* __restrict__ counts) {
+  __shared__ __align__(16) int32_t tile[RANK_J];
+  const int i0 = blockIdx.x * RANK_I, j0 = blockIdx.y * RANK_J;
+  if (j0 >= min(T, i0 + RANK_I) - 1 && blockIdx.y > 0) return;  // no t' < t in this tile
+  const int t = i0 + threadIdx.x;
   const int v = t < T ? ids[t] : -1;
   const bool own = t < T && v >= v0 && v < v1;
+  if (blockIdx.y == 0 && own) atomicAdd(counts + (v - v0), 1);
+  const int n = min(RANK_J, T - j0);
+  for (int i = threadIdx.x; i < n; i += RANK_I) tile[i] = ids[j0 + i];
+  __syncthreads();
+  const int lim = own ? max(0, min(n, t - j0)) : 0;  // tokens t' < t of this tile
   int r = 0;
-  const int last = min(T, (int)((blockIdx.x + 1) * blockDim.x));  // tokens before this block's end
-  for (int base = 0; base < last; base += RANK_TILE) {
-    const int n = min(RANK_TILE, last - base);
-    __syncthreads();
-    for (int i = threadIdx.x; i < n; i += blockDim.x) tile[i] = ids[base + i];
-    __syncthreads();
-    if (own) {
-      const int lim = min(n, t - base);  // only tokens t' < t
-      for (int i = 0; i < lim; ++i) r += tile[i] == v;
-    }
+  const int4* tile4 = reinterpret_cast<const int4*>(tile);
+  for (int q = 0; q < lim / 4; ++q) {
+    const int4 x = tile4[q];
+    r += (x.x == v) + (x.y == v) + (x.z == v) + (x.w == v);
   }
-  if (t < T) {
-    rank[t] = own ? r : -1;
-    if (own) atomicAdd(counts + (v - v0), 1);
-  }
+  for (int i = lim & ~3; i < lim; ++i) r += tile[i] == v;
+  if (r > 0) atomicAdd(rank + t, r);
 }
 
 // Exclusive scan of the per-row counts, in three steps:
@@ -183,41 +185,72 @@ __global__ void emb_scan_add(int n, const int32_t* __restrict__ totals, int nchu
   if (i == 0) offsets[n] = totals[nchunks];
 }
 
-__global__ void emb_place_kernel(int T, int v0, const int32_t* __restrict__ ids,
+// Token t goes to order[offsets[row] + rank[t]]; the first token of a row
+// also records the row and the end of its segment at that position.
+__global__ void emb_place_kernel(int T, int v0, int v1, const int32_t* __restrict__ ids,
                                  const int32_t* __restrict__ rank,
-                                 const int32_t* __restrict__ offsets, int32_t* __restrict__ order) {
+                                 const int32_t* __restrict__ offsets, int32_t* __restrict__ order,
+                                 int32_t* __restrict__ seg_row, int32_t* __restrict__ seg_end) {
   const int t = blockIdx.x * blockDim.x + threadIdx.x;
-  if (t < T && rank[t] >= 0) order[offsets[ids[t] - v0] + rank[t]] = t;
+  if (t >= T) return;
+  const int v = ids[t];
+  if (v < v0 || v >= v1) return;
+  const int row = v - v0, rk = rank[t], pos = offsets[row] + rk;
+  order[pos] = t;
+  seg_row[pos] = rk == 0 ? row : -1;
+  if (rk == 0) seg_end[pos] = offsets[row + 1];
 }
 
-// One block per shard row: sum its tokens' gradient rows in token order.
+// Sum of one row's token gradients in token order (float32), added to or
+// written over the row.
 template <typename T>
-__global__ void emb_accum_kernel(int rows, int H, const int32_t* __restrict__ offsets,
-                                 const int32_t* __restrict__ order, const T* __restrict__ dout,
-                                 T* __restrict__ d_emb, int accumulate) {
+__device__ __forceinline__ void emb_row_sum(int H, int a, int b, const int32_t* __restrict__ order,
+                                            const T* __restrict__ dout, T* __restrict__ dst,
+                                            bool accumulate) {
   constexpr int VN = EVec<T>::N;
   const int nvec = H / VN;
-  for (int row = blockIdx.x; row < rows; row += gridDim.x) {
-    const int a = offsets[row], b = offsets[row + 1];
-    if (a == b && accumulate) continue;
-    T* dst = d_emb + (int64_t)row * H;
-    for (int vi = threadIdx.x; vi < nvec; vi += blockDim.x) {
-      float acc[VN];
-      if (accumulate) {
-        eload(dst + vi * VN, acc);
-      } else {
+  for (int vi = threadIdx.x; vi < nvec; vi += blockDim.x) {
+    float acc[VN];
+    if (accumulate) {
+      eload(dst + vi * VN, acc);
+    } else {
 #pragma unroll
-        for (int j = 0; j < VN; ++j) acc[j] = 0.0f;
-      }
-      for (int i = a; i < b; ++i) {
-        float g[VN];
-        eload(dout + (int64_t)order[i] * H + vi * VN, g);
-#pragma unroll
-        for (int j = 0; j < VN; ++j) acc[j] += g[j];
-      }
-      estore(dst + vi * VN, acc);
+      for (int j = 0; j < VN; ++j) acc[j] = 0.0f;
     }
+    for (int i = a; i < b; ++i) {
+      float g[VN];
+      eload(dout + (int64_t)order[i] * H + vi * VN, g);
+#pragma unroll
+      for (int j = 0; j < VN; ++j) acc[j] += g[j];
+    }
+    estore(dst + vi * VN, acc);
   }
+}
+
+// Accumulate mode: one block per position of the token order; the block at
+// the head of a row's segment adds the row's sum, the others return. Rows
+// without tokens are not touched.
+template <typename T>
+__global__ void emb_accum_heads_kernel(int rows, int H, const int32_t* __restrict__ offsets,
+                                       const int32_t* __restrict__ order,
+                                       const int32_t* __restrict__ seg_row,
+                                       const int32_t* __restrict__ seg_end,
+                                       const T* __restrict__ dout, T* __restrict__ d_emb) {
+  const int p = blockIdx.x;
+  if (p >= offsets[rows]) return;
+  const int row = seg_row[p];
+  if (row < 0) return;
+  emb_row_sum<T>(H, p, seg_end[p], order, dout, d_emb + (int64_t)row * H, true);
+}
+
+// Overwrite mode: blocks stride over all shard rows; rows without tokens are
+// written as zeros.
+template <typename T>
+__global__ void emb_write_rows_kernel(int rows, int H, const int32_t* __restrict__ offsets,
+                                      const int32_t* __restrict__ order, const T* __restrict__ dout,
+                                      T* __restrict__ d_emb) {
+  for (int row = blockIdx.x; row < rows; row += gridDim.x)
+    emb_row_sum<T>(H, offsets[row], offsets[row + 1], order, dout, d_emb + (int64_t)row * H, false);
 }
 
 }  // namespace
@@ -225,8 +258,9 @@ __global__ void emb_accum_kernel(int rows, int H, const int32_t* __restrict__ of
 size_t embedding_bwd_ws(int T, int v0, int v1) {
   const size_t rows = v1 > v0 ? (size_t)(v1 - v0) : 0;
   const size_t chunks = (rows + SCAN_CHUNK - 1) / SCAN_CHUNK;
-  // rank, order [T]; counts [rows] (padded to 16 bytes); offsets [rows + 1]; chunk totals
-  return 4 * (2 * (size_t)T + (rows + 3) / 4 * 4 + rows + 1 + chunks + 1) + 256;
+  // rank, order, seg_row, seg_end [T]; counts [rows] (16-byte aligned, padded);
+  // offsets [rows + 1]; chunk totals [chunks + 1]
+  return 4 * (4 * (size_t)T + (rows + 3) / 4 * 4 + rows + 1 + chunks + 1) + 256;
 }
 
 mgb_status embedding_fwd_launch(int T, int H, int dtype, int v0, int v1, const int32_t* ids,
@@ -250,29 +284,50 @@ mgb_status embedding_bwd_launch(int T, int H, int dtype, int v0, int v1, const i
   const int nchunks = (rows + SCAN_CHUNK - 1) / SCAN_CHUNK;
   int32_t* rank = static_cast<int32_t*>(ws);
   int32_t* order = rank + T;
-  int32_t* counts = order + T;
+  int32_t* seg_row = order + T;
+  int32_t* seg_end = seg_row + T;
+  int32_t* counts = seg_end + T;
   counts += (4 - (reinterpret_cast<uintptr_t>(counts) / 4) % 4) % 4;  // 16-byte aligned
   int32_t* offsets = counts + (rows + 3) / 4 * 4;
   int32_t* totals = offsets + rows + 1;
-  LaunchScope scope(PROF_EMBEDDING, st, 6);
+  LaunchScope scope(PROF_EMBEDDING, st, 3 + (T > 0 ? 3 : (accumulate ? 0 : 1)));
   if (cudaMemsetAsync(counts, 0, sizeof(int32_t) * rows, st) != cudaSuccess) return MGB_ERR_CUDA;
-  if (T > 0) emb_rank_kernel<<<(T + 63) / 64, 64, 0, st>>>(T, v0, v1, ids, rank, counts);
+  if (T > 0) {
+    if (cudaMemsetAsync(rank, 0, sizeof(int32_t) * T, st) != cudaSuccess) return MGB_ERR_CUDA;
+    const dim3 grid((T + RANK_I - 1) / RANK_I, (T + RANK_J - 1) / RANK_J);
+    emb_rank_kernel<<<grid, RANK_I, 0, st>>>(T, v0, v1, ids, rank, counts);
+  }
   emb_scan_chunks<<<nchunks, SCAN_THREADS, 0, st>>>(rows, counts, offsets, totals);
   emb_scan_totals<<<1, SCAN_THREADS, 0, st>>>(nchunks, totals);
   emb_scan_add<<<(rows + 255) / 256, 256, 0, st>>>(rows, totals, nchunks, offsets);
-  if (T > 0) emb_place_kernel<<<(T + 255) / 256, 256, 0, st>>>(T, v0, ids, rank, offsets, order);
+  if (T > 0)
+    emb_place_kernel<<<(T + 255) / 256, 256, 0, st>>>(T, v0, v1, ids, rank, offsets, order, seg_row,
+                                                      seg_end);
   const int vn = dtype == MGB_BF16 ? 8 : 4;
   const int nvec = H / vn;
   const int threads = nvec >= 256 ? 256 : ((nvec + 31) / 32) * 32;
-  const int grid = rows < device_sm_count() * 32 ? rows : device_sm_count() * 32;
-  if (dtype == MGB_BF16)
-    emb_accum_kernel<bf16><<<grid, threads, 0, st>>>(rows, H, offsets, order,
-                                                     static_cast<const bf16*>(dout),
-                                                     static_cast<bf16*>(d_emb), accumulate);
-  else
-    emb_accum_kernel<float><<<grid, threads, 0, st>>>(rows, H, offsets, order,
-                                                      static_cast<const float*>(dout),
-                                                      static_cast<float*>(d_emb), accumulate);
+  if (accumulate) {
+    if (T > 0) {
+      if (dtype == MGB_BF16)
+        emb_accum_heads_kernel<bf16><<<T, threads, 0, st>>>(rows, H, offsets, order, seg_row, seg_end,
+                                                            static_cast<const bf16*>(dout),
+                                                            static_cast<bf16*>(d_emb));
+      else
+        emb_accum_heads_kernel<float><<<T, threads, 0, st>>>(rows, H, offsets, order, seg_row,
+                                                             seg_end, static_cast<const float*>(dout),
+                                                             static_cast<float*>(d_emb));
+    }
+  } else {
+    const int grid = rows < device_sm_count() * 32 ? rows : device_sm_count() * 32;
+    if (dtype == MGB_BF16)
+      emb_write_rows_kernel<bf16><<<grid, threads, 0, st>>>(rows, H, offsets, order,
+                                                            static_cast<const bf16*>(dout),
+                                                            static_cast<bf16*>(d_emb));
+    else
+      emb_write_rows_kernel<float><<<grid, threads, 0, st>>>(rows, H, offsets, order,
+                                                             static_cast<const float*>(dout),
+                                                             static_cast<float*>(d_emb));
+  }
   return cudaGetLastError() == cudaSuccess ? MGB_OK : MGB_ERR_CUDA;
 }
 

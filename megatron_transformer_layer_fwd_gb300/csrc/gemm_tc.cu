@@ -348,13 +348,13 @@ __device__ void epilogue_row(const EpiParams& p, uint32_t tmem_row, int row, int
 // Tile `tile` of the grouped raster: group_m row tiles per group, the row
 // tile advancing fastest inside a group.
 __device__ __forceinline__ void tile_origin(const EpiParams& p, int tile, int bn, int& m0,
-                                            int& n0) {
+                                            int& n0, int bm = BM) {
   const int per_group = p.group_m * p.tiles_n;
   const int group = tile / per_group;
   const int first_m = group * p.group_m;
   const int gm = min(p.tiles_m - first_m, p.group_m);
   const int in_group = tile - group * per_group;
-  m0 = (first_m + in_group % gm) * BM;
+  m0 = (first_m + in_group % gm) * bm;
   n0 = (in_group / gm) * bn;
 }
 
@@ -519,6 +519,182 @@ __global__ void __launch_bounds__(192, 1)
   }
 }
 
+// CTA-pair variant (cluster of two CTAs on two SMs): 256 x 256 output tiles,
+// one per pair. Each CTA stages its 128 rows of A and its 128 columns of B
+// (32 KB per 64-wide K block instead of 48 KB for a 128 x 256 tile on one SM,
+// so one SM's shared memory holds more K blocks in flight and each SM pulls a
+// third fewer bytes through L2). The leader (rank 0) issues M = 256, N = 256
+// tcgen05.mma.cta_group::2 products; each CTA's TMEM holds the float32
+// accumulator of its own 128 rows, and each CTA runs the epilogue of its rows.
+// Barriers, at the same offsets in both CTAs:
+//   full[s]   leader only: both CTAs' TMA bytes of stage s (the leader expects
+//             them all; the peer's copies signal the leader's barrier)
+//   empty[s]  both: the leader's commit, multicast, frees stage s in both
+//   accf[b]   both: the leader's commit, multicast: accumulator b complete
+//   acce[b]   leader only: the 4 epilogue warps of both CTAs have read b
+template <int STAGES, int A_MN, int B_MN>
+__global__ void __launch_bounds__(192, 1)
+    gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmA,
+                        const __grid_constant__ CUtensorMap tmB, const EpiParams p) {
+  constexpr int BNP = 256, HALF = 128;
+  constexpr int A_BYTES = HALF * BK * 2, B_BYTES = HALF * BK * 2;
+  constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 4);
+  volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  const uint32_t tiles = smem_u32(smem);
+  const uint32_t full0 = smem_u32(bars);
+  const uint32_t empty0 = full0 + 8 * STAGES;
+  const uint32_t accf0 = empty0 + 8 * STAGES;
+  const uint32_t acce0 = accf0 + 16;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
+  const int num_k = (p.K + BK - 1) / BK;
+  const int total = p.tiles_m * p.tiles_n;
+
+  if (threadIdx.x == 0) {
+    tma_prefetch_desc(&tmA);
+    tma_prefetch_desc(&tmB);
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(full0 + 8 * s, 1);
+      mbar_init(empty0 + 8 * s, 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(accf0 + 8 * b, 1);
+      mbar_init(acce0 + 8 * b, 8);  // 4 epilogue warps in each CTA
+    }
+    fence_mbar_init();
+    *abort = 0;
+  }
+  if (warp == 0) tmem_alloc_pair(smem_u32(tmem_slot), 2 * BNP);
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // both CTAs' barriers initialised before any remote signal
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ---------------- TMA producer (both CTAs)
+      uint32_t kg = 0;
+      for (int tile = pair; tile < total && !*abort; tile += npairs) {
+        int m0, n0;
+        tile_origin(p, tile, BNP, m0, n0, 2 * HALF);
+        const int ma = m0 + HALF * (int)rank, nb = n0 + HALF * (int)rank;
+        for (int kb = 0; kb < num_k; ++kb, ++kg) {
+          const int s = kg % STAGES;
+          if (!mbar_wait(empty0 + 8 * s, ((kg / STAGES) & 1) ^ 1, p.err)) {
+            *abort = 1;
+            break;
+          }
+          const uint32_t sa = tiles + s * STAGE_BYTES;
+          const uint32_t sb = sa + A_BYTES;
+          const uint32_t fb = mapa_shared(full0 + 8 * s, 0);
+          if (rank == 0) mbar_arrive_expect_tx(full0 + 8 * s, 2 * STAGE_BYTES);
+          const int k0 = kb * BK;
+          if (A_MN == 0) {
+            tma_load_2d_pair(sa, &tmA, k0, ma, fb);
+          } else {
+            tma_load_2d_pair(sa, &tmA, ma, k0, fb);
+            tma_load_2d_pair(sa + 8192, &tmA, ma + 64, k0, fb);
+          }
+          if (B_MN == 0) {
+            tma_load_2d_pair(sb, &tmB, k0, nb, fb);
+          } else {
+            tma_load_2d_pair(sb, &tmB, nb, k0, fb);
+            tma_load_2d_pair(sb + 8192, &tmB, nb + 64, k0, fb);
+          }
+        }
+      }
+      // drain: every stage released once more, so no multicast arrival on
+      // this CTA's empty barriers is still on its way when the CTA exits
+      for (int i = 0; i < STAGES && !*abort; ++i, ++kg) {
+        const int s = kg % STAGES;
+        if (!mbar_wait(empty0 + 8 * s, ((kg / STAGES) & 1) ^ 1, p.err)) *abort = 1;
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && rank == 0) {
+      // ---------------- MMA issuer (leader)
+      constexpr uint32_t idesc = idesc_bf16_f32(2 * HALF, BNP, A_MN, B_MN);
+      uint32_t kg = 0;
+      int t = 0;
+      for (int tile = pair; tile < total && !*abort; tile += npairs, ++t) {
+        const int buf = t & 1;
+        if (!mbar_wait(acce0 + 8 * buf, ((t >> 1) & 1) ^ 1, p.err)) {
+          *abort = 1;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t acc = tmem + buf * BNP;
+        bool good = true;
+        for (int kb = 0; kb < num_k; ++kb, ++kg) {
+          const int s = kg % STAGES;
+          if (!mbar_wait(full0 + 8 * s, (kg / STAGES) & 1, p.err)) {
+            good = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t sa = tiles + s * STAGE_BYTES;
+          const uint32_t sb = sa + A_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk) {
+            const uint64_t ad = A_MN ? smem_desc_sw128(sa + 2048 * kk, 8192, 1024)
+                                     : smem_desc_sw128(sa + 32 * kk, 16, 1024);
+            const uint64_t bd = B_MN ? smem_desc_sw128(sb + 2048 * kk, 8192, 1024)
+                                     : smem_desc_sw128(sb + 32 * kk, 16, 1024);
+            tc_mma_f16_pair(acc, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+          }
+          tc_commit_pair_mc(empty0 + 8 * s, 3);
+        }
+        if (!good) {
+          *abort = 1;
+          break;
+        }
+        tc_commit_pair_mc(accf0 + 8 * buf, 3);
+      }
+    }
+  } else {
+    // ---------------- epilogue warps 2..5 (both CTAs: this CTA's 128 rows)
+    const int q = warp & 3;
+    int t = 0;
+    for (int tile = pair; tile < total; tile += npairs, ++t) {
+      const int buf = t & 1;
+      const bool ready = !*abort && mbar_wait(accf0 + 8 * buf, (t >> 1) & 1, p.err);
+      if (!__all_sync(0xffffffffu, ready)) {
+        *abort = 1;
+        break;
+      }
+      tc_fence_after();
+      int m0, n0;
+      tile_origin(p, tile, BNP, m0, n0, 2 * HALF);
+      epilogue_row<BNP>(p, tmem + buf * BNP + ((uint32_t)(q * 32) << 16),
+                        m0 + HALF * (int)rank + q * 32 + lane, n0, num_k > 0);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(mapa_shared(acce0 + 8 * buf, 0));
+    }
+  }
+
+  __syncthreads();
+  if (*abort && threadIdx.x == 0) {
+    const uint64_t t0 = global_ns();
+    while (global_ns() - t0 < 10000000ull) {
+    }
+  }
+  tc_fence_before();
+  cluster_sync();  // neither CTA frees TMEM or exits while its peer may still signal it
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem, 2 * BNP);
+  }
+}
+
 // ---------------------------------------------------------------- host side
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -589,6 +765,69 @@ mgb_status launch_variant(const GemmArgs& g, const EpiParams& ep, cudaStream_t s
   return cudaGetLastError() == cudaSuccess ? MGB_OK : MGB_ERR_CUDA;
 }
 
+constexpr int PAIR_STAGES = 6;
+constexpr int pair_smem_bytes() { return PAIR_STAGES * 2 * (128 * BK * 2) + 1024 + 256; }
+
+template <int A_MN, int B_MN>
+mgb_status launch_pair_variant(const GemmArgs& g, const EpiParams& ep, cudaStream_t st) {
+  auto kern = gemm_tc_pair_kernel<PAIR_STAGES, A_MN, B_MN>;
+  constexpr int smem = pair_smem_bytes();
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
+    return MGB_ERR_CUDA;
+  CUtensorMap ta, tb;
+  bool ok = A_MN ? make_tmap(&ta, g.A, g.M, g.K, g.lda, 64, 64)
+                 : make_tmap(&ta, g.A, g.K, g.M, g.lda, 64, 128);
+  ok = ok && (B_MN ? make_tmap(&tb, g.B, g.N, g.K, g.ldb, 64, 64)
+                   : make_tmap(&tb, g.B, g.K, g.N, g.ldb, 64, 128));
+  if (!ok) return MGB_ERR_CUDA;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.blockDim = dim3(192, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  // persistent: as many pairs as can be resident at once (one CTA per SM),
+  // never more than there are tiles
+  static int max_pairs[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) dev = 0;
+  if (max_pairs[dev] == 0) {
+    int n = 0;
+    cfg.gridDim = dim3(2 * (device_sm_count() / 2), 1, 1);
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n < 1) {
+      cudaGetLastError();
+      n = device_sm_count() / 2;
+    }
+    max_pairs[dev] = n;
+  }
+  const long total = (long)ep.tiles_m * ep.tiles_n;
+  const int pairs = (int)std::max(1L, std::min<long>(total, max_pairs[dev]));
+  cfg.gridDim = dim3(2 * pairs, 1, 1);
+  LaunchScope scope(g.prof_kind >= 0 ? g.prof_kind
+                               : (A_MN ? PROF_GEMM_WGRAD : (B_MN ? PROF_GEMM_DGRAD : PROF_GEMM_FWD)),
+                    st);
+  if (cudaLaunchKernelEx(&cfg, kern, ta, tb, ep) != cudaSuccess) return MGB_ERR_CUDA;
+  return cudaGetLastError() == cudaSuccess ? MGB_OK : MGB_ERR_CUDA;
+}
+
+mgb_status launch_pair(const GemmArgs& g, EpiParams ep, cudaStream_t st) {
+  ep.tiles_m = (g.M + 255) / 256;
+  ep.tiles_n = (g.N + 255) / 256;
+  const long panel = 256L * g.K * 2;
+  ep.group_m = (int)std::max(2L, std::min(32L, (48L << 20) / panel));
+  ep.group_m = std::min(ep.group_m, ep.tiles_m);
+  if (!g.a_mn && !g.b_mn) return launch_pair_variant<0, 0>(g, ep, st);
+  if (!g.a_mn && g.b_mn) return launch_pair_variant<0, 1>(g, ep, st);
+  if (g.a_mn && g.b_mn) return launch_pair_variant<1, 1>(g, ep, st);
+  return launch_pair_variant<1, 0>(g, ep, st);
+}
+
 template <int BN, int STAGES>
 mgb_status launch_bn(const GemmArgs& g, EpiParams ep, cudaStream_t st) {
   ep.tiles_m = (g.M + BM - 1) / BM;
@@ -630,8 +869,17 @@ mgb_status gemm_tc_launch(const GemmArgs& g, cudaStream_t st) {
   ep.ce_scale = g.ce_scale;
   ep.tgt_v0 = g.tgt_v0;
   ep.tgt_out = g.tgt_out;
-  // Column tile: 256 unless the problem is too narrow to fill the GPU with it.
+  // Tile: 256 x 256 on a CTA pair when there are enough such tiles to fill
+  // the GPU; else 128 x 256 on one SM, or 128 x 128 when the problem is too
+  // narrow to fill the GPU with 256 columns. MGB_GEMM_PAIR=0 / =1 turns the
+  // pair tile off / on whenever K > 0 (tests cover both on small shapes).
   const long tiles256 = (long)((g.M + BM - 1) / BM) * ((g.N + 255) / 256);
+  const long pair_tiles = (long)((g.M + 255) / 256) * ((g.N + 255) / 256);
+  const char* pe = getenv("MGB_GEMM_PAIR");
+  const int force = pe == nullptr ? -1 : (pe[0] == '1' ? 1 : (pe[0] == '0' ? 0 : -1));
+  const bool pair = g.K > 0 && (force == 1 || (force == -1 && g.M > 128 && g.N > 128 &&
+                                               pair_tiles >= device_sm_count() / 2));
+  if (pair) return launch_pair(g, ep, st);
   if (g.epi == EPI_BIAS_SWIGLU || (tiles256 >= 148 && g.N > 128))
     return launch_bn<256, 4>(g, ep, st);
   return launch_bn<128, 6>(g, ep, st);

@@ -47,6 +47,25 @@ def test_ce_small_full_parity(mgb_lib, T, H, V, C, mode):
 
 
 @pytest.mark.parametrize("mode", MODES)
+def test_ce_pair_tiles(mgb_lib, monkeypatch, mode):
+    """The CE's GEMMs (logits with the statistics or gradient epilogue,
+    dgrad, wgrad) on CTA-pair tiles."""
+    monkeypatch.setenv("MGB_GEMM_PAIR", "1")
+    T, H, V, C = 300, 256, 1000, 136
+    shape = CEShape(T, H, V, C)
+    inp = ce_inputs(shape, seed=6)
+    r = _runner(shape, inp, mode)
+    r.run()
+    assert mgb.mgb_device_status() == mgb.MGB_OK
+    loss, lse, mean, _ = oracle.ce_chunked(inp["hidden"], inp["emb"], inp["targets"], C)
+    dh, de = oracle.ce_grads(inp["hidden"], inp["emb"], inp["targets"], lse, 1.0 / T)
+    assert np.abs(to_np(r.loss) - loss).max() < CE_LOSS_ABS
+    assert abs(float(r.loss_mean[0]) - mean) < CE_LOSS_ABS
+    assert rel_l2(to_np(r.d_hidden), dh) < 2e-2
+    assert rel_l2(to_np(r.d_emb), de) < 2e-2
+
+
+@pytest.mark.parametrize("mode", MODES)
 def test_ce_forward_only(mgb_lib, mode):
     shape = CEShape(128, 64, 256, 96)
     inp = ce_inputs(shape, seed=1)

@@ -89,6 +89,23 @@ def test_backward_deterministic(mgb_lib):
     assert torch.equal(a, b)
 
 
+@pytest.mark.parametrize("accumulate", [False, True])
+def test_backward_token_order_f32(mgb_lib, accumulate):
+    """In float32 the backward is bit-exact against adding each token's row in
+    token order (starting from the old row when accumulating): the order the
+    sums are taken in is fixed, whatever the blocks' schedule. Ids repeat
+    across several tiles of the rank computation; some fall outside the shard."""
+    T, H, V, v0, v1 = 3000, 64, 400, 37, 381
+    ids = _ids(T, V, repeats=True)
+    dout = RNG.standard_normal((T, H)).astype(np.float32)
+    init = RNG.standard_normal((v1 - v0, H)).astype(np.float32)
+    want = init.copy() if accumulate else np.zeros_like(init)
+    own = (ids >= v0) & (ids < v1)
+    np.add.at(want, ids[own] - v0, dout[own])  # unbuffered, in index order
+    got = to_np(_bwd(ids, dout, v0, v1, torch.float32, mgb.MGB_F32, init=init if accumulate else None))
+    assert np.array_equal(got.astype(np.float32), want)
+
+
 def test_empty_batch(mgb_lib):
     ids = np.zeros(0, dtype=np.int32)
     d = _bwd(ids, np.zeros((0, 16)), 0, 10, torch.bfloat16, mgb.MGB_BF16)

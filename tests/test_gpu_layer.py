@@ -64,6 +64,16 @@ def run_and_compare(shape, arr, dy_np, check_fwd=True, label=""):
     return r, ry
 
 
+@pytest.mark.parametrize("name", ["bf16_pre_swiglu_causal_gqa", "bf16_post_gelu_causal",
+                                  "bf16_post_swiglu_gqa_gb64"])
+def test_small_layer_parity_pair_tiles(mgb_lib, monkeypatch, name):
+    """Every GEMM of the layer on CTA-pair tiles (all fused epilogues)."""
+    monkeypatch.setenv("MGB_GEMM_PAIR", "1")
+    shape = SMALL[name]
+    arr = layer_inputs(shape, seed=12, random_affine=True, random_dy=True)
+    run_and_compare(shape, arr, arr["dy"], label=f"{name}/pair")
+
+
 @pytest.mark.parametrize("name", list(SMALL))
 @pytest.mark.parametrize("dy_kind", ["random", "mean"])
 def test_small_layer_parity(mgb_lib, name, dy_kind):
@@ -107,6 +117,38 @@ def test_deterministic_repeat(mgb_lib):
     y2 = r.fwd()
     dx2, g2 = r.bwd(dy)
     assert torch.equal(y1, y2) and torch.equal(dx1, dx2) and torch.equal(gw1, g2["w_qkv"])
+
+
+def test_graph_capture_replay(mgb_lib):
+    """The layer's forward and backward (including the backward's side stream
+    for weight gradients, forked and joined inside the call) captured into one
+    CUDA graph: replaying it reproduces the eager results bit for bit, also
+    after the inputs are changed in place."""
+    shape = SMALL["bf16_pre_swiglu_causal_gqa"]
+    arr = layer_inputs(shape, seed=4, random_affine=True, random_dy=True)
+    r = LayerRunner(shape, arr)
+    dy = to_device(arr["dy"], r.dtype)
+    side = torch.cuda.Stream()
+    with torch.cuda.stream(side):  # first calls on this thread: library streams and events
+        r.fwd()
+        r.bwd(dy)
+    side.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        r.fwd()
+        r.bwd(dy)
+    for scale in (1.0, -0.5):
+        r.x.copy_(to_device(arr["x"] * scale, r.dtype))
+        g.replay()
+        torch.cuda.synchronize()
+        got = [r.y.clone(), r.dx.clone()] + [v.clone() for v in r.grads.values() if v is not None]
+        r.fwd()
+        r.bwd(dy)
+        torch.cuda.synchronize()
+        want = [r.y, r.dx] + [v for v in r.grads.values() if v is not None]
+        for a, b in zip(got, want):
+            assert torch.equal(a, b)
+    assert mgb.mgb_device_status() == mgb.MGB_OK
 
 
 # ----------------------------------------------------------- named workloads

@@ -23,9 +23,13 @@ def _dev(a, dtype):
     return torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).to("cuda", dtype)
 
 
+@pytest.mark.parametrize("pair", ["0", "1"])
 @pytest.mark.parametrize("a_mn,b_mn", [(0, 0), (0, 1), (1, 1), (1, 0)])
 @pytest.mark.parametrize("M,N,K", [(128, 128, 64), (328, 200, 136), (256, 520, 1000), (1000, 1304, 64)])
-def test_gemm_bf16_layouts_f32_out(mgb_lib, a_mn, b_mn, M, N, K):
+def test_gemm_bf16_layouts_f32_out(mgb_lib, monkeypatch, pair, a_mn, b_mn, M, N, K):
+    """Every operand layout on one SM (128-row tiles) and on a CTA pair
+    (256 x 256 tiles): ragged M, N and K; a pair whose second CTA has no rows."""
+    monkeypatch.setenv("MGB_GEMM_PAIR", pair)
     A = _bf16((M, K))
     B = _bf16((N, K))
     a_st = A.T.copy() if a_mn else A
@@ -40,8 +44,10 @@ def test_gemm_bf16_layouts_f32_out(mgb_lib, a_mn, b_mn, M, N, K):
     assert err < 1e-5, err
 
 
+@pytest.mark.parametrize("pair", ["0", "1"])
 @pytest.mark.parametrize("M,N,K", [(384, 768, 256), (200, 136, 72)])
-def test_gemm_bf16_bias_out_and_accumulate(mgb_lib, M, N, K):
+def test_gemm_bf16_bias_out_and_accumulate(mgb_lib, monkeypatch, pair, M, N, K):
+    monkeypatch.setenv("MGB_GEMM_PAIR", pair)
     A, B, bias = _bf16((M, K)), _bf16((N, K)), _bf16((N,))
     c = torch.empty((M, N), device="cuda", dtype=torch.bfloat16)
     d = mgb.GemmDesc(m=M, n=N, k=K, a_major=0, b_major=0, lda=K, ldb=K, ldc=N, dtype=mgb.MGB_BF16,
@@ -55,6 +61,25 @@ def test_gemm_bf16_bias_out_and_accumulate(mgb_lib, M, N, K):
     mgb.mgb_gemm(d, _dev(A, torch.bfloat16), _dev(B, torch.bfloat16), None, c32)
     assert rel_l2(to_np(c32), ref + A @ B.T) < 1e-5
     assert mgb.mgb_device_status() == mgb.MGB_OK
+
+
+@pytest.mark.parametrize("a_mn,b_mn", [(0, 0), (0, 1), (1, 1)])
+def test_gemm_pair_tiles_many_waves(mgb_lib, a_mn, b_mn):
+    """Large enough for the CTA-pair tile to be chosen by itself, with more
+    tiles than resident pairs (each pair walks several tiles and reuses both
+    TMEM accumulators) and ragged edges in M and N."""
+    M, N, K = 2320, 4360, 320
+    A = _bf16((M, K))
+    B = _bf16((N, K))
+    a_st = A.T.copy() if a_mn else A
+    b_st = B.T.copy() if b_mn else B
+    c = torch.full((M, N), float("nan"), device="cuda", dtype=torch.float32)
+    d = mgb.GemmDesc(m=M, n=N, k=K, a_major=a_mn, b_major=b_mn, lda=a_st.shape[1], ldb=b_st.shape[1],
+                     ldc=N, dtype=mgb.MGB_BF16, c_f32=1, accumulate=0, alpha=1.0)
+    mgb.mgb_gemm(d, _dev(a_st, torch.bfloat16), _dev(b_st, torch.bfloat16), None, c)
+    assert mgb.mgb_device_status() == mgb.MGB_OK
+    err = rel_l2(to_np(c), A @ B.T)
+    assert err < 1e-5, err
 
 
 @pytest.mark.parametrize("a_mn,b_mn", [(0, 0), (0, 1), (1, 1)])
