@@ -138,10 +138,17 @@ typedef enum {
   MGB_CE_STREAM = 0,  /* the logits GEMM stores a chunk's bf16 logits; streaming
                          kernels read them for the max / sum exp partials and
                          rewrite them into the gradient */
-  MGB_CE_FUSED = 1    /* the logits GEMM's epilogue keeps per-(token, 128-column
+  MGB_CE_FUSED = 1,   /* the logits GEMM's epilogue keeps per-(token, 128-column
                          group) max / sum exp partials of its float32
                          accumulator and stores no logits; the recomputing
                          GEMM's epilogue writes the gradient directly */
+  MGB_CE_RESIDENT = 2 /* as MGB_CE_FUSED for the partials, and the epilogue
+                         also stores every chunk's bf16 logits into one
+                         [tokens, vocab] workspace buffer (2 bytes per logit):
+                         the backward rewrites them into the gradient in one
+                         streaming pass and runs one input-gradient and one
+                         weight-gradient GEMM over the whole vocabulary, with
+                         no logits recomputed */
 } mgb_ce_mode;
 
 /* Tied-embedding cross-entropy [P2 sections 3-4]. */
@@ -162,7 +169,10 @@ mgb_status mgb_vocab_ce_sizes(const mgb_ce_desc* desc, size_t* ws_bytes);
  * G = (softmax(l) - onehot(target)) * grad_scale, d_hidden = G E,
  * d_emb = G^T hidden, again chunk by chunk (logits recomputed per chunk).
  * MGB_CE_FUSED keeps one (max, sum) partial per token and 128 vocab columns
- * instead of one per chunk; the combine is the same merge.
+ * instead of one per chunk; the combine is the same merge. MGB_CE_RESIDENT
+ * needs a workspace of about 2 * tokens * vocab bytes (mgb_vocab_ce_sizes)
+ * and runs the weight gradient on a library-owned second stream, joined back
+ * into `stream` before the call returns (as mgb_block_bwd).
  *   targets [T] int32 in [0, vocab) (device); loss_per_token [T] f32;
  *   loss_mean: one f32 (device); lse [T] f32 or NULL;
  *   d_hidden [T,H], d_emb [V,H]: NULL skips that gradient (both NULL = fwd only). */

@@ -554,7 +554,8 @@ static mgb_status validate_ce(const mgb_ce_desc* d) {
   if (d->dtype != MGB_BF16) return MGB_ERR_UNSUPPORTED;
   if (d->hidden % 8 || d->vocab % 8 || d->chunk % 8) return MGB_ERR_MISALIGNED;
   if (!(d->grad_scale == d->grad_scale)) return MGB_ERR_INVALID_ARG;
-  if (d->mode != MGB_CE_STREAM && d->mode != MGB_CE_FUSED) return MGB_ERR_INVALID_ARG;
+  if (d->mode != MGB_CE_STREAM && d->mode != MGB_CE_FUSED && d->mode != MGB_CE_RESIDENT)
+    return MGB_ERR_INVALID_ARG;
   return MGB_OK;
 }
 
@@ -570,7 +571,8 @@ static void ce_plan(const mgb_ce_desc* d, CEPlan* p) {
   const size_t T = d->tokens;
   p->C = d->chunk < d->vocab ? d->chunk : d->vocab;
   p->n_chunks = (d->vocab + p->C - 1) / p->C;
-  const bool fused = d->mode == MGB_CE_FUSED;
+  const bool resident = d->mode == MGB_CE_RESIDENT;
+  const bool fused = d->mode == MGB_CE_FUSED || resident;
   p->n_parts = 0;
   for (int c = 0; c < p->n_chunks; ++c) {
     const int v0 = c * p->C, Cc = (d->vocab - v0) < p->C ? (d->vocab - v0) : p->C;
@@ -579,12 +581,12 @@ static void ce_plan(const mgb_ce_desc* d, CEPlan* p) {
   p->n_t = fused ? 1 : p->n_chunks;
   size_t o = 0;
   auto take = [&](size_t bytes) { const size_t a = o; o += al256(bytes); return a; };
-  p->logits = take(2 * T * p->C);
+  p->logits = take(2 * T * (resident ? (size_t)d->vocab : (size_t)p->C));
   p->m = take(4 * T * p->n_parts);
   p->s = take(4 * T * p->n_parts);
   p->t = take(4 * T * p->n_t);
   p->lse = take(4 * T);
-  p->dh = take(4 * T * d->hidden);
+  p->dh = resident ? 0 : take(4 * T * d->hidden);
   p->bl = take(4 * (size_t)ce_combine_blocks((int)T));
   p->split = p->n_parts > kCeSplits ? take(4 * 2 * (size_t)kCeSplits * T) : 0;
   p->total = o;
@@ -622,7 +624,8 @@ mgb_status mgb_vocab_ce_fwd_bwd(const mgb_ce_desc* desc, const void* hidden, con
   float* dh_acc = at<float>(ws, p.dh);
   float* bl = at<float>(ws, p.bl);
   const bf16* E = static_cast<const bf16*>(emb);
-  const bool fused = desc->mode == MGB_CE_FUSED;
+  const bool resident = desc->mode == MGB_CE_RESIDENT;
+  const bool fused = desc->mode == MGB_CE_FUSED || resident;
   // ---- forward: per-chunk partials, then the combine
   if (fused && T > 0 && cudaMemsetAsync(t, 0, sizeof(float) * T, st) != cudaSuccess)
     return MGB_ERR_CUDA;
@@ -634,6 +637,7 @@ mgb_status mgb_vocab_ce_fwd_bwd(const mgb_ce_desc* desc, const void* hidden, con
                            EPI_CE_STATS, m + (size_t)part * T, 8);
       g.C2 = s + (size_t)part * T; g.ldc2 = 8;
       g.tgt = targets; g.tgt_v0 = v0; g.tgt_out = t;
+      if (resident) { g.keep = static_cast<bf16*>(logits) + v0; g.ld_keep = V; }
       g.prof_kind = PROF_GEMM_CE_LOGITS;
       MGB_TRY(gemm_launch(g, st));
       part += (Cc + 127) / 128;
@@ -652,6 +656,21 @@ mgb_status mgb_vocab_ce_fwd_bwd(const mgb_ce_desc* desc, const void* hidden, con
   MGB_TRY(ce_combine_launch(T, p.n_parts, m, s, p.n_t, t, lse_buf, loss_per_token, loss_mean, bl,
                             p.n_parts > kCeSplits ? at<float>(ws, p.split) : nullptr, st));
   if (!d_hidden && !d_emb) return MGB_OK;
+  if (resident) {
+    // ---- backward over the resident logits: G in place, then
+    // d_hidden = G E on this stream and d_emb = G^T hidden on the side stream
+    MGB_TRY(ce_grad_launch(T, V, 0, logits, V, targets, lse_buf, desc->grad_scale, st));
+    SideLane lane(st);
+    if (d_emb) {
+      MGB_TRY(lane.fork());
+      MGB_TRY(gemm_launch(mk_gemm(MGB_BF16, V, H, T, 1, logits, V, 1, hidden, H, EPI_STORE,
+                                  d_emb, H), lane.side()));
+    }
+    if (d_hidden)
+      MGB_TRY(gemm_launch(mk_gemm(MGB_BF16, T, H, V, 0, logits, V, 1, E, H, EPI_STORE, d_hidden, H),
+                          st));
+    return lane.join();
+  }
   // ---- backward: per chunk, G then its two GEMMs
   for (int c = 0; c < p.n_chunks; ++c) {
     const int v0 = c * C, Cc = (V - v0) < C ? (V - v0) : C;

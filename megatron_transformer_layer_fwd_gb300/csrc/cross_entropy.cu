@@ -181,21 +181,31 @@ __global__ void __launch_bounds__(CE_THREADS) ce_grad_kernel(int T, int C, int v
   const float L2 = lse[row] * LOG2E;
   const int tc = tgt[row] - v0;
   const int nvec = C / 8;
-  for (int v = threadIdx.x; v < nvec; v += CE_THREADS) {
-    uint4 w = *(reinterpret_cast<const uint4*>(l) + v);
-    uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+  constexpr int U = 4;  // 16-byte vectors in flight per thread
+  for (int v0i = threadIdx.x; v0i < nvec; v0i += U * CE_THREADS) {
+    uint4 w[U];
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const float2 f = unpack_bf16x2(ww[i]);
-      float g0 = exp2f(f.x * LOG2E - L2);
-      float g1 = exp2f(f.y * LOG2E - L2);
-      const int c0 = v * 8 + 2 * i;
-      if (c0 == tc) g0 -= 1.0f;
-      if (c0 + 1 == tc) g1 -= 1.0f;
-      ww[i] = pack_bf16x2(g0 * scale, g1 * scale);
+    for (int u = 0; u < U; ++u) {
+      const int v = v0i + u * CE_THREADS;
+      if (v < nvec) w[u] = *(reinterpret_cast<const uint4*>(l) + v);
     }
-    w.x = ww[0]; w.y = ww[1]; w.z = ww[2]; w.w = ww[3];
-    *(reinterpret_cast<uint4*>(l) + v) = w;
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int v = v0i + u * CE_THREADS;
+      if (v >= nvec) break;
+      uint32_t ww[4] = {w[u].x, w[u].y, w[u].z, w[u].w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const float2 f = unpack_bf16x2(ww[i]);
+        float g0 = exp2f(f.x * LOG2E - L2);
+        float g1 = exp2f(f.y * LOG2E - L2);
+        const int c0 = v * 8 + 2 * i;
+        if (c0 == tc) g0 -= 1.0f;
+        if (c0 + 1 == tc) g1 -= 1.0f;
+        ww[i] = pack_bf16x2(g0 * scale, g1 * scale);
+      }
+      *(reinterpret_cast<uint4*>(l) + v) = make_uint4(ww[0], ww[1], ww[2], ww[3]);
+    }
   }
 }
 

@@ -177,6 +177,9 @@ mgb_status gemm_check(const GemmArgs& g) {
     if (g.ldc % c_mult || (g.C2 && g.ldc2 % 8) || (g.resid && g.ldr % 8) || (g.aux && g.ldaux % 8))
       return MGB_ERR_MISALIGNED;
     if (g.accumulate && g.epi != EPI_F32) return MGB_ERR_INVALID_ARG;
+    if (g.keep != nullptr && (g.epi != EPI_CE_STATS || !al(g.keep) || g.ld_keep % 8 ||
+                              g.ld_keep < g.N))
+      return MGB_ERR_INVALID_ARG;
   }
   return MGB_OK;
 }

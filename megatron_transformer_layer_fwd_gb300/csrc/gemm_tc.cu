@@ -68,6 +68,8 @@ struct EpiParams {
   float* tgt_out;
   const float* ce_lse;
   float ce_scale;
+  bf16* keep;
+  int64_t ld_keep;
 };
 
 template <int BN, int STAGES>
@@ -172,6 +174,12 @@ __device__ void epilogue_row(const EpiParams& p, uint32_t tmem_row, int row, int
 #pragma unroll
           for (int j = 0; j < 32; ++j) v = (j == tc) ? acc[j] : v;
           p.tgt_out[row] = v;
+        }
+        if (p.keep != nullptr) {
+          bf16* kp = p.keep + (int64_t)row * p.ld_keep + n;
+#pragma unroll
+          for (int q = 0; q < 4; ++q)
+            if (n + 8 * q < p.N) store8(kp + 8 * q, acc + 8 * q);
         }
         float cm = -INFINITY;
 #pragma unroll
@@ -867,6 +875,8 @@ mgb_status gemm_tc_launch(const GemmArgs& g, cudaStream_t st) {
   ep.tgt = (g.epi == EPI_STORE || g.epi == EPI_CE_STATS || g.epi == EPI_CE_GRAD) ? g.tgt : nullptr;
   ep.ce_lse = g.ce_lse;
   ep.ce_scale = g.ce_scale;
+  ep.keep = static_cast<bf16*>(g.keep);
+  ep.ld_keep = g.ld_keep;
   ep.tgt_v0 = g.tgt_v0;
   ep.tgt_out = g.tgt_out;
   // Tile: 256 x 256 on a CTA pair when there are enough such tiles to fill

@@ -48,6 +48,8 @@ struct GemmArgs {
   float* tgt_out = nullptr;
   const float* ce_lse = nullptr;  // EPI_CE_GRAD: LSE per row
   float ce_scale = 1.0f;          // EPI_CE_GRAD: dL/dloss per token
+  // EPI_CE_STATS only, may be null: the bf16 logits are also stored here
+  void* keep = nullptr; int64_t ld_keep = 0;
 };
 
 // Validates operand geometry for the chosen path; returns MGB_OK or an error.

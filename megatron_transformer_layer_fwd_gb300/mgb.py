@@ -28,7 +28,7 @@ MGB_ERR_DEVICE_TIMEOUT = -7
 MGB_ERR_NOT_IMPLEMENTED = -8
 
 MGB_F32, MGB_BF16 = 0, 1
-MGB_CE_STREAM, MGB_CE_FUSED = 0, 1
+MGB_CE_STREAM, MGB_CE_FUSED, MGB_CE_RESIDENT = 0, 1, 2
 MGB_PRE_LN, MGB_POST_LN = 0, 1
 MGB_GELU_ERF, MGB_SWIGLU = 0, 1
 MGB_K_MAJOR, MGB_MN_MAJOR = 0, 1

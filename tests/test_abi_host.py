@@ -95,13 +95,19 @@ def test_ce_validation(lib):
     assert lib.mgb_vocab_ce_sizes(ctypes.byref(bad), ctypes.byref(s)) == mgb.MGB_ERR_MISALIGNED
     f32 = mgb.CEDesc(tokens=8, hidden=8, vocab=8, chunk=8, dtype=mgb.MGB_F32, grad_scale=1.0)
     assert lib.mgb_vocab_ce_sizes(ctypes.byref(f32), ctypes.byref(s)) == mgb.MGB_ERR_UNSUPPORTED
-    badmode = mgb.ce_desc(8192, 4096, 128256, 16032, 1 / 8192, mode=2)
+    badmode = mgb.ce_desc(8192, 4096, 128256, 16032, 1 / 8192, mode=3)
     assert lib.mgb_vocab_ce_sizes(ctypes.byref(badmode), ctypes.byref(s)) == mgb.MGB_ERR_INVALID_ARG
     # fused partials: one per token and 128 vocab columns (126 per 16032-wide chunk)
     fused = mgb.mgb_vocab_ce_sizes(mgb.ce_desc(8192, 4096, 128256, 16032, 1 / 8192))
     stream = mgb.mgb_vocab_ce_sizes(mgb.ce_desc(8192, 4096, 128256, 16032, 1 / 8192,
                                                 mode=mgb.MGB_CE_STREAM))
     assert fused - stream >= 2 * 4 * 8192 * (8 * 126 - 8) - 4 * 8192 * 8
+    # resident logits: 2 bytes per logit of the whole vocabulary, no float32
+    # d_hidden accumulator
+    resident = mgb.mgb_vocab_ce_sizes(mgb.ce_desc(8192, 4096, 128256, 16032, 1 / 8192,
+                                                  mode=mgb.MGB_CE_RESIDENT))
+    assert resident >= 2 * 8192 * 128256
+    assert resident - fused == 2 * 8192 * (128256 - 16032) - 4 * 8192 * 4096
 
 
 def test_gemm_validation(lib):

@@ -15,7 +15,7 @@ from tests.util import CE_LOSS_ABS, rel_l2, to_np
 pytestmark = pytest.mark.gpu
 
 
-MODES = [mgb.MGB_CE_STREAM, mgb.MGB_CE_FUSED]
+MODES = [mgb.MGB_CE_STREAM, mgb.MGB_CE_FUSED, mgb.MGB_CE_RESIDENT]
 
 
 def _runner(shape, inp, mode):
@@ -105,7 +105,7 @@ def test_ce_full_size_sampled(mgb_lib, mode):
 
 
 def test_ce_modes_agree_and_are_deterministic(mgb_lib):
-    """The two modes agree to float32 rounding, and each repeats bit for bit."""
+    """The three modes agree to float32 rounding, and each repeats bit for bit."""
     shape = CEShape(384, 256, 2000, 704)
     inp = ce_inputs(shape, seed=9)
     outs = []
@@ -117,5 +117,7 @@ def test_ce_modes_agree_and_are_deterministic(mgb_lib):
         assert torch.equal(first[0], r.loss) and torch.equal(first[1], r.d_hidden)
         assert torch.equal(first[2], r.d_emb)
         outs.append(first)
-    assert float((outs[0][0] - outs[1][0]).abs().max()) < CE_LOSS_ABS
-    assert rel_l2(to_np(outs[0][1]), to_np(outs[1][1])) < 2e-2
+    for o in outs[1:]:
+        assert float((outs[0][0] - o[0]).abs().max()) < CE_LOSS_ABS
+        assert rel_l2(to_np(outs[0][1]), to_np(o[1])) < 2e-2
+        assert rel_l2(to_np(outs[0][2]), to_np(o[2])) < 2e-2
