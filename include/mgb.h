@@ -206,6 +206,45 @@ typedef struct {
 mgb_status mgb_gemm(const mgb_gemm_desc* desc, const void* a, const void* b, const void* bias,
                     void* c, void* stream);
 
+/* Fused epilogues of the same product, as the layer uses them [P1 section 2;
+ * P2 section 1]. With acc = alpha * op(A) op(B)^T:
+ *   MGB_EPI_STORE        C = acc (+ bias)                         (as mgb_gemm)
+ *   MGB_EPI_BIAS_GELU    u = acc + bias; C = u; C2 = gelu_erf(u)  (C2 [M, N])
+ *   MGB_EPI_BIAS_SWIGLU  u = acc + bias, the N columns interleaved gate/up in
+ *                        blocks of glu_block; C = u [M, N];
+ *                        C2 = silu(gate) * up [M, N/2]
+ *   MGB_EPI_BIAS_RESID   C = resid + acc + bias                   (resid [M, N])
+ *   MGB_EPI_DGELU        C = acc * gelu_erf'(aux)                 (aux = u [M, N])
+ *   MGB_EPI_DSWIGLU      acc = d(activation) [M, N]; aux = u [M, 2N] interleaved;
+ *                        C [M, 2N] = the interleaved (d gate, d up)
+ *   MGB_EPI_F32          C (float32) = (accumulate ? C : 0) + acc (+ bias); C2,
+ *                        if not NULL, = C rounded to dtype
+ * bias, C2, resid and aux have the dtype of A and B (bf16 or float32); NULL for
+ * the ones an epilogue does not use. `g.c_f32` is ignored (MGB_EPI_F32 selects
+ * the float32 output); `g.accumulate` needs MGB_EPI_F32. glu_block: bf16 needs
+ * a multiple of 32 that divides 128. Errors as mgb_gemm, plus
+ * MGB_ERR_INVALID_ARG for an unknown epilogue or a missing pointer. */
+typedef enum {
+  MGB_EPI_STORE = 0,
+  MGB_EPI_BIAS_GELU = 1,
+  MGB_EPI_BIAS_SWIGLU = 2,
+  MGB_EPI_BIAS_RESID = 3,
+  MGB_EPI_DGELU = 4,
+  MGB_EPI_DSWIGLU = 5,
+  MGB_EPI_F32 = 6
+} mgb_epilogue;
+
+typedef struct {
+  mgb_gemm_desc g;
+  int32_t epilogue;  /* mgb_epilogue */
+  int32_t glu_block;
+  int64_t ldc2, ldr, ldaux; /* in elements */
+} mgb_gemm_ex_desc;
+
+mgb_status mgb_gemm_ex(const mgb_gemm_ex_desc* desc, const void* a, const void* b,
+                       const void* bias, void* c, void* c2, const void* resid, const void* aux,
+                       void* stream);
+
 /* LayerNorm over the last dim [P1 section 2, F.layer_norm(x, (hidden,))]:
  * y = gamma*(x-mean)*rstd + beta, biased variance. mean/rstd [rows] f32
  * (may be NULL). gamma/beta NULL = no affine. */

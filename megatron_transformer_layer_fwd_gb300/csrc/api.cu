@@ -719,6 +719,31 @@ mgb_status mgb_gemm(const mgb_gemm_desc* d, const void* a, const void* b, const 
   return gemm_launch(g, as_stream(stream));
 }
 
+mgb_status mgb_gemm_ex(const mgb_gemm_ex_desc* e, const void* a, const void* b, const void* bias,
+                       void* c, void* c2, const void* resid, const void* aux, void* stream) {
+  if (e == nullptr) return MGB_ERR_INVALID_ARG;
+  if (fault_injected()) return MGB_ERR_INVALID_ARG;
+  const mgb_gemm_desc* d = &e->g;
+  if (e->epilogue < MGB_EPI_STORE || e->epilogue > MGB_EPI_F32) return MGB_ERR_INVALID_ARG;
+  if ((d->a_major | d->b_major) & ~1) return MGB_ERR_INVALID_ARG;
+  // the public values are the library's own epilogue codes
+  static_assert((int)MGB_EPI_BIAS_SWIGLU == (int)EPI_BIAS_SWIGLU && (int)MGB_EPI_F32 == (int)EPI_F32,
+                "epilogue codes");
+  if (d->accumulate && e->epilogue != MGB_EPI_F32) return MGB_ERR_INVALID_ARG;
+  GemmArgs g = mk_gemm(d->dtype, d->m, d->n, d->k, d->a_major, a, d->lda, d->b_major, b, d->ldb,
+                       e->epilogue, c, d->ldc);
+  g.bias = bias;
+  g.alpha = d->alpha;
+  g.accumulate = d->accumulate;
+  g.C2 = c2; g.ldc2 = e->ldc2;
+  g.resid = resid; g.ldr = e->ldr;
+  g.aux = aux; g.ldaux = e->ldaux;
+  g.glu_block = e->glu_block;
+  MGB_TRY(gemm_check(g));
+  MGB_TRY(check_arch());
+  return gemm_launch(g, as_stream(stream));
+}
+
 mgb_status mgb_layernorm_fwd(int32_t rows, int32_t cols, int32_t dtype, float eps, const void* x,
                              const void* gamma, const void* beta, void* y, float* mean, float* rstd,
                              void* stream) {

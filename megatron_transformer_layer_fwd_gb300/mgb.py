@@ -32,6 +32,8 @@ MGB_CE_STREAM, MGB_CE_FUSED, MGB_CE_RESIDENT = 0, 1, 2
 MGB_PRE_LN, MGB_POST_LN = 0, 1
 MGB_GELU_ERF, MGB_SWIGLU = 0, 1
 MGB_K_MAJOR, MGB_MN_MAJOR = 0, 1
+(MGB_EPI_STORE, MGB_EPI_BIAS_GELU, MGB_EPI_BIAS_SWIGLU, MGB_EPI_BIAS_RESID, MGB_EPI_DGELU,
+ MGB_EPI_DSWIGLU, MGB_EPI_F32) = range(7)
 
 _WEIGHT_FIELDS = ("w_qkv", "b_qkv", "w_o", "b_o", "w_1", "b_1", "w_2", "b_2",
                   "ln1_g", "ln1_b", "ln2_g", "ln2_b")
@@ -71,6 +73,11 @@ class GemmDesc(ctypes.Structure):
                 ("alpha", ctypes.c_float)]
 
 
+class GemmExDesc(ctypes.Structure):
+    _fields_ = [("g", GemmDesc), ("epilogue", ctypes.c_int32), ("glu_block", ctypes.c_int32),
+                ("ldc2", ctypes.c_int64), ("ldr", ctypes.c_int64), ("ldaux", ctypes.c_int64)]
+
+
 _lib = None
 
 
@@ -94,6 +101,7 @@ def load() -> ctypes.CDLL:
             "mgb_vocab_ce_sizes": [ctypes.POINTER(CEDesc), PSZ],
             "mgb_vocab_ce_fwd_bwd": [ctypes.POINTER(CEDesc), P, P, P, P, P, P, P, P, P, SZ, P],
             "mgb_gemm": [ctypes.POINTER(GemmDesc), P, P, P, P, P],
+            "mgb_gemm_ex": [ctypes.POINTER(GemmExDesc), P, P, P, P, P, P, P, P],
             "mgb_layernorm_fwd": [I32, I32, I32, F32, P, P, P, P, P, P, P],
             "mgb_layernorm_bwd": [I32, I32, I32, P, P, P, P, P, P, P, P, P, P, SZ, P],
             "mgb_layernorm_bwd_noalloc": [I32, I32, I32, P, P, P, P, P, P, P, P, P, P],
@@ -232,6 +240,11 @@ def mgb_vocab_ce_fwd_bwd(desc: CEDesc, hidden, emb, targets, loss_per_token, los
 def mgb_gemm(desc: GemmDesc, a, b, bias, c, stream=None) -> None:
     _check(load().mgb_gemm(ctypes.byref(desc), _ptr(a), _ptr(b), _ptr(bias), _ptr(c), _stream(stream)),
            "mgb_gemm")
+
+
+def mgb_gemm_ex(desc: GemmExDesc, a, b, bias, c, c2=None, resid=None, aux=None, stream=None) -> None:
+    _check(load().mgb_gemm_ex(ctypes.byref(desc), _ptr(a), _ptr(b), _ptr(bias), _ptr(c), _ptr(c2),
+                              _ptr(resid), _ptr(aux), _stream(stream)), "mgb_gemm_ex")
 
 
 def mgb_layernorm_fwd(rows: int, cols: int, dtype: int, eps: float, x, gamma, beta, y, mean, rstd,

@@ -120,6 +120,29 @@ def test_gemm_validation(lib):
     assert lib.mgb_gemm(ctypes.byref(d), 4096, 4096, None, 4096, None) == mgb.MGB_ERR_INVALID_ARG
 
 
+def test_gemm_ex_validation(lib):
+    """Fused-epilogue GEMM: every error is returned before any device work."""
+    g = mgb.GemmDesc(m=256, n=256, k=64, a_major=0, b_major=0, lda=64, ldb=64, ldc=256,
+                     dtype=mgb.MGB_BF16, c_f32=0, accumulate=0, alpha=1.0)
+    e = mgb.GemmExDesc(g=g, epilogue=7, glu_block=128, ldc2=128, ldr=256, ldaux=256)
+    call = lambda c2=4096, resid=None, aux=None: lib.mgb_gemm_ex(
+        ctypes.byref(e), 4096, 4096, None, 4096, c2, resid, aux, None)
+    assert call() == mgb.MGB_ERR_INVALID_ARG                 # unknown epilogue
+    e.epilogue = mgb.MGB_EPI_BIAS_GELU
+    assert call(c2=None) == mgb.MGB_ERR_INVALID_ARG          # GELU needs C2
+    e.epilogue = mgb.MGB_EPI_BIAS_RESID
+    assert call(resid=None) == mgb.MGB_ERR_INVALID_ARG       # residual input missing
+    e.epilogue = mgb.MGB_EPI_DSWIGLU
+    assert call(aux=None) == mgb.MGB_ERR_INVALID_ARG         # u missing
+    e.epilogue, e.glu_block = mgb.MGB_EPI_BIAS_SWIGLU, 96
+    assert call() in (mgb.MGB_ERR_INVALID_ARG, mgb.MGB_ERR_UNSUPPORTED)  # 256 % 192 != 0
+    e.epilogue, e.glu_block = mgb.MGB_EPI_STORE, 128
+    e.g.accumulate = 1                                       # accumulate needs MGB_EPI_F32
+    assert call() == mgb.MGB_ERR_INVALID_ARG
+    e.g.accumulate, e.g.a_major = 0, 2
+    assert call() == mgb.MGB_ERR_INVALID_ARG
+
+
 def test_injected_validation_fault(lib, monkeypatch):
     """MGB_FAULT=validate makes every descriptor check fail (host-side fault injection)."""
     d = _desc()
