@@ -26,6 +26,11 @@ Sources (web pages on the subject, cited by title and section):
     summed over shards; tied input/output table), section 4 (vocab-parallel
     cross-entropy from per-shard max, target logit and sum-exp partials;
     backward softmax - onehot).
+  * "02 - How a whole Transformer block is split", section 5 (the TP RNG
+    tracker: data-parallel, model-parallel and expert-parallel generator
+    states, fork, replay in recomputation), with Philox4x32-10 (Salmon et
+    al., "Parallel random numbers: as easy as 1, 2, 3", SC 2011) as the
+    counter-based generator (dropout.py).
   * "Megatron-LM" notes, split strategy section: attention cost grows with
     batch*seq^2*heads*head_dim.
 
@@ -40,10 +45,12 @@ from .attention import attention_fwd, attention_bwd
 from .layer import block_fwd, block_bwd, block_fwd_rows
 from .cross_entropy import ce_full, ce_chunked, ce_grads, ce_rows
 from .embedding import embedding_fwd, embedding_bwd
+from . import dropout
 from . import shard
 
 __all__ = [
     "ln_fwd", "ln_bwd", "gelu", "gelu_grad", "silu", "silu_grad", "swiglu_fwd", "swiglu_bwd",
     "glu_split", "attention_fwd", "attention_bwd", "block_fwd", "block_bwd", "block_fwd_rows",
-    "ce_full", "ce_chunked", "ce_grads", "ce_rows", "shard",
+    "ce_full", "ce_chunked", "ce_grads", "ce_rows", "embedding_fwd", "embedding_bwd", "dropout",
+    "shard",
 ]

@@ -19,6 +19,11 @@ dS_ij = P_ij (dP_ij - sum_k P_ik dP_ik) with dP = dO V^T:
     dV_g += P^T dO,  dQ = dS K_g / sqrt(d),  dK_g += dS^T Q_h / sqrt(d),
 summing over the query heads of each group.
 
+Dropout on the probabilities ("02 - How a whole Transformer block is split",
+section 5: inside the tensor-parallel region), given a keep mask M and scale
+s: O_h = (P o M s) V_g; the LSE is that of P. Backward: dV_g += (P o M s)^T dO,
+dP = (dO V_g^T) o M s, then dS as above.
+
 Test infrastructure only.
 """
 import numpy as np
@@ -40,8 +45,9 @@ def _softmax(s):
     return p / l, (m + np.log(l))[:, 0]
 
 
-def attention_fwd(q, k, v, causal=False):
-    """q [B, nq, S, d]; k, v [B, nkv, S, d] -> (o [B, nq, S, d], lse [B, nq, S])."""
+def attention_fwd(q, k, v, causal=False, keep=None, scale=1.0):
+    """q [B, nq, S, d]; k, v [B, nkv, S, d] -> (o [B, nq, S, d], lse [B, nq, S]).
+    keep: optional dropout keep mask [B, nq, S, S] (kept probabilities x scale)."""
     B, nq, S, d = q.shape
     nkv = k.shape[1]
     assert nq % nkv == 0
@@ -52,12 +58,14 @@ def attention_fwd(q, k, v, causal=False):
         for h in range(nq):
             g = h // rep
             p, lse[b, h] = _softmax(_scores(q[b, h], k[b, g], causal))
+            if keep is not None:
+                p = np.where(keep[b, h], p * scale, 0.0)
             o[b, h] = p @ v[b, g]
     return o, lse
 
 
-def attention_bwd(do, q, k, v, causal=False):
-    """Gradients (dq, dk, dv) of sum(do * attention_fwd(q, k, v)[0])."""
+def attention_bwd(do, q, k, v, causal=False, keep=None, scale=1.0):
+    """Gradients (dq, dk, dv) of sum(do * attention_fwd(q, k, v, causal, keep, scale)[0])."""
     B, nq, S, d = q.shape
     nkv = k.shape[1]
     rep = nq // nkv
@@ -68,8 +76,11 @@ def attention_bwd(do, q, k, v, causal=False):
         for h in range(nq):
             g = h // rep
             p, _ = _softmax(_scores(q[b, h], k[b, g], causal))
-            dv[b, g] += p.T @ do[b, h]
+            pd = p if keep is None else np.where(keep[b, h], p * scale, 0.0)
+            dv[b, g] += pd.T @ do[b, h]
             dp = do[b, h] @ v[b, g].T
+            if keep is not None:
+                dp = np.where(keep[b, h], dp * scale, 0.0)
             ds = p * (dp - (p * dp).sum(axis=-1, keepdims=True))
             dq[b, h] = ds @ k[b, g] / np.sqrt(d)
             dk[b, g] += ds.T @ q[b, h] / np.sqrt(d)

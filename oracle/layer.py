@@ -22,6 +22,15 @@ projection Wo (linear_proj, "02 ...", section 2) maps the nq*d concatenated
 head outputs back to H. act is erf-GELU, or SwiGLU on the interleaved fc1
 output (see activations.py).
 
+Dropout ("02 - How a whole Transformer block is split", section 5), when
+`drop` is given (masks from oracle/dropout.py): on the attention
+probabilities (attention.py), and on the outputs of the output projection and
+of fc2 before their residual adds:
+      h = x + D_proj(O Wo^T + bo),   y = h + D_fc2(a W2^T + b2)   (Pre-LN)
+(Post-LN likewise inside LN1 / LN2), D(z) = z o M s. The backward passes the
+residual gradient through unchanged and multiplies the sublayer branch's
+gradient by M s.
+
 The backward is written out by hand (no autograd), in reverse order:
   fc2:  db2 = sum_t dr2, dW2 = dr2^T a, da = dr2 W2
   act:  du = da * gelu'(u)   |  swiglu_bwd(da, u)
@@ -70,11 +79,20 @@ def _act_bwd(da, u, cfg):
     return swiglu_bwd(da, u, cfg.glu_block) if cfg.act == "swiglu" else da * gelu_grad(u)
 
 
-def block_fwd(cfg, w, x):
-    """Forward of one layer. Returns (y [T, H], cache for block_bwd)."""
+def _drop(z, site):
+    if site is None:
+        return z
+    keep, scale = site
+    return np.where(keep, z * scale, 0.0)
+
+
+def block_fwd(cfg, w, x, drop=None):
+    """Forward of one layer. Returns (y [T, H], cache for block_bwd).
+    drop: optional {"attn": (keep, scale) or None, "proj": ..., "fc2": ...}."""
     x = np.asarray(x, dtype=np.float64)
     eps = cfg.ln_eps
-    c = {"x": x}
+    drop = drop or {}
+    c = {"x": x, "drop": drop}
     if cfg.norm_pos == "pre":
         xn, c["mu1"], c["rs1"] = ln_fwd(x, w["ln1_g"], w["ln1_b"], eps)
         a_in = xn
@@ -83,11 +101,12 @@ def block_fwd(cfg, w, x):
     c["a_in"] = a_in
     qkv = _lin(a_in, w["w_qkv"], w["b_qkv"])
     q, k, v = _split_heads(qkv, cfg)
-    o, c["lse"] = attention_fwd(q, k, v, cfg.causal)
+    ad = drop.get("attn")
+    o, c["lse"] = attention_fwd(q, k, v, cfg.causal, *(ad if ad is not None else (None, 1.0)))
     c["q"], c["k"], c["v"] = q, k, v
     O = _merge_heads(o)
     c["O"] = O
-    r1 = x + _lin(O, w["w_o"], w["b_o"])
+    r1 = x + _drop(_lin(O, w["w_o"], w["b_o"]), drop.get("proj"))
     if cfg.norm_pos == "pre":
         h = r1
         f_in, c["mu2"], c["rs2"] = ln_fwd(h, w["ln2_g"], w["ln2_b"], eps)
@@ -99,7 +118,7 @@ def block_fwd(cfg, w, x):
     u = _lin(f_in, w["w_1"], w["b_1"])
     a = _act(u, cfg)
     c["u"], c["a"] = u, a
-    r2 = h + _lin(a, w["w_2"], w["b_2"])
+    r2 = h + _drop(_lin(a, w["w_2"], w["b_2"]), drop.get("fc2"))
     if cfg.norm_pos == "pre":
         y = r2
     else:
@@ -119,10 +138,13 @@ def block_bwd(cfg, w, c, dy):
         dr2 = dy
     else:
         dr2, g["ln2_g"], g["ln2_b"] = ln_bwd(dy, c["r2"], c["mu2"], c["rs2"], w["ln2_g"])
-    # fc2 (row-parallel linear in the pages; here the whole K range at once)
-    g["b_2"] = dr2.sum(axis=0) if w["b_2"] is not None else None
-    g["w_2"] = dr2.T @ c["a"]
-    da = dr2 @ w["w_2"]
+    drop = c.get("drop") or {}
+    # fc2 (row-parallel linear in the pages; here the whole K range at once),
+    # through its dropout
+    dz2 = _drop(dr2, drop.get("fc2"))
+    g["b_2"] = dz2.sum(axis=0) if w["b_2"] is not None else None
+    g["w_2"] = dz2.T @ c["a"]
+    da = dz2 @ w["w_2"]
     du = _act_bwd(da, c["u"], cfg)
     g["b_1"] = du.sum(axis=0) if w["b_1"] is not None else None
     g["w_1"] = du.T @ c["f_in"]
@@ -133,12 +155,15 @@ def block_bwd(cfg, w, c, dy):
     else:
         dh = df_in + dr2             # h feeds fc1 and the fc2 residual add
         dr1, g["ln1_g"], g["ln1_b"] = ln_bwd(dh, c["r1"], c["mu1"], c["rs1"], w["ln1_g"])
-    g["b_o"] = dr1.sum(axis=0) if w["b_o"] is not None else None
-    g["w_o"] = dr1.T @ c["O"]
-    dO = dr1 @ w["w_o"]
+    dz1 = _drop(dr1, drop.get("proj"))
+    g["b_o"] = dz1.sum(axis=0) if w["b_o"] is not None else None
+    g["w_o"] = dz1.T @ c["O"]
+    dO = dz1 @ w["w_o"]
     B, nq, S, d = c["q"].shape
     do = dO.reshape(B, S, nq, d).transpose(0, 2, 1, 3)
-    dq, dk, dv = attention_bwd(do, c["q"], c["k"], c["v"], cfg.causal)
+    ad = drop.get("attn")
+    dq, dk, dv = attention_bwd(do, c["q"], c["k"], c["v"], cfg.causal,
+                               *(ad if ad is not None else (None, 1.0)))
     dqkv = np.concatenate([_merge_heads(dq), _merge_heads(dk), _merge_heads(dv)], axis=1)
     g["b_qkv"] = dqkv.sum(axis=0) if w["b_qkv"] is not None else None
     g["w_qkv"] = dqkv.T @ c["a_in"]
