@@ -21,9 +21,9 @@ Readings (the pages fix no generator):
     into four bytes, lowest byte first. Byte position `offset + e` is the
     uniform of element e of a site, so a mask is a pure function of
     (seed, offset, element index): replay is exact by construction.
-  * An element is kept iff its byte < round((1 - p) * 256); kept elements are
-    scaled by 256 / round((1 - p) * 256) (the realized keep probability is a
-    multiple of 1/256).
+  * An element is kept iff its byte < thr = floor((1 - p) * 256 + 1/2)
+    (round half up, in double precision from the caller's p); kept elements
+    are scaled by 256 / thr (the realized keep probability is thr / 256).
   * The tracker's draw(n) hands out the current state's (seed, offset) and
     advances the offset by n rounded up to a multiple of 16 (one counter).
   * Sites of the layer: the attention probabilities (inside the TP region;
@@ -86,7 +86,7 @@ def keep_threshold(p):
     """Bytes below this value are kept."""
     if not 0.0 <= p < 1.0:
         raise ValueError("dropout probability must be in [0, 1)")
-    return int(round((1.0 - p) * 256.0))
+    return int(np.floor((1.0 - float(p)) * 256.0 + 0.5))
 
 
 def keep_scale(p):
