@@ -64,6 +64,17 @@ typedef enum { MGB_F32 = 0, MGB_BF16 = 1 } mgb_dtype;
 typedef enum { MGB_PRE_LN = 0, MGB_POST_LN = 1 } mgb_norm_pos;
 typedef enum { MGB_GELU_ERF = 0, MGB_SWIGLU = 1 } mgb_act;
 
+/* State of the counter-based generator behind dropout [P2 section 5]: the
+ * stream is Philox4x32-10 (Salmon et al., SC 2011) with key = the seed's two
+ * 32-bit halves and counters (q, 0, 0, 0), q = 0, 1, ..., each giving 16
+ * bytes (its words in order, lowest byte first). Element e of a dropout site
+ * at state (seed, offset) uses the byte at stream position offset + e; it is
+ * kept iff the byte < floor((1 - p) * 256 + 1/2), and kept values are scaled
+ * by 256 / that threshold. offset must be a multiple of 16. */
+typedef struct {
+  uint64_t seed, offset;
+} mgb_rng_state;
+
 /* Shape and options of one layer [P1 section 2; P2 sections 1-2].
  * Enum-valued fields are int32_t so the struct layout is fixed. */
 typedef struct {
@@ -78,6 +89,15 @@ typedef struct {
   int32_t has_bias;                        /* 1: the four linears have biases */
   int32_t glu_block;                       /* SwiGLU interleave block (fc1 columns) */
   float ln_eps;                            /* LayerNorm epsilon (1e-5) */
+  /* Dropout [P2 section 5]: hidden_dropout on the outputs of the output
+   * projection and of fc2 before their residual adds (element t*H + c of the
+   * [T, H] branch), attn_dropout on the attention probabilities. 0 = off.
+   * bf16 only; attn_dropout > 0 returns MGB_ERR_UNSUPPORTED. rng_*: the
+   * generator states of the three sites (mgb_block_dropout_plan draws them
+   * from a tracker); the backward must get the forward's values and
+   * regenerates the same masks. */
+  float hidden_dropout, attn_dropout;
+  mgb_rng_state rng_attn, rng_proj, rng_fc2;
 } mgb_block_desc;
 
 /* Layer parameters. Shapes (H hidden, d head_dim, W = ffn or 2*ffn for SwiGLU):
@@ -98,6 +118,38 @@ typedef struct {
   void *w_qkv, *b_qkv, *w_o, *b_o, *w_1, *b_1, *w_2, *b_2;
   void *ln1_g, *ln1_b, *ln2_g, *ln2_b;
 } mgb_block_grads;
+
+/* The tensor-parallel RNG tracker [P2 section 5]: three generator states,
+ * one current. Outside the TP region activations are replicated, so dropout
+ * there draws from the data-parallel state (seed: the same on every TP rank);
+ * inside it each rank holds a different shard and draws from the
+ * model-parallel state (seed + 2718 + tp_rank); MoE experts use
+ * seed + 1024 + 100 * ep_rank + etp_rank. Host-only calls, no device work. */
+typedef enum {
+  MGB_RNG_DATA_PARALLEL = 0,
+  MGB_RNG_MODEL_PARALLEL = 1,
+  MGB_RNG_EXPERT_PARALLEL = 2
+} mgb_rng_kind;
+
+typedef struct {
+  mgb_rng_state state[3]; /* indexed by mgb_rng_kind */
+  int32_t current;        /* the state draws come from */
+} mgb_rng_tracker;
+
+/* All three states at offset 0; the data-parallel one current. */
+mgb_status mgb_rng_tracker_init(mgb_rng_tracker* t, uint64_t seed, int32_t tp_rank,
+                                int32_t ep_rank, int32_t etp_rank);
+/* Makes `kind` current; returns the previous current kind (pass it to
+ * mgb_rng_restore), or MGB_ERR_INVALID_ARG. */
+int32_t mgb_rng_fork(mgb_rng_tracker* t, int32_t kind);
+mgb_status mgb_rng_restore(mgb_rng_tracker* t, int32_t prev);
+/* *out = the current state; its offset then advances by n rounded up to 16. */
+mgb_status mgb_rng_draw(mgb_rng_tracker* t, uint64_t n, mgb_rng_state* out);
+/* Fills desc->rng_attn (inside the TP region: forked to the model-parallel
+ * state; B * n_q_heads * S * Sp elements, element ((b*nq + h)*S + i)*Sp + j,
+ * Sp = S rounded up to 16), then rng_proj and rng_fc2 (B*S*H each) from the
+ * current state. Every call draws all three, whatever the probabilities. */
+mgb_status mgb_block_dropout_plan(mgb_block_desc* desc, mgb_rng_tracker* t);
 
 /* Sizes in bytes of the `saved` buffer (written by fwd, read by bwd) and of
  * the scratch workspaces of fwd and bwd. Host-only; no device work. */
@@ -354,6 +406,16 @@ mgb_status mgb_attention_bwd(int32_t batch, int32_t seq, int32_t n_q_heads, int3
 /* ---- status and diagnostics ---- */
 
 const char* mgb_status_string(mgb_status s);
+
+/* The generator's bytes at stream positions rng.offset .. + n - 1 of seed
+ * rng.seed (any offset) into out[n] (device). */
+mgb_status mgb_philox_bytes(uint64_t seed, uint64_t offset, uint64_t n, void* out, void* stream);
+
+/* y = dropout(x) over a [rows, cols] site at state rng (element r*cols + c),
+ * probability p in [0, 1); x, y of dtype with leading dims ldx, ldy (y may be
+ * x). The same call with the same rng is the backward (dx from dy). */
+mgb_status mgb_dropout(int64_t rows, int64_t cols, int32_t dtype, float p, mgb_rng_state rng,
+                       const void* x, int64_t ldx, void* y, int64_t ldy, void* stream);
 
 /* Synchronises `stream`, then returns and clears the current device's error
  * word (MGB_ERR_DEVICE_TIMEOUT if a bounded device wait ran out since the last

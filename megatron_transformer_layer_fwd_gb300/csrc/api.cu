@@ -164,9 +164,20 @@ struct Plan {
   size_t saved;
   // backward workspace
   size_t w_dffn, w_dh, w_dr2, w_du, w_dO, w_dqkv, w_dxn, w_delta, w_cparts, w_lparts;
+  size_t w_dz1, w_dz2;  // hidden dropout: the projection's / fc2's branch gradients
   size_t bwd;
   int cparts, lparts;
+  bool hdrop;
 };
+
+// Dropout of the hidden branch fused into a residual epilogue.
+void set_hidden_dropout(const mgb_block_desc* d, const mgb_rng_state& rng, GemmArgs* g) {
+  if (!(d->hidden_dropout > 0.0f)) return;
+  g->drop_thr = dropout_threshold(d->hidden_dropout);
+  g->drop_scale = 256.0f / (float)g->drop_thr;
+  g->drop_seed = rng.seed;
+  g->drop_offset = rng.offset;
+}
 
 mgb_status validate_desc(const mgb_block_desc* d) {
   if (d == nullptr) return MGB_ERR_INVALID_ARG;
@@ -198,6 +209,17 @@ mgb_status validate_desc(const mgb_block_desc* d) {
   // LayerNorm keeps a row in registers (at most 1024 threads x 4 vectors of 16
   // bytes) and its backward keeps dgamma/dbeta partials of a row in shared memory
   if (d->hidden > 16384) return MGB_ERR_UNSUPPORTED;
+  // dropout: probabilities in [0, 1); the hidden sites are fused into the bf16
+  // residual epilogues (whole 16-element stream blocks per 32-column chunk)
+  if (!(d->hidden_dropout >= 0.0f && d->hidden_dropout < 1.0f) ||
+      !(d->attn_dropout >= 0.0f && d->attn_dropout < 1.0f))
+    return MGB_ERR_INVALID_ARG;
+  if (d->attn_dropout > 0.0f) return MGB_ERR_UNSUPPORTED;
+  if (d->hidden_dropout > 0.0f) {
+    if (d->dtype != MGB_BF16) return MGB_ERR_UNSUPPORTED;
+    if (d->hidden % 16 || d->rng_proj.offset % 16 || d->rng_fc2.offset % 16)
+      return MGB_ERR_INVALID_ARG;
+  }
   return MGB_OK;
 }
 
@@ -242,6 +264,9 @@ void make_plan(const mgb_block_desc* d, Plan* p) {
   p->w_delta = take(attn_bwd_ws_bytes(p->B, p->S, p->nq));
   p->w_cparts = take(4 * (size_t)p->cparts * maxN);
   p->w_lparts = take(4 * 2 * (size_t)p->lparts * p->H);
+  p->hdrop = d->hidden_dropout > 0.0f;
+  p->w_dz1 = p->hdrop ? take(es * T * p->H) : 0;
+  p->w_dz2 = p->hdrop ? take(es * T * p->H) : 0;
   p->bwd = o;
 }
 
@@ -386,6 +411,7 @@ mgb_status mgb_block_fwd(const mgb_block_desc* desc, const mgb_block_weights* w,
   void* r1 = p.pre ? h : at<char>(saved, p.s_r1);
   g = mk_gemm(dt, T, H, p.Dq, 0, O, p.Dq, 0, w->w_o, p.Dq, EPI_BIAS_RESID, r1, H);
   g.bias = w->b_o; g.resid = x; g.ldr = H;
+  set_hidden_dropout(desc, desc->rng_proj, &g);
   MGB_TRY(gemm_launch(g, st));
   const void* f_in;
   if (p.pre) {
@@ -405,6 +431,7 @@ mgb_status mgb_block_fwd(const mgb_block_desc* desc, const mgb_block_weights* w,
   void* r2 = p.pre ? y : at<char>(saved, p.s_r2);
   g = mk_gemm(dt, T, H, p.F, 0, a, p.F, 0, w->w_2, p.F, EPI_BIAS_RESID, r2, H);
   g.bias = w->b_2; g.resid = h; g.ldr = H;
+  set_hidden_dropout(desc, desc->rng_fc2, &g);
   MGB_TRY(gemm_launch(g, st));
   if (!p.pre)
     MGB_TRY(layernorm_fwd_launch(T, H, dt, desc->ln_eps, r2, w->ln2_g, w->ln2_b, y, mu2, rs2, st));
@@ -470,13 +497,20 @@ mgb_status mgb_block_bwd(const mgb_block_desc* desc, const mgb_block_weights* w,
                                  d_r2, gr->ln2_g, gr->ln2_b, lparts, p.lparts, st));
     dr2 = d_r2;
   }
-  // fc2: db2, dW2 = dr2^T a, du = (dr2 W2) * act'(u)
+  // through the hidden dropout of fc2's branch (the residual path keeps dr2)
+  const void* dz2 = dr2;
+  if (p.hdrop) {
+    MGB_TRY(dropout_launch(T, H, dt, desc->hidden_dropout, desc->rng_fc2.seed, desc->rng_fc2.offset,
+                           dr2, H, at<char>(ws, p.w_dz2), H, st));
+    dz2 = at<char>(ws, p.w_dz2);
+  }
+  // fc2: db2, dW2 = dz2^T a, du = (dz2 W2) * act'(u)
   MGB_TRY(lane.fork());
-  if (gr->b_2) MGB_TRY(colsum_launch(T, H, dt, dr2, H, gr->b_2, cparts, p.cparts, s2));
+  if (gr->b_2) MGB_TRY(colsum_launch(T, H, dt, dz2, H, gr->b_2, cparts, p.cparts, s2));
   if (gr->w_2)
-    MGB_TRY(gemm_launch(mk_gemm(dt, H, p.F, T, 1, dr2, H, 1, a, p.F, EPI_STORE, gr->w_2, p.F), s2));
+    MGB_TRY(gemm_launch(mk_gemm(dt, H, p.F, T, 1, dz2, H, 1, a, p.F, EPI_STORE, gr->w_2, p.F), s2));
   {
-    GemmArgs g = mk_gemm(dt, T, p.F, H, 0, dr2, H, 1, w->w_2, p.F,
+    GemmArgs g = mk_gemm(dt, T, p.F, H, 0, dz2, H, 1, w->w_2, p.F,
                          p.swiglu ? EPI_DSWIGLU : EPI_DGELU, du, p.W);
     g.aux = u; g.ldaux = p.W; g.glu_block = desc->glu_block;
     MGB_TRY(gemm_launch(g, st));
@@ -502,12 +536,19 @@ mgb_status mgb_block_bwd(const mgb_block_desc* desc, const mgb_block_weights* w,
                                  nullptr, d_ffn, gr->ln1_g, gr->ln1_b, lparts, p.lparts, st));
     dr1 = d_ffn;
   }
-  // output projection: dbo, dWo = dr1^T O, dO = dr1 Wo
+  // through the hidden dropout of the projection's branch
+  const void* dz1 = dr1;
+  if (p.hdrop) {
+    MGB_TRY(dropout_launch(T, H, dt, desc->hidden_dropout, desc->rng_proj.seed,
+                           desc->rng_proj.offset, dr1, H, at<char>(ws, p.w_dz1), H, st));
+    dz1 = at<char>(ws, p.w_dz1);
+  }
+  // output projection: dbo, dWo = dz1^T O, dO = dz1 Wo
   MGB_TRY(lane.fork());
-  if (gr->b_o) MGB_TRY(colsum_launch(T, H, dt, dr1, H, gr->b_o, cparts, p.cparts, s2));
+  if (gr->b_o) MGB_TRY(colsum_launch(T, H, dt, dz1, H, gr->b_o, cparts, p.cparts, s2));
   if (gr->w_o)
-    MGB_TRY(gemm_launch(mk_gemm(dt, H, p.Dq, T, 1, dr1, H, 1, O, p.Dq, EPI_STORE, gr->w_o, p.Dq), s2));
-  MGB_TRY(gemm_launch(mk_gemm(dt, T, p.Dq, H, 0, dr1, H, 1, w->w_o, p.Dq, EPI_STORE, dO, p.Dq), st));
+    MGB_TRY(gemm_launch(mk_gemm(dt, H, p.Dq, T, 1, dz1, H, 1, O, p.Dq, EPI_STORE, gr->w_o, p.Dq), s2));
+  MGB_TRY(gemm_launch(mk_gemm(dt, T, p.Dq, H, 0, dz1, H, 1, w->w_o, p.Dq, EPI_STORE, dO, p.Dq), st));
   // attention backward into the fused dqkv buffer
   {
     AttnArgs at_{};
@@ -742,6 +783,23 @@ mgb_status mgb_gemm_ex(const mgb_gemm_ex_desc* e, const void* a, const void* b, 
   MGB_TRY(gemm_check(g));
   MGB_TRY(check_arch());
   return gemm_launch(g, as_stream(stream));
+}
+
+mgb_status mgb_philox_bytes(uint64_t seed, uint64_t offset, uint64_t n, void* out, void* stream) {
+  if (n > 0 && out == nullptr) return MGB_ERR_INVALID_ARG;
+  MGB_TRY(check_arch());
+  return philox_bytes_launch(seed, offset, n, out, as_stream(stream));
+}
+
+mgb_status mgb_dropout(int64_t rows, int64_t cols, int32_t dtype, float p, mgb_rng_state rng,
+                       const void* x, int64_t ldx, void* y, int64_t ldy, void* stream) {
+  if (rows < 0 || cols < 0 || !(p >= 0.0f && p < 1.0f)) return MGB_ERR_INVALID_ARG;
+  if (dtype != MGB_BF16 && dtype != MGB_F32) return MGB_ERR_INVALID_ARG;
+  if (rng.offset % 16 != 0) return MGB_ERR_INVALID_ARG;
+  if (rows > 0 && cols > 0 && (!x || !y || ldx < cols || ldy < cols)) return MGB_ERR_INVALID_ARG;
+  MGB_TRY(check_arch());
+  return dropout_launch(rows, cols, dtype, p, rng.seed, rng.offset, x, ldx, y, ldy,
+                        as_stream(stream));
 }
 
 mgb_status mgb_layernorm_fwd(int32_t rows, int32_t cols, int32_t dtype, float eps, const void* x,

@@ -149,6 +149,33 @@ __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
   asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
                : "memory");
 }
+// ---- counter-based random numbers: Philox4x32-10 (Salmon, Moraes, Dror,
+// Shaw, "Parallel random numbers: as easy as 1, 2, 3", SC 2011). Ten rounds
+// of two 32x32 -> 64-bit products mixed with the other two words and the
+// key; the key is bumped by the Weyl constants between rounds.
+__device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1) {
+#pragma unroll
+  for (int r = 0; r < 10; ++r) {
+    const uint32_t lo0 = 0xD2511F53u * c.x, hi0 = __umulhi(0xD2511F53u, c.x);
+    const uint32_t lo1 = 0xCD9E8D57u * c.z, hi1 = __umulhi(0xCD9E8D57u, c.z);
+    c = make_uint4(hi1 ^ c.y ^ k0, lo1, hi0 ^ c.w ^ k1, lo0);
+    k0 += 0x9E3779B9u;
+    k1 += 0xBB67AE85u;
+  }
+  return c;
+}
+// The 16 uniform bytes at stream positions 16q .. 16q+15 of generator
+// `seed`: counter (q, 0, 0, 0), key = the seed's two 32-bit halves; byte b of
+// the stream block is byte b%4 (lowest first) of word b/4.
+__device__ __forceinline__ uint4 philox_block(uint64_t seed, uint64_t q) {
+  return philox4x32_10(make_uint4((uint32_t)q, (uint32_t)(q >> 32), 0u, 0u), (uint32_t)seed,
+                       (uint32_t)(seed >> 32));
+}
+// keep[i] for the 4 bytes of word w: byte < thr (thr in [0, 256])
+__device__ __forceinline__ bool keep_byte(uint32_t w, int i, uint32_t thr) {
+  return ((w >> (8 * i)) & 0xFFu) < thr;
+}
+
 // ---- CTA pairs (cluster of two; rank 0 leads): tcgen05 with cta_group::2
 __device__ __forceinline__ uint32_t cluster_ctarank() {
   uint32_t r;

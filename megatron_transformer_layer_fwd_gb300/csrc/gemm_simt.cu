@@ -181,6 +181,11 @@ mgb_status gemm_check(const GemmArgs& g) {
                               g.ld_keep < g.N))
       return MGB_ERR_INVALID_ARG;
   }
+  if (g.drop_thr < 256) {
+    // dropout in the residual epilogue: bf16, whole 16-element stream blocks
+    if (g.epi != EPI_BIAS_RESID || g.dtype != MGB_BF16) return MGB_ERR_UNSUPPORTED;
+    if (g.N % 16 || g.drop_offset % 16 || g.drop_thr == 0) return MGB_ERR_INVALID_ARG;
+  }
   return MGB_OK;
 }
 

@@ -70,6 +70,9 @@ struct EpiParams {
   float ce_scale;
   bf16* keep;
   int64_t ld_keep;
+  uint32_t drop_thr;
+  float drop_scale;
+  uint64_t drop_seed, drop_offset;
 };
 
 template <int BN, int STAGES>
@@ -272,6 +275,16 @@ __device__ void epilogue_row(const EpiParams& p, uint32_t tmem_row, int row, int
       }
       case EPI_BIAS_RESID: {
         add_bias32(p.bias, n, p.N, acc);
+        if (p.drop_thr < 256) {
+          // dropout on the branch before the residual add: elements
+          // row * N + n .. + 31 are stream bytes of two Philox blocks
+          const uint64_t q = (p.drop_offset + (uint64_t)row * p.N + n) >> 4;
+          const uint4 w0 = philox_block(p.drop_seed, q), w1 = philox_block(p.drop_seed, q + 1);
+          const uint32_t ws[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            acc[j] = keep_byte(ws[j >> 2], j & 3, p.drop_thr) ? acc[j] * p.drop_scale : 0.0f;
+        }
         const bf16* r = p.resid + (int64_t)row * p.ldr + n;
         bf16* c = reinterpret_cast<bf16*>(p.C) + (int64_t)row * p.ldc + n;
 #pragma unroll
@@ -877,6 +890,10 @@ mgb_status gemm_tc_launch(const GemmArgs& g, cudaStream_t st) {
   ep.ce_scale = g.ce_scale;
   ep.keep = static_cast<bf16*>(g.keep);
   ep.ld_keep = g.ld_keep;
+  ep.drop_thr = g.drop_thr;
+  ep.drop_scale = g.drop_scale;
+  ep.drop_seed = g.drop_seed;
+  ep.drop_offset = g.drop_offset;
   ep.tgt_v0 = g.tgt_v0;
   ep.tgt_out = g.tgt_out;
   // Tile: 256 x 256 on a CTA pair when there are enough such tiles to fill

@@ -50,6 +50,12 @@ struct GemmArgs {
   float ce_scale = 1.0f;          // EPI_CE_GRAD: dL/dloss per token
   // EPI_CE_STATS only, may be null: the bf16 logits are also stored here
   void* keep = nullptr; int64_t ld_keep = 0;
+  // EPI_BIAS_RESID only: dropout on acc + bias before the residual add, element
+  // e = row * N + col of the site at stream state (drop_seed, drop_offset);
+  // drop_thr 256 = off (dropout.cu has the definition)
+  uint32_t drop_thr = 256;
+  float drop_scale = 1.0f;
+  uint64_t drop_seed = 0, drop_offset = 0;
 };
 
 // Validates operand geometry for the chosen path; returns MGB_OK or an error.
@@ -111,6 +117,15 @@ inline int ce_combine_blocks(int T) { return (T + 255) / 256; }
 mgb_status ce_grad_launch(int T, int C, int v0, void* logits, int64_t ldl, const int32_t* targets,
                           const float* lse, float scale, cudaStream_t st);
 
+// Dropout (dropout.cu): keep threshold of probability p; y = dropout(x) over
+// a [rows, cols] site at stream state (seed, offset); the raw byte stream.
+uint32_t dropout_threshold(float p);
+mgb_status dropout_launch(int64_t rows, int64_t cols, int dtype, float p, uint64_t seed,
+                          uint64_t offset, const void* x, int64_t ldx, void* y, int64_t ldy,
+                          cudaStream_t st);
+mgb_status philox_bytes_launch(uint64_t seed, uint64_t offset, uint64_t n, void* out,
+                               cudaStream_t st);
+
 // Vocab-parallel embedding (shard rows [v0, v1)); layouts as mgb_embedding_fwd/bwd.
 size_t embedding_bwd_ws(int T, int v0, int v1);
 mgb_status embedding_fwd_launch(int T, int H, int dtype, int v0, int v1, const int32_t* ids,
@@ -129,7 +144,7 @@ int* device_error_word();
 enum ProfKind : int {
   PROF_GEMM_FWD = 0, PROF_GEMM_DGRAD, PROF_GEMM_WGRAD, PROF_GEMM_F32, PROF_ATTN_FWD,
   PROF_ATTN_BWD, PROF_LN_FWD, PROF_LN_BWD, PROF_COLSUM, PROF_CE_STATS, PROF_CE_COMBINE,
-  PROF_CE_GRAD, PROF_GEMM_CE_LOGITS, PROF_EMBEDDING, PROF_KINDS
+  PROF_CE_GRAD, PROF_GEMM_CE_LOGITS, PROF_EMBEDDING, PROF_DROPOUT, PROF_KINDS
 };
 
 // Counts `launches` kernel launches and, when profiling is on, brackets them

@@ -59,7 +59,7 @@ mgb_status drain_locked() {
 const char* kKindNames[PROF_KINDS] = {
     "gemm_tc_fwd",  "gemm_tc_dgrad", "gemm_tc_wgrad", "gemm_f32",  "attn_fwd",   "attn_bwd",
     "layernorm_fwd", "layernorm_bwd", "colsum",       "ce_stats", "ce_combine", "ce_grad",
-    "gemm_tc_ce_logits", "embedding"};
+    "gemm_tc_ce_logits", "embedding", "dropout"};
 
 }  // namespace
 

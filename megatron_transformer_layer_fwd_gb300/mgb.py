@@ -32,6 +32,7 @@ MGB_CE_STREAM, MGB_CE_FUSED, MGB_CE_RESIDENT = 0, 1, 2
 MGB_PRE_LN, MGB_POST_LN = 0, 1
 MGB_GELU_ERF, MGB_SWIGLU = 0, 1
 MGB_K_MAJOR, MGB_MN_MAJOR = 0, 1
+MGB_RNG_DATA_PARALLEL, MGB_RNG_MODEL_PARALLEL, MGB_RNG_EXPERT_PARALLEL = 0, 1, 2
 (MGB_EPI_STORE, MGB_EPI_BIAS_GELU, MGB_EPI_BIAS_SWIGLU, MGB_EPI_BIAS_RESID, MGB_EPI_DGELU,
  MGB_EPI_DSWIGLU, MGB_EPI_F32) = range(7)
 
@@ -45,10 +46,21 @@ class MgbError(RuntimeError):
         super().__init__(f"{where}: {status_string(status)} ({status})")
 
 
+class RngState(ctypes.Structure):
+    _fields_ = [("seed", ctypes.c_uint64), ("offset", ctypes.c_uint64)]
+
+
+class RngTracker(ctypes.Structure):
+    _fields_ = [("state", RngState * 3), ("current", ctypes.c_int32)]
+
+
 class BlockDesc(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in (
         "batch", "seq", "hidden", "n_q_heads", "n_kv_heads", "head_dim", "ffn", "dtype",
-        "norm_pos", "act", "causal", "ln_affine", "has_bias", "glu_block")] + [("ln_eps", ctypes.c_float)]
+        "norm_pos", "act", "causal", "ln_affine", "has_bias", "glu_block")] + [
+        ("ln_eps", ctypes.c_float), ("hidden_dropout", ctypes.c_float),
+        ("attn_dropout", ctypes.c_float), ("rng_attn", RngState), ("rng_proj", RngState),
+        ("rng_fc2", RngState)]
 
 
 class BlockWeights(ctypes.Structure):
@@ -109,6 +121,13 @@ def load() -> ctypes.CDLL:
             "mgb_attention_bwd": [I32, I32, I32, I32, I32, I32, I32, P, P, P, I64, I64, P, P, P,
                                   I64, P, P, P, I64, I64, P, SZ, P],
             "mgb_embedding_fwd": [I32, I32, I32, I32, I32, P, P, P, P],
+            "mgb_rng_tracker_init": [ctypes.POINTER(RngTracker), U64, I32, I32, I32],
+            "mgb_rng_restore": [ctypes.POINTER(RngTracker), I32],
+            "mgb_rng_draw": [ctypes.POINTER(RngTracker), U64, ctypes.POINTER(RngState)],
+            "mgb_block_dropout_plan": [ctypes.POINTER(BlockDesc), ctypes.POINTER(RngTracker)],
+            "mgb_philox_bytes": [U64, U64, U64, P, P],
+            "mgb_dropout": [ctypes.c_int64, ctypes.c_int64, I32, F32, RngState, P, ctypes.c_int64, P,
+                            ctypes.c_int64, P],
             "mgb_embedding_bwd": [I32, I32, I32, I32, I32, P, P, P, I32, P, SZ, P],
             "mgb_device_status": [P],
             "mgb_selftest_wait_timeout": [U64, P],
@@ -117,6 +136,8 @@ def load() -> ctypes.CDLL:
             fn = getattr(lib, name)
             fn.argtypes = args
             fn.restype = ctypes.c_int
+        lib.mgb_rng_fork.argtypes = [ctypes.POINTER(RngTracker), I32]
+        lib.mgb_rng_fork.restype = I32
         lib.mgb_status_string.argtypes = [ctypes.c_int]
         lib.mgb_status_string.restype = ctypes.c_char_p
         lib.mgb_version.argtypes = []
@@ -245,6 +266,43 @@ def mgb_gemm(desc: GemmDesc, a, b, bias, c, stream=None) -> None:
 def mgb_gemm_ex(desc: GemmExDesc, a, b, bias, c, c2=None, resid=None, aux=None, stream=None) -> None:
     _check(load().mgb_gemm_ex(ctypes.byref(desc), _ptr(a), _ptr(b), _ptr(bias), _ptr(c), _ptr(c2),
                               _ptr(resid), _ptr(aux), _stream(stream)), "mgb_gemm_ex")
+
+
+def rng_tracker(seed: int, tp_rank: int = 0, ep_rank: int = 0, etp_rank: int = 0) -> RngTracker:
+    t = RngTracker()
+    _check(load().mgb_rng_tracker_init(ctypes.byref(t), seed, tp_rank, ep_rank, etp_rank),
+           "mgb_rng_tracker_init")
+    return t
+
+
+def mgb_rng_fork(t: RngTracker, kind: int) -> int:
+    prev = load().mgb_rng_fork(ctypes.byref(t), kind)
+    if prev < 0:
+        _check(prev, "mgb_rng_fork")
+    return prev
+
+
+def mgb_rng_restore(t: RngTracker, prev: int) -> None:
+    _check(load().mgb_rng_restore(ctypes.byref(t), prev), "mgb_rng_restore")
+
+
+def mgb_rng_draw(t: RngTracker, n: int) -> RngState:
+    out = RngState()
+    _check(load().mgb_rng_draw(ctypes.byref(t), n, ctypes.byref(out)), "mgb_rng_draw")
+    return out
+
+
+def mgb_block_dropout_plan(desc: BlockDesc, t: RngTracker) -> None:
+    _check(load().mgb_block_dropout_plan(ctypes.byref(desc), ctypes.byref(t)), "mgb_block_dropout_plan")
+
+
+def mgb_philox_bytes(seed: int, offset: int, n: int, out, stream=None) -> None:
+    _check(load().mgb_philox_bytes(seed, offset, n, _ptr(out), _stream(stream)), "mgb_philox_bytes")
+
+
+def mgb_dropout(rows, cols, dtype, p, rng: RngState, x, ldx, y, ldy, stream=None) -> None:
+    _check(load().mgb_dropout(rows, cols, dtype, p, rng, _ptr(x), ldx, _ptr(y), ldy, _stream(stream)),
+           "mgb_dropout")
 
 
 def mgb_layernorm_fwd(rows: int, cols: int, dtype: int, eps: float, x, gamma, beta, y, mean, rstd,

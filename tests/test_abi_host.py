@@ -143,6 +143,65 @@ def test_gemm_ex_validation(lib):
     assert call() == mgb.MGB_ERR_INVALID_ARG
 
 
+def test_rng_tracker_matches_the_oracle_tracker(lib):
+    """Seeds of the three states, fork / restore and draws (host-only calls)."""
+    from oracle import dropout as od
+    t = mgb.rng_tracker(1234, tp_rank=3, ep_rank=2, etp_rank=1)
+    o = od.model_parallel_seed(1234, tp_rank=3, ep_rank=2, etp_rank=1)
+    assert [t.state[i].seed for i in range(3)] == [o.states[k][0] for k in (o.DATA, o.MODEL, o.EXPERT)]
+    assert t.current == mgb.MGB_RNG_DATA_PARALLEL
+    for n in (10, 17, 1, 0, 4096):
+        r = mgb.mgb_rng_draw(t, n)
+        assert (r.seed, r.offset) == o.draw(n)
+    prev = mgb.mgb_rng_fork(t, mgb.MGB_RNG_MODEL_PARALLEL)
+    with o.fork(o.MODEL):
+        r = mgb.mgb_rng_draw(t, 33)
+        assert (r.seed, r.offset) == o.draw(33)
+    mgb.mgb_rng_restore(t, prev)
+    assert t.current == mgb.MGB_RNG_DATA_PARALLEL
+    assert lib.mgb_rng_fork(ctypes.byref(t), 3) == mgb.MGB_ERR_INVALID_ARG
+    assert lib.mgb_rng_restore(ctypes.byref(t), -2) == mgb.MGB_ERR_INVALID_ARG
+
+
+def test_block_dropout_plan_matches_the_oracle(lib):
+    from oracle import dropout as od
+    shape = LayerShape(2, 37, 64, 4, 2, 16, 96)
+    d = mgb.block_desc(shape)
+    t = mgb.rng_tracker(99, tp_rank=1)
+    o = od.model_parallel_seed(99, tp_rank=1)
+    for _ in range(2):  # two steps: the offsets move on
+        mgb.mgb_block_dropout_plan(d, t)
+        want = od.layer_dropout(shape, o, 0.0, 0.0)["states"]
+        assert (d.rng_attn.seed, d.rng_attn.offset) == want["attn"]
+        assert (d.rng_proj.seed, d.rng_proj.offset) == want["proj"]
+        assert (d.rng_fc2.seed, d.rng_fc2.offset) == want["fc2"]
+    assert d.rng_attn.seed == 99 + 2718 + 1 and d.rng_proj.seed == 99
+
+
+def test_dropout_desc_validation(lib):
+    s = ctypes.c_size_t()
+    d = _desc()
+    d.hidden_dropout = 1.0
+    assert lib.mgb_block_sizes(ctypes.byref(d), ctypes.byref(s), None, None) == mgb.MGB_ERR_INVALID_ARG
+    d.hidden_dropout = -0.1
+    assert lib.mgb_block_sizes(ctypes.byref(d), ctypes.byref(s), None, None) == mgb.MGB_ERR_INVALID_ARG
+    d.hidden_dropout, d.attn_dropout = 0.0, 0.1
+    assert lib.mgb_block_sizes(ctypes.byref(d), ctypes.byref(s), None, None) == mgb.MGB_ERR_UNSUPPORTED
+    d.attn_dropout, d.hidden_dropout = 0.0, 0.1
+    d.rng_proj.offset = 8
+    assert lib.mgb_block_sizes(ctypes.byref(d), ctypes.byref(s), None, None) == mgb.MGB_ERR_INVALID_ARG
+    d.rng_proj.offset = 16
+    b0 = mgb.mgb_block_sizes(_desc())[2]
+    b1 = mgb.mgb_block_sizes(d)[2]
+    assert b1 > b0  # two [T, H] branch-gradient buffers
+    f = _desc()
+    f.dtype, f.hidden_dropout = mgb.MGB_F32, 0.1
+    assert lib.mgb_block_sizes(ctypes.byref(f), ctypes.byref(s), None, None) == mgb.MGB_ERR_UNSUPPORTED
+    st = mgb.RngState(seed=1, offset=4)
+    assert lib.mgb_dropout(4, 16, mgb.MGB_BF16, ctypes.c_float(0.1), st, 4096, 16, 4096, 16,
+                           None) == mgb.MGB_ERR_INVALID_ARG
+
+
 def test_injected_validation_fault(lib, monkeypatch):
     """MGB_FAULT=validate makes every descriptor check fail (host-side fault injection)."""
     d = _desc()
