@@ -92,10 +92,11 @@ typedef struct {
   /* Dropout [P2 section 5]: hidden_dropout on the outputs of the output
    * projection and of fc2 before their residual adds (element t*H + c of the
    * [T, H] branch), attn_dropout on the attention probabilities. 0 = off.
-   * bf16 only; attn_dropout > 0 returns MGB_ERR_UNSUPPORTED. rng_*: the
-   * generator states of the three sites (mgb_block_dropout_plan draws them
-   * from a tracker); the backward must get the forward's values and
-   * regenerates the same masks. */
+   * bf16 only. The attention site's keep bits (one per query and key) are
+   * kept in `saved` for the backward; the hidden sites' masks are
+   * regenerated. rng_*: the generator states of the three sites
+   * (mgb_block_dropout_plan draws them from a tracker); the backward must get
+   * the forward's values. */
   float hidden_dropout, attn_dropout;
   mgb_rng_state rng_attn, rng_proj, rng_fc2;
 } mgb_block_desc;

@@ -161,6 +161,7 @@ struct Plan {
   bool pre, swiglu;
   // saved buffer
   size_t s_mu1, s_rs1, s_mu2, s_rs2, s_lse, s_xn, s_qkv, s_O, s_h, s_r1, s_hn, s_u, s_a, s_r2;
+  size_t s_dmask;  // attention keep bits (attn_dropout > 0)
   size_t saved;
   // backward workspace
   size_t w_dffn, w_dh, w_dr2, w_du, w_dO, w_dqkv, w_dxn, w_delta, w_cparts, w_lparts;
@@ -177,6 +178,17 @@ void set_hidden_dropout(const mgb_block_desc* d, const mgb_rng_state& rng, GemmA
   g->drop_scale = 256.0f / (float)g->drop_thr;
   g->drop_seed = rng.seed;
   g->drop_offset = rng.offset;
+}
+
+// Dropout of the attention probabilities inside the attention kernels; the
+// keep bits live in the saved buffer between the forward and the backward.
+void set_attn_dropout(const mgb_block_desc* d, const Plan& p, void* saved, AttnArgs* a) {
+  if (!(d->attn_dropout > 0.0f)) return;
+  a->drop_thr = dropout_threshold(d->attn_dropout);
+  a->drop_scale = 256.0f / (float)a->drop_thr;
+  a->drop_seed = d->rng_attn.seed;
+  a->drop_offset = d->rng_attn.offset;
+  a->drop_mask = reinterpret_cast<uint32_t*>(static_cast<char*>(saved) + p.s_dmask);
 }
 
 mgb_status validate_desc(const mgb_block_desc* d) {
@@ -214,7 +226,11 @@ mgb_status validate_desc(const mgb_block_desc* d) {
   if (!(d->hidden_dropout >= 0.0f && d->hidden_dropout < 1.0f) ||
       !(d->attn_dropout >= 0.0f && d->attn_dropout < 1.0f))
     return MGB_ERR_INVALID_ARG;
-  if (d->attn_dropout > 0.0f) return MGB_ERR_UNSUPPORTED;
+  if (d->attn_dropout > 0.0f) {
+    // applied in the tcgen05 attention kernels
+    if (d->dtype != MGB_BF16) return MGB_ERR_UNSUPPORTED;
+    if (d->rng_attn.offset % 16) return MGB_ERR_INVALID_ARG;
+  }
   if (d->hidden_dropout > 0.0f) {
     if (d->dtype != MGB_BF16) return MGB_ERR_UNSUPPORTED;
     if (d->hidden % 16 || d->rng_proj.offset % 16 || d->rng_fc2.offset % 16)
@@ -248,6 +264,7 @@ void make_plan(const mgb_block_desc* d, Plan* p) {
   p->s_u = take(es * T * p->W);
   p->s_a = take(es * T * p->F);
   p->s_r2 = p->pre ? 0 : take(es * T * p->H);
+  p->s_dmask = d->attn_dropout > 0.0f ? take(attn_mask_bytes(p->B, p->nq, p->S)) : 0;
   p->saved = o;
   o = 0;
   p->cparts = colsum_parts(p->T);
@@ -405,6 +422,7 @@ mgb_status mgb_block_fwd(const mgb_block_desc* desc, const mgb_block_weights* w,
   at_.v = static_cast<char*>(qkv) + p.es * (p.Dq + (size_t)p.nkv * p.d);
   at_.ld_q = p.Wqkv; at_.ld_kv = p.Wqkv;
   at_.o = O; at_.ld_o = p.Dq; at_.lse = lse;
+  set_attn_dropout(desc, p, saved, &at_);
   MGB_TRY(attention_fwd_launch(at_, st));
 
   // output projection + residual (Pre: h; Post: r1 then h = LN1(r1))
@@ -565,6 +583,7 @@ mgb_status mgb_block_bwd(const mgb_block_desc* desc, const mgb_block_weights* w,
     at_.dv = static_cast<char*>(dqkv) + p.es * (p.Dq + (size_t)p.nkv * p.d);
     at_.ld_dq = p.Wqkv; at_.ld_dkv = p.Wqkv;
     at_.delta = delta;
+    set_attn_dropout(desc, p, const_cast<void*>(saved), &at_);
     MGB_TRY(attention_bwd_launch(at_, st));
   }
   // QKV: dbqkv, dWqkv = dqkv^T a_in, d a_in = dqkv Wqkv

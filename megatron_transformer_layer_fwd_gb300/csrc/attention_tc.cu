@@ -40,6 +40,12 @@
 // MN-major operand (d contiguous). Every wait is bounded: one that runs out
 // sets a shared abort flag and every role leaves its loop before the closing
 // barrier.
+// Dropout on the probabilities ("02 - How a whole Transformer block is split",
+// section 5: inside the tensor-parallel region), the DROP variant: after the
+// row sums take the undropped P, each softmax thread draws its 64 keys' keep
+// bytes (element ((b*nq + h)*S + row)*Sp + key of the site's Philox stream:
+// four 16-byte blocks), zeroes the dropped probabilities and scales the kept
+// ones before P goes to TMEM, and writes the 64 keep bits for the backward.
 #include "common.cuh"
 #include "internal.h"
 
@@ -86,6 +92,12 @@ struct FwdParams {
   float* lse;
   int* err;
   float sl2;  // log2(e) / sqrt(d)
+  // dropout (DROP variant)
+  uint64_t dseed, doff;
+  uint32_t dthr;
+  float dscale;
+  uint32_t* dmask;
+  int mw, sp;  // mask words per row; Sp
 };
 
 struct Item {
@@ -106,7 +118,7 @@ __device__ __forceinline__ Item item_of(int i, const FwdParams& p) {
   return it;
 }
 
-template <int D>
+template <int D, bool DROP>
 __global__ void __launch_bounds__(NTHREADS, 1)
     attn_fwd_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
                        const __grid_constant__ CUtensorMap tmK,
@@ -331,6 +343,28 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       const uint32_t t_o = tmem + C::COL_O + half * (D / 2) + lane_base;
       float m_ref = -INFINITY, l_part = 0.0f;
       for (int j = 0; j < w.nkt; ++j, ++n) {
+        const int kv0 = j * TK;
+        // dropout: keep bits of this thread's 64 keys (4 blocks of the site's
+        // stream), drawn while the scores are computed and stored for the
+        // backward (bit c of kb0 / kb1: key kv0 + c_own + c / 32 + c)
+        uint32_t kb0 = 0, kb1 = 0;
+        if constexpr (DROP) {
+          const int64_t bh = (int64_t)w.b * p.nq + w.h;
+          const uint64_t q = (p.doff + ((uint64_t)(bh * p.S + row)) * p.sp + kv0 + c_own) >> 4;
+#pragma unroll
+          for (int gq = 0; gq < 4; ++gq) {
+            const uint4 wd = philox_block(p.dseed, q + gq);
+            const uint32_t ws[4] = {wd.x, wd.y, wd.z, wd.w};
+            uint32_t bits = 0;
+#pragma unroll
+            for (int i = 0; i < 16; ++i) bits |= (uint32_t)keep_byte(ws[i >> 2], i & 3, p.dthr) << i;
+            if (gq < 2) kb0 |= bits << (16 * gq);
+            else kb1 |= bits << (16 * (gq - 2));
+          }
+          const int wi = (kv0 + c_own) >> 5;
+          if (row < p.S && wi < p.mw)
+            *reinterpret_cast<uint2*>(p.dmask + (bh * p.S + row) * p.mw + wi) = make_uint2(kb0, kb1);
+        }
         if (warp_aborted(abort) || !warp_wait(s_full0 + 8 * (n & 1), (n >> 1) & 1, p.err)) {
           good = false;
           break;
@@ -339,7 +373,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         // the partner's 64 columns first, reduced to their max (so only 64
         // scores are live at a time), then this thread's own 64
         const uint32_t ts = tmem + (n & 1) * TK + lane_base;
-        const int kv0 = j * TK;
         const bool interior = kv0 + TK <= p.S && (!p.causal || kv0 + TK - 1 <= w.q0);
         float mo;
         {
@@ -410,8 +443,17 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         l_part += (r0 + r1) + (r2 + r3);
         // this half's 64 keys of P as bf16 pairs: 32 TMEM columns of P buffer n & 1
         uint32_t pk[32];
+        if constexpr (DROP) {
 #pragma unroll
-        for (int c = 0; c < 32; ++c) pk[c] = pack_bf16x2(so[2 * c], so[2 * c + 1]);
+          for (int c = 0; c < 32; ++c) {
+            const uint32_t kw = c < 16 ? kb0 : kb1, sh = (2 * c) & 31;
+            pk[c] = pack_bf16x2((kw >> sh) & 1u ? so[2 * c] * p.dscale : 0.0f,
+                                (kw >> (sh + 1)) & 1u ? so[2 * c + 1] * p.dscale : 0.0f);
+          }
+        } else {
+#pragma unroll
+          for (int c = 0; c < 32; ++c) pk[c] = pack_bf16x2(so[2 * c], so[2 * c + 1]);
+        }
         // P buffer n & 1 was last read by the PV product of tile n - 2
         if (n >= 2 && !warp_wait(pv_done0 + 8 * (n & 1), ((n - 2) >> 1) & 1, p.err)) {
           good = false;
@@ -472,7 +514,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   }
 }
 
-template <int D>
+template <int D, bool DROP>
 mgb_status fwd_tc_d(const AttnArgs& a, cudaStream_t st) {
   using C = FwdCfg<D>;
   const uint64_t T = (uint64_t)a.B * a.S;
@@ -489,7 +531,9 @@ mgb_status fwd_tc_d(const AttnArgs& a, cudaStream_t st) {
   p.o = reinterpret_cast<bf16*>(a.o); p.ld_o = a.ld_o; p.lse = a.lse;
   p.err = device_error_word();
   p.sl2 = LOG2E / sqrtf((float)D);
-  auto k = attn_fwd_tc_kernel<D>;
+  p.dseed = a.drop_seed; p.doff = a.drop_offset; p.dthr = a.drop_thr; p.dscale = a.drop_scale;
+  p.dmask = a.drop_mask; p.mw = attn_mask_words(a.S); p.sp = (a.S + 15) / 16 * 16;
+  auto k = attn_fwd_tc_kernel<D, DROP>;
   if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess)
     return MGB_ERR_CUDA;
   const int grid = n_items < device_sm_count() ? n_items : device_sm_count();
@@ -500,8 +544,11 @@ mgb_status fwd_tc_d(const AttnArgs& a, cudaStream_t st) {
 }  // namespace
 
 mgb_status attention_tc_fwd(const AttnArgs& a, cudaStream_t st) {
-  if (a.d == 64) return fwd_tc_d<64>(a, st);
-  if (a.d == 128) return fwd_tc_d<128>(a, st);
+  const bool drop = a.drop_thr < 256;
+  if (drop && (a.drop_mask == nullptr || a.drop_offset % 16 || a.drop_thr == 0))
+    return MGB_ERR_INVALID_ARG;
+  if (a.d == 64) return drop ? fwd_tc_d<64, true>(a, st) : fwd_tc_d<64, false>(a, st);
+  if (a.d == 128) return drop ? fwd_tc_d<128, true>(a, st) : fwd_tc_d<128, false>(a, st);
   return MGB_ERR_UNSUPPORTED;
 }
 

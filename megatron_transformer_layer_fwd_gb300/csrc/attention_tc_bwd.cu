@@ -49,6 +49,13 @@
 // the loop: the roles hand tiles to each other through mbarriers only. Every
 // wait is bounded; a wait that runs out sets a shared abort flag and every role
 // leaves its loop (warp-uniformly) before the single closing barrier.
+//
+// Dropout on the probabilities (the DROP variants): the forward wrote one keep
+// bit per (query, key). With keep mask M and scale s: dV uses P o M s, the
+// gradient reaching P is dP o M s, and dS = P (dP o M s - delta) (delta =
+// rowsum(dO o O) of the dropped output). Kernel A stages each tile's 64 x 128
+// bits with its Q/dO stage (a TMA box of 4 words x 64 query rows); kernel B
+// loads one word per 32 keys.
 #include "common.cuh"
 #include "internal.h"
 
@@ -56,6 +63,9 @@ namespace mgb {
 
 CUresult tmap_encode_bf16_2d(CUtensorMap* tm, const void* base, uint64_t inner, uint64_t outer,
                              int64_t ld, uint32_t box_inner, uint32_t box_outer);
+// 2-D uint32 tensor map without swizzle (gemm_tc.cu)
+CUresult tmap_encode_u32_2d(CUtensorMap* tm, const void* base, uint64_t inner, uint64_t outer,
+                            int64_t ld, uint32_t box_inner, uint32_t box_outer);
 
 namespace {
 
@@ -70,6 +80,9 @@ constexpr int W_PROD = 16, W_MMA = 17;
 
 struct BwdParams {
   int B, S, nq, nkv, causal, s_pad;
+  const uint32_t* dmask;  // keep bits [B*nq*S][mw] (DROP variants)
+  int mw;
+  float dscale;
   const float* lse2;   // [B * nq][s_pad]: LSE * log2(e)
   const float* delta;  // [B * nq][s_pad]
   bf16 *d0, *d1;       // A: dk, dv; B: dq
@@ -90,19 +103,22 @@ struct DkvCfg {
   static constexpr int OFF_Q = OFF_V + KV_BYTES;          // NSA stages
   static constexpr int OFF_DO = OFF_Q + NSA * QT_BYTES;   // NSA stages
   static constexpr int OFF_LD = OFF_DO + NSA * QT_BYTES;  // NSA stages
-  static constexpr int OFF_BAR = OFF_LD + NSA * LD_BYTES;
+  static constexpr int M_BYTES = TC * 16;                 // a tile's keep bits: [64 queries][4 words]
+  static constexpr int OFF_M = OFF_LD + NSA * LD_BYTES;   // NSA stages (DROP)
+  static constexpr int OFF_BAR = OFF_M + NSA * M_BYTES;
   static constexpr int SMEM = OFF_BAR + 256 + 1024;
   // TMEM: scores [0, 128), P^T/dS^T buffers [128, 256) (64 columns each: P^T
   // then dS^T, 32 columns = 64 bf16 queries apiece), dV, dK
   static constexpr int COL_PDS = 128, COL_DV = COL_ACC, COL_DK = COL_ACC + D;
 };
 
-template <int D>
+template <int D, bool DROP>
 __global__ void __launch_bounds__(NTHREADS, 1)
     attn_bwd_dkdv_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
                             const __grid_constant__ CUtensorMap tmK,
                             const __grid_constant__ CUtensorMap tmV,
-                            const __grid_constant__ CUtensorMap tmO, const BwdParams p) {
+                            const __grid_constant__ CUtensorMap tmO,
+                            const __grid_constant__ CUtensorMap tmM, const BwdParams p) {
   using C = DkvCfg<D>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -111,6 +127,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   const uint32_t sK = sb + C::OFF_K, sV = sb + C::OFF_V, sQ = sb + C::OFF_Q, sO = sb + C::OFF_DO,
                  sLDa = sb + C::OFF_LD;
   const float* sLD = reinterpret_cast<const float*>(smem + C::OFF_LD);
+  const uint32_t* sM = reinterpret_cast<const uint32_t*>(smem + C::OFF_M);
   const uint32_t bar = sb + C::OFF_BAR;
   const uint32_t kv_full = bar;          // K, V loaded                       (tx)
   const uint32_t qd_full0 = bar + 8;     // [4] Q/dO/LSE/delta stage loaded   (tx)
@@ -180,7 +197,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
         const uint32_t fb = qd_full0 + 8 * s;
         const int q0 = qt * TC;
-        mbar_arrive_expect_tx(fb, 2 * C::QT_BYTES + C::LD_BYTES);
+        mbar_arrive_expect_tx(fb, 2 * C::QT_BYTES + C::LD_BYTES + (DROP ? C::M_BYTES : 0));
+        if constexpr (DROP)  // keep bits of queries q0.. (rows of head h) x keys kv0..kv0+127
+          tma_load_2d(sb + C::OFF_M + s * C::M_BYTES, &tmM, kv0 >> 5,
+                      (int)(((int64_t)b * p.nq + h) * p.S + q0), fb);
 #pragma unroll
         for (int kb = 0; kb < C::KB; ++kb) {
           tma_load_2d(sQ + s * C::QT_BYTES + kb * 8192, &tmQ, h * D + kb * 64, grow0 + q0, fb);
@@ -281,6 +301,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       tc_fence_before();
       mbar_arrive(sp_free0 + 8 * grp);
       const float* ldp = sLD + (it % NSA) * (2 * TC) + col0;
+      // this key's keep bits against the tile's queries: word (warp & 3) of each
+      // query row of the staged [64][4] tile (the same word for the whole warp)
+      const uint32_t* mq = sM + (it % NSA) * (TC * 4) + col0 * 4 + (warp & 3);
       // P^T and dS^T of this key row against its 32 queries of the tile (past
       // the sequence end the workspace holds LSE = +inf, so P = 0 there);
       // LSE/delta are read from smem four at a time
@@ -303,8 +326,17 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             st[c + e] = vis ? ex2_ftz(fmaf(st[c + e], p.sl2, -l4[e])) : 0.0f;
           }
         }
+        if constexpr (DROP) {
 #pragma unroll
-        for (int e = 0; e < 4; ++e) dp[c + e] = st[c + e] * (dp[c + e] - d4[e]);
+          for (int e = 0; e < 4; ++e) {
+            const bool kp = (mq[(c + e) * 4] >> lane) & 1u;
+            dp[c + e] = st[c + e] * ((kp ? dp[c + e] * p.dscale : 0.0f) - d4[e]);
+            st[c + e] = kp ? st[c + e] * p.dscale : 0.0f;
+          }
+        } else {
+#pragma unroll
+          for (int e = 0; e < 4; ++e) dp[c + e] = st[c + e] * (dp[c + e] - d4[e]);
+        }
       }
       uint32_t pp[16], pd[16];
 #pragma unroll
@@ -369,7 +401,7 @@ struct DqCfg {
   static constexpr int COL_DS = 128, COL_DQ = COL_ACC;
 };
 
-template <int D>
+template <int D, bool DROP>
 __global__ void __launch_bounds__(NTHREADS, 1)
     attn_bwd_dq_tc_kernel(const __grid_constant__ CUtensorMap tmQ,
                           const __grid_constant__ CUtensorMap tmK,
@@ -513,6 +545,13 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const uint32_t col0 = half * 32;
     bool good = true;
     for (int j = grp; j < nkt; j += 2) {
+      // keep bits of this query row against the thread's 32 keys (issued before
+      // the wait so the load overlaps it)
+      uint32_t kbits = 0;
+      if constexpr (DROP) {
+        if (row < p.S)
+          kbits = p.dmask[(((int64_t)b * p.nq + h) * p.S + row) * p.mw + ((j * TC + col0) >> 5)];
+      }
       if (warp_aborted(abort) || !warp_wait(sp_full0 + 8 * grp, (j >> 1) & 1, p.err)) {
         good = false;
         break;
@@ -550,6 +589,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           const bool vis = kv < p.S && !(p.causal && kv > row);
           sc[c] = vis ? ex2_ftz(fmaf(sc[c], p.sl2, -L2)) : 0.0f;
         }
+      }
+      if constexpr (DROP) {
+#pragma unroll
+        for (int c = 0; c < 32; ++c) dp[c] = (kbits >> c) & 1u ? dp[c] * p.dscale : 0.0f;
       }
       uint32_t pd[16];
 #pragma unroll
@@ -593,7 +636,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   }
 }
 
-template <int D>
+template <int D, bool DROP>
 mgb_status bwd_tc_d(const AttnArgs& a, cudaStream_t st) {
   const uint64_t T = (uint64_t)a.B * a.S;
   BwdParams p{};
@@ -604,10 +647,18 @@ mgb_status bwd_tc_d(const AttnArgs& a, cudaStream_t st) {
   p.err = device_error_word();
   p.sl2 = 1.4426950408889634f / sqrtf((float)D);
   p.scale = 1.0f / sqrtf((float)D);
+  p.dmask = a.drop_mask;
+  p.mw = attn_mask_words(a.S);
+  p.dscale = a.drop_scale;
   // kernel A: K/V rows of 128, Q/dO tiles of 64
   {
     using C = DkvCfg<D>;
-    CUtensorMap tq, tk, tv, to;
+    CUtensorMap tq, tk, tv, to, tm;
+    // keep bits: [B*nq*S rows][mw words], boxes of 4 words x 64 query rows
+    // (without dropout a harmless map over the same rows of the output)
+    if ((DROP ? tmap_encode_u32_2d(&tm, a.drop_mask, p.mw, (uint64_t)a.B * a.nq * a.S, p.mw, 4, TC)
+              : tmap_encode_u32_2d(&tm, a.dk, 4, T, 4, 4, TC)) != CUDA_SUCCESS)
+      return MGB_ERR_CUDA;
     if (tmap_encode_bf16_2d(&tq, a.q, (uint64_t)a.nq * D, T, a.ld_q, 64, TC) != CUDA_SUCCESS ||
         tmap_encode_bf16_2d(&to, a.dout, (uint64_t)a.nq * D, T, a.ld_do, 64, TC) != CUDA_SUCCESS ||
         tmap_encode_bf16_2d(&tk, a.k, (uint64_t)a.nkv * D, T, a.ld_kv, 64, TR) != CUDA_SUCCESS ||
@@ -616,11 +667,11 @@ mgb_status bwd_tc_d(const AttnArgs& a, cudaStream_t st) {
     p.d0 = reinterpret_cast<bf16*>(a.dk);
     p.d1 = reinterpret_cast<bf16*>(a.dv);
     p.ld_out = a.ld_dkv;
-    auto k = attn_bwd_dkdv_tc_kernel<D>;
+    auto k = attn_bwd_dkdv_tc_kernel<D, DROP>;
     if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess)
       return MGB_ERR_CUDA;
     dim3 grid(a.nkv * a.B, (a.S + TR - 1) / TR);
-    k<<<grid, NTHREADS, C::SMEM, st>>>(tq, tk, tv, to, p);
+    k<<<grid, NTHREADS, C::SMEM, st>>>(tq, tk, tv, to, tm, p);
   }
   // kernel B: Q/dO rows of 128, K/V tiles of 64
   {
@@ -634,7 +685,7 @@ mgb_status bwd_tc_d(const AttnArgs& a, cudaStream_t st) {
     p.d0 = reinterpret_cast<bf16*>(a.dq);
     p.d1 = nullptr;
     p.ld_out = a.ld_dq;
-    auto k = attn_bwd_dq_tc_kernel<D>;
+    auto k = attn_bwd_dq_tc_kernel<D, DROP>;
     if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess)
       return MGB_ERR_CUDA;
     dim3 grid(a.nq * a.B, (a.S + TR - 1) / TR);
@@ -646,8 +697,10 @@ mgb_status bwd_tc_d(const AttnArgs& a, cudaStream_t st) {
 }  // namespace
 
 mgb_status attention_tc_bwd_main(const AttnArgs& a, cudaStream_t st) {
-  if (a.d == 64) return bwd_tc_d<64>(a, st);
-  if (a.d == 128) return bwd_tc_d<128>(a, st);
+  const bool drop = a.drop_thr < 256;
+  if (drop && a.drop_mask == nullptr) return MGB_ERR_INVALID_ARG;
+  if (a.d == 64) return drop ? bwd_tc_d<64, true>(a, st) : bwd_tc_d<64, false>(a, st);
+  if (a.d == 128) return drop ? bwd_tc_d<128, true>(a, st) : bwd_tc_d<128, false>(a, st);
   return MGB_ERR_UNSUPPORTED;
 }
 

@@ -91,7 +91,21 @@ struct AttnArgs {
   const void* dout; int64_t ld_do;
   void *dq, *dk, *dv; int64_t ld_dq, ld_dkv;
   float* delta;          // backward scratch (attn_bwd_ws_bytes)
+  // dropout on the probabilities (bf16 path; drop_thr 256 = off): the forward
+  // keeps element ((b*nq + h)*S + i)*Sp + j of stream (drop_seed, drop_offset),
+  // Sp = S rounded up to 16, and writes the keep bits to drop_mask
+  // [B*nq*S rows][attn_mask_words(S)] (bit j%32 of word j/32); the backward
+  // reads the bits
+  uint32_t drop_thr = 256;
+  float drop_scale = 1.0f;
+  uint64_t drop_seed = 0, drop_offset = 0;
+  uint32_t* drop_mask = nullptr;
 };
+// Words per query row of the attention keep-bit mask (rows padded to 128 keys).
+inline int attn_mask_words(int S) { return (S + 127) / 128 * 4; }
+inline size_t attn_mask_bytes(int B, int nq, int S) {
+  return 4 * (size_t)B * nq * S * attn_mask_words(S);
+}
 // The bf16 backward's per-query workspace: two float32 planes [B * nq][pad]
 // (LSE * log2(e), then delta) with rows padded to a multiple of 128 queries.
 inline int attn_bwd_row_pad(int S) { return (S + 127) / 128 * 128; }

@@ -186,7 +186,11 @@ def test_dropout_desc_validation(lib):
     d.hidden_dropout = -0.1
     assert lib.mgb_block_sizes(ctypes.byref(d), ctypes.byref(s), None, None) == mgb.MGB_ERR_INVALID_ARG
     d.hidden_dropout, d.attn_dropout = 0.0, 0.1
-    assert lib.mgb_block_sizes(ctypes.byref(d), ctypes.byref(s), None, None) == mgb.MGB_ERR_UNSUPPORTED
+    s0 = mgb.mgb_block_sizes(_desc())[0]
+    s1 = mgb.mgb_block_sizes(d)[0]
+    assert s1 - s0 >= 4 * 4 * 16 * 512 * 512 // 32  # one keep bit per query and key
+    d.rng_attn.offset = 4
+    assert lib.mgb_block_sizes(ctypes.byref(d), ctypes.byref(s), None, None) == mgb.MGB_ERR_INVALID_ARG
     d.attn_dropout, d.hidden_dropout = 0.0, 0.1
     d.rng_proj.offset = 8
     assert lib.mgb_block_sizes(ctypes.byref(d), ctypes.byref(s), None, None) == mgb.MGB_ERR_INVALID_ARG
@@ -196,6 +200,8 @@ def test_dropout_desc_validation(lib):
     assert b1 > b0  # two [T, H] branch-gradient buffers
     f = _desc()
     f.dtype, f.hidden_dropout = mgb.MGB_F32, 0.1
+    assert lib.mgb_block_sizes(ctypes.byref(f), ctypes.byref(s), None, None) == mgb.MGB_ERR_UNSUPPORTED
+    f.hidden_dropout, f.attn_dropout = 0.0, 0.1
     assert lib.mgb_block_sizes(ctypes.byref(f), ctypes.byref(s), None, None) == mgb.MGB_ERR_UNSUPPORTED
     st = mgb.RngState(seed=1, offset=4)
     assert lib.mgb_dropout(4, 16, mgb.MGB_BF16, ctypes.c_float(0.1), st, 4096, 16, 4096, 16,

@@ -56,9 +56,10 @@ SHAPES = {
 }
 
 
-def _dropout_runner(shape, arr, p, seed):
+def _dropout_runner(shape, arr, p, seed, p_attn=0.0):
     r = LayerRunner(shape, arr)
     r.desc.hidden_dropout = p
+    r.desc.attn_dropout = p_attn
     mgb.mgb_block_dropout_plan(r.desc, mgb.rng_tracker(seed))
     saved, _, bwd = mgb.mgb_block_sizes(r.desc)
     r.saved = torch.empty(max(saved, 16), dtype=torch.uint8, device="cuda")
@@ -105,3 +106,42 @@ def test_layer_dropout_replay_and_seeds(mgb_lib):
     y3 = r.fwd().clone()
     assert not torch.equal(y1, y3)
     assert mgb.mgb_device_status() == mgb.MGB_OK
+
+
+ATTN_SHAPES = {
+    "pre_gelu_d64": LayerShape(2, 100, 256, 4, 4, 64, 520),
+    "post_swiglu_gqa_causal_d128": LayerShape(2, 130, 256, 4, 2, 128, 384, norm_pos="post",
+                                              act="swiglu", causal=True),
+    "pre_gqa_causal_multitile": LayerShape(1, 300, 256, 4, 1, 64, 256, causal=True),
+}
+
+
+@pytest.mark.parametrize("name", list(ATTN_SHAPES))
+@pytest.mark.parametrize("p_attn,p_hidden", [(0.25, 0.0), (0.1, 0.15)])
+def test_layer_attention_dropout_parity(mgb_lib, name, p_attn, p_hidden):
+    """Dropout inside the attention kernels (the model-parallel stream): the
+    forward draws and stores the keep bits, both backward kernels read them."""
+    shape = ATTN_SHAPES[name]
+    pa, ph = float(np.float32(p_attn)), float(np.float32(p_hidden))
+    arr = layer_inputs(shape, seed=41, random_affine=True, random_dy=True)
+    r = _dropout_runner(shape, arr, ph, seed=777, p_attn=pa)
+    y = r.fwd().clone()
+    dy = to_device(arr["dy"], r.dtype)
+    dx, g = r.bwd(dy)
+    assert mgb.mgb_device_status() == mgb.MGB_OK
+    drop = od.layer_dropout(shape, od.model_parallel_seed(777), pa, ph)
+    w = {k: arr[k] for k in WEIGHT_KEYS}
+    ry, cache = oracle.block_fwd(shape, w, arr["x"], drop=drop)
+    rdx, rg = oracle.block_bwd(shape, w, cache, arr["dy"])
+    tol_o, tol_g = TOL["bf16"]
+    errs = {"y": rel_l2(to_np(y), ry), "dx": rel_l2(to_np(dx), rdx)}
+    for k in WEIGHT_KEYS:
+        if rg[k] is not None:
+            errs[k] = rel_l2(to_np(g[k]), rg[k])
+    print(name, pa, ph, {k: f"{v:.2e}" for k, v in errs.items()})
+    assert errs["y"] < tol_o and all(v < tol_g for k, v in errs.items() if k != "y"), errs
+    # without the attention masks the oracle's attention-side gradients are far off
+    drop_na = dict(drop, attn=None)
+    ry_na, cache_na = oracle.block_fwd(shape, w, arr["x"], drop=drop_na)
+    _, rg_na = oracle.block_bwd(shape, w, cache_na, arr["dy"])
+    assert rel_l2(to_np(g["w_qkv"]), rg_na["w_qkv"]) > 5 * errs["w_qkv"]
