@@ -473,6 +473,14 @@ def run_case(args):
         for name in names:
             shape = WORKLOADS[name]
             r = LayerRunner(shape, layer_inputs(shape, seed=0))
+            if args.dropout > 0:
+                # attention-probability and hidden dropout at the same rate, the
+                # sites' states drawn from the tensor-parallel RNG tracker
+                r.desc.attn_dropout = r.desc.hidden_dropout = args.dropout
+                mgb.mgb_block_dropout_plan(r.desc, mgb.rng_tracker(1234))
+                saved, _, bwd = mgb.mgb_block_sizes(r.desc)
+                r.saved = torch.empty(saved, dtype=torch.uint8, device="cuda")
+                r.ws = torch.empty(bwd, dtype=torch.uint8, device="cuda")
             dy = torch.full_like(r.x, 1.0 / (shape.tokens * shape.hidden))
 
             def fb():
@@ -481,7 +489,7 @@ def run_case(args):
             ms, prof = _time_loop(fb, args.steps, args.warmup, st)
             lf = layer_flops(shape)
             gem = ("gemm_tc_fwd", "gemm_tc_dgrad", "gemm_tc_wgrad")
-            out = {"case": args.case, "workload": name, "ms": round(ms, 4),
+            out = {"case": args.case, "workload": name, "dropout": args.dropout, "ms": round(ms, 4),
                    "tflops": round(lf["total"] / (ms / 1e3) / 1e12, 1),
                    "frac_of_nominal_2250": round(lf["total"] / (ms / 1e3) / 2.25e15, 4),
                    "tokens_per_s": round(shape.tokens / (ms / 1e3), 1),
@@ -594,6 +602,8 @@ def main():
                              "embedding"),
                     help="step (default, the driver's line) or a sub-path / single kernel")
     ap.add_argument("--mnk", type=int, nargs=3, default=(8192, 22016, 4096))
+    ap.add_argument("--dropout", type=float, default=0.0,
+                    help="--case layer|sweep: attention and hidden dropout probability")
     ap.add_argument("--ce-mode", default="all", choices=("all", "stream", "fused", "resident"),
                     help="--case ce: which CE mode(s) to time")
     args = ap.parse_args()

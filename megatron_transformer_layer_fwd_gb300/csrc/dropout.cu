@@ -80,6 +80,47 @@ __global__ void dropout_kernel(int64_t rows, int64_t cols, uint64_t seed, uint64
   }
 }
 
+// As dropout_kernel for rows of a multiple of 16 elements and 16-byte aligned
+// rows: group g = 16 elements of row g / gpr (the site's element 16 g), moved
+// as 16-byte vectors.
+template <typename T>
+__global__ void dropout_rows_kernel(int64_t rows, int gpr, uint64_t seed, uint64_t q0, uint32_t thr,
+                                    float scale, const T* __restrict__ x, int64_t ldx,
+                                    T* __restrict__ y, int64_t ldy) {
+  constexpr int VN = 16 / sizeof(T);  // elements per 16-byte vector
+  const int64_t total = rows * gpr;
+  for (int64_t g = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; g < total;
+       g += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t r = g / gpr;
+    const int c = (int)(g - r * gpr) * 16;
+    const uint4* xs = reinterpret_cast<const uint4*>(x + r * ldx + c);
+    uint4* ys = reinterpret_cast<uint4*>(y + r * ldy + c);
+    uint4 v[16 / VN];
+#pragma unroll
+    for (int i = 0; i < 16 / VN; ++i) v[i] = xs[i];
+    const uint4 w = philox_block(seed, q0 + (uint64_t)g);
+    const uint32_t ws[4] = {w.x, w.y, w.z, w.w};
+#pragma unroll
+    for (int i = 0; i < 16 / VN; ++i) {
+      uint32_t u[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        if constexpr (sizeof(T) == 2) {
+          const int e = i * 8 + 2 * k;  // element of the group
+          const float2 f = unpack_bf16x2(u[k]);
+          u[k] = pack_bf16x2(keep_byte(ws[e >> 2], e & 3, thr) ? f.x * scale : 0.0f,
+                             keep_byte(ws[e >> 2], (e & 3) + 1, thr) ? f.y * scale : 0.0f);
+        } else {
+          const int e = i * 4 + k;
+          u[k] = __float_as_uint(keep_byte(ws[e >> 2], e & 3, thr) ? __uint_as_float(u[k]) * scale
+                                                                   : 0.0f);
+        }
+      }
+      ys[i] = make_uint4(u[0], u[1], u[2], u[3]);
+    }
+  }
+}
+
 }  // namespace
 
 uint32_t dropout_threshold(float p) {
@@ -97,7 +138,20 @@ mgb_status dropout_launch(int64_t rows, int64_t cols, int dtype, float p, uint64
   const int64_t want = (groups + threads - 1) / threads;
   const int grid = (int)(want < device_sm_count() * 8 ? want : device_sm_count() * 8);
   LaunchScope scope(PROF_DROPOUT, st);
-  if (dtype == MGB_BF16)
+  const int vn = dtype == MGB_BF16 ? 8 : 4;
+  const bool vec = cols % 16 == 0 && ldx % vn == 0 && ldy % vn == 0 &&
+                   (reinterpret_cast<uintptr_t>(x) & 15u) == 0 &&
+                   (reinterpret_cast<uintptr_t>(y) & 15u) == 0 && cols / 16 < (1 << 30);
+  if (vec) {
+    if (dtype == MGB_BF16)
+      dropout_rows_kernel<bf16><<<grid, threads, 0, st>>>(rows, (int)(cols / 16), seed, offset / 16,
+                                                          thr, scale, static_cast<const bf16*>(x),
+                                                          ldx, static_cast<bf16*>(y), ldy);
+    else
+      dropout_rows_kernel<float><<<grid, threads, 0, st>>>(rows, (int)(cols / 16), seed, offset / 16,
+                                                           thr, scale, static_cast<const float*>(x),
+                                                           ldx, static_cast<float*>(y), ldy);
+  } else if (dtype == MGB_BF16)
     dropout_kernel<bf16><<<grid, threads, 0, st>>>(rows, cols, seed, offset, thr, scale,
                                                    static_cast<const bf16*>(x), ldx,
                                                    static_cast<bf16*>(y), ldy);

@@ -27,16 +27,19 @@ def test_philox_bytes_bit_exact(mgb_lib, seed, offset, n):
     assert np.array_equal(out.cpu().numpy(), od.uniform_bytes(seed, offset, n))
 
 
+@pytest.mark.parametrize("pad", [0, 3, 8])
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
 @pytest.mark.parametrize("rows,cols,p", [(64, 256, 0.1), (37, 100, 0.5), (3, 7, 0.9), (8, 32, 0.0)])
-def test_dropout_mask_exact(mgb_lib, dtype, rows, cols, p):
+def test_dropout_mask_exact(mgb_lib, dtype, rows, cols, p, pad):
+    """16-byte-vector rows (cols % 16 == 0, aligned strides) and the general
+    element path (ragged cols or an odd output stride)."""
     td = torch.bfloat16 if dtype == "bf16" else torch.float32
     dt = mgb.MGB_BF16 if dtype == "bf16" else mgb.MGB_F32
     p32 = float(np.float32(p))
     rng = mgb.RngState(seed=77, offset=16 * 9)
     x = (torch.rand((rows, cols), device="cuda") + 0.5).to(td)  # no zeros
-    y = torch.full((rows, cols + 3), float("nan"), device="cuda", dtype=td)
-    mgb.mgb_dropout(rows, cols, dt, p32, rng, x, cols, y, cols + 3)
+    y = torch.full((rows, cols + pad), float("nan"), device="cuda", dtype=td)
+    mgb.mgb_dropout(rows, cols, dt, p32, rng, x, cols, y, cols + pad)
     assert mgb.mgb_device_status() == mgb.MGB_OK
     keep = od.dropout_keep(77, 16 * 9, (rows, cols), p32)
     got = y[:, :cols].float().cpu().numpy()
