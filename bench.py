@@ -235,14 +235,18 @@ def run_ours(args, world, rank, local):
     emb = to_device(cin["emb"], torch.bfloat16, dev)
     targets = torch.from_numpy(cin["targets"]).to(dev)
     del cin, arr
-    cer = CERunner(ce.tokens, ce.hidden, ce.vocab, ce.chunk, layer.y, emb, targets,
-                   mode=mgb.MGB_CE_RESIDENT)
     stream = torch.cuda.current_stream(dev)
+    # the CE's weight gradient d_emb runs on its own stream, beside the layer
+    # backward (which needs only d_hidden); each step ends by joining it
+    emb_stream = torch.cuda.Stream(dev)
+    cer = CERunner(ce.tokens, ce.hidden, ce.vocab, ce.chunk, layer.y, emb, targets,
+                   mode=mgb.MGB_CE_RESIDENT, emb_stream=emb_stream)
 
     def step():
         layer.fwd(stream)
         cer.run(stream)
         layer.bwd(cer.d_hidden, stream)
+        stream.wait_stream(emb_stream)
 
     for _ in range(args.warmup):
         step()

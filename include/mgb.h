@@ -211,6 +211,13 @@ typedef struct {
   int32_t dtype;        /* MGB_BF16 (hidden/emb/grads bf16) */
   float grad_scale;     /* dL/dloss_t for every token: 1/tokens for the mean */
   int32_t mode;         /* mgb_ce_mode */
+  /* MGB_CE_RESIDENT only, may be NULL: a stream (cudaStream_t as void*) of the
+   * caller's for the weight gradient d_emb. It waits for the call's earlier
+   * work on `stream` and is not joined back: d_emb, `hidden` and the
+   * workspace stay in use on it, so the caller orders their next use after it
+   * (e.g. cudaStreamWaitEvent of `stream` on an event recorded on it). The
+   * input-gradient work that follows on `stream` then overlaps d_emb. */
+  void* emb_stream;
 } mgb_ce_desc;
 
 mgb_status mgb_vocab_ce_sizes(const mgb_ce_desc* desc, size_t* ws_bytes);

@@ -100,10 +100,12 @@ mgb_status check_arch() {
 // far; join() (also run by the destructor, on every return path) makes the
 // caller's stream wait for the side stream. Events are reused: a wait takes
 // the event's state when it is enqueued. If the stream cannot be created the
-// side work runs on the caller's stream.
+// side work runs on the caller's stream. With an `external` stream the side
+// work goes there instead and is not joined back (the caller orders it).
 class SideLane {
  public:
-  explicit SideLane(cudaStream_t main) : main_(main), side_(main), ev_(nullptr) {
+  explicit SideLane(cudaStream_t main, cudaStream_t external = nullptr)
+      : main_(main), side_(main), ev_(nullptr) {
     struct PerDevice {
       cudaStream_t side = nullptr;
       cudaEvent_t ev[kEvents] = {};
@@ -124,8 +126,9 @@ class SideLane {
       }
     }
     if (d.side != nullptr) {
-      side_ = d.side;
+      side_ = external != nullptr ? external : d.side;
       ev_ = d.ev;
+      detached_ = external != nullptr;
     }
   }
   ~SideLane() { join(); }
@@ -139,7 +142,7 @@ class SideLane {
     return MGB_OK;
   }
   mgb_status join() {
-    if (!forked_) return MGB_OK;
+    if (!forked_ || detached_) return MGB_OK;
     forked_ = false;
     cudaEvent_t e = ev_[kEvents - 1];
     if (cudaEventRecord(e, side_) != cudaSuccess || cudaStreamWaitEvent(main_, e, 0) != cudaSuccess)
@@ -153,6 +156,7 @@ class SideLane {
   cudaEvent_t* ev_;
   int next_ = 0;
   bool forked_ = false;
+  bool detached_ = false;
 };
 
 struct Plan {
@@ -720,7 +724,7 @@ mgb_status mgb_vocab_ce_fwd_bwd(const mgb_ce_desc* desc, const void* hidden, con
     // ---- backward over the resident logits: G in place, then
     // d_hidden = G E on this stream and d_emb = G^T hidden on the side stream
     MGB_TRY(ce_grad_launch(T, V, 0, logits, V, targets, lse_buf, desc->grad_scale, st));
-    SideLane lane(st);
+    SideLane lane(st, as_stream(desc->emb_stream));
     if (d_emb) {
       MGB_TRY(lane.fork());
       MGB_TRY(gemm_launch(mk_gemm(MGB_BF16, V, H, T, 1, logits, V, 1, hidden, H, EPI_STORE,

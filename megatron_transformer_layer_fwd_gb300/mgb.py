@@ -74,7 +74,7 @@ class BlockGrads(ctypes.Structure):
 class CEDesc(ctypes.Structure):
     _fields_ = [("tokens", ctypes.c_int32), ("hidden", ctypes.c_int32), ("vocab", ctypes.c_int32),
                 ("chunk", ctypes.c_int32), ("dtype", ctypes.c_int32), ("grad_scale", ctypes.c_float),
-                ("mode", ctypes.c_int32)]
+                ("mode", ctypes.c_int32), ("emb_stream", ctypes.c_void_p)]
 
 
 class GemmDesc(ctypes.Structure):

@@ -121,3 +121,28 @@ def test_ce_modes_agree_and_are_deterministic(mgb_lib):
         assert float((outs[0][0] - o[0]).abs().max()) < CE_LOSS_ABS
         assert rel_l2(to_np(outs[0][1]), to_np(o[1])) < 2e-2
         assert rel_l2(to_np(outs[0][2]), to_np(o[2])) < 2e-2
+
+
+def test_ce_resident_emb_stream(mgb_lib):
+    """Resident mode with d_emb left on a caller's stream: after joining it the
+    results equal those of the joined call bit for bit, while the caller's
+    stream went on with other work (here: a GEMM reading d_hidden)."""
+    shape = CEShape(384, 256, 2000, 704)
+    inp = ce_inputs(shape, seed=13)
+    r0 = _runner(shape, inp, mgb.MGB_CE_RESIDENT)
+    r0.run()
+    side = torch.cuda.Stream()
+    h = to_device(inp["hidden"], torch.bfloat16)
+    e = to_device(inp["emb"], torch.bfloat16)
+    t = torch.from_numpy(inp["targets"]).to("cuda")
+    r1 = CERunner(shape.tokens, shape.hidden, shape.vocab, shape.chunk, h, e, t,
+                  mode=mgb.MGB_CE_RESIDENT, emb_stream=side)
+    main = torch.cuda.current_stream()
+    r1.run(main)
+    after = r1.d_hidden.float() * 2  # work on the caller's stream meanwhile
+    main.wait_stream(side)
+    torch.cuda.synchronize()
+    assert mgb.mgb_device_status() == mgb.MGB_OK
+    assert torch.equal(r0.d_emb, r1.d_emb) and torch.equal(r0.d_hidden, r1.d_hidden)
+    assert torch.equal(r0.loss, r1.loss)
+    assert torch.equal(after, r0.d_hidden.float() * 2)
