@@ -174,12 +174,12 @@ mgb_status mgb_block_fwd(const mgb_block_desc* desc, const mgb_block_weights* w,
  * and the `saved` buffer of the matching forward (same x and weights), writes
  * dx = dL/dx [T, H] and every non-NULL gradient in `grads`. Attention
  * probabilities are recomputed from the saved log-sum-exp.
- * Weight and bias gradients are computed on a second stream that the library
- * owns (one per host thread and device), forked from and joined back into
- * `stream` inside the call: all results are ordered on `stream` as usual. The
- * first call on a thread and device creates that stream and its events; when
- * the call is to be captured into a CUDA graph, make one call before the
- * capture. */
+ * Weight and bias gradients, and the attention backward's dQ kernel, are
+ * computed on side streams that the library owns (two per host thread and
+ * device), forked from and joined back into `stream` inside the call: all
+ * results are ordered on `stream` as usual. The first call on a thread and
+ * device creates those streams and their events; when the call is to be
+ * captured into a CUDA graph, make one call before the capture. */
 mgb_status mgb_block_bwd(const mgb_block_desc* desc, const mgb_block_weights* w,
                          const void* x, const void* dy, const void* saved, size_t saved_bytes,
                          void* dx, const mgb_block_grads* grads,
@@ -403,7 +403,9 @@ size_t mgb_attention_bwd_ws_bytes(int32_t batch, int32_t seq, int32_t n_q_heads)
  * ld_dkv; the sum over the query heads of each GQA group). P is recomputed
  * from lse. `ws` (16-byte aligned, caller-owned, overwritten) holds the
  * per-query LSE and delta: at least mgb_attention_bwd_ws_bytes(batch, seq,
- * n_q_heads) bytes, else MGB_ERR_WORKSPACE_TOO_SMALL before any launch. */
+ * n_q_heads) bytes, else MGB_ERR_WORKSPACE_TOO_SMALL before any launch. The
+ * bf16 path runs its dQ kernel on a library-owned side stream beside the
+ * dK/dV kernel, joined back into `stream` before the call returns. */
 mgb_status mgb_attention_bwd(int32_t batch, int32_t seq, int32_t n_q_heads, int32_t n_kv_heads,
                              int32_t head_dim, int32_t causal, int32_t dtype,
                              const void* q, const void* k, const void* v, int64_t ld_q,

@@ -12,7 +12,7 @@
 
 namespace mgb {
 
-mgb_status attention_tc_bwd_main(const AttnArgs& a, cudaStream_t st);
+mgb_status attention_tc_bwd_main(const AttnArgs& a, cudaStream_t st, cudaStream_t st_dq);
 
 namespace {
 
@@ -63,7 +63,14 @@ mgb_status attention_bf16_bwd(const AttnArgs& a, cudaStream_t st) {
   else
     return MGB_ERR_UNSUPPORTED;
   if (cudaGetLastError() != cudaSuccess) return MGB_ERR_CUDA;
-  return attention_tc_bwd_main(a, st);
+  // the dK/dV and dQ kernels are independent: dQ on a side stream, so each
+  // fills the SMs the other leaves idle in its last wave
+  SideLane lane(st, nullptr, 1);
+  const mgb_status f = lane.fork();
+  if (f != MGB_OK) return f;
+  const mgb_status r = attention_tc_bwd_main(a, st, lane.side());
+  const mgb_status j = lane.join();
+  return r != MGB_OK ? r : j;
 }
 
 }  // namespace mgb

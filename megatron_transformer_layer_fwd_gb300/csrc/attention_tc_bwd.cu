@@ -637,7 +637,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
 }
 
 template <int D, bool DROP>
-mgb_status bwd_tc_d(const AttnArgs& a, cudaStream_t st) {
+mgb_status bwd_tc_d(const AttnArgs& a, cudaStream_t st, cudaStream_t st_dq) {
   const uint64_t T = (uint64_t)a.B * a.S;
   BwdParams p{};
   p.B = a.B; p.S = a.S; p.nq = a.nq; p.nkv = a.nkv; p.causal = a.causal;
@@ -689,18 +689,21 @@ mgb_status bwd_tc_d(const AttnArgs& a, cudaStream_t st) {
     if (cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM) != cudaSuccess)
       return MGB_ERR_CUDA;
     dim3 grid(a.nq * a.B, (a.S + TR - 1) / TR);
-    k<<<grid, NTHREADS, C::SMEM, st>>>(tq, tk, tv, to, p);
+    k<<<grid, NTHREADS, C::SMEM, st_dq>>>(tq, tk, tv, to, p);
   }
   return cudaGetLastError() == cudaSuccess ? MGB_OK : MGB_ERR_CUDA;
 }
 
 }  // namespace
 
-mgb_status attention_tc_bwd_main(const AttnArgs& a, cudaStream_t st) {
+// dK/dV on st, dQ on st_dq (which the caller has made wait for the inputs).
+mgb_status attention_tc_bwd_main(const AttnArgs& a, cudaStream_t st, cudaStream_t st_dq) {
   const bool drop = a.drop_thr < 256;
   if (drop && a.drop_mask == nullptr) return MGB_ERR_INVALID_ARG;
-  if (a.d == 64) return drop ? bwd_tc_d<64, true>(a, st) : bwd_tc_d<64, false>(a, st);
-  if (a.d == 128) return drop ? bwd_tc_d<128, true>(a, st) : bwd_tc_d<128, false>(a, st);
+  if (a.d == 64)
+    return drop ? bwd_tc_d<64, true>(a, st, st_dq) : bwd_tc_d<64, false>(a, st, st_dq);
+  if (a.d == 128)
+    return drop ? bwd_tc_d<128, true>(a, st, st_dq) : bwd_tc_d<128, false>(a, st, st_dq);
   return MGB_ERR_UNSUPPORTED;
 }
 

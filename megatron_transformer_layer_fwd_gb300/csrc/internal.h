@@ -58,6 +58,73 @@ struct GemmArgs {
   uint64_t drop_seed = 0, drop_offset = 0;
 };
 
+// A library-owned side stream per (host thread, device, slot) for work off a
+// call's critical path (slot 0: weight and bias gradients; slot 1: the
+// attention backward's dQ kernel beside its dK/dV kernel), so that its kernels
+// fill the SMs the critical-path kernels leave idle in their last wave. fork()
+// makes the side stream wait for everything issued on the caller's stream so
+// far; join() (also run by the destructor, on every return path) makes the
+// caller's stream wait for the side stream. Events are reused: a wait takes
+// the event's state when it is enqueued. If the stream cannot be created the
+// side work runs on the caller's stream. With an `external` stream the side
+// work goes there instead and is not joined back (the caller orders it).
+class SideLane {
+ public:
+  explicit SideLane(cudaStream_t main, cudaStream_t external = nullptr, int slot = 0)
+      : main_(main), side_(main), ev_(nullptr) {
+    struct PerDevice {
+      cudaStream_t side = nullptr;
+      cudaEvent_t ev[kEvents] = {};
+      bool failed = false;
+    };
+    thread_local PerDevice per[16][2];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 16 || slot < 0 || slot > 1) return;
+    PerDevice& d = per[dev][slot];
+    if (d.side == nullptr && !d.failed) {
+      bool ok = cudaStreamCreateWithFlags(&d.side, cudaStreamNonBlocking) == cudaSuccess;
+      for (int i = 0; ok && i < kEvents; ++i)
+        ok = cudaEventCreateWithFlags(&d.ev[i], cudaEventDisableTiming) == cudaSuccess;
+      if (!ok) {
+        d.failed = true;
+        d.side = nullptr;
+        cudaGetLastError();
+      }
+    }
+    if (d.side != nullptr) {
+      side_ = external != nullptr ? external : d.side;
+      ev_ = d.ev;
+      detached_ = external != nullptr;
+    }
+  }
+  ~SideLane() { join(); }
+  cudaStream_t side() const { return side_; }
+  mgb_status fork() {
+    if (side_ == main_) return MGB_OK;
+    cudaEvent_t e = ev_[next_++ % (kEvents - 1)];
+    if (cudaEventRecord(e, main_) != cudaSuccess || cudaStreamWaitEvent(side_, e, 0) != cudaSuccess)
+      return MGB_ERR_CUDA;
+    forked_ = true;
+    return MGB_OK;
+  }
+  mgb_status join() {
+    if (!forked_ || detached_) return MGB_OK;
+    forked_ = false;
+    cudaEvent_t e = ev_[kEvents - 1];
+    if (cudaEventRecord(e, side_) != cudaSuccess || cudaStreamWaitEvent(main_, e, 0) != cudaSuccess)
+      return MGB_ERR_CUDA;
+    return MGB_OK;
+  }
+
+ private:
+  static constexpr int kEvents = 8;
+  cudaStream_t main_, side_;
+  cudaEvent_t* ev_;
+  int next_ = 0;
+  bool forked_ = false;
+  bool detached_ = false;
+};
+
 // Validates operand geometry for the chosen path; returns MGB_OK or an error.
 mgb_status gemm_check(const GemmArgs& g);
 // Launches the bf16 tcgen05 GEMM (dtype MGB_BF16) or the float32 SIMT GEMM.
