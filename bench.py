@@ -609,7 +609,7 @@ def main():
     ap.add_argument("--case", default="step",
                     choices=("step", "layer", "sweep", "ce", "gemm", "gemm_layer", "attention",
                              "embedding"),
-                    help="step (default, the driver's line) or a sub-path / single kernel")
+                    help="step (default: the whole hot path, one JSON line) or a sub-path / single kernel")
     ap.add_argument("--mnk", type=int, nargs=3, default=(8192, 22016, 4096))
     ap.add_argument("--dropout", type=float, default=0.0,
                     help="--case layer|sweep: attention and hidden dropout probability")

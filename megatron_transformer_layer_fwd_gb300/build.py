@@ -2,7 +2,7 @@
 
 Each .cu under csrc/ compiles to an object in parallel, then one shared
 library is linked next to this file. The CUDA runtime is linked statically;
-the driver's tensor-map encoder is looked up at run time, so the library
+the CUDA driver's tensor-map encoder is looked up at run time, so the library
 needs no libcuda at link time and loads on machines without a GPU.
 
     python -m megatron_transformer_layer_fwd_gb300.build
