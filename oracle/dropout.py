@@ -40,7 +40,7 @@ import contextlib
 
 import numpy as np
 
-# Philox4x32 round multipliers and Weyl key increments (SC 2011, section 5)
+# Philox4x32 round multipliers and Weyl key increments (Salmon et al., SC 2011)
 PHILOX_M0, PHILOX_M1 = 0xD2511F53, 0xCD9E8D57
 PHILOX_W0, PHILOX_W1 = 0x9E3779B9, 0xBB67AE85
 MASK32 = 0xFFFFFFFF
