@@ -26,9 +26,11 @@
 // dK and dV stay in TMEM across the whole loop, so the GQA sum costs nothing.
 //
 // Kernel B (dQ): one CTA = 128 queries of one head; per 64-key tile (K/V in a
-// 5-stage ring): S = Q K^T, dP = dO V^T (TMEM [0, 128)), dS in registers -> TMEM
-// buffer j & 1 (bf16 pairs, [128, 192)), dQ += dS K (TMEM [256, 256+d), A from
-// TMEM, the K tile read as MN-major).
+// 5-stage ring): S = Q K^T, dP = dO V^T (TMEM [0, 128); Q and dO are copied once
+// into TMEM [384, 512) and read from there, so the products read only K and V
+// from shared memory), dS in registers -> TMEM buffer j & 1 (bf16 pairs,
+// [128, 192)), dQ += dS K (TMEM [256, 256+d), A from TMEM, the K tile read as
+// MN-major).
 //
 // Warp-specialised, 18 warps:
 //   warps 0-15 compute, in two groups of 8 that take alternate tiles (group
@@ -397,8 +399,11 @@ struct DqCfg {
   static constexpr int OFF_V = OFF_K + NSB * KV_BYTES;   // NSB stages
   static constexpr int OFF_BAR = OFF_V + NSB * KV_BYTES;
   static constexpr int SMEM = OFF_BAR + 256 + 1024;
-  // TMEM: scores [0, 128), dS buffers [128, 192) (32 columns = 64 bf16 keys each), dQ
+  // TMEM: scores [0, 128), dS buffers [128, 192) (32 columns = 64 bf16 keys each), dQ,
+  // and the CTA's Q and dO rows (bf16 pairs) as the A operands of the score products
   static constexpr int COL_DS = 128, COL_DQ = COL_ACC;
+  static constexpr int COL_QT = 384, COL_OT = 384 + D / 2;
+  static_assert(COL_DQ + D <= COL_QT && COL_OT + D / 2 <= 512, "TMEM columns");
 };
 
 template <int D, bool DROP>
@@ -422,6 +427,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   const uint32_t ds_full0 = bar + 120;   // [2] dS buffer written         (256 arrivals)
   const uint32_t ds_empty0 = bar + 136;  // [2] dQ read the buffer        (commit)
   const uint32_t acc_done = bar + 152;   // all products done             (commit)
+  const uint32_t qo_tmem = bar + 160;    // Q, dO copied into TMEM        (128 arrivals)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_BAR + 176);
   volatile int* abort = reinterpret_cast<volatile int*>(smem + C::OFF_BAR + 180);
 
@@ -452,6 +458,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       mbar_init(ds_empty0 + 8 * i, 1);
     }
     mbar_init(acc_done, 1);
+    mbar_init(qo_tmem, 128);
     fence_mbar_init();
     *abort = 0;
   }
@@ -489,7 +496,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     // ---------------- MMA issuer
     constexpr uint32_t idesc_sp = idesc_bf16_f32(TR, TC, 0, 0);
     constexpr uint32_t idesc_acc = idesc_bf16_f32(TR, D, 0, 1);
-    const uint64_t dq = smem_desc_sw128(sQ, 16, 1024), dob = smem_desc_sw128(sO, 16, 1024);
     const uint64_t dkk = smem_desc_sw128(sK, 16, 1024), dvk = smem_desc_sw128(sV, 16, 1024);
     const uint64_t dkm = smem_desc_sw128(sK, 8192, 1024);
     auto issue_sp = [&](int j) -> bool {
@@ -499,17 +505,16 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       if (elect_one()) {
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = ((kk >> 2) * (TR * 128) + (kk & 3) * 32) >> 4;
           const uint32_t offk = (s * C::KV_BYTES + (kk >> 2) * 8192 + (kk & 3) * 32) >> 4;
-          tc_mma_f16(tmem, dq + off, dkk + offk, idesc_sp, kk > 0);
-          tc_mma_f16(tmem + 64, dob + off, dvk + offk, idesc_sp, kk > 0);
+          tc_mma_f16_ts(tmem, tmem + C::COL_QT + kk * 8, dkk + offk, idesc_sp, kk > 0);
+          tc_mma_f16_ts(tmem + 64, tmem + C::COL_OT + kk * 8, dvk + offk, idesc_sp, kk > 0);
         }
         tc_commit(sp_full0 + 8 * (j & 1));
       }
       __syncwarp();
       return true;
     };
-    bool good = warp_wait(qo_full, 0, p.err) && issue_sp(0);
+    bool good = warp_wait(qo_tmem, 0, p.err) && issue_sp(0);
     for (int j = 0; j < nkt && good; ++j) {
       // the group of tile j has its scores in registers: the next tile's go in
       if (!warp_wait(sp_free0 + 8 * (j & 1), (j >> 1) & 1, p.err) ||
@@ -544,7 +549,34 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
     const uint32_t col0 = half * 32;
     bool good = true;
-    for (int j = grp; j < nkt; j += 2) {
+    if (warp < 4) {
+      // Q and dO rows of this lane quarter from the (128-byte swizzled) smem
+      // tiles into TMEM, bf16 pairs in column order: the score products then
+      // read them from TMEM instead of shared memory for every key tile
+      if (!warp_wait(qo_full, 0, p.err)) {
+        good = false;
+      } else {
+        const uint32_t r = (uint32_t)rrow, sw = r & 7;
+#pragma unroll
+        for (int mtx = 0; mtx < 2; ++mtx) {
+          const uint8_t* base = smem + (mtx == 0 ? C::OFF_Q : C::OFF_DO) + r * 128;
+#pragma unroll
+          for (int kb = 0; kb < C::KB; ++kb) {
+            uint32_t v[32];
+#pragma unroll
+            for (int c = 0; c < 8; ++c) {
+              const uint4 w = *reinterpret_cast<const uint4*>(base + kb * (TR * 128) + ((c ^ sw) << 4));
+              v[4 * c] = w.x; v[4 * c + 1] = w.y; v[4 * c + 2] = w.z; v[4 * c + 3] = w.w;
+            }
+            tmem_st32(tmem + lane_base + (mtx == 0 ? C::COL_QT : C::COL_OT) + kb * 32, v);
+          }
+        }
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(qo_tmem);
+      }
+    }
+    for (int j = grp; j < nkt && good; j += 2) {
       // keep bits of this query row against the thread's 32 keys (issued before
       // the wait so the load overlaps it)
       uint32_t kbits = 0;
