@@ -422,8 +422,9 @@ const char* mgb_status_string(mgb_status s);
 mgb_status mgb_philox_bytes(uint64_t seed, uint64_t offset, uint64_t n, void* out, void* stream);
 
 /* y = dropout(x) over a [rows, cols] site at state rng (element r*cols + c),
- * probability p in [0, 1); x, y of dtype with leading dims ldx, ldy (y may be
- * x). The same call with the same rng is the backward (dx from dy). */
+ * probability p in [0, 1) with a keep threshold of at least 1 (p below about
+ * 0.998); x, y of dtype with leading dims ldx, ldy (y may be x). The same call
+ * with the same rng is the backward (dx from dy). */
 mgb_status mgb_dropout(int64_t rows, int64_t cols, int32_t dtype, float p, mgb_rng_state rng,
                        const void* x, int64_t ldx, void* y, int64_t ldy, void* stream);
 

@@ -161,8 +161,11 @@ mgb_status validate_desc(const mgb_block_desc* d) {
   if (d->hidden > 16384) return MGB_ERR_UNSUPPORTED;
   // dropout: probabilities in [0, 1); the hidden sites are fused into the bf16
   // residual epilogues (whole 16-element stream blocks per 32-column chunk)
+  // (a probability so close to 1 that no byte is kept is rejected here, before
+  // any launch, rather than by a kernel launcher midway through the layer)
   if (!(d->hidden_dropout >= 0.0f && d->hidden_dropout < 1.0f) ||
-      !(d->attn_dropout >= 0.0f && d->attn_dropout < 1.0f))
+      !(d->attn_dropout >= 0.0f && d->attn_dropout < 1.0f) ||
+      dropout_threshold(d->hidden_dropout) == 0 || dropout_threshold(d->attn_dropout) == 0)
     return MGB_ERR_INVALID_ARG;
   if (d->attn_dropout > 0.0f) {
     // applied in the tcgen05 attention kernels
@@ -750,7 +753,8 @@ mgb_status mgb_philox_bytes(uint64_t seed, uint64_t offset, uint64_t n, void* ou
 
 mgb_status mgb_dropout(int64_t rows, int64_t cols, int32_t dtype, float p, mgb_rng_state rng,
                        const void* x, int64_t ldx, void* y, int64_t ldy, void* stream) {
-  if (rows < 0 || cols < 0 || !(p >= 0.0f && p < 1.0f)) return MGB_ERR_INVALID_ARG;
+  if (rows < 0 || cols < 0 || !(p >= 0.0f && p < 1.0f) || dropout_threshold(p) == 0)
+    return MGB_ERR_INVALID_ARG;
   if (dtype != MGB_BF16 && dtype != MGB_F32) return MGB_ERR_INVALID_ARG;
   if (rng.offset % 16 != 0) return MGB_ERR_INVALID_ARG;
   if (rows > 0 && cols > 0 && (!x || !y || ldx < cols || ldy < cols)) return MGB_ERR_INVALID_ARG;

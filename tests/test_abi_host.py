@@ -185,6 +185,8 @@ def test_dropout_desc_validation(lib):
     assert lib.mgb_block_sizes(ctypes.byref(d), ctypes.byref(s), None, None) == mgb.MGB_ERR_INVALID_ARG
     d.hidden_dropout = -0.1
     assert lib.mgb_block_sizes(ctypes.byref(d), ctypes.byref(s), None, None) == mgb.MGB_ERR_INVALID_ARG
+    d.hidden_dropout = 0.999  # keeps no byte: rejected before any launch
+    assert lib.mgb_block_sizes(ctypes.byref(d), ctypes.byref(s), None, None) == mgb.MGB_ERR_INVALID_ARG
     d.hidden_dropout, d.attn_dropout = 0.0, 0.1
     s0 = mgb.mgb_block_sizes(_desc())[0]
     s1 = mgb.mgb_block_sizes(d)[0]
