@@ -119,14 +119,23 @@ def test_deterministic_repeat(mgb_lib):
     assert torch.equal(y1, y2) and torch.equal(dx1, dx2) and torch.equal(gw1, g2["w_qkv"])
 
 
-def test_graph_capture_replay(mgb_lib):
-    """The layer's forward and backward (including the backward's side stream
-    for weight gradients, forked and joined inside the call) captured into one
-    CUDA graph: replaying it reproduces the eager results bit for bit, also
-    after the inputs are changed in place."""
+@pytest.mark.parametrize("dropout", [0.0, 0.15])
+def test_graph_capture_replay(mgb_lib, dropout):
+    """The layer's forward and backward (including the backward's side streams
+    for weight gradients and the attention dQ kernel, forked and joined inside
+    the call) captured into one CUDA graph: replaying it reproduces the eager
+    results bit for bit, also after the inputs are changed in place; with
+    dropout, the masks come from the descriptor's generator states, so the
+    replay draws the same ones."""
     shape = SMALL["bf16_pre_swiglu_causal_gqa"]
     arr = layer_inputs(shape, seed=4, random_affine=True, random_dy=True)
     r = LayerRunner(shape, arr)
+    if dropout > 0:
+        r.desc.attn_dropout = r.desc.hidden_dropout = dropout
+        mgb.mgb_block_dropout_plan(r.desc, mgb.rng_tracker(99))
+        saved, _, bwd = mgb.mgb_block_sizes(r.desc)
+        r.saved = torch.empty(saved, dtype=torch.uint8, device="cuda")
+        r.ws = torch.empty(bwd, dtype=torch.uint8, device="cuda")
     dy = to_device(arr["dy"], r.dtype)
     side = torch.cuda.Stream()
     with torch.cuda.stream(side):  # first calls on this thread: library streams and events
