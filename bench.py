@@ -362,6 +362,17 @@ def run_ours(args, world, rank, local):
                    "achieved": round(ce_gbs, 1) if ce_gbs else None, "peak": peaks["hbm_gbs"],
                    "unit": "GB/s", "frac": round(ce_gbs / peaks["hbm_gbs"], 4) if ce_gbs else None,
                    "peak_source": f"{peaks['source']} hbm_gbs", "bytes_per_pass": ce_bytes}
+    # the HBM-bound CE kernel of the step itself: one ce_grad launch over the
+    # resident [T, V] logits, read and rewritten in place with G (4 B/entry)
+    rg_ms, rg_n = prof.get("ce_grad", (0.0, 0))
+    rg_bytes = 2.0 * 2 * ce.tokens * ce.vocab
+    rg_gbs = rg_bytes / (rg_ms / rg_n / 1e3) / 1e9 if rg_n > 0 and rg_ms > 0 else None
+    roofline_ce_resident = {
+        "kernel": "ce_grad over the resident logits (one launch per step, in place)",
+        "bound": "hbm", "achieved": round(rg_gbs, 1) if rg_gbs else None, "peak": peaks["hbm_gbs"],
+        "unit": "GB/s", "frac": round(rg_gbs / peaks["hbm_gbs"], 4) if rg_gbs else None,
+        "peak_source": f"{peaks['source']} hbm_gbs", "bytes_per_launch": rg_bytes,
+        "avg_launch_ms": round(rg_ms / rg_n, 4) if rg_n > 0 else None}
     layer_kinds = ("attn_fwd", "attn_bwd", "layernorm_fwd", "layernorm_bwd", "colsum")
     breakdown = {k: round(v[0] / args.steps, 4) for k, v in prof.items() if v[1] > 0}
     out = {
@@ -389,6 +400,7 @@ def run_ours(args, world, rank, local):
         "gpu_launches": int(launches),
         "roofline": roofline,
         "roofline_ce": roofline_ce,
+        "roofline_ce_resident": roofline_ce_resident,
         "gemm_all_launches": gemm_all,
         "kernel_ms_per_step": breakdown,
         "kernel_ms_note": "per kind, the span between library CUDA events on the launching "

@@ -9,9 +9,11 @@
 // Backward is local per shard: G = (softmax - onehot(target)) * scale.
 // Here the shards are vocab chunks processed one after another on one GPU.
 //
-//   ce_stats   one block per token row of a [T, C] bf16 logits chunk: a single
-//              pass of 16-byte loads with a running (max, sum) pair per thread
-//              (rescaled when the max grows), merged across the block.
+//   ce_stats   one warp per token row of a [T, C] bf16 logits chunk: a single
+//              pass of 16-byte loads with a running (max, sum) pair per lane
+//              (rescaled only when the max passes the reference by more than
+//              8 in log2 units: one exponential per logit), merged across the
+//              warp.
 //   ce_combine one thread per token: partials -> LSE, per-token loss; block
 //              sums of the loss then summed in fixed order (deterministic).
 // The same combine serves the partials the logits GEMM's epilogue writes when
@@ -36,76 +38,72 @@ __device__ __forceinline__ void ms_merge(float& m, float& s, float m2, float s2)
   m = mn;
 }
 
+// One 8-value vector into a thread's running (max, sum) pair, log2 domain.
+// The reference max moves only when the vector's max passes it by more than
+// 8 (so terms stay below 2^8), which makes the rescale rare after the first
+// vectors: one exponential per value.
+__device__ __forceinline__ void ms_vec8(const uint4& w, float& m, float& s) {
+  const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
+  float x[8];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float2 f = unpack_bf16x2(ww[i]);
+    x[2 * i] = f.x;
+    x[2 * i + 1] = f.y;
+  }
+  const float mx = fmaxf(fmax3(x[0], x[1], x[2]), fmax3(fmax3(x[3], x[4], x[5]), x[6], x[7])) * LOG2E;
+  if (mx > m + 8.0f) {
+    s = m == -INFINITY ? 0.0f : s * ex2_ftz(m - mx);
+    m = mx;
+  }
+  if (m == -INFINITY) return;  // nothing but -inf so far
+  const float nm = -m;
+  float a0 = 0.0f, a1 = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 8; i += 2) {
+    float e0, e1;
+    fma2(e0, e1, x[i], x[i + 1], LOG2E, LOG2E, nm, nm);
+    add2(a0, a1, a0, a1, ex2_ftz(e0), ex2_ftz(e1));
+  }
+  s += a0 + a1;
+}
+
+// One warp per token row (no block-wide barrier): each lane keeps eight
+// 16-byte loads in flight and a running (max, sum) pair; the warp merges the
+// pairs with shuffles.
 __global__ void __launch_bounds__(CE_THREADS) ce_stats_kernel(int T, int C, int v0,
                                                                const bf16* __restrict__ logits,
                                                                int64_t ldl,
                                                                const int32_t* __restrict__ tgt,
                                                                float* m_out, float* s_out,
                                                                float* t_out) {
-  const int row = blockIdx.x;
+  const int row = blockIdx.x * (CE_THREADS / 32) + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (row >= T) return;  // whole warps leave together
   const bf16* l = logits + (int64_t)row * ldl;
   const int nvec = C / 8;
   float m = -INFINITY, s = 0.0f;
-  int v = threadIdx.x;
-  // four 16-byte loads in flight per thread
-  for (; v + 3 * CE_THREADS < nvec; v += 4 * CE_THREADS) {
-    uint4 w[4];
+  constexpr int U = 8;
+  for (int v0i = lane; v0i < nvec; v0i += U * 32) {
+    uint4 w[U];
 #pragma unroll
-    for (int u = 0; u < 4; ++u) w[u] = __ldg(reinterpret_cast<const uint4*>(l) + v + u * CE_THREADS);
-#pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const uint32_t ww[4] = {w[u].x, w[u].y, w[u].z, w[u].w};
-      float x[8];
-      float mx = -INFINITY;
-#pragma unroll
-      for (int i = 0; i < 4; ++i) {
-        const float2 f = unpack_bf16x2(ww[i]);
-        x[2 * i] = f.x * LOG2E;
-        x[2 * i + 1] = f.y * LOG2E;
-        mx = fmaxf(mx, fmaxf(x[2 * i], x[2 * i + 1]));
-      }
-      float acc = 0.0f;
-#pragma unroll
-      for (int i = 0; i < 8; ++i) acc += exp2f(x[i] - mx);
-      ms_merge(m, s, mx, acc);
+    for (int u = 0; u < U; ++u) {
+      const int v = v0i + u * 32;
+      if (v < nvec) w[u] = __ldg(reinterpret_cast<const uint4*>(l) + v);
     }
-  }
-  for (; v < nvec; v += CE_THREADS) {
-    const uint4 w = __ldg(reinterpret_cast<const uint4*>(l) + v);
-    const uint32_t ww[4] = {w.x, w.y, w.z, w.w};
-    float x[8];
-    float mx = -INFINITY;
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const float2 f = unpack_bf16x2(ww[i]);
-      x[2 * i] = f.x * LOG2E;
-      x[2 * i + 1] = f.y * LOG2E;
-      mx = fmaxf(mx, fmaxf(x[2 * i], x[2 * i + 1]));
-    }
-    float acc = 0.0f;
-#pragma unroll
-    for (int i = 0; i < 8; ++i) acc += exp2f(x[i] - mx);
-    ms_merge(m, s, mx, acc);
+    for (int u = 0; u < U; ++u)
+      if (v0i + u * 32 < nvec) ms_vec8(w[u], m, s);
   }
-  // block merge
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
     const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
     const float s2 = __shfl_xor_sync(0xffffffffu, s, o);
     ms_merge(m, s, m2, s2);
   }
-  __shared__ float sm_m[CE_THREADS / 32], sm_s[CE_THREADS / 32];
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (lane == 0) {
-    sm_m[warp] = m;
-    sm_s[warp] = s;
-  }
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    float M = sm_m[0], Ssum = sm_s[0];
-    for (int w = 1; w < CE_THREADS / 32; ++w) ms_merge(M, Ssum, sm_m[w], sm_s[w]);
-    m_out[row] = M * LN2;
-    s_out[row] = Ssum;
+    m_out[row] = m * LN2;
+    s_out[row] = s;
     // rows whose target lies in this chunk already hold the float32 target
     // logit (written by the logits GEMM epilogue); the rest contribute 0
     const int tc = tgt[row] - v0;
@@ -197,8 +195,8 @@ __global__ void __launch_bounds__(CE_THREADS) ce_grad_kernel(int T, int C, int v
 #pragma unroll
       for (int i = 0; i < 4; ++i) {
         const float2 f = unpack_bf16x2(ww[i]);
-        float g0 = exp2f(f.x * LOG2E - L2);
-        float g1 = exp2f(f.y * LOG2E - L2);
+        float g0 = ex2_ftz(fmaf(f.x, LOG2E, -L2));
+        float g1 = ex2_ftz(fmaf(f.y, LOG2E, -L2));
         const int c0 = v * 8 + 2 * i;
         if (c0 == tc) g0 -= 1.0f;
         if (c0 + 1 == tc) g1 -= 1.0f;
@@ -215,7 +213,9 @@ mgb_status ce_stats_launch(int T, int C, int v0, const void* logits, int64_t ldl
                            const int32_t* targets, float* m, float* s, float* t, cudaStream_t st) {
   if (T == 0) return MGB_OK;
   LaunchScope scope(PROF_CE_STATS, st);
-  ce_stats_kernel<<<T, CE_THREADS, 0, st>>>(T, C, v0, (const bf16*)logits, ldl, targets, m, s, t);
+  constexpr int rows_per_block = CE_THREADS / 32;
+  ce_stats_kernel<<<(T + rows_per_block - 1) / rows_per_block, CE_THREADS, 0, st>>>(
+      T, C, v0, (const bf16*)logits, ldl, targets, m, s, t);
   return cudaGetLastError() == cudaSuccess ? MGB_OK : MGB_ERR_CUDA;
 }
 
