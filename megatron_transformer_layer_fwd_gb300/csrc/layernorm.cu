@@ -164,11 +164,12 @@ __device__ __forceinline__ float2 block_sum2(float2 v, float2* red) {
 // dres are all requested before the row reduction, so each thread keeps
 // 3 * VPT loads in flight.
 template <typename T, int VPT>
-__global__ void ln_bwd_kernel(int rows, int cols, const T* __restrict__ x,
-                              const float* __restrict__ mean, const float* __restrict__ rstd,
-                              const T* __restrict__ gamma, const T* __restrict__ dy,
-                              const T* __restrict__ dres, T* __restrict__ dx,
-                              float* __restrict__ part) {
+__device__ __forceinline__ void ln_bwd_rows(int rows, int cols, const T* __restrict__ x,
+                                            const float* __restrict__ mean,
+                                            const float* __restrict__ rstd,
+                                            const T* __restrict__ gamma, const T* __restrict__ dy,
+                                            const T* __restrict__ dres, T* __restrict__ dx,
+                                            float* __restrict__ part) {
   constexpr int VN = Vec<T>::N;
   __shared__ float2 red[32];
   const int nvec = cols / VN;
@@ -248,6 +249,27 @@ __global__ void ln_bwd_kernel(int rows, int cols, const T* __restrict__ x,
       }
     }
   }
+}
+
+// Rows of up to 1024 vectors: one vector per thread.
+template <typename T, int VPT>
+__global__ void ln_bwd_kernel(int rows, int cols, const T* __restrict__ x,
+                              const float* __restrict__ mean, const float* __restrict__ rstd,
+                              const T* __restrict__ gamma, const T* __restrict__ dy,
+                              const T* __restrict__ dres, T* __restrict__ dx,
+                              float* __restrict__ part) {
+  ln_bwd_rows<T, VPT>(rows, cols, x, mean, rstd, gamma, dy, dres, dx, part);
+}
+
+// Wider rows (VPT 2 or 4 vectors per thread, up to 1024 threads): the register
+// count is held to 64 a thread so a full block always launches; these spill a
+// little instead.
+template <typename T, int VPT>
+__global__ void __launch_bounds__(1024, 1) ln_bwd_wide_kernel(
+    int rows, int cols, const T* __restrict__ x, const float* __restrict__ mean,
+    const float* __restrict__ rstd, const T* __restrict__ gamma, const T* __restrict__ dy,
+    const T* __restrict__ dres, T* __restrict__ dx, float* __restrict__ part) {
+  ln_bwd_rows<T, VPT>(rows, cols, x, mean, rstd, gamma, dy, dres, dx, part);
 }
 
 // out0[c] = sum_p part[p, c] and out1[c] = sum_p part[nparts + p, c], written
@@ -367,9 +389,14 @@ template <typename T, int VPT>
 void ln_bwd_go(int nparts, int threads, int rows, int cols, const void* x, const float* mean,
                const float* rstd, const void* gamma, const void* dy, const void* dres, void* dx,
                float* part, cudaStream_t st) {
-  ln_bwd_kernel<T, VPT><<<nparts, threads, 0, st>>>(rows, cols, (const T*)x, mean, rstd,
-                                                      (const T*)gamma, (const T*)dy,
-                                                      (const T*)dres, (T*)dx, part);
+  if constexpr (VPT == 1)
+    ln_bwd_kernel<T, 1><<<nparts, threads, 0, st>>>(rows, cols, (const T*)x, mean, rstd,
+                                                    (const T*)gamma, (const T*)dy,
+                                                    (const T*)dres, (T*)dx, part);
+  else
+    ln_bwd_wide_kernel<T, VPT><<<nparts, threads, 0, st>>>(rows, cols, (const T*)x, mean, rstd,
+                                                           (const T*)gamma, (const T*)dy,
+                                                           (const T*)dres, (T*)dx, part);
 }
 
 template <typename T>

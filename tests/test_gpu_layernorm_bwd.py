@@ -19,7 +19,11 @@ def _dev(a, dtype):
 
 @pytest.mark.parametrize("dtype,rows,cols,affine,resid", [
     ("bf16", 300, 1024, True, True), ("bf16", 2048, 4096, True, False), ("bf16", 5, 256, False, True),
-    ("f32", 130, 256, True, True), ("f32", 64, 64, False, False)])
+    ("f32", 130, 256, True, True), ("f32", 64, 64, False, False),
+    # rows wider than 1024 vectors: two or four vectors per thread, up to 1024
+    # threads a block (the widest rows the layer accepts)
+    ("bf16", 40, 12288, True, True), ("bf16", 33, 16384, True, False),
+    ("f32", 20, 8192, True, True), ("f32", 17, 16384, True, True)])
 def test_layernorm_bwd(mgb_lib, dtype, rows, cols, affine, resid):
     x = RNG.standard_normal((rows, cols)) * 1.5 + 0.3
     dy = RNG.standard_normal((rows, cols))
