@@ -102,10 +102,10 @@ struct Plan {
   size_t s_dmask;  // attention keep bits (attn_dropout > 0)
   size_t saved;
   // backward workspace
-  size_t w_dffn, w_dh, w_dr2, w_du, w_dO, w_dqkv, w_dxn, w_delta, w_cparts, w_lparts;
+  size_t w_dffn, w_dh, w_dr2, w_du, w_dO, w_dqkv, w_dxn, w_delta, w_cparts, w_lparts, w_fparts;
   size_t w_dz1, w_dz2;  // hidden dropout: the projection's / fc2's branch gradients
   size_t bwd;
-  int cparts, lparts;
+  int cparts, lparts, fparts;
   bool hdrop;
 };
 
@@ -222,6 +222,13 @@ void make_plan(const mgb_block_desc* d, Plan* p) {
   p->w_delta = take(attn_bwd_ws_bytes(p->B, p->S, p->nq));
   p->w_cparts = take(4 * (size_t)p->cparts * maxN);
   p->w_lparts = take(4 * 2 * (size_t)p->lparts * p->H);
+  // bf16 with biases: the fc2 input-gradient epilogue leaves db1's partial sums
+  // per 32 rows here (the float32 path sums du with the column-sum kernel)
+  // (at least one row: with no tokens the reduction zeroes one and sums it)
+  p->fparts = (p->T + 31) / 32;
+  p->w_fparts = (d->dtype == MGB_BF16 && d->has_bias)
+                    ? take(4 * (size_t)(p->fparts > 0 ? p->fparts : 1) * p->W)
+                    : 0;
   p->hdrop = d->hidden_dropout > 0.0f;
   p->w_dz1 = p->hdrop ? take(es * T * p->H) : 0;
   p->w_dz2 = p->hdrop ? take(es * T * p->H) : 0;
@@ -468,15 +475,21 @@ mgb_status mgb_block_bwd(const mgb_block_desc* desc, const mgb_block_weights* w,
   if (gr->b_2) MGB_TRY(colsum_launch(T, H, dt, dz2, H, gr->b_2, cparts, p.cparts, s2));
   if (gr->w_2)
     MGB_TRY(gemm_launch(mk_gemm(dt, H, p.F, T, 1, dz2, H, 1, a, p.F, EPI_STORE, gr->w_2, p.F), s2));
+  const bool fused_db1 = gr->b_1 != nullptr && dt == MGB_BF16;
   {
     GemmArgs g = mk_gemm(dt, T, p.F, H, 0, dz2, H, 1, w->w_2, p.F,
                          p.swiglu ? EPI_DSWIGLU : EPI_DGELU, du, p.W);
     g.aux = u; g.ldaux = p.W; g.glu_block = desc->glu_block;
+    if (fused_db1) g.colsum_part = at<float>(ws, p.w_fparts);
     MGB_TRY(gemm_launch(g, st));
+    if (fused_db1)
+      MGB_TRY(colsum_reduce_launch(T > 0 ? p.fparts : 0, p.W, dt, at<float>(ws, p.w_fparts),
+                                   gr->b_1, st));
   }
   // fc1: db1, dW1 = du^T f_in, d f_in = du W1
   MGB_TRY(lane.fork());
-  if (gr->b_1) MGB_TRY(colsum_launch(T, p.W, dt, du, p.W, gr->b_1, cparts, p.cparts, s2));
+  if (gr->b_1 && !fused_db1)
+    MGB_TRY(colsum_launch(T, p.W, dt, du, p.W, gr->b_1, cparts, p.cparts, s2));
   if (gr->w_1)
     MGB_TRY(gemm_launch(mk_gemm(dt, p.W, H, T, 1, du, p.W, 1, f_in, H, EPI_STORE, gr->w_1, H), s2));
   const void* dr1;

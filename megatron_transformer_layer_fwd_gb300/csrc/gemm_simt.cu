@@ -157,6 +157,10 @@ mgb_status gemm_check(const GemmArgs& g) {
   if ((g.epi == EPI_BIAS_GELU || g.epi == EPI_BIAS_SWIGLU) && g.C2 == nullptr) return MGB_ERR_INVALID_ARG;
   if (g.epi == EPI_BIAS_RESID && g.resid == nullptr) return MGB_ERR_INVALID_ARG;
   if ((g.epi == EPI_DGELU || g.epi == EPI_DSWIGLU) && g.aux == nullptr) return MGB_ERR_INVALID_ARG;
+  // fused bias-gradient partials: activation-backward epilogues, tensor-core path
+  if (g.colsum_part != nullptr &&
+      (g.dtype != MGB_BF16 || (g.epi != EPI_DGELU && g.epi != EPI_DSWIGLU)))
+    return MGB_ERR_INVALID_ARG;
   if (g.epi == EPI_BIAS_SWIGLU || g.epi == EPI_DSWIGLU) {
     const int gb = g.glu_block;
     if (gb <= 0) return MGB_ERR_INVALID_ARG;

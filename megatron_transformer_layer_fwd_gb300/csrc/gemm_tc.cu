@@ -73,6 +73,7 @@ struct EpiParams {
   uint32_t drop_thr;
   float drop_scale;
   uint64_t drop_seed, drop_offset;
+  float* cpart;
 };
 
 template <int BN, int STAGES>
@@ -124,6 +125,28 @@ __device__ __forceinline__ void tmem_chunk(uint32_t taddr, float alpha, bool hav
   tmem_ld_wait();
 #pragma unroll
   for (int j = 0; j < 32; ++j) acc[j] = have_acc ? alpha * __uint_as_float(r[j]) : 0.0f;
+}
+
+// Column sums over the warp's 32 rows (one row per lane) of 32 columns held
+// as v[0..31] in each lane: a butterfly that halves the columns a lane keeps
+// at each of five shuffle steps, so lane l ends with column l's sum; it is
+// stored as row `row / 32` of the partials, which exist for the blocks of 32
+// rows that start below M (a warp wholly past M stores nothing). Every lane of
+// the warp must call it.
+__device__ __forceinline__ void colsum32_store(float* part, int64_t ld, int row, int M, int c0,
+                                               int ncols, float (&v)[32]) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int off = 16; off >= 1; off >>= 1) {
+    const bool up = (lane & off) != 0;
+#pragma unroll
+    for (int j = 0; j < off; ++j) {
+      const float send = up ? v[j] : v[j + off];
+      const float keep = up ? v[j + off] : v[j];
+      v[j] = keep + __shfl_xor_sync(0xffffffffu, send, off);
+    }
+  }
+  if ((row & ~31) < M && c0 + lane < ncols) part[(int64_t)(row >> 5) * ld + c0 + lane] = v[0];
 }
 
 // Epilogue for one thread = one output row `row` of the tile.
@@ -233,6 +256,71 @@ __device__ void epilogue_row(const EpiParams& p, uint32_t tmem_row, int row, int
     }
     return;
   }
+  if (p.epi == EPI_DGELU || p.epi == EPI_DSWIGLU) {
+    // activation backward: da (the accumulator) times act'(u); rows past M
+    // take no loads or stores but join the warp's bias-gradient column sums
+    const int gb = p.glu_block;
+    for (int lc = 0; lc < BN; lc += 32) {
+      float acc[32];
+      tmem_chunk(tmem_row + lc, p.alpha, have_acc, acc);
+      const int n = n0 + lc;
+      if (n >= p.N) continue;  // the same for the whole warp
+      if (p.epi == EPI_DGELU) {
+        if (row_ok) {
+          const bf16* ua = p.aux + (int64_t)row * p.ldaux + n;
+          bf16* c = reinterpret_cast<bf16*>(p.C) + (int64_t)row * p.ldc + n;
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            if (n + 8 * q < p.N) {
+              float u[8];
+              load8(ua + 8 * q, u);
+#pragma unroll
+              for (int j = 0; j < 8; ++j) acc[8 * q + j] *= gelu_erf_grad(u[j]);
+              store8(c + 8 * q, acc + 8 * q);
+            } else {
+#pragma unroll
+              for (int j = 0; j < 8; ++j) acc[8 * q + j] = 0.0f;
+            }
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) acc[j] = 0.0f;
+        }
+        if (p.cpart) colsum32_store(p.cpart, p.N, row, p.M, n, p.N, acc);
+      } else {
+        const int i = n / gb, cc = n % gb;
+        const int colg = 2 * i * gb + cc, colu = colg + gb;
+        float dg[32], du[32];
+        if (row_ok) {
+          const bf16* ar = p.aux + (int64_t)row * p.ldaux;
+          bf16* c = reinterpret_cast<bf16*>(p.C) + (int64_t)row * p.ldc;
+#pragma unroll
+          for (int q = 0; q < 4; ++q) {
+            float g[8], u[8];
+            load8(ar + colg + 8 * q, g);
+            load8(ar + colu + 8 * q, u);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+              const float sg = sigmoidf_(g[j]);
+              const float da = acc[8 * q + j];
+              du[8 * q + j] = da * g[j] * sg;
+              dg[8 * q + j] = da * u[j] * sg * (1.0f + g[j] * (1.0f - sg));
+            }
+            store8(c + colg + 8 * q, dg + 8 * q);
+            store8(c + colu + 8 * q, du + 8 * q);
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) dg[j] = du[j] = 0.0f;
+        }
+        if (p.cpart) {
+          colsum32_store(p.cpart, 2 * (int64_t)p.N, row, p.M, colg, 2 * p.N, dg);
+          colsum32_store(p.cpart, 2 * (int64_t)p.N, row, p.M, colu, 2 * p.N, du);
+        }
+      }
+    }
+    return;
+  }
   // target column of this row relative to the tile (CE logits: fp32 capture)
   int tcol = -1;
   if (p.tgt != nullptr && row_ok) tcol = p.tgt[row] - p.tgt_v0 - n0;
@@ -296,44 +384,6 @@ __device__ void epilogue_row(const EpiParams& p, uint32_t tmem_row, int row, int
             for (int j = 0; j < 8; ++j) x[j] += acc[8 * q + j];
             store8(c + 8 * q, x);
           }
-        }
-        break;
-      }
-      case EPI_DGELU: {
-        const bf16* ua = p.aux + (int64_t)row * p.ldaux + n;
-        bf16* c = reinterpret_cast<bf16*>(p.C) + (int64_t)row * p.ldc + n;
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          if (n + 8 * q < p.N) {
-            float u[8];
-            load8(ua + 8 * q, u);
-#pragma unroll
-            for (int j = 0; j < 8; ++j) u[j] = acc[8 * q + j] * gelu_erf_grad(u[j]);
-            store8(c + 8 * q, u);
-          }
-        }
-        break;
-      }
-      case EPI_DSWIGLU: {
-        const int gb = p.glu_block;
-        const int i = n / gb, cc = n % gb;
-        const int colg = 2 * i * gb + cc, colu = colg + gb;
-        const bf16* ar = p.aux + (int64_t)row * p.ldaux;
-        bf16* c = reinterpret_cast<bf16*>(p.C) + (int64_t)row * p.ldc;
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          float g[8], u[8], dg[8], du[8];
-          load8(ar + colg + 8 * q, g);
-          load8(ar + colu + 8 * q, u);
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const float s = sigmoidf_(g[j]);
-            const float da = acc[8 * q + j];
-            du[j] = da * g[j] * s;
-            dg[j] = da * u[j] * s * (1.0f + g[j] * (1.0f - s));
-          }
-          store8(c + colg + 8 * q, dg);
-          store8(c + colu + 8 * q, du);
         }
         break;
       }
@@ -910,6 +960,7 @@ mgb_status gemm_tc_launch(const GemmArgs& g, cudaStream_t st) {
   ep.drop_offset = g.drop_offset;
   ep.tgt_v0 = g.tgt_v0;
   ep.tgt_out = g.tgt_out;
+  ep.cpart = (g.epi == EPI_DGELU || g.epi == EPI_DSWIGLU) ? g.colsum_part : nullptr;
   // Tile: 256 x 256 on a CTA pair when there are enough such tiles to fill
   // the GPU; else 128 x 256 on one SM, or 128 x 128 when the problem is too
   // narrow to fill the GPU with 256 columns. MGB_GEMM_PAIR=0 / =1 turns the

@@ -56,6 +56,12 @@ struct GemmArgs {
   uint32_t drop_thr = 256;
   float drop_scale = 1.0f;
   uint64_t drop_seed = 0, drop_offset = 0;
+  // EPI_DGELU / EPI_DSWIGLU with bf16 operands, may be null: bias-gradient
+  // partials of the stored output. For each block p of 32 rows,
+  // colsum_part[p * W + c] = the float32 sum over the block's rows (< M) of
+  // output column c before bf16 rounding; W = N (DGELU) or 2N (DSWIGLU);
+  // ceil(M / 32) blocks. colsum_reduce_launch folds them.
+  float* colsum_part = nullptr;
 };
 
 // A library-owned side stream per (host thread, device, slot) for work off a
@@ -146,6 +152,9 @@ int layernorm_bwd_parts(int rows);
 mgb_status colsum_launch(int M, int N, int dtype, const void* dY, int64_t ld, void* db,
                          float* part, int nparts, cudaStream_t st);
 int colsum_parts(int M);
+// out[c] = sum over p < nparts of part[p * N + c], fixed order, as dtype.
+mgb_status colsum_reduce_launch(int nparts, int N, int dtype, const float* part, void* out,
+                                cudaStream_t st);
 
 // Attention (fused online softmax); layouts as mgb_attention_fwd.
 struct AttnArgs {

@@ -506,6 +506,23 @@ mgb_status colsum_launch(int M, int N, int dtype, const void* dY, int64_t ld, vo
   return cudaGetLastError() == cudaSuccess ? MGB_OK : MGB_ERR_CUDA;
 }
 
+mgb_status colsum_reduce_launch(int nparts, int N, int dtype, const float* part, void* out,
+                                cudaStream_t st) {
+  if (N < 0 || nparts < 0) return MGB_ERR_INVALID_ARG;
+  if (N == 0) return MGB_OK;
+  LaunchScope scope(PROF_COLSUM, st);
+  if (nparts == 0) {
+    cudaMemsetAsync(const_cast<float*>(part), 0, sizeof(float) * N, st);
+    nparts = 1;
+  }
+  const dim3 blocks((N + 31) / 32), block(32, 8);
+  if (dtype == MGB_BF16)
+    reduce_parts_kernel<bf16><<<blocks, block, 0, st>>>(nparts, N, part, (bf16*)out, nullptr);
+  else
+    reduce_parts_kernel<float><<<blocks, block, 0, st>>>(nparts, N, part, (float*)out, nullptr);
+  return cudaGetLastError() == cudaSuccess ? MGB_OK : MGB_ERR_CUDA;
+}
+
 }  // namespace mgb
 
 extern "C" mgb_status mgb_layernorm_bwd_noalloc(int32_t rows, int32_t cols, int32_t dtype,
