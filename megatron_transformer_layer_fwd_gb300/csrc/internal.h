@@ -152,8 +152,9 @@ int layernorm_bwd_parts(int rows);
 mgb_status colsum_launch(int M, int N, int dtype, const void* dY, int64_t ld, void* db,
                          float* part, int nparts, cudaStream_t st);
 int colsum_parts(int M);
-// out[c] = sum over p < nparts of part[p * N + c], fixed order, as dtype.
-mgb_status colsum_reduce_launch(int nparts, int N, int dtype, const float* part, void* out,
+// out[c] = sum over p < nparts of part[p * N + c], fixed order, as dtype; the
+// partial buffer is scratch (overwritten). nparts 0: out = 0 (one row zeroed).
+mgb_status colsum_reduce_launch(int nparts, int N, int dtype, float* part, void* out,
                                 cudaStream_t st);
 
 // Attention (fused online softmax); layouts as mgb_attention_fwd.

@@ -14,7 +14,9 @@
 // dgamma = sum dy*xhat and dbeta = sum dy partials of its own columns in
 // registers, written per block and reduced by a second small kernel.
 // Column sums db[n] = sum_m dY[m, n] (bias gradients) use the same
-// partial-then-reduce scheme with coalesced 16-byte row reads.
+// partial-then-reduce scheme with coalesced 16-byte row reads. Many partial
+// rows (the backward's 1024) are folded in two stages: 16 splits of rows
+// folded in place, then the split results.
 #include <mutex>
 
 #include "common.cuh"
@@ -272,20 +274,23 @@ __global__ void __launch_bounds__(1024, 1) ln_bwd_wide_kernel(
   ln_bwd_rows<T, VPT>(rows, cols, x, mean, rstd, gamma, dy, dres, dx, part);
 }
 
-// out0[c] = sum_p part[p, c] and out1[c] = sum_p part[nparts + p, c], written
-// as T (nullable outputs skipped). Block (32 x 8): lane = column (coalesced
-// 128-byte rows of the partial buffer), the 8 warps split the partials, fixed
-// order of summation (deterministic).
+// out0[c] = sum_p part[p * stride, c] and out1[c] = sum_p part[half + p * stride, c]
+// for p < nparts (rows of `cols` floats), written as T (nullable outputs
+// skipped). Block (32 x 8): lane = column (coalesced 128-byte rows of the
+// partial buffer), the 8 warps split the partials, fixed order of summation
+// (deterministic).
 template <typename T>
-__global__ void reduce_parts_kernel(int nparts, int cols, const float* __restrict__ part,
-                                    T* __restrict__ out0, T* __restrict__ out1) {
+__global__ void reduce_parts_kernel(int nparts, int stride, int64_t half, int cols,
+                                    const float* __restrict__ part, T* __restrict__ out0,
+                                    T* __restrict__ out1) {
   __shared__ float red[2][8][33];
   const int c = blockIdx.x * 32 + threadIdx.x;
   float s0 = 0.0f, s1 = 0.0f;
   if (c < cols) {
     for (int p = threadIdx.y; p < nparts; p += 8) {
-      if (out0) s0 += part[(int64_t)p * cols + c];
-      if (out1) s1 += part[(int64_t)(nparts + p) * cols + c];
+      const int64_t o = (int64_t)p * stride * cols + c;
+      if (out0) s0 += part[o];
+      if (out1) s1 += part[half + o];
     }
   }
   red[0][threadIdx.y][threadIdx.x] = s0;
@@ -300,6 +305,68 @@ __global__ void reduce_parts_kernel(int nparts, int cols, const float* __restric
     }
     if (out0) out0[c] = from_f<T>(a);
     if (out1) out1[c] = from_f<T>(b);
+  }
+}
+
+// First stage for many partial rows: split blockIdx.y folds rows
+// [p0, p0 + per) of 128 columns (four per lane, 16-byte loads) into row p0,
+// in place, and the same rows of the second half when `two` is set. Each block
+// alone reads and writes its rows and columns, so the in-place write races
+// with nothing. Fixed order of summation.
+__global__ void __launch_bounds__(256) fold_parts_kernel(int nparts, int per, int cols,
+                                                         float* __restrict__ part, int two) {
+  __shared__ float4 red[2][8][32];
+  const int c = (blockIdx.x * 32 + threadIdx.x) * 4;
+  const int p0 = blockIdx.y * per, p1 = min(nparts, p0 + per);
+  const int64_t half = (int64_t)nparts * cols;
+  float4 a0 = make_float4(0.0f, 0.0f, 0.0f, 0.0f), a1 = a0;
+  if (c < cols) {
+    for (int p = p0 + threadIdx.y; p < p1; p += 8) {
+      const float4 v = *reinterpret_cast<const float4*>(part + (int64_t)p * cols + c);
+      a0.x += v.x; a0.y += v.y; a0.z += v.z; a0.w += v.w;
+      if (two) {
+        const float4 w = *reinterpret_cast<const float4*>(part + half + (int64_t)p * cols + c);
+        a1.x += w.x; a1.y += w.y; a1.z += w.z; a1.w += w.w;
+      }
+    }
+  }
+  red[0][threadIdx.y][threadIdx.x] = a0;
+  red[1][threadIdx.y][threadIdx.x] = a1;
+  __syncthreads();
+  if (threadIdx.y == 0 && c < cols && p0 < p1) {
+    float4 s0 = red[0][0][threadIdx.x], s1 = red[1][0][threadIdx.x];
+#pragma unroll
+    for (int y = 1; y < 8; ++y) {
+      const float4 u = red[0][y][threadIdx.x], w = red[1][y][threadIdx.x];
+      s0.x += u.x; s0.y += u.y; s0.z += u.z; s0.w += u.w;
+      s1.x += w.x; s1.y += w.y; s1.z += w.z; s1.w += w.w;
+    }
+    *reinterpret_cast<float4*>(part + (int64_t)p0 * cols + c) = s0;
+    if (two) *reinterpret_cast<float4*>(part + half + (int64_t)p0 * cols + c) = s1;
+  }
+}
+
+constexpr int kFoldSplits = 16;
+// Partial counts from which the reduction folds in two stages.
+bool fold_first(int nparts, int cols) { return nparts >= 8 * kFoldSplits && cols % 4 == 0; }
+int reduce_launches(int nparts, int cols) { return fold_first(nparts, cols) ? 2 : 1; }
+
+// out0/out1 from [2][nparts][cols] float32 partials (the second half only read
+// when out1 is set); the partial buffer may be overwritten (first stage).
+template <typename T>
+void reduce_parts_go(int nparts, int cols, float* part, T* out0, T* out1, cudaStream_t st) {
+  const int64_t half = (int64_t)nparts * cols;
+  const dim3 block(32, 8);
+  if (fold_first(nparts, cols)) {
+    const int per = (nparts + kFoldSplits - 1) / kFoldSplits;
+    const int splits = (nparts + per - 1) / per;
+    fold_parts_kernel<<<dim3((cols + 127) / 128, splits), block, 0, st>>>(nparts, per, cols, part,
+                                                                          out1 != nullptr);
+    reduce_parts_kernel<T><<<(cols + 31) / 32, block, 0, st>>>(splits, per, half, cols, part,
+                                                               out0, out1);
+  } else {
+    reduce_parts_kernel<T><<<(cols + 31) / 32, block, 0, st>>>(nparts, 1, half, cols, part, out0,
+                                                               out1);
   }
 }
 
@@ -431,7 +498,7 @@ mgb_status layernorm_bwd_launch(int rows, int cols, int dtype, const void* x, co
   // the dgamma/dbeta partial rows of the workspace are sized for this width
   if (want && cols > kLnBwdMaxCols) return MGB_ERR_UNSUPPORTED;
   if (rows == 0) nparts = 1;
-  LaunchScope scope(PROF_LN_BWD, st, (rows > 0 ? 1 : 0) + (want ? 1 : 0));
+  LaunchScope scope(PROF_LN_BWD, st, (rows > 0 ? 1 : 0) + (want ? reduce_launches(nparts, cols) : 0));
   if (rows > 0) {
     const mgb_status s =
         dtype == MGB_BF16
@@ -444,13 +511,10 @@ mgb_status layernorm_bwd_launch(int rows, int cols, int dtype, const void* x, co
     cudaMemsetAsync(part, 0, sizeof(float) * 2 * cols, st);
   }
   if (want) {
-    const dim3 blocks((cols + 31) / 32), block(32, 8);
     if (dtype == MGB_BF16)
-      reduce_parts_kernel<bf16><<<blocks, block, 0, st>>>(nparts, cols, part, (bf16*)dgamma,
-                                                           (bf16*)dbeta);
+      reduce_parts_go<bf16>(nparts, cols, part, (bf16*)dgamma, (bf16*)dbeta, st);
     else
-      reduce_parts_kernel<float><<<blocks, block, 0, st>>>(nparts, cols, part, (float*)dgamma,
-                                                            (float*)dbeta);
+      reduce_parts_go<float>(nparts, cols, part, (float*)dgamma, (float*)dbeta, st);
   }
   return cudaGetLastError() == cudaSuccess ? MGB_OK : MGB_ERR_CUDA;
 }
@@ -486,10 +550,10 @@ mgb_status colsum_launch(int M, int N, int dtype, const void* dY, int64_t ld, vo
   const int vn = dtype == MGB_BF16 ? 8 : 4;
   if (N % vn || ld % vn) return MGB_ERR_INVALID_ARG;
   if (N == 0) return MGB_OK;
-  LaunchScope scope(PROF_COLSUM, st, M == 0 ? 1 : 2);
+  if (M == 0) nparts = 1;
+  LaunchScope scope(PROF_COLSUM, st, (M == 0 ? 0 : 1) + reduce_launches(nparts, N));
   if (M == 0) {
     cudaMemsetAsync(part, 0, sizeof(float) * N, st);
-    nparts = 1;
   } else {
     dim3 grid((N / vn + 31) / 32, nparts);
     dim3 block(32, 8);
@@ -498,28 +562,26 @@ mgb_status colsum_launch(int M, int N, int dtype, const void* dY, int64_t ld, vo
     else
       colsum_kernel<float><<<grid, block, 0, st>>>(M, N, (const float*)dY, ld, part);
   }
-  const dim3 blocks((N + 31) / 32), block(32, 8);
   if (dtype == MGB_BF16)
-    reduce_parts_kernel<bf16><<<blocks, block, 0, st>>>(nparts, N, part, (bf16*)db, nullptr);
+    reduce_parts_go<bf16>(nparts, N, part, (bf16*)db, nullptr, st);
   else
-    reduce_parts_kernel<float><<<blocks, block, 0, st>>>(nparts, N, part, (float*)db, nullptr);
+    reduce_parts_go<float>(nparts, N, part, (float*)db, nullptr, st);
   return cudaGetLastError() == cudaSuccess ? MGB_OK : MGB_ERR_CUDA;
 }
 
-mgb_status colsum_reduce_launch(int nparts, int N, int dtype, const float* part, void* out,
+mgb_status colsum_reduce_launch(int nparts, int N, int dtype, float* part, void* out,
                                 cudaStream_t st) {
   if (N < 0 || nparts < 0) return MGB_ERR_INVALID_ARG;
   if (N == 0) return MGB_OK;
-  LaunchScope scope(PROF_COLSUM, st);
   if (nparts == 0) {
-    cudaMemsetAsync(const_cast<float*>(part), 0, sizeof(float) * N, st);
+    if (cudaMemsetAsync(part, 0, sizeof(float) * N, st) != cudaSuccess) return MGB_ERR_CUDA;
     nparts = 1;
   }
-  const dim3 blocks((N + 31) / 32), block(32, 8);
+  LaunchScope scope(PROF_COLSUM, st, reduce_launches(nparts, N));
   if (dtype == MGB_BF16)
-    reduce_parts_kernel<bf16><<<blocks, block, 0, st>>>(nparts, N, part, (bf16*)out, nullptr);
+    reduce_parts_go<bf16>(nparts, N, part, (bf16*)out, nullptr, st);
   else
-    reduce_parts_kernel<float><<<blocks, block, 0, st>>>(nparts, N, part, (float*)out, nullptr);
+    reduce_parts_go<float>(nparts, N, part, (float*)out, nullptr, st);
   return cudaGetLastError() == cudaSuccess ? MGB_OK : MGB_ERR_CUDA;
 }
 
