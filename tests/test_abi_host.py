@@ -60,6 +60,25 @@ def test_block_sizes_cover_saved_activations(lib):
     assert saved >= floor and fwd == 0 and bwd > 0
 
 
+def test_bwd_workspace_holds_the_fused_bias_partials(lib):
+    """bf16 with biases: the backward workspace also holds the fc1 bias
+    gradient's float32 partial sums, one row of 2F (SwiGLU) or F columns per
+    32 tokens, which the fp32 path and bias-free layers do without."""
+    shape = WORKLOADS["bf16_gqa_swiglu_b2s4096h4096"]
+    d = mgb.block_desc(shape)
+    with_bias = mgb.mgb_block_sizes(d)[2]
+    d.has_bias = 0
+    without = mgb.mgb_block_sizes(d)[2]
+    rows = (shape.tokens + 31) // 32
+    assert with_bias - without >= 4 * rows * 2 * shape.ffn
+    # no tokens: still one zeroed row
+    d0 = mgb.block_desc(shape)
+    d0.batch = 0
+    b0 = mgb.mgb_block_sizes(d0)[2]
+    d0.has_bias = 0
+    assert b0 - mgb.mgb_block_sizes(d0)[2] >= 4 * 2 * shape.ffn
+
+
 def test_fwd_argument_errors_before_any_launch(lib):
     d = _desc()
     w = mgb.BlockWeights()
