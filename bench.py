@@ -206,9 +206,9 @@ class OracleSample:
 
 # ------------------------------------------------------------ our arm
 
-def traffic_record(kernel_src: str) -> float | None:
-    """Per-launch DRAM bytes from the committed ncu summary, if it was taken
-    on the current kernel source."""
+def traffic_record(kernel_src: str, kind: str) -> float | None:
+    """Per-launch DRAM bytes (read + write) of a kernel kind from the committed
+    ncu summary, if it was taken on the current kernel source."""
     p = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(p):
         return None
@@ -216,7 +216,7 @@ def traffic_record(kernel_src: str) -> float | None:
     h = hashlib.sha256(open(kernel_src, "rb").read()).hexdigest()[:16]
     if d.get("source_sha256_16") != h:
         return None
-    return d.get("bytes_per_launch")
+    return d.get("kinds", {}).get(kind, {}).get("bytes_per_launch")
 
 
 def run_ours(args, world, rank, local):
@@ -235,19 +235,27 @@ def run_ours(args, world, rank, local):
     emb = to_device(cin["emb"], torch.bfloat16, dev)
     targets = torch.from_numpy(cin["targets"]).to(dev)
     del cin, arr
-    stream = torch.cuda.current_stream(dev)
-    # the CE's weight gradient d_emb runs on its own stream, beside the layer
-    # backward (which needs only d_hidden); each step ends by joining it
+    # the step's stream outranks the library's side streams (lowest priority):
+    # when SMs free up, the critical path's pending blocks start first
+    torch.cuda.synchronize(dev)  # inputs copied on the default stream are in place
+    stream = torch.cuda.Stream(dev, priority=-1)
+    torch.cuda.set_stream(stream)
+    # the CE's weight gradient d_emb (its last token block) runs on its own
+    # stream, beside the layer backward (which needs only d_hidden); each step
+    # ends by joining it
     emb_stream = torch.cuda.Stream(dev)
     cer = CERunner(ce.tokens, ce.hidden, ce.vocab, ce.chunk, layer.y, emb, targets,
-                   mode=mgb.MGB_CE_RESIDENT, emb_stream=emb_stream)
+                   mode=mgb.MGB_CE_BLOCKED, emb_stream=emb_stream, token_block=args.token_block)
 
-    def step():
-        layer.fwd(stream)
-        cer.run(stream)
-        layer.bwd(cer.d_hidden, stream)
-        stream.wait_stream(emb_stream)
+    def make_step(c):
+        def step():
+            layer.fwd(stream)
+            c.run(stream)
+            layer.bwd(c.d_hidden, stream)
+            stream.wait_stream(emb_stream)
+        return step
 
+    step = make_step(cer)
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize(dev)
@@ -312,67 +320,79 @@ def run_ours(args, world, rank, local):
     step_flops = lf["total"] + cf["total"]
     value = world * step_flops / (ms / 1e3) / 1e12
     peaks = load_peaks()
-    # Dominant kernel: the tcgen05 GEMM on the CE logits shape (T x chunk x H,
-    # one launch per chunk: the resident-logits CE recomputes none). Algorithmic
-    # FLOPs per launch = 2*T*chunk*H; duration from the live events.
-    lg_ms, lg_n = prof["gemm_tc_ce_logits"]
-    lg_flops = 2.0 * ce.tokens * ce.chunk * ce.hidden
-    lg_tflops = lg_flops / (lg_ms / lg_n / 1e3) / 1e12 if lg_n else None
+    tb = cer.token_block
+    # Dominant kernel: of the CE's three GEMM kinds (logits with the statistics
+    # epilogue; G E split over K; G^T hidden accumulated across token blocks),
+    # each 2*T*V*H FLOPs per step, the one with the most device time. Its
+    # algorithmic FLOPs per launch / its mean launch time from the live events.
+    kinds = {"gemm_tc_ce_logits": f"CE logits, per token block and vocab chunk "
+                                  f"{tb}x{ce.chunk}x{ce.hidden} (K/K, statistics epilogue storing "
+                                  "the block's logits)",
+             "gemm_tc_ce_dgrad": f"CE d_hidden = G E per token block, {tb}x{ce.hidden}x{ce.vocab} "
+                                 "(K/MN, split over K into float32 planes)",
+             "gemm_tc_ce_wgrad": f"CE d_emb += G^T hidden per token block, "
+                                 f"{ce.vocab}x{ce.hidden}x{tb} (MN/MN, float32 accumulate)"}
+    dom = max(kinds, key=lambda k: prof.get(k, (0.0, 0))[0])
+    d_ms, d_n = prof[dom]
+    d_flops = 2.0 * ce.tokens * ce.vocab * ce.hidden * args.steps / d_n if d_n else 0.0
+    d_tflops = d_flops / (d_ms / d_n / 1e3) / 1e12 if d_n else None
     traffic = traffic_record(os.path.join(ROOT, "megatron_transformer_layer_fwd_gb300", "csrc",
-                                          "gemm_tc.cu"))
-    roofline = {"kernel": f"gemm_tc_pair_kernel, CE logits {ce.tokens}x{ce.chunk}x{ce.hidden} (K/K, "
-                          "statistics epilogue storing the resident logits)",
-                "bound": "tensor", "achieved": round(lg_tflops, 1) if lg_tflops else None,
+                                          "gemm_tc.cu"), dom)
+    roofline = {"kernel": f"{dom}: {kinds[dom]}",
+                "bound": "tensor", "achieved": round(d_tflops, 1) if d_tflops else None,
                 "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s",
-                "frac": round(lg_tflops / peaks["bf16_tflops_sustained"], 4) if lg_tflops else None,
+                "frac": round(d_tflops / peaks["bf16_tflops_sustained"], 4) if d_tflops else None,
                 "peak_source": f"{peaks['source']} bf16_tflops_sustained (kernel inside a long step)",
-                "flops_per_launch": lg_flops, "launches_per_step": lg_n / args.steps,
-                "avg_launch_ms": round(lg_ms / lg_n, 4) if lg_n else None,
-                "traffic": traffic}
-    # all tcgen05 GEMM work of the step (2MNK each; the CE's logits,
-    # input-gradient and weight-gradient GEMMs, none recomputed) against the
-    # whole step: GEMMs on the side streams overlap other work, so per-kind
-    # event spans overlap and are not summed
+                "flops_per_launch": d_flops, "launches_per_step": d_n / args.steps,
+                "avg_launch_ms": round(d_ms / d_n, 4) if d_n else None,
+                "traffic": traffic,
+                "per_kind_tflops": {k: round(2.0 * ce.tokens * ce.vocab * ce.hidden * args.steps
+                                             / (prof[k][0] / 1e3) / 1e12, 1)
+                                    for k in kinds if prof.get(k, (0, 0))[0] > 0}}
+    # all tcgen05 GEMM work of the step (2MNK each, none recomputed)
     gemm_flops_step = 3 * lf["gemm_fwd"] + 3 * 2.0 * ce.tokens * ce.vocab * ce.hidden
-    gemm_kinds = ("gemm_tc_fwd", "gemm_tc_dgrad", "gemm_tc_wgrad", "gemm_tc_ce_logits")
+    gemm_kinds = ("gemm_tc_fwd", "gemm_tc_dgrad", "gemm_tc_wgrad", "gemm_tc_ce_logits",
+                  "gemm_tc_ce_dgrad", "gemm_tc_ce_wgrad")
     gemm_all = {"tflop_per_step": round(gemm_flops_step / 1e12, 3),
                 "share_of_step_flops": round(gemm_flops_step / step_flops, 4),
                 "launches_per_step": sum(prof[k][1] for k in gemm_kinds) / args.steps}
-    # The step's CE takes its statistics in the logits GEMM's epilogue and keeps
-    # the logits resident (MGB_CE_RESIDENT). The streaming CE kernels (the
-    # HBM-bound form of the same rows) are timed on two extra passes of
-    # MGB_CE_STREAM on the same tensors, after the timed region.
-    sr = CERunner(ce.tokens, ce.hidden, ce.vocab, ce.chunk, layer.y, emb, targets,
-                  mode=mgb.MGB_CE_STREAM)
-    sr.run(stream)
-    torch.cuda.synchronize(dev)
-    mgb.mgb_profile_reset()
-    mgb.mgb_profile_enable(True)
-    for _ in range(2):
-        sr.run(stream)
-    torch.cuda.synchronize(dev)
-    mgb.mgb_profile_enable(False)
-    sprof = mgb.mgb_profile_read()
-    del sr
-    ce_ms = (sprof["ce_stats"][0] + sprof["ce_grad"][0]) / 2
-    ce_bytes = ce_stream_bytes(ce)
-    ce_gbs = ce_bytes / (ce_ms / 1e3) / 1e9 if ce_ms > 0 else None
-    roofline_ce = {"kernel": "ce_stats + ce_grad (streaming CE mode, 2 passes after the timed region)",
-                   "bound": "hbm",
-                   "achieved": round(ce_gbs, 1) if ce_gbs else None, "peak": peaks["hbm_gbs"],
-                   "unit": "GB/s", "frac": round(ce_gbs / peaks["hbm_gbs"], 4) if ce_gbs else None,
-                   "peak_source": f"{peaks['source']} hbm_gbs", "bytes_per_pass": ce_bytes}
-    # the HBM-bound CE kernel of the step itself: one ce_grad launch over the
-    # resident [T, V] logits, read and rewritten in place with G (4 B/entry)
+    # the HBM-bound CE kernel of the step: ce_grad over each token block's
+    # logits [rows, V], read and rewritten in place with G (4 B per logit)
     rg_ms, rg_n = prof.get("ce_grad", (0.0, 0))
-    rg_bytes = 2.0 * 2 * ce.tokens * ce.vocab
-    rg_gbs = rg_bytes / (rg_ms / rg_n / 1e3) / 1e9 if rg_n > 0 and rg_ms > 0 else None
-    roofline_ce_resident = {
-        "kernel": "ce_grad over the resident logits (one launch per step, in place)",
+    rg_bytes = 4.0 * ce.tokens * ce.vocab * args.steps
+    rg_gbs = rg_bytes / (rg_ms / 1e3) / 1e9 if rg_ms > 0 else None
+    roofline_ce = {
+        "kernel": f"ce_grad over each token block's logits ({tb} x {ce.vocab}, in place)",
         "bound": "hbm", "achieved": round(rg_gbs, 1) if rg_gbs else None, "peak": peaks["hbm_gbs"],
         "unit": "GB/s", "frac": round(rg_gbs / peaks["hbm_gbs"], 4) if rg_gbs else None,
-        "peak_source": f"{peaks['source']} hbm_gbs", "bytes_per_launch": rg_bytes,
+        "peak_source": f"{peaks['source']} hbm_gbs",
+        "bytes_per_launch": 4.0 * tb * ce.vocab, "launches_per_step": rg_n / args.steps,
         "avg_launch_ms": round(rg_ms / rg_n, 4) if rg_n > 0 else None}
+    # The same step with the resident-logits CE (the whole [T, V] logits held:
+    # outside the pages' memory bound), for comparison; a few steps after the
+    # timed region.
+    res = CERunner(ce.tokens, ce.hidden, ce.vocab, ce.chunk, layer.y, emb, targets,
+                   mode=mgb.MGB_CE_RESIDENT, emb_stream=emb_stream)
+    rstep = make_step(res)
+    for _ in range(2):
+        rstep()
+    torch.cuda.synchronize(dev)
+    r0, r1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    r_steps = max(3, args.steps // 3)
+    r0.record(stream)
+    for _ in range(r_steps):
+        rstep()
+    r1.record(stream)
+    torch.cuda.synchronize(dev)
+    res_ms = r0.elapsed_time(r1) / r_steps
+    del res
+    step_resident = {"ms_per_step": round(res_ms, 4),
+                     "tflops": round(world * step_flops / (res_ms / 1e3) / 1e12, 2),
+                     "ce_workspace_gb": round(mgb.mgb_vocab_ce_sizes(mgb.ce_desc(
+                         ce.tokens, ce.hidden, ce.vocab, ce.chunk, 1.0 / ce.tokens,
+                         mgb.MGB_CE_RESIDENT)) / 1e9, 3),
+                     "note": "same step with MGB_CE_RESIDENT (whole [T, V] logits kept); "
+                             "outside the pages' memory bound, for comparison only"}
     layer_kinds = ("attn_fwd", "attn_bwd", "layernorm_fwd", "layernorm_bwd", "colsum")
     breakdown = {k: round(v[0] / args.steps, 4) for k, v in prof.items() if v[1] > 0}
     out = {
@@ -400,7 +420,10 @@ def run_ours(args, world, rank, local):
         "gpu_launches": int(launches),
         "roofline": roofline,
         "roofline_ce": roofline_ce,
-        "roofline_ce_resident": roofline_ce_resident,
+        "ce": {"mode": "MGB_CE_BLOCKED", "token_block": tb,
+               "workspace_gb": round(cer.ws.numel() / 1e9, 3),
+               "full_logits_gb": round(2.0 * ce.tokens * ce.vocab / 1e9, 3)},
+        "step_resident_ce": step_resident,
         "gemm_all_launches": gemm_all,
         "kernel_ms_per_step": breakdown,
         "kernel_ms_note": "per kind, the span between library CUDA events on the launching "
@@ -431,6 +454,26 @@ def _time_loop(fn, steps, warmup, stream):
     return e0.elapsed_time(e1) / steps, prof
 
 
+def _layer_line(args, name, shape, ms, prof):
+    """One JSON line of --case layer / sweep: the layer's fwd+bwd time, the
+    pages' three stages and the attention core, from the library's events."""
+    lf = layer_flops(shape)
+    gem = ("gemm_tc_fwd", "gemm_tc_dgrad", "gemm_tc_wgrad")
+    return {"case": args.case, "workload": name, "dropout": args.dropout, "ms": round(ms, 4),
+            "tflops": round(lf["total"] / (ms / 1e3) / 1e12, 1),
+            "frac_of_nominal_2250": round(lf["total"] / (ms / 1e3) / 2.25e15, 4),
+            "tokens_per_s": round(shape.tokens / (ms / 1e3), 1),
+            # page 1's three segments, each between library CUDA events on the
+            # stream: Attention (LN1, QKV, attention, projection + residual),
+            # FFN (LN2, fc1 + activation, fc2 + residual), Backward (all of it)
+            "stage_ms": {"attention": prof.get("stage_attention", 0),
+                         "ffn": prof.get("stage_ffn", 0),
+                         "backward": prof.get("stage_backward", 0)},
+            "attention_core_ms": {"fwd": prof.get("attn_fwd", 0), "bwd": prof.get("attn_bwd", 0)},
+            "gemm_ms": round(sum(prof.get(k, 0) for k in gem), 4),
+            "kernel_ms": prof}
+
+
 def run_case(args):
     """Sub-paths and single kernels of the step (for ncu captures and the
     sequence sweep); prints one JSON line per measurement."""
@@ -440,6 +483,8 @@ def run_case(args):
     build.build()
     torch.cuda.set_device(0)
     st = torch.cuda.current_stream()
+    # the critical path's stream outranks the library's side streams
+    hi = torch.cuda.Stream(priority=-1)
     peaks = load_peaks()
     if args.case == "gemm":
         M, N, K = args.mnk
@@ -491,6 +536,7 @@ def run_case(args):
     if args.case in ("layer", "sweep"):
         names = [LAYER] if args.case == "layer" else [f"bf16_causal_b8s{s}h2048"
                                                       for s in (128, 256, 512, 1024, 2048)]
+        sweep = []
         for name in names:
             shape = WORKLOADS[name]
             r = LayerRunner(shape, layer_inputs(shape, seed=0))
@@ -503,26 +549,38 @@ def run_case(args):
                 r.saved = torch.empty(saved, dtype=torch.uint8, device="cuda")
                 r.ws = torch.empty(bwd, dtype=torch.uint8, device="cuda")
             dy = torch.full_like(r.x, 1.0 / (shape.tokens * shape.hidden))
+            variants = [("high-priority stream, side streams", hi, "1")]
+            if args.case == "layer":
+                variants += [("default-priority stream, side streams", st, "1"),
+                             ("high-priority stream, serial (MGB_SIDE_STREAMS=0)", hi, "0")]
+            for vname, vst, side in variants:
+                os.environ["MGB_SIDE_STREAMS"] = side
 
-            def fb():
-                r.fwd(st)
-                r.bwd(dy, st)
-            ms, prof = _time_loop(fb, args.steps, args.warmup, st)
-            lf = layer_flops(shape)
-            gem = ("gemm_tc_fwd", "gemm_tc_dgrad", "gemm_tc_wgrad")
-            out = {"case": args.case, "workload": name, "dropout": args.dropout, "ms": round(ms, 4),
-                   "tflops": round(lf["total"] / (ms / 1e3) / 1e12, 1),
-                   "frac_of_nominal_2250": round(lf["total"] / (ms / 1e3) / 2.25e15, 4),
-                   "tokens_per_s": round(shape.tokens / (ms / 1e3), 1),
-                   "attention_ms": round(prof.get("attn_fwd", 0) + prof.get("attn_bwd", 0), 4),
-                   "gemm_ms": round(sum(prof.get(k, 0) for k in gem), 4),
-                   "kernel_ms": prof}
-            if args.case == "sweep":
-                # page 1's three segments: Attention (LN1..proj), FFN (LN2..fc2), Backward
-                out["stage_ms"] = {"attention_fwd_core": prof.get("attn_fwd", 0),
-                                   "attention_bwd_core": prof.get("attn_bwd", 0)}
-            print(json.dumps(out), flush=True)
+                def fb():
+                    r.fwd(vst)
+                    r.bwd(dy, vst)
+                ms, prof = _time_loop(fb, args.steps, args.warmup, vst)
+                os.environ.pop("MGB_SIDE_STREAMS", None)
+                out = _layer_line(args, name, shape, ms, prof)
+                out["streams"] = vname
+                if args.case == "sweep":
+                    sweep.append((shape.seq, out["stage_ms"], out["attention_core_ms"]))
+                print(json.dumps(out), flush=True)
             del r
+        if args.case == "sweep":
+            # growth per doubling of seq: attention work grows 4x (S^2), the
+            # FFN's 2x (linear in tokens) at fixed batch
+            def growth(f):
+                return [round(f(b) / f(a), 3) for a, b in zip(sweep, sweep[1:]) if f(a) > 0]
+            print(json.dumps({
+                "case": "sweep_summary", "seq": [q for q, _, _ in sweep],
+                "stage_ms": {k: [st_[k] for _, st_, _ in sweep] for k in ("attention", "ffn", "backward")},
+                "growth_per_doubling": {
+                    "stage_attention": growth(lambda e: e[1]["attention"]),
+                    "stage_ffn": growth(lambda e: e[1]["ffn"]),
+                    "stage_backward": growth(lambda e: e[1]["backward"]),
+                    "attention_core_fwd_bwd": growth(lambda e: e[2]["fwd"] + e[2]["bwd"])},
+                "work_growth": {"attention_core": 4.0, "ffn": 2.0}}), flush=True)
         return
     if args.case == "attention":
         # the attention core of the layer workload: forward, then backward
@@ -590,15 +648,22 @@ def run_case(args):
         emb = to_device(cin["emb"], torch.bfloat16)
         tg = torch.from_numpy(cin["targets"]).to("cuda")
         cf = ce_flops(ce)
-        modes = [(mgb.MGB_CE_STREAM, "stream"), (mgb.MGB_CE_FUSED, "fused"),
-                 (mgb.MGB_CE_RESIDENT, "resident")]
+        modes = [(mgb.MGB_CE_STREAM, "stream", 0), (mgb.MGB_CE_FUSED, "fused", 0),
+                 (mgb.MGB_CE_RESIDENT, "resident", 0), (mgb.MGB_CE_BLOCKED, "blocked",
+                                                        args.token_block)]
+        if args.ce_mode == "blocked" and args.token_block == 0:
+            modes += [(mgb.MGB_CE_BLOCKED, "blocked", tb) for tb in (1024, 4096)]
         modes = [m for m in modes if args.ce_mode in (m[1], "all")]
-        for mode, name in modes:
-            r = CERunner(ce.tokens, ce.hidden, ce.vocab, ce.chunk, hid, emb, tg, mode=mode)
-            ms, prof = _time_loop(lambda: r.run(st), args.steps, args.warmup, st)
+        for mode, name, tb in modes:
+            r = CERunner(ce.tokens, ce.hidden, ce.vocab, ce.chunk, hid, emb, tg, mode=mode,
+                         token_block=tb)
+            ms, prof = _time_loop(lambda: r.run(hi), args.steps, args.warmup, hi)
             out = {"case": "ce", "mode": name, "ms": round(ms, 4),
-                   "tflops": round(cf["total"] / (ms / 1e3) / 1e12, 1), "kernel_ms": prof}
-            if mode != mgb.MGB_CE_RESIDENT:
+                   "tflops": round(cf["total"] / (ms / 1e3) / 1e12, 1),
+                   "workspace_gb": round(r.ws.numel() / 1e9, 3), "kernel_ms": prof}
+            if mode == mgb.MGB_CE_BLOCKED:
+                out["token_block"] = r.token_block
+            if mode in (mgb.MGB_CE_STREAM, mgb.MGB_CE_FUSED):
                 out["tflops_with_recompute"] = round((cf["total"] + cf["recompute"]) / (ms / 1e3) / 1e12, 1)
             if mode == mgb.MGB_CE_STREAM:
                 sb = ce_stream_bytes(ce)
@@ -625,8 +690,11 @@ def main():
     ap.add_argument("--mnk", type=int, nargs=3, default=(8192, 22016, 4096))
     ap.add_argument("--dropout", type=float, default=0.0,
                     help="--case layer|sweep: attention and hidden dropout probability")
-    ap.add_argument("--ce-mode", default="all", choices=("all", "stream", "fused", "resident"),
+    ap.add_argument("--ce-mode", default="all",
+                    choices=("all", "stream", "fused", "resident", "blocked"),
                     help="--case ce: which CE mode(s) to time")
+    ap.add_argument("--token-block", type=int, default=0,
+                    help="tokens per block of the blocked CE (0: the library's default)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -195,13 +195,28 @@ typedef enum {
                          group) max / sum exp partials of its float32
                          accumulator and stores no logits; the recomputing
                          GEMM's epilogue writes the gradient directly */
-  MGB_CE_RESIDENT = 2 /* as MGB_CE_FUSED for the partials, and the epilogue
+  MGB_CE_RESIDENT = 2, /* as MGB_CE_FUSED for the partials, and the epilogue
                          also stores every chunk's bf16 logits into one
                          [tokens, vocab] workspace buffer (2 bytes per logit):
                          the backward rewrites them into the gradient in one
                          streaming pass and runs one input-gradient and one
                          weight-gradient GEMM over the whole vocabulary, with
-                         no logits recomputed */
+                         no logits recomputed. Holds the full [tokens, vocab]
+                         logits: outside the pages' memory bound */
+  MGB_CE_BLOCKED = 3  /* tokens in blocks of token_block rows; per block, the
+                         logits GEMM of every vocab chunk keeps per-(token,
+                         128-column group) max / sum exp partials (as
+                         MGB_CE_FUSED) and stores the block's bf16 logits
+                         [token_block, vocab]; the partials are combined into
+                         the block's LSE and losses; one streaming pass
+                         rewrites the block's logits into G; then
+                         d_hidden rows = G E (K split into ranges, float32
+                         partial planes summed in fixed order) and
+                         d_emb += G^T hidden (float32 accumulator across
+                         blocks). Never more than one block of logits is
+                         held and none is recomputed: the workspace is
+                         O(token_block * vocab + vocab * hidden), whatever
+                         the number of tokens */
 } mgb_ce_mode;
 
 /* Tied-embedding cross-entropy [P2 sections 3-4]. */
@@ -211,13 +226,18 @@ typedef struct {
   int32_t dtype;        /* MGB_BF16 (hidden/emb/grads bf16) */
   float grad_scale;     /* dL/dloss_t for every token: 1/tokens for the mean */
   int32_t mode;         /* mgb_ce_mode */
-  /* MGB_CE_RESIDENT only, may be NULL: a stream (cudaStream_t as void*) of the
-   * caller's for the weight gradient d_emb. It waits for the call's earlier
-   * work on `stream` and is not joined back: d_emb, `hidden` and the
-   * workspace stay in use on it, so the caller orders their next use after it
-   * (e.g. cudaStreamWaitEvent of `stream` on an event recorded on it). The
-   * input-gradient work that follows on `stream` then overlaps d_emb. */
+  /* MGB_CE_RESIDENT and MGB_CE_BLOCKED, may be NULL: a stream (cudaStream_t
+   * as void*) of the caller's for the weight gradient d_emb (BLOCKED: the last
+   * block's part of it). It waits for the call's earlier work on `stream` and
+   * is not joined back: d_emb, `hidden` and the workspace stay in use on it,
+   * so the caller orders their next use after it (e.g. cudaStreamWaitEvent of
+   * `stream` on an event recorded on it). The work that follows on `stream`
+   * then overlaps d_emb. */
   void* emb_stream;
+  /* MGB_CE_BLOCKED only: tokens per block (0 = 2048), rounded up to a
+   * multiple of 256; the logits block takes 2 * token_block * vocab bytes of
+   * the workspace. Other modes ignore it. */
+  int32_t token_block;
 } mgb_ce_desc;
 
 mgb_status mgb_vocab_ce_sizes(const mgb_ce_desc* desc, size_t* ws_bytes);
@@ -229,7 +249,10 @@ mgb_status mgb_vocab_ce_sizes(const mgb_ce_desc* desc, size_t* ws_bytes);
  * G = (softmax(l) - onehot(target)) * grad_scale, d_hidden = G E,
  * d_emb = G^T hidden, again chunk by chunk (logits recomputed per chunk).
  * MGB_CE_FUSED keeps one (max, sum) partial per token and 128 vocab columns
- * instead of one per chunk; the combine is the same merge. MGB_CE_RESIDENT
+ * instead of one per chunk; the combine is the same merge. MGB_CE_BLOCKED
+ * walks the tokens in blocks (see mgb_ce_mode) and needs about
+ * 2 * token_block * vocab + 4 * vocab * hidden bytes of workspace (the second
+ * term only with d_emb and more than one block). MGB_CE_RESIDENT
  * needs a workspace of about 2 * tokens * vocab bytes (mgb_vocab_ce_sizes)
  * and runs the weight gradient on a library-owned second stream, joined back
  * into `stream` before the call returns (as mgb_block_bwd).
@@ -339,15 +362,21 @@ mgb_status mgb_layernorm_bwd(int32_t rows, int32_t cols, int32_t dtype, const vo
  *   - size: 2 x 64 x 16384 floats (8 MiB), held by every GPU that loads the
  *     library until the process exits; cols > 16384 with dgamma or dbeta
  *     requested returns MGB_ERR_UNSUPPORTED before any launch;
+ *   - a call uses min(the row blocks mgb_layernorm_bwd would use,
+ *     2^20 / cols) partial rows of the array (256 at cols = 4096), so the
+ *     backward still spreads over the whole GPU;
  *   - the library calls no cudaMalloc/cudaFree or allocating routine (keep
  *     the tracing of mgb_profile_enable off: when on, it creates CUDA events);
  *   - the first call on each device looks up the array's device address with
- *     that device current; make that first call before any stream capture;
+ *     that device current (again after the device's context was destroyed
+ *     and created anew, e.g. by cudaDeviceReset); make that first call before
+ *     any stream capture;
  *   - every call on a device shares the array: calls that may run at the same
  *     time on the GPU (different streams, no ordering between them) race and
  *     give wrong dgamma/dbeta; serialise them.
- * The dgamma/dbeta sums use 64 row blocks (mgb_layernorm_bwd uses more), so
- * the two entry points agree to float32 rounding, not bit for bit. */
+ * With fewer partial rows than mgb_layernorm_bwd for wide rows, the two entry
+ * points agree to float32 rounding, not always bit for bit. MGB_FAULT=validate
+ * makes it fail validation like every other entry point. */
 mgb_status mgb_layernorm_bwd_noalloc(int32_t rows, int32_t cols, int32_t dtype, const void* x,
                                      const float* mean, const float* rstd, const void* gamma,
                                      const void* dy, const void* dres, void* dx, void* dgamma,

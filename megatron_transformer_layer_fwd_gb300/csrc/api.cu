@@ -13,6 +13,7 @@
 #include <stdlib.h>
 #include <string.h>
 
+#include <memory>
 #include <mutex>
 
 #include "common.cuh"
@@ -23,16 +24,37 @@ namespace mgb {
 // One error word per device that loads the library (see mgb_device_status).
 __device__ int g_error_word = 0;
 
+void* current_cuda_context() {
+  typedef int (*GetCurrent)(void**);  // cuCtxGetCurrent(CUcontext*)
+  static GetCurrent fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<GetCurrent>(f);
+  });
+  void* ctx = nullptr;
+  if (fn == nullptr || fn(&ctx) != 0) return nullptr;
+  return ctx;
+}
+
 int* device_error_word() {
+  // looked up once per device and context (a reset device gets a new one)
   static int* addr[64] = {};
+  static void* ctx_of[64] = {};
   static std::mutex mu;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  void* ctx = current_cuda_context();
   std::lock_guard<std::mutex> lock(mu);
-  if (addr[dev] == nullptr) {
+  if (addr[dev] == nullptr || ctx == nullptr || ctx_of[dev] != ctx) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_error_word) != cudaSuccess) return nullptr;
     addr[dev] = static_cast<int*>(p);
+    ctx_of[dev] = current_cuda_context();  // the lookup made the context current
   }
   return addr[dev];
 }
@@ -51,6 +73,21 @@ mgb_status attention_bwd_launch(const AttnArgs& a, cudaStream_t st) {
   if (a.B == 0 || a.S == 0) return MGB_OK;
   LaunchScope scope(PROF_ATTN_BWD, st, 3);
   return a.dtype == MGB_BF16 ? attention_bf16_bwd(a, st) : attention_f32_bwd(a, st);
+}
+
+bool fault_injected() {
+  const char* f = getenv("MGB_FAULT");
+  return f != nullptr && strcmp(f, "validate") == 0;
+}
+
+mgb_status check_arch() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return MGB_ERR_CUDA;
+  int major = 0, minor = 0;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+    return MGB_ERR_CUDA;
+  return (major == 10 && minor == 3) ? MGB_OK : MGB_ERR_ARCH;
 }
 
 namespace {
@@ -77,21 +114,6 @@ __global__ void selftest_wait_kernel(unsigned long long limit_ns, int* err) {
 inline size_t al256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
 inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 inline cudaStream_t as_stream(void* s) { return reinterpret_cast<cudaStream_t>(s); }
-
-bool fault_injected() {
-  const char* f = getenv("MGB_FAULT");
-  return f != nullptr && strcmp(f, "validate") == 0;
-}
-
-mgb_status check_arch() {
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return MGB_ERR_CUDA;
-  int major = 0, minor = 0;
-  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
-      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
-    return MGB_ERR_CUDA;
-  return (major == 10 && minor == 3) ? MGB_OK : MGB_ERR_ARCH;
-}
 
 struct Plan {
   int B, S, T, H, nq, nkv, d, F, W, Wqkv, Dq;
@@ -352,6 +374,7 @@ mgb_status mgb_block_fwd(const mgb_block_desc* desc, const mgb_block_weights* w,
   void* a = at<char>(saved, p.s_a);
 
   // attention sublayer input
+  std::unique_ptr<LaunchScope> stage(new LaunchScope(PROF_STAGE_ATTN, st, 1, false));
   const void* a_in = x;
   if (p.pre) {
     void* xn = at<char>(saved, p.s_xn);
@@ -380,12 +403,14 @@ mgb_status mgb_block_fwd(const mgb_block_desc* desc, const mgb_block_weights* w,
   set_hidden_dropout(desc, desc->rng_proj, &g);
   MGB_TRY(gemm_launch(g, st));
   const void* f_in;
+  if (!p.pre)
+    MGB_TRY(layernorm_fwd_launch(T, H, dt, desc->ln_eps, r1, w->ln1_g, w->ln1_b, h, mu1, rs1, st));
+  stage.reset(new LaunchScope(PROF_STAGE_FFN, st, 1, false));
   if (p.pre) {
     void* hn = at<char>(saved, p.s_hn);
     MGB_TRY(layernorm_fwd_launch(T, H, dt, desc->ln_eps, h, w->ln2_g, w->ln2_b, hn, mu2, rs2, st));
     f_in = hn;
   } else {
-    MGB_TRY(layernorm_fwd_launch(T, H, dt, desc->ln_eps, r1, w->ln1_g, w->ln1_b, h, mu1, rs1, st));
     f_in = h;
   }
   // fc1 + activation
@@ -427,6 +452,8 @@ mgb_status mgb_block_bwd(const mgb_block_desc* desc, const mgb_block_weights* w,
   if (ws_bytes < p.bwd) return MGB_ERR_WORKSPACE_TOO_SMALL;
   MGB_TRY(check_arch());
   cudaStream_t st = as_stream(stream);
+  // ends (destroyed last) after the side streams are joined back
+  LaunchScope stage(PROF_STAGE_BWD, st, 1, false);
   const int dt = desc->dtype;
   const int T = p.T, H = p.H;
   const float* mu1 = at<float>(saved, p.s_mu1); const float* rs1 = at<float>(saved, p.s_rs1);
@@ -568,25 +595,59 @@ static mgb_status validate_ce(const mgb_ce_desc* d) {
   if (d->dtype != MGB_BF16) return MGB_ERR_UNSUPPORTED;
   if (d->hidden % 8 || d->vocab % 8 || d->chunk % 8) return MGB_ERR_MISALIGNED;
   if (!(d->grad_scale == d->grad_scale)) return MGB_ERR_INVALID_ARG;
-  if (d->mode != MGB_CE_STREAM && d->mode != MGB_CE_FUSED && d->mode != MGB_CE_RESIDENT)
+  if (d->mode != MGB_CE_STREAM && d->mode != MGB_CE_FUSED && d->mode != MGB_CE_RESIDENT &&
+      d->mode != MGB_CE_BLOCKED)
     return MGB_ERR_INVALID_ARG;
+  if (d->token_block < 0) return MGB_ERR_INVALID_ARG;
   return MGB_OK;
 }
 
 struct CEPlan {
   int n_chunks, C, n_parts, n_t;
   size_t logits, m, s, t, lse, dh, bl, split, total;
+  // MGB_CE_BLOCKED: rows per token block, blocks, K ranges of the d_hidden
+  // product and their partial planes, the float32 d_emb accumulator
+  int tb, n_blocks, dh_splits;
+  size_t dh_part, de_acc;
 };
+
+constexpr int kCeDefaultTokenBlock = 2048;
+
+// K ranges (whole 64-wide blocks) of the split-K GEMM for a request of
+// `want` ranges, as the kernel cuts them.
+static int splitk_ranges(int K, int want) {
+  const int num_k = (K + 63) / 64;
+  if (want <= 1 || num_k <= 1) return 1;
+  const int per = (num_k + want - 1) / want;
+  return (num_k + per - 1) / per;
+}
 
 // Partials: one per chunk (streaming) or one per chunk and 128-column group
 // (fused, written by the GEMM epilogue); target logits per chunk (streaming,
 // zero outside the chunk) or one array each token's owning tile writes (fused).
 static void ce_plan(const mgb_ce_desc* d, CEPlan* p) {
-  const size_t T = d->tokens;
+  size_t T = d->tokens;
   p->C = d->chunk < d->vocab ? d->chunk : d->vocab;
   p->n_chunks = (d->vocab + p->C - 1) / p->C;
   const bool resident = d->mode == MGB_CE_RESIDENT;
-  const bool fused = d->mode == MGB_CE_FUSED || resident;
+  const bool blocked = d->mode == MGB_CE_BLOCKED;
+  const bool fused = d->mode == MGB_CE_FUSED || resident || blocked;
+  p->tb = 0;
+  p->n_blocks = 0;
+  p->dh_splits = 1;
+  p->dh_part = p->de_acc = 0;
+  const size_t T_all = T;
+  if (blocked) {
+    // rows per block: a multiple of 256 (the combine's block sums then fall
+    // on the same 256-token groups as a single combine over all tokens)
+    int tb = d->token_block > 0 ? d->token_block : kCeDefaultTokenBlock;
+    tb = (tb + 255) / 256 * 256;
+    const int t_all = (d->tokens + 255) / 256 * 256;
+    p->tb = tb < t_all ? tb : (t_all > 0 ? t_all : 256);
+    p->n_blocks = (d->tokens + p->tb - 1) / p->tb;
+    p->dh_splits = splitk_ranges(d->vocab, gemm_splitk_count(p->tb, d->hidden, d->vocab, 16));
+    T = p->tb;  // the per-block planes below are sized for one block
+  }
   p->n_parts = 0;
   for (int c = 0; c < p->n_chunks; ++c) {
     const int v0 = c * p->C, Cc = (d->vocab - v0) < p->C ? (d->vocab - v0) : p->C;
@@ -595,15 +656,95 @@ static void ce_plan(const mgb_ce_desc* d, CEPlan* p) {
   p->n_t = fused ? 1 : p->n_chunks;
   size_t o = 0;
   auto take = [&](size_t bytes) { const size_t a = o; o += al256(bytes); return a; };
-  p->logits = take(2 * T * (resident ? (size_t)d->vocab : (size_t)p->C));
+  p->logits = take(2 * T * ((resident || blocked) ? (size_t)d->vocab : (size_t)p->C));
   p->m = take(4 * T * p->n_parts);
   p->s = take(4 * T * p->n_parts);
   p->t = take(4 * T * p->n_t);
-  p->lse = take(4 * T);
-  p->dh = resident ? 0 : take(4 * T * d->hidden);
-  p->bl = take(4 * (size_t)ce_combine_blocks((int)T));
+  p->lse = take(4 * T_all);
+  p->dh = (resident || blocked) ? 0 : take(4 * T * d->hidden);
+  p->bl = take(4 * (size_t)ce_combine_blocks((int)T_all));
   p->split = p->n_parts > kCeSplits ? take(4 * 2 * (size_t)kCeSplits * T) : 0;
+  if (blocked) {
+    p->dh_part = take(4 * (size_t)p->dh_splits * T * d->hidden);
+    p->de_acc = p->n_blocks > 1 ? take(4 * (size_t)d->vocab * d->hidden) : 0;
+  }
   p->total = o;
+}
+
+// MGB_CE_BLOCKED: per block of tokens, the logits of every vocab chunk with
+// their partials, the block's LSE and losses, G in place, then d_hidden rows
+// (split-K) beside d_emb += G^T hidden on the side stream.
+static mgb_status ce_blocked(const mgb_ce_desc* desc, const CEPlan& p, const void* hidden,
+                             const bf16* E, const int32_t* targets, float* loss_per_token,
+                             float* loss_mean, float* lse_buf, void* d_hidden, void* d_emb,
+                             void* ws, cudaStream_t st) {
+  const int T = desc->tokens, H = desc->hidden, V = desc->vocab, C = p.C;
+  bf16* logits = at<bf16>(ws, p.logits);
+  float* m = at<float>(ws, p.m);
+  float* s = at<float>(ws, p.s);
+  float* t = at<float>(ws, p.t);
+  float* bl = at<float>(ws, p.bl);
+  float* split = p.n_parts > kCeSplits ? at<float>(ws, p.split) : nullptr;
+  float* dh_part = at<float>(ws, p.dh_part);
+  float* de_acc = at<float>(ws, p.de_acc);
+  const bf16* hid = static_cast<const bf16*>(hidden);
+  const bool grads = d_hidden || d_emb;
+  for (int b = 0; b < p.n_blocks; ++b) {
+    const int r0 = b * p.tb;
+    const int rows = (T - r0) < p.tb ? (T - r0) : p.tb;
+    const bool last = b == p.n_blocks - 1;
+    // ---- forward of the block: partials per chunk and 128-column group
+    if (cudaMemsetAsync(t, 0, sizeof(float) * rows, st) != cudaSuccess) return MGB_ERR_CUDA;
+    {
+      // every vocab chunk in one launch (tiles never straddle two chunks):
+      // chunk c's partials are planes c * ceil(C / 128) .. of m and s
+      GemmArgs g = mk_gemm(MGB_BF16, rows, V, H, 0, hid + (size_t)r0 * H, H, 0, E, H,
+                           EPI_CE_STATS, m, 8);
+      g.C2 = s; g.ldc2 = 8;
+      g.n_chunk = C;
+      g.tgt = targets + r0; g.tgt_v0 = 0; g.tgt_out = t;
+      if (grads) { g.keep = logits; g.ld_keep = V; }
+      g.prof_kind = PROF_GEMM_CE_LOGITS;
+      MGB_TRY(gemm_launch(g, st));
+    }
+    MGB_TRY(ce_combine_launch(rows, p.n_parts, m, s, 1, t, lse_buf + r0, loss_per_token + r0,
+                              nullptr, bl + r0 / 256, split, st));
+    if (!grads) continue;
+    // ---- backward of the block: G in place, then its two products
+    MGB_TRY(ce_grad_launch(rows, V, 0, logits, V, targets + r0, lse_buf + r0, desc->grad_scale,
+                           st));
+    SideLane lane(st, last ? as_stream(desc->emb_stream) : nullptr);
+    if (d_emb) {
+      MGB_TRY(lane.fork());
+      GemmArgs g;
+      if (p.n_blocks == 1) {
+        g = mk_gemm(MGB_BF16, V, H, rows, 1, logits, V, 1, hid + (size_t)r0 * H, H, EPI_STORE,
+                    d_emb, H);
+      } else {
+        // float32 accumulator across blocks: the first block stores its
+        // product, the others reduce-add theirs in L2 (TMA bulk copies)
+        g = mk_gemm(MGB_BF16, V, H, rows, 1, logits, V, 1, hid + (size_t)r0 * H, H, EPI_F32,
+                    de_acc, H);
+        g.accumulate = b > 0;
+        g.f32_tma = 1;
+      }
+      g.prof_kind = PROF_GEMM_CE_WGRAD;
+      MGB_TRY(gemm_launch(g, lane.side()));
+      if (last && p.n_blocks > 1)  // d_emb = bf16(accumulator)
+        MGB_TRY(splitk_reduce_launch(V, H, 1, de_acc, 0, H, d_emb, H, lane.side()));
+    }
+    if (d_hidden) {
+      GemmArgs g = mk_gemm(MGB_BF16, rows, H, V, 0, logits, V, 1, E, H, EPI_F32, dh_part, H);
+      g.k_splits = p.dh_splits;
+      g.split_stride = (int64_t)rows * H;
+      g.prof_kind = PROF_GEMM_CE_DGRAD;
+      MGB_TRY(gemm_launch(g, st));
+      MGB_TRY(splitk_reduce_launch(rows, H, p.dh_splits, dh_part, (int64_t)rows * H, H,
+                                   static_cast<bf16*>(d_hidden) + (size_t)r0 * H, H, st));
+    }
+    MGB_TRY(lane.join());  // the next block overwrites the logits
+  }
+  return ce_mean_launch(ce_combine_blocks(T), T, bl, loss_mean, st);
 }
 
 mgb_status mgb_vocab_ce_sizes(const mgb_ce_desc* desc, size_t* ws_bytes) {
@@ -638,6 +779,9 @@ mgb_status mgb_vocab_ce_fwd_bwd(const mgb_ce_desc* desc, const void* hidden, con
   float* dh_acc = at<float>(ws, p.dh);
   float* bl = at<float>(ws, p.bl);
   const bf16* E = static_cast<const bf16*>(emb);
+  if (desc->mode == MGB_CE_BLOCKED)
+    return ce_blocked(desc, p, hidden, E, targets, loss_per_token, loss_mean, lse_buf, d_hidden,
+                      d_emb, ws, st);
   const bool resident = desc->mode == MGB_CE_RESIDENT;
   const bool fused = desc->mode == MGB_CE_FUSED || resident;
   // ---- forward: per-chunk partials, then the combine
@@ -677,12 +821,15 @@ mgb_status mgb_vocab_ce_fwd_bwd(const mgb_ce_desc* desc, const void* hidden, con
     SideLane lane(st, as_stream(desc->emb_stream));
     if (d_emb) {
       MGB_TRY(lane.fork());
-      MGB_TRY(gemm_launch(mk_gemm(MGB_BF16, V, H, T, 1, logits, V, 1, hidden, H, EPI_STORE,
-                                  d_emb, H), lane.side()));
+      GemmArgs g = mk_gemm(MGB_BF16, V, H, T, 1, logits, V, 1, hidden, H, EPI_STORE, d_emb, H);
+      g.prof_kind = PROF_GEMM_CE_WGRAD;
+      MGB_TRY(gemm_launch(g, lane.side()));
     }
-    if (d_hidden)
-      MGB_TRY(gemm_launch(mk_gemm(MGB_BF16, T, H, V, 0, logits, V, 1, E, H, EPI_STORE, d_hidden, H),
-                          st));
+    if (d_hidden) {
+      GemmArgs g = mk_gemm(MGB_BF16, T, H, V, 0, logits, V, 1, E, H, EPI_STORE, d_hidden, H);
+      g.prof_kind = PROF_GEMM_CE_DGRAD;
+      MGB_TRY(gemm_launch(g, st));
+    }
     return lane.join();
   }
   // ---- backward: per chunk, G then its two GEMMs
@@ -706,11 +853,15 @@ mgb_status mgb_vocab_ce_fwd_bwd(const mgb_ce_desc* desc, const void* hidden, con
                            dh_acc, H);
       g.accumulate = c > 0;
       if (c == p.n_chunks - 1) { g.C2 = d_hidden; g.ldc2 = H; }
+      g.prof_kind = PROF_GEMM_CE_DGRAD;
       MGB_TRY(gemm_launch(g, st));
     }
-    if (d_emb)
-      MGB_TRY(gemm_launch(mk_gemm(MGB_BF16, Cc, H, T, 1, logits, C, 1, hidden, H, EPI_STORE,
-                                  static_cast<bf16*>(d_emb) + (size_t)v0 * H, H), st));
+    if (d_emb) {
+      GemmArgs g = mk_gemm(MGB_BF16, Cc, H, T, 1, logits, C, 1, hidden, H, EPI_STORE,
+                           static_cast<bf16*>(d_emb) + (size_t)v0 * H, H);
+      g.prof_kind = PROF_GEMM_CE_WGRAD;
+      MGB_TRY(gemm_launch(g, st));
+    }
   }
   return MGB_OK;
 }

@@ -242,6 +242,13 @@ mgb_status ce_combine_launch(int T, int n_parts, const float* m, const float* s,
   return cudaGetLastError() == cudaSuccess ? MGB_OK : MGB_ERR_CUDA;
 }
 
+mgb_status ce_mean_launch(int nb, int T, const float* block_loss, float* loss_mean,
+                          cudaStream_t st) {
+  LaunchScope scope(PROF_CE_COMBINE, st);
+  ce_mean_kernel<<<1, 32, 0, st>>>(nb, T, block_loss, loss_mean);
+  return cudaGetLastError() == cudaSuccess ? MGB_OK : MGB_ERR_CUDA;
+}
+
 mgb_status ce_grad_launch(int T, int C, int v0, void* logits, int64_t ldl, const int32_t* targets,
                           const float* lse, float scale, cudaStream_t st) {
   if (T == 0) return MGB_OK;

@@ -140,7 +140,8 @@ __global__ void swiglu_f32_kernel(int M, int F, int gb, const float* u, int64_t 
 }  // namespace
 
 mgb_status gemm_check(const GemmArgs& g) {
-  if (g.M < 0 || g.N < 0 || g.K < 0) return MGB_ERR_INVALID_ARG;
+  if (g.M < 0 || g.N < 0 || g.K < 0 || g.k_splits < 1) return MGB_ERR_INVALID_ARG;
+  if (g.k_splits > 1 && g.dtype != MGB_BF16) return MGB_ERR_UNSUPPORTED;
   if (g.dtype != MGB_BF16 && g.dtype != MGB_F32) return MGB_ERR_INVALID_ARG;
   if (g.epi < EPI_STORE || g.epi > EPI_CE_GRAD) return MGB_ERR_INVALID_ARG;
   if (g.epi == EPI_CE_STATS || g.epi == EPI_CE_GRAD) {
@@ -181,6 +182,15 @@ mgb_status gemm_check(const GemmArgs& g) {
     if (g.ldc % c_mult || (g.C2 && g.ldc2 % 8) || (g.resid && g.ldr % 8) || (g.aux && g.ldaux % 8))
       return MGB_ERR_MISALIGNED;
     if (g.accumulate && g.epi != EPI_F32) return MGB_ERR_INVALID_ARG;
+    if (g.f32_tma && (g.epi != EPI_F32 || g.C2 != nullptr || g.k_splits > 1 || g.ldc % 4))
+      return MGB_ERR_INVALID_ARG;
+    if (g.n_chunk != 0 && (g.n_chunk < 0 || g.n_chunk % 8 || g.tgt_v0 != 0 ||
+                           (g.epi != EPI_CE_STATS && g.epi != EPI_CE_GRAD)))
+      return MGB_ERR_INVALID_ARG;
+    if (g.k_splits > 1 && (g.epi != EPI_F32 || g.accumulate || g.C2 != nullptr ||
+                           g.bias != nullptr || g.split_stride % 4 ||
+                           g.split_stride < (int64_t)g.M * g.ldc))
+      return MGB_ERR_INVALID_ARG;
     if (g.keep != nullptr && (g.epi != EPI_CE_STATS || !al(g.keep) || g.ld_keep % 8 ||
                               g.ld_keep < g.N))
       return MGB_ERR_INVALID_ARG;

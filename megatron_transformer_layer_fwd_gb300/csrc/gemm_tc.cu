@@ -34,6 +34,7 @@
 // error and the CTA drains and frees its TMEM instead of spinning forever.
 #include <cudaTypedefs.h>
 
+#include <climits>
 #include <mutex>
 
 #include "common.cuh"
@@ -74,7 +75,23 @@ struct EpiParams {
   float drop_scale;
   uint64_t drop_seed, drop_offset;
   float* cpart;
+  // split-K (EPI_F32 only): the K blocks are cut into k_splits ranges of
+  // kb_per_split blocks; split s stores its partial product at C + s * split_stride
+  int k_splits, kb_per_split;
+  int64_t split_stride;
+  // EPI_F32 through TMA (0 off): 1 stores, 2 reduce-adds each staged 32 x 32
+  // float32 box into C (tensor map tmC)
+  int c_tma;
+  // column chunks (EPI_CE_STATS / EPI_CE_GRAD; 0 = off): the N columns are cut
+  // into chunks of n_chunk, tpc column tiles each, so no tile straddles two
+  // chunks; a chunk's statistics groups start at its first column (gpc groups
+  // of 128 per chunk)
+  int n_chunk, tpc, gpc;
 };
+
+// Shared memory the TMA float32 epilogue stages through: two 4 KB boxes per
+// epilogue warp, 1024-byte aligned after the barrier area.
+constexpr int kEpiStageBytes = 4 * 2 * 4096;
 
 template <int BN, int STAGES>
 struct Cfg {
@@ -82,7 +99,8 @@ struct Cfg {
   static constexpr int B_BYTES = BN * BK * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int TILE_BYTES = STAGE_BYTES * STAGES;
-  static constexpr int SMEM_BYTES = TILE_BYTES + 1024 + 256;
+  // operand stages, 1 KB of barriers, the epilogue's TMA boxes, alignment slack
+  static constexpr int SMEM_BYTES = TILE_BYTES + 1024 + kEpiStageBytes + 1024;
 };
 
 __device__ __forceinline__ void load8(const bf16* p, float (&f)[8]) {
@@ -152,7 +170,8 @@ __device__ __forceinline__ void colsum32_store(float* part, int64_t ld, int row,
 // Epilogue for one thread = one output row `row` of the tile.
 template <int BN>
 __device__ void epilogue_row(const EpiParams& p, uint32_t tmem_row, int row, int n0,
-                             bool have_acc) {
+                             bool have_acc, int64_t c_off = 0, int cbase = 0, int nend = INT_MAX,
+                             int pbase = 0) {
   const bool row_ok = row < p.M;
   if (p.epi == EPI_BIAS_SWIGLU) {
     const int gb = p.glu_block;
@@ -183,6 +202,9 @@ __device__ void epilogue_row(const EpiParams& p, uint32_t tmem_row, int row, int
   if (p.epi == EPI_CE_STATS) {
     // per 128-column group: running (max, sum exp) of the float32 logits in
     // the log2 domain (the sum rescaled when the max grows); no logits stored
+    // (with column chunks: this tile's chunk ends at nend, its groups are
+    // numbered from pbase at column cbase)
+    const int NE = min(p.N, nend);
     int tcol = -1;
     if (p.tgt != nullptr && row_ok) tcol = p.tgt[row] - p.tgt_v0 - n0;
     float* pm = reinterpret_cast<float*>(p.C);
@@ -193,9 +215,9 @@ __device__ void epilogue_row(const EpiParams& p, uint32_t tmem_row, int row, int
         float acc[32];
         tmem_chunk(tmem_row + lc, p.alpha, have_acc, acc);
         const int n = n0 + lc;
-        if (!row_ok || n >= p.N) continue;
+        if (!row_ok || n >= NE) continue;
         const int tc = tcol - lc;
-        if (tc >= 0 && tc < 32 && n + tc < p.N) {
+        if (tc >= 0 && tc < 32 && n + tc < NE) {
           float v = 0.0f;
 #pragma unroll
           for (int j = 0; j < 32; ++j) v = (j == tc) ? acc[j] : v;
@@ -205,12 +227,12 @@ __device__ void epilogue_row(const EpiParams& p, uint32_t tmem_row, int row, int
           bf16* kp = p.keep + (int64_t)row * p.ld_keep + n;
 #pragma unroll
           for (int q = 0; q < 4; ++q)
-            if (n + 8 * q < p.N) store8(kp + 8 * q, acc + 8 * q);
+            if (n + 8 * q < NE) store8(kp + 8 * q, acc + 8 * q);
         }
         float cm = -INFINITY;
 #pragma unroll
         for (int j = 0; j < 32; ++j) {
-          acc[j] = n + j < p.N ? acc[j] * 1.4426950408889634f : -INFINITY;
+          acc[j] = n + j < NE ? acc[j] * 1.4426950408889634f : -INFINITY;
           cm = fmaxf(cm, acc[j]);
         }
         if (cm > mx) {
@@ -221,8 +243,8 @@ __device__ void epilogue_row(const EpiParams& p, uint32_t tmem_row, int row, int
         for (int j = 0; j < 32; ++j) sum += ex2_ftz(acc[j] - mx);
       }
       const int n = n0 + h;
-      if (row_ok && n < p.N) {
-        const int64_t o = (int64_t)(n / 128) * p.M + row;
+      if (row_ok && n < NE) {
+        const int64_t o = (int64_t)(pbase + (n - cbase) / 128) * p.M + row;
         pm[o] = mx * 0.6931471805599453f;
         ps[o] = sum;
       }
@@ -231,6 +253,7 @@ __device__ void epilogue_row(const EpiParams& p, uint32_t tmem_row, int row, int
   }
   if (p.epi == EPI_CE_GRAD) {
     // G = (softmax - onehot(target)) * scale from the float32 logits
+    const int NE = min(p.N, nend);
     int tcol = -1;
     float l2 = 0.0f;
     if (row_ok) {
@@ -241,7 +264,7 @@ __device__ void epilogue_row(const EpiParams& p, uint32_t tmem_row, int row, int
       float acc[32];
       tmem_chunk(tmem_row + lc, p.alpha, have_acc, acc);
       const int n = n0 + lc;
-      if (!row_ok || n >= p.N) continue;
+      if (!row_ok || n >= NE) continue;
       const int tc = tcol - lc;
 #pragma unroll
       for (int j = 0; j < 32; ++j) {
@@ -252,7 +275,7 @@ __device__ void epilogue_row(const EpiParams& p, uint32_t tmem_row, int row, int
       bf16* c = reinterpret_cast<bf16*>(p.C) + (int64_t)row * p.ldc + n;
 #pragma unroll
       for (int q = 0; q < 4; ++q)
-        if (n + 8 * q < p.N) store8(c + 8 * q, acc + 8 * q);
+        if (n + 8 * q < NE) store8(c + 8 * q, acc + 8 * q);
     }
     return;
   }
@@ -389,7 +412,7 @@ __device__ void epilogue_row(const EpiParams& p, uint32_t tmem_row, int row, int
       }
       case EPI_F32: {
         add_bias32(p.bias, n, p.N, acc);
-        float* c = reinterpret_cast<float*>(p.C) + (int64_t)row * p.ldc + n;
+        float* c = reinterpret_cast<float*>(p.C) + c_off + (int64_t)row * p.ldc + n;
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
           if (n + 4 * q < p.N) {
@@ -416,6 +439,44 @@ __device__ void epilogue_row(const EpiParams& p, uint32_t tmem_row, int row, int
   }
 }
 
+// EPI_F32 through TMA for one warp (rows row0 .. row0 + 31, one per lane):
+// each 32-column chunk of the float32 accumulator is written to a shared
+// memory box in the 128-byte swizzled layout the tensor map describes (16-byte
+// chunk j of row r at r * 128 + ((j ^ (r % 8)) * 16): conflict-free vector
+// stores) and one lane stores or reduce-adds the box to C with a bulk tensor
+// copy; rows and columns past C's edges are clipped by the copy. Two boxes
+// per warp alternate; `cnt` counts the warp's boxes so far.
+template <int BN>
+__device__ void epilogue_f32_tma(const EpiParams& p, const CUtensorMap* tmC, uint32_t tmem_row,
+                                 int row0, int n0, bool have_acc, uint32_t stage, uint32_t& cnt) {
+  const int lane = threadIdx.x & 31;
+  for (int lc = 0; lc < BN; lc += 32) {
+    float acc[32];
+    tmem_chunk(tmem_row + lc, p.alpha, have_acc, acc);
+    const int n = n0 + lc;
+    if (row0 >= p.M || n >= p.N) continue;  // the same for the whole warp
+    add_bias32(p.bias, n, p.N, acc);
+    const uint32_t box = stage + (cnt & 1) * 4096;
+    if (lane == 0) bulk_wait_read<1>();  // the copy that last read this box is done
+    __syncwarp();
+    const uint32_t rb = box + lane * 128;
+#pragma unroll
+    for (int j = 0; j < 8; ++j)
+      st_shared_v4(rb + ((j ^ (lane & 7)) << 4), acc[4 * j], acc[4 * j + 1], acc[4 * j + 2],
+                   acc[4 * j + 3]);
+    fence_proxy_async();
+    __syncwarp();
+    if (lane == 0) {
+      if (p.c_tma == 2)
+        tma_reduce_add_2d(tmC, box, n, row0);
+      else
+        tma_store_2d(tmC, box, n, row0);
+      bulk_commit();
+    }
+    ++cnt;
+  }
+}
+
 // Tile `tile` of the grouped raster: group_m row tiles per group, the row
 // tile advancing fastest inside a group.
 __device__ __forceinline__ void tile_origin(const EpiParams& p, int tile, int bn, int& m0,
@@ -427,6 +488,40 @@ __device__ __forceinline__ void tile_origin(const EpiParams& p, int tile, int bn
   const int in_group = tile - group * per_group;
   m0 = (first_m + in_group % gm) * bm;
   n0 = (in_group / gm) * bn;
+}
+
+// Tile `tile` of the split-K grid: splits outermost (a wave of CTAs works on
+// one K range, so its A and B slices are shared in L2), then the grouped
+// raster of output tiles. [kb0, kb1) are the tile's K blocks.
+__device__ __forceinline__ void tile_decode(const EpiParams& p, int tile, int bn, int num_k,
+                                            int& m0, int& n0, int& kb0, int& kb1, int& split,
+                                            int bm = BM) {
+  const int per_split = p.tiles_m * p.tiles_n;
+  split = tile / per_split;
+  tile_origin(p, tile - split * per_split, bn, m0, n0, bm);
+  if (p.n_chunk > 0) {
+    // column tile n0 / bn = tile j of chunk c
+    const int jn = n0 / bn, c = jn / p.tpc;
+    n0 = c * p.n_chunk + (jn - c * p.tpc) * bn;
+  }
+  kb0 = split * p.kb_per_split;
+  kb1 = min(num_k, kb0 + p.kb_per_split);
+}
+
+// Column chunk of a tile at n0 (column chunks on): first column, end, first
+// statistics group.
+__device__ __forceinline__ void chunk_of(const EpiParams& p, int n0, int& cbase, int& nend,
+                                         int& pbase) {
+  if (p.n_chunk > 0) {
+    const int c = n0 / p.n_chunk;
+    cbase = c * p.n_chunk;
+    nend = cbase + p.n_chunk;
+    pbase = c * p.gpc;
+  } else {
+    cbase = 0;
+    nend = INT_MAX;
+    pbase = 0;
+  }
 }
 
 // Persistent and warp-specialised: one CTA per SM walks the tiles
@@ -441,7 +536,8 @@ __device__ __forceinline__ void tile_origin(const EpiParams& p, int tile, int bn
 template <int BN, int STAGES, int A_MN, int B_MN>
 __global__ void __launch_bounds__(192, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
-                   const __grid_constant__ CUtensorMap tmB, const EpiParams p) {
+                   const __grid_constant__ CUtensorMap tmB,
+                   const __grid_constant__ CUtensorMap tmC, const EpiParams p) {
   using C = Cfg<BN, STAGES>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -457,7 +553,7 @@ __global__ void __launch_bounds__(192, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int num_k = (p.K + BK - 1) / BK;
-  const int total = p.tiles_m * p.tiles_n;
+  const int total = p.tiles_m * p.tiles_n * p.k_splits;
 
   if (threadIdx.x == 0) {
     tma_prefetch_desc(&tmA);
@@ -484,9 +580,9 @@ __global__ void __launch_bounds__(192, 1)
       // ---------------- TMA producer
       uint32_t kg = 0;  // k-blocks issued by this CTA so far (ring position)
       for (int tile = blockIdx.x; tile < total && !*abort; tile += gridDim.x) {
-        int m0, n0;
-        tile_origin(p, tile, BN, m0, n0);
-        for (int kb = 0; kb < num_k; ++kb, ++kg) {
+        int m0, n0, kb0, kb1, sp;
+        tile_decode(p, tile, BN, num_k, m0, n0, kb0, kb1, sp);
+        for (int kb = kb0; kb < kb1; ++kb, ++kg) {
           const int s = kg % STAGES;
           if (!mbar_wait(empty0 + 8 * s, ((kg / STAGES) & 1) ^ 1, p.err)) {
             *abort = 1;
@@ -527,7 +623,9 @@ __global__ void __launch_bounds__(192, 1)
         tc_fence_after();
         const uint32_t acc = tmem + buf * BN;
         bool good = true;
-        for (int kb = 0; kb < num_k; ++kb, ++kg) {
+        int m0, n0, kb0, kb1, sp;
+        tile_decode(p, tile, BN, num_k, m0, n0, kb0, kb1, sp);
+        for (int kb = kb0; kb < kb1; ++kb, ++kg) {
           const int s = kg % STAGES;
           if (!mbar_wait(full0 + 8 * s, (kg / STAGES) & 1, p.err)) {
             good = false;
@@ -542,7 +640,7 @@ __global__ void __launch_bounds__(192, 1)
                                      : smem_desc_sw128(sa + 32 * kk, 16, 1024);
             const uint64_t bd = B_MN ? smem_desc_sw128(sb + 2048 * kk, 8192, 1024)
                                      : smem_desc_sw128(sb + 32 * kk, 16, 1024);
-            tc_mma_f16(acc, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+            tc_mma_f16(acc, ad, bd, idesc, (kb != kb0 || kk != 0) ? 1u : 0u);
           }
           tc_commit(empty0 + 8 * s);
         }
@@ -556,6 +654,8 @@ __global__ void __launch_bounds__(192, 1)
   } else {
     // ---------------- epilogue warps 2..5
     const int q = warp & 3;  // TMEM lane quarter of this warp
+    const uint32_t stage = tiles + C::TILE_BYTES + 1024 + q * 8192;
+    uint32_t cnt = 0;
     int t = 0;
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++t) {
       const int buf = t & 1;
@@ -565,14 +665,22 @@ __global__ void __launch_bounds__(192, 1)
         break;
       }
       tc_fence_after();
-      int m0, n0;
-      tile_origin(p, tile, BN, m0, n0);
-      epilogue_row<BN>(p, tmem + buf * BN + ((uint32_t)(q * 32) << 16), m0 + q * 32 + lane, n0,
-                       num_k > 0);
+      int m0, n0, kb0, kb1, sp;
+      tile_decode(p, tile, BN, num_k, m0, n0, kb0, kb1, sp);
+      const uint32_t trow = tmem + buf * BN + ((uint32_t)(q * 32) << 16);
+      if (p.c_tma) {
+        epilogue_f32_tma<BN>(p, &tmC, trow, m0 + q * 32, n0, kb1 > kb0, stage, cnt);
+      } else {
+        int cb, ne, pb;
+        chunk_of(p, n0, cb, ne, pb);
+        epilogue_row<BN>(p, trow, m0 + q * 32 + lane, n0, kb1 > kb0, sp * p.split_stride, cb, ne,
+                         pb);
+      }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(acce0 + 8 * buf);
     }
+    if (p.c_tma && lane == 0) bulk_wait<0>();  // this warp's copies complete before exit
   }
 
   __syncthreads();
@@ -606,7 +714,8 @@ __global__ void __launch_bounds__(192, 1)
 template <int STAGES, int A_MN, int B_MN>
 __global__ void __launch_bounds__(192, 1)
     gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmA,
-                        const __grid_constant__ CUtensorMap tmB, const EpiParams p) {
+                        const __grid_constant__ CUtensorMap tmB,
+                        const __grid_constant__ CUtensorMap tmC, const EpiParams p) {
   constexpr int BNP = 256, HALF = 128;
   constexpr int A_BYTES = HALF * BK * 2, B_BYTES = HALF * BK * 2;
   constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
@@ -626,7 +735,7 @@ __global__ void __launch_bounds__(192, 1)
   const uint32_t rank = cluster_ctarank();
   const int pair = blockIdx.x >> 1, npairs = gridDim.x >> 1;
   const int num_k = (p.K + BK - 1) / BK;
-  const int total = p.tiles_m * p.tiles_n;
+  const int total = p.tiles_m * p.tiles_n * p.k_splits;
 
   if (threadIdx.x == 0) {
     tma_prefetch_desc(&tmA);
@@ -654,10 +763,10 @@ __global__ void __launch_bounds__(192, 1)
       // ---------------- TMA producer (both CTAs)
       uint32_t kg = 0;
       for (int tile = pair; tile < total && !*abort; tile += npairs) {
-        int m0, n0;
-        tile_origin(p, tile, BNP, m0, n0, 2 * HALF);
+        int m0, n0, kb0, kb1, sp;
+        tile_decode(p, tile, BNP, num_k, m0, n0, kb0, kb1, sp, 2 * HALF);
         const int ma = m0 + HALF * (int)rank, nb = n0 + HALF * (int)rank;
-        for (int kb = 0; kb < num_k; ++kb, ++kg) {
+        for (int kb = kb0; kb < kb1; ++kb, ++kg) {
           const int s = kg % STAGES;
           if (!mbar_wait(empty0 + 8 * s, ((kg / STAGES) & 1) ^ 1, p.err)) {
             *abort = 1;
@@ -704,7 +813,9 @@ __global__ void __launch_bounds__(192, 1)
         tc_fence_after();
         const uint32_t acc = tmem + buf * BNP;
         bool good = true;
-        for (int kb = 0; kb < num_k; ++kb, ++kg) {
+        int m0, n0, kb0, kb1, sp;
+        tile_decode(p, tile, BNP, num_k, m0, n0, kb0, kb1, sp, 2 * HALF);
+        for (int kb = kb0; kb < kb1; ++kb, ++kg) {
           const int s = kg % STAGES;
           if (!mbar_wait(full0 + 8 * s, (kg / STAGES) & 1, p.err)) {
             good = false;
@@ -719,7 +830,7 @@ __global__ void __launch_bounds__(192, 1)
                                      : smem_desc_sw128(sa + 32 * kk, 16, 1024);
             const uint64_t bd = B_MN ? smem_desc_sw128(sb + 2048 * kk, 8192, 1024)
                                      : smem_desc_sw128(sb + 32 * kk, 16, 1024);
-            tc_mma_f16_pair(acc, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+            tc_mma_f16_pair(acc, ad, bd, idesc, (kb != kb0 || kk != 0) ? 1u : 0u);
           }
           tc_commit_pair_mc(empty0 + 8 * s, 3);
         }
@@ -733,6 +844,8 @@ __global__ void __launch_bounds__(192, 1)
   } else {
     // ---------------- epilogue warps 2..5 (both CTAs: this CTA's 128 rows)
     const int q = warp & 3;
+    const uint32_t stage = tiles + STAGES * STAGE_BYTES + 1024 + q * 8192;
+    uint32_t cnt = 0;
     int t = 0;
     for (int tile = pair; tile < total; tile += npairs, ++t) {
       const int buf = t & 1;
@@ -742,14 +855,22 @@ __global__ void __launch_bounds__(192, 1)
         break;
       }
       tc_fence_after();
-      int m0, n0;
-      tile_origin(p, tile, BNP, m0, n0, 2 * HALF);
-      epilogue_row<BNP>(p, tmem + buf * BNP + ((uint32_t)(q * 32) << 16),
-                        m0 + HALF * (int)rank + q * 32 + lane, n0, num_k > 0);
+      int m0, n0, kb0, kb1, sp;
+      tile_decode(p, tile, BNP, num_k, m0, n0, kb0, kb1, sp, 2 * HALF);
+      const uint32_t trow = tmem + buf * BNP + ((uint32_t)(q * 32) << 16);
+      const int r0 = m0 + HALF * (int)rank + q * 32;
+      if (p.c_tma) {
+        epilogue_f32_tma<BNP>(p, &tmC, trow, r0, n0, kb1 > kb0, stage, cnt);
+      } else {
+        int cb, ne, pb;
+        chunk_of(p, n0, cb, ne, pb);
+        epilogue_row<BNP>(p, trow, r0 + lane, n0, kb1 > kb0, sp * p.split_stride, cb, ne, pb);
+      }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(mapa_shared(acce0 + 8 * buf, 0));
     }
+    if (p.c_tma && lane == 0) bulk_wait<0>();  // this warp's copies complete before exit
   }
 
   __syncthreads();
@@ -798,10 +919,25 @@ bool make_tmap(CUtensorMap* tm, const void* base, uint64_t inner, uint64_t outer
   return r == CUDA_SUCCESS;
 }
 
+// 2-D float32 tensor map of C for the TMA epilogue: boxes of 32 columns x 32
+// rows, 128-byte swizzle.
+bool make_tmap_f32(CUtensorMap* tm, const void* base, uint64_t inner, uint64_t outer, int64_t ld) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {(cuuint64_t)ld * 4};
+  cuuint32_t box[2] = {32, 32};
+  cuuint32_t es[2] = {1, 1};
+  CUresult r = fn(tm, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(base), dims, strides,
+                  box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 // One persistent CTA per SM (the kernel's shared memory allows one), never
 // more CTAs than tiles.
 int persistent_grid(const EpiParams& ep) {
-  const long total = (long)ep.tiles_m * ep.tiles_n;
+  const long total = (long)ep.tiles_m * ep.tiles_n * ep.k_splits;
   return (int)std::max(1L, std::min<long>(total, device_sm_count()));
 }
 
@@ -812,32 +948,35 @@ mgb_status launch_variant(const GemmArgs& g, const EpiParams& ep, cudaStream_t s
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES) !=
       cudaSuccess)
     return MGB_ERR_CUDA;
-  CUtensorMap ta, tb;
+  CUtensorMap ta, tb, tc;
   if (g.K == 0) {
     // no K blocks: the kernel writes the epilogue of a zero accumulator and
     // never reads the operands; encode harmless maps over the output buffer
     const bool ok0 = make_tmap(&ta, g.C, 64, 64, 64, 64, 64) && make_tmap(&tb, g.C, 64, 64, 64, 64, 64);
     if (!ok0) return MGB_ERR_CUDA;
-    LaunchScope scope(g.prof_kind >= 0 ? g.prof_kind
-                               : (A_MN ? PROF_GEMM_WGRAD : (B_MN ? PROF_GEMM_DGRAD : PROF_GEMM_FWD)),
-                    st);
-    kern<<<persistent_grid(ep), 192, C::SMEM_BYTES, st>>>(ta, tb, ep);
-    return cudaGetLastError() == cudaSuccess ? MGB_OK : MGB_ERR_CUDA;
+  } else {
+    bool ok = A_MN ? make_tmap(&ta, g.A, g.M, g.K, g.lda, 64, 64)
+                   : make_tmap(&ta, g.A, g.K, g.M, g.lda, 64, BM);
+    ok = ok && (B_MN ? make_tmap(&tb, g.B, g.N, g.K, g.ldb, 64, 64)
+                     : make_tmap(&tb, g.B, g.K, g.N, g.ldb, 64, BN));
+    if (!ok) return MGB_ERR_CUDA;
   }
-  bool ok = A_MN ? make_tmap(&ta, g.A, g.M, g.K, g.lda, 64, 64)
-                 : make_tmap(&ta, g.A, g.K, g.M, g.lda, 64, BM);
-  ok = ok && (B_MN ? make_tmap(&tb, g.B, g.N, g.K, g.ldb, 64, 64)
-                   : make_tmap(&tb, g.B, g.K, g.N, g.ldb, 64, BN));
-  if (!ok) return MGB_ERR_CUDA;
+  if (ep.c_tma) {
+    if (!make_tmap_f32(&tc, g.C, g.N, g.M, g.ldc)) return MGB_ERR_CUDA;
+  } else {
+    tc = ta;  // not read
+  }
   LaunchScope scope(g.prof_kind >= 0 ? g.prof_kind
                                : (A_MN ? PROF_GEMM_WGRAD : (B_MN ? PROF_GEMM_DGRAD : PROF_GEMM_FWD)),
                     st);
-  kern<<<persistent_grid(ep), 192, C::SMEM_BYTES, st>>>(ta, tb, ep);
+  kern<<<persistent_grid(ep), 192, C::SMEM_BYTES, st>>>(ta, tb, tc, ep);
   return cudaGetLastError() == cudaSuccess ? MGB_OK : MGB_ERR_CUDA;
 }
 
 constexpr int PAIR_STAGES = 6;
-constexpr int pair_smem_bytes() { return PAIR_STAGES * 2 * (128 * BK * 2) + 1024 + 256; }
+constexpr int pair_smem_bytes() {
+  return PAIR_STAGES * 2 * (128 * BK * 2) + 1024 + kEpiStageBytes + 1024;
+}
 
 template <int A_MN, int B_MN>
 mgb_status launch_pair_variant(const GemmArgs& g, const EpiParams& ep, cudaStream_t st) {
@@ -845,11 +984,15 @@ mgb_status launch_pair_variant(const GemmArgs& g, const EpiParams& ep, cudaStrea
   constexpr int smem = pair_smem_bytes();
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem) != cudaSuccess)
     return MGB_ERR_CUDA;
-  CUtensorMap ta, tb;
+  CUtensorMap ta, tb, tc;
   bool ok = A_MN ? make_tmap(&ta, g.A, g.M, g.K, g.lda, 64, 64)
                  : make_tmap(&ta, g.A, g.K, g.M, g.lda, 64, 128);
   ok = ok && (B_MN ? make_tmap(&tb, g.B, g.N, g.K, g.ldb, 64, 64)
                    : make_tmap(&tb, g.B, g.K, g.N, g.ldb, 64, 128));
+  if (ep.c_tma)
+    ok = ok && make_tmap_f32(&tc, g.C, g.N, g.M, g.ldc);
+  else
+    tc = ta;  // not read
   if (!ok) return MGB_ERR_CUDA;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -877,19 +1020,30 @@ mgb_status launch_pair_variant(const GemmArgs& g, const EpiParams& ep, cudaStrea
     }
     max_pairs[dev] = n;
   }
-  const long total = (long)ep.tiles_m * ep.tiles_n;
+  const long total = (long)ep.tiles_m * ep.tiles_n * ep.k_splits;
   const int pairs = (int)std::max(1L, std::min<long>(total, max_pairs[dev]));
   cfg.gridDim = dim3(2 * pairs, 1, 1);
   LaunchScope scope(g.prof_kind >= 0 ? g.prof_kind
                                : (A_MN ? PROF_GEMM_WGRAD : (B_MN ? PROF_GEMM_DGRAD : PROF_GEMM_FWD)),
                     st);
-  if (cudaLaunchKernelEx(&cfg, kern, ta, tb, ep) != cudaSuccess) return MGB_ERR_CUDA;
+  if (cudaLaunchKernelEx(&cfg, kern, ta, tb, tc, ep) != cudaSuccess) return MGB_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? MGB_OK : MGB_ERR_CUDA;
+}
+
+// Column tiles of width bn, per column chunk when chunks are on.
+void set_tiles_n(EpiParams& ep, int N, int bn) {
+  if (ep.n_chunk > 0) {
+    ep.tpc = (ep.n_chunk + bn - 1) / bn;
+    ep.gpc = (ep.n_chunk + 127) / 128;
+    ep.tiles_n = (N + ep.n_chunk - 1) / ep.n_chunk * ep.tpc;
+  } else {
+    ep.tiles_n = (N + bn - 1) / bn;
+  }
 }
 
 mgb_status launch_pair(const GemmArgs& g, EpiParams ep, cudaStream_t st) {
   ep.tiles_m = (g.M + 255) / 256;
-  ep.tiles_n = (g.N + 255) / 256;
+  set_tiles_n(ep, g.N, 256);
   const long panel = 256L * g.K * 2;
   ep.group_m = (int)std::max(2L, std::min(32L, (48L << 20) / panel));
   ep.group_m = std::min(ep.group_m, ep.tiles_m);
@@ -902,7 +1056,7 @@ mgb_status launch_pair(const GemmArgs& g, EpiParams ep, cudaStream_t st) {
 template <int BN, int STAGES>
 mgb_status launch_bn(const GemmArgs& g, EpiParams ep, cudaStream_t st) {
   ep.tiles_m = (g.M + BM - 1) / BM;
-  ep.tiles_n = (g.N + BN - 1) / BN;
+  set_tiles_n(ep, g.N, BN);
   // Row tiles per raster group: the group's A panel (group_m x 128 rows x K)
   // should stay resident in L2 (about 48 MB) while the B columns stream by.
   const long panel = (long)BM * (g.K > 0 ? g.K : 1) * 2;
@@ -961,6 +1115,18 @@ mgb_status gemm_tc_launch(const GemmArgs& g, cudaStream_t st) {
   ep.tgt_v0 = g.tgt_v0;
   ep.tgt_out = g.tgt_out;
   ep.cpart = (g.epi == EPI_DGELU || g.epi == EPI_DSWIGLU) ? g.colsum_part : nullptr;
+  ep.c_tma = (g.epi == EPI_F32 && g.f32_tma) ? (g.accumulate ? 2 : 1) : 0;
+  ep.n_chunk = (g.epi == EPI_CE_STATS || g.epi == EPI_CE_GRAD) && g.n_chunk < g.N ? g.n_chunk : 0;
+  ep.tpc = ep.gpc = 0;
+  const int num_k = (g.K + BK - 1) / BK;
+  ep.k_splits = 1;
+  ep.kb_per_split = num_k;
+  ep.split_stride = 0;
+  if (g.k_splits > 1 && num_k > 1) {
+    ep.kb_per_split = (num_k + g.k_splits - 1) / g.k_splits;
+    ep.k_splits = (num_k + ep.kb_per_split - 1) / ep.kb_per_split;  // no empty range
+    ep.split_stride = g.split_stride;
+  }
   // Tile: 256 x 256 on a CTA pair when there are enough such tiles to fill
   // the GPU; else 128 x 256 on one SM, or 128 x 128 when the problem is too
   // narrow to fill the GPU with 256 columns. MGB_GEMM_PAIR=0 / =1 turns the
@@ -970,11 +1136,69 @@ mgb_status gemm_tc_launch(const GemmArgs& g, cudaStream_t st) {
   const char* pe = getenv("MGB_GEMM_PAIR");
   const int force = pe == nullptr ? -1 : (pe[0] == '1' ? 1 : (pe[0] == '0' ? 0 : -1));
   const bool pair = g.K > 0 && (force == 1 || (force == -1 && g.M > 128 && g.N > 128 &&
-                                               pair_tiles >= device_sm_count() / 2));
+                                               pair_tiles * ep.k_splits >= device_sm_count() / 2));
   if (pair) return launch_pair(g, ep, st);
   if (g.epi == EPI_BIAS_SWIGLU || (tiles256 >= 148 && g.N > 128))
     return launch_bn<256, 4>(g, ep, st);
   return launch_bn<128, 6>(g, ep, st);
+}
+
+int gemm_splitk_count(int M, int N, int K, int max_splits) {
+  const long tiles = (long)((M + 255) / 256) * ((N + 255) / 256);
+  const int num_k = (K + BK - 1) / BK;
+  const int npairs = std::max(1, device_sm_count() / 2);
+  if (tiles <= 0 || num_k < 16) return 1;
+  // fraction of the pair slots busy over the waves a split count needs
+  auto fill = [&](int s) {
+    const long t = tiles * s;
+    const long waves = (t + npairs - 1) / npairs;
+    return (double)t / (double)(waves * npairs);
+  };
+  int best = 1;
+  double best_fill = fill(1);
+  const int lim = std::min(max_splits, num_k / 8);
+  for (int s = 2; s <= lim && best_fill < 0.93; ++s) {
+    const double f = fill(s);
+    if (f > best_fill + 1e-9) {
+      best = s;
+      best_fill = f;
+    }
+  }
+  return best;
+}
+
+namespace {
+__global__ void __launch_bounds__(256) splitk_reduce_kernel(int M, int N, int splits,
+                                                            const float* __restrict__ part,
+                                                            int64_t split_stride, int64_t ldp,
+                                                            bf16* __restrict__ out, int64_t ldo) {
+  const int nv = N / 8;
+  const int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= (int64_t)M * nv) return;
+  const int m = (int)(i / nv), c = (int)(i % nv) * 8;
+  float a[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  const float* pp = part + (int64_t)m * ldp + c;
+  for (int s = 0; s < splits; ++s) {
+    const float4 x = *reinterpret_cast<const float4*>(pp);
+    const float4 y = *reinterpret_cast<const float4*>(pp + 4);
+    a[0] += x.x; a[1] += x.y; a[2] += x.z; a[3] += x.w;
+    a[4] += y.x; a[5] += y.y; a[6] += y.z; a[7] += y.w;
+    pp += split_stride;
+  }
+  store8(out + (int64_t)m * ldo + c, a);
+}
+}  // namespace
+
+mgb_status splitk_reduce_launch(int M, int N, int splits, const float* part, int64_t split_stride,
+                                int64_t ldp, void* out, int64_t ldo, cudaStream_t st) {
+  if (M < 0 || N < 0 || splits < 1 || N % 8 || ldp % 4 || ldo % 8 || split_stride % 4)
+    return MGB_ERR_INVALID_ARG;
+  const int64_t n = (int64_t)M * (N / 8);
+  if (n == 0) return MGB_OK;
+  LaunchScope scope(PROF_SPLITK_REDUCE, st);
+  splitk_reduce_kernel<<<(unsigned)((n + 255) / 256), 256, 0, st>>>(M, N, splits, part, split_stride,
+                                                                    ldp, static_cast<bf16*>(out), ldo);
+  return cudaGetLastError() == cudaSuccess ? MGB_OK : MGB_ERR_CUDA;
 }
 
 int device_sm_count() {

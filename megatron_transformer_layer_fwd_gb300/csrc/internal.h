@@ -3,6 +3,7 @@
 
 #include <cuda_runtime.h>
 #include <stdint.h>
+#include <stdlib.h>
 
 #include "../../include/mgb.h"
 
@@ -62,6 +63,24 @@ struct GemmArgs {
   // output column c before bf16 rounding; W = N (DGELU) or 2N (DSWIGLU);
   // ceil(M / 32) blocks. colsum_reduce_launch folds them.
   float* colsum_part = nullptr;
+  // split-K, EPI_F32 without accumulate only: the K dimension is cut into
+  // k_splits ranges (whole 64-wide K blocks) and range s writes its float32
+  // partial product to C + s * split_stride (elements); splitk_reduce_launch
+  // sums the planes. gemm_splitk_count picks k_splits for a shape.
+  int k_splits = 1;
+  int64_t split_stride = 0;
+  // EPI_F32 (no split, no C2) through TMA bulk copies of staged 32 x 32 boxes:
+  // stores C, or with `accumulate` reduce-adds into C in L2 (no read of C by
+  // the SMs). The order in which concurrent tiles add is not fixed, but each
+  // element receives exactly one addition per call, so the result of one
+  // call is the float32 sum C + acc as with the plain path.
+  int f32_tma = 0;
+  // EPI_CE_STATS / EPI_CE_GRAD, 0 = off: the N columns are vocab chunks of
+  // n_chunk columns (the last may be narrower) handled in one launch; no
+  // output tile straddles two chunks, and chunk c's statistics groups are
+  // numbered from c * ceil(n_chunk / 128) (the same planes as one launch per
+  // chunk); tgt_v0 must be 0 (targets are global columns)
+  int n_chunk = 0;
 };
 
 // A library-owned side stream per (host thread, device, slot) for work off a
@@ -74,6 +93,10 @@ struct GemmArgs {
 // the event's state when it is enqueued. If the stream cannot be created the
 // side work runs on the caller's stream. With an `external` stream the side
 // work goes there instead and is not joined back (the caller orders it).
+// The side streams have the lowest stream priority, so when SMs free up the
+// block scheduler starts pending blocks of a caller's stream created with a
+// higher priority first. MGB_SIDE_STREAMS=0 in the environment puts all side
+// work on the caller's stream (serial order; for timing comparisons).
 class SideLane {
  public:
   explicit SideLane(cudaStream_t main, cudaStream_t external = nullptr, int slot = 0)
@@ -86,9 +109,13 @@ class SideLane {
     thread_local PerDevice per[16][2];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 16 || slot < 0 || slot > 1) return;
+    const char* env = getenv("MGB_SIDE_STREAMS");
+    if (env != nullptr && env[0] == '0' && external == nullptr) return;
     PerDevice& d = per[dev][slot];
     if (d.side == nullptr && !d.failed) {
-      bool ok = cudaStreamCreateWithFlags(&d.side, cudaStreamNonBlocking) == cudaSuccess;
+      int least = 0, greatest = 0;
+      if (cudaDeviceGetStreamPriorityRange(&least, &greatest) != cudaSuccess) least = 0;
+      bool ok = cudaStreamCreateWithPriority(&d.side, cudaStreamNonBlocking, least) == cudaSuccess;
       for (int i = 0; ok && i < kEvents; ++i)
         ok = cudaEventCreateWithFlags(&d.ev[i], cudaEventDisableTiming) == cudaSuccess;
       if (!ok) {
@@ -133,6 +160,14 @@ class SideLane {
 
 // Validates operand geometry for the chosen path; returns MGB_OK or an error.
 mgb_status gemm_check(const GemmArgs& g);
+// K ranges for a bf16 M x N x K product on CTA-pair tiles so that the tiles
+// of all ranges fill whole waves of the GPU (at most max_splits, and ranges
+// of at least 8 K blocks); 1 when splitting does not help.
+int gemm_splitk_count(int M, int N, int K, int max_splits);
+// out[m, n] = bf16(sum over s < splits of part[s * split_stride + m * ldp + n])
+// in fixed order; N a multiple of 8, 16-byte aligned rows.
+mgb_status splitk_reduce_launch(int M, int N, int splits, const float* part, int64_t split_stride,
+                                int64_t ldp, void* out, int64_t ldo, cudaStream_t st);
 // Launches the bf16 tcgen05 GEMM (dtype MGB_BF16) or the float32 SIMT GEMM.
 mgb_status gemm_launch(const GemmArgs& g, cudaStream_t st);
 
@@ -205,6 +240,9 @@ mgb_status ce_combine_launch(int T, int n_parts, const float* m, const float* s,
                              const float* t, float* lse, float* loss, float* loss_mean,
                              float* block_loss, float* split, cudaStream_t st);
 inline int ce_combine_blocks(int T) { return (T + 255) / 256; }
+// loss_mean = (sum of the first nb block sums, fixed order) / T.
+mgb_status ce_mean_launch(int nb, int T, const float* block_loss, float* loss_mean,
+                          cudaStream_t st);
 mgb_status ce_grad_launch(int T, int C, int v0, void* logits, int64_t ldl, const int32_t* targets,
                           const float* lse, float scale, cudaStream_t st);
 
@@ -231,18 +269,38 @@ int device_sm_count();
 // Device address of the current device's error word (nullptr on failure).
 int* device_error_word();
 
+// Host-side fault injection: true when MGB_FAULT=validate, which makes every
+// entry point's argument validation fail before any launch.
+bool fault_injected();
+// MGB_OK when the current device is sm_103 (GB300), else MGB_ERR_ARCH /
+// MGB_ERR_CUDA.
+mgb_status check_arch();
+// The current thread's CUDA driver context (a CUcontext), or nullptr. A
+// per-device cache of device-symbol addresses is keyed on it, so a context
+// that was destroyed and created again (cudaDeviceReset) is noticed.
+void* current_cuda_context();
+
 // Kernel kinds for timing (mgb_profile_*).
 enum ProfKind : int {
   PROF_GEMM_FWD = 0, PROF_GEMM_DGRAD, PROF_GEMM_WGRAD, PROF_GEMM_F32, PROF_ATTN_FWD,
   PROF_ATTN_BWD, PROF_LN_FWD, PROF_LN_BWD, PROF_COLSUM, PROF_CE_STATS, PROF_CE_COMBINE,
-  PROF_CE_GRAD, PROF_GEMM_CE_LOGITS, PROF_EMBEDDING, PROF_DROPOUT, PROF_KINDS
+  PROF_CE_GRAD, PROF_GEMM_CE_LOGITS, PROF_EMBEDDING, PROF_DROPOUT,
+  // the CE's input-gradient (G E) and weight-gradient (G^T hidden) products
+  PROF_GEMM_CE_DGRAD, PROF_GEMM_CE_WGRAD, PROF_SPLITK_REDUCE,
+  // stages of the layer (CUDA events around groups of launches, not kernels):
+  // attention sublayer forward (LN1, QKV, attention, output projection +
+  // residual), MLP sublayer forward (LN2, fc1 + activation, fc2 + residual),
+  // the whole backward (side streams joined)
+  PROF_STAGE_ATTN, PROF_STAGE_FFN, PROF_STAGE_BWD, PROF_KINDS
 };
 
 // Counts `launches` kernel launches and, when profiling is on, brackets them
 // with CUDA events on stream `st` (construct right before the launches).
+// count_launches = false: a stage timer around launches that have their own
+// scopes (counted once per stage in the profile, not in mgb_launch_count).
 class LaunchScope {
  public:
-  LaunchScope(int kind, cudaStream_t st, int launches = 1);
+  LaunchScope(int kind, cudaStream_t st, int launches = 1, bool count_launches = true);
   ~LaunchScope();
   LaunchScope(const LaunchScope&) = delete;
   LaunchScope& operator=(const LaunchScope&) = delete;

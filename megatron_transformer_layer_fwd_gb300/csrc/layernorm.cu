@@ -521,28 +521,41 @@ mgb_status layernorm_bwd_launch(int rows, int cols, int dtype, const void* x, co
 
 // ------------------------------------------- LayerNorm backward, no allocation
 // Scratch of mgb_layernorm_bwd_noalloc: the float32 partial sums of dgamma and
-// dbeta, [2][kNoAllocParts][cols] with cols <= kNoAllocMaxCols (8 MiB). It is
-// a file-scope device array, so every GPU that loads the library holds it until
-// the process exits, and every call on a device shares it.
-constexpr int kNoAllocParts = 64;
+// dbeta, [2][nparts][cols] in a file-scope device array of kNoAllocFloats
+// floats (8 MiB). Every GPU that loads the library holds it until the process
+// exits, and every call on a device shares it. A call with cols columns uses
+// nparts = min(the workspace version's row blocks, kNoAllocFloats / (2 cols))
+// partial rows: 256 at cols 4096, 64 at the widest row, 16384.
+constexpr int kNoAllocFloats = 2 * 64 * 16384;
 constexpr int kNoAllocMaxCols = 16384;
-static __device__ __align__(256) float g_ln_bwd_scratch[2 * kNoAllocParts * kNoAllocMaxCols];
+static __device__ __align__(256) float g_ln_bwd_scratch[kNoAllocFloats];
 
-// Device address of g_ln_bwd_scratch on the current device. Looked up once per
-// device (the first call on that device), with that device current; host code
-// must never pass the symbol itself to a kernel.
+// Device address of g_ln_bwd_scratch on the current device. Looked up on the
+// first call on each device, with that device current, and again only when
+// the device's context changed (a reset device gets a new one); host code
+// never passes the symbol itself to a kernel.
 static float* ln_bwd_scratch_address() {
   static float* addr[64] = {};
+  static void* ctx_of[64] = {};
   static std::mutex mu;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return nullptr;
+  void* ctx = current_cuda_context();
   std::lock_guard<std::mutex> lock(mu);
-  if (addr[dev] == nullptr) {
+  if (addr[dev] == nullptr || ctx == nullptr || ctx_of[dev] != ctx) {
     void* p = nullptr;
     if (cudaGetSymbolAddress(&p, g_ln_bwd_scratch) != cudaSuccess) return nullptr;
     addr[dev] = static_cast<float*>(p);
+    ctx_of[dev] = current_cuda_context();
   }
   return addr[dev];
+}
+
+// Partial rows the no-allocation backward uses for `rows` x `cols`.
+static int noalloc_parts(int rows, int cols) {
+  const int fit = kNoAllocFloats / (2 * (cols > 0 ? cols : 1));
+  const int want = layernorm_bwd_parts(rows);
+  return want < fit ? want : fit;
 }
 
 mgb_status colsum_launch(int M, int N, int dtype, const void* dY, int64_t ld, void* db,
@@ -593,6 +606,7 @@ extern "C" mgb_status mgb_layernorm_bwd_noalloc(int32_t rows, int32_t cols, int3
                                                 const void* dy, const void* dres, void* dx,
                                                 void* dgamma, void* dbeta, void* stream) {
   using namespace mgb;
+  if (fault_injected()) return MGB_ERR_INVALID_ARG;
   if (dtype != MGB_BF16 && dtype != MGB_F32) return MGB_ERR_INVALID_ARG;
   if (rows < 0 || cols < 1 || !x || !mean || !rstd || !dy || !dx) return MGB_ERR_INVALID_ARG;
   if (!gamma && (dgamma || dbeta)) return MGB_ERR_INVALID_ARG;
@@ -600,22 +614,18 @@ extern "C" mgb_status mgb_layernorm_bwd_noalloc(int32_t rows, int32_t cols, int3
   for (const void* q : ps)
     if ((reinterpret_cast<uintptr_t>(q) & 15u) != 0) return MGB_ERR_MISALIGNED;
   const bool want = dgamma || dbeta;
-  // the partial sums must fit the fixed scratch array
+  // at least one partial row of the widest allowed row must fit the array
   if (want && cols > kNoAllocMaxCols) return MGB_ERR_UNSUPPORTED;
-  int dev = 0, major = 0, minor = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess ||
-      cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
-      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
-    return MGB_ERR_CUDA;
-  if (major != 10 || minor != 3) return MGB_ERR_ARCH;
+  const mgb_status arch = check_arch();
+  if (arch != MGB_OK) return arch;
   float* part = nullptr;
   if (want) {
     part = ln_bwd_scratch_address();
     if (part == nullptr) return MGB_ERR_CUDA;
   }
   // each row block overwrites its whole partial row, so nothing left in the
-  // array by an earlier call is read (rows == 0 zeroes the slots it reduces)
-  const int nparts = rows < kNoAllocParts ? (rows > 0 ? rows : 1) : kNoAllocParts;
+  // array by an earlier call is read (rows == 0 zeroes the one row it reduces)
+  const int nparts = want ? noalloc_parts(rows, cols) : layernorm_bwd_parts(rows);
   return layernorm_bwd_launch(rows, cols, dtype, x, mean, rstd, gamma, dy, dres, dx, dgamma, dbeta,
                               part, nparts, reinterpret_cast<cudaStream_t>(stream));
 }

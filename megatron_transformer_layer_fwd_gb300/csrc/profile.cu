@@ -59,13 +59,15 @@ mgb_status drain_locked() {
 const char* kKindNames[PROF_KINDS] = {
     "gemm_tc_fwd",  "gemm_tc_dgrad", "gemm_tc_wgrad", "gemm_f32",  "attn_fwd",   "attn_bwd",
     "layernorm_fwd", "layernorm_bwd", "colsum",       "ce_stats", "ce_combine", "ce_grad",
-    "gemm_tc_ce_logits", "embedding", "dropout"};
+    "gemm_tc_ce_logits", "embedding", "dropout", "gemm_tc_ce_dgrad", "gemm_tc_ce_wgrad",
+    "splitk_reduce",
+    "stage_attention", "stage_ffn", "stage_backward"};
 
 }  // namespace
 
-LaunchScope::LaunchScope(int kind, cudaStream_t st, int launches)
+LaunchScope::LaunchScope(int kind, cudaStream_t st, int launches, bool count_launches)
     : kind_(kind), launches_(launches), st_(st), a_(nullptr) {
-  g_launches.fetch_add((uint64_t)launches, std::memory_order_relaxed);
+  if (count_launches) g_launches.fetch_add((uint64_t)launches, std::memory_order_relaxed);
   if (g_enabled.load(std::memory_order_relaxed)) {
     std::lock_guard<std::mutex> lock(g_mu);
     a_ = take_event();

@@ -28,7 +28,7 @@ MGB_ERR_DEVICE_TIMEOUT = -7
 MGB_ERR_NOT_IMPLEMENTED = -8
 
 MGB_F32, MGB_BF16 = 0, 1
-MGB_CE_STREAM, MGB_CE_FUSED, MGB_CE_RESIDENT = 0, 1, 2
+MGB_CE_STREAM, MGB_CE_FUSED, MGB_CE_RESIDENT, MGB_CE_BLOCKED = 0, 1, 2, 3
 MGB_PRE_LN, MGB_POST_LN = 0, 1
 MGB_GELU_ERF, MGB_SWIGLU = 0, 1
 MGB_K_MAJOR, MGB_MN_MAJOR = 0, 1
@@ -74,7 +74,8 @@ class BlockGrads(ctypes.Structure):
 class CEDesc(ctypes.Structure):
     _fields_ = [("tokens", ctypes.c_int32), ("hidden", ctypes.c_int32), ("vocab", ctypes.c_int32),
                 ("chunk", ctypes.c_int32), ("dtype", ctypes.c_int32), ("grad_scale", ctypes.c_float),
-                ("mode", ctypes.c_int32), ("emb_stream", ctypes.c_void_p)]
+                ("mode", ctypes.c_int32), ("emb_stream", ctypes.c_void_p),
+                ("token_block", ctypes.c_int32)]
 
 
 class GemmDesc(ctypes.Structure):
@@ -238,9 +239,9 @@ def mgb_block_bwd(desc: BlockDesc, weights: dict, x, dy, saved, dx, grads: dict,
 
 
 def ce_desc(tokens: int, hidden: int, vocab: int, chunk: int, grad_scale: float,
-            mode: int = MGB_CE_FUSED) -> CEDesc:
+            mode: int = MGB_CE_FUSED, token_block: int = 0) -> CEDesc:
     return CEDesc(tokens=tokens, hidden=hidden, vocab=vocab, chunk=chunk, dtype=MGB_BF16,
-                  grad_scale=grad_scale, mode=mode)
+                  grad_scale=grad_scale, mode=mode, token_block=token_block)
 
 
 def mgb_vocab_ce_sizes(desc: CEDesc) -> int:

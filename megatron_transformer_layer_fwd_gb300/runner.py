@@ -56,13 +56,19 @@ class CERunner:
 
     def __init__(self, tokens: int, hidden: int, vocab: int, chunk: int, hidden_t: torch.Tensor,
                  emb_t: torch.Tensor, targets_t: torch.Tensor, grad_scale: float | None = None,
-                 want_grads: bool = True, mode: int = mgb.MGB_CE_FUSED, emb_stream=None):
+                 want_grads: bool = True, mode: int = mgb.MGB_CE_FUSED, emb_stream=None,
+                 token_block: int = 0):
         dev = hidden_t.device
         self.desc = mgb.ce_desc(tokens, hidden, vocab, chunk,
-                                grad_scale if grad_scale is not None else 1.0 / max(tokens, 1), mode)
-        # resident mode: d_emb is left running on this stream (the caller joins it)
+                                grad_scale if grad_scale is not None else 1.0 / max(tokens, 1), mode,
+                                token_block)
+        # resident / blocked mode: d_emb (its last part) is left running on this
+        # stream (the caller joins it)
         self.desc.emb_stream = emb_stream.cuda_stream if emb_stream is not None else None
         self.hidden, self.emb, self.targets = hidden_t, emb_t, targets_t
+        # the blocked mode's rows per block as the library rounds them
+        tb = token_block if token_block > 0 else 2048
+        self.token_block = min((tb + 255) // 256 * 256, (tokens + 255) // 256 * 256)
         self.ws = torch.empty(max(mgb.mgb_vocab_ce_sizes(self.desc), 16), dtype=torch.uint8, device=dev)
         self.loss = torch.empty(max(tokens, 1), dtype=torch.float32, device=dev)
         self.lse = torch.empty(max(tokens, 1), dtype=torch.float32, device=dev)

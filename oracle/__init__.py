@@ -43,7 +43,7 @@ from .layernorm import ln_fwd, ln_bwd
 from .activations import gelu, gelu_grad, silu, silu_grad, swiglu_fwd, swiglu_bwd, glu_split
 from .attention import attention_fwd, attention_bwd
 from .layer import block_fwd, block_bwd, block_fwd_rows
-from .cross_entropy import ce_full, ce_chunked, ce_grads, ce_rows
+from .cross_entropy import ce_full, ce_chunked, ce_grads, ce_rows, ce_emb_rows
 from .embedding import embedding_fwd, embedding_bwd
 from . import dropout
 from . import shard
@@ -51,6 +51,6 @@ from . import shard
 __all__ = [
     "ln_fwd", "ln_bwd", "gelu", "gelu_grad", "silu", "silu_grad", "swiglu_fwd", "swiglu_bwd",
     "glu_split", "attention_fwd", "attention_bwd", "block_fwd", "block_bwd", "block_fwd_rows",
-    "ce_full", "ce_chunked", "ce_grads", "ce_rows", "embedding_fwd", "embedding_bwd", "dropout",
+    "ce_full", "ce_chunked", "ce_grads", "ce_rows", "ce_emb_rows", "embedding_fwd", "embedding_bwd", "dropout",
     "shard",
 ]

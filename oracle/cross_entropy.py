@@ -107,3 +107,20 @@ def ce_rows(hidden_rows, emb, targets_rows, scale):
     G = np.exp(l - lse[:, None])
     G[np.arange(n), targets_rows] -= 1.0
     return loss, lse, (G * scale) @ emb
+
+
+def ce_emb_rows(hidden, emb, targets, lse, scale, vocab_ids):
+    """Selected rows of dL/demb for L = scale * sum_t loss_t (full-size checks).
+
+    Row v of demb = G^T hidden is sum_t G[t, v] hidden[t] with
+    G[t, v] = (exp(l_tv - LSE_t) - [targets_t = v]) * scale: it needs the
+    logits of column v for every token and every token's LSE (from ce_full),
+    and nothing else, so it equals those rows of ce_grads' demb.
+    """
+    vocab_ids = np.asarray(vocab_ids)
+    l = hidden @ emb[vocab_ids].T                        # [T, n]
+    G = np.exp(l - lse[:, None])
+    G -= (targets[:, None] == vocab_ids[None, :])
+    G *= scale
+    return G.T @ hidden
+

@@ -114,8 +114,10 @@ def test_ce_validation(lib):
     assert lib.mgb_vocab_ce_sizes(ctypes.byref(bad), ctypes.byref(s)) == mgb.MGB_ERR_MISALIGNED
     f32 = mgb.CEDesc(tokens=8, hidden=8, vocab=8, chunk=8, dtype=mgb.MGB_F32, grad_scale=1.0)
     assert lib.mgb_vocab_ce_sizes(ctypes.byref(f32), ctypes.byref(s)) == mgb.MGB_ERR_UNSUPPORTED
-    badmode = mgb.ce_desc(8192, 4096, 128256, 16032, 1 / 8192, mode=3)
+    badmode = mgb.ce_desc(8192, 4096, 128256, 16032, 1 / 8192, mode=4)
     assert lib.mgb_vocab_ce_sizes(ctypes.byref(badmode), ctypes.byref(s)) == mgb.MGB_ERR_INVALID_ARG
+    badtb = mgb.ce_desc(8192, 4096, 128256, 16032, 1 / 8192, mode=mgb.MGB_CE_BLOCKED, token_block=-1)
+    assert lib.mgb_vocab_ce_sizes(ctypes.byref(badtb), ctypes.byref(s)) == mgb.MGB_ERR_INVALID_ARG
     # fused partials: one per token and 128 vocab columns (126 per 16032-wide chunk)
     fused = mgb.mgb_vocab_ce_sizes(mgb.ce_desc(8192, 4096, 128256, 16032, 1 / 8192))
     stream = mgb.mgb_vocab_ce_sizes(mgb.ce_desc(8192, 4096, 128256, 16032, 1 / 8192,
@@ -127,6 +129,24 @@ def test_ce_validation(lib):
                                                   mode=mgb.MGB_CE_RESIDENT))
     assert resident >= 2 * 8192 * 128256
     assert resident - fused == 2 * 8192 * (128256 - 16032) - 4 * 8192 * 4096
+
+
+def test_ce_blocked_workspace_is_bounded_by_the_block(lib):
+    """The token-blocked CE holds one block of logits [token_block, vocab] and
+    a float32 [vocab, hidden] d_emb accumulator, however many tokens there
+    are: its workspace does not grow with the token count (only the per-token
+    LSE and loss sums do)."""
+    V, H = 128256, 4096
+    sizes = {T: mgb.mgb_vocab_ce_sizes(mgb.ce_desc(T, H, V, 16032, 1 / T, mode=mgb.MGB_CE_BLOCKED,
+                                                    token_block=2048))
+             for T in (8192, 65536)}
+    assert sizes[8192] >= 2 * 2048 * V + 4 * V * H
+    assert sizes[8192] < 2 * 8192 * V + 4 * V * H     # less than the whole logits beside it
+    assert sizes[65536] - sizes[8192] < 16 * (65536 - 8192)  # per-token float32 arrays only
+    # one block (all tokens fit): no float32 accumulator
+    one = mgb.mgb_vocab_ce_sizes(mgb.ce_desc(2048, H, V, 16032, 1 / 2048, mode=mgb.MGB_CE_BLOCKED,
+                                             token_block=2048))
+    assert one < 2 * 2048 * V + 4 * V * H
 
 
 def test_gemm_validation(lib):
@@ -236,6 +256,11 @@ def test_injected_validation_fault(lib, monkeypatch):
     assert lib.mgb_block_sizes(ctypes.byref(d), ctypes.byref(s), None, None) == mgb.MGB_OK
     monkeypatch.setenv("MGB_FAULT", "validate")
     assert lib.mgb_block_sizes(ctypes.byref(d), ctypes.byref(s), None, None) == mgb.MGB_ERR_INVALID_ARG
+    # the allocation-free LayerNorm backward takes the same injection, before
+    # anything else (no device is needed to see it)
+    p = 4096
+    assert lib.mgb_layernorm_bwd_noalloc(8, 64, mgb.MGB_BF16, p, p, p, p, p, None, p, p, p,
+                                         None) == mgb.MGB_ERR_INVALID_ARG
     monkeypatch.delenv("MGB_FAULT")
     assert lib.mgb_block_sizes(ctypes.byref(d), ctypes.byref(s), None, None) == mgb.MGB_OK
 

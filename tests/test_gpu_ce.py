@@ -15,14 +15,58 @@ from tests.util import CE_LOSS_ABS, rel_l2, to_np
 pytestmark = pytest.mark.gpu
 
 
-MODES = [mgb.MGB_CE_STREAM, mgb.MGB_CE_FUSED, mgb.MGB_CE_RESIDENT]
+MODES = [mgb.MGB_CE_STREAM, mgb.MGB_CE_FUSED, mgb.MGB_CE_RESIDENT, mgb.MGB_CE_BLOCKED]
 
 
-def _runner(shape, inp, mode):
+def _runner(shape, inp, mode, token_block=0, emb_stream=None):
     h = to_device(inp["hidden"], torch.bfloat16)
     e = to_device(inp["emb"], torch.bfloat16)
     t = torch.from_numpy(inp["targets"]).to("cuda")
-    return CERunner(shape.tokens, shape.hidden, shape.vocab, shape.chunk, h, e, t, mode=mode)
+    return CERunner(shape.tokens, shape.hidden, shape.vocab, shape.chunk, h, e, t, mode=mode,
+                    token_block=token_block, emb_stream=emb_stream)
+
+
+@pytest.mark.parametrize("T,H,V,C,tb", [(300, 256, 1000, 136, 256), (512, 1024, 8192, 1000, 256),
+                                        (1100, 128, 2048, 2048, 512), (130, 64, 520, 64, 256)])
+def test_ce_blocked_token_blocks(mgb_lib, T, H, V, C, tb):
+    """The token-blocked CE with several blocks (a ragged last one): each
+    block's losses from its own partials, d_hidden rows from the split-K
+    product, d_emb accumulated in float32 across blocks."""
+    shape = CEShape(T, H, V, C)
+    inp = ce_inputs(shape, seed=15)
+    r = _runner(shape, inp, mgb.MGB_CE_BLOCKED, token_block=tb)
+    r.run()
+    assert mgb.mgb_device_status() == mgb.MGB_OK
+    loss, lse, mean, _ = oracle.ce_chunked(inp["hidden"], inp["emb"], inp["targets"], C)
+    dh, de = oracle.ce_grads(inp["hidden"], inp["emb"], inp["targets"], lse, 1.0 / T)
+    assert np.abs(to_np(r.loss) - loss).max() < CE_LOSS_ABS
+    assert np.abs(to_np(r.lse) - lse).max() < CE_LOSS_ABS
+    assert abs(float(r.loss_mean[0]) - mean) < CE_LOSS_ABS
+    assert rel_l2(to_np(r.d_hidden), dh) < 2e-2
+    assert rel_l2(to_np(r.d_emb), de) < 2e-2
+    # the same call again gives the same bits (fixed-order sums throughout)
+    first = (r.loss.clone(), r.d_hidden.clone(), r.d_emb.clone())
+    r.run()
+    assert torch.equal(first[0], r.loss) and torch.equal(first[1], r.d_hidden)
+    assert torch.equal(first[2], r.d_emb)
+
+
+def test_ce_blocked_emb_stream(mgb_lib):
+    """Blocked mode with the last block's d_emb left on a caller's stream:
+    after joining it, the results equal those of the joined call bit for bit."""
+    shape = CEShape(600, 256, 2000, 704)
+    inp = ce_inputs(shape, seed=21)
+    r0 = _runner(shape, inp, mgb.MGB_CE_BLOCKED, token_block=256)
+    r0.run()
+    side = torch.cuda.Stream()
+    r1 = _runner(shape, inp, mgb.MGB_CE_BLOCKED, token_block=256, emb_stream=side)
+    main = torch.cuda.current_stream()
+    r1.run(main)
+    main.wait_stream(side)
+    torch.cuda.synchronize()
+    assert mgb.mgb_device_status() == mgb.MGB_OK
+    assert torch.equal(r0.d_emb, r1.d_emb) and torch.equal(r0.d_hidden, r1.d_hidden)
+    assert torch.equal(r0.loss, r1.loss)
 
 
 @pytest.mark.parametrize("mode", MODES)
@@ -78,39 +122,60 @@ def test_ce_forward_only(mgb_lib, mode):
     assert np.abs(to_np(r.loss) - loss).max() < CE_LOSS_ABS
 
 
+_FULL = {}
+
+
+def _full_size_oracle():
+    """The full CE workload's inputs and the oracle's whole forward over it
+    (every token's LSE and loss; about 8.6 TFLOP in float64, once per run),
+    plus sampled vocab ids: 24 that are some token's target, 24 that are not."""
+    if not _FULL:
+        shape = CE_WORKLOADS["bf16_ce_t8192h4096v128256"]
+        inp = ce_inputs(shape, seed=0)
+        t0 = time.time()
+        loss, lse, mean = oracle.ce_full(inp["hidden"], inp["emb"], inp["targets"])
+        rng = np.random.default_rng(0)
+        hit = rng.choice(np.unique(inp["targets"]), 24, replace=False)
+        miss_pool = np.setdiff1d(np.arange(shape.vocab), inp["targets"])
+        ids = np.sort(np.concatenate([hit, rng.choice(miss_pool, 24, replace=False)]))
+        d_emb_rows = oracle.ce_emb_rows(inp["hidden"], inp["emb"], inp["targets"], lse,
+                                        1.0 / shape.tokens, ids)
+        print(f"oracle full CE forward + {len(ids)} d_emb rows {time.time() - t0:.1f}s")
+        _FULL.update(shape=shape, inp=inp, loss=loss, lse=lse, mean=mean, ids=ids,
+                     d_emb_rows=d_emb_rows)
+    return _FULL
+
+
 @pytest.mark.slow
 @pytest.mark.parametrize("mode", MODES)
 def test_ce_full_size_sampled(mgb_lib, mode):
-    """Full tied-embedding CE workload: sampled tokens' loss / LSE / d_hidden
-    rows against the oracle one row at a time; the mean against the per-token
-    losses; d_emb column sums vanish (grad rows sum to 0)."""
-    shape = CE_WORKLOADS["bf16_ce_t8192h4096v128256"]
-    inp = ce_inputs(shape, seed=0)
+    """Full tied-embedding CE workload against the oracle: every token's loss
+    and LSE and the mean loss (the oracle's whole forward); sampled tokens'
+    d_hidden rows (one row at a time); sampled d_emb rows, ids that are some
+    token's target and ids that are none (each needs every token's LSE)."""
+    f = _full_size_oracle()
+    shape, inp = f["shape"], f["inp"]
     r = _runner(shape, inp, mode)
     r.run()
     assert mgb.mgb_device_status() == mgb.MGB_OK
+    assert np.abs(to_np(r.loss) - f["loss"]).max() < CE_LOSS_ABS
+    assert np.abs(to_np(r.lse) - f["lse"]).max() < CE_LOSS_ABS
+    assert abs(float(r.loss_mean[0]) - f["mean"]) < CE_LOSS_ABS
     rows = np.random.default_rng(0).choice(shape.tokens, 48, replace=False)
-    t0 = time.time()
-    loss, lse, dh = oracle.ce_rows(inp["hidden"][rows], inp["emb"], inp["targets"][rows],
-                                   1.0 / shape.tokens)
-    print(f"oracle rows {time.time() - t0:.1f}s")
-    gl = to_np(r.loss)
-    assert np.abs(gl[rows] - loss).max() < CE_LOSS_ABS
-    assert np.abs(to_np(r.lse)[rows] - lse).max() < CE_LOSS_ABS
-    assert abs(float(r.loss_mean[0]) - gl.mean()) < 1e-4
+    _, _, dh = oracle.ce_rows(inp["hidden"][rows], inp["emb"], inp["targets"][rows],
+                              1.0 / shape.tokens)
     assert rel_l2(to_np(r.d_hidden)[rows], dh) < 2e-2
-    de = r.d_emb.double()
-    col = de.sum(dim=0)
-    assert float(col.norm() / de.norm()) < 2e-2
+    assert rel_l2(to_np(r.d_emb[torch.from_numpy(f["ids"]).cuda()]), f["d_emb_rows"]) < 2e-2
 
 
 def test_ce_modes_agree_and_are_deterministic(mgb_lib):
-    """The three modes agree to float32 rounding, and each repeats bit for bit."""
+    """The modes agree to float32 rounding, and each repeats bit for bit
+    (the blocked mode with two token blocks)."""
     shape = CEShape(384, 256, 2000, 704)
     inp = ce_inputs(shape, seed=9)
     outs = []
     for mode in MODES:
-        r = _runner(shape, inp, mode)
+        r = _runner(shape, inp, mode, token_block=256)
         r.run()
         first = (r.loss.clone(), r.d_hidden.clone(), r.d_emb.clone())
         r.run()

@@ -187,7 +187,7 @@ def test_fp32_post_ln_layer(mgb_lib):
 
 
 @pytest.mark.parametrize("name", ["bf16_preln_b4s512h1024", "bf16_causal_b8s128h2048",
-                                  "bf16_causal_b8s512h2048"])
+                                  "bf16_causal_b8s256h2048", "bf16_causal_b8s512h2048"])
 def test_bf16_workload_full(mgb_lib, name):
     shape = WORKLOADS[name]
     arr = layer_inputs(shape, seed=0)
@@ -195,7 +195,8 @@ def test_bf16_workload_full(mgb_lib, name):
 
 
 @pytest.mark.slow
-@pytest.mark.parametrize("name", ["bf16_causal_b8s2048h2048", "bf16_gqa_swiglu_b2s4096h4096"])
+@pytest.mark.parametrize("name", ["bf16_causal_b8s1024h2048", "bf16_causal_b8s2048h2048",
+                                  "bf16_gqa_swiglu_b2s4096h4096"])
 def test_bf16_workload_full_large(mgb_lib, name):
     shape = WORKLOADS[name]
     arr = layer_inputs(shape, seed=0)

@@ -59,7 +59,7 @@ def _ln(x, g, b):
     return y
 
 
-def _attention(sh, qkv, nq, nkv, q0, k0, v0):
+def _attention(sh, qkv, nq, nkv, q0, k0, v0, with_lse=False):
     """Attention over nq query heads starting at column q0 of qkv (K at k0, V at v0)."""
     T, W = qkv.shape
     d = sh.head_dim
@@ -67,7 +67,18 @@ def _attention(sh, qkv, nq, nkv, q0, k0, v0):
     lse = torch.empty((sh.batch * nq * sh.seq,), device="cuda", dtype=torch.float32)
     mgb.mgb_attention_fwd(sh.batch, sh.seq, nq, nkv, d, sh.causal, mgb.MGB_BF16, qkv[:, q0:],
                           qkv[:, k0:], qkv[:, v0:], W, W, o, lse)
-    return o
+    return (o, lse) if with_lse else o
+
+
+def _attention_bwd(sh, qkv, o, lse, dO, dqkv, nq, nkv, q0, k0, v0):
+    """Attention backward over nq query heads into the matching columns of dqkv."""
+    T, W = qkv.shape
+    d = sh.head_dim
+    ws = torch.empty(mgb.mgb_attention_bwd_ws_bytes(sh.batch, sh.seq, nq), dtype=torch.uint8,
+                     device="cuda")
+    mgb.mgb_attention_bwd(sh.batch, sh.seq, nq, nkv, d, sh.causal, mgb.MGB_BF16, qkv[:, q0:],
+                          qkv[:, k0:], qkv[:, v0:], W, W, o, lse, dO, nq * d, dqkv[:, q0:],
+                          dqkv[:, k0:], dqkv[:, v0:], W, W, ws)
 
 
 class Sharded:
@@ -79,6 +90,11 @@ class Sharded:
         nq, nkv = sh.n_q_heads, sh.n_kv_heads
         self.Dq, self.Wqkv, self.W = nq * d, sh.qkv_width, sh.fc1_width
         self.nqs, self.nkvs = nq // k, nkv // k
+
+    def cols(self, i):
+        """First columns of shard i's Q, K and V heads in the fused qkv buffer."""
+        d, nq, nkv = self.sh.head_dim, self.sh.n_q_heads, self.sh.n_kv_heads
+        return (i * self.nqs * d, nq * d + i * self.nkvs * d, (nq + nkv) * d + i * self.nkvs * d)
 
     def forward(self):
         sh, w, k = self.sh, self.w, self.k
@@ -94,9 +110,11 @@ class Sharded:
                 r0, n = base + h0 * d, nh * d
                 _gemm(T, n, H, xn, H, w["w_qkv"][r0:r0 + n], H, qkv[:, r0:], self.Wqkv,
                       bias=w["b_qkv"][r0:r0 + n])
+        self.lses = []
         for i in range(k):
-            Os.append(_attention(sh, qkv, self.nqs, self.nkvs, i * self.nqs * d,
-                                 nq * d + i * self.nkvs * d, (nq + nkv) * d + i * self.nkvs * d))
+            o, lse = _attention(sh, qkv, self.nqs, self.nkvs, *self.cols(i), with_lse=True)
+            Os.append(o)
+            self.lses.append(lse)
         # row-parallel projection: partials summed on the device (float32)
         h32 = self.x.float() + w["b_o"].float()[None, :]
         for i in range(k):
@@ -148,6 +166,34 @@ class Sharded:
             _gemm(T, H, Ws, du, Ws, w["w_1"][i * Ws:], H, dhn32, H, b_mn=1, epi=mgb.MGB_EPI_F32,
                   accumulate=1)
         return dW2, dW1, dhn32
+
+    def attention_backward(self, dh):
+        """Per shard, from dh = dL/dh at the attention sublayer's output:
+        dWo[:, cols_i] = dh^T O_i (row-parallel weight gradient); dO_i =
+        dh Wo[:, cols_i]; the attention backward over its heads into its
+        columns of dqkv; dWqkv[rows_i] = dqkv_i^T xn (column-parallel weight
+        gradient); and the input gradient of the column-parallel QKV,
+        d xn = sum over shards of dqkv_i Wqkv[rows_i], summed in float32 (the
+        backward all-reduce)."""
+        sh, w, k = self.sh, self.w, self.k
+        T, H, d = sh.tokens, sh.hidden, sh.head_dim
+        dWo = torch.empty((H, self.Dq), device="cuda", dtype=BF)
+        dWqkv = torch.empty((self.Wqkv, H), device="cuda", dtype=BF)
+        dqkv = torch.full((T, self.Wqkv), float("nan"), device="cuda", dtype=BF)
+        dxn32 = torch.zeros((T, H), device="cuda", dtype=torch.float32)
+        for i in range(k):
+            q0, k0, v0 = self.cols(i)
+            n_q = self.nqs * d
+            _gemm(H, n_q, T, dh, H, self.Os[i], n_q, dWo[:, q0:], self.Dq, a_mn=1, b_mn=1)
+            dO = torch.empty((T, n_q), device="cuda", dtype=BF)
+            _gemm(T, n_q, H, dh, H, w["w_o"][:, q0:], self.Dq, dO, n_q, b_mn=1)
+            _attention_bwd(sh, self.qkv, self.Os[i], self.lses[i], dO, dqkv, self.nqs, self.nkvs,
+                           q0, k0, v0)
+            for r0, n in ((q0, n_q), (k0, self.nkvs * d), (v0, self.nkvs * d)):
+                _gemm(n, H, T, dqkv[:, r0:], self.Wqkv, self.xn, H, dWqkv[r0:], H, a_mn=1, b_mn=1)
+                _gemm(T, H, n, dqkv[:, r0:], self.Wqkv, w["w_qkv"][r0:], H, dxn32, H, b_mn=1,
+                      epi=mgb.MGB_EPI_F32, accumulate=1)
+        return dWo, dWqkv, dqkv, dxn32
 
 
 @pytest.mark.parametrize("name", list(SHAPES))
@@ -223,3 +269,59 @@ def test_tp_split_forward_and_mlp_backward(mgb_lib, name, k):
     assert rel_l2(to_np(dW2), g["w_2"]) < tol_g
     assert rel_l2(to_np(dW1), g["w_1"]) < tol_g
     assert mgb.mgb_device_status() == mgb.MGB_OK
+
+
+@pytest.mark.parametrize("name", list(SHAPES))
+@pytest.mark.parametrize("k", [2, 4])
+def test_tp_split_attention_backward(mgb_lib, name, k):
+    """The attention sublayer's backward split k ways by head: each shard's
+    dWqkv rows and dWo columns are exact slices of the unsplit gradients, its
+    dqkv columns equal the unsplit attention backward's, and the shards'
+    input gradients sum (float32) to the unsplit one; every shard also
+    matches the oracle's shard backward."""
+    sh = SHAPES[name]
+    if sh.n_kv_heads % k:
+        pytest.skip("shards need whole KV heads")
+    arr = layer_inputs(sh, seed=23, random_affine=True, random_dy=True)
+    r = LayerRunner(sh, arr)
+    w = r.w
+    T, H, d = sh.tokens, sh.hidden, sh.head_dim
+    nq, nkv = sh.n_q_heads, sh.n_kv_heads
+    s = Sharded(sh, w, r.x, k)
+    s.forward()
+    dh = to_device(arr["dy"], BF)  # an upstream gradient at the sublayer output
+    dWo, dWqkv, dqkv, dxn32 = s.attention_backward(dh)
+    assert mgb.mgb_device_status() == mgb.MGB_OK
+
+    # the unsplit sublayer backward from the same tensors
+    O_full, lse_full = _attention(sh, s.qkv, nq, nkv, 0, s.Dq, s.Dq + nkv * d, with_lse=True)
+    dWo_full = torch.empty_like(dWo)
+    _gemm(H, s.Dq, T, dh, H, O_full, s.Dq, dWo_full, s.Dq, a_mn=1, b_mn=1)
+    dO_full = torch.empty((T, s.Dq), device="cuda", dtype=BF)
+    _gemm(T, s.Dq, H, dh, H, w["w_o"], s.Dq, dO_full, s.Dq, b_mn=1)
+    dqkv_full = torch.empty_like(dqkv)
+    _attention_bwd(sh, s.qkv, O_full, lse_full, dO_full, dqkv_full, nq, nkv, 0, s.Dq, s.Dq + nkv * d)
+    dWqkv_full = torch.empty_like(dWqkv)
+    _gemm(s.Wqkv, H, T, dqkv_full, s.Wqkv, s.xn, H, dWqkv_full, H, a_mn=1, b_mn=1)
+    dxn_full = torch.empty((T, H), device="cuda", dtype=torch.float32)
+    _gemm(T, H, s.Wqkv, dqkv_full, s.Wqkv, w["w_qkv"], H, dxn_full, H, b_mn=1, epi=mgb.MGB_EPI_F32)
+    assert mgb.mgb_device_status() == mgb.MGB_OK
+    assert torch.equal(dWo, dWo_full)            # row-parallel weight gradient: column slices
+    assert torch.equal(dqkv, dqkv_full)          # per-head attention backward: column slices
+    assert torch.equal(dWqkv, dWqkv_full)        # column-parallel weight gradient: row slices
+    assert rel_l2(to_np(dxn32), to_np(dxn_full)) < 1e-5  # input gradients sum
+
+    # each shard against the oracle's shard backward (from its own float64 forward)
+    tol_g = TOL["bf16"][1]
+    wo = {kk: arr[kk] for kk in w}
+    xn, _, _ = oracle.ln_fwd(arr["x"], arr["ln1_g"], arr["ln1_b"])
+    dxn_o = np.zeros((T, H))
+    for i in range(k):
+        _, c = oracle.shard.attn_partial_fwd(sh, wo, xn, i, k)
+        da, dW, _, dWo_i = oracle.shard.attn_partial_bwd(sh, wo, c, arr["dy"])
+        rows, o_cols = oracle.shard.head_shard(sh, i, k)
+        assert rel_l2(to_np(dWo)[:, o_cols], dWo_i) < tol_g
+        assert rel_l2(to_np(dWqkv)[rows], dW) < tol_g
+        dxn_o += da
+    assert rel_l2(to_np(dxn32), dxn_o) < tol_g
+

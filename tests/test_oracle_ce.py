@@ -113,6 +113,21 @@ def test_rows_match_full():
     np.testing.assert_allclose(dh_r, d_hid[rows], rtol=1e-12)
 
 
+def test_emb_rows_match_full():
+    """Selected rows of demb, including ids that are some token's target (the
+    one-hot term) and ids that are none, equal those rows of ce_grads' demb,
+    which torch autograd pins; dropping the one-hot term is caught."""
+    hid, emb, tg = _case(T=8)
+    _, lse, _ = oracle.ce_full(hid, emb, tg)
+    _, d_emb = oracle.ce_grads(hid, emb, tg, lse, 0.125)
+    ids = np.unique(np.concatenate([tg[:3], [0, emb.shape[0] - 1, 7]]))
+    rows = oracle.ce_emb_rows(hid, emb, tg, lse, 0.125, ids)
+    np.testing.assert_allclose(rows, d_emb[ids], rtol=1e-12, atol=1e-15)
+    l = hid @ emb[ids].T
+    no_onehot = (np.exp(l - lse[:, None]) * 0.125).T @ hid
+    assert np.abs(no_onehot - d_emb[ids]).max() > 1e-3
+
+
 def test_chunk_partials_planted_mistake_is_caught():
     """Combining chunk sums without rescaling to the global max is wrong."""
     hid, emb, tg = _case()

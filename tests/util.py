@@ -19,3 +19,44 @@ def rel_l2(got, ref) -> float:
 # absolute error 1e-3.
 TOL = {"f32": (1e-4, 1e-4), "bf16": (1e-2, 2e-2)}
 CE_LOSS_ABS = 1e-3
+
+
+class Guarded:
+    """Out-of-bounds write detection (compute-sanitizer is not available):
+    tensors placed inside one larger allocation between two guard regions of
+    `guard` bytes filled with a byte pattern. `check()` asserts that no guard
+    byte changed, i.e. no kernel wrote before the start or past the end of any
+    of the tensors handed out. Views start 256-byte aligned (as the library's
+    16-byte rule needs)."""
+
+    PATTERN = 0xA7
+
+    def __init__(self, guard: int = 4096):
+        self.guard = guard
+        self.bufs = []
+
+    def empty(self, shape, dtype, fill=None):
+        es = torch.empty((), dtype=dtype).element_size()
+        n = 1
+        for s in shape:
+            n *= s
+        body = (n * es + 255) // 256 * 256
+        raw = torch.full((self.guard + body + self.guard,), self.PATTERN, dtype=torch.uint8,
+                         device="cuda")
+        view = raw[self.guard:self.guard + n * es].view(dtype).view(*shape)
+        if fill is not None:
+            view.fill_(fill)
+        self.bufs.append((raw, n * es))
+        return view
+
+    def like(self, t: torch.Tensor, fill=None):
+        return self.empty(tuple(t.shape), t.dtype, fill)
+
+    def check(self):
+        torch.cuda.synchronize()
+        for i, (raw, nbytes) in enumerate(self.bufs):
+            head = raw[:self.guard]
+            tail = raw[self.guard + nbytes:]
+            bad_h = int((head != self.PATTERN).sum())
+            bad_t = int((tail != self.PATTERN).sum())
+            assert bad_h == 0 and bad_t == 0, f"buffer {i}: {bad_h} bytes before, {bad_t} after it changed"
