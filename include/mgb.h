@@ -153,7 +153,9 @@ mgb_status mgb_rng_draw(mgb_rng_tracker* t, uint64_t n, mgb_rng_state* out);
 mgb_status mgb_block_dropout_plan(mgb_block_desc* desc, mgb_rng_tracker* t);
 
 /* Sizes in bytes of the `saved` buffer (written by fwd, read by bwd) and of
- * the scratch workspaces of fwd and bwd. Host-only; no device work. */
+ * the scratch workspaces of fwd and bwd (the forward's is 0 for bf16; for
+ * float32 it holds the split operands of the three-TF32 GEMMs, and `ws` of
+ * mgb_block_fwd must then be 256-byte aligned). Host-only; no device work. */
 mgb_status mgb_block_sizes(const mgb_block_desc* desc, size_t* saved_bytes,
                            size_t* fwd_ws_bytes, size_t* bwd_ws_bytes);
 
@@ -275,7 +277,9 @@ typedef enum { MGB_K_MAJOR = 0, MGB_MN_MAJOR = 1 } mgb_major;
  * input/weight gradients are this product with one of the three operand
  * layouts (K/K forward, K/MN input grad, MN/MN weight grad).
  * dtype MGB_BF16: A, B, bias bf16; C bf16 unless c_f32 (then float32).
- * dtype MGB_F32: everything float32. `accumulate` needs c_f32 or MGB_F32. */
+ * dtype MGB_F32: everything float32, on the CUDA cores (FFMA; see
+ * mgb_gemm_f32_tc for the tensor-core form). `accumulate` needs c_f32 or
+ * MGB_F32. */
 typedef struct {
   int32_t m, n, k;
   int32_t a_major, b_major;   /* mgb_major */
@@ -327,6 +331,22 @@ typedef struct {
 mgb_status mgb_gemm_ex(const mgb_gemm_ex_desc* desc, const void* a, const void* b,
                        const void* bias, void* c, void* c2, const void* resid, const void* aux,
                        void* stream);
+
+/* The float32 product of mgb_gemm_ex (desc->g.dtype MGB_F32, the same
+ * operand layouts and epilogues) on the tensor cores [P1 section 2: the
+ * float32 layer's linears]: each operand x is split into hi = x rounded to
+ * TF32 (10 mantissa bits) and lo = x - hi rounded to TF32, and the product is
+ * A_hi B_hi^T + A_hi B_lo^T + A_lo B_hi^T (tcgen05 kind::tf32, float32
+ * accumulation): about float32 accuracy, unlike one TF32 product. The split
+ * operands are written as K-major copies into `ws` (caller-owned, 256-byte
+ * aligned, at least mgb_gemm_f32_tc_ws_bytes(m, n, k) bytes, overwritten).
+ * mgb_block_fwd / mgb_block_bwd with dtype MGB_F32 run their GEMMs this way,
+ * the split copies in their workspaces. Errors as mgb_gemm_ex, plus
+ * MGB_ERR_WORKSPACE_TOO_SMALL. */
+size_t mgb_gemm_f32_tc_ws_bytes(int32_t m, int32_t n, int32_t k);
+mgb_status mgb_gemm_f32_tc(const mgb_gemm_ex_desc* desc, const void* a, const void* b,
+                           const void* bias, void* c, void* c2, const void* resid,
+                           const void* aux, void* ws, size_t ws_bytes, void* stream);
 
 /* LayerNorm over the last dim [P1 section 2, F.layer_norm(x, (hidden,))]:
  * y = gamma*(x-mean)*rstd + beta, biased variance. mean/rstd [rows] f32

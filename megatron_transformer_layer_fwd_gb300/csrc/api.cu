@@ -13,6 +13,7 @@
 #include <stdlib.h>
 #include <string.h>
 
+#include <algorithm>
 #include <memory>
 #include <mutex>
 
@@ -126,7 +127,9 @@ struct Plan {
   // backward workspace
   size_t w_dffn, w_dh, w_dr2, w_du, w_dO, w_dqkv, w_dxn, w_delta, w_cparts, w_lparts, w_fparts;
   size_t w_dz1, w_dz2;  // hidden dropout: the projection's / fc2's branch gradients
+  size_t w_tf32, tf32_bwd;  // float32: split operands of the three-TF32 GEMMs
   size_t bwd;
+  size_t fwd, tf32_fwd;     // forward workspace (float32: the same split scratch)
   int cparts, lparts, fparts;
   bool hdrop;
 };
@@ -254,7 +257,20 @@ void make_plan(const mgb_block_desc* d, Plan* p) {
   p->hdrop = d->hidden_dropout > 0.0f;
   p->w_dz1 = p->hdrop ? take(es * T * p->H) : 0;
   p->w_dz2 = p->hdrop ? take(es * T * p->H) : 0;
+  // float32: the largest split-operand scratch of the layer's GEMMs (the
+  // backward issues its GEMMs in order on one stream, so one region serves)
+  p->tf32_fwd = p->tf32_bwd = 0;
+  if (d->dtype == MGB_F32) {
+    const int Tn = p->T, H = p->H, W = p->W, F = p->F, Dq = p->Dq, Wq = p->Wqkv;
+    const int fwd[4][3] = {{Tn, Wq, H}, {Tn, H, Dq}, {Tn, W, H}, {Tn, H, F}};
+    const int bwd[8][3] = {{H, F, Tn}, {Tn, F, H}, {W, H, Tn}, {Tn, H, W},
+                           {H, Dq, Tn}, {Tn, Dq, H}, {Wq, H, Tn}, {Tn, H, Wq}};
+    for (auto& g : fwd) p->tf32_fwd = std::max(p->tf32_fwd, gemm_tf32_scratch_bytes(g[0], g[1], g[2]));
+    for (auto& g : bwd) p->tf32_bwd = std::max(p->tf32_bwd, gemm_tf32_scratch_bytes(g[0], g[1], g[2]));
+  }
+  p->w_tf32 = p->tf32_bwd ? take(p->tf32_bwd) : 0;
   p->bwd = o;
+  p->fwd = p->tf32_fwd;
 }
 
 mgb_status check_weights(const mgb_block_desc* d, const mgb_block_weights* w) {
@@ -343,7 +359,7 @@ mgb_status mgb_block_sizes(const mgb_block_desc* desc, size_t* saved_bytes, size
   Plan p;
   make_plan(desc, &p);
   if (saved_bytes) *saved_bytes = p.saved;
-  if (fwd_ws_bytes) *fwd_ws_bytes = 0;
+  if (fwd_ws_bytes) *fwd_ws_bytes = p.fwd;
   if (bwd_ws_bytes) *bwd_ws_bytes = p.bwd;
   return MGB_OK;
 }
@@ -351,19 +367,24 @@ mgb_status mgb_block_sizes(const mgb_block_desc* desc, size_t* saved_bytes, size
 mgb_status mgb_block_fwd(const mgb_block_desc* desc, const mgb_block_weights* w, const void* x,
                          void* y, void* saved, size_t saved_bytes, void* ws, size_t ws_bytes,
                          void* stream) {
-  (void)ws; (void)ws_bytes;
   MGB_TRY(validate_desc(desc));
   MGB_TRY(check_weights(desc, w));
   Plan p;
   make_plan(desc, &p);
-  if (!x || !y || !saved) return MGB_ERR_INVALID_ARG;
+  if (!x || !y || !saved || (p.fwd > 0 && !ws)) return MGB_ERR_INVALID_ARG;
   if (!aligned16(x) || !aligned16(y) || !aligned16(saved)) return MGB_ERR_MISALIGNED;
-  if (saved_bytes < p.saved) return MGB_ERR_WORKSPACE_TOO_SMALL;
+  if (ws && (reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return MGB_ERR_MISALIGNED;
+  if (saved_bytes < p.saved || ws_bytes < p.fwd) return MGB_ERR_WORKSPACE_TOO_SMALL;
   MGB_TRY(check_arch());
   if (p.T == 0) return MGB_OK;
   cudaStream_t st = as_stream(stream);
   const int dt = desc->dtype;
   const int T = p.T, H = p.H;
+  // float32: every GEMM runs as three TF32 products with its split operands in ws
+  auto scr = [&](GemmArgs g) {
+    if (dt == MGB_F32) { g.scratch = ws; g.scratch_bytes = p.fwd; }
+    return g;
+  };
   float* mu1 = at<float>(saved, p.s_mu1); float* rs1 = at<float>(saved, p.s_rs1);
   float* mu2 = at<float>(saved, p.s_mu2); float* rs2 = at<float>(saved, p.s_rs2);
   float* lse = at<float>(saved, p.s_lse);
@@ -383,7 +404,7 @@ mgb_status mgb_block_fwd(const mgb_block_desc* desc, const mgb_block_weights* w,
   }
   GemmArgs g = mk_gemm(dt, T, p.Wqkv, H, 0, a_in, H, 0, w->w_qkv, H, EPI_STORE, qkv, p.Wqkv);
   g.bias = w->b_qkv;
-  MGB_TRY(gemm_launch(g, st));
+  MGB_TRY(gemm_launch(scr(g), st));
 
   AttnArgs at_{};
   at_.B = p.B; at_.S = p.S; at_.nq = p.nq; at_.nkv = p.nkv; at_.d = p.d;
@@ -401,7 +422,7 @@ mgb_status mgb_block_fwd(const mgb_block_desc* desc, const mgb_block_weights* w,
   g = mk_gemm(dt, T, H, p.Dq, 0, O, p.Dq, 0, w->w_o, p.Dq, EPI_BIAS_RESID, r1, H);
   g.bias = w->b_o; g.resid = x; g.ldr = H;
   set_hidden_dropout(desc, desc->rng_proj, &g);
-  MGB_TRY(gemm_launch(g, st));
+  MGB_TRY(gemm_launch(scr(g), st));
   const void* f_in;
   if (!p.pre)
     MGB_TRY(layernorm_fwd_launch(T, H, dt, desc->ln_eps, r1, w->ln1_g, w->ln1_b, h, mu1, rs1, st));
@@ -417,13 +438,13 @@ mgb_status mgb_block_fwd(const mgb_block_desc* desc, const mgb_block_weights* w,
   g = mk_gemm(dt, T, p.W, H, 0, f_in, H, 0, w->w_1, H,
               p.swiglu ? EPI_BIAS_SWIGLU : EPI_BIAS_GELU, u, p.W);
   g.bias = w->b_1; g.C2 = a; g.ldc2 = p.F; g.glu_block = desc->glu_block;
-  MGB_TRY(gemm_launch(g, st));
+  MGB_TRY(gemm_launch(scr(g), st));
   // fc2 + residual (Pre: y; Post: r2 then y = LN2(r2))
   void* r2 = p.pre ? y : at<char>(saved, p.s_r2);
   g = mk_gemm(dt, T, H, p.F, 0, a, p.F, 0, w->w_2, p.F, EPI_BIAS_RESID, r2, H);
   g.bias = w->b_2; g.resid = h; g.ldr = H;
   set_hidden_dropout(desc, desc->rng_fc2, &g);
-  MGB_TRY(gemm_launch(g, st));
+  MGB_TRY(gemm_launch(scr(g), st));
   if (!p.pre)
     MGB_TRY(layernorm_fwd_launch(T, H, dt, desc->ln_eps, r2, w->ln2_g, w->ln2_b, y, mu2, rs2, st));
   return MGB_OK;
@@ -456,6 +477,12 @@ mgb_status mgb_block_bwd(const mgb_block_desc* desc, const mgb_block_weights* w,
   LaunchScope stage(PROF_STAGE_BWD, st, 1, false);
   const int dt = desc->dtype;
   const int T = p.T, H = p.H;
+  // float32: every GEMM runs as three TF32 products with its split operands in
+  // the workspace, in order on one stream (one scratch region)
+  auto scr = [&](GemmArgs g) {
+    if (dt == MGB_F32) { g.scratch = at<char>(ws, p.w_tf32); g.scratch_bytes = p.tf32_bwd; }
+    return g;
+  };
   const float* mu1 = at<float>(saved, p.s_mu1); const float* rs1 = at<float>(saved, p.s_rs1);
   const float* mu2 = at<float>(saved, p.s_mu2); const float* rs2 = at<float>(saved, p.s_rs2);
   const float* lse = at<float>(saved, p.s_lse);
@@ -481,7 +508,7 @@ mgb_status mgb_block_bwd(const mgb_block_desc* desc, const mgb_block_weights* w,
   // runs on the caller's stream; each weight gradient and bias column sum is
   // issued on the side stream once its inputs exist there. Only the side
   // stream uses cparts; only the caller's stream uses lparts.
-  SideLane lane(st);
+  SideLane lane(st, nullptr, 0, dt == MGB_F32);
   cudaStream_t s2 = lane.side();
   // gradient at the fc2 residual sum (Pre: dy itself; Post: through LN2)
   const void* dr2 = dy;
@@ -501,14 +528,14 @@ mgb_status mgb_block_bwd(const mgb_block_desc* desc, const mgb_block_weights* w,
   MGB_TRY(lane.fork());
   if (gr->b_2) MGB_TRY(colsum_launch(T, H, dt, dz2, H, gr->b_2, cparts, p.cparts, s2));
   if (gr->w_2)
-    MGB_TRY(gemm_launch(mk_gemm(dt, H, p.F, T, 1, dz2, H, 1, a, p.F, EPI_STORE, gr->w_2, p.F), s2));
+    MGB_TRY(gemm_launch(scr(mk_gemm(dt, H, p.F, T, 1, dz2, H, 1, a, p.F, EPI_STORE, gr->w_2, p.F)), s2));
   const bool fused_db1 = gr->b_1 != nullptr && dt == MGB_BF16;
   {
     GemmArgs g = mk_gemm(dt, T, p.F, H, 0, dz2, H, 1, w->w_2, p.F,
                          p.swiglu ? EPI_DSWIGLU : EPI_DGELU, du, p.W);
     g.aux = u; g.ldaux = p.W; g.glu_block = desc->glu_block;
     if (fused_db1) g.colsum_part = at<float>(ws, p.w_fparts);
-    MGB_TRY(gemm_launch(g, st));
+    MGB_TRY(gemm_launch(scr(g), st));
     if (fused_db1)
       MGB_TRY(colsum_reduce_launch(T > 0 ? p.fparts : 0, p.W, dt, at<float>(ws, p.w_fparts),
                                    gr->b_1, st));
@@ -518,10 +545,10 @@ mgb_status mgb_block_bwd(const mgb_block_desc* desc, const mgb_block_weights* w,
   if (gr->b_1 && !fused_db1)
     MGB_TRY(colsum_launch(T, p.W, dt, du, p.W, gr->b_1, cparts, p.cparts, s2));
   if (gr->w_1)
-    MGB_TRY(gemm_launch(mk_gemm(dt, p.W, H, T, 1, du, p.W, 1, f_in, H, EPI_STORE, gr->w_1, H), s2));
+    MGB_TRY(gemm_launch(scr(mk_gemm(dt, p.W, H, T, 1, du, p.W, 1, f_in, H, EPI_STORE, gr->w_1, H)), s2));
   const void* dr1;
   if (p.pre) {
-    MGB_TRY(gemm_launch(mk_gemm(dt, T, H, p.W, 0, du, p.W, 1, w->w_1, H, EPI_STORE, d_ffn, H), st));
+    MGB_TRY(gemm_launch(scr(mk_gemm(dt, T, H, p.W, 0, du, p.W, 1, w->w_1, H, EPI_STORE, d_ffn, H)), st));
     // dh = dy + LN2_bwd(d hn)
     MGB_TRY(layernorm_bwd_launch(T, H, dt, h, mu2, rs2, w->ln2_g, d_ffn, dy, d_h, gr->ln2_g,
                                  gr->ln2_b, lparts, p.lparts, st));
@@ -530,7 +557,7 @@ mgb_status mgb_block_bwd(const mgb_block_desc* desc, const mgb_block_weights* w,
     // dh = du W1 + dr2 (h feeds fc1 and the fc2 residual), dr1 = LN1_bwd(dh)
     GemmArgs g = mk_gemm(dt, T, H, p.W, 0, du, p.W, 1, w->w_1, H, EPI_BIAS_RESID, d_h, H);
     g.resid = dr2; g.ldr = H;
-    MGB_TRY(gemm_launch(g, st));
+    MGB_TRY(gemm_launch(scr(g), st));
     MGB_TRY(layernorm_bwd_launch(T, H, dt, at<char>(saved, p.s_r1), mu1, rs1, w->ln1_g, d_h,
                                  nullptr, d_ffn, gr->ln1_g, gr->ln1_b, lparts, p.lparts, st));
     dr1 = d_ffn;
@@ -546,8 +573,8 @@ mgb_status mgb_block_bwd(const mgb_block_desc* desc, const mgb_block_weights* w,
   MGB_TRY(lane.fork());
   if (gr->b_o) MGB_TRY(colsum_launch(T, H, dt, dz1, H, gr->b_o, cparts, p.cparts, s2));
   if (gr->w_o)
-    MGB_TRY(gemm_launch(mk_gemm(dt, H, p.Dq, T, 1, dz1, H, 1, O, p.Dq, EPI_STORE, gr->w_o, p.Dq), s2));
-  MGB_TRY(gemm_launch(mk_gemm(dt, T, p.Dq, H, 0, dz1, H, 1, w->w_o, p.Dq, EPI_STORE, dO, p.Dq), st));
+    MGB_TRY(gemm_launch(scr(mk_gemm(dt, H, p.Dq, T, 1, dz1, H, 1, O, p.Dq, EPI_STORE, gr->w_o, p.Dq)), s2));
+  MGB_TRY(gemm_launch(scr(mk_gemm(dt, T, p.Dq, H, 0, dz1, H, 1, w->w_o, p.Dq, EPI_STORE, dO, p.Dq)), st));
   // attention backward into the fused dqkv buffer
   {
     AttnArgs at_{};
@@ -572,16 +599,16 @@ mgb_status mgb_block_bwd(const mgb_block_desc* desc, const mgb_block_weights* w,
   if (gr->b_qkv) MGB_TRY(colsum_launch(T, p.Wqkv, dt, dqkv, p.Wqkv, gr->b_qkv, cparts, p.cparts, s2));
   if (gr->w_qkv)
     MGB_TRY(gemm_launch(
-        mk_gemm(dt, p.Wqkv, H, T, 1, dqkv, p.Wqkv, 1, a_in, H, EPI_STORE, gr->w_qkv, H), s2));
+        scr(mk_gemm(dt, p.Wqkv, H, T, 1, dqkv, p.Wqkv, 1, a_in, H, EPI_STORE, gr->w_qkv, H)), s2));
   if (p.pre) {
-    MGB_TRY(gemm_launch(mk_gemm(dt, T, H, p.Wqkv, 0, dqkv, p.Wqkv, 1, w->w_qkv, H, EPI_STORE, dxn, H),
+    MGB_TRY(gemm_launch(scr(mk_gemm(dt, T, H, p.Wqkv, 0, dqkv, p.Wqkv, 1, w->w_qkv, H, EPI_STORE, dxn, H)),
                         st));
     MGB_TRY(layernorm_bwd_launch(T, H, dt, x, mu1, rs1, w->ln1_g, dxn, dr1, dx, gr->ln1_g, gr->ln1_b,
                                  lparts, p.lparts, st));
   } else {
     GemmArgs g = mk_gemm(dt, T, H, p.Wqkv, 0, dqkv, p.Wqkv, 1, w->w_qkv, H, EPI_BIAS_RESID, dx, H);
     g.resid = dr1; g.ldr = H;
-    MGB_TRY(gemm_launch(g, st));
+    MGB_TRY(gemm_launch(scr(g), st));
   }
   return lane.join();
 }
@@ -906,6 +933,39 @@ mgb_status mgb_gemm_ex(const mgb_gemm_ex_desc* e, const void* a, const void* b, 
   g.glu_block = e->glu_block;
   MGB_TRY(gemm_check(g));
   MGB_TRY(check_arch());
+  return gemm_launch(g, as_stream(stream));
+}
+
+size_t mgb_gemm_f32_tc_ws_bytes(int32_t m, int32_t n, int32_t k) {
+  return gemm_tf32_scratch_bytes(m, n, k);
+}
+
+mgb_status mgb_gemm_f32_tc(const mgb_gemm_ex_desc* e, const void* a, const void* b,
+                           const void* bias, void* c, void* c2, const void* resid, const void* aux,
+                           void* ws, size_t ws_bytes, void* stream) {
+  if (e == nullptr) return MGB_ERR_INVALID_ARG;
+  if (fault_injected()) return MGB_ERR_INVALID_ARG;
+  const mgb_gemm_desc* d = &e->g;
+  if (d->dtype != MGB_F32) return MGB_ERR_INVALID_ARG;
+  if (e->epilogue < MGB_EPI_STORE || e->epilogue > MGB_EPI_F32) return MGB_ERR_INVALID_ARG;
+  if ((d->a_major | d->b_major) & ~1) return MGB_ERR_INVALID_ARG;
+  if (d->accumulate && e->epilogue != MGB_EPI_F32) return MGB_ERR_INVALID_ARG;
+  GemmArgs g = mk_gemm(d->dtype, d->m, d->n, d->k, d->a_major, a, d->lda, d->b_major, b, d->ldb,
+                       e->epilogue, c, d->ldc);
+  g.bias = bias;
+  g.alpha = d->alpha;
+  g.accumulate = d->accumulate;
+  g.C2 = c2; g.ldc2 = e->ldc2;
+  g.resid = resid; g.ldr = e->ldr;
+  g.aux = aux; g.ldaux = e->ldaux;
+  g.glu_block = e->glu_block;
+  MGB_TRY(gemm_check(g));
+  const size_t need = gemm_tf32_scratch_bytes(d->m, d->n, d->k);
+  if (need > 0 && (ws == nullptr || ws_bytes < need)) return MGB_ERR_WORKSPACE_TOO_SMALL;
+  if (need > 0 && (reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return MGB_ERR_MISALIGNED;
+  MGB_TRY(check_arch());
+  g.scratch = ws;
+  g.scratch_bytes = ws_bytes;
   return gemm_launch(g, as_stream(stream));
 }
 

@@ -249,6 +249,16 @@ __device__ __forceinline__ void tc_mma_f16(uint32_t d_tmem, uint64_t a_desc, uin
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
+// D (+)= A B^T with tf32 operands (32-bit containers in shared memory, K
+// steps of 8 elements = 32 bytes) and float32 D, one CTA.
+__device__ __forceinline__ void tc_mma_tf32(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                            uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::tf32 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
 // As tc_mma_f16, with the A operand read from tensor memory at a_tmem (row m
 // of A in TMEM lane m; two bf16 K-elements per 32-bit column, lower index in
 // the low half).
@@ -435,6 +445,16 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int m, int n, int a_mn, in
          | (1u << 10)                    // B format: bf16
          | ((uint32_t)a_mn << 15)        // A major: 0 = K, 1 = MN
          | ((uint32_t)b_mn << 16)        // B major
+         | ((uint32_t)(n >> 3) << 17)    // N / 8
+         | ((uint32_t)(m >> 4) << 24);   // M / 16
+}
+
+// Instruction descriptor for kind::tf32 with tf32 A/B and f32 D, both
+// operands K-major.
+__host__ __device__ constexpr uint32_t idesc_tf32_f32(int m, int n) {
+  return (1u << 4)                       // D format: f32
+         | (2u << 7)                     // A format: tf32
+         | (2u << 10)                    // B format: tf32
          | ((uint32_t)(n >> 3) << 17)    // N / 8
          | ((uint32_t)(m >> 4) << 24);   // M / 16
 }

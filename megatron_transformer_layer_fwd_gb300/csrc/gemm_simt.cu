@@ -2,76 +2,24 @@
 //
 // Same contract as the tensor-core GEMM (internal.h GemmArgs): acc[m][n] =
 // alpha * sum_k A(m,k) B(n,k) with either operand K-major or MN-major, and the
-// same epilogues. TF32 tensor cores are not used: their 10-bit mantissa inputs
-// cannot meet a 1e-4 relative error on float32 layers.
+// same epilogues (f32_epilogue.cuh). gemm_launch sends float32 products to the
+// three-TF32 tensor-core kernel (gemm_tf32.cu) when the caller provides its
+// split-operand scratch, and here otherwise.
 //
 // 64 x 64 output tile per 256-thread block, 4 x 4 outputs per thread, K
 // staged through shared memory 16 at a time.
 #include "common.cuh"
+#include "f32_epilogue.cuh"
 #include "internal.h"
 
 namespace mgb {
 
 mgb_status gemm_tc_launch(const GemmArgs& g, cudaStream_t st);
+mgb_status gemm_tf32_launch(const GemmArgs& g, cudaStream_t st);
 
 namespace {
 
 constexpr int TM = 64, TN = 64, TK = 16;
-
-struct SimtParams {
-  int M, N, K, a_mn, b_mn;
-  const float* A; int64_t lda;
-  const float* B; int64_t ldb;
-  int epi; float alpha;
-  float* C; int64_t ldc;
-  const float* bias;
-  const float* resid; int64_t ldr;
-  float* C2; int64_t ldc2;
-  const float* aux; int64_t ldaux;
-  int glu_block, accumulate;
-};
-
-__device__ __forceinline__ void epi_elem(const SimtParams& p, int m, int n, float acc) {
-  switch (p.epi) {
-    case EPI_STORE:
-    case EPI_F32: {
-      float v = acc + (p.bias ? p.bias[n] : 0.0f);
-      float* c = p.C + (int64_t)m * p.ldc + n;
-      if (p.accumulate) v += *c;
-      *c = v;
-      if (p.C2) p.C2[(int64_t)m * p.ldc2 + n] = v;
-      break;
-    }
-    case EPI_BIAS_GELU: {
-      const float u = acc + (p.bias ? p.bias[n] : 0.0f);
-      p.C[(int64_t)m * p.ldc + n] = u;
-      p.C2[(int64_t)m * p.ldc2 + n] = gelu_erf(u);
-      break;
-    }
-    case EPI_BIAS_SWIGLU:  // u only; the activation is a separate pass
-      p.C[(int64_t)m * p.ldc + n] = acc + (p.bias ? p.bias[n] : 0.0f);
-      break;
-    case EPI_BIAS_RESID:
-      p.C[(int64_t)m * p.ldc + n] =
-          p.resid[(int64_t)m * p.ldr + n] + acc + (p.bias ? p.bias[n] : 0.0f);
-      break;
-    case EPI_DGELU:
-      p.C[(int64_t)m * p.ldc + n] = acc * gelu_erf_grad(p.aux[(int64_t)m * p.ldaux + n]);
-      break;
-    case EPI_DSWIGLU: {
-      const int gb = p.glu_block;
-      const int i = n / gb, cc = n % gb;
-      const int64_t cg = (int64_t)2 * i * gb + cc, cu = cg + gb;
-      const float g = p.aux[(int64_t)m * p.ldaux + cg], u = p.aux[(int64_t)m * p.ldaux + cu];
-      const float s = 1.0f / (1.0f + expf(-g));
-      p.C[(int64_t)m * p.ldc + cg] = acc * u * s * (1.0f + g * (1.0f - s));
-      p.C[(int64_t)m * p.ldc + cu] = acc * g * s;
-      break;
-    }
-    default:
-      break;
-  }
-}
 
 __global__ void __launch_bounds__(256) gemm_simt_kernel(const SimtParams p) {
   __shared__ float As[TK][TM + 4];
@@ -208,23 +156,33 @@ mgb_status gemm_launch(const GemmArgs& g, cudaStream_t st) {
   if (s != MGB_OK) return s;
   if (g.M == 0 || g.N == 0) return MGB_OK;
   if (g.dtype == MGB_BF16) return gemm_tc_launch(g, st);
-  SimtParams p{};
-  p.M = g.M; p.N = g.N; p.K = g.K; p.a_mn = g.a_mn; p.b_mn = g.b_mn;
-  p.A = static_cast<const float*>(g.A); p.lda = g.lda;
-  p.B = static_cast<const float*>(g.B); p.ldb = g.ldb;
-  p.epi = g.epi; p.alpha = g.alpha;
-  p.C = static_cast<float*>(g.C); p.ldc = g.ldc;
-  p.bias = static_cast<const float*>(g.bias);
-  p.resid = static_cast<const float*>(g.resid); p.ldr = g.ldr;
-  p.C2 = static_cast<float*>(g.C2); p.ldc2 = g.ldc2;
-  p.aux = static_cast<const float*>(g.aux); p.ldaux = g.ldaux;
-  p.glu_block = g.glu_block; p.accumulate = g.accumulate;
-  dim3 grid((g.N + TN - 1) / TN, (g.M + TM - 1) / TM);
-  LaunchScope scope(PROF_GEMM_F32, st, g.epi == EPI_BIAS_SWIGLU ? 2 : 1);
-  gemm_simt_kernel<<<grid, 256, 0, st>>>(p);
+  // float32: three TF32 products on the tensor cores when the caller gave the
+  // split operands' scratch, else the FFMA kernel (MGB_F32_SIMT=1 forces it)
+  const char* simt = getenv("MGB_F32_SIMT");
+  if (g.scratch != nullptr && g.K > 0 && !(simt != nullptr && simt[0] == '1')) {
+    s = gemm_tf32_launch(g, st);
+    if (s != MGB_OK) return s;
+  } else {
+    SimtParams p{};
+    p.M = g.M; p.N = g.N; p.K = g.K; p.a_mn = g.a_mn; p.b_mn = g.b_mn;
+    p.A = static_cast<const float*>(g.A); p.lda = g.lda;
+    p.B = static_cast<const float*>(g.B); p.ldb = g.ldb;
+    p.epi = g.epi; p.alpha = g.alpha;
+    p.C = static_cast<float*>(g.C); p.ldc = g.ldc;
+    p.bias = static_cast<const float*>(g.bias);
+    p.resid = static_cast<const float*>(g.resid); p.ldr = g.ldr;
+    p.C2 = static_cast<float*>(g.C2); p.ldc2 = g.ldc2;
+    p.aux = static_cast<const float*>(g.aux); p.ldaux = g.ldaux;
+    p.glu_block = g.glu_block; p.accumulate = g.accumulate;
+    dim3 grid((g.N + TN - 1) / TN, (g.M + TM - 1) / TM);
+    LaunchScope scope(PROF_GEMM_F32, st);
+    gemm_simt_kernel<<<grid, 256, 0, st>>>(p);
+  }
   if (g.epi == EPI_BIAS_SWIGLU) {
+    LaunchScope scope(PROF_GEMM_F32, st);
     const int F = g.N / 2;
-    swiglu_f32_kernel<<<1024, 256, 0, st>>>(g.M, F, g.glu_block, p.C, g.ldc, p.C2, g.ldc2);
+    swiglu_f32_kernel<<<1024, 256, 0, st>>>(g.M, F, g.glu_block, static_cast<const float*>(g.C),
+                                            g.ldc, static_cast<float*>(g.C2), g.ldc2);
   }
   return cudaGetLastError() == cudaSuccess ? MGB_OK : MGB_ERR_CUDA;
 }

@@ -81,7 +81,14 @@ struct GemmArgs {
   // numbered from c * ceil(n_chunk / 128) (the same planes as one launch per
   // chunk); tgt_v0 must be 0 (targets are global columns)
   int n_chunk = 0;
+  // dtype MGB_F32, may be null: scratch (256-byte aligned, at least
+  // gemm_tf32_scratch_bytes(M, N, K)) for the hi / lo split copies of the
+  // operands; with it the product runs as three TF32 tensor-core products
+  void* scratch = nullptr;
+  size_t scratch_bytes = 0;
 };
+// Scratch bytes of the three-TF32 float32 GEMM of an M x N x K product.
+size_t gemm_tf32_scratch_bytes(int M, int N, int K);
 
 // A library-owned side stream per (host thread, device, slot) for work off a
 // call's critical path (slot 0: weight and bias gradients; slot 1: the
@@ -99,8 +106,10 @@ struct GemmArgs {
 // work on the caller's stream (serial order; for timing comparisons).
 class SideLane {
  public:
-  explicit SideLane(cudaStream_t main, cudaStream_t external = nullptr, int slot = 0)
+  explicit SideLane(cudaStream_t main, cudaStream_t external = nullptr, int slot = 0,
+                    bool serial = false)
       : main_(main), side_(main), ev_(nullptr) {
+    if (serial && external == nullptr) return;  // side work on the caller's stream
     struct PerDevice {
       cudaStream_t side = nullptr;
       cudaEvent_t ev[kEvents] = {};

@@ -115,6 +115,7 @@ def load() -> ctypes.CDLL:
             "mgb_vocab_ce_fwd_bwd": [ctypes.POINTER(CEDesc), P, P, P, P, P, P, P, P, P, SZ, P],
             "mgb_gemm": [ctypes.POINTER(GemmDesc), P, P, P, P, P],
             "mgb_gemm_ex": [ctypes.POINTER(GemmExDesc), P, P, P, P, P, P, P, P],
+            "mgb_gemm_f32_tc": [ctypes.POINTER(GemmExDesc), P, P, P, P, P, P, P, P, SZ, P],
             "mgb_layernorm_fwd": [I32, I32, I32, F32, P, P, P, P, P, P, P],
             "mgb_layernorm_bwd": [I32, I32, I32, P, P, P, P, P, P, P, P, P, P, SZ, P],
             "mgb_layernorm_bwd_noalloc": [I32, I32, I32, P, P, P, P, P, P, P, P, P, P],
@@ -147,6 +148,8 @@ def load() -> ctypes.CDLL:
         lib.mgb_layernorm_bwd_ws_bytes.restype = SZ
         lib.mgb_attention_bwd_ws_bytes.argtypes = [I32, I32, I32]
         lib.mgb_attention_bwd_ws_bytes.restype = SZ
+        lib.mgb_gemm_f32_tc_ws_bytes.argtypes = [I32, I32, I32]
+        lib.mgb_gemm_f32_tc_ws_bytes.restype = SZ
         lib.mgb_embedding_bwd_ws_bytes.argtypes = [I32, I32, I32]
         lib.mgb_embedding_bwd_ws_bytes.restype = SZ
         lib.mgb_launch_count.argtypes = []
@@ -267,6 +270,18 @@ def mgb_gemm(desc: GemmDesc, a, b, bias, c, stream=None) -> None:
 def mgb_gemm_ex(desc: GemmExDesc, a, b, bias, c, c2=None, resid=None, aux=None, stream=None) -> None:
     _check(load().mgb_gemm_ex(ctypes.byref(desc), _ptr(a), _ptr(b), _ptr(bias), _ptr(c), _ptr(c2),
                               _ptr(resid), _ptr(aux), _stream(stream)), "mgb_gemm_ex")
+
+
+def mgb_gemm_f32_tc_ws_bytes(m: int, n: int, k: int) -> int:
+    return int(load().mgb_gemm_f32_tc_ws_bytes(m, n, k))
+
+
+def mgb_gemm_f32_tc(desc: GemmExDesc, a, b, bias, c, c2=None, resid=None, aux=None, ws=None,
+                    stream=None) -> None:
+    ws_bytes = ws.numel() * ws.element_size() if ws is not None else 0
+    _check(load().mgb_gemm_f32_tc(ctypes.byref(desc), _ptr(a), _ptr(b), _ptr(bias), _ptr(c),
+                                  _ptr(c2), _ptr(resid), _ptr(aux), _ptr(ws), ws_bytes,
+                                  _stream(stream)), "mgb_gemm_f32_tc")
 
 
 def rng_tracker(seed: int, tp_rank: int = 0, ep_rank: int = 0, etp_rank: int = 0) -> RngTracker:

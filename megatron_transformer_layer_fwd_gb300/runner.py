@@ -34,15 +34,17 @@ class LayerRunner:
         self.w = {k: (to_device(arrays[k], self.dtype, device) if arrays.get(k) is not None else None)
                   for k in WEIGHT_KEYS}
         self.x = to_device(arrays["x"], self.dtype, device)
-        saved, _, bwd = mgb.mgb_block_sizes(self.desc)
+        saved, fwd, bwd = mgb.mgb_block_sizes(self.desc)
         self.saved = torch.empty(max(saved, 16), dtype=torch.uint8, device=device)
         self.ws = torch.empty(max(bwd, 16), dtype=torch.uint8, device=device)
+        # float32: the forward's GEMMs keep their split operands here
+        self.fwd_ws = torch.empty(fwd, dtype=torch.uint8, device=device) if fwd > 0 else None
         self.y = torch.empty_like(self.x)
         self.dx = torch.empty_like(self.x)
         self.grads = {k: (torch.empty_like(v) if v is not None else None) for k, v in self.w.items()}
 
     def fwd(self, stream=None):
-        mgb.mgb_block_fwd(self.desc, self.w, self.x, self.y, self.saved, None, stream)
+        mgb.mgb_block_fwd(self.desc, self.w, self.x, self.y, self.saved, self.fwd_ws, stream)
         return self.y
 
     def bwd(self, dy: torch.Tensor, stream=None):

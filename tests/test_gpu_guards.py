@@ -137,13 +137,14 @@ def test_layer_stays_in_bounds(mgb_lib, shape):
     w = {k: (to_device(arr[k], td) if arr.get(k) is not None else None) for k in WEIGHT_KEYS}
     x = to_device(arr["x"], td)
     dy = to_device(arr["dy"], td)
-    saved_b, _, bwd_b = mgb.mgb_block_sizes(desc)
+    saved_b, fwd_b, bwd_b = mgb.mgb_block_sizes(desc)
     g = Guarded()
     saved = g.empty((saved_b,), torch.uint8)
+    fws = g.empty((fwd_b,), torch.uint8) if fwd_b > 0 else None  # float32: split operands
     ws = g.empty((max(bwd_b, 16),), torch.uint8)
     y, dx = g.like(x), g.like(x)
     grads = {k: (g.like(v) if v is not None else None) for k, v in w.items()}
-    mgb.mgb_block_fwd(desc, w, x, y, saved)
+    mgb.mgb_block_fwd(desc, w, x, y, saved, fws)
     mgb.mgb_block_bwd(desc, w, x, dy, saved, dx, grads, ws)
     assert mgb.mgb_device_status() == mgb.MGB_OK
     g.check()
@@ -161,3 +162,22 @@ def test_embedding_stays_in_bounds(mgb_lib):
     mgb.mgb_embedding_bwd(T, H, v0, v1, mgb.MGB_BF16, ids, _rand((T, H)), d_emb, 0, ws)
     assert mgb.mgb_device_status() == mgb.MGB_OK
     g.check()
+
+
+@pytest.mark.parametrize("epi", [mgb.MGB_EPI_STORE, mgb.MGB_EPI_F32, mgb.MGB_EPI_BIAS_RESID])
+def test_gemm_f32_tc_stays_in_bounds(mgb_lib, epi):
+    """The three-TF32 float32 GEMM: output and the split-operand scratch."""
+    M, N, K = 200, 136, 70
+    g = Guarded()
+    a = _rand((K, M), torch.float32)
+    b = _rand((N, K), torch.float32)
+    c = g.empty((M, N), torch.float32, fill=0.0)
+    ws = g.empty((mgb.mgb_gemm_f32_tc_ws_bytes(M, N, K),), torch.uint8)
+    d = mgb.GemmExDesc(g=mgb.GemmDesc(m=M, n=N, k=K, a_major=1, b_major=0, lda=M, ldb=K, ldc=N,
+                                      dtype=mgb.MGB_F32, c_f32=0, accumulate=0, alpha=1.0),
+                       epilogue=epi, glu_block=64, ldc2=N, ldr=N, ldaux=N)
+    resid = _rand((M, N), torch.float32) if epi == mgb.MGB_EPI_BIAS_RESID else None
+    mgb.mgb_gemm_f32_tc(d, a, b, None, c, resid=resid, ws=ws)
+    assert mgb.mgb_device_status() == mgb.MGB_OK
+    g.check()
+

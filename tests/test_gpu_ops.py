@@ -63,6 +63,76 @@ def test_gemm_bf16_bias_out_and_accumulate(mgb_lib, monkeypatch, pair, M, N, K):
     assert mgb.mgb_device_status() == mgb.MGB_OK
 
 
+def _f32(shape, scale=1.0):
+    return (RNG.standard_normal(shape) * scale).astype(np.float32).astype(np.float64)
+
+
+@pytest.mark.parametrize("a_mn,b_mn", [(0, 0), (0, 1), (1, 1), (1, 0)])
+@pytest.mark.parametrize("M,N,K", [(128, 128, 32), (200, 136, 70), (300, 520, 1000)])
+def test_gemm_f32_tc_layouts(mgb_lib, a_mn, b_mn, M, N, K):
+    """The float32 product as three TF32 tensor-core products (hi/lo operand
+    splits): every operand layout, ragged M, N and K (K not a multiple of the
+    32-wide K block nor of 4), against the float64 product of the same float32
+    operands: about 7e-6 at K = 1000, set by the tensor core's float32
+    accumulation (the bf16 tests above allow 1e-5 at that K); one TF32 product
+    would give about 1e-3."""
+    A, B = _f32((M, K)), _f32((N, K))
+    a_st = A.T.copy() if a_mn else A
+    b_st = B.T.copy() if b_mn else B
+    c = torch.full((M, N), float("nan"), device="cuda", dtype=torch.float32)
+    ws = torch.empty(mgb.mgb_gemm_f32_tc_ws_bytes(M, N, K), dtype=torch.uint8, device="cuda")
+    d = mgb.GemmExDesc(g=mgb.GemmDesc(m=M, n=N, k=K, a_major=a_mn, b_major=b_mn, lda=a_st.shape[1],
+                                      ldb=b_st.shape[1], ldc=N, dtype=mgb.MGB_F32, c_f32=0,
+                                      accumulate=0, alpha=1.0),
+                       epilogue=mgb.MGB_EPI_STORE, glu_block=16, ldc2=0, ldr=0, ldaux=0)
+    mgb.mgb_gemm_f32_tc(d, _dev(a_st, torch.float32), _dev(b_st, torch.float32), None, c, ws=ws)
+    assert mgb.mgb_device_status() == mgb.MGB_OK
+    err = rel_l2(to_np(c), A @ B.T)
+    assert err < 1.5e-5, err
+
+
+@pytest.mark.parametrize("epi", [mgb.MGB_EPI_BIAS_GELU, mgb.MGB_EPI_BIAS_SWIGLU, mgb.MGB_EPI_BIAS_RESID,
+                                 mgb.MGB_EPI_DGELU, mgb.MGB_EPI_DSWIGLU, mgb.MGB_EPI_F32])
+def test_gemm_f32_tc_epilogues(mgb_lib, epi):
+    """The layer's fused epilogues on the three-TF32 product equal the same
+    epilogues on the FFMA product (both float32) to float32 rounding."""
+    M, N, K = 130, 96, 72
+    gb = 16
+    A, B, bias = _f32((M, K)), _f32((N, K)), _f32((N,), 0.1)
+    w_out = {mgb.MGB_EPI_DSWIGLU: 2 * N}.get(epi, N)
+    aux = _f32((M, 2 * N if epi == mgb.MGB_EPI_DSWIGLU else N))
+    resid = _f32((M, N))
+    outs = []
+    for tc in (True, False):
+        c = torch.zeros((M, w_out), device="cuda", dtype=torch.float32)
+        if epi == mgb.MGB_EPI_F32:
+            c.copy_(_dev(resid, torch.float32))
+        c2 = torch.zeros((M, N // 2 if epi == mgb.MGB_EPI_BIAS_SWIGLU else N), device="cuda",
+                         dtype=torch.float32)
+        d = mgb.GemmExDesc(g=mgb.GemmDesc(m=M, n=N, k=K, a_major=0, b_major=0, lda=K, ldb=K,
+                                          ldc=w_out, dtype=mgb.MGB_F32, c_f32=0,
+                                          accumulate=int(epi == mgb.MGB_EPI_F32), alpha=1.0),
+                           epilogue=epi, glu_block=gb, ldc2=c2.shape[1], ldr=N, ldaux=aux.shape[1])
+        has_bias = epi in (mgb.MGB_EPI_BIAS_GELU, mgb.MGB_EPI_BIAS_SWIGLU, mgb.MGB_EPI_BIAS_RESID,
+                           mgb.MGB_EPI_F32)
+        args = (d, _dev(A, torch.float32), _dev(B, torch.float32),
+                _dev(bias, torch.float32) if has_bias else None, c)
+        kw = dict(c2=c2 if epi in (mgb.MGB_EPI_BIAS_GELU, mgb.MGB_EPI_BIAS_SWIGLU) else None,
+                  resid=_dev(resid, torch.float32) if epi == mgb.MGB_EPI_BIAS_RESID else None,
+                  aux=_dev(aux, torch.float32) if epi in (mgb.MGB_EPI_DGELU, mgb.MGB_EPI_DSWIGLU)
+                  else None)
+        if tc:
+            ws = torch.empty(mgb.mgb_gemm_f32_tc_ws_bytes(M, N, K), dtype=torch.uint8, device="cuda")
+            mgb.mgb_gemm_f32_tc(*args, ws=ws, **kw)
+        else:
+            mgb.mgb_gemm_ex(*args, **kw)
+        outs.append((to_np(c), to_np(c2)))
+    assert mgb.mgb_device_status() == mgb.MGB_OK
+    assert rel_l2(outs[0][0], outs[1][0]) < 1e-5
+    if epi in (mgb.MGB_EPI_BIAS_GELU, mgb.MGB_EPI_BIAS_SWIGLU):
+        assert rel_l2(outs[0][1], outs[1][1]) < 1e-5
+
+
 @pytest.mark.parametrize("a_mn,b_mn", [(0, 0), (0, 1), (1, 1)])
 def test_gemm_pair_tiles_many_waves(mgb_lib, a_mn, b_mn):
     """Large enough for the CTA-pair tile to be chosen by itself, with more
