@@ -35,9 +35,9 @@ import numpy as np
 ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
-from megatron_transformer_layer_fwd_gb300.inputs import (CE_WORKLOADS, WORKLOADS, ce_flops,  # noqa: E402
-                                                         ce_inputs, ce_stream_bytes, layer_flops,
-                                                         layer_inputs)
+from megatron_transformer_layer_fwd_gb300.inputs import (CE_WORKLOADS, WORKLOADS, CEShape,  # noqa: E402
+                                                         ce_flops, ce_inputs, ce_stream_bytes,
+                                                         layer_flops, layer_inputs)
 
 METRIC = "layer fwd+bwd TFLOP/s and tokens/s (bf16) + vocab-CE GB/s, % of roofline"
 LAYER = "bf16_gqa_swiglu_b2s4096h4096"
@@ -298,57 +298,84 @@ def run_ours(args, world, rank, local):
     torch.cuda.synchronize(dev)
     layer_ms = max_over_ranks(world, l0.elapsed_time(l1) / args.steps)
 
-    # ---- end to end through host buffers
+    # ---- end to end through host buffers: every step copies x and the
+    # targets from pinned host memory with the library's copy call and reads
+    # the mean loss back; device-only steps are interleaved with them (each
+    # step between its own events), so that clock drift under the power cap
+    # falls on both alike and the difference is the copies' cost
     x_host = layer.x.cpu().pin_memory()
     t_host = targets.cpu().pin_memory()
     loss_host = torch.empty(1, dtype=torch.float32).pin_memory()
-    e2e_steps = max(3, args.steps // 2)
+    h2d = layer.x.numel() * layer.x.element_size() + targets.numel() * 4
+
+    def e2e_step():
+        mgb.mgb_memcpy_async(layer.x, x_host, layer.x.numel() * layer.x.element_size(), stream)
+        mgb.mgb_memcpy_async(targets, t_host, targets.numel() * 4, stream)
+        step()
+        mgb.mgb_memcpy_async(loss_host, cer.loss_mean, 4, stream)
+
     barrier(world)
     torch.cuda.synchronize(dev)
-    h0, h1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    h0.record(stream)
-    for _ in range(e2e_steps):
-        layer.x.copy_(x_host, non_blocking=True)
-        targets.copy_(t_host, non_blocking=True)
-        step()
-        loss_host.copy_(cer.loss_mean[:1], non_blocking=True)
-    h1.record(stream)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(2 * args.steps)]
+    for i, (a, b) in enumerate(ev):
+        a.record(stream)
+        (e2e_step if i % 2 == 0 else step)()
+        b.record(stream)
     torch.cuda.synchronize(dev)
-    e2e_ms = max_over_ranks(world, h0.elapsed_time(h1) / e2e_steps)
+    e2e_times = [a.elapsed_time(b) for a, b in ev[0::2]]
+    dev_times = [a.elapsed_time(b) for a, b in ev[1::2]]
+    e2e_ms = max_over_ranks(world, statistics.median(e2e_times))
+    dev_inter_ms = max_over_ranks(world, statistics.median(dev_times))
 
     lf, cf = layer_flops(shape), ce_flops(ce)
     step_flops = lf["total"] + cf["total"]
     value = world * step_flops / (ms / 1e3) / 1e12
     peaks = load_peaks()
     tb = cer.token_block
-    # Dominant kernel: of the CE's three GEMM kinds (logits with the statistics
-    # epilogue; G E split over K; G^T hidden accumulated across token blocks),
-    # each 2*T*V*H FLOPs per step, the one with the most device time. Its
-    # algorithmic FLOPs per launch / its mean launch time from the live events.
-    kinds = {"gemm_tc_ce_logits": f"CE logits, per token block and vocab chunk "
-                                  f"{tb}x{ce.chunk}x{ce.hidden} (K/K, statistics epilogue storing "
-                                  "the block's logits)",
-             "gemm_tc_ce_dgrad": f"CE d_hidden = G E per token block, {tb}x{ce.hidden}x{ce.vocab} "
-                                 "(K/MN, split over K into float32 planes)",
-             "gemm_tc_ce_wgrad": f"CE d_emb += G^T hidden per token block, "
-                                 f"{ce.vocab}x{ce.hidden}x{tb} (MN/MN, float32 accumulate)"}
-    dom = max(kinds, key=lambda k: prof.get(k, (0.0, 0))[0])
-    d_ms, d_n = prof[dom]
-    d_flops = 2.0 * ce.tokens * ce.vocab * ce.hidden * args.steps / d_n if d_n else 0.0
+    # Dominant kernel: the CE logits GEMM (per token block, every vocab chunk
+    # in one launch, statistics epilogue storing the block's logits), the
+    # longest kernel of the step that runs alone on its stream (the two CE
+    # gradient products run side by side and are timed as one phase below).
+    # Algorithmic FLOPs per launch (2*rows*V*H) / mean launch time from the
+    # library's events on the launching stream inside the timed region.
+    ce_kind_flops = 2.0 * ce.tokens * ce.vocab * ce.hidden  # per kind per step
+    d_ms, d_n = prof["gemm_tc_ce_logits"]
+    d_flops = ce_kind_flops * args.steps / d_n if d_n else 0.0
     d_tflops = d_flops / (d_ms / d_n / 1e3) / 1e12 if d_n else None
     traffic = traffic_record(os.path.join(ROOT, "megatron_transformer_layer_fwd_gb300", "csrc",
-                                          "gemm_tc.cu"), dom)
-    roofline = {"kernel": f"{dom}: {kinds[dom]}",
+                                          "gemm_tc.cu"), "gemm_tc_ce_logits")
+    roofline = {"kernel": f"gemm_tc_pair_kernel, CE logits per token block {tb}x{ce.vocab}x"
+                          f"{ce.hidden} (all vocab chunks of {ce.chunk} in one launch; statistics "
+                          "epilogue storing the block's bf16 logits)",
                 "bound": "tensor", "achieved": round(d_tflops, 1) if d_tflops else None,
                 "peak": peaks["bf16_tflops_sustained"], "unit": "TFLOP/s",
                 "frac": round(d_tflops / peaks["bf16_tflops_sustained"], 4) if d_tflops else None,
                 "peak_source": f"{peaks['source']} bf16_tflops_sustained (kernel inside a long step)",
                 "flops_per_launch": d_flops, "launches_per_step": d_n / args.steps,
                 "avg_launch_ms": round(d_ms / d_n, 4) if d_n else None,
-                "traffic": traffic,
-                "per_kind_tflops": {k: round(2.0 * ce.tokens * ce.vocab * ce.hidden * args.steps
-                                             / (prof[k][0] / 1e3) / 1e12, 1)
-                                    for k in kinds if prof.get(k, (0, 0))[0] > 0}}
+                "traffic": traffic}
+    # the block's d_hidden (split-K) and d_emb (float32 reduce-add) products,
+    # side by side: FLOPs of both / the phase from fork to join
+    p_ms, p_n = prof.get("stage_ce_products", (0.0, 0))
+    roofline_ce_products = {
+        "kernel": "gemm_tc_ce_dgrad (G E, split over K) beside gemm_tc_ce_wgrad (G^T hidden, "
+                  "float32 TMA reduce-add) per token block, fork to join",
+        "bound": "tensor", "unit": "TFLOP/s", "peak": peaks["bf16_tflops_sustained"],
+        "phases_per_step": p_n / args.steps,
+        "avg_phase_ms": round(p_ms / p_n, 4) if p_n else None,
+        "note": "the last block's d_emb runs on the caller's stream beside the layer backward "
+                "and is not inside its phase"}
+    if p_n:
+        # the phases cover both products of every block but the last one's
+        # d_emb: flops = 2 kinds x per-block share for blocks before the last,
+        # d_hidden only for the last
+        nb = p_n // args.steps
+        per_block = ce_kind_flops / nb
+        fl = (2 * (nb - 1) + 1) * per_block * args.steps
+        roofline_ce_products["achieved"] = round(fl / (p_ms / 1e3) / 1e12, 1)
+        roofline_ce_products["frac"] = round(roofline_ce_products["achieved"] /
+                                             peaks["bf16_tflops_sustained"], 4)
     # all tcgen05 GEMM work of the step (2MNK each, none recomputed)
     gemm_flops_step = 3 * lf["gemm_fwd"] + 3 * 2.0 * ce.tokens * ce.vocab * ce.hidden
     gemm_kinds = ("gemm_tc_fwd", "gemm_tc_dgrad", "gemm_tc_wgrad", "gemm_tc_ce_logits",
@@ -385,7 +412,6 @@ def run_ours(args, world, rank, local):
     r1.record(stream)
     torch.cuda.synchronize(dev)
     res_ms = r0.elapsed_time(r1) / r_steps
-    del res
     step_resident = {"ms_per_step": round(res_ms, 4),
                      "tflops": round(world * step_flops / (res_ms / 1e3) / 1e12, 2),
                      "ce_workspace_gb": round(mgb.mgb_vocab_ce_sizes(mgb.ce_desc(
@@ -393,8 +419,11 @@ def run_ours(args, world, rank, local):
                          mgb.MGB_CE_RESIDENT)) / 1e9, 3),
                      "note": "same step with MGB_CE_RESIDENT (whole [T, V] logits kept); "
                              "outside the pages' memory bound, for comparison only"}
-    layer_kinds = ("attn_fwd", "attn_bwd", "layernorm_fwd", "layernorm_bwd", "colsum")
     breakdown = {k: round(v[0] / args.steps, 4) for k, v in prof.items() if v[1] > 0}
+    # page 1's sequence sweep on the causal workloads (B 8, H 2048, 16 x 128, F
+    # 8192): the Attention / FFN / Backward stages per length (library events)
+    del res
+    sweep = None if args.no_sweep else stage_sweep(stream)
     out = {
         "metric": METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 4),
@@ -415,21 +444,62 @@ def run_ours(args, world, rank, local):
         "clocks": clk,
         "e2e": {"value": round(world * step_flops / (e2e_ms / 1e3) / 1e12, 2), "unit": "TFLOP/s",
                 "ms_per_step": round(e2e_ms, 4),
-                "h2d_bytes_per_step": layer.x.numel() * layer.x.element_size() + targets.numel() * 4,
-                "d2h_bytes_per_step": 4},
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": 4,
+                "how": "median of steps that copy x and the targets from pinned host memory "
+                       "(mgb_memcpy_async) and read the mean loss back, interleaved with "
+                       "device-only steps",
+                "device_only_interleaved_ms": round(dev_inter_ms, 4),
+                "copy_overhead_ms": round(e2e_ms - dev_inter_ms, 4)},
         "gpu_launches": int(launches),
         "roofline": roofline,
+        "roofline_ce_products": roofline_ce_products,
         "roofline_ce": roofline_ce,
         "ce": {"mode": "MGB_CE_BLOCKED", "token_block": tb,
                "workspace_gb": round(cer.ws.numel() / 1e9, 3),
                "full_logits_gb": round(2.0 * ce.tokens * ce.vocab / 1e9, 3)},
         "step_resident_ce": step_resident,
+        "seq_sweep": sweep,
         "gemm_all_launches": gemm_all,
         "kernel_ms_per_step": breakdown,
         "kernel_ms_note": "per kind, the span between library CUDA events on the launching "
                           "stream; kernels on the side streams run beside others, so the spans "
                           "overlap and do not add up to ms_per_step",
     }
+    return out
+
+
+def stage_sweep(stream, steps: int = 5, warmup: int = 3) -> dict:
+    """Layer fwd+bwd on the causal workloads at S = 128 ... 2048 (batch 8):
+    per length the whole layer and page 1's three stages (Attention: LN1, QKV,
+    attention, projection; FFN: LN2, fc1, fc2; Backward), and the growth per
+    doubling of S against the work's (attention core 4x, FFN 2x)."""
+    import torch
+    from megatron_transformer_layer_fwd_gb300.runner import LayerRunner
+    out = {"workloads": "bf16_causal_b8s{S}h2048", "seq": [], "layer_ms": [],
+           "stage_ms": {"attention": [], "ffn": [], "backward": []}, "attention_core_ms": []}
+    for seq in (128, 256, 512, 1024, 2048):
+        shape = WORKLOADS[f"bf16_causal_b8s{seq}h2048"]
+        r = LayerRunner(shape, layer_inputs(shape, seed=0))
+        dy = torch.full_like(r.x, 1.0 / (shape.tokens * shape.hidden))
+
+        def fb():
+            r.fwd(stream)
+            r.bwd(dy, stream)
+        ms, prof = _time_loop(fb, steps, warmup, stream)
+        out["seq"].append(seq)
+        out["layer_ms"].append(round(ms, 4))
+        for k in ("attention", "ffn", "backward"):
+            out["stage_ms"][k].append(prof.get("stage_" + k, 0))
+        out["attention_core_ms"].append(round(prof.get("attn_fwd", 0) + prof.get("attn_bwd", 0), 4))
+        del r, dy
+
+    def growth(v):
+        return [round(b / a, 3) for a, b in zip(v, v[1:]) if a > 0]
+    out["growth_per_doubling"] = {"stage_attention": growth(out["stage_ms"]["attention"]),
+                                  "stage_ffn": growth(out["stage_ms"]["ffn"]),
+                                  "stage_backward": growth(out["stage_ms"]["backward"]),
+                                  "attention_core": growth(out["attention_core_ms"])}
+    out["work_growth_per_doubling"] = {"attention_core": 4.0, "ffn": 2.0}
     return out
 
 
@@ -643,6 +713,10 @@ def run_case(args):
         return
     if args.case == "ce":
         ce = CE_WORKLOADS[CE]
+        if args.ce_shape:
+            # a smaller case of the same kernels (for counter captures)
+            T_, H_, V_, C_ = (int(v) for v in args.ce_shape.split(","))
+            ce = CEShape(T_, H_, V_, C_)
         cin = ce_inputs(ce, seed=0)
         hid = to_device(cin["hidden"], torch.bfloat16)
         emb = to_device(cin["emb"], torch.bfloat16)
@@ -683,6 +757,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-sweep", action="store_true",
+                    help="skip the sequence sweep of the causal workloads in the step run")
     ap.add_argument("--case", default="step",
                     choices=("step", "layer", "sweep", "ce", "gemm", "gemm_layer", "attention",
                              "embedding"),
@@ -693,6 +769,8 @@ def main():
     ap.add_argument("--ce-mode", default="all",
                     choices=("all", "stream", "fused", "resident", "blocked"),
                     help="--case ce: which CE mode(s) to time")
+    ap.add_argument("--ce-shape", default="",
+                    help="--case ce: tokens,hidden,vocab,chunk instead of the CE workload's")
     ap.add_argument("--token-block", type=int, default=0,
                     help="tokens per block of the blocked CE (0: the library's default)")
     args = ap.parse_args()

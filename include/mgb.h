@@ -477,6 +477,12 @@ mgb_status mgb_philox_bytes(uint64_t seed, uint64_t offset, uint64_t n, void* ou
 mgb_status mgb_dropout(int64_t rows, int64_t cols, int32_t dtype, float p, mgb_rng_state rng,
                        const void* x, int64_t ldx, void* y, int64_t ldy, void* stream);
 
+/* Copies `bytes` from src to dst on `stream` (asynchronous; host pointers
+ * must be pinned for the copy to overlap other work): how inputs in host
+ * memory (a token batch, targets) reach the device buffers the calls above
+ * take, and results (a loss) come back. No counterpart on the pages. */
+mgb_status mgb_memcpy_async(void* dst, const void* src, size_t bytes, void* stream);
+
 /* Synchronises `stream`, then returns and clears the current device's error
  * word (MGB_ERR_DEVICE_TIMEOUT if a bounded device wait ran out since the last
  * call, else MGB_OK), or MGB_ERR_CUDA if the synchronisation failed. */

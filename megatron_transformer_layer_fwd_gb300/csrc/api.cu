@@ -344,6 +344,14 @@ mgb_status mgb_device_status(void* stream) {
   return (w & kErrTimeout) ? MGB_ERR_DEVICE_TIMEOUT : MGB_OK;
 }
 
+mgb_status mgb_memcpy_async(void* dst, const void* src, size_t bytes, void* stream) {
+  if (bytes == 0) return MGB_OK;
+  if (dst == nullptr || src == nullptr) return MGB_ERR_INVALID_ARG;
+  return cudaMemcpyAsync(dst, src, bytes, cudaMemcpyDefault, as_stream(stream)) == cudaSuccess
+             ? MGB_OK
+             : MGB_ERR_CUDA;
+}
+
 mgb_status mgb_selftest_wait_timeout(uint64_t limit_ns, void* stream) {
   if (limit_ns > 5000000000ull) return MGB_ERR_INVALID_ARG;
   MGB_TRY(check_arch());
@@ -740,6 +748,8 @@ static mgb_status ce_blocked(const mgb_ce_desc* desc, const CEPlan& p, const voi
     // ---- backward of the block: G in place, then its two products
     MGB_TRY(ce_grad_launch(rows, V, 0, logits, V, targets + r0, lse_buf + r0, desc->grad_scale,
                            st));
+    // (destroyed after the lane below: ends once the side stream is joined)
+    LaunchScope products(PROF_STAGE_CE_PRODUCTS, st, 1, false);
     SideLane lane(st, last ? as_stream(desc->emb_stream) : nullptr);
     if (d_emb) {
       MGB_TRY(lane.fork());

@@ -1041,12 +1041,31 @@ void set_tiles_n(EpiParams& ep, int N, int bn) {
   }
 }
 
+// Row tiles per raster group. Tiles are visited group by group, the row tile
+// advancing fastest inside a group, so a group's A rows stay in L2 while its
+// B columns stream past. With the K range of one split (kb_per_split blocks):
+// if all of B fits comfortably in L2 (e.g. a weight gradient's short token
+// panel), one row tile per group reads every A panel once and keeps B
+// resident; if all of A fits, one group of all rows reads B once; otherwise
+// groups of about 48 MB of A rows.
+int raster_group(const EpiParams& ep, int M, int N, int bm, int min_g, int max_g) {
+  const long k_eff = (long)ep.kb_per_split * BK;
+  const long fits = 40L << 20;
+  if ((long)N * k_eff * 2 <= fits) return 1;
+  if ((long)M * k_eff * 2 <= fits) return ep.tiles_m;
+  // split-K with few row tiles: each wave spans every row tile and the
+  // fewest column tiles, so the concurrent tiles (which walk their K range
+  // together) share the most A and B slices in L2
+  if (ep.k_splits > 1 && ep.tiles_m <= 16) return ep.tiles_m;
+  const long panel = (long)bm * (k_eff > 0 ? k_eff : 1) * 2;
+  const int g = (int)std::max((long)min_g, std::min((long)max_g, (48L << 20) / panel));
+  return std::min(g, ep.tiles_m);
+}
+
 mgb_status launch_pair(const GemmArgs& g, EpiParams ep, cudaStream_t st) {
   ep.tiles_m = (g.M + 255) / 256;
   set_tiles_n(ep, g.N, 256);
-  const long panel = 256L * g.K * 2;
-  ep.group_m = (int)std::max(2L, std::min(32L, (48L << 20) / panel));
-  ep.group_m = std::min(ep.group_m, ep.tiles_m);
+  ep.group_m = raster_group(ep, g.M, g.N, 256, 2, 32);
   if (!g.a_mn && !g.b_mn) return launch_pair_variant<0, 0>(g, ep, st);
   if (!g.a_mn && g.b_mn) return launch_pair_variant<0, 1>(g, ep, st);
   if (g.a_mn && g.b_mn) return launch_pair_variant<1, 1>(g, ep, st);
@@ -1057,11 +1076,7 @@ template <int BN, int STAGES>
 mgb_status launch_bn(const GemmArgs& g, EpiParams ep, cudaStream_t st) {
   ep.tiles_m = (g.M + BM - 1) / BM;
   set_tiles_n(ep, g.N, BN);
-  // Row tiles per raster group: the group's A panel (group_m x 128 rows x K)
-  // should stay resident in L2 (about 48 MB) while the B columns stream by.
-  const long panel = (long)BM * (g.K > 0 ? g.K : 1) * 2;
-  ep.group_m = (int)std::max(4L, std::min(64L, (48L << 20) / panel));
-  ep.group_m = std::min(ep.group_m, ep.tiles_m);
+  ep.group_m = raster_group(ep, g.M, g.N, BM, 4, 64);
   if (!g.a_mn && !g.b_mn) return launch_variant<BN, STAGES, 0, 0>(g, ep, st);
   if (!g.a_mn && g.b_mn) return launch_variant<BN, STAGES, 0, 1>(g, ep, st);
   if (g.a_mn && g.b_mn) return launch_variant<BN, STAGES, 1, 1>(g, ep, st);

@@ -300,7 +300,10 @@ enum ProfKind : int {
   // attention sublayer forward (LN1, QKV, attention, output projection +
   // residual), MLP sublayer forward (LN2, fc1 + activation, fc2 + residual),
   // the whole backward (side streams joined)
-  PROF_STAGE_ATTN, PROF_STAGE_FFN, PROF_STAGE_BWD, PROF_KINDS
+  PROF_STAGE_ATTN, PROF_STAGE_FFN, PROF_STAGE_BWD,
+  // token-blocked CE: one block's d_hidden and d_emb products, run side by
+  // side (from the fork to the join, on the caller's stream)
+  PROF_STAGE_CE_PRODUCTS, PROF_KINDS
 };
 
 // Counts `launches` kernel launches and, when profiling is on, brackets them

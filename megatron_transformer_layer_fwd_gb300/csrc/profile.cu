@@ -61,7 +61,7 @@ const char* kKindNames[PROF_KINDS] = {
     "layernorm_fwd", "layernorm_bwd", "colsum",       "ce_stats", "ce_combine", "ce_grad",
     "gemm_tc_ce_logits", "embedding", "dropout", "gemm_tc_ce_dgrad", "gemm_tc_ce_wgrad",
     "splitk_reduce",
-    "stage_attention", "stage_ffn", "stage_backward"};
+    "stage_attention", "stage_ffn", "stage_backward", "stage_ce_products"};
 
 }  // namespace
 

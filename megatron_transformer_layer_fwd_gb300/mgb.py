@@ -116,6 +116,7 @@ def load() -> ctypes.CDLL:
             "mgb_gemm": [ctypes.POINTER(GemmDesc), P, P, P, P, P],
             "mgb_gemm_ex": [ctypes.POINTER(GemmExDesc), P, P, P, P, P, P, P, P],
             "mgb_gemm_f32_tc": [ctypes.POINTER(GemmExDesc), P, P, P, P, P, P, P, P, SZ, P],
+            "mgb_memcpy_async": [P, P, SZ, P],
             "mgb_layernorm_fwd": [I32, I32, I32, F32, P, P, P, P, P, P, P],
             "mgb_layernorm_bwd": [I32, I32, I32, P, P, P, P, P, P, P, P, P, P, SZ, P],
             "mgb_layernorm_bwd_noalloc": [I32, I32, I32, P, P, P, P, P, P, P, P, P, P],
@@ -384,6 +385,12 @@ def mgb_attention_bwd(batch, seq, n_q_heads, n_kv_heads, head_dim, causal, dtype
                                     _ptr(dout), ld_do, _ptr(dq), _ptr(dk), _ptr(dv), ld_dq, ld_dkv,
                                     _ptr(ws), ws.numel() * ws.element_size(), _stream(stream)),
            "mgb_attention_bwd")
+
+
+def mgb_memcpy_async(dst, src, nbytes: int, stream=None) -> None:
+    """Copy nbytes between (pinned host or device) tensors on `stream`."""
+    _check(load().mgb_memcpy_async(_ptr(dst), _ptr(src), nbytes, _stream(stream)),
+           "mgb_memcpy_async")
 
 
 def mgb_device_status(stream=None) -> int:
