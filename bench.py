@@ -682,6 +682,41 @@ def run_case(args):
                               "tflop": round(f / 1e12, 4), "tflops": round(f / (ms / 1e3) / 1e12, 1),
                               "kernel_ms": prof}), flush=True)
         return
+    if args.case == "ln":
+        # the layer's LayerNorms at its shape (T 8192, H 4096, bf16, affine):
+        # forward (the warp-per-row kernel, and the block-per-row kernel for
+        # comparison) and backward with the residual input (plus its
+        # dgamma/dbeta partial-sum reduction)
+        T, H = WORKLOADS[LAYER].tokens, WORKLOADS[LAYER].hidden
+        g = torch.Generator(device="cuda").manual_seed(0)
+        mk = lambda *sh: torch.randn(*sh, device="cuda", generator=g).to(torch.bfloat16)
+        x, dy, dres, gm, bt = mk(T, H), mk(T, H), mk(T, H), mk(H), mk(H)
+        y, dx = torch.empty_like(x), torch.empty_like(x)
+        mu = torch.empty(T, device="cuda")
+        rs = torch.empty(T, device="cuda")
+        dg, db = torch.empty_like(gm), torch.empty_like(bt)
+        ws = torch.empty(mgb.mgb_layernorm_bwd_ws_bytes(T, H), dtype=torch.uint8, device="cuda")
+        fwd_bytes = 2 * T * H * 2 + 8 * T
+        bwd_bytes = 4 * T * H * 2 + 8 * T
+        fwd = lambda: mgb.mgb_layernorm_fwd(T, H, mgb.MGB_BF16, 1e-5, x, gm, bt, y, mu, rs, hi)
+        bwd = lambda: mgb.mgb_layernorm_bwd(T, H, mgb.MGB_BF16, x, mu, rs, gm, dy, dres, dx, dg, db,
+                                            ws, hi)
+        # MGB_LN_KERNEL: tma (default: rows streamed into shared memory by bulk
+        # copies), warp (register prefetch, forward only), block (block per row)
+        for name, env, fn, nb in (("layernorm_fwd_tma", "tma", fwd, fwd_bytes),
+                                  ("layernorm_fwd_warp", "warp", fwd, fwd_bytes),
+                                  ("layernorm_fwd_block", "block", fwd, fwd_bytes),
+                                  ("layernorm_bwd_tma", "tma", bwd, bwd_bytes),
+                                  ("layernorm_bwd_block", "block", bwd, bwd_bytes)):
+            os.environ["MGB_LN_KERNEL"] = env
+            ms, prof = _time_loop(fn, args.steps, args.warmup, hi)
+            os.environ.pop("MGB_LN_KERNEL", None)
+            gbs = nb / (ms / 1e3) / 1e9
+            print(json.dumps({"case": name, "tokens": T, "hidden": H, "ms": round(ms, 4),
+                              "algorithmic_bytes": nb, "gbs": round(gbs, 1),
+                              "frac_of_hbm": round(gbs / peaks["hbm_gbs"], 4), "kernel_ms": prof}),
+                  flush=True)
+        return
     if args.case == "embedding":
         # the input-side lookup of the tied table (vocab-parallel embedding, one
         # shard = the whole vocabulary) at the CE workload's sizes; ids drawn
@@ -761,7 +796,7 @@ def main():
                     help="skip the sequence sweep of the causal workloads in the step run")
     ap.add_argument("--case", default="step",
                     choices=("step", "layer", "sweep", "ce", "gemm", "gemm_layer", "attention",
-                             "embedding"),
+                             "embedding", "ln"),
                     help="step (default: the whole hot path, one JSON line) or a sub-path / single kernel")
     ap.add_argument("--mnk", type=int, nargs=3, default=(8192, 22016, 4096))
     ap.add_argument("--dropout", type=float, default=0.0,

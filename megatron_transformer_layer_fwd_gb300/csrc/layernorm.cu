@@ -17,6 +17,8 @@
 // partial-then-reduce scheme with coalesced 16-byte row reads. Many partial
 // rows (the backward's 1024) are folded in two stages: 16 splits of rows
 // folded in place, then the split results.
+#include <algorithm>
+#include <cstring>
 #include <mutex>
 
 #include "common.cuh"
@@ -50,6 +52,22 @@ __device__ __forceinline__ void vload(const T* p, float* f) {
     f[2] = __uint_as_float(v.z); f[3] = __uint_as_float(v.w);
   }
 }
+template <typename T>
+__device__ __forceinline__ void vunpack(const uint4& v, float* f) {
+  if constexpr (sizeof(T) == 2) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 t = unpack_bf16x2(w[i]);
+      f[2 * i] = t.x;
+      f[2 * i + 1] = t.y;
+    }
+  } else {
+    f[0] = __uint_as_float(v.x); f[1] = __uint_as_float(v.y);
+    f[2] = __uint_as_float(v.z); f[3] = __uint_as_float(v.w);
+  }
+}
+
 template <typename T>
 __device__ __forceinline__ void vstore(T* p, const float* f) {
   uint4 v;
@@ -139,6 +157,436 @@ __global__ void ln_fwd_kernel(int rows, int cols, float eps, const T* __restrict
   }
 }
 
+// Forward, one warp per row, bf16 rows of VPL * 256 elements (each lane holds
+// VPL 16-byte vectors: columns 8 * (lane + 32 * i) .. + 7). Persistent warps
+// stride over the rows and issue the next row's loads before normalising the
+// current one, so about two rows per warp are in flight and the row's
+// reductions (warp shuffles only, no block barrier) overlap that traffic.
+// Two-pass mean / variance from registers, as the block kernel.
+__device__ __forceinline__ void unpack8(const uint4& u, float (&v)[8]) {
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int j = 0; j < 4; ++j) {
+    const float2 t = unpack_bf16x2(w[j]);
+    v[2 * j] = t.x;
+    v[2 * j + 1] = t.y;
+  }
+}
+
+template <int VPL>
+__global__ void __launch_bounds__(256) ln_fwd_warp_kernel(int rows, int cols, float eps,
+                                                          const bf16* __restrict__ x,
+                                                          const bf16* __restrict__ gamma,
+                                                          const bf16* __restrict__ beta,
+                                                          bf16* __restrict__ y,
+                                                          float* __restrict__ mean_out,
+                                                          float* __restrict__ rstd_out) {
+  const int lane = threadIdx.x & 31;
+  const int wid = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const int nw = gridDim.x * (blockDim.x >> 5);
+  const float inv_cols = 1.0f / (float)cols;
+  uint4 cur[VPL], nxt[VPL];
+  int row = wid;
+  if (row < rows) {
+    const uint4* xr = reinterpret_cast<const uint4*>(x + (int64_t)row * cols);
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) cur[i] = __ldg(xr + lane + 32 * i);
+  }
+  for (; row < rows; row += nw) {
+    const int nrow = row + nw;
+    if (nrow < rows) {
+      const uint4* xr = reinterpret_cast<const uint4*>(x + (int64_t)nrow * cols);
+#pragma unroll
+      for (int i = 0; i < VPL; ++i) nxt[i] = __ldg(xr + lane + 32 * i);
+    }
+    // the row stays packed (bf16 pairs) in registers and is unpacked on each
+    // of the three passes: half the registers of a float copy
+    float s = 0.0f;
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) {
+      float v[8];
+      unpack8(cur[i], v);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) s += v[j];
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+    const float mean = s * inv_cols;
+    float ss = 0.0f;
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) {
+      float v[8];
+      unpack8(cur[i], v);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const float d = v[j] - mean;
+        ss += d * d;
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    const float rstd = rsqrtf(ss * inv_cols + eps);
+    uint4* yr = reinterpret_cast<uint4*>(y + (int64_t)row * cols);
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) {
+      const int c = 8 * (lane + 32 * i);
+      float g[8], b[8];
+      if (gamma) vload(gamma + c, g);
+      if (beta) vload(beta + c, b);
+      float o8[8], v[8];
+      unpack8(cur[i], v);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        float t = (v[j] - mean) * rstd;
+        if (gamma) t *= g[j];
+        if (beta) t += b[j];
+        o8[j] = t;
+      }
+      uint4 ov;
+      ov.x = pack_bf16x2(o8[0], o8[1]); ov.y = pack_bf16x2(o8[2], o8[3]);
+      ov.z = pack_bf16x2(o8[4], o8[5]); ov.w = pack_bf16x2(o8[6], o8[7]);
+      yr[lane + 32 * i] = ov;
+    }
+    if (lane == 0) {
+      if (mean_out) mean_out[row] = mean;
+      if (rstd_out) rstd_out[row] = rstd;
+    }
+#pragma unroll
+    for (int i = 0; i < VPL; ++i) cur[i] = nxt[i];
+  }
+}
+
+template <int VPL>
+void ln_fwd_warp_go(int rows, int cols, float eps, const void* x, const void* gamma,
+                    const void* beta, void* y, float* mean, float* rstd, cudaStream_t st) {
+  // persistent: as many 8-warp blocks as are resident at once (by the
+  // kernel's registers), never more than the rows need
+  static int per_sm[64] = {};
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) dev = 0;
+  if (per_sm[dev] == 0) {
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, ln_fwd_warp_kernel<VPL>, 256, 0) !=
+            cudaSuccess ||
+        n < 1) {
+      cudaGetLastError();
+      n = 1;
+    }
+    per_sm[dev] = n;
+  }
+  const int want_blocks = (rows + 7) / 8;
+  const int cap = per_sm[dev] * device_sm_count();
+  const int blocks = want_blocks < cap ? want_blocks : cap;
+  ln_fwd_warp_kernel<VPL><<<blocks, 256, 0, st>>>(rows, cols, eps, (const bf16*)x,
+                                                  (const bf16*)gamma, (const bf16*)beta, (bf16*)y,
+                                                  mean, rstd);
+}
+
+// ------------------------------------------------ rows streamed by TMA bulk copies
+// The two bf16 kernels below keep their rows in a ring of shared-memory slots
+// filled by cp.async.bulk copies (one producer lane per CTA, completion on an
+// mbarrier per slot), so many rows per SM are in flight without registers
+// holding them. Every wait is bounded; a wait that runs out records the
+// error, sets the CTA's abort flag, and the CTA waits 10 ms for copies still
+// in flight before it exits.
+constexpr int kLnConsumers = 8;  // consumer warps per CTA (plus one producer warp)
+
+__device__ __forceinline__ void ln_abort_drain(volatile int* abort) {
+  __syncthreads();
+  if (*abort && threadIdx.x == 0) {
+    const uint64_t t0 = global_ns();
+    while (global_ns() - t0 < 10000000ull) {
+    }
+  }
+}
+
+// Forward: consumer warp w of the CTA normalises the CTA's rows i = w, w + 8,
+// ... (row = blockIdx.x + i * gridDim.x), each from slot i % nslot; it copies
+// the row into registers (VPL 16-byte vectors per lane) and frees the slot
+// before the reductions, then writes y with 16-byte stores.
+template <int VPL>
+__global__ void __launch_bounds__(32 * (1 + kLnConsumers), VPL >= 16 ? 1 : 2) ln_fwd_tma_kernel(
+    int rows, int cols, float eps, const bf16* __restrict__ x, const bf16* __restrict__ gamma,
+    const bf16* __restrict__ beta, bf16* __restrict__ y, float* __restrict__ mean_out,
+    float* __restrict__ rstd_out, int nslot, int* err) {
+  extern __shared__ __align__(128) uint8_t ln_smem[];
+  const uint32_t slot_bytes = (uint32_t)cols * 2;
+  const uint32_t slots = smem_u32(ln_smem);
+  const uint32_t full0 = slots + nslot * slot_bytes;  // 8-byte aligned (slot_bytes % 16 == 0)
+  const uint32_t empty0 = full0 + 8 * nslot;
+  volatile int* abort = reinterpret_cast<volatile int*>(ln_smem + nslot * slot_bytes + 16 * nslot);
+  // gamma and beta of the whole row, staged once (16-byte aligned after the flag)
+  uint4* sgb = reinterpret_cast<uint4*>(ln_smem + nslot * slot_bytes + 16 * nslot + 16);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nvec = cols / 8;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < nslot; ++i) {
+      mbar_init(full0 + 8 * i, 1);
+      mbar_init(empty0 + 8 * i, 1);
+    }
+    fence_mbar_init();
+    *abort = 0;
+  }
+  for (int v = threadIdx.x; v < nvec; v += blockDim.x) {
+    sgb[v] = gamma ? reinterpret_cast<const uint4*>(gamma)[v] : make_uint4(0, 0, 0, 0);
+    sgb[nvec + v] = beta ? reinterpret_cast<const uint4*>(beta)[v] : make_uint4(0, 0, 0, 0);
+  }
+  __syncthreads();
+  const int n = rows > (int)blockIdx.x ? (rows - (int)blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
+  if (warp == 0) {
+    if (lane == 0) {
+      for (int i = 0; i < n && !*abort; ++i) {
+        const int s = i % nslot;
+        if (i >= nslot && !mbar_wait(empty0 + 8 * s, ((i / nslot) - 1) & 1, err)) {
+          *abort = 1;
+          break;
+        }
+        const int row = blockIdx.x + i * gridDim.x;
+        mbar_arrive_expect_tx(full0 + 8 * s, slot_bytes);
+        bulk_load(slots + s * slot_bytes, x + (int64_t)row * cols, slot_bytes, full0 + 8 * s);
+      }
+    }
+  } else {
+    const float inv_cols = 1.0f / (float)cols;
+    for (int i = warp - 1; i < n; i += kLnConsumers) {
+      const int s = i % nslot;
+      const bool ok = !*abort && mbar_wait(full0 + 8 * s, (i / nslot) & 1, err);
+      if (!__all_sync(0xffffffffu, ok)) {
+        *abort = 1;
+        break;
+      }
+      uint4 cur[VPL];
+      const uint4* src = reinterpret_cast<const uint4*>(ln_smem + s * slot_bytes);
+#pragma unroll
+      for (int j = 0; j < VPL; ++j) cur[j] = src[lane + 32 * j];
+      __syncwarp();
+      if (lane == 0) mbar_arrive(empty0 + 8 * s);  // slot free: the producer refills it
+      const int row = blockIdx.x + i * gridDim.x;
+      // eight independent partial sums (one per element of a vector): short
+      // dependency chains instead of one chain over the lane's elements
+      float a8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int j = 0; j < VPL; ++j) {
+        float v[8];
+        unpack8(cur[j], v);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) a8[e] += v[e];
+      }
+      float sm = ((a8[0] + a8[1]) + (a8[2] + a8[3])) + ((a8[4] + a8[5]) + (a8[6] + a8[7]));
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) sm += __shfl_xor_sync(0xffffffffu, sm, o);
+      const float mean = sm * inv_cols;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) a8[e] = 0.0f;
+#pragma unroll
+      for (int j = 0; j < VPL; ++j) {
+        float v[8];
+        unpack8(cur[j], v);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const float d = v[e] - mean;
+          a8[e] = fmaf(d, d, a8[e]);
+        }
+      }
+      float ss = ((a8[0] + a8[1]) + (a8[2] + a8[3])) + ((a8[4] + a8[5]) + (a8[6] + a8[7]));
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+      const float rstd = rsqrtf(ss * inv_cols + eps);
+      uint4* yr = reinterpret_cast<uint4*>(y + (int64_t)row * cols);
+#pragma unroll
+      for (int j = 0; j < VPL; ++j) {
+        const int vi = lane + 32 * j;
+        float v[8], g[8], b[8], o8[8];
+        unpack8(cur[j], v);
+        unpack8(sgb[vi], g);
+        unpack8(sgb[nvec + vi], b);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          float t = (v[e] - mean) * rstd;
+          if (gamma) t *= g[e];
+          if (beta) t += b[e];
+          o8[e] = t;
+        }
+        uint4 ov;
+        ov.x = pack_bf16x2(o8[0], o8[1]); ov.y = pack_bf16x2(o8[2], o8[3]);
+        ov.z = pack_bf16x2(o8[4], o8[5]); ov.w = pack_bf16x2(o8[6], o8[7]);
+        yr[vi] = ov;
+      }
+      if (lane == 0) {
+        if (mean_out) mean_out[row] = mean;
+        if (rstd_out) rstd_out[row] = rstd;
+      }
+    }
+  }
+  ln_abort_drain(abort);
+}
+
+// Backward: the CTA's 8 consumer warps (256 threads, VPT vectors each) take
+// the CTA's rows one after another, each from slot i % nslot holding x, dy and
+// dres (three bulk copies); the row reduction uses two float2 slots per warp
+// in shared memory (alternating by row) and one named barrier of the 256
+// consumer threads; dgamma/dbeta partials stay in registers and are written
+// once at the end as partial row blockIdx.x.
+template <int VPT>
+__global__ void __launch_bounds__(32 * (1 + kLnConsumers)) ln_bwd_tma_kernel(
+    int rows, int cols, const bf16* __restrict__ x, const float* __restrict__ mean,
+    const float* __restrict__ rstd, const bf16* __restrict__ gamma, const bf16* __restrict__ dy,
+    const bf16* __restrict__ dres, bf16* __restrict__ dx, float* __restrict__ part, int nslot,
+    int* err) {
+  extern __shared__ __align__(128) uint8_t ln_smem[];
+  const uint32_t row_bytes = (uint32_t)cols * 2;
+  const uint32_t slot_bytes = 3 * row_bytes;
+  const uint32_t slots = smem_u32(ln_smem);
+  const uint32_t full0 = slots + nslot * slot_bytes;
+  const uint32_t empty0 = full0 + 8 * nslot;
+  float2* red = reinterpret_cast<float2*>(ln_smem + nslot * slot_bytes + 16 * nslot);  // [2][8]
+  volatile int* abort = reinterpret_cast<volatile int*>(red + 16);
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nvec = cols / 8;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < nslot; ++i) {
+      mbar_init(full0 + 8 * i, 1);
+      mbar_init(empty0 + 8 * i, kLnConsumers);
+    }
+    fence_mbar_init();
+    *abort = 0;
+  }
+  __syncthreads();
+  const int n = rows > (int)blockIdx.x ? (rows - (int)blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
+  if (warp == 0) {
+    if (lane == 0) {
+      const uint32_t bytes = dres ? slot_bytes : 2 * row_bytes;
+      for (int i = 0; i < n && !*abort; ++i) {
+        const int s = i % nslot;
+        if (i >= nslot && !mbar_wait(empty0 + 8 * s, ((i / nslot) - 1) & 1, err)) {
+          *abort = 1;
+          break;
+        }
+        const int64_t ro = (int64_t)(blockIdx.x + i * gridDim.x) * cols;
+        const uint32_t dst = slots + s * slot_bytes, fb = full0 + 8 * s;
+        mbar_arrive_expect_tx(fb, bytes);
+        bulk_load(dst, x + ro, row_bytes, fb);
+        bulk_load(dst + row_bytes, dy + ro, row_bytes, fb);
+        if (dres) bulk_load(dst + 2 * row_bytes, dres + ro, row_bytes, fb);
+      }
+    }
+  } else {
+    const int t = threadIdx.x - 32, cw = warp - 1;  // consumer thread / warp
+    float pg[VPT][8], pb[VPT][8];
+#pragma unroll
+    for (int q = 0; q < VPT; ++q)
+#pragma unroll
+      for (int e = 0; e < 8; ++e) pg[q][e] = pb[q][e] = 0.0f;
+    const float inv_cols = 1.0f / (float)cols;
+    for (int i = 0; i < n; ++i) {
+      const int s = i % nslot;
+      // every consumer thread takes the same decision (a barrier with an OR
+      // vote), so none is left waiting at the row barrier below
+      const bool ok = !*abort && mbar_wait(full0 + 8 * s, (i / nslot) & 1, err);
+      int bad = 0;
+      asm volatile(
+          "{\n .reg .pred p, q;\n setp.eq.u32 p, %1, 0;\n"
+          " bar.red.or.pred q, 2, %2, p;\n selp.u32 %0, 1, 0, q;\n}\n"
+          : "=r"(bad)
+          : "r"((uint32_t)ok), "r"(32 * kLnConsumers)
+          : "memory");
+      if (bad) {
+        *abort = 1;
+        break;
+      }
+      const uint8_t* sl = ln_smem + s * slot_bytes;
+      uint4 rx[VPT], rd[VPT], rr[VPT];
+#pragma unroll
+      for (int q = 0; q < VPT; ++q) {
+        const int vi = t + 256 * q;
+        if (vi < nvec) {
+          rx[q] = reinterpret_cast<const uint4*>(sl)[vi];
+          rd[q] = reinterpret_cast<const uint4*>(sl + row_bytes)[vi];
+          if (dres) rr[q] = reinterpret_cast<const uint4*>(sl + 2 * row_bytes)[vi];
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(empty0 + 8 * s);
+      const int row = blockIdx.x + i * gridDim.x;
+      const float mu = mean[row], rs = rstd[row];
+      float s1 = 0.0f, s2 = 0.0f;
+#pragma unroll
+      for (int q = 0; q < VPT; ++q) {
+        const int vi = t + 256 * q;
+        if (vi < nvec) {
+          float xv[8], dv[8], gm[8];
+          unpack8(rx[q], xv);
+          unpack8(rd[q], dv);
+          if (gamma) vload(gamma + vi * 8, gm);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const float xh = (xv[e] - mu) * rs;
+            const float g = gamma ? dv[e] * gm[e] : dv[e];
+            s1 += g;
+            s2 += g * xh;
+            pg[q][e] += dv[e] * xh;
+            pb[q][e] += dv[e];
+          }
+        }
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        s1 += __shfl_xor_sync(0xffffffffu, s1, o);
+        s2 += __shfl_xor_sync(0xffffffffu, s2, o);
+      }
+      float2* rb = red + 8 * (i & 1);
+      if (lane == 0) rb[cw] = make_float2(s1, s2);
+      asm volatile("bar.sync 1, %0;" ::"r"(32 * kLnConsumers) : "memory");
+      float a = 0.0f, b2 = 0.0f;
+#pragma unroll
+      for (int w = 0; w < kLnConsumers; ++w) {
+        const float2 v = rb[w];
+        a += v.x;
+        b2 += v.y;
+      }
+      const float mg = a * inv_cols, mgx = b2 * inv_cols;
+#pragma unroll
+      for (int q = 0; q < VPT; ++q) {
+        const int vi = t + 256 * q;
+        if (vi < nvec) {
+          float xv[8], dv[8], gm[8], rv[8], o[8];
+          unpack8(rx[q], xv);
+          unpack8(rd[q], dv);
+          if (gamma) vload(gamma + vi * 8, gm);
+          if (dres) unpack8(rr[q], rv);
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const float xh = (xv[e] - mu) * rs;
+            const float g = gamma ? dv[e] * gm[e] : dv[e];
+            o[e] = rs * (g - mg - xh * mgx);
+            if (dres) o[e] += rv[e];
+          }
+          vstore(dx + (int64_t)row * cols + vi * 8, o);
+        }
+      }
+    }
+    if (part) {
+      float* pgr = part + (int64_t)blockIdx.x * cols;
+      float* pbr = part + (int64_t)(gridDim.x + blockIdx.x) * cols;
+#pragma unroll
+      for (int q = 0; q < VPT; ++q) {
+        const int vi = t + 256 * q;
+        if (vi < nvec) {
+#pragma unroll
+          for (int e = 0; e < 8; e += 4) {
+            *reinterpret_cast<float4*>(pgr + vi * 8 + e) =
+                make_float4(pg[q][e], pg[q][e + 1], pg[q][e + 2], pg[q][e + 3]);
+            *reinterpret_cast<float4*>(pbr + vi * 8 + e) =
+                make_float4(pb[q][e], pb[q][e + 1], pb[q][e + 2], pb[q][e + 3]);
+          }
+        }
+      }
+    }
+  }
+  ln_abort_drain(abort);
+}
+
 // Sum of a float2 over the block (one pass of shuffles + shared memory).
 __device__ __forceinline__ float2 block_sum2(float2 v, float2* red) {
 #pragma unroll
@@ -165,7 +613,7 @@ __device__ __forceinline__ float2 block_sum2(float2 v, float2* red) {
 // of those columns stay in registers for the whole block. A row's x, dy and
 // dres are all requested before the row reduction, so each thread keeps
 // 3 * VPT loads in flight.
-template <typename T, int VPT>
+template <typename T, int VPT, bool PF>
 __device__ __forceinline__ void ln_bwd_rows(int rows, int cols, const T* __restrict__ x,
                                             const float* __restrict__ mean,
                                             const float* __restrict__ rstd,
@@ -175,45 +623,53 @@ __device__ __forceinline__ void ln_bwd_rows(int rows, int cols, const T* __restr
   constexpr int VN = Vec<T>::N;
   __shared__ float2 red[32];
   const int nvec = cols / VN;
-  float gm[VPT][VN], pg[VPT][VN], pb[VPT][VN];
+  float pg[VPT][VN], pb[VPT][VN];
 #pragma unroll
-  for (int i = 0; i < VPT; ++i) {
-    const int vi = threadIdx.x + i * blockDim.x;
+  for (int i = 0; i < VPT; ++i)
 #pragma unroll
-    for (int j = 0; j < VN; ++j) {
-      gm[i][j] = 1.0f;
-      pg[i][j] = pb[i][j] = 0.0f;
-    }
-    if (gamma && vi < nvec) vload(gamma + vi * VN, gm[i]);
-  }
-  for (int row = blockIdx.x; row < rows; row += gridDim.x) {
-    const float mu = mean[row], rs = rstd[row];
+    for (int j = 0; j < VN; ++j) pg[i][j] = pb[i][j] = 0.0f;
+  // The row is kept as raw 16-byte vectors (x, dy, dres) and unpacked in each
+  // of the two passes; with PF the next row's vectors are requested before
+  // this row's reduction. gamma is read per row (an L1 hit after the first).
+  uint4 rx[VPT], rd[VPT], rr[VPT], nx[VPT], nd[VPT], nr[VPT];
+  auto fetch = [&](int row, uint4 (&ax)[VPT], uint4 (&ad)[VPT], uint4 (&ar)[VPT]) {
     const int64_t ro = (int64_t)row * cols;
-    float xv[VPT][VN], dv[VPT][VN], rv[VPT][VN];
 #pragma unroll
     for (int i = 0; i < VPT; ++i) {
       const int vi = threadIdx.x + i * blockDim.x;
       if (vi < nvec) {
-        vload(x + ro + vi * VN, xv[i]);
-        vload(dy + ro + vi * VN, dv[i]);
-        if (dres) vload(dres + ro + vi * VN, rv[i]);
+        ax[i] = *reinterpret_cast<const uint4*>(x + ro + vi * VN);
+        ad[i] = *reinterpret_cast<const uint4*>(dy + ro + vi * VN);
+        if (dres) ar[i] = *reinterpret_cast<const uint4*>(dres + ro + vi * VN);
       }
+    }
+  };
+  if (PF && blockIdx.x < rows) fetch(blockIdx.x, rx, rd, rr);
+  for (int row = blockIdx.x; row < rows; row += gridDim.x) {
+    const float mu = mean[row], rs = rstd[row];
+    const int64_t ro = (int64_t)row * cols;
+    if (PF) {
+      if (row + (int)gridDim.x < rows) fetch(row + gridDim.x, nx, nd, nr);
+    } else {
+      fetch(row, rx, rd, rr);
     }
     float s1 = 0.0f, s2 = 0.0f;
 #pragma unroll
     for (int i = 0; i < VPT; ++i) {
       const int vi = threadIdx.x + i * blockDim.x;
       if (vi < nvec) {
+        float xv[VN], dv[VN], gm[VN];
+        vunpack<T>(rx[i], xv);
+        vunpack<T>(rd[i], dv);
+        if (gamma) vload(gamma + vi * VN, gm);
 #pragma unroll
         for (int j = 0; j < VN; ++j) {
-          const float xh = (xv[i][j] - mu) * rs;
-          const float g = dv[i][j] * gm[i][j];
+          const float xh = (xv[j] - mu) * rs;
+          const float g = gamma ? dv[j] * gm[j] : dv[j];
           s1 += g;
           s2 += g * xh;
-          pg[i][j] += dv[i][j] * xh;
-          pb[i][j] += dv[i][j];
-          xv[i][j] = xh;  // keep xhat
-          dv[i][j] = g;   // keep g
+          pg[i][j] += dv[j] * xh;
+          pb[i][j] += dv[j];
         }
       }
     }
@@ -224,13 +680,27 @@ __device__ __forceinline__ void ln_bwd_rows(int rows, int cols, const T* __restr
     for (int i = 0; i < VPT; ++i) {
       const int vi = threadIdx.x + i * blockDim.x;
       if (vi < nvec) {
-        float o[VN];
+        float xv[VN], dv[VN], gm[VN], rv[VN], o[VN];
+        vunpack<T>(rx[i], xv);
+        vunpack<T>(rd[i], dv);
+        if (gamma) vload(gamma + vi * VN, gm);
+        if (dres) vunpack<T>(rr[i], rv);
 #pragma unroll
         for (int j = 0; j < VN; ++j) {
-          o[j] = rs * (dv[i][j] - mg - xv[i][j] * mgx);
-          if (dres) o[j] += rv[i][j];
+          const float xh = (xv[j] - mu) * rs;
+          const float g = gamma ? dv[j] * gm[j] : dv[j];
+          o[j] = rs * (g - mg - xh * mgx);
+          if (dres) o[j] += rv[j];
         }
         vstore(dx + ro + vi * VN, o);
+      }
+    }
+    if (PF) {
+#pragma unroll
+      for (int i = 0; i < VPT; ++i) {
+        rx[i] = nx[i];
+        rd[i] = nd[i];
+        rr[i] = nr[i];
       }
     }
   }
@@ -253,14 +723,15 @@ __device__ __forceinline__ void ln_bwd_rows(int rows, int cols, const T* __restr
   }
 }
 
-// Rows of up to 1024 vectors: one vector per thread.
+// Rows of up to 1024 vectors: one vector per thread (64 registers: two
+// 512-thread blocks per SM).
 template <typename T, int VPT>
-__global__ void ln_bwd_kernel(int rows, int cols, const T* __restrict__ x,
+__global__ void __launch_bounds__(1024, 1) ln_bwd_kernel(int rows, int cols, const T* __restrict__ x,
                               const float* __restrict__ mean, const float* __restrict__ rstd,
                               const T* __restrict__ gamma, const T* __restrict__ dy,
                               const T* __restrict__ dres, T* __restrict__ dx,
                               float* __restrict__ part) {
-  ln_bwd_rows<T, VPT>(rows, cols, x, mean, rstd, gamma, dy, dres, dx, part);
+  ln_bwd_rows<T, VPT, true>(rows, cols, x, mean, rstd, gamma, dy, dres, dx, part);
 }
 
 // Wider rows (VPT 2 or 4 vectors per thread, up to 1024 threads): the register
@@ -271,7 +742,7 @@ __global__ void __launch_bounds__(1024, 1) ln_bwd_wide_kernel(
     int rows, int cols, const T* __restrict__ x, const float* __restrict__ mean,
     const float* __restrict__ rstd, const T* __restrict__ gamma, const T* __restrict__ dy,
     const T* __restrict__ dres, T* __restrict__ dx, float* __restrict__ part) {
-  ln_bwd_rows<T, VPT>(rows, cols, x, mean, rstd, gamma, dy, dres, dx, part);
+  ln_bwd_rows<T, VPT, false>(rows, cols, x, mean, rstd, gamma, dy, dres, dx, part);
 }
 
 // out0[c] = sum_p part[p * stride, c] and out1[c] = sum_p part[half + p * stride, c]
@@ -428,8 +899,88 @@ int ln_threads(int cols, int vn) {
 // Row blocks of the backward: about one resident wave (several blocks per SM)
 // to hide the latency of the per-row reductions; each writes one partial
 // dgamma/dbeta row.
-int layernorm_bwd_parts(int rows) { return rows < 1024 ? (rows > 0 ? rows : 1) : 1024; }
+// (608 = four 512-thread blocks on each of 152 SMs: one resident wave)
+int layernorm_bwd_parts(int rows) { return rows < 608 ? (rows > 0 ? rows : 1) : 608; }
 int colsum_parts(int M) { return M < 64 * 8 ? 1 : 64; }
+
+namespace {
+
+// Resident CTAs per SM of a kernel at `smem` bytes of dynamic shared memory.
+template <typename K>
+int resident_ctas(K kern, int threads, size_t smem) {
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, threads, smem) != cudaSuccess) {
+    cudaGetLastError();
+    return 1;
+  }
+  return n > 0 ? n : 1;
+}
+
+template <int VPL>
+mgb_status ln_fwd_tma_vpl(int rows, int cols, float eps, const void* x, const void* gamma,
+                          const void* beta, void* y, float* mean, float* rstd, cudaStream_t st) {
+  const int slot = cols * 2;
+  const int nslot = std::max(2, std::min(16, (96 << 10) / slot));
+  const size_t smem = (size_t)nslot * slot + 16 * nslot + 16 + 2 * (size_t)cols * 2;
+  auto kern = ln_fwd_tma_kernel<VPL>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+      cudaSuccess)
+    return MGB_ERR_CUDA;
+  const int threads = 32 * (1 + kLnConsumers);
+  const int cap = resident_ctas(kern, threads, smem) * device_sm_count();
+  const int want = (rows + kLnConsumers - 1) / kLnConsumers;
+  const int grid = std::max(1, std::min(cap, want));
+  kern<<<grid, threads, smem, st>>>(rows, cols, eps, (const bf16*)x, (const bf16*)gamma,
+                                    (const bf16*)beta, (bf16*)y, mean, rstd, nslot,
+                                    device_error_word());
+  return MGB_OK;
+}
+
+mgb_status ln_fwd_tma_go(int rows, int cols, float eps, const void* x, const void* gamma,
+                         const void* beta, void* y, float* mean, float* rstd, cudaStream_t st) {
+  switch (cols / 256) {
+    case 1: return ln_fwd_tma_vpl<1>(rows, cols, eps, x, gamma, beta, y, mean, rstd, st);
+    case 2: return ln_fwd_tma_vpl<2>(rows, cols, eps, x, gamma, beta, y, mean, rstd, st);
+    case 4: return ln_fwd_tma_vpl<4>(rows, cols, eps, x, gamma, beta, y, mean, rstd, st);
+    case 8: return ln_fwd_tma_vpl<8>(rows, cols, eps, x, gamma, beta, y, mean, rstd, st);
+    case 16: return ln_fwd_tma_vpl<16>(rows, cols, eps, x, gamma, beta, y, mean, rstd, st);
+    default: return MGB_ERR_UNSUPPORTED;
+  }
+}
+
+template <int VPT>
+int ln_bwd_tma_vpt(int nparts, int rows, int cols, const void* x, const float* mean,
+                   const float* rstd, const void* gamma, const void* dy, const void* dres,
+                   void* dx, float* part, cudaStream_t st) {
+  const int slot = 3 * cols * 2;
+  const int nslot = std::max(2, std::min(8, (96 << 10) / slot));
+  const size_t smem = (size_t)nslot * slot + 16 * nslot + 16 * 8 + 32;
+  auto kern = ln_bwd_tma_kernel<VPT>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+      cudaSuccess)
+    return -1;
+  const int threads = 32 * (1 + kLnConsumers);
+  const int cap = resident_ctas(kern, threads, smem) * device_sm_count();
+  const int grid = std::max(1, std::min(cap, nparts));
+  kern<<<grid, threads, smem, st>>>(rows, cols, (const bf16*)x, mean, rstd, (const bf16*)gamma,
+                                    (const bf16*)dy, (const bf16*)dres, (bf16*)dx, part, nslot,
+                                    device_error_word());
+  return grid;
+}
+
+// Launches the TMA-fed backward when it applies; returns the partial rows it
+// wrote (its grid), 0 when it does not apply, -1 on a launch-setup error.
+int ln_bwd_tma_go(int nparts, int rows, int cols, const void* x, const float* mean,
+                  const float* rstd, const void* gamma, const void* dy, const void* dres,
+                  void* dx, float* part, cudaStream_t st) {
+  const int nvec = cols / 8;
+  if (nvec <= 256) return ln_bwd_tma_vpt<1>(nparts, rows, cols, x, mean, rstd, gamma, dy, dres, dx, part, st);
+  if (nvec <= 512) return ln_bwd_tma_vpt<2>(nparts, rows, cols, x, mean, rstd, gamma, dy, dres, dx, part, st);
+  if (nvec <= 1024) return ln_bwd_tma_vpt<4>(nparts, rows, cols, x, mean, rstd, gamma, dy, dres, dx, part, st);
+  return 0;
+}
+
+}  // namespace
 
 mgb_status layernorm_fwd_launch(int rows, int cols, int dtype, float eps, const void* x,
                                 const void* gamma, const void* beta, void* y, float* mean,
@@ -440,6 +991,28 @@ mgb_status layernorm_fwd_launch(int rows, int cols, int dtype, float eps, const 
   if (threads > 1024) return MGB_ERR_UNSUPPORTED;
   if (rows == 0) return MGB_OK;
   LaunchScope scope(PROF_LN_FWD, st);
+  // MGB_LN_KERNEL=block / warp picks the block-per-row or register-prefetch
+  // kernel instead of the TMA-fed one (comparisons)
+  const char* kenv = getenv("MGB_LN_KERNEL");
+  const bool force_block = kenv && strcmp(kenv, "block") == 0;
+  const bool force_warp = kenv && strcmp(kenv, "warp") == 0;
+  if (dtype == MGB_BF16 && cols % 256 == 0 && cols <= 4096 && !force_block && !force_warp) {
+    const mgb_status s = ln_fwd_tma_go(rows, cols, eps, x, gamma, beta, y, mean, rstd, st);
+    if (s != MGB_ERR_UNSUPPORTED) return s;
+  }
+  const bool warp_ok = dtype == MGB_BF16 && cols % 256 == 0 && !force_block;
+  if (warp_ok) {
+    switch (cols / 256) {
+      case 1: ln_fwd_warp_go<1>(rows, cols, eps, x, gamma, beta, y, mean, rstd, st); break;
+      case 2: ln_fwd_warp_go<2>(rows, cols, eps, x, gamma, beta, y, mean, rstd, st); break;
+      case 4: ln_fwd_warp_go<4>(rows, cols, eps, x, gamma, beta, y, mean, rstd, st); break;
+      case 8: ln_fwd_warp_go<8>(rows, cols, eps, x, gamma, beta, y, mean, rstd, st); break;
+      case 16: ln_fwd_warp_go<16>(rows, cols, eps, x, gamma, beta, y, mean, rstd, st); break;
+      default: goto block_kernel;
+    }
+    return cudaGetLastError() == cudaSuccess ? MGB_OK : MGB_ERR_CUDA;
+  }
+block_kernel:
   if (dtype == MGB_BF16)
     ln_fwd_kernel<bf16><<<rows, threads, 0, st>>>(
         rows, cols, eps, (const bf16*)x, (const bf16*)gamma, (const bf16*)beta, (bf16*)y, mean, rstd);
@@ -452,37 +1025,48 @@ mgb_status layernorm_fwd_launch(int rows, int cols, int dtype, float eps, const 
 
 namespace {
 
+// Launches with at most as many blocks as are resident at once (the blocks
+// stride over the rows, so a second wave would only serialise); returns the
+// grid, which is the number of partial rows written.
 template <typename T, int VPT>
-void ln_bwd_go(int nparts, int threads, int rows, int cols, const void* x, const float* mean,
-               const float* rstd, const void* gamma, const void* dy, const void* dres, void* dx,
-               float* part, cudaStream_t st) {
+int ln_bwd_go(int nparts, int threads, int rows, int cols, const void* x, const float* mean,
+              const float* rstd, const void* gamma, const void* dy, const void* dres, void* dx,
+              float* part, cudaStream_t st) {
+  int per_sm = 0;
+  auto k1 = ln_bwd_kernel<T, VPT>;
+  auto kw = ln_bwd_wide_kernel<T, VPT>;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, VPT == 1 ? k1 : kw, threads, 0) !=
+          cudaSuccess ||
+      per_sm < 1) {
+    cudaGetLastError();
+    per_sm = 1;
+  }
+  const int grid = std::max(1, std::min(nparts, per_sm * device_sm_count()));
   if constexpr (VPT == 1)
-    ln_bwd_kernel<T, 1><<<nparts, threads, 0, st>>>(rows, cols, (const T*)x, mean, rstd,
-                                                    (const T*)gamma, (const T*)dy,
-                                                    (const T*)dres, (T*)dx, part);
+    k1<<<grid, threads, 0, st>>>(rows, cols, (const T*)x, mean, rstd, (const T*)gamma,
+                                 (const T*)dy, (const T*)dres, (T*)dx, part);
   else
-    ln_bwd_wide_kernel<T, VPT><<<nparts, threads, 0, st>>>(rows, cols, (const T*)x, mean, rstd,
-                                                           (const T*)gamma, (const T*)dy,
-                                                           (const T*)dres, (T*)dx, part);
+    kw<<<grid, threads, 0, st>>>(rows, cols, (const T*)x, mean, rstd, (const T*)gamma,
+                                 (const T*)dy, (const T*)dres, (T*)dx, part);
+  return grid;
 }
 
+// Returns the partial rows written (the grid), or -1 for an unsupported width.
 template <typename T>
-mgb_status ln_bwd_dispatch(int nparts, int rows, int cols, const void* x, const float* mean,
-                           const float* rstd, const void* gamma, const void* dy, const void* dres,
-                           void* dx, float* part, cudaStream_t st) {
+int ln_bwd_dispatch(int nparts, int rows, int cols, const void* x, const float* mean,
+                    const float* rstd, const void* gamma, const void* dy, const void* dres,
+                    void* dx, float* part, cudaStream_t st) {
   // one 16-byte vector per thread (64 registers: full occupancy), two or four
   // for rows wider than 1024 vectors
   const int nvec = cols / Vec<T>::N;
   auto thr = [&](int vpt) { return ((nvec + vpt - 1) / vpt + 31) / 32 * 32; };
   if (nvec <= 1024)
-    ln_bwd_go<T, 1>(nparts, thr(1), rows, cols, x, mean, rstd, gamma, dy, dres, dx, part, st);
-  else if (nvec <= 2048)
-    ln_bwd_go<T, 2>(nparts, thr(2), rows, cols, x, mean, rstd, gamma, dy, dres, dx, part, st);
-  else if (nvec <= 4096)
-    ln_bwd_go<T, 4>(nparts, thr(4), rows, cols, x, mean, rstd, gamma, dy, dres, dx, part, st);
-  else
-    return MGB_ERR_UNSUPPORTED;
-  return MGB_OK;
+    return ln_bwd_go<T, 1>(nparts, thr(1), rows, cols, x, mean, rstd, gamma, dy, dres, dx, part, st);
+  if (nvec <= 2048)
+    return ln_bwd_go<T, 2>(nparts, thr(2), rows, cols, x, mean, rstd, gamma, dy, dres, dx, part, st);
+  if (nvec <= 4096)
+    return ln_bwd_go<T, 4>(nparts, thr(4), rows, cols, x, mean, rstd, gamma, dy, dres, dx, part, st);
+  return -1;
 }
 
 }  // namespace
@@ -498,15 +1082,45 @@ mgb_status layernorm_bwd_launch(int rows, int cols, int dtype, const void* x, co
   // the dgamma/dbeta partial rows of the workspace are sized for this width
   if (want && cols > kLnBwdMaxCols) return MGB_ERR_UNSUPPORTED;
   if (rows == 0) nparts = 1;
-  LaunchScope scope(PROF_LN_BWD, st, (rows > 0 ? 1 : 0) + (want ? reduce_launches(nparts, cols) : 0));
+  // the TMA-fed bf16 kernel writes as many partial rows as its grid (at most
+  // nparts); the reduction then folds that many
+  // (the block kernel is the default: measured faster at the layer's shape;
+  // MGB_LN_KERNEL=tma selects the bulk-copy kernel)
+  const char* kenv = getenv("MGB_LN_KERNEL");
+  const bool tma = dtype == MGB_BF16 && rows > 0 && cols * 2 * 3 <= (96 << 10) && kenv &&
+                   strcmp(kenv, "tma") == 0;
+  if (tma) {
+    int used;
+    {
+      LaunchScope pre(PROF_LN_BWD, st);
+      used = ln_bwd_tma_go(nparts, rows, cols, x, mean, rstd, gamma, dy, dres, dx,
+                           want ? part : nullptr, st);
+    }
+    if (used < 0) return MGB_ERR_CUDA;
+    if (used > 0) {
+      if (want) {
+        LaunchScope scope(PROF_LN_BWD, st, reduce_launches(used, cols));
+        if (dtype == MGB_BF16)
+          reduce_parts_go<bf16>(used, cols, part, (bf16*)dgamma, (bf16*)dbeta, st);
+      }
+      return cudaGetLastError() == cudaSuccess ? MGB_OK : MGB_ERR_CUDA;
+    }
+  }
   if (rows > 0) {
-    const mgb_status s =
-        dtype == MGB_BF16
-            ? ln_bwd_dispatch<bf16>(nparts, rows, cols, x, mean, rstd, gamma, dy, dres, dx,
-                                    want ? part : nullptr, st)
-            : ln_bwd_dispatch<float>(nparts, rows, cols, x, mean, rstd, gamma, dy, dres, dx,
-                                     want ? part : nullptr, st);
-    if (s != MGB_OK) return s;
+    int used;
+    {
+      LaunchScope scope(PROF_LN_BWD, st);
+      used = dtype == MGB_BF16
+                 ? ln_bwd_dispatch<bf16>(nparts, rows, cols, x, mean, rstd, gamma, dy, dres, dx,
+                                         want ? part : nullptr, st)
+                 : ln_bwd_dispatch<float>(nparts, rows, cols, x, mean, rstd, gamma, dy, dres, dx,
+                                          want ? part : nullptr, st);
+    }
+    if (used < 0) return MGB_ERR_UNSUPPORTED;
+    nparts = used;
+  }
+  LaunchScope scope(PROF_LN_BWD, st, want ? reduce_launches(nparts, cols) : 0);
+  if (rows > 0) {
   } else if (want) {
     cudaMemsetAsync(part, 0, sizeof(float) * 2 * cols, st);
   }

@@ -23,8 +23,14 @@ def _dev(a, dtype):
     # rows wider than 1024 vectors: two or four vectors per thread, up to 1024
     # threads a block (the widest rows the layer accepts)
     ("bf16", 40, 12288, True, True), ("bf16", 33, 16384, True, False),
-    ("f32", 20, 8192, True, True), ("f32", 17, 16384, True, True)])
-def test_layernorm_bwd(mgb_lib, dtype, rows, cols, affine, resid):
+    ("f32", 20, 8192, True, True), ("f32", 17, 16384, True, True),
+    # many rows per CTA: the bf16 kernel's shared-memory ring refilled many times
+    ("bf16", 8192, 4096, True, True), ("bf16", 3000, 2048, True, False)])
+@pytest.mark.parametrize("kernel", ["tma", "block"])
+def test_layernorm_bwd(mgb_lib, monkeypatch, kernel, dtype, rows, cols, affine, resid):
+    """bf16 rows up to 16384 wide go through the kernel fed by bulk copies
+    (three rows per shared-memory slot) unless MGB_LN_KERNEL=block."""
+    monkeypatch.setenv("MGB_LN_KERNEL", kernel)
     x = RNG.standard_normal((rows, cols)) * 1.5 + 0.3
     dy = RNG.standard_normal((rows, cols))
     dres = RNG.standard_normal((rows, cols)) if resid else None

@@ -176,8 +176,16 @@ def test_gemm_zero_k_writes_bias_only(mgb_lib):
     np.testing.assert_array_equal(to_np(c), np.broadcast_to(bias, (M, N)))
 
 
-@pytest.mark.parametrize("dtype,rows,cols", [("bf16", 300, 1024), ("bf16", 7, 4096), ("f32", 64, 256)])
-def test_layernorm_fwd(mgb_lib, dtype, rows, cols):
+@pytest.mark.parametrize("kernel", ["tma", "warp", "block"])
+@pytest.mark.parametrize("dtype,rows,cols", [("bf16", 300, 1024), ("bf16", 7, 4096), ("f32", 64, 256),
+                                             ("bf16", 5000, 4096), ("bf16", 1000, 256),
+                                             ("bf16", 333, 2048), ("bf16", 40, 1032)])
+def test_layernorm_fwd(mgb_lib, monkeypatch, kernel, dtype, rows, cols):
+    """Each forward kernel (rows streamed into shared memory by bulk copies,
+    one warp per row with register prefetch, one block per row): many rows per
+    CTA (the shared-memory ring refilled several times), few rows, and widths
+    only the block kernel takes."""
+    monkeypatch.setenv("MGB_LN_KERNEL", kernel)
     x = RNG.standard_normal((rows, cols)) * 2 + 0.5
     g, b = 1 + 0.1 * RNG.standard_normal(cols), 0.1 * RNG.standard_normal(cols)
     if dtype == "bf16":
