@@ -543,7 +543,13 @@ mgb_status fwd_tc_d(const AttnArgs& a, cudaStream_t st) {
 
 }  // namespace
 
+mgb_status attention_tc2_fwd(const AttnArgs& a, cudaStream_t st);
+
+// Two query tiles per work item (attention_tc2.cu) unless MGB_ATTN_FWD=1 picks
+// the one-tile kernel above.
 mgb_status attention_tc_fwd(const AttnArgs& a, cudaStream_t st) {
+  const char* v = getenv("MGB_ATTN_FWD");
+  if (!(v != nullptr && v[0] == '1')) return attention_tc2_fwd(a, st);
   const bool drop = a.drop_thr < 256;
   if (drop && (a.drop_mask == nullptr || a.drop_offset % 16 || a.drop_thr == 0))
     return MGB_ERR_INVALID_ARG;
