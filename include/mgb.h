@@ -57,7 +57,12 @@ typedef enum {
   MGB_ERR_ARCH = -5,                /* current device is not sm_103 */
   MGB_ERR_CUDA = -6,                /* a CUDA runtime call failed */
   MGB_ERR_DEVICE_TIMEOUT = -7,      /* a bounded device-side wait ran out */
-  MGB_ERR_NOT_IMPLEMENTED = -8
+  MGB_ERR_NOT_IMPLEMENTED = -8,
+  MGB_ERR_DEVICE_CHECK = -9         /* checking build (libmgb_check.so) only: a kernel's
+                                       own consistency check failed (an output address
+                                       outside its tensor, a misaligned TMA coordinate,
+                                       a CE target outside [0, vocab)); the access it
+                                       guards was skipped */
 } mgb_status;
 
 typedef enum { MGB_F32 = 0, MGB_BF16 = 1 } mgb_dtype;
@@ -485,7 +490,8 @@ mgb_status mgb_memcpy_async(void* dst, const void* src, size_t bytes, void* stre
 
 /* Synchronises `stream`, then returns and clears the current device's error
  * word (MGB_ERR_DEVICE_TIMEOUT if a bounded device wait ran out since the last
- * call, else MGB_OK), or MGB_ERR_CUDA if the synchronisation failed. */
+ * call; MGB_ERR_DEVICE_CHECK if a device-side check of the checking build
+ * failed; else MGB_OK), or MGB_ERR_CUDA if the synchronisation failed. */
 mgb_status mgb_device_status(void* stream);
 
 /* Launches one block that waits on a device flag nothing ever sets, bounded

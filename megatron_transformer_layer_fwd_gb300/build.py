@@ -19,6 +19,10 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libmgb.so")
+# the checking build: kernels compiled with -DMGB_CHECK=1 (device-side
+# consistency checks that record MGB_ERR_DEVICE_CHECK); loaded by MGB_LIB=check
+BUILD_CHECK = os.path.join(HERE, "_build_check")
+LIB_CHECK = os.path.join(HERE, "libmgb_check.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
@@ -40,8 +44,8 @@ def _stamp(paths) -> float:
     return max(os.path.getmtime(p) for p in paths)
 
 
-def _compile(src: str, extra: list[str]) -> str:
-    obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
+def _compile(src: str, extra: list[str], bdir: str = BUILD) -> str:
+    obj = os.path.join(bdir, os.path.basename(src)[:-3] + ".o")
     cmd = [nvcc(), *ARCH, *FLAGS, *extra, "-c", src, "-o", obj]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
@@ -49,27 +53,32 @@ def _compile(src: str, extra: list[str]) -> str:
     return obj
 
 
-def build(force: bool = False, verbose: bool = False, extra: list[str] | None = None) -> str:
-    """Compile csrc/*.cu and link libmgb.so; skipped when it is up to date."""
+def build(force: bool = False, verbose: bool = False, extra: list[str] | None = None,
+          check: bool = False) -> str:
+    """Compile csrc/*.cu and link libmgb.so (check: libmgb_check.so with the
+    device-side checks); skipped when it is up to date."""
     extra = list(extra or [])
+    lib, bdir = (LIB_CHECK, BUILD_CHECK) if check else (LIB, BUILD)
+    if check:
+        extra.append("-DMGB_CHECK=1")
     srcs = sources()
     headers = [os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".cuh", ".h"))]
     headers.append(os.path.join(os.path.dirname(HERE), "include", "mgb.h"))
-    if not force and os.path.exists(LIB) and os.path.getmtime(LIB) >= _stamp(srcs + headers):
-        return LIB
-    os.makedirs(BUILD, exist_ok=True)
+    if not force and os.path.exists(lib) and os.path.getmtime(lib) >= _stamp(srcs + headers):
+        return lib
+    os.makedirs(bdir, exist_ok=True)
     if verbose:
         extra.append("-Xptxas=-v")
     with concurrent.futures.ThreadPoolExecutor(max_workers=min(8, os.cpu_count() or 4)) as ex:
-        objs = list(ex.map(lambda s: _compile(s, extra), srcs))
-    tmp = LIB + ".tmp"
+        objs = list(ex.map(lambda s: _compile(s, extra, bdir), srcs))
+    tmp = lib + ".tmp"
     cmd = [nvcc(), *ARCH, "-shared", "-o", tmp, *objs, "-cudart", "static"]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv))
+    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv, check="--check" in sys.argv))

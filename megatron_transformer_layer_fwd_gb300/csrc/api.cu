@@ -329,6 +329,7 @@ const char* mgb_status_string(mgb_status s) {
     case MGB_ERR_CUDA: return "CUDA runtime error";
     case MGB_ERR_DEVICE_TIMEOUT: return "a bounded device-side wait ran out";
     case MGB_ERR_NOT_IMPLEMENTED: return "not implemented";
+    case MGB_ERR_DEVICE_CHECK: return "a device-side consistency check failed (checking build)";
   }
   return "unknown status";
 }
@@ -341,7 +342,8 @@ mgb_status mgb_device_status(void* stream) {
     const int zero = 0;
     if (cudaMemcpyToSymbol(g_error_word, &zero, sizeof(int)) != cudaSuccess) return MGB_ERR_CUDA;
   }
-  return (w & kErrTimeout) ? MGB_ERR_DEVICE_TIMEOUT : MGB_OK;
+  if (w & kErrTimeout) return MGB_ERR_DEVICE_TIMEOUT;
+  return (w & kErrCheck) ? MGB_ERR_DEVICE_CHECK : MGB_OK;
 }
 
 mgb_status mgb_memcpy_async(void* dst, const void* src, size_t bytes, void* stream) {
@@ -816,6 +818,7 @@ mgb_status mgb_vocab_ce_fwd_bwd(const mgb_ce_desc* desc, const void* hidden, con
   float* dh_acc = at<float>(ws, p.dh);
   float* bl = at<float>(ws, p.bl);
   const bf16* E = static_cast<const bf16*>(emb);
+  MGB_TRY(ce_check_targets_launch(T, V, targets, st));
   if (desc->mode == MGB_CE_BLOCKED)
     return ce_blocked(desc, p, hidden, E, targets, loss_per_token, loss_mean, lse_buf, d_hidden,
                       d_emb, ws, st);

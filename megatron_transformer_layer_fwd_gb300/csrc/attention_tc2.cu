@@ -184,6 +184,14 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         const Item w = item_of(i, p);
         const int grow0 = w.b * p.S;
         const int xcol = (w.h / (p.nq / p.nkv)) * D;
+        // the item lies in the problem and the TMA x coordinates are 16-byte
+        // multiples (head columns: multiples of 64)
+        if (!dcheck(w.q0 >= 0 && w.q0 < p.S && w.b < p.B && w.h < p.nq && (xcol & 7) == 0 &&
+                        ((w.h * D) & 7) == 0,
+                    p.err)) {
+          *abort = 1;
+          break;
+        }
         if (k >= 1 && !mbar_wait(q_empty, (k - 1) & 1, p.err)) {
           *abort = 1;
           break;

@@ -17,12 +17,32 @@ typedef __nv_bfloat16 bf16;
 // Kernels that wait on barriers get a pointer to the per-device error word
 // (owned by the C-ABI translation unit) and OR-in MGB error bits;
 // mgb_device_status() reads and clears it.
-enum : int { kErrTimeout = 1 };
+enum : int { kErrTimeout = 1, kErrCheck = 2 };
 // Upper bound of any single device-side wait, in nanoseconds.
 constexpr unsigned long long kWaitLimitNs = 2000000000ull;
 
 __device__ __forceinline__ void record_error(int* err, int bits) {
   if (err != nullptr) atomicOr(err, bits);
+}
+
+// Device-side consistency checks, compiled in only in the checking build of
+// the library (-DMGB_CHECK=1: libmgb_check.so). dcheck(ok, err) is true when
+// `ok` holds; otherwise it records kErrCheck (read back as
+// MGB_ERR_DEVICE_CHECK) and returns false, and the caller skips the access
+// it guards. In the normal build it is always true and costs nothing.
+#ifndef MGB_CHECK
+#define MGB_CHECK 0
+#endif
+__device__ __forceinline__ bool dcheck(bool ok, int* err) {
+#if MGB_CHECK
+  if (!ok) {
+    record_error(err, kErrCheck);
+    return false;
+  }
+#endif
+  (void)ok;
+  (void)err;
+  return true;
 }
 
 __device__ __forceinline__ uint64_t global_ns() {

@@ -207,7 +207,26 @@ __global__ void __launch_bounds__(CE_THREADS) ce_grad_kernel(int T, int C, int v
   }
 }
 
+// Checking build: every target id lies in [0, vocab).
+__global__ void ce_check_targets_kernel(int T, int V, const int32_t* __restrict__ tgt, int* err) {
+  for (int i = blockIdx.x * blockDim.x + threadIdx.x; i < T; i += gridDim.x * blockDim.x)
+    dcheck(tgt[i] >= 0 && tgt[i] < V, err);
+}
+
 }  // namespace
+
+mgb_status ce_check_targets_launch(int T, int V, const int32_t* targets, cudaStream_t st) {
+#if MGB_CHECK
+  if (T > 0) {
+    LaunchScope scope(PROF_CE_COMBINE, st);
+    ce_check_targets_kernel<<<(T + 255) / 256 < 1024 ? (T + 255) / 256 : 1024, 256, 0, st>>>(
+        T, V, targets, device_error_word());
+  }
+#else
+  (void)T; (void)V; (void)targets; (void)st;
+#endif
+  return MGB_OK;
+}
 
 mgb_status ce_stats_launch(int T, int C, int v0, const void* logits, int64_t ldl,
                            const int32_t* targets, float* m, float* s, float* t, cudaStream_t st) {

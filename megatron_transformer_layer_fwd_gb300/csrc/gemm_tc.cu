@@ -347,6 +347,8 @@ __device__ void epilogue_row(const EpiParams& p, uint32_t tmem_row, int row, int
   // target column of this row relative to the tile (CE logits: fp32 capture)
   int tcol = -1;
   if (p.tgt != nullptr && row_ok) tcol = p.tgt[row] - p.tgt_v0 - n0;
+  // every element this row stores lies in the M x N output
+  if (!dcheck(row >= 0 && n0 >= 0 && (n0 & 7) == 0, p.err)) return;
   for (int lc = 0; lc < BN; lc += 32) {
     float acc[32];
     tmem_chunk(tmem_row + lc, p.alpha, have_acc, acc);
@@ -466,7 +468,7 @@ __device__ void epilogue_f32_tma(const EpiParams& p, const CUtensorMap* tmC, uin
                    acc[4 * j + 3]);
     fence_proxy_async();
     __syncwarp();
-    if (lane == 0) {
+    if (lane == 0 && dcheck((n & 3) == 0 && row0 >= 0, p.err)) {
       if (p.c_tma == 2)
         tma_reduce_add_2d(tmC, box, n, row0);
       else
@@ -506,6 +508,13 @@ __device__ __forceinline__ void tile_decode(const EpiParams& p, int tile, int bn
   }
   kb0 = split * p.kb_per_split;
   kb1 = min(num_k, kb0 + p.kb_per_split);
+}
+
+// Columns the tile grid spans: N, or with column chunks the whole chunk grid
+// (a ragged last chunk can hold a tile that starts past N: its loads read the
+// fill value and its epilogue stores nothing).
+__device__ __forceinline__ int n_extent(const EpiParams& p) {
+  return p.n_chunk > 0 ? (p.N + p.n_chunk - 1) / p.n_chunk * p.n_chunk : p.N;
 }
 
 // Column chunk of a tile at n0 (column chunks on): first column, end, first
@@ -591,8 +600,17 @@ __global__ void __launch_bounds__(192, 1)
           const uint32_t sa = tiles + s * C::STAGE_BYTES;
           const uint32_t sb = sa + C::A_BYTES;
           const uint32_t fb = full0 + 8 * s;
-          mbar_arrive_expect_tx(fb, C::STAGE_BYTES);
           const int k0 = kb * BK;
+          // the tile lies in the problem and every TMA x coordinate is a
+          // multiple of 8 bf16 (16 bytes); a failed check skips the copies
+          // (the stage then never fills and the bounded waits end the kernel)
+          if (!dcheck(m0 < p.M && n0 < n_extent(p) && kb < num_k && (k0 & 7) == 0 &&
+                          (m0 & 7) == 0 && (n0 & 7) == 0,
+                      p.err)) {
+            *abort = 1;
+            break;
+          }
+          mbar_arrive_expect_tx(fb, C::STAGE_BYTES);
           if (A_MN == 0) {
             tma_load_2d(sa, &tmA, k0, m0, fb);
           } else {
@@ -775,8 +793,14 @@ __global__ void __launch_bounds__(192, 1)
           const uint32_t sa = tiles + s * STAGE_BYTES;
           const uint32_t sb = sa + A_BYTES;
           const uint32_t fb = mapa_shared(full0 + 8 * s, 0);
-          if (rank == 0) mbar_arrive_expect_tx(full0 + 8 * s, 2 * STAGE_BYTES);
           const int k0 = kb * BK;
+          if (!dcheck(m0 < p.M && n0 < n_extent(p) && kb < num_k && (k0 & 7) == 0 &&
+                          (ma & 7) == 0 && (nb & 7) == 0,
+                      p.err)) {
+            *abort = 1;
+            break;
+          }
+          if (rank == 0) mbar_arrive_expect_tx(full0 + 8 * s, 2 * STAGE_BYTES);
           if (A_MN == 0) {
             tma_load_2d_pair(sa, &tmA, k0, ma, fb);
           } else {

@@ -147,8 +147,13 @@ __global__ void __launch_bounds__(192, 1)
           }
           const uint32_t st = tiles + s * TSTAGE;
           const uint32_t fb = full0 + 8 * s;
-          mbar_arrive_expect_tx(fb, TSTAGE);
           const int k0 = kb * TBK;
+          // x coordinates multiples of 4 float32 (16 bytes), tile inside the problem
+          if (!dcheck((k0 & 3) == 0 && m0 < p.e.M && n0 < p.e.N, p.err)) {
+            *abort = 1;
+            break;
+          }
+          mbar_arrive_expect_tx(fb, TSTAGE);
           tma_load_2d(st, &tmAh, k0, m0, fb);
           tma_load_2d(st + TILE4, &tmAl, k0, m0, fb);
           tma_load_2d(st + 2 * TILE4, &tmBh, k0, n0, fb);

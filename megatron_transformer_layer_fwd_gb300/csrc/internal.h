@@ -249,6 +249,9 @@ mgb_status ce_combine_launch(int T, int n_parts, const float* m, const float* s,
                              const float* t, float* lse, float* loss, float* loss_mean,
                              float* block_loss, float* split, cudaStream_t st);
 inline int ce_combine_blocks(int T) { return (T + 255) / 256; }
+// Checking build (MGB_CHECK): records MGB_ERR_DEVICE_CHECK when a target id is
+// outside [0, V); no launch in the normal build.
+mgb_status ce_check_targets_launch(int T, int V, const int32_t* targets, cudaStream_t st);
 // loss_mean = (sum of the first nb block sums, fixed order) / T.
 mgb_status ce_mean_launch(int nb, int T, const float* block_loss, float* loss_mean,
                           cudaStream_t st);

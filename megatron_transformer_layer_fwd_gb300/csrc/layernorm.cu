@@ -343,8 +343,16 @@ __global__ void __launch_bounds__(32 * (1 + kLnConsumers), VPL >= 16 ? 1 : 2) ln
           break;
         }
         const int row = blockIdx.x + i * gridDim.x;
+        const bf16* src = x + (int64_t)row * cols;
+        // bulk copies need 16-byte aligned addresses and sizes
+        if (!dcheck(row < rows && (reinterpret_cast<uintptr_t>(src) & 15) == 0 &&
+                        (slot_bytes & 15) == 0,
+                    err)) {
+          *abort = 1;
+          break;
+        }
         mbar_arrive_expect_tx(full0 + 8 * s, slot_bytes);
-        bulk_load(slots + s * slot_bytes, x + (int64_t)row * cols, slot_bytes, full0 + 8 * s);
+        bulk_load(slots + s * slot_bytes, src, slot_bytes, full0 + 8 * s);
       }
     }
   } else {

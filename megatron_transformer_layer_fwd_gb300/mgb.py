@@ -14,7 +14,9 @@ import re
 from typing import Optional
 
 HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(HERE, "libmgb.so")
+# MGB_LIB=check loads the checking build (device-side consistency checks)
+LIB_PATH = os.path.join(HERE, "libmgb_check.so" if os.environ.get("MGB_LIB") == "check"
+                        else "libmgb.so")
 HEADER = os.path.join(os.path.dirname(HERE), "include", "mgb.h")
 
 MGB_OK = 0
@@ -26,6 +28,7 @@ MGB_ERR_ARCH = -5
 MGB_ERR_CUDA = -6
 MGB_ERR_DEVICE_TIMEOUT = -7
 MGB_ERR_NOT_IMPLEMENTED = -8
+MGB_ERR_DEVICE_CHECK = -9
 
 MGB_F32, MGB_BF16 = 0, 1
 MGB_CE_STREAM, MGB_CE_FUSED, MGB_CE_RESIDENT, MGB_CE_BLOCKED = 0, 1, 2, 3

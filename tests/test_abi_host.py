@@ -299,3 +299,16 @@ def test_embedding_validation(lib):
     assert mgb.mgb_embedding_bwd_ws_bytes(100, 10, 10) == 0
     assert lib.mgb_embedding_bwd(100, 64, 10, 60, mgb.MGB_BF16, p, p, p, 1, p, need - 16,
                                  None) == mgb.MGB_ERR_WORKSPACE_TOO_SMALL
+
+
+def test_checking_build_exports_the_same_calls():
+    """The checking build (device-side checks, -DMGB_CHECK=1) compiles and
+    exports every call of the header, like the normal build."""
+    import ctypes as ct
+    from megatron_transformer_layer_fwd_gb300 import build
+    path = build.build(check=True)
+    lib = ct.CDLL(path)
+    for name in mgb.header_functions():
+        assert hasattr(lib, name), name
+    lib.mgb_status_string.restype = ct.c_char_p
+    assert b"check" in lib.mgb_status_string(mgb.MGB_ERR_DEVICE_CHECK)
