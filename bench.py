@@ -568,6 +568,45 @@ def run_case(args):
         print(json.dumps({"case": "gemm", "mnk": [M, N, K], "ms": round(ms, 4), "tflops": round(tf, 1),
                           "frac_of_burst_peak": round(tf / peaks["bf16_tflops"], 4)}))
         return
+    if args.case == "gemm_f32":
+        # the float32 product (forward layout) as three TF32 tensor-core
+        # products, beside the FFMA path and cuBLAS float32 / single-TF32 for
+        # scale; the tensor pipe runs 3 x 2MNK TF32 FLOPs, against the
+        # measured bf16 burst peak x the nominal TF32 / bf16 ratio (1.1 / 2.25)
+        M, N, K = args.mnk
+        a = torch.randn(M, K, device="cuda")
+        b = torch.randn(N, K, device="cuda")
+        c = torch.empty(M, N, device="cuda")
+        ws = torch.empty(mgb.mgb_gemm_f32_tc_ws_bytes(M, N, K), dtype=torch.uint8, device="cuda")
+        d = mgb.GemmExDesc(g=mgb.GemmDesc(m=M, n=N, k=K, a_major=0, b_major=0, lda=K, ldb=K, ldc=N,
+                                          dtype=mgb.MGB_F32, c_f32=0, accumulate=0, alpha=1.0),
+                           epilogue=mgb.MGB_EPI_STORE, glu_block=16, ldc2=0, ldr=0, ldaux=0)
+        fl = 2.0 * M * N * K
+        tf32_peak = peaks["bf16_tflops"] * 1.1 / 2.25
+        ref = (a.double() @ b.double().t())
+        runs = [("tf32x3", lambda: mgb.mgb_gemm_f32_tc(d, a, b, None, c, ws=ws)),
+                ("ffma", lambda: mgb.mgb_gemm_ex(d, a, b, None, c))]
+        for name, fn in runs:
+            ms, prof = _time_loop(fn, args.steps if name == "tf32x3" else 3, args.warmup, st)
+            err = float(torch.linalg.norm(c.double() - ref) / torch.linalg.norm(ref))
+            out = {"case": "gemm_f32_" + name, "mnk": [M, N, K], "ms": round(ms, 4),
+                   "tflops": round(fl / (ms / 1e3) / 1e12, 1), "rel_l2_vs_f64": err,
+                   "kernel_ms": prof}
+            if name == "tf32x3":
+                out["tensor_tflops"] = round(3 * fl / (ms / 1e3) / 1e12, 1)
+                out["tf32_peak"] = round(tf32_peak, 1)
+                out["frac_of_tf32_peak"] = round(3 * fl / (ms / 1e3) / 1e12 / tf32_peak, 4)
+            print(json.dumps(out), flush=True)
+        for name, tf in (("cublas_fp32", False), ("cublas_tf32_single", True)):
+            torch.backends.cuda.matmul.allow_tf32 = tf
+            ms, _ = _time_loop(lambda: torch.matmul(a, b.t(), out=c), 3 if not tf else args.steps,
+                               args.warmup, st)
+            err = float(torch.linalg.norm(c.double() - ref) / torch.linalg.norm(ref))
+            print(json.dumps({"case": "gemm_f32_" + name, "mnk": [M, N, K], "ms": round(ms, 4),
+                              "tflops": round(fl / (ms / 1e3) / 1e12, 1), "rel_l2_vs_f64": err}),
+                  flush=True)
+        torch.backends.cuda.matmul.allow_tf32 = False
+        return
     if args.case == "gemm_layer":
         # the layer's twelve GEMM shapes and operand layouts (forward, input
         # gradient, weight gradient), each alone, beside torch.matmul (cuBLAS)
@@ -795,8 +834,8 @@ def main():
     ap.add_argument("--no-sweep", action="store_true",
                     help="skip the sequence sweep of the causal workloads in the step run")
     ap.add_argument("--case", default="step",
-                    choices=("step", "layer", "sweep", "ce", "gemm", "gemm_layer", "attention",
-                             "embedding", "ln"),
+                    choices=("step", "layer", "sweep", "ce", "gemm", "gemm_f32", "gemm_layer",
+                             "attention", "embedding", "ln"),
                     help="step (default: the whole hot path, one JSON line) or a sub-path / single kernel")
     ap.add_argument("--mnk", type=int, nargs=3, default=(8192, 22016, 4096))
     ap.add_argument("--dropout", type=float, default=0.0,

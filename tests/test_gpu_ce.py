@@ -51,6 +51,27 @@ def test_ce_blocked_token_blocks(mgb_lib, T, H, V, C, tb):
     assert torch.equal(first[2], r.d_emb)
 
 
+def test_ce_blocked_block_size_changes_only_rounding(mgb_lib):
+    """The token block is a memory device: token blocks of 256, 768, 1024 and one
+    larger than T give the same per-token losses, mean and gradients up to
+    float32 rounding order (each also within tolerance of the oracle)."""
+    shape = CEShape(1000, 256, 3000, 1000)
+    inp = ce_inputs(shape, seed=33)
+    loss, lse, mean, _ = oracle.ce_chunked(inp["hidden"], inp["emb"], inp["targets"], shape.chunk)
+    outs = []
+    for tb in (256, 768, 1024, 4096):
+        r = _runner(shape, inp, mgb.MGB_CE_BLOCKED, token_block=tb)
+        r.run()
+        assert mgb.mgb_device_status() == mgb.MGB_OK
+        assert np.abs(to_np(r.loss) - loss).max() < CE_LOSS_ABS
+        outs.append((to_np(r.loss), float(r.loss_mean[0]), to_np(r.d_hidden), to_np(r.d_emb)))
+    for o in outs[1:]:
+        assert np.abs(o[0] - outs[0][0]).max() < 1e-5
+        assert abs(o[1] - outs[0][1]) < 1e-6
+        assert rel_l2(o[2], outs[0][2]) < 1e-2
+        assert rel_l2(o[3], outs[0][3]) < 1e-2
+
+
 def test_ce_blocked_emb_stream(mgb_lib):
     """Blocked mode with the last block's d_emb left on a caller's stream:
     after joining it, the results equal those of the joined call bit for bit."""
