@@ -82,6 +82,10 @@ struct EpiParams {
   // EPI_F32 through TMA (0 off): 1 stores, 2 reduce-adds each staged 32 x 32
   // float32 box into C (tensor map tmC)
   int c_tma;
+  // bf16 outputs through TMA (0 off, 1 on): every 32-column chunk of the
+  // warp's 32 rows is staged in shared memory and stored by a bulk tensor
+  // copy: C (or the kept logits of EPI_CE_STATS) through tmC, C2 through tmC2
+  int o_tma;
   // column chunks (EPI_CE_STATS / EPI_CE_GRAD; 0 = off): the N columns are cut
   // into chunks of n_chunk, tpc column tiles each, so no tile straddles two
   // chunks; a chunk's statistics groups start at its first column (gpc groups
@@ -167,9 +171,11 @@ __device__ __forceinline__ void colsum32_store(float* part, int64_t ld, int row,
   if ((row & ~31) < M && c0 + lane < ncols) part[(int64_t)(row >> 5) * ld + c0 + lane] = v[0];
 }
 
-// Epilogue for one thread = one output row `row` of the tile.
+// Epilogue for one thread = one output row `row` of the tile. The epilogue
+// functions are kept out of line: a kernel whose epilogue code is inlined in
+// full (every kind, both store paths) ran its products about 1 % slower.
 template <int BN>
-__device__ void epilogue_row(const EpiParams& p, uint32_t tmem_row, int row, int n0,
+__device__ __noinline__ void epilogue_row(const EpiParams& p, uint32_t tmem_row, int row, int n0,
                              bool have_acc, int64_t c_off = 0, int cbase = 0, int nend = INT_MAX,
                              int pbase = 0) {
   const bool row_ok = row < p.M;
@@ -449,7 +455,7 @@ __device__ void epilogue_row(const EpiParams& p, uint32_t tmem_row, int row, int
 // copy; rows and columns past C's edges are clipped by the copy. Two boxes
 // per warp alternate; `cnt` counts the warp's boxes so far.
 template <int BN>
-__device__ void epilogue_f32_tma(const EpiParams& p, const CUtensorMap* tmC, uint32_t tmem_row,
+__device__ __noinline__ void epilogue_f32_tma(const EpiParams& p, const CUtensorMap* tmC, uint32_t tmem_row,
                                  int row0, int n0, bool have_acc, uint32_t stage, uint32_t& cnt) {
   const int lane = threadIdx.x & 31;
   for (int lc = 0; lc < BN; lc += 32) {
@@ -476,6 +482,250 @@ __device__ void epilogue_f32_tma(const EpiParams& p, const CUtensorMap* tmC, uin
       bulk_commit();
     }
     ++cnt;
+  }
+}
+
+// One 32-column bf16 chunk of a warp's 32 rows (row row0 + lane holds v[0..31])
+// through TMA: the lane's values go to a shared-memory box in the 64-byte
+// swizzled layout of the tensor map (16-byte chunk j of row r at
+// r * 64 + ((j ^ ((r / 2) % 4)) * 16): conflict-free vector stores), then one
+// lane stores the box at column n with a bulk tensor copy, which clips rows
+// and columns past the tensor's edges. Four 2 KB boxes per warp take turns;
+// `cnt` counts the warp's boxes so far. Every lane of the warp calls it.
+__device__ __forceinline__ void put32_tma(const CUtensorMap* tm, uint32_t stage, uint32_t& cnt,
+                                          int n, int row0, const float* v, int* err) {
+  const int lane = threadIdx.x & 31;
+  const uint32_t box = stage + (cnt & 3) * 2048;
+  if (lane == 0) bulk_wait_read<3>();  // the copy that last read this box is done
+  __syncwarp();
+  const uint32_t rb = box + lane * 64;
+  const uint32_t sw = (lane >> 1) & 3;
+#pragma unroll
+  for (int j = 0; j < 4; ++j)
+    st_shared_v4u(rb + ((j ^ sw) << 4), pack_bf16x2(v[8 * j], v[8 * j + 1]),
+                  pack_bf16x2(v[8 * j + 2], v[8 * j + 3]), pack_bf16x2(v[8 * j + 4], v[8 * j + 5]),
+                  pack_bf16x2(v[8 * j + 6], v[8 * j + 7]));
+  fence_proxy_async();
+  __syncwarp();
+  if (lane == 0 && dcheck((n & 31) == 0 && n >= 0 && row0 >= 0, err)) {
+    tma_store_2d(tm, box, n, row0);
+    bulk_commit();
+  }
+  ++cnt;
+}
+
+// The bf16-output epilogues with every store through put32_tma, for one warp
+// (rows row0 .. row0 + 31, lane = row): the arithmetic of epilogue_row, with
+// the loads of rows past M skipped (their staged values are clipped by the
+// copy). cbase / nend / pbase: the column chunk of an EPI_CE_STATS tile.
+template <int BN>
+__device__ __noinline__ void epilogue_tma16(const EpiParams& p, const CUtensorMap* tmC, const CUtensorMap* tmC2,
+                               uint32_t tmem_row, int row0, int n0, bool have_acc, uint32_t stage,
+                               uint32_t& cnt, int cbase, int nend, int pbase) {
+  const int lane = threadIdx.x & 31;
+  const int row = row0 + lane;
+  const bool row_ok = row < p.M;
+  const bool warp_in = row0 < p.M;  // the same for the whole warp
+  if (p.epi == EPI_BIAS_SWIGLU) {
+    const int gb = p.glu_block;
+    for (int lc = 0; lc < BN; lc += 32) {
+      if ((lc / gb) & 1) continue;  // visit gate chunks; the up chunk is gb further
+      float g[32], u[32];
+      tmem_chunk(tmem_row + lc, p.alpha, have_acc, g);
+      tmem_chunk(tmem_row + lc + gb, p.alpha, have_acc, u);
+      const int ng = n0 + lc, nu = ng + gb;
+      if (!warp_in || ng >= p.N) continue;
+      add_bias32(p.bias, ng, p.N, g);
+      add_bias32(p.bias, nu, p.N, u);
+      const int na = (ng / (2 * gb)) * gb + (ng % gb);
+      float a[32];
+#pragma unroll
+      for (int j = 0; j < 32; ++j) a[j] = g[j] * sigmoidf_(g[j]) * u[j];
+      put32_tma(tmC, stage, cnt, ng, row0, g, p.err);
+      put32_tma(tmC, stage, cnt, nu, row0, u, p.err);
+      put32_tma(tmC2, stage, cnt, na, row0, a, p.err);
+    }
+    return;
+  }
+  if (p.epi == EPI_CE_STATS) {
+    // as epilogue_row: (max, sum exp) per 128-column group from the float32
+    // accumulator; the kept bf16 logits (if any) go out through TMA
+    const int NE = min(p.N, nend);
+    int tcol = -1;
+    if (p.tgt != nullptr && row_ok) tcol = p.tgt[row] - p.tgt_v0 - n0;
+    float* pm = reinterpret_cast<float*>(p.C);
+    float* ps = reinterpret_cast<float*>(p.C2);
+    for (int h = 0; h < BN; h += 128) {
+      float mx = -INFINITY, sum = 0.0f;
+      for (int lc = h; lc < h + 128; lc += 32) {
+        float acc[32];
+        tmem_chunk(tmem_row + lc, p.alpha, have_acc, acc);
+        const int n = n0 + lc;
+        if (!warp_in || n >= NE) continue;
+        const int tc = tcol - lc;
+        if (tc >= 0 && tc < 32 && n + tc < NE) {
+          float v = 0.0f;
+#pragma unroll
+          for (int j = 0; j < 32; ++j) v = (j == tc) ? acc[j] : v;
+          p.tgt_out[row] = v;
+        }
+        if (p.keep != nullptr) put32_tma(tmC, stage, cnt, n, row0, acc, p.err);
+        float cm = -INFINITY;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          acc[j] = n + j < NE ? acc[j] * 1.4426950408889634f : -INFINITY;
+          cm = fmaxf(cm, acc[j]);
+        }
+        if (cm > mx) {
+          sum = mx == -INFINITY ? 0.0f : sum * ex2_ftz(mx - cm);
+          mx = cm;
+        }
+#pragma unroll
+        for (int j = 0; j < 32; ++j) sum += ex2_ftz(acc[j] - mx);
+      }
+      const int n = n0 + h;
+      if (row_ok && n < NE) {
+        const int64_t o = (int64_t)(pbase + (n - cbase) / 128) * p.M + row;
+        pm[o] = mx * 0.6931471805599453f;
+        ps[o] = sum;
+      }
+    }
+    return;
+  }
+  if (p.epi == EPI_DGELU) {
+    for (int lc = 0; lc < BN; lc += 32) {
+      float acc[32];
+      tmem_chunk(tmem_row + lc, p.alpha, have_acc, acc);
+      const int n = n0 + lc;
+      if (n >= p.N) continue;  // the same for the whole warp
+      if (row_ok) {
+        const bf16* ua = p.aux + (int64_t)row * p.ldaux + n;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          if (n + 8 * q < p.N) {
+            float u[8];
+            load8(ua + 8 * q, u);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) acc[8 * q + j] *= gelu_erf_grad(u[j]);
+          } else {
+#pragma unroll
+            for (int j = 0; j < 8; ++j) acc[8 * q + j] = 0.0f;
+          }
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) acc[j] = 0.0f;
+      }
+      if (warp_in) put32_tma(tmC, stage, cnt, n, row0, acc, p.err);
+      if (p.cpart) colsum32_store(p.cpart, p.N, row, p.M, n, p.N, acc);
+    }
+    return;
+  }
+  if (p.epi == EPI_DSWIGLU) {
+    const int gb = p.glu_block;
+    for (int lc = 0; lc < BN; lc += 32) {
+      float acc[32];
+      tmem_chunk(tmem_row + lc, p.alpha, have_acc, acc);
+      const int n = n0 + lc;
+      if (n >= p.N) continue;  // the same for the whole warp
+      const int i = n / gb, cc = n % gb;
+      const int colg = 2 * i * gb + cc, colu = colg + gb;
+      float dg[32], du[32];
+      if (row_ok) {
+        const bf16* ar = p.aux + (int64_t)row * p.ldaux;
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          float g[8], u[8];
+          load8(ar + colg + 8 * q, g);
+          load8(ar + colu + 8 * q, u);
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const float sg = sigmoidf_(g[j]);
+            const float da = acc[8 * q + j];
+            du[8 * q + j] = da * g[j] * sg;
+            dg[8 * q + j] = da * u[j] * sg * (1.0f + g[j] * (1.0f - sg));
+          }
+        }
+      } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) dg[j] = du[j] = 0.0f;
+      }
+      if (warp_in) {
+        put32_tma(tmC, stage, cnt, colg, row0, dg, p.err);
+        put32_tma(tmC, stage, cnt, colu, row0, du, p.err);
+      }
+      if (p.cpart) {
+        colsum32_store(p.cpart, 2 * (int64_t)p.N, row, p.M, colg, 2 * p.N, dg);
+        colsum32_store(p.cpart, 2 * (int64_t)p.N, row, p.M, colu, 2 * p.N, du);
+      }
+    }
+    return;
+  }
+  // EPI_STORE, EPI_BIAS_GELU, EPI_BIAS_RESID: one loop each, so the loop a
+  // tile runs holds only its own epilogue's instructions
+  if (p.epi == EPI_STORE) {
+    int tcol = -1;
+    if (p.tgt != nullptr && row_ok) tcol = p.tgt[row] - p.tgt_v0 - n0;
+    for (int lc = 0; lc < BN; lc += 32) {
+      float acc[32];
+      tmem_chunk(tmem_row + lc, p.alpha, have_acc, acc);
+      const int n = n0 + lc;
+      if (!warp_in || n >= p.N) continue;
+      add_bias32(p.bias, n, p.N, acc);
+      const int tc = tcol - lc;
+      if (tc >= 0 && tc < 32 && n + tc < p.N) {
+        float v = 0.0f;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v = (j == tc) ? acc[j] : v;
+        p.tgt_out[row] = v;
+      }
+      put32_tma(tmC, stage, cnt, n, row0, acc, p.err);
+    }
+    return;
+  }
+  if (p.epi == EPI_BIAS_GELU) {
+    for (int lc = 0; lc < BN; lc += 32) {
+      float acc[32];
+      tmem_chunk(tmem_row + lc, p.alpha, have_acc, acc);
+      const int n = n0 + lc;
+      if (!warp_in || n >= p.N) continue;
+      add_bias32(p.bias, n, p.N, acc);
+      float a[32];
+#pragma unroll
+      for (int j = 0; j < 32; ++j) a[j] = gelu_erf(acc[j]);
+      put32_tma(tmC, stage, cnt, n, row0, acc, p.err);
+      put32_tma(tmC2, stage, cnt, n, row0, a, p.err);
+    }
+    return;
+  }
+  // EPI_BIAS_RESID
+  for (int lc = 0; lc < BN; lc += 32) {
+    float acc[32];
+    tmem_chunk(tmem_row + lc, p.alpha, have_acc, acc);
+    const int n = n0 + lc;
+    if (!warp_in || n >= p.N) continue;
+    add_bias32(p.bias, n, p.N, acc);
+    if (p.drop_thr < 256) {
+      const uint64_t q = (p.drop_offset + (uint64_t)row * p.N + n) >> 4;
+      const uint4 w0 = philox_block(p.drop_seed, q), w1 = philox_block(p.drop_seed, q + 1);
+      const uint32_t ws[8] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w};
+#pragma unroll
+      for (int j = 0; j < 32; ++j)
+        acc[j] = keep_byte(ws[j >> 2], j & 3, p.drop_thr) ? acc[j] * p.drop_scale : 0.0f;
+    }
+    if (row_ok) {
+      const bf16* r = p.resid + (int64_t)row * p.ldr + n;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        if (n + 8 * q < p.N) {
+          float x[8];
+          load8(r + 8 * q, x);
+#pragma unroll
+          for (int j = 0; j < 8; ++j) acc[8 * q + j] += x[j];
+        }
+      }
+    }
+    put32_tma(tmC, stage, cnt, n, row0, acc, p.err);
   }
 }
 
@@ -546,7 +796,9 @@ template <int BN, int STAGES, int A_MN, int B_MN>
 __global__ void __launch_bounds__(192, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA,
                    const __grid_constant__ CUtensorMap tmB,
-                   const __grid_constant__ CUtensorMap tmC, const EpiParams p) {
+                   const __grid_constant__ CUtensorMap tmC,
+                   const __grid_constant__ CUtensorMap tmC2,
+                   const __grid_constant__ EpiParams p) {
   using C = Cfg<BN, STAGES>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -691,14 +943,19 @@ __global__ void __launch_bounds__(192, 1)
       } else {
         int cb, ne, pb;
         chunk_of(p, n0, cb, ne, pb);
-        epilogue_row<BN>(p, trow, m0 + q * 32 + lane, n0, kb1 > kb0, sp * p.split_stride, cb, ne,
-                         pb);
+        if (p.o_tma)
+          epilogue_tma16<BN>(p, &tmC, &tmC2, trow, m0 + q * 32, n0, kb1 > kb0, stage, cnt, cb, ne,
+                             pb);
+        else
+          epilogue_row<BN>(p, trow, m0 + q * 32 + lane, n0, kb1 > kb0, sp * p.split_stride, cb,
+                           ne, pb);
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(acce0 + 8 * buf);
     }
-    if (p.c_tma && lane == 0) bulk_wait<0>();  // this warp's copies complete before exit
+    // this warp's copies complete before exit
+    if ((p.c_tma || p.o_tma) && lane == 0) bulk_wait<0>();
   }
 
   __syncthreads();
@@ -733,7 +990,9 @@ template <int STAGES, int A_MN, int B_MN>
 __global__ void __launch_bounds__(192, 1)
     gemm_tc_pair_kernel(const __grid_constant__ CUtensorMap tmA,
                         const __grid_constant__ CUtensorMap tmB,
-                        const __grid_constant__ CUtensorMap tmC, const EpiParams p) {
+                        const __grid_constant__ CUtensorMap tmC,
+                        const __grid_constant__ CUtensorMap tmC2,
+                        const __grid_constant__ EpiParams p) {
   constexpr int BNP = 256, HALF = 128;
   constexpr int A_BYTES = HALF * BK * 2, B_BYTES = HALF * BK * 2;
   constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
@@ -888,13 +1147,17 @@ __global__ void __launch_bounds__(192, 1)
       } else {
         int cb, ne, pb;
         chunk_of(p, n0, cb, ne, pb);
-        epilogue_row<BNP>(p, trow, r0 + lane, n0, kb1 > kb0, sp * p.split_stride, cb, ne, pb);
+        if (p.o_tma)
+          epilogue_tma16<BNP>(p, &tmC, &tmC2, trow, r0, n0, kb1 > kb0, stage, cnt, cb, ne, pb);
+        else
+          epilogue_row<BNP>(p, trow, r0 + lane, n0, kb1 > kb0, sp * p.split_stride, cb, ne, pb);
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(mapa_shared(acce0 + 8 * buf, 0));
     }
-    if (p.c_tma && lane == 0) bulk_wait<0>();  // this warp's copies complete before exit
+    // this warp's copies complete before exit
+    if ((p.c_tma || p.o_tma) && lane == 0) bulk_wait<0>();
   }
 
   __syncthreads();
@@ -958,6 +1221,45 @@ bool make_tmap_f32(CUtensorMap* tm, const void* base, uint64_t inner, uint64_t o
   return r == CUDA_SUCCESS;
 }
 
+// 2-D bf16 tensor map of an epilogue output for put32_tma: boxes of 32
+// columns x 32 rows, 64-byte swizzle.
+bool make_tmap_out(CUtensorMap* tm, const void* base, uint64_t inner, uint64_t outer, int64_t ld) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {(cuuint64_t)ld * 2};
+  cuuint32_t box[2] = {32, 32};
+  cuuint32_t es[2] = {1, 1};
+  CUresult r = fn(tm, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+                  box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// The epilogue's output maps: C (or the kept logits) and C2 for the TMA
+// epilogues (o_tma), C as float32 boxes for the float32 TMA epilogue (c_tma);
+// maps that are not read are copies of `fill`.
+bool make_out_maps(const GemmArgs& g, const EpiParams& ep, const CUtensorMap& fill, CUtensorMap* tc,
+                   CUtensorMap* tc2) {
+  *tc = fill;
+  *tc2 = fill;
+  if (ep.c_tma) return make_tmap_f32(tc, g.C, g.N, g.M, g.ldc);
+  if (!ep.o_tma) return true;
+  switch (g.epi) {
+    case EPI_CE_STATS:
+      return make_tmap_out(tc, g.keep, g.N, g.M, g.ld_keep);
+    case EPI_DSWIGLU:
+      return make_tmap_out(tc, g.C, 2 * (uint64_t)g.N, g.M, g.ldc);
+    case EPI_BIAS_SWIGLU:
+      return make_tmap_out(tc, g.C, g.N, g.M, g.ldc) &&
+             make_tmap_out(tc2, g.C2, g.N / 2, g.M, g.ldc2);
+    case EPI_BIAS_GELU:
+      return make_tmap_out(tc, g.C, g.N, g.M, g.ldc) && make_tmap_out(tc2, g.C2, g.N, g.M, g.ldc2);
+    default:
+      return make_tmap_out(tc, g.C, g.N, g.M, g.ldc);
+  }
+}
+
 // One persistent CTA per SM (the kernel's shared memory allows one), never
 // more CTAs than tiles.
 int persistent_grid(const EpiParams& ep) {
@@ -985,15 +1287,12 @@ mgb_status launch_variant(const GemmArgs& g, const EpiParams& ep, cudaStream_t s
                      : make_tmap(&tb, g.B, g.K, g.N, g.ldb, 64, BN));
     if (!ok) return MGB_ERR_CUDA;
   }
-  if (ep.c_tma) {
-    if (!make_tmap_f32(&tc, g.C, g.N, g.M, g.ldc)) return MGB_ERR_CUDA;
-  } else {
-    tc = ta;  // not read
-  }
+  CUtensorMap tc2;
+  if (!make_out_maps(g, ep, ta, &tc, &tc2)) return MGB_ERR_CUDA;
   LaunchScope scope(g.prof_kind >= 0 ? g.prof_kind
                                : (A_MN ? PROF_GEMM_WGRAD : (B_MN ? PROF_GEMM_DGRAD : PROF_GEMM_FWD)),
                     st);
-  kern<<<persistent_grid(ep), 192, C::SMEM_BYTES, st>>>(ta, tb, tc, ep);
+  kern<<<persistent_grid(ep), 192, C::SMEM_BYTES, st>>>(ta, tb, tc, tc2, ep);
   return cudaGetLastError() == cudaSuccess ? MGB_OK : MGB_ERR_CUDA;
 }
 
@@ -1013,10 +1312,8 @@ mgb_status launch_pair_variant(const GemmArgs& g, const EpiParams& ep, cudaStrea
                  : make_tmap(&ta, g.A, g.K, g.M, g.lda, 64, 128);
   ok = ok && (B_MN ? make_tmap(&tb, g.B, g.N, g.K, g.ldb, 64, 64)
                    : make_tmap(&tb, g.B, g.K, g.N, g.ldb, 64, 128));
-  if (ep.c_tma)
-    ok = ok && make_tmap_f32(&tc, g.C, g.N, g.M, g.ldc);
-  else
-    tc = ta;  // not read
+  CUtensorMap tc2;
+  ok = ok && make_out_maps(g, ep, ta, &tc, &tc2);
   if (!ok) return MGB_ERR_CUDA;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -1050,7 +1347,7 @@ mgb_status launch_pair_variant(const GemmArgs& g, const EpiParams& ep, cudaStrea
   LaunchScope scope(g.prof_kind >= 0 ? g.prof_kind
                                : (A_MN ? PROF_GEMM_WGRAD : (B_MN ? PROF_GEMM_DGRAD : PROF_GEMM_FWD)),
                     st);
-  if (cudaLaunchKernelEx(&cfg, kern, ta, tb, tc, ep) != cudaSuccess) return MGB_ERR_CUDA;
+  if (cudaLaunchKernelEx(&cfg, kern, ta, tb, tc, tc2, ep) != cudaSuccess) return MGB_ERR_CUDA;
   return cudaGetLastError() == cudaSuccess ? MGB_OK : MGB_ERR_CUDA;
 }
 
@@ -1131,6 +1428,36 @@ CUresult tmap_encode_u32_2d(CUtensorMap* tm, const void* base, uint64_t inner, u
             CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
 }
 
+// Whether the bf16 outputs of this product go through TMA (epilogue_tma16):
+// the bf16-output epilogues with 32-column-aligned output chunks (gate/up
+// blocks and vocab chunks multiples of 32), rows that are multiples of 16
+// bytes apart, 16-byte-aligned outputs, no split over K. MGB_GEMM_TMA_OUT=0
+// keeps every store on the per-thread path.
+bool out_tma_ok(const GemmArgs& g, int n_chunk) {
+  const char* e = getenv("MGB_GEMM_TMA_OUT");
+  if (e != nullptr && e[0] == '0') return false;
+  if (g.k_splits > 1) return false;
+  auto al = [](const void* q, int64_t ld) {
+    return q != nullptr && (reinterpret_cast<uintptr_t>(q) & 15u) == 0 && ld % 8 == 0;
+  };
+  switch (g.epi) {
+    case EPI_STORE:
+    case EPI_BIAS_RESID:
+    case EPI_DGELU:
+      return al(g.C, g.ldc);
+    case EPI_DSWIGLU:
+      return al(g.C, g.ldc) && g.glu_block % 32 == 0;
+    case EPI_BIAS_GELU:
+      return al(g.C, g.ldc) && al(g.C2, g.ldc2);
+    case EPI_BIAS_SWIGLU:
+      return al(g.C, g.ldc) && al(g.C2, g.ldc2) && g.glu_block % 32 == 0;
+    case EPI_CE_STATS:
+      return g.keep != nullptr && al(g.keep, g.ld_keep) && n_chunk % 32 == 0;
+    default:
+      return false;
+  }
+}
+
 mgb_status gemm_tc_launch(const GemmArgs& g, cudaStream_t st) {
   EpiParams ep{};
   ep.M = g.M; ep.N = g.N; ep.K = g.K;
@@ -1157,6 +1484,7 @@ mgb_status gemm_tc_launch(const GemmArgs& g, cudaStream_t st) {
   ep.c_tma = (g.epi == EPI_F32 && g.f32_tma) ? (g.accumulate ? 2 : 1) : 0;
   ep.n_chunk = (g.epi == EPI_CE_STATS || g.epi == EPI_CE_GRAD) && g.n_chunk < g.N ? g.n_chunk : 0;
   ep.tpc = ep.gpc = 0;
+  ep.o_tma = out_tma_ok(g, ep.n_chunk) ? 1 : 0;
   const int num_k = (g.K + BK - 1) / BK;
   ep.k_splits = 1;
   ep.kb_per_split = num_k;

@@ -72,6 +72,25 @@ def test_ce_blocked_block_size_changes_only_rounding(mgb_lib):
         assert rel_l2(o[3], outs[0][3]) < 1e-2
 
 
+@pytest.mark.parametrize("mode", [mgb.MGB_CE_RESIDENT, mgb.MGB_CE_BLOCKED])
+def test_ce_kept_logits_through_tma(mgb_lib, monkeypatch, mode):
+    """The logits kept by the statistics epilogue, stored by TMA boxes (vocab
+    chunks of 32-column multiples, a ragged last chunk and ragged rows) or by
+    each thread: the same bits in every output."""
+    shape = CEShape(600, 256, 2000, 704)
+    inp = ce_inputs(shape, seed=8)
+    outs = []
+    for tma in ("0", "1"):
+        monkeypatch.setenv("MGB_GEMM_TMA_OUT", tma)
+        r = _runner(shape, inp, mode, token_block=256)
+        r.run()
+        torch.cuda.synchronize()
+        assert mgb.mgb_device_status() == mgb.MGB_OK
+        outs.append([x.clone() for x in (r.loss, r.lse, r.d_hidden, r.d_emb)])
+    for x0, x1 in zip(*outs):
+        assert torch.equal(x0, x1)
+
+
 def test_ce_blocked_emb_stream(mgb_lib):
     """Blocked mode with the last block's d_emb left on a caller's stream:
     after joining it, the results equal those of the joined call bit for bit."""

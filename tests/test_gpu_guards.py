@@ -21,12 +21,16 @@ def _rand(shape, dtype=torch.bfloat16, scale=1.0):
     return (torch.from_numpy(RNG.standard_normal(shape).astype(np.float32)) * scale).to("cuda", dtype)
 
 
+@pytest.mark.parametrize("tma_out", ["0", "1"])
 @pytest.mark.parametrize("pair", ["0", "1"])
 @pytest.mark.parametrize("a_mn,b_mn", [(0, 0), (0, 1), (1, 1)])
 @pytest.mark.parametrize("epi", range(7))
-def test_gemm_epilogues_stay_in_bounds(mgb_lib, monkeypatch, pair, a_mn, b_mn, epi):
-    """Every fused epilogue on both tile kinds, M / N / K ragged."""
+def test_gemm_epilogues_stay_in_bounds(mgb_lib, monkeypatch, tma_out, pair, a_mn, b_mn, epi):
+    """Every fused epilogue on both tile kinds, M / N / K ragged, with the
+    bf16 outputs stored by each thread and through TMA boxes (clipped at the
+    edges by the copy)."""
     monkeypatch.setenv("MGB_GEMM_PAIR", pair)
+    monkeypatch.setenv("MGB_GEMM_TMA_OUT", tma_out)
     M, N, K = 328, 200 if epi != mgb.MGB_EPI_BIAS_SWIGLU else 256, 136
     if epi == mgb.MGB_EPI_DSWIGLU:
         N = 192
@@ -87,7 +91,8 @@ def test_attention_stays_in_bounds(mgb_lib, B, S, nq, nkv, d, causal):
 def test_ce_stays_in_bounds(mgb_lib, mode, T, H, V, C):
     """Ragged tokens and vocab chunks: per-token outputs, both gradients and
     the whole workspace (logits, partial planes, accumulators; the blocked
-    mode with 256-token blocks, the last one ragged)."""
+    mode with 256-token blocks, the last one ragged). The vocab chunks of the
+    second shape are multiples of 32, so its kept logits go out through TMA."""
     shape = CEShape(T, H, V, C)
     inp = ce_inputs(shape, seed=2)
     h = to_device(inp["hidden"], torch.bfloat16)

@@ -91,6 +91,46 @@ def test_gemm_f32_tc_layouts(mgb_lib, a_mn, b_mn, M, N, K):
     assert err < 1.5e-5, err
 
 
+@pytest.mark.parametrize("pair", ["0", "1"])
+@pytest.mark.parametrize("M,N,K", [(328, 256, 136), (1000, 1280, 200)])
+@pytest.mark.parametrize("epi,gb", [(mgb.MGB_EPI_STORE, 0), (mgb.MGB_EPI_BIAS_GELU, 0),
+                                    (mgb.MGB_EPI_BIAS_SWIGLU, 128), (mgb.MGB_EPI_BIAS_SWIGLU, 64),
+                                    (mgb.MGB_EPI_BIAS_RESID, 0), (mgb.MGB_EPI_DGELU, 0),
+                                    (mgb.MGB_EPI_DSWIGLU, 64)])
+def test_gemm_tma_out_equals_thread_stores(mgb_lib, monkeypatch, pair, M, N, K, epi, gb):
+    """The bf16 epilogues with their outputs staged in shared memory and
+    stored by TMA boxes give the same bits as the per-thread stores (the same
+    arithmetic; only the store path differs), ragged rows included."""
+    monkeypatch.setenv("MGB_GEMM_PAIR", pair)
+    a, b = _dev(_bf16((M, K)), torch.bfloat16), _dev(_bf16((N, K)), torch.bfloat16)
+    bias = _dev(_bf16((N,), 0.1), torch.bfloat16)
+    resid = _dev(_bf16((M, N)), torch.bfloat16)
+    w_c = 2 * N if epi == mgb.MGB_EPI_DSWIGLU else N
+    w_c2 = N // 2 if epi == mgb.MGB_EPI_BIAS_SWIGLU else N
+    aux = _dev(_bf16((M, w_c)), torch.bfloat16)
+    outs = []
+    for tma in ("0", "1"):
+        monkeypatch.setenv("MGB_GEMM_TMA_OUT", tma)
+        c = torch.full((M, w_c), float("nan"), device="cuda", dtype=torch.bfloat16)
+        c2 = torch.full((M, w_c2), float("nan"), device="cuda", dtype=torch.bfloat16)
+        d = mgb.GemmExDesc(g=mgb.GemmDesc(m=M, n=N, k=K, a_major=0, b_major=0, lda=K, ldb=K,
+                                          ldc=w_c, dtype=mgb.MGB_BF16, c_f32=0, accumulate=0,
+                                          alpha=1.0),
+                           epilogue=epi, glu_block=gb or 16, ldc2=w_c2, ldr=N, ldaux=w_c)
+        two = epi in (mgb.MGB_EPI_BIAS_GELU, mgb.MGB_EPI_BIAS_SWIGLU)
+        has_bias = epi not in (mgb.MGB_EPI_DGELU, mgb.MGB_EPI_DSWIGLU)
+        mgb.mgb_gemm_ex(d, a, b, bias if has_bias else None, c, c2=c2 if two else None,
+                        resid=resid if epi == mgb.MGB_EPI_BIAS_RESID else None,
+                        aux=aux if epi in (mgb.MGB_EPI_DGELU, mgb.MGB_EPI_DSWIGLU) else None)
+        assert mgb.mgb_device_status() == mgb.MGB_OK
+        outs.append((c.clone(), c2.clone() if two else None))
+    assert not torch.isnan(outs[1][0].float()).any()
+    assert torch.equal(outs[0][0], outs[1][0])
+    if outs[0][1] is not None:
+        assert not torch.isnan(outs[1][1].float()).any()
+        assert torch.equal(outs[0][1], outs[1][1])
+
+
 @pytest.mark.parametrize("epi", [mgb.MGB_EPI_BIAS_GELU, mgb.MGB_EPI_BIAS_SWIGLU, mgb.MGB_EPI_BIAS_RESID,
                                  mgb.MGB_EPI_DGELU, mgb.MGB_EPI_DSWIGLU, mgb.MGB_EPI_F32])
 def test_gemm_f32_tc_epilogues(mgb_lib, epi):
