@@ -447,8 +447,10 @@ mgb_status mgb_embedding_bwd(int32_t tokens, int32_t hidden, int32_t v0, int32_t
 
 /* Bytes of the workspace mgb_attention_bwd needs: two float32 planes
  * [batch * n_q_heads][seq rounded up to a multiple of 128] (LSE * log2(e) and
- * delta = rowsum(dO * O), per query; the padding holds +inf and 0). No
- * counterpart on the pages: it sizes the buffer below. 0 for negative sizes. */
+ * delta = rowsum(dO * O), per query; the padding holds +inf and 0), then the
+ * float32 dQ accumulator [batch * seq][n_q_heads * 128] of the one-pass
+ * backward (sized for head_dim up to 128). No counterpart on the pages: it
+ * sizes the buffer below. 0 for negative sizes. */
 size_t mgb_attention_bwd_ws_bytes(int32_t batch, int32_t seq, int32_t n_q_heads);
 
 /* Attention core backward [P1 section 2, end-to-end backward]: given the
@@ -457,9 +459,16 @@ size_t mgb_attention_bwd_ws_bytes(int32_t batch, int32_t seq, int32_t n_q_heads)
  * ld_dkv; the sum over the query heads of each GQA group). P is recomputed
  * from lse. `ws` (16-byte aligned, caller-owned, overwritten) holds the
  * per-query LSE and delta: at least mgb_attention_bwd_ws_bytes(batch, seq,
- * n_q_heads) bytes, else MGB_ERR_WORKSPACE_TOO_SMALL before any launch. The
- * bf16 path runs its dQ kernel on a library-owned side stream beside the
- * dK/dV kernel, joined back into `stream` before the call returns. */
+ * n_q_heads) bytes, else MGB_ERR_WORKSPACE_TOO_SMALL before any launch.
+ * bf16, head_dim 128: one pass over key blocks forms dK, dV and each query
+ * tile's share of dQ, added into the workspace's float32 accumulator by
+ * reduce-add copies in no fixed order (so dq can differ between runs at
+ * float32 rounding level), then rounded to bf16. MGB_DETERMINISTIC=1 (or
+ * MGB_ATTN_BWD=split) in the environment, and head_dim 64, take two kernels
+ * instead, the dQ kernel on a library-owned side stream beside the dK/dV
+ * kernel, joined back into `stream` before the call returns; every sum is
+ * then in a fixed order and runs repeat bit for bit. mgb_block_bwd inherits
+ * both. */
 mgb_status mgb_attention_bwd(int32_t batch, int32_t seq, int32_t n_q_heads, int32_t n_kv_heads,
                              int32_t head_dim, int32_t causal, int32_t dtype,
                              const void* q, const void* k, const void* v, int64_t ld_q,

@@ -78,7 +78,8 @@ mgb_status attention_bf16_bwd(const AttnArgs& a, cudaStream_t st) {
   else
     return MGB_ERR_UNSUPPORTED;
   if (cudaGetLastError() != cudaSuccess) return MGB_ERR_CUDA;
-  // the dK/dV and dQ kernels are independent: dQ on a side stream, so each
+  if (attention_bwd_fused_ok(a)) return attention_tc_bwd_fused(a, st);
+  // two kernels: dK/dV and dQ are independent, dQ on a side stream, so each
   // fills the SMs the other leaves idle in its last wave
   SideLane lane(st, nullptr, 1);
   const mgb_status f = lane.fork();

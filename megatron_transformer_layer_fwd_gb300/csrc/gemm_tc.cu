@@ -1414,6 +1414,20 @@ CUresult tmap_encode_bf16_2d(CUtensorMap* tm, const void* base, uint64_t inner, 
                                                                      : CUDA_ERROR_INVALID_VALUE;
 }
 
+// 2-D float32 tensor map with 128-byte swizzle (box_inner 32 or fewer words).
+CUresult tmap_encode_f32_2d(CUtensorMap* tm, const void* base, uint64_t inner, uint64_t outer,
+                            int64_t ld, uint32_t box_inner, uint32_t box_outer) {
+  auto fn = encode_fn();
+  if (!fn) return CUDA_ERROR_NOT_INITIALIZED;
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {(cuuint64_t)ld * 4};
+  cuuint32_t box[2] = {box_inner, box_outer};
+  cuuint32_t es[2] = {1, 1};
+  return fn(tm, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+}
+
 // 2-D uint32 tensor map without swizzle (box rows of box_inner words).
 CUresult tmap_encode_u32_2d(CUtensorMap* tm, const void* base, uint64_t inner, uint64_t outer,
                             int64_t ld, uint32_t box_inner, uint32_t box_outer) {

@@ -227,14 +227,22 @@ inline int attn_mask_words(int S) { return (S + 127) / 128 * 4; }
 inline size_t attn_mask_bytes(int B, int nq, int S) {
   return 4 * (size_t)B * nq * S * attn_mask_words(S);
 }
-// The bf16 backward's per-query workspace: two float32 planes [B * nq][pad]
-// (LSE * log2(e), then delta) with rows padded to a multiple of 128 queries.
+// The bf16 backward's workspace: two float32 planes [B * nq][pad] (LSE *
+// log2(e), then delta) with rows padded to a multiple of 128 queries, then the
+// one-pass backward's float32 dQ accumulator [B * S][nq * d] (room for d up
+// to 128).
 inline int attn_bwd_row_pad(int S) { return (S + 127) / 128 * 128; }
 inline size_t attn_bwd_ws_bytes(int B, int S, int nq) {
-  return 2 * sizeof(float) * (size_t)B * nq * attn_bwd_row_pad(S);
+  return 2 * sizeof(float) * (size_t)B * nq * attn_bwd_row_pad(S) +
+         sizeof(float) * (size_t)B * S * nq * 128;
 }
 mgb_status attention_fwd_launch(const AttnArgs& a, cudaStream_t st);
 mgb_status attention_bwd_launch(const AttnArgs& a, cudaStream_t st);
+// The one-pass bf16 backward (dQ accumulated in float32 by TMA reduce-adds):
+// whether it serves these arguments (head dim 128; not with
+// MGB_DETERMINISTIC=1 or MGB_ATTN_BWD=split), and the pass itself.
+bool attention_bwd_fused_ok(const AttnArgs& a);
+mgb_status attention_tc_bwd_fused(const AttnArgs& a, cudaStream_t st);
 
 // Cross-entropy streaming kernels over one logits chunk [T, C] (row stride ldl).
 mgb_status ce_stats_launch(int T, int C, int v0, const void* logits, int64_t ldl,

@@ -270,10 +270,11 @@ def test_selftest_limit_is_validated(lib):
 
 
 def test_attention_bwd_workspace_size(lib):
-    """Two float32 planes with rows padded to 128 queries; too small a
-    workspace is refused before any launch."""
-    assert mgb.mgb_attention_bwd_ws_bytes(2, 4096, 32) == 2 * 4 * 2 * 32 * 4096
-    assert mgb.mgb_attention_bwd_ws_bytes(1, 130, 4) == 2 * 4 * 4 * 256
+    """Two float32 planes with rows padded to 128 queries, then the float32
+    dQ accumulator [batch * seq][n_q_heads * 128]; too small a workspace is
+    refused before any launch."""
+    assert mgb.mgb_attention_bwd_ws_bytes(2, 4096, 32) == 2 * 4 * 2 * 32 * 4096 + 4 * 2 * 4096 * 32 * 128
+    assert mgb.mgb_attention_bwd_ws_bytes(1, 130, 4) == 2 * 4 * 4 * 256 + 4 * 130 * 4 * 128
     assert mgb.mgb_attention_bwd_ws_bytes(-1, 8, 1) == 0
     need = mgb.mgb_attention_bwd_ws_bytes(1, 130, 4)
     p = 4096

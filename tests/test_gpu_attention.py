@@ -29,12 +29,58 @@ CASES = [
 ]
 
 
+@pytest.mark.parametrize("bwd", ["one_pass", "split"])
 @pytest.mark.parametrize("dtype", ["bf16", "f32"])
 @pytest.mark.parametrize("B,S,nq,nkv,d,causal", CASES)
-def test_attention_fwd_bwd(mgb_lib, dtype, B, S, nq, nkv, d, causal):
+def test_attention_fwd_bwd(mgb_lib, monkeypatch, bwd, dtype, B, S, nq, nkv, d, causal):
+    """The bf16 backward both ways: one pass over key blocks with dQ added up
+    in float32 by reduce-add copies (head dim 128), and the two kernels
+    (MGB_ATTN_BWD=split; always for head dim 64)."""
     if dtype == "f32" and S > 400:
         pytest.skip("float32 path is for the small float32 layer")
+    if bwd == "split" and (dtype == "f32" or d != 128):
+        pytest.skip("one backward path only")
+    if bwd == "split":
+        monkeypatch.setenv("MGB_ATTN_BWD", "split")
     _check(dtype, B, S, nq, nkv, d, causal, 1.0, 0.0)
+
+
+@pytest.mark.parametrize("B,S,nq,nkv,d,causal", [(2, 130, 4, 2, 128, True), (1, 700, 8, 2, 128, True),
+                                                 (2, 200, 2, 2, 128, False)])
+def test_attention_bwd_one_pass_matches_split(mgb_lib, monkeypatch, B, S, nq, nkv, d, causal):
+    """The one-pass backward against the two-kernel one on the same inputs:
+    dK and dV bit for bit (the same products in the same order), dQ to float32
+    rounding of its reordered sums (then rounded to bf16), and a second
+    one-pass run within the same bound of the first."""
+    rng = np.random.default_rng(5)
+    qkv = torch.from_numpy(rng.standard_normal((B * S, (nq + 2 * nkv) * d)).astype(np.float32))
+    qkv = qkv.to("cuda", torch.bfloat16)
+    W = qkv.shape[1]
+    qs, ks, vs = qkv, qkv[:, nq * d:], qkv[:, (nq + nkv) * d:]
+    o = torch.empty((B * S, nq * d), device="cuda", dtype=torch.bfloat16)
+    lse = torch.empty((B, nq, S), device="cuda", dtype=torch.float32)
+    mgb.mgb_attention_fwd(B, S, nq, nkv, d, causal, mgb.MGB_BF16, qs, ks, vs, W, W, o, lse)
+    do = torch.from_numpy(rng.standard_normal((B * S, nq * d)).astype(np.float32)).to("cuda", torch.bfloat16)
+    ws = torch.empty(mgb.mgb_attention_bwd_ws_bytes(B, S, nq), dtype=torch.uint8, device="cuda")
+    outs = []
+    for path in ("split", "one_pass", "one_pass"):
+        if path == "split":
+            monkeypatch.setenv("MGB_ATTN_BWD", "split")
+        else:
+            monkeypatch.delenv("MGB_ATTN_BWD", raising=False)
+        g = torch.full((B * S, W), float("nan"), device="cuda", dtype=torch.bfloat16)
+        mgb.mgb_attention_bwd(B, S, nq, nkv, d, causal, mgb.MGB_BF16, qs, ks, vs, W, W, o, lse, do,
+                              nq * d, g, g[:, nq * d:], g[:, (nq + nkv) * d:], W, W, ws)
+        torch.cuda.synchronize()
+        assert mgb.mgb_device_status() == mgb.MGB_OK
+        outs.append(g.float())
+    split, one, again = outs
+    kv = slice(nq * d, W)
+    assert torch.equal(split[:, kv], one[:, kv]) and torch.equal(one[:, kv], again[:, kv])
+    dq = slice(0, nq * d)
+    scale = float(split[:, dq].abs().max())
+    assert float((one[:, dq] - split[:, dq]).abs().max()) <= 2 ** -7 * scale
+    assert float((one[:, dq] - again[:, dq]).abs().max()) <= 2 ** -7 * scale
 
 
 @pytest.mark.parametrize("B,S,nq,nkv,d,causal", [(1, 700, 2, 1, 128, True), (2, 384, 2, 2, 64, False)])

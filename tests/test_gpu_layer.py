@@ -105,7 +105,10 @@ def test_empty_batch(mgb_lib):
     del x0
 
 
-def test_deterministic_repeat(mgb_lib):
+def test_deterministic_repeat(mgb_lib, monkeypatch):
+    """With MGB_DETERMINISTIC=1 (the attention backward in two kernels, every
+    sum in a fixed order) two runs give the same bits."""
+    monkeypatch.setenv("MGB_DETERMINISTIC", "1")
     shape = SMALL["bf16_pre_swiglu_causal_gqa"]
     arr = layer_inputs(shape, seed=3, random_affine=True, random_dy=True)
     r = LayerRunner(shape, arr)
@@ -119,14 +122,19 @@ def test_deterministic_repeat(mgb_lib):
     assert torch.equal(y1, y2) and torch.equal(dx1, dx2) and torch.equal(gw1, g2["w_qkv"])
 
 
+@pytest.mark.parametrize("deterministic", [True, False])
 @pytest.mark.parametrize("dropout", [0.0, 0.15])
-def test_graph_capture_replay(mgb_lib, dropout):
+def test_graph_capture_replay(mgb_lib, monkeypatch, dropout, deterministic):
     """The layer's forward and backward (including the backward's side streams
-    for weight gradients and the attention dQ kernel, forked and joined inside
-    the call) captured into one CUDA graph: replaying it reproduces the eager
-    results bit for bit, also after the inputs are changed in place; with
-    dropout, the masks come from the descriptor's generator states, so the
-    replay draws the same ones."""
+    for weight gradients, forked and joined inside the call, and the attention
+    backward's zeroed dQ accumulator) captured into one CUDA graph: replaying
+    it reproduces the eager results, also after the inputs are changed in
+    place; with dropout, the masks come from the descriptor's generator
+    states, so the replay draws the same ones. With MGB_DETERMINISTIC=1 the
+    results agree bit for bit; without it the attention dQ sums arrive in no
+    fixed order, and they agree to bf16 rounding."""
+    if deterministic:
+        monkeypatch.setenv("MGB_DETERMINISTIC", "1")
     shape = SMALL["bf16_pre_swiglu_causal_gqa"]
     arr = layer_inputs(shape, seed=4, random_affine=True, random_dy=True)
     r = LayerRunner(shape, arr)
@@ -156,7 +164,10 @@ def test_graph_capture_replay(mgb_lib, dropout):
         torch.cuda.synchronize()
         want = [r.y, r.dx] + [v for v in r.grads.values() if v is not None]
         for a, b in zip(got, want):
-            assert torch.equal(a, b)
+            if deterministic:
+                assert torch.equal(a, b)
+            else:
+                assert rel_l2(to_np(a), to_np(b)) < 1e-2
     assert mgb.mgb_device_status() == mgb.MGB_OK
 
 
