@@ -16,8 +16,10 @@ mgb_status attention_tc_bwd_main(const AttnArgs& a, cudaStream_t st, cudaStream_
 
 namespace {
 
+// acc (the one-pass backward's float32 dQ accumulator [B*S][nq*128], or
+// null): each slot of a real position also zeroes its head's 128 floats.
 template <int D>
-__global__ void attn_delta_kernel(const AttnArgs a, int pad) {
+__global__ void attn_delta_kernel(const AttnArgs a, int pad, float* acc) {
   // 8 lanes per (batch, head, position) slot, positions fastest (the planes'
   // order), each lane a 16-byte vector of O and dO per 64 head dims
   constexpr int NV = D / 64;
@@ -37,6 +39,11 @@ __global__ void attn_delta_kernel(const AttnArgs a, int pad) {
     return;
   }
   const int64_t tok = (int64_t)b * a.S + si;
+  if (acc != nullptr) {
+    float4* z = reinterpret_cast<float4*>(acc + (tok * a.nq + h) * 128 + sub * 16);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) z[k] = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
   const bf16* O = reinterpret_cast<const bf16*>(a.o) + tok * a.ld_o + h * D;
   const bf16* dO = reinterpret_cast<const bf16*>(a.dout) + tok * a.ld_do + h * D;
   uint4 x[NV], y[NV];
@@ -71,14 +78,17 @@ mgb_status attention_bf16_bwd(const AttnArgs& a, cudaStream_t st) {
   const int pad = attn_bwd_row_pad(a.S);
   const int64_t slots = (int64_t)a.B * pad * a.nq;  // 8 threads each
   const int blocks = (int)((slots * 8 + 255) / 256);
+  const bool one_pass = attention_bwd_fused_ok(a);
+  // the one-pass backward's dQ accumulator follows the two planes
+  float* acc = one_pass ? a.delta + 2 * (size_t)a.B * a.nq * pad : nullptr;
   if (a.d == 64)
-    attn_delta_kernel<64><<<blocks, 256, 0, st>>>(a, pad);
+    attn_delta_kernel<64><<<blocks, 256, 0, st>>>(a, pad, nullptr);
   else if (a.d == 128)
-    attn_delta_kernel<128><<<blocks, 256, 0, st>>>(a, pad);
+    attn_delta_kernel<128><<<blocks, 256, 0, st>>>(a, pad, acc);
   else
     return MGB_ERR_UNSUPPORTED;
   if (cudaGetLastError() != cudaSuccess) return MGB_ERR_CUDA;
-  if (attention_bwd_fused_ok(a)) return attention_tc_bwd_fused(a, st);
+  if (one_pass) return attention_tc_bwd_fused(a, st);
   // two kernels: dK/dV and dQ are independent, dQ on a side stream, so each
   // fills the SMs the other leaves idle in its last wave
   SideLane lane(st, nullptr, 1);

@@ -491,14 +491,13 @@ bool attention_bwd_fused_ok(const AttnArgs& a) {
   return e == nullptr || strcmp(e, "split") != 0;
 }
 
-// dK/dV and a float32 dQ accumulator (zeroed here, in the workspace after the
-// LSE/delta planes) in one pass, then dQ = bf16(accumulator / sqrt(d)).
+// dK/dV and the float32 dQ accumulator (in the workspace after the LSE/delta
+// planes, zeroed by the pre-pass) in one pass, then dQ = bf16(accumulator /
+// sqrt(d)).
 mgb_status attention_tc_bwd_fused(const AttnArgs& a, cudaStream_t st) {
   float* acc = a.delta + 2 * (size_t)a.B * a.nq * attn_bwd_row_pad(a.S);
   const int64_t rows = (int64_t)a.B * a.S;
   const int cols = a.nq * D;
-  if (cudaMemsetAsync(acc, 0, sizeof(float) * (size_t)rows * cols, st) != cudaSuccess)
-    return MGB_ERR_CUDA;
   const mgb_status r = fused_go(a, acc, st);
   if (r != MGB_OK) return r;
   const int64_t n = rows * (cols / 8);

@@ -242,6 +242,7 @@ mgb_status attention_bwd_launch(const AttnArgs& a, cudaStream_t st);
 // whether it serves these arguments (head dim 128; not with
 // MGB_DETERMINISTIC=1 or MGB_ATTN_BWD=split), and the pass itself.
 bool attention_bwd_fused_ok(const AttnArgs& a);
+// (runs after the pre-pass, which zeroes the accumulator)
 mgb_status attention_tc_bwd_fused(const AttnArgs& a, cudaStream_t st);
 
 // Cross-entropy streaming kernels over one logits chunk [T, C] (row stride ldl).
