@@ -504,24 +504,32 @@ def stage_sweep(stream, steps: int = 5, warmup: int = 3) -> dict:
 
 
 def _time_loop(fn, steps, warmup, stream):
+    """Mean ms per call over `steps` timed calls (after `warmup`), with the
+    library's per-kind events off (they sit between the kernels on the stream),
+    then the per-kind spans from a second pass with them on."""
     import torch
     from megatron_transformer_layer_fwd_gb300 import mgb
     for _ in range(warmup):
         fn()
     torch.cuda.synchronize()
-    mgb.mgb_profile_reset()
-    mgb.mgb_profile_enable(True)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for _ in range(steps):
         fn()
     e1.record(stream)
     torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    mgb.mgb_profile_reset()
+    mgb.mgb_profile_enable(True)
+    n = max(1, min(steps, 5))
+    for _ in range(n):
+        fn()
+    torch.cuda.synchronize()
     mgb.mgb_profile_enable(False)
-    prof = {k: round(v[0] / steps, 4) for k, v in mgb.mgb_profile_read().items() if v[1] > 0}
+    prof = {k: round(v[0] / n, 4) for k, v in mgb.mgb_profile_read().items() if v[1] > 0}
     if mgb.mgb_device_status(stream) != mgb.MGB_OK:
         raise RuntimeError("device error")
-    return e0.elapsed_time(e1) / steps, prof
+    return ms, prof
 
 
 def _layer_line(args, name, shape, ms, prof):
