@@ -399,38 +399,49 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
         tc_fence_after();
         const bool interior = kv0 + TK <= p.S && (!p.causal || kv0 + TK - 1 <= row0);
-        // pass 1: the row maximum over the 128 scores
-        float mx = -INFINITY;
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          float sc[32];
-          ld_cols32(ts + c * 32, sc);
-          if (!interior) {
-#pragma unroll
-            for (int e = 0; e < 32; ++e) {
-              const int key = kv0 + c * 32 + e;
-              if (key >= p.S || (p.causal && key > row)) sc[e] = -INFINITY;
-            }
-          }
-          float m4[4] = {mx, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
-          for (int e = 0; e < 32; e += 8) {
-            m4[0] = fmax3(m4[0], sc[e], sc[e + 1]);
-            m4[1] = fmax3(m4[1], sc[e + 2], sc[e + 3]);
-            m4[2] = fmax3(m4[2], sc[e + 4], sc[e + 5]);
-            m4[3] = fmax3(m4[3], sc[e + 6], sc[e + 7]);
-          }
-          mx = fmaxf(fmax3(m4[0], m4[1], m4[2]), m4[3]);
-        }
-        mx *= p.sl2;
-        const bool need = mx > m_ref + TAU;
+        // From the second key tile on (m_ref is then finite: the first tile
+        // holds a visible key of every row) one pass: each 32-key chunk's
+        // maximum is checked against the reference as it is read, and only a
+        // chunk that exceeds it by more than TAU moves it, by a whole number k
+        // of log2 units, so that the P already written for this tile and the
+        // O row scale by 2^-k exactly. The first tile takes the row maximum in
+        // a pass of its own.
+        const bool one_pass = j > 0 && __all_sync(0xffffffffu, m_ref > -INFINITY);
+        bool need = false;
         float alpha = 1.0f;
-        if (need) {
-          alpha = exp2f(m_ref - mx);
-          m_ref = mx;
-          l *= alpha;
+        if (!one_pass) {
+          // pass 1: the row maximum over the 128 scores
+          float mx = -INFINITY;
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            float sc[32];
+            ld_cols32(ts + c * 32, sc);
+            if (!interior) {
+#pragma unroll
+              for (int e = 0; e < 32; ++e) {
+                const int key = kv0 + c * 32 + e;
+                if (key >= p.S || (p.causal && key > row)) sc[e] = -INFINITY;
+              }
+            }
+            float m4[4] = {mx, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+            for (int e = 0; e < 32; e += 8) {
+              m4[0] = fmax3(m4[0], sc[e], sc[e + 1]);
+              m4[1] = fmax3(m4[1], sc[e + 2], sc[e + 3]);
+              m4[2] = fmax3(m4[2], sc[e + 4], sc[e + 5]);
+              m4[3] = fmax3(m4[3], sc[e + 6], sc[e + 7]);
+            }
+            mx = fmaxf(fmax3(m4[0], m4[1], m4[2]), m4[3]);
+          }
+          mx *= p.sl2;
+          need = mx > m_ref + TAU;
+          if (need) {
+            alpha = exp2f(m_ref - mx);
+            m_ref = mx;
+            l *= alpha;
+          }
         }
-        const float nref = m_ref == -INFINITY ? 0.0f : -m_ref;
+        float nref = m_ref == -INFINITY ? 0.0f : -m_ref;
         // pass 2: P = 2^(s log2e / sqrt(d) - m_ref) as bf16 pairs over the
         // tile's first 64 score columns (chunk c's 32 keys -> columns 16c ..),
         // which only ever cover scores already read in this pass
@@ -444,6 +455,45 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             for (int e = 0; e < 32; ++e) {
               const int key = kv0 + c * 32 + e;
               if (key >= p.S || (p.causal && key > row)) sc[e] = -INFINITY;
+            }
+          }
+          if (one_pass) {
+            float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+            for (int e = 0; e < 32; e += 8) {
+              m4[0] = fmax3(m4[0], sc[e], sc[e + 1]);
+              m4[1] = fmax3(m4[1], sc[e + 2], sc[e + 3]);
+              m4[2] = fmax3(m4[2], sc[e + 4], sc[e + 5]);
+              m4[3] = fmax3(m4[3], sc[e + 6], sc[e + 7]);
+            }
+            const float cm = fmaxf(fmax3(m4[0], m4[1], m4[2]), m4[3]) * p.sl2;
+            const bool up = cm > m_ref + TAU;
+            if (__any_sync(0xffffffffu, up)) {
+              // this row's reference moves up by k: l, the P chunks already
+              // written for this tile and (after the pass) O scale by 2^-k
+              float a = 1.0f;
+              if (up) {
+                const float k = ceilf(cm - m_ref);
+                a = k < 126.0f ? __int_as_float((127 - (int)k) << 23) : 0.0f;
+                m_ref += k;
+                l *= a;
+                r0 *= a; r1 *= a; r2 *= a; r3 *= a;
+                alpha *= a;
+                need = true;
+              }
+              tmem_st_wait();  // the chunks' P stores have landed
+              for (int cc = 0; cc < c; ++cc) {
+                uint32_t pw[16];
+                tmem_ld16(ts + cc * 16, pw);
+                tmem_ld_wait();
+#pragma unroll
+                for (int e = 0; e < 16; ++e) {
+                  const float2 f = unpack_bf16x2(pw[e]);
+                  pw[e] = pack_bf16x2(f.x * a, f.y * a);
+                }
+                tmem_st16(ts + cc * 16, pw);
+              }
+              nref = -m_ref;
             }
           }
 #pragma unroll
