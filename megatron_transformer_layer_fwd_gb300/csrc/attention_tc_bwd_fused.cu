@@ -119,9 +119,11 @@ __device__ __forceinline__ bool dq_out(int j, uint32_t tcol, uint32_t box, uint3
   fence_proxy_async();
   __syncwarp();
   if (lane == 0) {
-    tma_reduce_add_2d(tm, box, x, y);
-    bulk_commit();
-    bulk_wait_read<0>();  // the copy has read the box: the other group may refill it
+    if (dcheck((x & 31) == 0 && x >= 0 && y >= 0, err)) {
+      tma_reduce_add_2d(tm, box, x, y);
+      bulk_commit();
+      bulk_wait_read<0>();  // the copy has read the box: the other group may refill it
+    }
     mbar_arrive(box_free);
   }
   return true;
@@ -216,6 +218,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
         const uint32_t fb = qd_full0 + 8 * s;
         const int q0 = qt * TC;
+        if (!dcheck(h < p.nq && q0 < p.S, p.err)) {
+          *abort = 1;
+          break;
+        }
         mbar_arrive_expect_tx(fb, 2 * C::QT_BYTES + C::LD_BYTES);
 #pragma unroll
         for (int kb = 0; kb < D / 64; ++kb) {
