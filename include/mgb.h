@@ -342,7 +342,8 @@ mgb_status mgb_gemm_ex(const mgb_gemm_ex_desc* desc, const void* a, const void* 
  * float32 layer's linears]: each operand x is split into hi = x rounded to
  * TF32 (10 mantissa bits) and lo = x - hi rounded to TF32, and the product is
  * A_hi B_hi^T + A_hi B_lo^T + A_lo B_hi^T (tcgen05 kind::tf32, float32
- * accumulation): about float32 accuracy, unlike one TF32 product. The split
+ * accumulation): rel. error about 1e-5 at K ~ 1000 (5.7e-5 at K 8192), where
+ * one TF32 product gives a few 1e-4 and FFMA about 1e-6. The split
  * operands are written as K-major copies into `ws` (caller-owned, 256-byte
  * aligned, at least mgb_gemm_f32_tc_ws_bytes(m, n, k) bytes, overwritten).
  * mgb_block_fwd / mgb_block_bwd with dtype MGB_F32 run their GEMMs this way,

@@ -75,7 +75,7 @@ def test_gemm_f32_tc_layouts(mgb_lib, a_mn, b_mn, M, N, K):
     32-wide K block nor of 4), against the float64 product of the same float32
     operands: about 7e-6 at K = 1000, set by the tensor core's float32
     accumulation (the bf16 tests above allow 1e-5 at that K); one TF32 product
-    would give about 1e-3."""
+    gives several times 1e-4."""
     A, B = _f32((M, K)), _f32((N, K))
     a_st = A.T.copy() if a_mn else A
     b_st = B.T.copy() if b_mn else B
