@@ -7,9 +7,12 @@
 // acc = A_hi B_hi^T + A_hi B_lo^T + A_lo B_hi^T with float32 accumulation in
 // TMEM. Every product of two tf32 values is exact in float32; the dropped
 // A_lo B_lo^T term and the rounding of lo are each about 2^-22 relative to
-// |a||b| per product; what remains is the tensor core's float32
-// accumulation (about 1e-5 relative at K ~ 1000, 6e-5 at K 8192, where one
-// TF32 product gives a few 1e-4).
+// |a||b| per product. The tensor core's own float32 accumulation loses more
+// as K grows (6e-5 relative at K 8192 when it runs over the whole K), so the
+// accumulator is promoted every 128 K: the MMA warp starts each K chunk in the
+// next of four TMEM buffers, and the epilogue warps add the chunks in float32
+// registers (9e-7 relative at K 8192, below the FFMA product's 1.6e-6; one
+// TF32 product gives 3e-4).
 //
 // A pre-pass writes hi and lo of both operands as K-major float32 copies
 // (transposing an MN-major operand) into the caller's scratch, with K padded
@@ -36,6 +39,8 @@ namespace {
 
 constexpr int TBM = 128, TBN = 128, TBK = 32;  // tile rows, tile columns, K per block
 constexpr int TSTAGES = 3;
+constexpr int TACC = 4;  // accumulator buffers in TMEM (one per K chunk in turn)
+
 constexpr int TILE4 = TBM * TBK * 4;           // one 128 x 32 float32 tile: 16 KB
 constexpr int TSTAGE = 4 * TILE4;              // A_hi, A_lo, B_hi, B_lo
 constexpr int TSMEM = TSTAGES * TSTAGE + 1024 + 1024;
@@ -43,6 +48,9 @@ constexpr int TSMEM = TSTAGES * TSTAGE + 1024 + 1024;
 struct Tf32Params {
   SimtParams e;  // epilogue (C, bias, ...; A/B fields unused)
   int tiles_m, tiles_n, num_k;
+  // K blocks per accumulation chunk: the tensor core sums one chunk in its
+  // float32 accumulator, the epilogue adds the chunks in float32 registers
+  int kchunk;
   int* err;
 };
 
@@ -103,15 +111,16 @@ __global__ void __launch_bounds__(192, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + TSTAGES * TSTAGE);
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * TSTAGES + 4);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * TSTAGES + 2 * TACC);
   volatile int* abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
   const uint32_t tiles = smem_u32(smem);
   const uint32_t full0 = smem_u32(bars);
   const uint32_t empty0 = full0 + 8 * TSTAGES;
   const uint32_t accf0 = empty0 + 8 * TSTAGES;
-  const uint32_t acce0 = accf0 + 16;
+  const uint32_t acce0 = accf0 + 8 * TACC;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int total = p.tiles_m * p.tiles_n;
+  const int nkc = p.num_k > 0 ? p.num_k : 1;  // K blocks, or one empty chunk when K = 0
 
   if (threadIdx.x == 0) {
     tma_prefetch_desc(&tmAh);
@@ -122,14 +131,14 @@ __global__ void __launch_bounds__(192, 1)
       mbar_init(full0 + 8 * s, 1);
       mbar_init(empty0 + 8 * s, 1);
     }
-    for (int b = 0; b < 2; ++b) {
+    for (int b = 0; b < TACC; ++b) {
       mbar_init(accf0 + 8 * b, 1);
       mbar_init(acce0 + 8 * b, 4);
     }
     fence_mbar_init();
     *abort = 0;
   }
-  if (warp == 0) tmem_alloc(smem_u32(tmem_slot), 2 * TBN);
+  if (warp == 0) tmem_alloc(smem_u32(tmem_slot), TACC * TBN);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -170,16 +179,18 @@ __global__ void __launch_bounds__(192, 1)
       constexpr uint32_t idesc = idesc_tf32_f32(TBM, TBN);
       uint32_t kg = 0;
       int t = 0;
-      for (int tile = blockIdx.x; tile < total && !*abort; tile += gridDim.x, ++t) {
-        const int buf = t & 1;
-        if (!mbar_wait(acce0 + 8 * buf, ((t >> 1) & 1) ^ 1, p.err)) {
-          *abort = 1;
+      bool good = true;
+      for (int tile = blockIdx.x; tile < total && !*abort && good; tile += gridDim.x) {
+       for (int c0 = 0; c0 < nkc; c0 += p.kchunk, ++t) {  // one accumulator buffer per chunk
+        const int buf = t % TACC;
+        if (!mbar_wait_spin(acce0 + 8 * buf, ((t / TACC) & 1) ^ 1, p.err)) {
+          good = false;
           break;
         }
         tc_fence_after();
         const uint32_t acc = tmem + buf * TBN;
-        bool good = true;
-        for (int kb = 0; kb < p.num_k; ++kb, ++kg) {
+        const int c1 = min(c0 + p.kchunk, p.num_k);
+        for (int kb = c0; kb < c1; ++kb, ++kg) {
           const int s = kg % TSTAGES;
           if (!mbar_wait(full0 + 8 * s, (kg / TSTAGES) & 1, p.err)) {
             good = false;
@@ -193,51 +204,63 @@ __global__ void __launch_bounds__(192, 1)
             const uint64_t al = smem_desc_sw128(st + TILE4 + 32 * kk, 16, 1024);
             const uint64_t bh = smem_desc_sw128(st + 2 * TILE4 + 32 * kk, 16, 1024);
             const uint64_t bl = smem_desc_sw128(st + 3 * TILE4 + 32 * kk, 16, 1024);
-            tc_mma_tf32(acc, al, bh, idesc, (kb | kk) != 0 ? 1u : 0u);
+            tc_mma_tf32(acc, al, bh, idesc, (kb != c0 || kk != 0) ? 1u : 0u);
             tc_mma_tf32(acc, ah, bl, idesc, 1u);
             tc_mma_tf32(acc, ah, bh, idesc, 1u);
           }
           tc_commit(empty0 + 8 * s);
         }
-        if (!good) {
-          *abort = 1;
-          break;
-        }
+        if (!good) break;
         tc_commit(accf0 + 8 * buf);
+       }
       }
+      if (!good) *abort = 1;
     }
   } else {
-    // ---------------- epilogue warps 2..5: one output row per thread
+    // ---------------- epilogue warps 2..5: one output row per thread, the
+    // tile's K chunks summed in float32 registers, then the epilogue
     const int q = warp & 3;
     int t = 0;
-    for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++t) {
-      const int buf = t & 1;
-      const bool ready = !*abort && mbar_wait(accf0 + 8 * buf, (t >> 1) & 1, p.err);
-      if (!__all_sync(0xffffffffu, ready)) {
-        *abort = 1;
-        break;
-      }
-      tc_fence_after();
+    bool good = true;
+    for (int tile = blockIdx.x; tile < total && good; tile += gridDim.x) {
       const int m0 = (tile % p.tiles_m) * TBM, n0 = (tile / p.tiles_m) * TBN;
       const int row = m0 + q * 32 + lane;
-      const uint32_t trow = tmem + buf * TBN + ((uint32_t)(q * 32) << 16);
-      for (int lc = 0; lc < TBN; lc += 32) {
-        uint32_t r[32];
-        tmem_ld32(trow + lc, r);
-        tmem_ld_wait();
-        if (row < p.e.M) {
+      float sum[TBN];
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            const int n = n0 + lc + j;
-            const float a = p.num_k > 0 ? p.e.alpha * __uint_as_float(r[j]) : 0.0f;
-            if (n < p.e.N) epi_elem(p.e, row, n, a);
+      for (int j = 0; j < TBN; ++j) sum[j] = 0.0f;
+      for (int c0 = 0; c0 < nkc; c0 += p.kchunk, ++t) {
+        const int buf = t % TACC;
+        const bool ready = !*abort && mbar_wait_spin(accf0 + 8 * buf, (t / TACC) & 1, p.err);
+        if (!__all_sync(0xffffffffu, ready)) {
+          good = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t trow = tmem + buf * TBN + ((uint32_t)(q * 32) << 16);
+#pragma unroll
+        for (int lc = 0; lc < TBN; lc += 32) {
+          uint32_t r[32];
+          tmem_ld32(trow + lc, r);
+          tmem_ld_wait();
+          if (p.num_k > 0) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) sum[lc + j] += __uint_as_float(r[j]);
           }
         }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(acce0 + 8 * buf);
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(acce0 + 8 * buf);
+      if (!good) break;
+      if (row < p.e.M) {
+#pragma unroll
+        for (int j = 0; j < TBN; ++j) {
+          const int n = n0 + j;
+          if (n < p.e.N) epi_elem(p.e, row, n, p.e.alpha * sum[j]);
+        }
+      }
     }
+    if (!good) *abort = 1;
   }
 
   __syncthreads();
@@ -250,7 +273,7 @@ __global__ void __launch_bounds__(192, 1)
   __syncthreads();
   if (warp == 0) {
     tc_fence_after();
-    tmem_dealloc(tmem, 2 * TBN);
+    tmem_dealloc(tmem, TACC * TBN);
   }
 }
 
@@ -329,6 +352,13 @@ mgb_status gemm_tf32_launch(const GemmArgs& g, cudaStream_t st) {
   p.tiles_m = (g.M + TBM - 1) / TBM;
   p.tiles_n = (g.N + TBN - 1) / TBN;
   p.num_k = (g.K + TBK - 1) / TBK;
+  // 4 K blocks (128 K) per chunk: at 8192^3 the relative error is 9e-7
+  // against 5.7e-5 with one chunk over the whole K (FFMA: 1.6e-6), for about
+  // 40 % more time; MGB_TF32_CHUNK=<blocks> for another length, 0 for one
+  // chunk over the whole K
+  p.kchunk = 4;
+  if (const char* e = getenv("MGB_TF32_CHUNK")) p.kchunk = atoi(e);
+  if (p.kchunk <= 0) p.kchunk = p.num_k > 0 ? p.num_k : 1;
   p.err = device_error_word();
   if (cudaFuncSetAttribute(gemm_tf32x3_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                            TSMEM) != cudaSuccess)
