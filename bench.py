@@ -748,11 +748,14 @@ def run_case(args):
         fwd = lambda: mgb.mgb_layernorm_fwd(T, H, mgb.MGB_BF16, 1e-5, x, gm, bt, y, mu, rs, hi)
         bwd = lambda: mgb.mgb_layernorm_bwd(T, H, mgb.MGB_BF16, x, mu, rs, gm, dy, dres, dx, dg, db,
                                             ws, hi)
-        # MGB_LN_KERNEL: tma (default: rows streamed into shared memory by bulk
-        # copies), warp (register prefetch, forward only), block (block per row)
+        # MGB_LN_KERNEL: tma (rows streamed into shared memory by bulk copies;
+        # the forward's default), warp (register prefetch, forward only), block
+        # (block per row; backward: register prefetch), async (backward's
+        # default: per-thread asynchronous copies into a shared-memory ring)
         for name, env, fn, nb in (("layernorm_fwd_tma", "tma", fwd, fwd_bytes),
                                   ("layernorm_fwd_warp", "warp", fwd, fwd_bytes),
                                   ("layernorm_fwd_block", "block", fwd, fwd_bytes),
+                                  ("layernorm_bwd_async", "async", bwd, bwd_bytes),
                                   ("layernorm_bwd_tma", "tma", bwd, bwd_bytes),
                                   ("layernorm_bwd_block", "block", bwd, bwd_bytes)):
             os.environ["MGB_LN_KERNEL"] = env

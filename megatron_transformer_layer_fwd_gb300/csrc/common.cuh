@@ -542,6 +542,13 @@ __device__ __forceinline__ void add2(float& r0, float& r1, float a0, float a1, f
       : "=f"(r0), "=f"(r1)
       : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
 }
+// (a0, a1) * (b0, b1), round to nearest.
+__device__ __forceinline__ void mul2(float& r0, float& r1, float a0, float a1, float b0, float b1) {
+  asm("{\n .reg .b64 a, b, d;\n mov.b64 a, {%2, %3};\n mov.b64 b, {%4, %5};\n"
+      " mul.rn.f32x2 d, a, b;\n mov.b64 {%0, %1}, d;\n}\n"
+      : "=f"(r0), "=f"(r1)
+      : "f"(a0), "f"(a1), "f"(b0), "f"(b1));
+}
 
 __device__ __forceinline__ float gelu_erf(float u) {
   return 0.5f * u * (1.0f + erff(u * 0.70710678118654752f));

@@ -316,8 +316,9 @@ __global__ void __launch_bounds__(32 * (1 + kLnConsumers), VPL >= 16 ? 1 : 2) ln
   const uint32_t full0 = slots + nslot * slot_bytes;  // 8-byte aligned (slot_bytes % 16 == 0)
   const uint32_t empty0 = full0 + 8 * nslot;
   volatile int* abort = reinterpret_cast<volatile int*>(ln_smem + nslot * slot_bytes + 16 * nslot);
-  // gamma and beta of the whole row, staged once (16-byte aligned after the flag)
-  uint4* sgb = reinterpret_cast<uint4*>(ln_smem + nslot * slot_bytes + 16 * nslot + 16);
+  // gamma and beta of the whole row as float32 (1 and 0 when absent), staged
+  // once (16-byte aligned after the flag)
+  float4* sgb = reinterpret_cast<float4*>(ln_smem + nslot * slot_bytes + 16 * nslot + 16);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nvec = cols / 8;
   if (threadIdx.x == 0) {
@@ -329,8 +330,23 @@ __global__ void __launch_bounds__(32 * (1 + kLnConsumers), VPL >= 16 ? 1 : 2) ln
     *abort = 0;
   }
   for (int v = threadIdx.x; v < nvec; v += blockDim.x) {
-    sgb[v] = gamma ? reinterpret_cast<const uint4*>(gamma)[v] : make_uint4(0, 0, 0, 0);
-    sgb[nvec + v] = beta ? reinterpret_cast<const uint4*>(beta)[v] : make_uint4(0, 0, 0, 0);
+    float g[8], b[8];
+    if (gamma) {
+      unpack8(reinterpret_cast<const uint4*>(gamma)[v], g);
+    } else {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) g[e] = 1.0f;
+    }
+    if (beta) {
+      unpack8(reinterpret_cast<const uint4*>(beta)[v], b);
+    } else {
+#pragma unroll
+      for (int e = 0; e < 8; ++e) b[e] = 0.0f;
+    }
+    sgb[2 * v] = make_float4(g[0], g[1], g[2], g[3]);
+    sgb[2 * v + 1] = make_float4(g[4], g[5], g[6], g[7]);
+    sgb[2 * (nvec + v)] = make_float4(b[0], b[1], b[2], b[3]);
+    sgb[2 * (nvec + v) + 1] = make_float4(b[4], b[5], b[6], b[7]);
   }
   __syncthreads();
   const int n = rows > (int)blockIdx.x ? (rows - (int)blockIdx.x + gridDim.x - 1) / gridDim.x : 0;
@@ -372,14 +388,15 @@ __global__ void __launch_bounds__(32 * (1 + kLnConsumers), VPL >= 16 ? 1 : 2) ln
       if (lane == 0) mbar_arrive(empty0 + 8 * s);  // slot free: the producer refills it
       const int row = blockIdx.x + i * gridDim.x;
       // eight independent partial sums (one per element of a vector): short
-      // dependency chains instead of one chain over the lane's elements
+      // dependency chains instead of one chain over the lane's elements;
+      // element pairs in packed float32x2 arithmetic
       float a8[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
 #pragma unroll
       for (int j = 0; j < VPL; ++j) {
         float v[8];
         unpack8(cur[j], v);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) a8[e] += v[e];
+        for (int e = 0; e < 8; e += 2) add2(a8[e], a8[e + 1], a8[e], a8[e + 1], v[e], v[e + 1]);
       }
       float sm = ((a8[0] + a8[1]) + (a8[2] + a8[3])) + ((a8[4] + a8[5]) + (a8[6] + a8[7]));
 #pragma unroll
@@ -392,9 +409,9 @@ __global__ void __launch_bounds__(32 * (1 + kLnConsumers), VPL >= 16 ? 1 : 2) ln
         float v[8];
         unpack8(cur[j], v);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const float d = v[e] - mean;
-          a8[e] = fmaf(d, d, a8[e]);
+        for (int e = 0; e < 8; e += 2) {
+          add2(v[e], v[e + 1], v[e], v[e + 1], -mean, -mean);
+          fma2(a8[e], a8[e + 1], v[e], v[e + 1], v[e], v[e + 1], a8[e], a8[e + 1]);
         }
       }
       float ss = ((a8[0] + a8[1]) + (a8[2] + a8[3])) + ((a8[4] + a8[5]) + (a8[6] + a8[7]));
@@ -405,16 +422,18 @@ __global__ void __launch_bounds__(32 * (1 + kLnConsumers), VPL >= 16 ? 1 : 2) ln
 #pragma unroll
       for (int j = 0; j < VPL; ++j) {
         const int vi = lane + 32 * j;
-        float v[8], g[8], b[8], o8[8];
+        float v[8], o8[8];
         unpack8(cur[j], v);
-        unpack8(sgb[vi], g);
-        unpack8(sgb[nvec + vi], b);
+        const float4 g0 = sgb[2 * vi], g1 = sgb[2 * vi + 1];
+        const float4 b0 = sgb[2 * (nvec + vi)], b1 = sgb[2 * (nvec + vi) + 1];
+        const float g[8] = {g0.x, g0.y, g0.z, g0.w, g1.x, g1.y, g1.z, g1.w};
+        const float b[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+        // y = (x - mean) rstd gamma + beta
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          float t = (v[e] - mean) * rstd;
-          if (gamma) t *= g[e];
-          if (beta) t += b[e];
-          o8[e] = t;
+        for (int e = 0; e < 8; e += 2) {
+          add2(o8[e], o8[e + 1], v[e], v[e + 1], -mean, -mean);
+          mul2(o8[e], o8[e + 1], o8[e], o8[e + 1], rstd, rstd);
+          fma2(o8[e], o8[e + 1], o8[e], o8[e + 1], g[e], g[e + 1], b[e], b[e + 1]);
         }
         uint4 ov;
         ov.x = pack_bf16x2(o8[0], o8[1]); ov.y = pack_bf16x2(o8[2], o8[3]);
@@ -753,37 +772,234 @@ __global__ void __launch_bounds__(1024, 1) ln_bwd_wide_kernel(
   ln_bwd_rows<T, VPT, false>(rows, cols, x, mean, rstd, gamma, dy, dres, dx, part);
 }
 
-// out0[c] = sum_p part[p * stride, c] and out1[c] = sum_p part[half + p * stride, c]
-// for p < nparts (rows of `cols` floats), written as T (nullable outputs
-// skipped). Block (32 x 8): lane = column (coalesced 128-byte rows of the
-// partial buffer), the 8 warps split the partials, fixed order of summation
-// (deterministic).
-template <typename T>
-__global__ void reduce_parts_kernel(int nparts, int stride, int64_t half, int cols,
-                                    const float* __restrict__ part, T* __restrict__ out0,
-                                    T* __restrict__ out1) {
-  __shared__ float red[2][8][33];
-  const int c = blockIdx.x * 32 + threadIdx.x;
-  float s0 = 0.0f, s1 = 0.0f;
-  if (c < cols) {
-    for (int p = threadIdx.y; p < nparts; p += 8) {
-      const int64_t o = (int64_t)p * stride * cols + c;
-      if (out0) s0 += part[o];
-      if (out1) s1 += part[half + o];
+// 16-byte asynchronous copy global -> shared (bypassing L1); completion is
+// tracked per thread by commit groups.
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// Backward for rows of up to 1024 vectors, fed by per-thread asynchronous
+// copies. Blocks stride over the rows as in ln_bwd_kernel (thread t owns
+// vector t of every row; gamma and the dgamma/dbeta partial sums stay in its
+// registers). Each thread copies its own vector of x, dy and dres of the
+// block's next P - 1 rows into its private slots of a P-row shared-memory ring
+// and reads them back itself, so no barrier guards the ring: only the row
+// reduction synchronises the block (once per row, alternating between two
+// reduction buffers). P - 1 rows per block are in flight while one is worked
+// on, without registers holding them.
+// With CL > 1 the grid is launched in clusters of CL CTAs, which combine their
+// dgamma/dbeta partial sums through distributed shared memory before they are
+// written: partial row blockIdx.x / CL, CTA rank r of the cluster summing the
+// r-th share of the columns over the cluster's CTAs in rank order.
+template <typename T, int P, int CL>
+__global__ void __launch_bounds__(1024, 1) ln_bwd_async_kernel(
+    int rows, int cols, const T* __restrict__ x, const float* __restrict__ mean,
+    const float* __restrict__ rstd, const T* __restrict__ gamma, const T* __restrict__ dy,
+    const T* __restrict__ dres, T* __restrict__ dx, float* __restrict__ part) {
+  constexpr int VN = Vec<T>::N;
+  extern __shared__ uint4 ln_ring[];  // [P][3][blockDim.x]
+  __shared__ float2 red[2][32];
+  const int nt = blockDim.x, t = threadIdx.x, warp = t >> 5, lane = t & 31;
+  const int nvec = cols / VN;
+  const bool have = t < nvec;
+  const int nrow = rows > (int)blockIdx.x ? (rows - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
+  // the block's i-th row into slot i % P (an empty group past the end keeps
+  // one group per row)
+  auto issue = [&](int i) {
+    if (i < nrow && have) {
+      const int64_t o = (int64_t)((int)blockIdx.x + (int64_t)i * gridDim.x) * cols + t * VN;
+      uint4* s = ln_ring + (i % P) * 3 * nt + t;
+      cp_async16(s, x + o);
+      cp_async16(s + nt, dy + o);
+      if (dres) cp_async16(s + 2 * nt, dres + o);
+    }
+    cp_async_commit();
+  };
+#pragma unroll
+  for (int i = 0; i < P - 1; ++i) issue(i);
+  float gm[VN], pg[VN], pb[VN];
+#pragma unroll
+  for (int j = 0; j < VN; ++j) {
+    gm[j] = 1.0f;
+    pg[j] = pb[j] = 0.0f;
+  }
+  if (gamma && have) vload(gamma + t * VN, gm);
+  const float inv_cols = 1.0f / (float)cols;
+  // the block's row statistics: staged in shared memory up front when the
+  // block has at most 64 rows, else loaded one row ahead into registers
+  __shared__ float2 stat[64];
+  const bool staged = nrow <= 64;
+  float mu_n = 0.0f, rs_n = 0.0f;
+  if (staged) {
+    for (int k = t; k < nrow; k += nt) {
+      const int r = (int)blockIdx.x + k * (int)gridDim.x;
+      stat[k] = make_float2(mean[r], rstd[r]);
+    }
+    __syncthreads();
+  } else if (nrow > 0) {
+    mu_n = mean[blockIdx.x];
+    rs_n = rstd[blockIdx.x];
+  }
+  for (int i = 0; i < nrow; ++i) {
+    const int row = (int)blockIdx.x + i * (int)gridDim.x;
+    float mu = mu_n, rs = rs_n;
+    if (staged) {
+      const float2 m = stat[i];
+      mu = m.x;
+      rs = m.y;
+    } else if (i + 1 < nrow) {
+      mu_n = mean[row + gridDim.x];
+      rs_n = rstd[row + gridDim.x];
+    }
+    // refill the slot of row i - 1 (read into registers last iteration) with
+    // row i + P - 1; then row i's own copies are complete
+    issue(i + P - 1);
+    cp_async_wait<P - 1>();
+    float xv[VN], dv[VN];
+    float s1 = 0.0f, s2 = 0.0f;
+    const uint4* slot = ln_ring + (i % P) * 3 * nt + t;
+    if (have) {
+      vunpack<T>(slot[0], xv);
+      vunpack<T>(slot[nt], dv);
+      // column pairs in packed float32x2 arithmetic (half the instructions)
+      float s1b = 0.0f, s2b = 0.0f;
+#pragma unroll
+      for (int j = 0; j < VN; j += 2) {
+        float g0, g1;
+        add2(xv[j], xv[j + 1], xv[j], xv[j + 1], -mu, -mu);
+        mul2(xv[j], xv[j + 1], xv[j], xv[j + 1], rs, rs);  // x-hat
+        mul2(g0, g1, dv[j], dv[j + 1], gm[j], gm[j + 1]);
+        add2(s1, s1b, s1, s1b, g0, g1);
+        fma2(s2, s2b, g0, g1, xv[j], xv[j + 1], s2, s2b);
+        fma2(pg[j], pg[j + 1], dv[j], dv[j + 1], xv[j], xv[j + 1], pg[j], pg[j + 1]);
+        add2(pb[j], pb[j + 1], pb[j], pb[j + 1], dv[j], dv[j + 1]);
+      }
+      s1 += s1b;
+      s2 += s2b;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      s1 += __shfl_xor_sync(0xffffffffu, s1, o);
+      s2 += __shfl_xor_sync(0xffffffffu, s2, o);
+    }
+    float2* rb = red[i & 1];
+    if (lane == 0) rb[warp] = make_float2(s1, s2);
+    __syncthreads();
+    float2 tot = lane < (nt >> 5) ? rb[lane] : make_float2(0.0f, 0.0f);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      tot.x += __shfl_xor_sync(0xffffffffu, tot.x, o);
+      tot.y += __shfl_xor_sync(0xffffffffu, tot.y, o);
+    }
+    if (have) {
+      const float nmg = -tot.x * inv_cols, nmgx = -tot.y * inv_cols;
+      float rv[VN], o[VN];
+      if (dres) {
+        // (the slot is refilled only in the next iteration)
+        vunpack<T>(slot[2 * nt], rv);
+      } else {
+#pragma unroll
+        for (int j = 0; j < VN; ++j) rv[j] = 0.0f;
+      }
+      // dx = rs (g - mean(g) - x-hat mean(g x-hat)) (+ dres)
+#pragma unroll
+      for (int j = 0; j < VN; j += 2) {
+        mul2(o[j], o[j + 1], dv[j], dv[j + 1], gm[j], gm[j + 1]);
+        add2(o[j], o[j + 1], o[j], o[j + 1], nmg, nmg);
+        fma2(o[j], o[j + 1], xv[j], xv[j + 1], nmgx, nmgx, o[j], o[j + 1]);
+        fma2(o[j], o[j + 1], o[j], o[j + 1], rs, rs, rv[j], rv[j + 1]);
+      }
+      vstore(dx + (int64_t)row * cols + t * VN, o);
     }
   }
-  red[0][threadIdx.y][threadIdx.x] = s0;
-  red[1][threadIdx.y][threadIdx.x] = s1;
+  cp_async_wait<0>();
+  if (part == nullptr) return;
+  if constexpr (CL == 1) {
+    if (have) {
+      float* pgr = part + (int64_t)blockIdx.x * cols + t * VN;
+      float* pbr = part + (int64_t)(gridDim.x + blockIdx.x) * cols + t * VN;
+#pragma unroll
+      for (int j = 0; j < VN; j += 4) {
+        *reinterpret_cast<float4*>(pgr + j) = make_float4(pg[j], pg[j + 1], pg[j + 2], pg[j + 3]);
+        *reinterpret_cast<float4*>(pbr + j) = make_float4(pb[j], pb[j + 1], pb[j + 2], pb[j + 3]);
+      }
+    }
+  } else {
+    // this CTA's partials as [2][cols] float32 over the start of the ring
+    // (every thread's copies into it have completed)
+    __syncthreads();
+    float4* sp = reinterpret_cast<float4*>(ln_ring);
+    const int c4n = cols / 4;
+    if (have) {
+#pragma unroll
+      for (int j = 0; j < VN; j += 4) {
+        sp[(t * VN + j) / 4] = make_float4(pg[j], pg[j + 1], pg[j + 2], pg[j + 3]);
+        sp[c4n + (t * VN + j) / 4] = make_float4(pb[j], pb[j + 1], pb[j + 2], pb[j + 3]);
+      }
+    }
+    cluster_sync();  // every CTA's partials are in its shared memory
+    const int rank = (int)cluster_ctarank();
+    const int share = (c4n + CL - 1) / CL;
+    const int c_end = min(c4n, (rank + 1) * share);
+    const int64_t prow = blockIdx.x / CL, nrows = gridDim.x / CL;
+    const uint32_t sp_addr = smem_u32(sp);
+    for (int c = rank * share + t; c < c_end; c += nt) {
+      float4 a = make_float4(0.0f, 0.0f, 0.0f, 0.0f), b = a;
+#pragma unroll 1
+      for (int k = 0; k < CL; ++k) {
+        const uint32_t ra = mapa_shared(sp_addr + c * 16, k);
+        const uint32_t rb = mapa_shared(sp_addr + (c4n + c) * 16, k);
+        float4 u, w;
+        asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+                     : "=f"(u.x), "=f"(u.y), "=f"(u.z), "=f"(u.w) : "r"(ra) : "memory");
+        asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+                     : "=f"(w.x), "=f"(w.y), "=f"(w.z), "=f"(w.w) : "r"(rb) : "memory");
+        a.x += u.x; a.y += u.y; a.z += u.z; a.w += u.w;
+        b.x += w.x; b.y += w.y; b.z += w.z; b.w += w.w;
+      }
+      reinterpret_cast<float4*>(part + prow * cols)[c] = a;
+      reinterpret_cast<float4*>(part + (nrows + prow) * cols)[c] = b;
+    }
+    cluster_sync();  // no CTA leaves while the others still read its shared memory
+  }
+}
+
+// out0[c] = sum_p part[p * stride, c] and out1[c] = sum_p part[half + p * stride, c]
+// for p < nparts (rows of `cols` floats), written as T (nullable outputs
+// skipped). Block (32 x 16), grid (column blocks, 2): lane = column (coalesced
+// 128-byte rows of the partial buffer), blockIdx.y = which output, the 16
+// warps split the partials (four rows' loads in flight per thread), fixed
+// order of summation (deterministic).
+template <typename T>
+__global__ void __launch_bounds__(512) reduce_parts_kernel(int nparts, int stride, int64_t half,
+                                                           int cols, const float* __restrict__ part,
+                                                           T* __restrict__ out0,
+                                                           T* __restrict__ out1) {
+  __shared__ float red[16][33];
+  T* out = blockIdx.y == 0 ? out0 : out1;
+  if (out == nullptr) return;
+  const float* src = part + (blockIdx.y == 0 ? 0 : half);
+  const int c = blockIdx.x * 32 + threadIdx.x;
+  float s = 0.0f;
+  if (c < cols) {
+#pragma unroll 4
+    for (int p = threadIdx.y; p < nparts; p += 16) s += src[(int64_t)p * stride * cols + c];
+  }
+  red[threadIdx.y][threadIdx.x] = s;
   __syncthreads();
   if (threadIdx.y == 0 && c < cols) {
-    float a = 0.0f, b = 0.0f;
+    float a = 0.0f;
 #pragma unroll
-    for (int y = 0; y < 8; ++y) {
-      a += red[0][y][threadIdx.x];
-      b += red[1][y][threadIdx.x];
-    }
-    if (out0) out0[c] = from_f<T>(a);
-    if (out1) out1[c] = from_f<T>(b);
+    for (int y = 0; y < 16; ++y) a += red[y][threadIdx.x];
+    out[c] = from_f<T>(a);
   }
 }
 
@@ -841,11 +1057,11 @@ void reduce_parts_go(int nparts, int cols, float* part, T* out0, T* out1, cudaSt
     const int splits = (nparts + per - 1) / per;
     fold_parts_kernel<<<dim3((cols + 127) / 128, splits), block, 0, st>>>(nparts, per, cols, part,
                                                                           out1 != nullptr);
-    reduce_parts_kernel<T><<<(cols + 31) / 32, block, 0, st>>>(splits, per, half, cols, part,
-                                                               out0, out1);
+    reduce_parts_kernel<T><<<dim3((cols + 31) / 32, 2), dim3(32, 16), 0, st>>>(
+        splits, per, half, cols, part, out0, out1);
   } else {
-    reduce_parts_kernel<T><<<(cols + 31) / 32, block, 0, st>>>(nparts, 1, half, cols, part, out0,
-                                                               out1);
+    reduce_parts_kernel<T><<<dim3((cols + 31) / 32, 2), dim3(32, 16), 0, st>>>(
+        nparts, 1, half, cols, part, out0, out1);
   }
 }
 
@@ -929,7 +1145,8 @@ mgb_status ln_fwd_tma_vpl(int rows, int cols, float eps, const void* x, const vo
                           const void* beta, void* y, float* mean, float* rstd, cudaStream_t st) {
   const int slot = cols * 2;
   const int nslot = std::max(2, std::min(16, (96 << 10) / slot));
-  const size_t smem = (size_t)nslot * slot + 16 * nslot + 16 + 2 * (size_t)cols * 2;
+  // ring, barriers, abort flag, float32 gamma and beta
+  const size_t smem = (size_t)nslot * slot + 16 * nslot + 16 + 2 * (size_t)cols * 4;
   auto kern = ln_fwd_tma_kernel<VPL>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
       cudaSuccess)
@@ -1059,7 +1276,103 @@ int ln_bwd_go(int nparts, int threads, int rows, int cols, const void* x, const 
   return grid;
 }
 
-// Returns the partial rows written (the grid), or -1 for an unsupported width.
+// The asynchronous-copy backward (rows of up to 1024 vectors): a ring of 4 rows
+// while it fits in 100 KB of shared memory (two blocks of 512 threads per SM at
+// bf16 H = 4096), else 2. Returns the grid (partial rows written), -2 on a
+// launch-setup error.
+//
+// With partial sums wanted and enough rows, the CTAs run in clusters of four
+// (partial rows: a quarter of the CTAs, so the final reduction is one small
+// pass) when clusters of four still fill the machine to within 6 %.
+template <typename T, int P, int CL>
+int ln_bwd_async_cl(int clusters, int threads, size_t smem, int rows, int cols, const void* x,
+                    const float* mean, const float* rstd, const void* gamma, const void* dy,
+                    const void* dres, void* dx, float* part, cudaStream_t st) {
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = CL;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(CL * clusters, 1, 1);
+  cfg.blockDim = dim3(threads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, ln_bwd_async_kernel<T, P, CL>, rows, cols, (const T*)x, mean, rstd,
+                         (const T*)gamma, (const T*)dy, (const T*)dres, (T*)dx, part) != cudaSuccess)
+    return -2;
+  return clusters;
+}
+
+// Clusters of CL resident at once for this launch shape (0 if the query fails).
+template <typename T, int P, int CL>
+int ln_bwd_max_clusters(int threads, size_t smem) {
+  auto kern = ln_bwd_async_kernel<T, P, CL>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+      cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = CL;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(CL * 64, 1, 1);
+  cfg.blockDim = dim3(threads, 1, 1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int n = 0;
+  if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  return n;
+}
+
+template <typename T, int P>
+int ln_bwd_async_p(int nparts, int threads, int rows, int cols, const void* x, const float* mean,
+                   const float* rstd, const void* gamma, const void* dy, const void* dres,
+                   void* dx, float* part, cudaStream_t st) {
+  constexpr int CL = 4;
+  const size_t smem = (size_t)P * 3 * threads * 16;
+  auto kern = ln_bwd_async_kernel<T, P, 1>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+      cudaSuccess)
+    return -2;
+  const int resident = resident_ctas(kern, threads, smem) * device_sm_count();
+  // the partials of a cluster fit in its CTAs' rings
+  if (part && std::min(nparts, rows) >= 2 * CL && 2 * (size_t)cols * 4 <= smem) {
+    const int mc = ln_bwd_max_clusters<T, P, CL>(threads, smem);
+    if (mc > 0 && (int64_t)mc * CL * 100 >= (int64_t)resident * 94) {
+      const int clusters = std::min(mc, std::min(nparts, rows) / CL);
+      return ln_bwd_async_cl<T, P, CL>(clusters, threads, smem, rows, cols, x, mean, rstd, gamma,
+                                       dy, dres, dx, part, st);
+    }
+  }
+  const int grid = std::max(1, std::min(nparts, resident));
+  kern<<<grid, threads, smem, st>>>(rows, cols, (const T*)x, mean, rstd, (const T*)gamma,
+                                    (const T*)dy, (const T*)dres, (T*)dx, part);
+  return grid;
+}
+
+template <typename T>
+int ln_bwd_async_go(int nparts, int threads, int rows, int cols, const void* x, const float* mean,
+                    const float* rstd, const void* gamma, const void* dy, const void* dres,
+                    void* dx, float* part, cudaStream_t st) {
+  if ((size_t)4 * 3 * threads * 16 <= (100u << 10))
+    return ln_bwd_async_p<T, 4>(nparts, threads, rows, cols, x, mean, rstd, gamma, dy, dres, dx,
+                                part, st);
+  return ln_bwd_async_p<T, 2>(nparts, threads, rows, cols, x, mean, rstd, gamma, dy, dres, dx,
+                              part, st);
+}
+
+// Returns the partial rows written (the grid), -1 for an unsupported width,
+// -2 on a launch-setup error.
 template <typename T>
 int ln_bwd_dispatch(int nparts, int rows, int cols, const void* x, const float* mean,
                     const float* rstd, const void* gamma, const void* dy, const void* dres,
@@ -1068,8 +1381,16 @@ int ln_bwd_dispatch(int nparts, int rows, int cols, const void* x, const float* 
   // for rows wider than 1024 vectors
   const int nvec = cols / Vec<T>::N;
   auto thr = [&](int vpt) { return ((nvec + vpt - 1) / vpt + 31) / 32 * 32; };
-  if (nvec <= 1024)
-    return ln_bwd_go<T, 1>(nparts, thr(1), rows, cols, x, mean, rstd, gamma, dy, dres, dx, part, st);
+  if (nvec <= 1024) {
+    // MGB_LN_KERNEL=block: the register-prefetch kernel instead of the
+    // asynchronous-copy one
+    const char* kenv = getenv("MGB_LN_KERNEL");
+    if (kenv && strcmp(kenv, "block") == 0)
+      return ln_bwd_go<T, 1>(nparts, thr(1), rows, cols, x, mean, rstd, gamma, dy, dres, dx, part,
+                             st);
+    return ln_bwd_async_go<T>(nparts, thr(1), rows, cols, x, mean, rstd, gamma, dy, dres, dx, part,
+                              st);
+  }
   if (nvec <= 2048)
     return ln_bwd_go<T, 2>(nparts, thr(2), rows, cols, x, mean, rstd, gamma, dy, dres, dx, part, st);
   if (nvec <= 4096)
@@ -1092,8 +1413,8 @@ mgb_status layernorm_bwd_launch(int rows, int cols, int dtype, const void* x, co
   if (rows == 0) nparts = 1;
   // the TMA-fed bf16 kernel writes as many partial rows as its grid (at most
   // nparts); the reduction then folds that many
-  // (the block kernel is the default: measured faster at the layer's shape;
-  // MGB_LN_KERNEL=tma selects the bulk-copy kernel)
+  // (MGB_LN_KERNEL=tma selects the bulk-copy kernel; otherwise rows of up to
+  // 1024 vectors take the asynchronous-copy kernel, wider ones the block kernel)
   const char* kenv = getenv("MGB_LN_KERNEL");
   const bool tma = dtype == MGB_BF16 && rows > 0 && cols * 2 * 3 <= (96 << 10) && kenv &&
                    strcmp(kenv, "tma") == 0;
@@ -1124,6 +1445,7 @@ mgb_status layernorm_bwd_launch(int rows, int cols, int dtype, const void* x, co
                  : ln_bwd_dispatch<float>(nparts, rows, cols, x, mean, rstd, gamma, dy, dres, dx,
                                           want ? part : nullptr, st);
     }
+    if (used == -2) return MGB_ERR_CUDA;
     if (used < 0) return MGB_ERR_UNSUPPORTED;
     nparts = used;
   }

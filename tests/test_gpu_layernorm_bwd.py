@@ -25,11 +25,16 @@ def _dev(a, dtype):
     ("bf16", 40, 12288, True, True), ("bf16", 33, 16384, True, False),
     ("f32", 20, 8192, True, True), ("f32", 17, 16384, True, True),
     # many rows per CTA: the bf16 kernel's shared-memory ring refilled many times
-    ("bf16", 8192, 4096, True, True), ("bf16", 3000, 2048, True, False)])
-@pytest.mark.parametrize("kernel", ["tma", "block"])
+    ("bf16", 8192, 4096, True, True), ("bf16", 3000, 2048, True, False),
+    # more than 64 rows per block: row statistics read one row ahead instead
+    # of staged up front
+    ("bf16", 70000, 256, True, True)])
+@pytest.mark.parametrize("kernel", ["async", "tma", "block"])
 def test_layernorm_bwd(mgb_lib, monkeypatch, kernel, dtype, rows, cols, affine, resid):
-    """bf16 rows up to 16384 wide go through the kernel fed by bulk copies
-    (three rows per shared-memory slot) unless MGB_LN_KERNEL=block."""
+    """Rows of up to 1024 vectors go through the kernel fed by per-thread
+    asynchronous copies (the default), the bf16 kernel fed by bulk copies
+    (MGB_LN_KERNEL=tma, rows up to 16384 wide) or the register-prefetch block
+    kernel (MGB_LN_KERNEL=block); wider rows always take the block kernel."""
     monkeypatch.setenv("MGB_LN_KERNEL", kernel)
     x = RNG.standard_normal((rows, cols)) * 1.5 + 0.3
     dy = RNG.standard_normal((rows, cols))
