@@ -74,7 +74,7 @@ __global__ void emb_fwd_kernel(int T, int H, int elt, int v0, int v1, const int3
   }
 }
 
-constexpr int RANK_I = 256, RANK_J = 1024;
+constexpr int RANK_I = 128, RANK_J = 512;
 
 // rank[t] += number of tokens t' < t with ids[t'] = ids[t], over the tokens t'
 // of tile blockIdx.y (RANK_J of them) and the tokens t of tile blockIdx.x
@@ -98,6 +98,7 @@ __global__ void __launch_bounds__(RANK_I) emb_rank_kernel(int T, int v0, int v1,
   const int lim = own ? max(0, min(n, t - j0)) : 0;  // tokens t' < t of this tile
   int r = 0;
   const int4* tile4 = reinterpret_cast<const int4*>(tile);
+#pragma unroll 4
   for (int q = 0; q < lim / 4; ++q) {
     const int4 x = tile4[q];
     r += (x.x == v) + (x.y == v) + (x.z == v) + (x.w == v);
@@ -201,6 +202,49 @@ __global__ void emb_place_kernel(int T, int v0, int v1, const int32_t* __restric
   if (rk == 0) seg_end[pos] = offsets[row + 1];
 }
 
+// As emb_place_kernel, for accumulate mode, from the chunk-local offsets of
+// emb_scan_chunks and the raw chunk totals (nchunks <= 1024): each block scans
+// the chunk totals itself (fixed order), so the last two scan steps are not
+// launched. *npos = the in-shard tokens (written by block 0).
+__global__ void __launch_bounds__(256) emb_place_chunked_kernel(
+    int T, int v0, int v1, const int32_t* __restrict__ ids, const int32_t* __restrict__ rank,
+    const int32_t* __restrict__ counts, const int32_t* __restrict__ local_off,
+    const int32_t* __restrict__ totals, int nchunks, int32_t* __restrict__ order,
+    int32_t* __restrict__ seg_row, int32_t* __restrict__ seg_end, int32_t* __restrict__ npos) {
+  __shared__ int cbase[1025];  // exclusive chunk bases, then the grand total
+  if (threadIdx.x < 32) {
+    const int lane = threadIdx.x;
+    int carry = 0;
+    for (int c0 = 0; c0 < nchunks; c0 += 32) {
+      const int c = c0 + lane;
+      const int v = c < nchunks ? totals[c] : 0;
+      int incl = v;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int x = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += x;
+      }
+      if (c < nchunks) cbase[c] = carry + incl - v;
+      carry += __shfl_sync(0xffffffffu, incl, 31);
+    }
+    if (lane == 0) {
+      cbase[nchunks] = carry;
+      if (blockIdx.x == 0) *npos = carry;
+    }
+  }
+  __syncthreads();
+  const int t = blockIdx.x * blockDim.x + threadIdx.x;
+  if (t >= T) return;
+  const int v = ids[t];
+  if (v < v0 || v >= v1) return;
+  const int row = v - v0, rk = rank[t];
+  const int start = local_off[row] + cbase[row / SCAN_CHUNK];
+  const int pos = start + rk;
+  order[pos] = t;
+  seg_row[pos] = rk == 0 ? row : -1;
+  if (rk == 0) seg_end[pos] = start + counts[row];
+}
+
 // Sum of one row's token gradients in token order (float32), added to or
 // written over the row.
 template <typename T>
@@ -227,20 +271,54 @@ __device__ __forceinline__ void emb_row_sum(int H, int a, int b, const int32_t* 
   }
 }
 
-// Accumulate mode: one block per position of the token order; the block at
-// the head of a row's segment adds the row's sum, the others return. Rows
-// without tokens are not touched.
+// Accumulate mode, one block per position of the token order (*npos
+// positions): the block at the head of a row's segment adds
+// the row's tokens in token order onto the row, the others return. Two
+// vectors per thread per step, with the row's and the first token's vectors
+// requested together.
 template <typename T>
-__global__ void emb_accum_heads_kernel(int rows, int H, const int32_t* __restrict__ offsets,
+__global__ void emb_accum_heads_kernel(int H, const int32_t* __restrict__ npos,
                                        const int32_t* __restrict__ order,
                                        const int32_t* __restrict__ seg_row,
                                        const int32_t* __restrict__ seg_end,
                                        const T* __restrict__ dout, T* __restrict__ d_emb) {
+  constexpr int VN = EVec<T>::N;
   const int p = blockIdx.x;
-  if (p >= offsets[rows]) return;
+  if (p >= *npos) return;
   const int row = seg_row[p];
   if (row < 0) return;
-  emb_row_sum<T>(H, p, seg_end[p], order, dout, d_emb + (int64_t)row * H, true);
+  const int end = seg_end[p], t0 = order[p];
+  const int nvec = H / VN;
+  T* dst = d_emb + (int64_t)row * H;
+  const T* g0 = dout + (int64_t)t0 * H;
+  for (int vi = threadIdx.x; vi < nvec; vi += 2 * blockDim.x) {
+    const int vj = vi + blockDim.x;
+    const bool two = vj < nvec;
+    float a[VN], b[VN], ga[VN], gb[VN];
+    eload(dst + vi * VN, a);
+    eload(g0 + vi * VN, ga);
+    if (two) {
+      eload(dst + vj * VN, b);
+      eload(g0 + vj * VN, gb);
+    }
+#pragma unroll
+    for (int j = 0; j < VN; ++j) {
+      a[j] += ga[j];
+      b[j] = two ? b[j] + gb[j] : 0.0f;
+    }
+    for (int i = p + 1; i < end; ++i) {
+      const T* gi = dout + (int64_t)order[i] * H;
+      eload(gi + vi * VN, ga);
+      if (two) eload(gi + vj * VN, gb);
+#pragma unroll
+      for (int j = 0; j < VN; ++j) {
+        a[j] += ga[j];
+        if (two) b[j] += gb[j];
+      }
+    }
+    estore(dst + vi * VN, a);
+    if (two) estore(dst + vj * VN, b);
+  }
 }
 
 // Overwrite mode: blocks stride over all shard rows; rows without tokens are
@@ -258,9 +336,9 @@ __global__ void emb_write_rows_kernel(int rows, int H, const int32_t* __restrict
 size_t embedding_bwd_ws(int T, int v0, int v1) {
   const size_t rows = v1 > v0 ? (size_t)(v1 - v0) : 0;
   const size_t chunks = (rows + SCAN_CHUNK - 1) / SCAN_CHUNK;
-  // rank, order, seg_row, seg_end [T]; counts [rows] (16-byte aligned, padded);
-  // offsets [rows + 1]; chunk totals [chunks + 1]
-  return 4 * (4 * (size_t)T + (rows + 3) / 4 * 4 + rows + 1 + chunks + 1) + 256;
+  // counts [rows] (padded to a multiple of 4), rank, order, seg_row, seg_end
+  // [T]; offsets [rows + 1]; chunk totals [chunks + 1]; positions [1]
+  return 4 * ((rows + 3) / 4 * 4 + 4 * (size_t)T + rows + 1 + chunks + 1 + 1) + 256;
 }
 
 mgb_status embedding_fwd_launch(int T, int H, int dtype, int v0, int v1, const int32_t* ids,
@@ -282,42 +360,54 @@ mgb_status embedding_bwd_launch(int T, int H, int dtype, int v0, int v1, const i
                                 cudaStream_t st) {
   const int rows = v1 - v0;
   const int nchunks = (rows + SCAN_CHUNK - 1) / SCAN_CHUNK;
-  int32_t* rank = static_cast<int32_t*>(ws);
+  // counts and rank side by side (one zeroing); counts first, so 16-byte aligned
+  int32_t* counts = static_cast<int32_t*>(ws);
+  int32_t* rank = counts + (rows + 3) / 4 * 4;
   int32_t* order = rank + T;
   int32_t* seg_row = order + T;
   int32_t* seg_end = seg_row + T;
-  int32_t* counts = seg_end + T;
-  counts += (4 - (reinterpret_cast<uintptr_t>(counts) / 4) % 4) % 4;  // 16-byte aligned
-  int32_t* offsets = counts + (rows + 3) / 4 * 4;
+  int32_t* offsets = seg_end + T;
   int32_t* totals = offsets + rows + 1;
-  LaunchScope scope(PROF_EMBEDDING, st, 3 + (T > 0 ? 3 : (accumulate ? 0 : 1)));
-  if (cudaMemsetAsync(counts, 0, sizeof(int32_t) * rows, st) != cudaSuccess) return MGB_ERR_CUDA;
+  int32_t* npos = totals + nchunks + 1;
+  const int vn = dtype == MGB_BF16 ? 8 : 4;
+  const int nvec = H / vn;
+  if (accumulate && T == 0) return MGB_OK;  // nothing to add
+  // accumulate: rank, chunk scan, placement (finishing the scan), sums;
+  // overwrite: rank, the three scan steps, placement, every row written
+  const bool chunked = accumulate && nchunks <= 1024;
+  LaunchScope scope(PROF_EMBEDDING, st, chunked ? 4 : 3 + (T > 0 ? 3 : 1));
+  if (cudaMemsetAsync(counts, 0, sizeof(int32_t) * ((rows + 3) / 4 * 4 + (size_t)T), st) !=
+      cudaSuccess)
+    return MGB_ERR_CUDA;
   if (T > 0) {
-    if (cudaMemsetAsync(rank, 0, sizeof(int32_t) * T, st) != cudaSuccess) return MGB_ERR_CUDA;
     const dim3 grid((T + RANK_I - 1) / RANK_I, (T + RANK_J - 1) / RANK_J);
     emb_rank_kernel<<<grid, RANK_I, 0, st>>>(T, v0, v1, ids, rank, counts);
   }
   emb_scan_chunks<<<nchunks, SCAN_THREADS, 0, st>>>(rows, counts, offsets, totals);
-  emb_scan_totals<<<1, SCAN_THREADS, 0, st>>>(nchunks, totals);
-  emb_scan_add<<<(rows + 255) / 256, 256, 0, st>>>(rows, totals, nchunks, offsets);
-  if (T > 0)
-    emb_place_kernel<<<(T + 255) / 256, 256, 0, st>>>(T, v0, v1, ids, rank, offsets, order, seg_row,
-                                                      seg_end);
-  const int vn = dtype == MGB_BF16 ? 8 : 4;
-  const int nvec = H / vn;
-  const int threads = nvec >= 256 ? 256 : ((nvec + 31) / 32) * 32;
-  if (accumulate) {
-    if (T > 0) {
-      if (dtype == MGB_BF16)
-        emb_accum_heads_kernel<bf16><<<T, threads, 0, st>>>(rows, H, offsets, order, seg_row, seg_end,
-                                                            static_cast<const bf16*>(dout),
-                                                            static_cast<bf16*>(d_emb));
-      else
-        emb_accum_heads_kernel<float><<<T, threads, 0, st>>>(rows, H, offsets, order, seg_row,
-                                                             seg_end, static_cast<const float*>(dout),
-                                                             static_cast<float*>(d_emb));
-    }
+  if (chunked) {
+    emb_place_chunked_kernel<<<(T + 255) / 256, 256, 0, st>>>(
+        T, v0, v1, ids, rank, counts, offsets, totals, nchunks, order, seg_row, seg_end, npos);
   } else {
+    emb_scan_totals<<<1, SCAN_THREADS, 0, st>>>(nchunks, totals);
+    emb_scan_add<<<(rows + 255) / 256, 256, 0, st>>>(rows, totals, nchunks, offsets);
+    if (T > 0)
+      emb_place_kernel<<<(T + 255) / 256, 256, 0, st>>>(T, v0, v1, ids, rank, offsets, order,
+                                                        seg_row, seg_end);
+  }
+  if (accumulate) {
+    // one block per position; two vectors per thread per step
+    const int athreads = std::min(256, ((nvec + 1) / 2 + 31) / 32 * 32);
+    const int32_t* np = chunked ? npos : offsets + rows;
+    if (dtype == MGB_BF16)
+      emb_accum_heads_kernel<bf16><<<T, athreads, 0, st>>>(H, np, order, seg_row, seg_end,
+                                                           static_cast<const bf16*>(dout),
+                                                           static_cast<bf16*>(d_emb));
+    else
+      emb_accum_heads_kernel<float><<<T, athreads, 0, st>>>(H, np, order, seg_row, seg_end,
+                                                            static_cast<const float*>(dout),
+                                                            static_cast<float*>(d_emb));
+  } else {
+    const int threads = nvec >= 256 ? 256 : ((nvec + 31) / 32) * 32;
     const int grid = rows < device_sm_count() * 32 ? rows : device_sm_count() * 32;
     if (dtype == MGB_BF16)
       emb_write_rows_kernel<bf16><<<grid, threads, 0, st>>>(rows, H, offsets, order,
