@@ -388,9 +388,11 @@ mgb_status mgb_layernorm_bwd(int32_t rows, int32_t cols, int32_t dtype, const vo
  *   - size: 2 x 64 x 16384 floats (8 MiB), held by every GPU that loads the
  *     library until the process exits; cols > 16384 with dgamma or dbeta
  *     requested returns MGB_ERR_UNSUPPORTED before any launch;
- *   - a call uses min(the row blocks mgb_layernorm_bwd would use,
- *     2^20 / cols) partial rows of the array (256 at cols = 4096), so the
- *     backward still spreads over the whole GPU;
+ *   - a call uses at most min(the partial rows mgb_layernorm_bwd would use,
+ *     2^20 / cols) rows of the array (256 at cols = 4096; the kernel for rows
+ *     of up to 1024 vectors combines its partials in clusters of CTAs and
+ *     writes one row per cluster), so the backward still spreads over the
+ *     whole GPU;
  *   - the library calls no cudaMalloc/cudaFree or allocating routine (keep
  *     the tracing of mgb_profile_enable off: when on, it creates CUDA events);
  *   - the first call on each device looks up the array's device address with

@@ -1349,7 +1349,8 @@ int ln_bwd_async_p(int nparts, int threads, int rows, int cols, const void* x, c
   if (part && std::min(nparts, rows) >= 2 * CL && 2 * (size_t)cols * 4 <= smem) {
     const int mc = ln_bwd_max_clusters<T, P, CL>(threads, smem);
     if (mc > 0 && (int64_t)mc * CL * 100 >= (int64_t)resident * 94) {
-      const int clusters = std::min(mc, std::min(nparts, rows) / CL);
+      // one partial row per cluster: at most nparts of them
+      const int clusters = std::min(mc, std::min(nparts, (rows + CL - 1) / CL));
       return ln_bwd_async_cl<T, P, CL>(clusters, threads, smem, rows, cols, x, mean, rstd, gamma,
                                        dy, dres, dx, part, st);
     }
