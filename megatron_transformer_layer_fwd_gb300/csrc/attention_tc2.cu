@@ -28,7 +28,8 @@
 //              ring; a stage is refilled once its last reader is done
 //   warps 2-5  softmax of tile A, warps 6-9 softmax of tile B: one thread per
 //              query row (warp w reads TMEM lane quarter w % 4) over all 128
-//              keys: a pass for the row maximum, then a pass for the
+//              keys, in chunks of 64 (32 with dropout): on a row's first key
+//              tile a pass for the row maximum, then one pass for the
 //              exponentials, the row sum and P; then, at the item's end, O / l
 //              and LSE to global memory
 // Online softmax in the log2 domain with a lazy reference: a row's reference
@@ -399,13 +400,51 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
         tc_fence_after();
         const bool interior = kv0 + TK <= p.S && (!p.causal || kv0 + TK - 1 <= row0);
-        // From the second key tile on (m_ref is then finite: the first tile
-        // holds a visible key of every row) one pass: each 32-key chunk's
-        // maximum is checked against the reference as it is read, and only a
-        // chunk that exceeds it by more than TAU moves it, by a whole number k
-        // of log2 units, so that the P already written for this tile and the
-        // O row scale by 2^-k exactly. The first tile takes the row maximum in
-        // a pass of its own.
+        // The scores are read in chunks of CW keys (64 without dropout: two
+        // TMEM round trips per pass; 32 with dropout, whose keep bits need
+        // the registers). From the second key tile on (m_ref is then finite:
+        // the first tile holds a visible key of every row) one pass: each
+        // chunk's maximum is checked against the reference as it is read, and
+        // only a chunk that exceeds it by more than TAU moves it, by a whole
+        // number k of log2 units, so that the P already written for this tile
+        // and the O row scale by 2^-k exactly. The first tile takes the row
+        // maximum in a pass of its own.
+        constexpr int CW = DROP ? 32 : 64;
+        auto load_chunk = [&](int c, float (&sc)[CW]) {
+          uint32_t qa[32];
+          tmem_ld32(ts + c * CW, qa);
+          if constexpr (CW == 64) {
+            uint32_t qb[32];
+            tmem_ld32(ts + c * CW + 32, qb);
+            tmem_ld_wait();
+            tmem_regs_ready(qb);
+#pragma unroll
+            for (int e = 0; e < 32; ++e) sc[32 + e] = __uint_as_float(qb[e]);
+          } else {
+            tmem_ld_wait();
+          }
+          tmem_regs_ready(qa);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) sc[e] = __uint_as_float(qa[e]);
+          if (!interior) {
+#pragma unroll
+            for (int e = 0; e < CW; ++e) {
+              const int key = kv0 + c * CW + e;
+              if (key >= p.S || (p.causal && key > row)) sc[e] = -INFINITY;
+            }
+          }
+        };
+        auto chunk_max = [&](const float (&sc)[CW], float m0) {
+          float m4[4] = {m0, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+          for (int e = 0; e < CW; e += 8) {
+            m4[0] = fmax3(m4[0], sc[e], sc[e + 1]);
+            m4[1] = fmax3(m4[1], sc[e + 2], sc[e + 3]);
+            m4[2] = fmax3(m4[2], sc[e + 4], sc[e + 5]);
+            m4[3] = fmax3(m4[3], sc[e + 6], sc[e + 7]);
+          }
+          return fmaxf(fmax3(m4[0], m4[1], m4[2]), m4[3]);
+        };
         const bool one_pass = j > 0 && __all_sync(0xffffffffu, m_ref > -INFINITY);
         bool need = false;
         float alpha = 1.0f;
@@ -413,25 +452,10 @@ __global__ void __launch_bounds__(NTHREADS, 1)
           // pass 1: the row maximum over the 128 scores
           float mx = -INFINITY;
 #pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            float sc[32];
-            ld_cols32(ts + c * 32, sc);
-            if (!interior) {
-#pragma unroll
-              for (int e = 0; e < 32; ++e) {
-                const int key = kv0 + c * 32 + e;
-                if (key >= p.S || (p.causal && key > row)) sc[e] = -INFINITY;
-              }
-            }
-            float m4[4] = {mx, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
-            for (int e = 0; e < 32; e += 8) {
-              m4[0] = fmax3(m4[0], sc[e], sc[e + 1]);
-              m4[1] = fmax3(m4[1], sc[e + 2], sc[e + 3]);
-              m4[2] = fmax3(m4[2], sc[e + 4], sc[e + 5]);
-              m4[3] = fmax3(m4[3], sc[e + 6], sc[e + 7]);
-            }
-            mx = fmaxf(fmax3(m4[0], m4[1], m4[2]), m4[3]);
+          for (int c = 0; c < TK / CW; ++c) {
+            float sc[CW];
+            load_chunk(c, sc);
+            mx = chunk_max(sc, mx);
           }
           mx *= p.sl2;
           need = mx > m_ref + TAU;
@@ -443,30 +467,15 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
         float nref = m_ref == -INFINITY ? 0.0f : -m_ref;
         // pass 2: P = 2^(s log2e / sqrt(d) - m_ref) as bf16 pairs over the
-        // tile's first 64 score columns (chunk c's 32 keys -> columns 16c ..),
+        // tile's first 64 score columns (chunk c's keys -> columns c CW / 2 ..),
         // which only ever cover scores already read in this pass
         float r0 = 0.0f, r1 = 0.0f, r2 = 0.0f, r3 = 0.0f;
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          float sc[32];
-          ld_cols32(ts + c * 32, sc);
-          if (!interior) {
-#pragma unroll
-            for (int e = 0; e < 32; ++e) {
-              const int key = kv0 + c * 32 + e;
-              if (key >= p.S || (p.causal && key > row)) sc[e] = -INFINITY;
-            }
-          }
+        for (int c = 0; c < TK / CW; ++c) {
+          float sc[CW];
+          load_chunk(c, sc);
           if (one_pass) {
-            float m4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
-            for (int e = 0; e < 32; e += 8) {
-              m4[0] = fmax3(m4[0], sc[e], sc[e + 1]);
-              m4[1] = fmax3(m4[1], sc[e + 2], sc[e + 3]);
-              m4[2] = fmax3(m4[2], sc[e + 4], sc[e + 5]);
-              m4[3] = fmax3(m4[3], sc[e + 6], sc[e + 7]);
-            }
-            const float cm = fmaxf(fmax3(m4[0], m4[1], m4[2]), m4[3]) * p.sl2;
+            const float cm = chunk_max(sc, -INFINITY) * p.sl2;
             const bool up = cm > m_ref + TAU;
             if (__any_sync(0xffffffffu, up)) {
               // this row's reference moves up by k: l, the P chunks already
@@ -482,22 +491,23 @@ __global__ void __launch_bounds__(NTHREADS, 1)
                 need = true;
               }
               tmem_st_wait();  // the chunks' P stores have landed
-              for (int cc = 0; cc < c; ++cc) {
+              for (int g = 0; g < c * CW / 32; ++g) {
                 uint32_t pw[16];
-                tmem_ld16(ts + cc * 16, pw);
+                tmem_ld16(ts + g * 16, pw);
                 tmem_ld_wait();
+                tmem_regs_ready(pw);
 #pragma unroll
                 for (int e = 0; e < 16; ++e) {
                   const float2 f = unpack_bf16x2(pw[e]);
                   pw[e] = pack_bf16x2(f.x * a, f.y * a);
                 }
-                tmem_st16(ts + cc * 16, pw);
+                tmem_st16(ts + g * 16, pw);
               }
               nref = -m_ref;
             }
           }
 #pragma unroll
-          for (int e = 0; e < 32; e += 4) {
+          for (int e = 0; e < CW; e += 4) {
             fma2(sc[e], sc[e + 1], sc[e], sc[e + 1], p.sl2, p.sl2, nref, nref);
             fma2(sc[e + 2], sc[e + 3], sc[e + 2], sc[e + 3], p.sl2, p.sl2, nref, nref);
             sc[e] = ex2_ftz(sc[e]);
@@ -507,18 +517,19 @@ __global__ void __launch_bounds__(NTHREADS, 1)
             add2(r0, r1, r0, r1, sc[e], sc[e + 1]);
             add2(r2, r3, r2, r3, sc[e + 2], sc[e + 3]);
           }
-          uint32_t pk[16];
+          uint32_t pk[CW / 2];
           if constexpr (DROP) {
             const uint32_t kw = kb[c];
 #pragma unroll
-            for (int e = 0; e < 16; ++e)
+            for (int e = 0; e < CW / 2; ++e)
               pk[e] = pack_bf16x2((kw >> (2 * e)) & 1u ? sc[2 * e] * p.dscale : 0.0f,
                                   (kw >> (2 * e + 1)) & 1u ? sc[2 * e + 1] * p.dscale : 0.0f);
+            tmem_st16(ts + c * 16, pk);
           } else {
 #pragma unroll
-            for (int e = 0; e < 16; ++e) pk[e] = pack_bf16x2(sc[2 * e], sc[2 * e + 1]);
+            for (int e = 0; e < CW / 2; ++e) pk[e] = pack_bf16x2(sc[2 * e], sc[2 * e + 1]);
+            tmem_st32(ts + c * 32, pk);
           }
-          tmem_st16(ts + c * 16, pk);
         }
         l += (r0 + r1) + (r2 + r3);
         if (j > 0 && __any_sync(0xffffffffu, need)) {
