@@ -28,7 +28,10 @@ def _dev(a, dtype):
     ("bf16", 8192, 4096, True, True), ("bf16", 3000, 2048, True, False),
     # more than 64 rows per block: row statistics read one row ahead instead
     # of staged up front
-    ("bf16", 70000, 256, True, True)])
+    ("bf16", 70000, 256, True, True),
+    # widths whose float4 count does not split evenly over a cluster of four
+    # (the cluster-combined partial sums) and whose vectors do not fill whole warps
+    ("bf16", 300, 1000, True, True), ("f32", 260, 100, True, False)])
 @pytest.mark.parametrize("kernel", ["async", "tma", "block"])
 def test_layernorm_bwd(mgb_lib, monkeypatch, kernel, dtype, rows, cols, affine, resid):
     """Rows of up to 1024 vectors go through the kernel fed by per-thread
