@@ -344,7 +344,7 @@ def run_ours(args, world, rank, local):
     d_flops = ce_kind_flops * args.steps / d_n if d_n else 0.0
     d_tflops = d_flops / (d_ms / d_n / 1e3) / 1e12 if d_n else None
     traffic = traffic_record(os.path.join(ROOT, "megatron_transformer_layer_fwd_gb300", "csrc",
-                                          "gemm_tc.cu"), "gemm_tc_ce_logits")
+                                          "gemm_tc.cu"), f"gemm_tc_ce_logits_tb{tb}")
     roofline = {"kernel": f"gemm_tc_pair_kernel, CE logits per token block {tb}x{ce.vocab}x"
                           f"{ce.hidden} (all vocab chunks of {ce.chunk} in one launch; statistics "
                           "epilogue storing the block's bf16 logits)",
@@ -419,6 +419,30 @@ def run_ours(args, world, rank, local):
                          mgb.MGB_CE_RESIDENT)) / 1e9, 3),
                      "note": "same step with MGB_CE_RESIDENT (whole [T, V] logits kept); "
                              "outside the pages' memory bound, for comparison only"}
+    # the same step with MGB_CE_FUSED: vocab chunks through the logits GEMM's
+    # epilogue, no logits stored at all, the logits recomputed for the gradient
+    fus = CERunner(ce.tokens, ce.hidden, ce.vocab, ce.chunk, layer.y, emb, targets,
+                   mode=mgb.MGB_CE_FUSED, emb_stream=emb_stream)
+    fstep = make_step(fus)
+    for _ in range(2):
+        fstep()
+    torch.cuda.synchronize(dev)
+    f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    f0.record(stream)
+    for _ in range(r_steps):
+        fstep()
+    f1.record(stream)
+    torch.cuda.synchronize(dev)
+    fus_ms = f0.elapsed_time(f1) / r_steps
+    step_fused = {"ms_per_step": round(fus_ms, 4),
+                  "tflops": round(world * step_flops / (fus_ms / 1e3) / 1e12, 2),
+                  "ce_workspace_gb": round(mgb.mgb_vocab_ce_sizes(mgb.ce_desc(
+                      ce.tokens, ce.hidden, ce.vocab, ce.chunk, 1.0 / ce.tokens,
+                      mgb.MGB_CE_FUSED)) / 1e9, 3),
+                  "note": "same step with MGB_CE_FUSED (per-chunk statistics and G in the "
+                          "logits GEMM's epilogue, no logits stored; the logits are computed "
+                          "twice, so its TFLOP/s counts the step's work, not the recompute)"}
+    del fus
     breakdown = {k: round(v[0] / args.steps, 4) for k, v in prof.items() if v[1] > 0}
     # page 1's sequence sweep on the causal workloads (B 8, H 2048, 16 x 128, F
     # 8192): the Attention / FFN / Backward stages per length (library events)
@@ -458,6 +482,7 @@ def run_ours(args, world, rank, local):
                "workspace_gb": round(cer.ws.numel() / 1e9, 3),
                "full_logits_gb": round(2.0 * ce.tokens * ce.vocab / 1e9, 3)},
         "step_resident_ce": step_resident,
+        "step_fused_ce": step_fused,
         "seq_sweep": sweep,
         "gemm_all_launches": gemm_all,
         "kernel_ms_per_step": breakdown,

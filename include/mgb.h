@@ -241,7 +241,7 @@ typedef struct {
    * `stream` on an event recorded on it). The work that follows on `stream`
    * then overlaps d_emb. */
   void* emb_stream;
-  /* MGB_CE_BLOCKED only: tokens per block (0 = 2048), rounded up to a
+  /* MGB_CE_BLOCKED only: tokens per block (0 = 4096), rounded up to a
    * multiple of 256; the logits block takes 2 * token_block * vocab bytes of
    * the workspace. Other modes ignore it. */
   int32_t token_block;

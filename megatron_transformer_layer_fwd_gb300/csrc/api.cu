@@ -648,7 +648,7 @@ struct CEPlan {
   size_t dh_part, de_acc;
 };
 
-constexpr int kCeDefaultTokenBlock = 2048;
+constexpr int kCeDefaultTokenBlock = 4096;
 
 // K ranges (whole 64-wide blocks) of the split-K GEMM for a request of
 // `want` ranges, as the kernel cuts them.

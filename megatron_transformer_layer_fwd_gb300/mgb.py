@@ -32,6 +32,9 @@ MGB_ERR_DEVICE_CHECK = -9
 
 MGB_F32, MGB_BF16 = 0, 1
 MGB_CE_STREAM, MGB_CE_FUSED, MGB_CE_RESIDENT, MGB_CE_BLOCKED = 0, 1, 2, 3
+# tokens per block of MGB_CE_BLOCKED when mgb_ce_desc.token_block is 0 (the
+# library's default, restated here for callers that size their own views)
+CE_DEFAULT_TOKEN_BLOCK = 4096
 MGB_PRE_LN, MGB_POST_LN = 0, 1
 MGB_GELU_ERF, MGB_SWIGLU = 0, 1
 MGB_K_MAJOR, MGB_MN_MAJOR = 0, 1

@@ -69,7 +69,7 @@ class CERunner:
         self.desc.emb_stream = emb_stream.cuda_stream if emb_stream is not None else None
         self.hidden, self.emb, self.targets = hidden_t, emb_t, targets_t
         # the blocked mode's rows per block as the library rounds them
-        tb = token_block if token_block > 0 else 2048
+        tb = token_block if token_block > 0 else mgb.CE_DEFAULT_TOKEN_BLOCK
         self.token_block = min((tb + 255) // 256 * 256, (tokens + 255) // 256 * 256)
         self.ws = torch.empty(max(mgb.mgb_vocab_ce_sizes(self.desc), 16), dtype=torch.uint8, device=dev)
         self.loss = torch.empty(max(tokens, 1), dtype=torch.float32, device=dev)

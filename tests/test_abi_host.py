@@ -149,6 +149,16 @@ def test_ce_blocked_workspace_is_bounded_by_the_block(lib):
     assert one < 2 * 2048 * V + 4 * V * H
 
 
+def test_ce_default_token_block(lib):
+    """token_block = 0 selects the library's default block, which the binding
+    restates (the bench and the runner size their views with it)."""
+    V, H, T = 128256, 4096, 16384
+    size = lambda tb: mgb.mgb_vocab_ce_sizes(mgb.ce_desc(T, H, V, 16032, 1 / T,
+                                                         mode=mgb.MGB_CE_BLOCKED, token_block=tb))
+    assert size(0) == size(mgb.CE_DEFAULT_TOKEN_BLOCK)
+    assert size(0) != size(mgb.CE_DEFAULT_TOKEN_BLOCK // 2)
+
+
 def test_gemm_validation(lib):
     d = mgb.GemmDesc(m=128, n=100, k=64, a_major=0, b_major=0, lda=64, ldb=64, ldc=100,
                      dtype=mgb.MGB_BF16, c_f32=0, accumulate=0, alpha=1.0)
