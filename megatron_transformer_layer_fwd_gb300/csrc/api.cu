@@ -546,12 +546,13 @@ mgb_status mgb_block_bwd(const mgb_block_desc* desc, const mgb_block_weights* w,
     g.aux = u; g.ldaux = p.W; g.glu_block = desc->glu_block;
     if (fused_db1) g.colsum_part = at<float>(ws, p.w_fparts);
     MGB_TRY(gemm_launch(scr(g), st));
-    if (fused_db1)
-      MGB_TRY(colsum_reduce_launch(T > 0 ? p.fparts : 0, p.W, dt, at<float>(ws, p.w_fparts),
-                                   gr->b_1, st));
   }
-  // fc1: db1, dW1 = du^T f_in, d f_in = du W1
+  // fc1: db1 (from the partials of the epilogue above, or a column sum of du),
+  // dW1 = du^T f_in, d f_in = du W1
   MGB_TRY(lane.fork());
+  if (fused_db1)
+    MGB_TRY(colsum_reduce_launch(T > 0 ? p.fparts : 0, p.W, dt, at<float>(ws, p.w_fparts),
+                                 gr->b_1, s2));
   if (gr->b_1 && !fused_db1)
     MGB_TRY(colsum_launch(T, p.W, dt, du, p.W, gr->b_1, cparts, p.cparts, s2));
   if (gr->w_1)
