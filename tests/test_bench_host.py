@@ -50,3 +50,14 @@ def test_single_rank_is_identity(monkeypatch):
     w, r, l = bench.dist_setup()
     assert (w, r, l) == (1, 0, 0)
     assert bench.max_over_ranks(1, 3.5) == 3.5
+
+
+def test_traffic_records_match_the_gemm_source():
+    """The DRAM-traffic records the bench reports beside its roofline were
+    taken on the current GEMM source, for the library's default token block
+    (a change to the kernel, or to the default block, needs a new capture)."""
+    import bench
+    from megatron_transformer_layer_fwd_gb300 import mgb
+    src = os.path.join(bench.ROOT, "megatron_transformer_layer_fwd_gb300", "csrc", "gemm_tc.cu")
+    rec = bench.traffic_record(src, f"gemm_tc_ce_logits_tb{mgb.CE_DEFAULT_TOKEN_BLOCK}")
+    assert rec is not None and rec > 0
