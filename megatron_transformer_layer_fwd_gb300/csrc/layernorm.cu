@@ -4,19 +4,23 @@
 // section 2: F.layer_norm(x, (hidden,)) - per token, mean and biased variance
 // over the hidden features, eps 1e-5; optional affine gamma/beta.
 //
-// Forward: one block per row; each thread keeps up to 4 16-byte vectors of the
-// row in registers (one global read, one write), warp-shuffle + shared-memory
-// block reduction for the mean, then for the centred sum of squares (two-pass
-// in registers; no E[x^2]-E[x]^2 cancellation).
+// Forward: for bf16 rows of 256..4096 columns, rows streamed into a shared-
+// memory ring by bulk copies and normalised one warp per row (ln_fwd_tma);
+// otherwise one warp per row from registers, or one block per row (each
+// thread up to 4 16-byte vectors). Mean, then the centred sum of squares, both
+// from registers (two passes, no E[x^2]-E[x]^2 cancellation).
 // Backward (per row, xhat = (x - mean) * rstd, g = dy * gamma):
 //   dx = dres + rstd * (g - mean(g) - xhat * mean(g * xhat))
 // rows are strided over a fixed number of blocks; each thread accumulates the
 // dgamma = sum dy*xhat and dbeta = sum dy partials of its own columns in
-// registers, written per block and reduced by a second small kernel.
+// registers. Rows of up to 1024 vectors stream through per-thread
+// asynchronous copies (ln_bwd_async), and clusters of four CTAs combine their
+// partials in distributed shared memory; a second small kernel sums the
+// partial rows in a fixed order.
 // Column sums db[n] = sum_m dY[m, n] (bias gradients) use the same
 // partial-then-reduce scheme with coalesced 16-byte row reads. Many partial
-// rows (the backward's 1024) are folded in two stages: 16 splits of rows
-// folded in place, then the split results.
+// rows are folded in two stages: 16 splits of rows folded in place, then the
+// split results.
 #include <algorithm>
 #include <cstring>
 #include <mutex>
