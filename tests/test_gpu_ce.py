@@ -27,7 +27,9 @@ def _runner(shape, inp, mode, token_block=0, emb_stream=None):
 
 
 @pytest.mark.parametrize("T,H,V,C,tb", [(300, 256, 1000, 136, 256), (512, 1024, 8192, 1000, 256),
-                                        (1100, 128, 2048, 2048, 512), (130, 64, 520, 64, 256)])
+                                        (1100, 128, 2048, 2048, 512), (130, 64, 520, 64, 256),
+                                        # the library's default block (0): 4096 + a ragged 404
+                                        (4500, 128, 1024, 520, 0)])
 def test_ce_blocked_token_blocks(mgb_lib, T, H, V, C, tb):
     """The token-blocked CE with several blocks (a ragged last one): each
     block's losses from its own partials, d_hidden rows from the split-K
