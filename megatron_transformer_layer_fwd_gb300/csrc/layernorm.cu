@@ -23,7 +23,9 @@
 // split results.
 #include <algorithm>
 #include <cstring>
+#include <map>
 #include <mutex>
+#include <utility>
 
 #include "common.cuh"
 #include "internal.h"
@@ -1304,6 +1306,9 @@ int ln_bwd_async_cl(int clusters, int threads, size_t smem, int rows, int cols, 
   cfg.stream = st;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
+  if (cudaFuncSetAttribute(ln_bwd_async_kernel<T, P, CL>,
+                           cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) != cudaSuccess)
+    return -2;
   if (cudaLaunchKernelEx(&cfg, ln_bwd_async_kernel<T, P, CL>, rows, cols, (const T*)x, mean, rstd,
                          (const T*)gamma, (const T*)dy, (const T*)dres, (T*)dx, part) != cudaSuccess)
     return -2;
@@ -1338,6 +1343,37 @@ int ln_bwd_max_clusters(int threads, size_t smem) {
   return n;
 }
 
+// Launch shape of the asynchronous-copy backward for a block size: the plain
+// kernel's resident CTAs and the clusters of CL resident at once. Queried once
+// per CUDA context and block size, so that a call costs no occupancy queries
+// on the host. (The shared-memory size attribute is still set before every
+// launch: another block size may have lowered it since.)
+struct AsyncShape {
+  bool ok = false;
+  int resident = 0, clusters = 0;
+};
+template <typename T, int P, int CL>
+AsyncShape ln_bwd_async_shape(int threads, size_t smem) {
+  static std::mutex mu;
+  static std::map<std::pair<void*, int>, AsyncShape> cache;
+  const std::pair<void*, int> key(current_cuda_context(), threads);
+  std::lock_guard<std::mutex> lock(mu);
+  const auto it = cache.find(key);
+  if (it != cache.end() && key.first != nullptr) return it->second;
+  AsyncShape sh;
+  auto kern = ln_bwd_async_kernel<T, P, 1>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) ==
+      cudaSuccess) {
+    sh.ok = true;
+    sh.resident = resident_ctas(kern, threads, smem) * device_sm_count();
+    sh.clusters = ln_bwd_max_clusters<T, P, CL>(threads, smem);
+  } else {
+    cudaGetLastError();
+  }
+  if (key.first != nullptr) cache[key] = sh;
+  return sh;
+}
+
 template <typename T, int P>
 int ln_bwd_async_p(int nparts, int threads, int rows, int cols, const void* x, const float* mean,
                    const float* rstd, const void* gamma, const void* dy, const void* dres,
@@ -1345,13 +1381,12 @@ int ln_bwd_async_p(int nparts, int threads, int rows, int cols, const void* x, c
   constexpr int CL = 4;
   const size_t smem = (size_t)P * 3 * threads * 16;
   auto kern = ln_bwd_async_kernel<T, P, 1>;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
-      cudaSuccess)
-    return -2;
-  const int resident = resident_ctas(kern, threads, smem) * device_sm_count();
+  const AsyncShape sh = ln_bwd_async_shape<T, P, CL>(threads, smem);
+  if (!sh.ok) return -2;
+  const int resident = sh.resident;
   // the partials of a cluster fit in its CTAs' rings
   if (part && std::min(nparts, rows) >= 2 * CL && 2 * (size_t)cols * 4 <= smem) {
-    const int mc = ln_bwd_max_clusters<T, P, CL>(threads, smem);
+    const int mc = sh.clusters;
     if (mc > 0 && (int64_t)mc * CL * 100 >= (int64_t)resident * 94) {
       // one partial row per cluster: at most nparts of them
       const int clusters = std::min(mc, std::min(nparts, (rows + CL - 1) / CL));
@@ -1360,6 +1395,9 @@ int ln_bwd_async_p(int nparts, int threads, int rows, int cols, const void* x, c
     }
   }
   const int grid = std::max(1, std::min(nparts, resident));
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+      cudaSuccess)
+    return -2;
   kern<<<grid, threads, smem, st>>>(rows, cols, (const T*)x, mean, rstd, (const T*)gamma,
                                     (const T*)dy, (const T*)dres, (T*)dx, part);
   return grid;
