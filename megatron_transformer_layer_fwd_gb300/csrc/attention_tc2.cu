@@ -123,6 +123,20 @@ __device__ __forceinline__ Item item_of(int i, const Params& p) {
   return it;
 }
 
+// The item a CTA takes in its k-th round. Round k covers items k G .. k G +
+// G - 1 (G CTAs); CTA c takes item k G + c in even rounds and k G + G - 1 - c
+// in odd ones. With the items ordered from the longest causal rows down, a
+// CTA that took a longer item in one round takes a shorter one in the next,
+// so the CTAs' totals come out nearly equal (plain strides hand the first
+// CTAs the longest item of every round: on 16 query blocks of a 4096-long
+// causal sequence the busiest CTA then has 14 % more key tiles than the
+// mean, against 1 % this way). Once k G + c passes the item count, every
+// later round does too.
+__device__ __forceinline__ int item_index(int k) {
+  const int g = (int)gridDim.x, c = (int)blockIdx.x;
+  return k * g + ((k & 1) ? g - 1 - c : c);
+}
+
 template <int D, bool DROP>
 __global__ void __launch_bounds__(NTHREADS, 1)
     attn_fwd2_kernel(const __grid_constant__ CUtensorMap tmQ,
@@ -150,7 +164,6 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   volatile int* abort = reinterpret_cast<volatile int*>(smem + C::OFF_BAR + 244);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int stride = gridDim.x;
 
   if (tid == 0) {
     tma_prefetch_desc(&tmQ);
@@ -181,7 +194,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     // ---------------- producer: per item Q_A, Q_B, then K_0, V_0, K_1, V_1, ...
     if (lane == 0) {
       int nk = 0, nv = 0;  // K / V tiles loaded so far (ring positions)
-      for (int k = 0, i = blockIdx.x; i < p.n_items && !*abort; ++k, i += stride) {
+      for (int k = 0, i = item_index(0); i < p.n_items && !*abort; ++k, i = item_index(k)) {
         const Item w = item_of(i, p);
         const int grow0 = w.b * p.S;
         const int xcol = (w.h / (p.nq / p.nkv)) * D;
@@ -281,7 +294,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       __syncwarp();
       ++np[x];
     };
-    for (int k = 0, i = blockIdx.x; i < p.n_items && good; ++k, i += stride) {
+    for (int k = 0, i = item_index(0); i < p.n_items && good; ++k, i = item_index(k)) {
       const Item w = item_of(i, p);
       const int nt = max(w.n[0], w.n[1]);
       if (warp_aborted(abort) || !warp_wait(q_full, k & 1, p.err)) {
@@ -367,7 +380,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
     bool good = true;
     int n = 0;   // S_X products consumed so far
     int ko = 0;  // items with a non-empty tile X so far
-    for (int i = blockIdx.x; i < p.n_items && good; i += stride) {
+    for (int k = 0, i = item_index(0); i < p.n_items && good; ++k, i = item_index(k)) {
       const Item w = item_of(i, p);
       if (w.n[x] == 0) continue;  // tile past the sequence end: nothing to do
       const int row = w.q0 + x * TQ + r;
