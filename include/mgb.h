@@ -448,6 +448,40 @@ mgb_status mgb_embedding_bwd(int32_t tokens, int32_t hidden, int32_t v0, int32_t
                              const int32_t* ids, const void* d_out, void* d_emb_shard,
                              int32_t accumulate, void* ws, size_t ws_bytes, void* stream);
 
+/* The backward above in two steps, so that the part that depends on the ids
+ * alone can run early (e.g. beside the forward, once the ids are known) and
+ * the part that needs d_out is the row sums only [P2 section 3, as
+ * mgb_embedding_bwd].
+ *
+ * mgb_embedding_bwd_prepare writes into `ws` (16-byte aligned, caller-owned, at
+ * least mgb_embedding_bwd_ws_bytes(tokens, v0, v1)) the token order of the
+ * shard's rows: each token's stable rank among the tokens with the same id,
+ * the per-row counts scanned into row offsets, and the tokens placed row by
+ * row in token order. It fills *plan (host memory) with tokens, v0, v1, ws and
+ * ws_bytes; nothing is read back from the device. The ids are not read again.
+ *
+ * mgb_embedding_bwd_apply runs the row sums of mgb_embedding_bwd from a plan:
+ * d_emb_shard[v - v0] = (accumulate ? d_emb_shard[v - v0] : 0) + the sum over
+ * the plan's tokens t with ids[t] = v of d_out[t], in token order, in float32
+ * (bit for bit the result of mgb_embedding_bwd with the same ids). A plan
+ * serves any number of applies, in either mode, as long as its workspace is
+ * left unchanged and each apply is ordered after the prepare (same stream, or
+ * an event between the streams).
+ * Errors: as mgb_embedding_bwd (a NULL plan or plan->ws is MGB_ERR_INVALID_ARG),
+ * all before any launch. */
+typedef struct {
+  int32_t tokens, v0, v1;
+  void* ws;
+  size_t ws_bytes;
+} mgb_embedding_bwd_plan;
+
+mgb_status mgb_embedding_bwd_prepare(int32_t tokens, int32_t v0, int32_t v1, const int32_t* ids,
+                                     void* ws, size_t ws_bytes, mgb_embedding_bwd_plan* plan,
+                                     void* stream);
+mgb_status mgb_embedding_bwd_apply(const mgb_embedding_bwd_plan* plan, int32_t hidden,
+                                   int32_t dtype, const void* d_out, void* d_emb_shard,
+                                   int32_t accumulate, void* stream);
+
 /* Bytes of the workspace mgb_attention_bwd needs: two float32 planes
  * [batch * n_q_heads][seq rounded up to a multiple of 128] (LSE * log2(e) and
  * delta = rowsum(dO * O), per query; the padding holds +inf and 0), then the

@@ -1104,6 +1104,40 @@ mgb_status mgb_embedding_bwd(int32_t tokens, int32_t hidden, int32_t v0, int32_t
                               accumulate ? 1 : 0, ws, as_stream(stream));
 }
 
+mgb_status mgb_embedding_bwd_prepare(int32_t tokens, int32_t v0, int32_t v1, const int32_t* ids,
+                                     void* ws, size_t ws_bytes, mgb_embedding_bwd_plan* plan,
+                                     void* stream) {
+  if (fault_injected()) return MGB_ERR_INVALID_ARG;
+  if (tokens < 0 || v0 < 0 || v1 <= v0 || !plan || !ws || (tokens > 0 && !ids))
+    return MGB_ERR_INVALID_ARG;
+  if (!aligned16(ws) || (reinterpret_cast<uintptr_t>(ids) & 3u)) return MGB_ERR_MISALIGNED;
+  if (ws_bytes < embedding_bwd_ws(tokens, v0, v1)) return MGB_ERR_WORKSPACE_TOO_SMALL;
+  MGB_TRY(check_arch());
+  MGB_TRY(embedding_bwd_prepare_launch(tokens, v0, v1, ids, ws, as_stream(stream)));
+  plan->tokens = tokens;
+  plan->v0 = v0;
+  plan->v1 = v1;
+  plan->ws = ws;
+  plan->ws_bytes = ws_bytes;
+  return MGB_OK;
+}
+
+mgb_status mgb_embedding_bwd_apply(const mgb_embedding_bwd_plan* plan, int32_t hidden,
+                                   int32_t dtype, const void* d_out, void* d_emb_shard,
+                                   int32_t accumulate, void* stream) {
+  if (!plan) return MGB_ERR_INVALID_ARG;
+  // the plan's ids only decided the workspace's contents; d_out stands in for them
+  MGB_TRY(check_embedding(plan->tokens, hidden, plan->v0, plan->v1, dtype, d_out, d_emb_shard,
+                          d_out));
+  if (!plan->ws) return MGB_ERR_INVALID_ARG;
+  if (!aligned16(plan->ws)) return MGB_ERR_MISALIGNED;
+  if (plan->ws_bytes < embedding_bwd_ws(plan->tokens, plan->v0, plan->v1))
+    return MGB_ERR_WORKSPACE_TOO_SMALL;
+  MGB_TRY(check_arch());
+  return embedding_bwd_apply_launch(plan->tokens, hidden, dtype, plan->v0, plan->v1, d_out,
+                                    d_emb_shard, accumulate ? 1 : 0, plan->ws, as_stream(stream));
+}
+
 size_t mgb_attention_bwd_ws_bytes(int32_t batch, int32_t seq, int32_t n_q_heads) {
   if (batch < 0 || seq < 0 || n_q_heads < 0) return 0;
   return attn_bwd_ws_bytes(batch, seq, n_q_heads);

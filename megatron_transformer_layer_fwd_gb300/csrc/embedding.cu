@@ -271,8 +271,8 @@ __device__ __forceinline__ void emb_row_sum(int H, int a, int b, const int32_t* 
   }
 }
 
-// Accumulate mode, one block per position of the token order (*npos
-// positions): the block at the head of a row's segment adds
+// Accumulate mode, one block per position of the token order (T blocks, *npos
+// positions used): the block at the head of a row's segment adds
 // the row's tokens in token order onto the row, the others return. Two
 // vectors per thread per step, with the row's and the first token's vectors
 // requested together.
@@ -284,10 +284,12 @@ __global__ void emb_accum_heads_kernel(int H, const int32_t* __restrict__ npos,
                                        const T* __restrict__ dout, T* __restrict__ d_emb) {
   constexpr int VN = EVec<T>::N;
   const int p = blockIdx.x;
-  if (p >= *npos) return;
-  const int row = seg_row[p];
-  if (row < 0) return;
-  const int end = seg_end[p], t0 = order[p];
+  // the position's entries are requested together with the position count
+  // (one round trip instead of three; p < T, so every read is in bounds, and
+  // the values past *npos are not used)
+  const int n = *npos;
+  const int row = seg_row[p], end = seg_end[p], t0 = order[p];
+  if (p >= n || row < 0) return;
   const int nvec = H / VN;
   T* dst = d_emb + (int64_t)row * H;
   const T* g0 = dout + (int64_t)t0 * H;
@@ -355,70 +357,119 @@ mgb_status embedding_fwd_launch(int T, int H, int dtype, int v0, int v1, const i
   return cudaGetLastError() == cudaSuccess ? MGB_OK : MGB_ERR_CUDA;
 }
 
-mgb_status embedding_bwd_launch(int T, int H, int dtype, int v0, int v1, const int32_t* ids,
-                                const void* dout, void* d_emb, int accumulate, void* ws,
-                                cudaStream_t st) {
+namespace {
+
+// The workspace's arrays (layout of embedding_bwd_ws).
+struct EmbWs {
+  int32_t *counts, *rank, *order, *seg_row, *seg_end, *offsets, *totals, *npos;
+  EmbWs(void* ws, int T, int rows) {
+    const int nchunks = (rows + SCAN_CHUNK - 1) / SCAN_CHUNK;
+    // counts and rank side by side (one zeroing); counts first, so 16-byte aligned
+    counts = static_cast<int32_t*>(ws);
+    rank = counts + (rows + 3) / 4 * 4;
+    order = rank + T;
+    seg_row = order + T;
+    seg_end = seg_row + T;
+    offsets = seg_end + T;
+    totals = offsets + rows + 1;
+    npos = totals + nchunks + 1;
+  }
+};
+
+// The token order: ranks, the scan of the per-row counts and the placement.
+// chunked (accumulate mode only, at most 1024 scan chunks): the placement
+// finishes the scan itself and writes *npos, and the row offsets stay
+// chunk-local; otherwise the full scan, offsets[rows] = the in-shard tokens.
+mgb_status emb_plan(int T, int v0, int v1, const int32_t* ids, bool chunked, const EmbWs& w,
+                    cudaStream_t st) {
   const int rows = v1 - v0;
   const int nchunks = (rows + SCAN_CHUNK - 1) / SCAN_CHUNK;
-  // counts and rank side by side (one zeroing); counts first, so 16-byte aligned
-  int32_t* counts = static_cast<int32_t*>(ws);
-  int32_t* rank = counts + (rows + 3) / 4 * 4;
-  int32_t* order = rank + T;
-  int32_t* seg_row = order + T;
-  int32_t* seg_end = seg_row + T;
-  int32_t* offsets = seg_end + T;
-  int32_t* totals = offsets + rows + 1;
-  int32_t* npos = totals + nchunks + 1;
-  const int vn = dtype == MGB_BF16 ? 8 : 4;
-  const int nvec = H / vn;
-  if (accumulate && T == 0) return MGB_OK;  // nothing to add
-  // accumulate: rank, chunk scan, placement (finishing the scan), sums;
-  // overwrite: rank, the three scan steps, placement, every row written
-  const bool chunked = accumulate && nchunks <= 1024;
-  LaunchScope scope(PROF_EMBEDDING, st, chunked ? 4 : 3 + (T > 0 ? 3 : 1));
-  if (cudaMemsetAsync(counts, 0, sizeof(int32_t) * ((rows + 3) / 4 * 4 + (size_t)T), st) !=
+  if (cudaMemsetAsync(w.counts, 0, sizeof(int32_t) * ((rows + 3) / 4 * 4 + (size_t)T), st) !=
       cudaSuccess)
     return MGB_ERR_CUDA;
   if (T > 0) {
     const dim3 grid((T + RANK_I - 1) / RANK_I, (T + RANK_J - 1) / RANK_J);
-    emb_rank_kernel<<<grid, RANK_I, 0, st>>>(T, v0, v1, ids, rank, counts);
+    emb_rank_kernel<<<grid, RANK_I, 0, st>>>(T, v0, v1, ids, w.rank, w.counts);
   }
-  emb_scan_chunks<<<nchunks, SCAN_THREADS, 0, st>>>(rows, counts, offsets, totals);
+  emb_scan_chunks<<<nchunks, SCAN_THREADS, 0, st>>>(rows, w.counts, w.offsets, w.totals);
   if (chunked) {
     emb_place_chunked_kernel<<<(T + 255) / 256, 256, 0, st>>>(
-        T, v0, v1, ids, rank, counts, offsets, totals, nchunks, order, seg_row, seg_end, npos);
+        T, v0, v1, ids, w.rank, w.counts, w.offsets, w.totals, nchunks, w.order, w.seg_row,
+        w.seg_end, w.npos);
   } else {
-    emb_scan_totals<<<1, SCAN_THREADS, 0, st>>>(nchunks, totals);
-    emb_scan_add<<<(rows + 255) / 256, 256, 0, st>>>(rows, totals, nchunks, offsets);
+    emb_scan_totals<<<1, SCAN_THREADS, 0, st>>>(nchunks, w.totals);
+    emb_scan_add<<<(rows + 255) / 256, 256, 0, st>>>(rows, w.totals, nchunks, w.offsets);
     if (T > 0)
-      emb_place_kernel<<<(T + 255) / 256, 256, 0, st>>>(T, v0, v1, ids, rank, offsets, order,
-                                                        seg_row, seg_end);
+      emb_place_kernel<<<(T + 255) / 256, 256, 0, st>>>(T, v0, v1, ids, w.rank, w.offsets,
+                                                        w.order, w.seg_row, w.seg_end);
   }
+  return cudaGetLastError() == cudaSuccess ? MGB_OK : MGB_ERR_CUDA;
+}
+
+// The row sums from a token order made by emb_plan (chunked as there).
+mgb_status emb_apply(int T, int H, int dtype, int rows, const void* dout, void* d_emb,
+                     bool accumulate, bool chunked, const EmbWs& w, cudaStream_t st) {
+  const int vn = dtype == MGB_BF16 ? 8 : 4;
+  const int nvec = H / vn;
   if (accumulate) {
+    if (T == 0) return MGB_OK;  // nothing to add
     // one block per position; two vectors per thread per step
     const int athreads = std::min(256, ((nvec + 1) / 2 + 31) / 32 * 32);
-    const int32_t* np = chunked ? npos : offsets + rows;
+    const int32_t* np = chunked ? w.npos : w.offsets + rows;
     if (dtype == MGB_BF16)
-      emb_accum_heads_kernel<bf16><<<T, athreads, 0, st>>>(H, np, order, seg_row, seg_end,
+      emb_accum_heads_kernel<bf16><<<T, athreads, 0, st>>>(H, np, w.order, w.seg_row, w.seg_end,
                                                            static_cast<const bf16*>(dout),
                                                            static_cast<bf16*>(d_emb));
     else
-      emb_accum_heads_kernel<float><<<T, athreads, 0, st>>>(H, np, order, seg_row, seg_end,
+      emb_accum_heads_kernel<float><<<T, athreads, 0, st>>>(H, np, w.order, w.seg_row, w.seg_end,
                                                             static_cast<const float*>(dout),
                                                             static_cast<float*>(d_emb));
   } else {
     const int threads = nvec >= 256 ? 256 : ((nvec + 31) / 32) * 32;
     const int grid = rows < device_sm_count() * 32 ? rows : device_sm_count() * 32;
     if (dtype == MGB_BF16)
-      emb_write_rows_kernel<bf16><<<grid, threads, 0, st>>>(rows, H, offsets, order,
+      emb_write_rows_kernel<bf16><<<grid, threads, 0, st>>>(rows, H, w.offsets, w.order,
                                                             static_cast<const bf16*>(dout),
                                                             static_cast<bf16*>(d_emb));
     else
-      emb_write_rows_kernel<float><<<grid, threads, 0, st>>>(rows, H, offsets, order,
+      emb_write_rows_kernel<float><<<grid, threads, 0, st>>>(rows, H, w.offsets, w.order,
                                                              static_cast<const float*>(dout),
                                                              static_cast<float*>(d_emb));
   }
   return cudaGetLastError() == cudaSuccess ? MGB_OK : MGB_ERR_CUDA;
+}
+
+}  // namespace
+
+mgb_status embedding_bwd_launch(int T, int H, int dtype, int v0, int v1, const int32_t* ids,
+                                const void* dout, void* d_emb, int accumulate, void* ws,
+                                cudaStream_t st) {
+  const int rows = v1 - v0;
+  const int nchunks = (rows + SCAN_CHUNK - 1) / SCAN_CHUNK;
+  if (accumulate && T == 0) return MGB_OK;  // nothing to add
+  // accumulate: rank, chunk scan, placement (finishing the scan), sums;
+  // overwrite: rank, the three scan steps, placement, every row written
+  const bool chunked = accumulate && nchunks <= 1024;
+  LaunchScope scope(PROF_EMBEDDING, st, chunked ? 4 : 3 + (T > 0 ? 3 : 1));
+  const EmbWs w(ws, T, rows);
+  const mgb_status planned = emb_plan(T, v0, v1, ids, chunked, w, st);
+  if (planned != MGB_OK) return planned;
+  return emb_apply(T, H, dtype, rows, dout, d_emb, accumulate != 0, chunked, w, st);
+}
+
+mgb_status embedding_bwd_prepare_launch(int T, int v0, int v1, const int32_t* ids, void* ws,
+                                        cudaStream_t st) {
+  LaunchScope scope(PROF_EMBEDDING, st, 3 + (T > 0 ? 2 : 0));
+  return emb_plan(T, v0, v1, ids, false, EmbWs(ws, T, v1 - v0), st);
+}
+
+mgb_status embedding_bwd_apply_launch(int T, int H, int dtype, int v0, int v1, const void* dout,
+                                      void* d_emb, int accumulate, const void* ws,
+                                      cudaStream_t st) {
+  if (accumulate && T == 0) return MGB_OK;
+  LaunchScope scope(PROF_EMBEDDING, st, 1);
+  return emb_apply(T, H, dtype, v1 - v0, dout, d_emb, accumulate != 0, false,
+                   EmbWs(const_cast<void*>(ws), T, v1 - v0), st);
 }
 
 }  // namespace mgb

@@ -278,6 +278,13 @@ mgb_status philox_bytes_launch(uint64_t seed, uint64_t offset, uint64_t n, void*
 
 // Vocab-parallel embedding (shard rows [v0, v1)); layouts as mgb_embedding_fwd/bwd.
 size_t embedding_bwd_ws(int T, int v0, int v1);
+// The backward in two steps: the token order from the ids alone (the full row
+// offsets, usable by both apply modes), then the row sums.
+mgb_status embedding_bwd_prepare_launch(int T, int v0, int v1, const int32_t* ids, void* ws,
+                                        cudaStream_t st);
+mgb_status embedding_bwd_apply_launch(int T, int H, int dtype, int v0, int v1, const void* dout,
+                                      void* d_emb, int accumulate, const void* ws,
+                                      cudaStream_t st);
 mgb_status embedding_fwd_launch(int T, int H, int dtype, int v0, int v1, const int32_t* ids,
                                 const void* emb, void* out, cudaStream_t st);
 mgb_status embedding_bwd_launch(int T, int H, int dtype, int v0, int v1, const int32_t* ids,

@@ -84,6 +84,11 @@ class CEDesc(ctypes.Structure):
                 ("token_block", ctypes.c_int32)]
 
 
+class EmbeddingBwdPlan(ctypes.Structure):
+    _fields_ = [("tokens", ctypes.c_int32), ("v0", ctypes.c_int32), ("v1", ctypes.c_int32),
+                ("ws", ctypes.c_void_p), ("ws_bytes", ctypes.c_size_t)]
+
+
 class GemmDesc(ctypes.Structure):
     _fields_ = [("m", ctypes.c_int32), ("n", ctypes.c_int32), ("k", ctypes.c_int32),
                 ("a_major", ctypes.c_int32), ("b_major", ctypes.c_int32),
@@ -138,6 +143,9 @@ def load() -> ctypes.CDLL:
             "mgb_dropout": [ctypes.c_int64, ctypes.c_int64, I32, F32, RngState, P, ctypes.c_int64, P,
                             ctypes.c_int64, P],
             "mgb_embedding_bwd": [I32, I32, I32, I32, I32, P, P, P, I32, P, SZ, P],
+            "mgb_embedding_bwd_prepare": [I32, I32, I32, P, P, SZ,
+                                          ctypes.POINTER(EmbeddingBwdPlan), P],
+            "mgb_embedding_bwd_apply": [ctypes.POINTER(EmbeddingBwdPlan), I32, I32, P, P, I32, P],
             "mgb_device_status": [P],
             "mgb_selftest_wait_timeout": [U64, P],
         }
@@ -357,6 +365,24 @@ def mgb_embedding_bwd(tokens, hidden, v0, v1, dtype, ids, d_out, d_emb_shard, ac
                                     _ptr(d_emb_shard), int(accumulate), _ptr(ws),
                                     ws.numel() * ws.element_size(), _stream(stream)),
            "mgb_embedding_bwd")
+
+
+def mgb_embedding_bwd_prepare(tokens, v0, v1, ids, ws, stream=None) -> "EmbeddingBwdPlan":
+    """The token order of the backward from the ids alone; returns the plan
+    (host struct) that mgb_embedding_bwd_apply takes. `ws` must outlive it."""
+    plan = EmbeddingBwdPlan()
+    _check(load().mgb_embedding_bwd_prepare(tokens, v0, v1, _ptr(ids), _ptr(ws),
+                                            ws.numel() * ws.element_size(), ctypes.byref(plan),
+                                            _stream(stream)),
+           "mgb_embedding_bwd_prepare")
+    return plan
+
+
+def mgb_embedding_bwd_apply(plan, hidden, dtype, d_out, d_emb_shard, accumulate,
+                            stream=None) -> None:
+    _check(load().mgb_embedding_bwd_apply(ctypes.byref(plan), hidden, dtype, _ptr(d_out),
+                                          _ptr(d_emb_shard), int(accumulate), _stream(stream)),
+           "mgb_embedding_bwd_apply")
 
 
 def mgb_layernorm_bwd(rows: int, cols: int, dtype: int, x, mean, rstd, gamma, dy, dres, dx, dgamma,

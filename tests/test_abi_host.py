@@ -312,6 +312,42 @@ def test_embedding_validation(lib):
                                  None) == mgb.MGB_ERR_WORKSPACE_TOO_SMALL
 
 
+def test_embedding_prepare_apply_validation(lib):
+    """The two-step backward refuses bad arguments before any launch; the plan
+    is a host struct that carries the sizes from prepare to apply."""
+    import ctypes as ct
+    p = 4096
+    need = mgb.mgb_embedding_bwd_ws_bytes(100, 10, 60)
+    plan = mgb.EmbeddingBwdPlan()
+    assert ct.sizeof(plan) == 32
+    prep = lib.mgb_embedding_bwd_prepare
+    assert prep(100, 10, 10, p, p, need, ct.byref(plan), None) == mgb.MGB_ERR_INVALID_ARG
+    assert prep(-1, 10, 60, p, p, need, ct.byref(plan), None) == mgb.MGB_ERR_INVALID_ARG
+    assert prep(100, 10, 60, p, p, need, None, None) == mgb.MGB_ERR_INVALID_ARG
+    assert prep(100, 10, 60, None, p, need, ct.byref(plan), None) == mgb.MGB_ERR_INVALID_ARG
+    assert prep(100, 10, 60, p, None, need, ct.byref(plan), None) == mgb.MGB_ERR_INVALID_ARG
+    assert prep(100, 10, 60, p, p + 8, need, ct.byref(plan), None) == mgb.MGB_ERR_MISALIGNED
+    assert prep(100, 10, 60, p + 2, p, need, ct.byref(plan), None) == mgb.MGB_ERR_MISALIGNED
+    assert prep(100, 10, 60, p, p, need - 16, ct.byref(plan), None) == \
+        mgb.MGB_ERR_WORKSPACE_TOO_SMALL
+    # nothing was filled in by the refused calls
+    assert (plan.tokens, plan.v0, plan.v1, plan.ws, plan.ws_bytes) == (0, 0, 0, None, 0)
+    apply = lib.mgb_embedding_bwd_apply
+    assert apply(None, 64, mgb.MGB_BF16, p, p, 1, None) == mgb.MGB_ERR_INVALID_ARG
+    plan.tokens, plan.v0, plan.v1, plan.ws, plan.ws_bytes = 100, 10, 60, p, need
+    assert apply(ct.byref(plan), 60, mgb.MGB_BF16, p, p, 1, None) == mgb.MGB_ERR_MISALIGNED
+    assert apply(ct.byref(plan), 64, 7, p, p, 1, None) == mgb.MGB_ERR_INVALID_ARG
+    assert apply(ct.byref(plan), 64, mgb.MGB_BF16, None, p, 1, None) == mgb.MGB_ERR_INVALID_ARG
+    assert apply(ct.byref(plan), 64, mgb.MGB_BF16, p, p + 8, 1, None) == mgb.MGB_ERR_MISALIGNED
+    plan.ws_bytes = need - 16
+    assert apply(ct.byref(plan), 64, mgb.MGB_BF16, p, p, 1, None) == \
+        mgb.MGB_ERR_WORKSPACE_TOO_SMALL
+    plan.ws_bytes, plan.ws = need, None
+    assert apply(ct.byref(plan), 64, mgb.MGB_BF16, p, p, 1, None) == mgb.MGB_ERR_INVALID_ARG
+    plan.ws = p + 8
+    assert apply(ct.byref(plan), 64, mgb.MGB_BF16, p, p, 1, None) == mgb.MGB_ERR_MISALIGNED
+
+
 def test_checking_build_exports_the_same_calls():
     """The checking build (device-side checks, -DMGB_CHECK=1) compiles and
     exports every call of the header, like the normal build."""

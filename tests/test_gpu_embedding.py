@@ -106,6 +106,76 @@ def test_backward_token_order_f32(mgb_lib, accumulate):
     assert np.array_equal(got.astype(np.float32), want)
 
 
+def test_prepare_apply_token_order_f32(mgb_lib):
+    """The two-step backward: one prepare from the ids, then applies in both
+    modes with different d_out, all bit-exact (float32) against adding each
+    token's row in token order. The ids are overwritten after the prepare (the
+    plan holds everything the applies need), and the applies run on another
+    stream, ordered after the prepare by an event."""
+    T, H, V, v0, v1 = 3000, 64, 400, 37, 381
+    ids = _ids(T, V, repeats=True)
+    ids_d = torch.from_numpy(ids).cuda()
+    ws = torch.empty(mgb.mgb_embedding_bwd_ws_bytes(T, v0, v1), dtype=torch.uint8, device="cuda")
+    s1, s2 = torch.cuda.Stream(), torch.cuda.Stream()
+    with torch.cuda.stream(s1):
+        plan = mgb.mgb_embedding_bwd_prepare(T, v0, v1, ids_d, ws, stream=s1)
+        ids_d.fill_(v0)  # not read again
+    ev = torch.cuda.Event()
+    ev.record(s1)
+    s2.wait_event(ev)
+    assert (plan.tokens, plan.v0, plan.v1, plan.ws_bytes) == (T, v0, v1, ws.numel())
+    own = (ids >= v0) & (ids < v1)
+    d1 = RNG.standard_normal((T, H)).astype(np.float32)
+    d2 = RNG.standard_normal((T, H)).astype(np.float32)
+    want = np.zeros((v1 - v0, H), dtype=np.float32)
+    np.add.at(want, ids[own] - v0, d1[own])
+    with torch.cuda.stream(s2):
+        d_emb = torch.full((v1 - v0, H), float("nan"), device="cuda", dtype=torch.float32)
+        mgb.mgb_embedding_bwd_apply(plan, H, mgb.MGB_F32, _dev(d1, torch.float32), d_emb, 0,
+                                    stream=s2)
+    torch.cuda.synchronize()
+    assert np.array_equal(to_np(d_emb).astype(np.float32), want)
+    np.add.at(want, ids[own] - v0, d2[own])
+    with torch.cuda.stream(s2):
+        mgb.mgb_embedding_bwd_apply(plan, H, mgb.MGB_F32, _dev(d2, torch.float32), d_emb, 1,
+                                    stream=s2)
+    torch.cuda.synchronize()
+    assert np.array_equal(to_np(d_emb).astype(np.float32), want)
+    assert mgb.mgb_device_status() == mgb.MGB_OK
+
+
+@pytest.mark.parametrize("accumulate", [False, True])
+@pytest.mark.parametrize("T,V,v0,v1,rep", [(2048, 300, 0, 300, True), (700, 1000, 250, 613, True),
+                                           (5000, 3000, 0, 3000, False)])
+def test_prepare_apply_equals_one_call_bf16(mgb_lib, accumulate, T, V, v0, v1, rep):
+    """bf16: the two steps give the one-call backward's result bit for bit."""
+    H = 128
+    ids = _ids(T, V, repeats=rep)
+    dout = round_to_bf16(RNG.standard_normal((T, H)))
+    init = round_to_bf16(RNG.standard_normal((v1 - v0, H))) if accumulate else None
+    one = _bwd(ids, dout, v0, v1, torch.bfloat16, mgb.MGB_BF16, init=init)
+    ws = torch.empty(mgb.mgb_embedding_bwd_ws_bytes(T, v0, v1), dtype=torch.uint8, device="cuda")
+    plan = mgb.mgb_embedding_bwd_prepare(T, v0, v1, torch.from_numpy(ids).cuda(), ws)
+    two = (_dev(init, torch.bfloat16) if accumulate else
+           torch.full((v1 - v0, H), float("nan"), device="cuda", dtype=torch.bfloat16))
+    mgb.mgb_embedding_bwd_apply(plan, H, mgb.MGB_BF16, _dev(dout, torch.bfloat16), two, accumulate)
+    assert torch.equal(one, two)
+    ref = oracle.embedding_bwd(ids, dout, v0, v1) + (init if accumulate else 0.0)
+    assert rel_l2(to_np(two), ref) <= 1e-2
+    assert mgb.mgb_device_status() == mgb.MGB_OK
+
+
+def test_prepare_apply_empty_batch(mgb_lib):
+    ws = torch.empty(mgb.mgb_embedding_bwd_ws_bytes(0, 0, 10), dtype=torch.uint8, device="cuda")
+    plan = mgb.mgb_embedding_bwd_prepare(0, 0, 10, None, ws)
+    d = torch.full((10, 16), 3.0, device="cuda", dtype=torch.bfloat16)
+    mgb.mgb_embedding_bwd_apply(plan, 16, mgb.MGB_BF16, None, d, 1)  # nothing to add
+    assert float(d.float().min()) == 3.0 and float(d.float().max()) == 3.0
+    mgb.mgb_embedding_bwd_apply(plan, 16, mgb.MGB_BF16, None, d, 0)  # rows written as zeros
+    assert float(d.float().abs().max()) == 0.0
+    assert mgb.mgb_device_status() == mgb.MGB_OK
+
+
 def test_empty_batch(mgb_lib):
     ids = np.zeros(0, dtype=np.int32)
     d = _bwd(ids, np.zeros((0, 16)), 0, 10, torch.bfloat16, mgb.MGB_BF16)
