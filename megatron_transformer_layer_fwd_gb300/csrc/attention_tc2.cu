@@ -157,9 +157,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   const uint32_t v_full0 = bar + 48;   // [2] V stage loaded                    (tx)
   const uint32_t v_empty0 = bar + 64;  // [2] PV products with it done          (commit)
   const uint32_t s_full0 = bar + 80;   // [tile] S_X(j) complete                (commit)
-  const uint32_t p_full0 = bar + 96;   // [tile] P_X(j) written, O_X rescaled   (128 arrivals)
+  const uint32_t p_full0 = bar + 96;   // [tile] P_X(j) written, O_X rescaled   (4: one per warp)
   const uint32_t o_full0 = bar + 112;  // [tile] the item's last PV_X done      (commit)
-  const uint32_t o_empty0 = bar + 128; // [tile] O_X read out                   (128 arrivals)
+  const uint32_t o_empty0 = bar + 128; // [tile] O_X read out                   (4: one per warp)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_BAR + 240);
   volatile int* abort = reinterpret_cast<volatile int*>(smem + C::OFF_BAR + 244);
 
@@ -177,9 +177,9 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       mbar_init(v_full0 + 8 * i, 1);
       mbar_init(v_empty0 + 8 * i, 1);
       mbar_init(s_full0 + 8 * i, 1);
-      mbar_init(p_full0 + 8 * i, NSOFT);
+      mbar_init(p_full0 + 8 * i, NSOFT / 32);
       mbar_init(o_full0 + 8 * i, 1);
-      mbar_init(o_empty0 + 8 * i, NSOFT);
+      mbar_init(o_empty0 + 8 * i, NSOFT / 32);
     }
     fence_mbar_init();
     *abort = 0;
@@ -559,7 +559,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         }
         tmem_st_wait();
         tc_fence_before();
-        mbar_arrive(pfull);
+        __syncwarp();  // the warp's P stores are done: one arrival for the warp
+        if (lane == 0) mbar_arrive(pfull);
       }
       if (!good) break;
       // ---- tile done: O / l and LSE
@@ -574,7 +575,8 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       bf16* out = p.o + (int64_t)(w.b * p.S + row) * p.ld_o + w.h * D;
       store_tmem_row<D>(t_o, inv, row_ok ? out : nullptr);
       tc_fence_before();
-      mbar_arrive(oempty);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(oempty);
       if (row_ok) p.lse[((int64_t)w.b * p.nq + w.h) * p.S + row] = (m_ref + log2f(l)) * LN2;
     }
     if (!good) *abort = 1;
