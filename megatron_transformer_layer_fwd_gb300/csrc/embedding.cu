@@ -271,17 +271,57 @@ __device__ __forceinline__ void emb_row_sum(int H, int a, int b, const int32_t* 
   }
 }
 
+// 16 bytes of a row as raw bits (converted to float32 where they are added).
+template <typename T>
+__device__ __forceinline__ uint4 eraw(const T* p) {
+  return *reinterpret_cast<const uint4*>(p);
+}
+// f[j] = x[j] + y[j] from two raw vectors.
+template <typename T>
+__device__ __forceinline__ void eadd_raw(const uint4& x, const uint4& y, float* f) {
+  if constexpr (sizeof(T) == 2) {
+    const uint32_t wx[4] = {x.x, x.y, x.z, x.w}, wy[4] = {y.x, y.y, y.z, y.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 a = unpack_bf16x2(wx[i]), b = unpack_bf16x2(wy[i]);
+      f[2 * i] = a.x + b.x;
+      f[2 * i + 1] = a.y + b.y;
+    }
+  } else {
+    f[0] = __uint_as_float(x.x) + __uint_as_float(y.x);
+    f[1] = __uint_as_float(x.y) + __uint_as_float(y.y);
+    f[2] = __uint_as_float(x.z) + __uint_as_float(y.z);
+    f[3] = __uint_as_float(x.w) + __uint_as_float(y.w);
+  }
+}
+// f[j] += y[j] from a raw vector.
+template <typename T>
+__device__ __forceinline__ void eacc_raw(const uint4& y, float* f) {
+  if constexpr (sizeof(T) == 2) {
+    const uint32_t wy[4] = {y.x, y.y, y.z, y.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 b = unpack_bf16x2(wy[i]);
+      f[2 * i] += b.x;
+      f[2 * i + 1] += b.y;
+    }
+  } else {
+    f[0] += __uint_as_float(y.x); f[1] += __uint_as_float(y.y);
+    f[2] += __uint_as_float(y.z); f[3] += __uint_as_float(y.w);
+  }
+}
+
 // Accumulate mode, one block per position of the token order (T blocks, *npos
 // positions used): the block at the head of a row's segment adds
 // the row's tokens in token order onto the row, the others return. Two
 // vectors per thread per step, with the row's and the first token's vectors
-// requested together.
+// requested together and held as raw bits until they are added, so that the
+// kernel fits six 256-thread blocks per SM (40 registers a thread).
 template <typename T>
-__global__ void emb_accum_heads_kernel(int H, const int32_t* __restrict__ npos,
-                                       const int32_t* __restrict__ order,
-                                       const int32_t* __restrict__ seg_row,
-                                       const int32_t* __restrict__ seg_end,
-                                       const T* __restrict__ dout, T* __restrict__ d_emb) {
+__global__ void __launch_bounds__(256, 6) emb_accum_heads_kernel(
+    int H, const int32_t* __restrict__ npos, const int32_t* __restrict__ order,
+    const int32_t* __restrict__ seg_row, const int32_t* __restrict__ seg_end,
+    const T* __restrict__ dout, T* __restrict__ d_emb) {
   constexpr int VN = EVec<T>::N;
   const int p = blockIdx.x;
   // the position's entries are requested together with the position count
@@ -296,27 +336,22 @@ __global__ void emb_accum_heads_kernel(int H, const int32_t* __restrict__ npos,
   for (int vi = threadIdx.x; vi < nvec; vi += 2 * blockDim.x) {
     const int vj = vi + blockDim.x;
     const bool two = vj < nvec;
-    float a[VN], b[VN], ga[VN], gb[VN];
-    eload(dst + vi * VN, a);
-    eload(g0 + vi * VN, ga);
+    const uint4 ra = eraw(dst + vi * VN), qa = eraw(g0 + vi * VN);
+    uint4 rb = make_uint4(0u, 0u, 0u, 0u), qb = rb;
     if (two) {
-      eload(dst + vj * VN, b);
-      eload(g0 + vj * VN, gb);
+      rb = eraw(dst + vj * VN);
+      qb = eraw(g0 + vj * VN);
     }
-#pragma unroll
-    for (int j = 0; j < VN; ++j) {
-      a[j] += ga[j];
-      b[j] = two ? b[j] + gb[j] : 0.0f;
-    }
+    float a[VN], b[VN];
+    eadd_raw<T>(ra, qa, a);
+    eadd_raw<T>(rb, qb, b);
     for (int i = p + 1; i < end; ++i) {
       const T* gi = dout + (int64_t)order[i] * H;
-      eload(gi + vi * VN, ga);
-      if (two) eload(gi + vj * VN, gb);
-#pragma unroll
-      for (int j = 0; j < VN; ++j) {
-        a[j] += ga[j];
-        if (two) b[j] += gb[j];
-      }
+      const uint4 ga = eraw(gi + vi * VN);
+      uint4 gb = make_uint4(0u, 0u, 0u, 0u);
+      if (two) gb = eraw(gi + vj * VN);
+      eacc_raw<T>(ga, a);
+      eacc_raw<T>(gb, b);
     }
     estore(dst + vi * VN, a);
     if (two) estore(dst + vj * VN, b);
